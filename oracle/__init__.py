@@ -1,0 +1,264 @@
+"""CPU oracle for the fused NF4 dequantise-and-multiply.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The GPU library never imports, links or calls it, and it never imports
+the GPU library.
+
+The arithmetic lives in plain C (``nf4_oracle.c``, fp64 sums, no fast-math, no
+FMA contraction); this module only builds it, loads it with ctypes and moves
+numpy arrays in and out.  Codebooks come from ``oracle.codebooks``.
+
+Every function is pinned by the ``-m "not gpu"`` tests against values that the
+definition fixes (codebook end points and zero, quantise/dequantise round trips of
+codebook-aligned blocks, the absmax scaling invariant, hand-built packed bytes,
+brute force and closed forms of the products).  Parity of the codebook values
+and of the nibble order with bitsandbytes itself is unpinned: bitsandbytes is not
+available and the pages print neither.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nf4_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MEAN_CHUNK = 1024  # chunk length of the fixed summation order of the mean offset
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (OpenMP, no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            P = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            i32 = ctypes.c_int32
+            L.oracle_quantize_nf4.argtypes = [P, i64, i32, P, P, P]
+            L.oracle_double_quant.argtypes = [P, i64, i32, i32, P, P, P, P]
+            L.oracle_decode_absmax.argtypes = [P, P, ctypes.c_float, i64, i32, P, P]
+            L.oracle_dequantize_nf4.argtypes = [P, P, i64, i32, P, P, P]
+            L.oracle_linear_fwd.argtypes = [P, i64, i64, P, i64, P, i64, P]
+            L.oracle_linear_dgrad.argtypes = [P, i64, i64, P, i64, P, i64, P]
+            L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
+            L.oracle_bf16_from_f32.restype = ctypes.c_uint16
+            L.oracle_num_threads.restype = ctypes.c_int
+            for name in ("oracle_quantize_nf4", "oracle_double_quant", "oracle_decode_absmax",
+                         "oracle_dequantize_nf4", "oracle_linear_fwd", "oracle_linear_dgrad"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+# ------------------------------------------------------------------ bf16 ----
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp32 values (exact widening)."""
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(f: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns by round-to-nearest-even (the C oracle's rule)."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    flat = f.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+    fn = lib().oracle_bf16_from_f32
+    for i, v in enumerate(flat.tolist()):
+        out[i] = fn(v)
+    return out.reshape(f.shape)
+
+
+# --------------------------------------------------------- quantisation ----
+
+class QuantState:
+    """Plain container of one quantised weight: the oracle's view of the pages'
+    QuantState (packed bytes, fp32 absmax, and under double quantisation the 8-bit
+    codes, nested absmax and offset)."""
+
+    def __init__(self, shape, blocksize, packed, absmax, code4, double_quant=False,
+                 absmax_q=None, nested_absmax=None, nested_offset=None, code8=None,
+                 nested_blocksize=256):
+        self.shape = tuple(shape)
+        self.blocksize = blocksize
+        self.packed = packed
+        self.absmax = absmax
+        self.code4 = code4
+        self.double_quant = double_quant
+        self.absmax_q = absmax_q
+        self.nested_absmax = nested_absmax
+        self.nested_offset = nested_offset
+        self.code8 = code8
+        self.nested_blocksize = nested_blocksize
+
+    @property
+    def numel(self) -> int:
+        n = 1
+        for s in self.shape:
+            n *= s
+        return n
+
+
+def quantize_nf4(w: np.ndarray, code4: np.ndarray, blocksize: int = 64):
+    """Blockwise NF4 quantisation of a flat view of w (fp32).  Returns (packed, absmax)."""
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    code4 = np.ascontiguousarray(code4, dtype=np.float32)
+    numel = w.size
+    packed = np.zeros((numel + 1) // 2, dtype=np.uint8)
+    absmax = np.zeros((numel + blocksize - 1) // blocksize, dtype=np.float32)
+    _check(lib().oracle_quantize_nf4(_p(w), numel, blocksize, _p(code4), _p(packed), _p(absmax)),
+           "quantize_nf4")
+    return packed, absmax
+
+
+def double_quant(absmax: np.ndarray, code8: np.ndarray, nested_blocksize: int = 256):
+    """8-bit blockwise quantisation of the absmax array.  Returns (absmax_q, nested_absmax, offset)."""
+    absmax = np.ascontiguousarray(absmax, dtype=np.float32).reshape(-1)
+    code8 = np.ascontiguousarray(code8, dtype=np.float32)
+    nb = absmax.size
+    absmax_q = np.zeros(nb, dtype=np.uint8)
+    nested = np.zeros((nb + nested_blocksize - 1) // nested_blocksize, dtype=np.float32)
+    off = np.zeros(1, dtype=np.float32)
+    _check(lib().oracle_double_quant(_p(absmax), nb, nested_blocksize, MEAN_CHUNK, _p(code8),
+                                     _p(absmax_q), _p(nested), _p(off)), "double_quant")
+    return absmax_q, nested, off
+
+
+def decode_absmax(absmax_q, nested_absmax, offset, code8, nested_blocksize: int = 256):
+    absmax_q = np.ascontiguousarray(absmax_q, dtype=np.uint8).reshape(-1)
+    nested_absmax = np.ascontiguousarray(nested_absmax, dtype=np.float32)
+    code8 = np.ascontiguousarray(code8, dtype=np.float32)
+    out = np.zeros(absmax_q.size, dtype=np.float32)
+    off = float(np.asarray(offset, dtype=np.float32).reshape(-1)[0])
+    _check(lib().oracle_decode_absmax(_p(absmax_q), _p(nested_absmax), ctypes.c_float(off),
+                                      absmax_q.size, nested_blocksize, _p(code8), _p(out)),
+           "decode_absmax")
+    return out
+
+
+def quantize(w: np.ndarray, code4, blocksize: int = 64, double_quant_: bool = False,
+             code8=None, nested_blocksize: int = 256) -> QuantState:
+    packed, absmax = quantize_nf4(w, code4, blocksize)
+    st = QuantState(np.shape(w), blocksize, packed, absmax, np.asarray(code4, np.float32))
+    if double_quant_:
+        aq, nested, off = double_quant(absmax, code8, nested_blocksize)
+        st.double_quant = True
+        st.absmax_q, st.nested_absmax, st.nested_offset = aq, nested, off
+        st.code8 = np.asarray(code8, np.float32)
+        st.nested_blocksize = nested_blocksize
+    return st
+
+
+def block_scale(st: QuantState) -> np.ndarray:
+    """The per-block fp32 scale the dequantisation multiplies by (absmax, or the
+    decoded absmax under double quantisation)."""
+    if st.double_quant:
+        return decode_absmax(st.absmax_q, st.nested_absmax, st.nested_offset, st.code8,
+                             st.nested_blocksize)
+    return st.absmax
+
+
+def dequantize(st: QuantState, dtype: str = "bf16") -> np.ndarray:
+    """Dense dequantised weight: fp32 values, or bf16 bit patterns (uint16)."""
+    scale = np.ascontiguousarray(block_scale(st), dtype=np.float32)
+    n = st.numel
+    if dtype == "f32":
+        out = np.zeros(n, dtype=np.float32)
+        _check(lib().oracle_dequantize_nf4(_p(st.packed), _p(scale), n, st.blocksize,
+                                           _p(st.code4), _p(out), None), "dequantize")
+    elif dtype == "bf16":
+        out = np.zeros(n, dtype=np.uint16)
+        _check(lib().oracle_dequantize_nf4(_p(st.packed), _p(scale), n, st.blocksize,
+                                           _p(st.code4), None, _p(out)), "dequantize")
+    else:
+        raise ValueError(dtype)
+    return out.reshape(st.shape)
+
+
+# ------------------------------------------------------------- products ----
+
+def linear_fwd(x_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None) -> np.ndarray:
+    """y = x W^T in fp64 from bf16 bit patterns x [M,K] and Wb [N,K]; only `rows` of y
+    when given."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    wb = np.ascontiguousarray(wb_bf16, dtype=np.uint16)
+    M, K = x.shape
+    N, K2 = wb.shape
+    assert K == K2
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = M if r is None else r.size
+    y = np.zeros((nrows, N), dtype=np.float64)
+    _check(lib().oracle_linear_fwd(_p(x), M, K, _p(wb), N, _p(r), nrows, _p(y)), "linear_fwd")
+    return y
+
+
+def linear_dgrad(gy_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None) -> np.ndarray:
+    """grad_x = grad_y W in fp64 from bf16 bit patterns gy [M,N] and Wb [N,K]."""
+    gy = np.ascontiguousarray(gy_bf16, dtype=np.uint16)
+    wb = np.ascontiguousarray(wb_bf16, dtype=np.uint16)
+    M, N = gy.shape
+    N2, K = wb.shape
+    assert N == N2
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = M if r is None else r.size
+    gx = np.zeros((nrows, K), dtype=np.float64)
+    _check(lib().oracle_linear_dgrad(_p(gy), M, N, _p(wb), K, _p(r), nrows, _p(gx)), "linear_dgrad")
+    return gx
+
+
+def grouped_fwd(x_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray) -> np.ndarray:
+    """Per-expert forward: rows offsets[e]..offsets[e+1] of x use expert e's weight
+    wb_stack[e] ([E,N,K] bf16 bits).  Returns fp64 [T,N]."""
+    E, N, K = wb_stack_bf16.shape
+    T = x_bf16.shape[0]
+    y = np.zeros((T, N), dtype=np.float64)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            y[a:b] = linear_fwd(x_bf16[a:b], wb_stack_bf16[e])
+    return y
+
+
+def grouped_dgrad(gy_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray) -> np.ndarray:
+    E, N, K = wb_stack_bf16.shape
+    T = gy_bf16.shape[0]
+    gx = np.zeros((T, K), dtype=np.float64)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            gx[a:b] = linear_dgrad(gy_bf16[a:b], wb_stack_bf16[e])
+    return gx

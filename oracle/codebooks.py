@@ -1,0 +1,71 @@
+"""Codebooks of the oracle, computed in fp64 from their definitions and rounded
+once to fp32.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  The GPU package derives
+its own tables with its own code; the tests check that the two agree bit for bit.
+
+``nf4_code4`` -- the 4-bit NormalFloat levels.  The pages call the type "nf4"
+(bitsandbytes issue "MatMul4Bit keeps B and quant_state on ctx", section
+"Minimal reproducer": ``quantize_4bit(..., quant_type="nf4")``) but never print
+its 16 values.  Reading: the NormalFloat construction of the QLoRA paper
+(Dettmers et al., 2023, section 3, "4-bit NormalFloat"): levels are quantiles of
+the standard normal, asymmetric so that an exact zero exists -- 8 positive levels
+at the probabilities ``linspace(1 - delta, 1/2, 9)`` without the last point, 7
+negative levels mirrored from ``linspace(1 - delta, 1/2, 8)`` without the last
+point, plus 0 -- and the whole set divided by its largest value so that both
+extremes are exactly +-1.  ``delta = (1/30 + 1/32) / 2``.
+
+``dynamic_code8`` -- the signed 8-bit dynamic ("tree") map used for the nested
+absmax codes.  The pages name only "blockwise dynamic map" (fork PR "Experts
+trainability", commit 1 table, int8 row) and BASELINE fixes "8-bit blockwise".
+Reading: the dynamic tree quantisation of Dettmers et al., 2022 ("8-bit
+Optimizers via Block-wise Quantization"): a sign, a run of leading zero bits that
+sets a decimal exponent, an indicator bit, and the remaining bits a linear
+fraction.  With 7 magnitude bits the exponent group e = 0..6 has 2**e fraction
+values; each is the midpoint of one of 2**e equal bins of [0.1, 1], scaled by
+10**(e - 6).  Both signs, plus an exact 0 and the value 1.0, give 256 levels.
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.special import ndtri
+
+NF4_DELTA = 0.5 * (1.0 / 30.0 + 1.0 / 32.0)
+
+
+def nf4_code4_f64() -> np.ndarray:
+    top = 1.0 - NF4_DELTA
+    pos = ndtri(np.linspace(top, 0.5, 9)[:-1])  # 8 values, largest first
+    neg = -ndtri(np.linspace(top, 0.5, 8)[:-1])  # 7 values
+    levels = np.sort(np.concatenate([neg, [0.0], pos]))
+    return levels / levels.max()
+
+
+def nf4_code4() -> np.ndarray:
+    """16 strictly increasing fp32 levels, code4[0] = -1, code4[7] = 0, code4[15] = 1."""
+    return nf4_code4_f64().astype(np.float32)
+
+
+def dynamic_code8_f64() -> np.ndarray:
+    mags = []
+    for e in range(7):
+        nbins = 2 ** e
+        edges = np.linspace(0.1, 1.0, nbins + 1)
+        mids = 0.5 * (edges[:-1] + edges[1:])
+        mags.append(mids * 10.0 ** (e - 6))
+    mags = np.concatenate(mags)  # 127 positive magnitudes
+    levels = np.concatenate([-mags, mags, [0.0, 1.0]])
+    return np.sort(levels)
+
+
+def dynamic_code8() -> np.ndarray:
+    """256 strictly increasing fp32 levels with an exact 0 and a largest level of 1."""
+    return dynamic_code8_f64().astype(np.float32)
+
+
+def linear_code8() -> np.ndarray:
+    """A plain linear 8-bit map, (j - 128) / 128 for j = 0..255 (exact 0 at j = 128,
+    -1 at j = 0); used by the tests so that kernel parity does not hinge on one
+    choice of code8."""
+    j = np.arange(256, dtype=np.float64)
+    return ((j - 128.0) / 128.0).astype(np.float32)

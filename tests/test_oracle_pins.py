@@ -1,0 +1,382 @@
+"""Pins of the CPU oracle against what the definitions and the mathematics fix.
+
+Each test targets a plausible mistake (a wrong sign, a swapped nibble, a transposed
+operand, an FMA where two roundings are required, a wrong tie rule) and must fail
+if the oracle made it.  None of them re-derives an expected value with the oracle's
+own formula: expected values are literals, closed forms, library routines (numpy
+matmul, math.erf) or constructions whose answer is known by design.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import codebooks
+
+CODE4 = codebooks.nf4_code4()
+CODE8 = codebooks.dynamic_code8()
+LIN8 = codebooks.linear_code8()
+
+
+# --------------------------------------------------------------- codebooks ----
+
+def test_code4_shape_endpoints_zero():
+    # BASELINE north star: "the 16-level codebook with an exact zero and +-1 endpoints".
+    assert CODE4.dtype == np.float32 and CODE4.shape == (16,)
+    assert np.all(np.diff(CODE4) > 0)
+    assert CODE4[0] == -1.0 and CODE4[15] == 1.0 and CODE4[7] == 0.0
+    assert (CODE4 < 0).sum() == 7 and (CODE4 > 0).sum() == 8
+
+
+def _phi(x):
+    return 0.5 * (1.0 + math.erf(x / math.sqrt(2.0)))
+
+
+def _phi_inv_bisect(p):
+    lo, hi = -10.0, 10.0
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if _phi(mid) < p:
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+def test_code4_levels_are_normal_quantiles():
+    # Each non-zero level times the normaliser is a standard-normal quantile at the
+    # probabilities of the NormalFloat construction; checked through the forward CDF
+    # (math.erf) and a bisection, not through the oracle's ndtri.
+    delta = 0.5 * (1 / 30 + 1 / 32)
+    z_top = _phi_inv_bisect(1 - delta)
+    p_pos = np.linspace(1 - delta, 0.5, 9)[:-1][::-1]  # ascending, 8 values
+    p_neg = np.linspace(1 - delta, 0.5, 8)[:-1]        # 7 values, largest first
+    for j, p in zip(range(8, 16), p_pos):
+        assert abs(_phi(float(CODE4[j]) * z_top) - p) < 2e-7, j
+    for j, p in zip(range(0, 7), p_neg):
+        assert abs(_phi(-float(CODE4[j]) * z_top) - p) < 2e-7, j
+
+
+def test_code8_dynamic_map_structure():
+    assert CODE8.shape == (256,) and np.all(np.diff(CODE8) > 0)
+    assert 0.0 in CODE8 and CODE8.max() == 1.0
+    pos = CODE8[(CODE8 > 0) & (CODE8 < 1)]
+    neg = CODE8[CODE8 < 0]
+    assert pos.size == 127 and neg.size == 127
+    np.testing.assert_array_equal(np.sort(-neg), pos)  # mirror image
+    # 2**e fraction values in each decade (1e-7, 1e-6), ..., (0.1, 1)
+    for e in range(7):
+        lo, hi = 10.0 ** (e - 7), 10.0 ** (e - 6)
+        assert ((pos > lo) & (pos < hi)).sum() == 2 ** e
+    # the top decade: midpoints of 64 equal bins of [0.1, 1]
+    assert abs(float(pos.max()) - (1.0 - 0.9 / 128)) < 1e-7
+
+
+def test_linear_code8():
+    assert LIN8[0] == -1.0 and LIN8[128] == 0.0 and np.all(np.diff(LIN8) > 0)
+
+
+# ----------------------------------------------------------------- bf16 ----
+
+@pytest.mark.parametrize("bits,expect", [
+    (0x3F808000, 0x3F80),  # tie, even stays
+    (0x3F818000, 0x3F82),  # tie, odd rounds up
+    (0x3F808001, 0x3F81),  # above tie
+    (0x3F807FFF, 0x3F80),  # below tie
+    (0xBF818000, 0xBF82),  # negative tie
+    (0x7F7FFFFF, 0x7F80),  # rounds to +inf
+    (0x00000000, 0x0000),
+    (0x80000000, 0x8000),
+])
+def test_bf16_round_to_nearest_even(oracle_lib, bits, expect):
+    f = np.array([bits], dtype=np.uint32).view(np.float32)[0]
+    assert oracle_lib.oracle_bf16_from_f32(float(f)) == expect
+
+
+# -------------------------------------------------------- quantisation ----
+
+def test_packing_hand_built_bytes():
+    # indices 15, 0, 7, 12 at absmax 1: even element in the high nibble.
+    w = np.array([1.0, -1.0, 0.0, CODE4[12]], dtype=np.float32)
+    packed, absmax = oracle.quantize_nf4(w, CODE4, blocksize=4)
+    assert packed.tolist() == [0xF0, 0x7C]
+    assert absmax.tolist() == [1.0]
+    # odd length: the missing low nibble is zero
+    packed, _ = oracle.quantize_nf4(w[:3], CODE4, blocksize=4)
+    assert packed.tolist() == [0xF0, 0x70]
+
+
+def test_dequantize_hand_built_bytes():
+    st = oracle.QuantState((4,), 4, np.array([0xF0, 0x7C], np.uint8), np.array([2.0], np.float32), CODE4)
+    out = oracle.dequantize(st, "f32")
+    assert out.tolist() == [2.0, -2.0, 0.0, float(np.float32(CODE4[12]) * np.float32(2.0))]
+
+
+def _aligned_blocks(rng, nblocks, bs=64):
+    """Blocks whose values are exactly fp32(code4[j] * a), with one value at +-a."""
+    idx = rng.integers(0, 16, size=(nblocks, bs))
+    pos = rng.integers(0, bs, size=nblocks)
+    idx[np.arange(nblocks), pos] = rng.choice([0, 15], size=nblocks)
+    a = (rng.uniform(0.5, 1.0, size=nblocks) * 2.0 ** rng.integers(-20, 5, size=nblocks)).astype(np.float32)
+    w = (CODE4[idx] * a[:, None]).astype(np.float32)
+    return w, idx, a
+
+
+def test_round_trip_codebook_aligned_blocks():
+    rng = np.random.default_rng(1)
+    w, idx, a = _aligned_blocks(rng, 200)
+    packed, absmax = oracle.quantize_nf4(w, CODE4, 64)
+    np.testing.assert_array_equal(absmax, a)
+    hi, lo = packed >> 4, packed & 15
+    q = np.stack([hi, lo], axis=1).reshape(-1)
+    np.testing.assert_array_equal(q, idx.reshape(-1))
+    st = oracle.QuantState(w.shape, 64, packed, absmax, CODE4)
+    np.testing.assert_array_equal(oracle.dequantize(st, "f32"), w)
+
+
+def test_absmax_scaling_invariant():
+    rng = np.random.default_rng(2)
+    w = (rng.standard_normal((64, 64)) * 0.02).astype(np.float32)
+    p0, a0 = oracle.quantize_nf4(w, CODE4)
+    for k in (-3, 1, 7):
+        pk, ak = oracle.quantize_nf4(w * np.float32(2.0 ** k), CODE4)
+        np.testing.assert_array_equal(pk, p0)
+        np.testing.assert_array_equal(ak, a0 * np.float32(2.0 ** k))
+    # every dequantised block reaches its absmax exactly
+    st = oracle.QuantState(w.shape, 64, p0, a0, CODE4)
+    wf = oracle.dequantize(st, "f32").reshape(-1, 64)
+    np.testing.assert_array_equal(np.abs(wf).max(axis=1), a0)
+
+
+def test_sign_flip_mirrors_where_codebook_is_symmetric():
+    # Levels k/7 for k = -7..7 are symmetric about 0; the 16th level (-8/7) lies
+    # outside [-1, 1] and is never nearest.  Negating a block must then negate
+    # every dequantised value exactly.
+    sym = np.array([-8 / 7] + [k / 7 for k in range(-7, 8)], np.float32)
+    rng = np.random.default_rng(3)
+    w = rng.uniform(-0.8, 0.8, size=(8, 64)).astype(np.float32)
+    w[:, 0] = 0.9
+    p, a = oracle.quantize_nf4(w, sym)
+    pn, an = oracle.quantize_nf4(-w, sym)
+    np.testing.assert_array_equal(a, an)
+    d = oracle.dequantize(oracle.QuantState(w.shape, 64, p, a, sym), "f32")
+    dn = oracle.dequantize(oracle.QuantState(w.shape, 64, pn, an, sym), "f32")
+    np.testing.assert_array_equal(d, -dn)
+    assert not np.any((p >> 4) == 0) and not np.any((p & 15) == 0)
+
+
+def test_tie_goes_to_lower_index_and_nearest_otherwise():
+    code = np.array([-1, -.875, -.75, -.625, -.5, -.375, -.25, 0, .125, .25, .375, .5, .625, .75, .875, 1],
+                    np.float32)
+    mid = np.float32(0.0625)  # exact midpoint of levels 7 (0) and 8 (0.125)
+    above = np.nextafter(mid, np.float32(1))
+    below = np.nextafter(mid, np.float32(0))
+    w = np.array([1.0, mid, above, below], np.float32)
+    packed, _ = oracle.quantize_nf4(w, code, blocksize=4)
+    assert packed.tolist() == [(15 << 4) | 7, (8 << 4) | 7]
+
+
+def test_zero_block():
+    w = np.zeros(64, np.float32)
+    packed, absmax = oracle.quantize_nf4(w, CODE4)
+    assert absmax.tolist() == [0.0]
+    assert packed.tolist() == [0x77] * 32
+    st = oracle.QuantState(w.shape, 64, packed, absmax, CODE4)
+    assert np.all(oracle.dequantize(st, "f32") == 0)
+
+
+def test_short_last_block():
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal(64 * 3 + 17) * 0.02).astype(np.float32)
+    packed, absmax = oracle.quantize_nf4(w, CODE4)
+    assert absmax.size == 4 and packed.size == (w.size + 1) // 2
+    assert absmax[3] == np.abs(w[192:]).max()
+    # the last block is quantised on its own: same result as quantising it alone
+    p_tail, a_tail = oracle.quantize_nf4(w[192:], CODE4)
+    assert a_tail[0] == absmax[3]
+    np.testing.assert_array_equal(p_tail, packed[96:])
+
+
+def test_quantisation_error_bound():
+    # nearest-level rounding: |w - wf| <= a * (largest half-gap of the codebook) + fp32 slack
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((32, 256)) * 0.02).astype(np.float32)
+    st = oracle.quantize(w, CODE4)
+    wf = oracle.dequantize(st, "f32").reshape(-1, 64)
+    a = st.absmax[:, None]
+    half_gap = float(np.max(np.diff(CODE4.astype(np.float64))) / 2)
+    err = np.abs(wf - w.reshape(-1, 64))
+    assert np.all(err <= a * (half_gap + 1e-6))
+
+
+# ------------------------------------------------- double quantisation ----
+
+def test_mean_offset_exact_for_exact_sums():
+    absmax = np.array([0.5, 1.0, 1.5, 2.0] * 300, np.float32)  # 1200 values: two chunks
+    _, _, off = oracle.double_quant(absmax, LIN8)
+    assert off.tolist() == [1.25]
+
+
+def test_double_quant_round_trip_linear_map():
+    # residuals k/128 * na with sum 0 and max |r| = na: offset, na and every code exact.
+    ks = [-128, 64, 64, 5, -5, 17, -17, 127, -127, 0, 33, -33]
+    na = np.float32(0.125)
+    r = np.array(ks, np.float64) / 128.0 * float(na)
+    absmax = (1.0 + r).astype(np.float32)
+    aq, nested, off = oracle.double_quant(absmax, LIN8)
+    assert off.tolist() == [1.0] and nested.tolist() == [0.125]
+    assert aq.tolist() == [k + 128 for k in ks]
+    dec = oracle.decode_absmax(aq, nested, off, LIN8)
+    np.testing.assert_array_equal(dec, absmax)
+
+
+def test_double_quant_nested_blocks_and_error_bound():
+    rng = np.random.default_rng(6)
+    absmax = rng.uniform(0.01, 0.08, size=256 * 5 + 37).astype(np.float32)
+    aq, nested, off = oracle.double_quant(absmax, CODE8)
+    assert nested.size == 6
+    r = absmax.astype(np.float64) - float(off[0])
+    for c in range(6):
+        blk = slice(256 * c, min(256 * (c + 1), absmax.size))
+        assert nested[c] == np.float32(np.abs((absmax[blk] - off[0]).astype(np.float32)).max())
+    dec = oracle.decode_absmax(aq, nested, off, CODE8).astype(np.float64)
+    # nearest level of an 8-bit map: error at most half the local gap times na (+ rounding)
+    gaps = np.diff(CODE8.astype(np.float64)).max()
+    na = nested.astype(np.float64).repeat(256)[:absmax.size]
+    assert np.all(np.abs(dec - absmax) <= na * (gaps / 2 + 1e-6) + 1e-7)
+    del r
+
+
+def test_decode_absmax_two_roundings_no_fma():
+    # a*b+c with a = b = 1 + 2^-12, c = -1: two roundings give 2^-11, an FMA gives 2^-11 + 2^-24.
+    a = np.float32(1.0 + 2.0 ** -12)
+    code8 = np.linspace(-1.0, 1.0, 256).astype(np.float32)
+    code8[128] = 0.0
+    code8 = np.sort(code8)
+    code8[255] = a
+    dec = oracle.decode_absmax(np.array([255], np.uint8), np.array([a], np.float32),
+                               np.array([-1.0], np.float32), code8)
+    assert dec.tolist() == [2.0 ** -11]
+
+
+def test_zero_nested_block_maps_to_exact_zero_code():
+    absmax = np.full(256, 0.03125, np.float32)
+    aq, nested, off = oracle.double_quant(absmax, CODE8)
+    assert off.tolist() == [0.03125] and nested.tolist() == [0.0]
+    assert np.all(CODE8[aq] == 0.0)
+    np.testing.assert_array_equal(oracle.decode_absmax(aq, nested, off, CODE8), absmax)
+
+
+# ------------------------------------------------------------- products ----
+
+def _bf16(a):
+    return oracle.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def _small_weight(rng, N, K, dq=False):
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    st = oracle.quantize(w, CODE4, 64, dq, CODE8)
+    return oracle.dequantize(st, "bf16")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (3, 5, 128), (8, 8, 192), (7, 2, 64)])
+def test_fwd_dgrad_brute_force_vs_numpy(M, N, K):
+    rng = np.random.default_rng(M * 100 + N * 10 + K)
+    wb = _small_weight(rng, N, K)
+    x = _bf16(rng.standard_normal((M, K)))
+    gy = _bf16(rng.standard_normal((M, N)))
+    W = oracle.bf16_bits_to_f32(wb).astype(np.float64)
+    X = oracle.bf16_bits_to_f32(x).astype(np.float64)
+    GY = oracle.bf16_bits_to_f32(gy).astype(np.float64)
+    np.testing.assert_allclose(oracle.linear_fwd(x, wb), X @ W.T, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(oracle.linear_dgrad(gy, wb), GY @ W, rtol=1e-12, atol=1e-14)
+
+
+def test_identity_probe_is_exact():
+    rng = np.random.default_rng(7)
+    N, K = 24, 128
+    wb = _small_weight(rng, N, K, dq=True)
+    eye_k = _bf16(np.eye(K))
+    eye_n = _bf16(np.eye(N))
+    np.testing.assert_array_equal(oracle.linear_fwd(eye_k, wb), oracle.bf16_bits_to_f32(wb).T)
+    np.testing.assert_array_equal(oracle.linear_dgrad(eye_n, wb), oracle.bf16_bits_to_f32(wb))
+
+
+def test_constant_input_closed_form():
+    rng = np.random.default_rng(8)
+    wb = _small_weight(rng, 16, 256)
+    ones = _bf16(np.ones((3, 256)))
+    y = oracle.linear_fwd(ones, wb)
+    rowsum = oracle.bf16_bits_to_f32(wb).astype(np.float64).sum(axis=1)
+    np.testing.assert_allclose(y, np.broadcast_to(rowsum, y.shape), rtol=1e-12, atol=1e-15)
+
+
+def test_dgrad_is_fwd_with_transposed_operand_exact():
+    # Integer-valued bf16 data: every partial sum is exact, so any order gives the
+    # same value and a transposed or shifted index shows as a mismatch.
+    rng = np.random.default_rng(9)
+    M, N, K = 5, 12, 64
+    wb = _bf16(rng.integers(-8, 9, size=(N, K)))
+    gy = _bf16(rng.integers(-8, 9, size=(M, N)))
+    gx = oracle.linear_dgrad(gy, wb)
+    np.testing.assert_array_equal(gx, oracle.linear_fwd(gy, np.ascontiguousarray(wb.T)))
+    exact = oracle.bf16_bits_to_f32(gy).astype(np.int64) @ oracle.bf16_bits_to_f32(wb).astype(np.int64)
+    np.testing.assert_array_equal(gx, exact.astype(np.float64))
+
+
+def test_row_subset_matches_full():
+    rng = np.random.default_rng(10)
+    wb = _small_weight(rng, 8, 128)
+    x = _bf16(rng.standard_normal((6, 128)))
+    full = oracle.linear_fwd(x, wb)
+    rows = np.array([5, 0, 3])
+    np.testing.assert_array_equal(oracle.linear_fwd(x, wb, rows=rows), full[rows])
+    gy = _bf16(rng.standard_normal((6, 8)))
+    fullg = oracle.linear_dgrad(gy, wb)
+    np.testing.assert_array_equal(oracle.linear_dgrad(gy, wb, rows=rows), fullg[rows])
+
+
+def test_fp32_accumulation_is_well_inside_tolerance():
+    # The GPU accumulates in fp32 and rounds to bf16; that arithmetic, emulated with
+    # numpy, must sit far inside the 5e-3 relative Frobenius bound against fp64.
+    rng = np.random.default_rng(11)
+    M, N, K = 16, 64, 2048
+    wb = _small_weight(rng, N, K)
+    x = _bf16(rng.standard_normal((M, K)))
+    ref = oracle.linear_fwd(x, wb)
+    y32 = (oracle.bf16_bits_to_f32(x) @ oracle.bf16_bits_to_f32(wb).T).astype(np.float32)
+    y16 = oracle.bf16_bits_to_f32(_bf16(y32)).astype(np.float64)
+    rel = np.linalg.norm(y16 - ref) / np.linalg.norm(ref)
+    assert rel < 5e-3 / 2
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.all(np.abs(y16 - ref) <= 1e-2 * (np.abs(ref) + rms))
+
+
+def test_grouped_matches_per_expert_numpy():
+    rng = np.random.default_rng(12)
+    E, N, K = 4, 8, 64
+    wbs = np.stack([_small_weight(rng, N, K) for _ in range(E)])
+    offsets = np.array([0, 3, 3, 7, 10])
+    x = _bf16(rng.standard_normal((10, K)))
+    y = oracle.grouped_fwd(x, offsets, wbs)
+    X = oracle.bf16_bits_to_f32(x).astype(np.float64)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        W = oracle.bf16_bits_to_f32(wbs[e]).astype(np.float64)
+        np.testing.assert_allclose(y[a:b], X[a:b] @ W.T, rtol=1e-12, atol=1e-14)
+    gy = _bf16(rng.standard_normal((10, N)))
+    gx = oracle.grouped_dgrad(gy, offsets, wbs)
+    GY = oracle.bf16_bits_to_f32(gy).astype(np.float64)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        W = oracle.bf16_bits_to_f32(wbs[e]).astype(np.float64)
+        np.testing.assert_allclose(gx[a:b], GY[a:b] @ W, rtol=1e-12, atol=1e-14)
+
+
+def test_mean_offset_sums_in_fp64():
+    # 2^24 followed by 1023 ones: an fp32 running sum loses every 1 (mean 16384.0);
+    # the fp64 sum keeps them, and (2^24 + 1023) / 1024 rounds to 16385.0 in fp32.
+    absmax = np.array([2.0 ** 24] + [1.0] * 1023, np.float32)
+    _, _, off = oracle.double_quant(absmax, LIN8)
+    assert off.tolist() == [16385.0]
