@@ -1,0 +1,126 @@
+"""ctypes binding of ``libnf4.so`` (the C ABI declared in ``include/nf4.h``).
+
+Argument marshalling only.  Loading fails loudly when the library has not been
+built: there is no fallback path of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libnf4.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "nf4.h")
+
+NF4_OK = 0
+STATUS_NAMES = {
+    0: "NF4_OK", 1: "NF4_ERR_INVALID_ARG", 2: "NF4_ERR_UNSUPPORTED_SHAPE", 3: "NF4_ERR_ALIGNMENT",
+    4: "NF4_ERR_WORKSPACE", 5: "NF4_ERR_CUDA", 6: "NF4_ERR_TIMEOUT", 7: "NF4_ERR_UNSUPPORTED",
+    8: "NF4_ERR_BAD_OFFSETS",
+}
+DTYPE_F32, DTYPE_BF16 = 0, 1
+OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD = range(5)
+PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
+         "dequantize", "quantize", "total"]
+
+
+class NF4Error(RuntimeError):
+    def __init__(self, what: str, code: int):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class nf4_weight(ctypes.Structure):
+    _fields_ = [
+        ("packed", ctypes.c_void_p),
+        ("absmax", ctypes.c_void_p),
+        ("absmax_q", ctypes.c_void_p),
+        ("nested_absmax", ctypes.c_void_p),
+        ("nested_offset", ctypes.c_void_p),
+        ("code4", ctypes.c_void_p),
+        ("code8", ctypes.c_void_p),
+        ("N", ctypes.c_int64),
+        ("K", ctypes.c_int64),
+        ("blocksize", ctypes.c_int32),
+        ("nested_blocksize", ctypes.c_int32),
+        ("double_quant", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/nf4.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf4_[a-z_0-9]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        W = ctypes.POINTER(nf4_weight)
+        sig = {
+            "nf4_quantize": [P, I32, I64, I64, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
+            "nf4_dequantize": [W, P, I32, P],
+            "nf4_linear_fwd": [P, I64, I64, W, P, I64, P, SZ, P],
+            "nf4_linear_dgrad": [P, I64, I64, W, P, I64, P, SZ, P],
+            "nf4_grouped_fwd": [P, P, I32, I64, I64, W, I64, P, I64, P],
+            "nf4_grouped_dgrad": [P, P, I32, I64, I64, W, I64, P, I64, P],
+            "nf4_workspace_size": [I32, I64, I64, I64, I32],
+            "nf4_status_string": [I32],
+            "nf4_get_path_counters": [P],
+            "nf4_reset_path_counters": [],
+            "nf4_device_status": [P, I32],
+            "nf4_device_check": [P],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.nf4_workspace_size.restype = ctypes.c_size_t
+        L.nf4_status_string.restype = ctypes.c_char_p
+        L.nf4_get_path_counters.restype = None
+        L.nf4_reset_path_counters.restype = None
+        _lib = L
+        return _lib
+
+
+def check(rc: int, what: str):
+    if rc != NF4_OK:
+        raise NF4Error(what, rc)
+
+
+def path_counters() -> dict:
+    arr = (ctypes.c_uint64 * 8)()
+    lib().nf4_get_path_counters(ctypes.cast(arr, ctypes.c_void_p))
+    return {name: int(v) for name, v in zip(PATHS, arr)}
+
+
+def reset_path_counters():
+    lib().nf4_reset_path_counters()
+
+
+def device_status(clear: bool = False) -> int:
+    v = ctypes.c_int32(0)
+    check(lib().nf4_device_status(ctypes.byref(v), 1 if clear else 0), "nf4_device_status")
+    return int(v.value)
+
+
+def device_check() -> int:
+    sms = ctypes.c_int32(0)
+    check(lib().nf4_device_check(ctypes.byref(sms)), "nf4_device_check")
+    return int(sms.value)

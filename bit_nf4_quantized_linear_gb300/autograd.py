@@ -1,0 +1,102 @@
+"""Autograd Functions over the fused kernels.
+
+The backward of a frozen 4-bit Linear needs the packed weight and its statistics.
+bitsandbytes' MatMul4Bit keeps them as plain ctx attributes, which activation
+checkpointing cannot see, so a caller that re-materialises the weight into a
+recycled buffer gets silently wrong gradients (bitsandbytes issue "MatMul4Bit
+keeps B and quant_state on ctx ...", sections "Summary" and "Root cause").  Here
+every tensor the backward reads -- the packed codes, the absmax or its 8-bit codes,
+the nested absmax and offset, and both codebooks -- goes through
+``ctx.save_for_backward`` (same issue, "Why save_for_backward fixes it"; Soup issue
+#842, "Design sketch"); ctx holds Python ints only.  The backward computes only
+grad_x (the base is frozen, Soup issue #842 "Scope") with the fused transposed
+kernel; no dense weight is saved or materialised (fork PR "Experts trainability",
+commit 2).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+
+
+class NF4LinearFn(torch.autograd.Function):
+    """y = x W^T for a frozen NF4 weight; grad only for x."""
+
+    @staticmethod
+    def forward(ctx, x, packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8,
+                N: int, K: int, double_quant: bool):
+        w = ops.NF4Weight.from_tensors(
+            (packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8), N, K,
+            double_quant)
+        lead = tuple(x.shape[:-1])
+        y = ops.linear_fwd(x.reshape(-1, K).contiguous(), w)
+        ctx.save_for_backward(packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8)
+        ctx.N, ctx.K, ctx.double_quant = int(N), int(K), bool(double_quant)
+        ctx.lead = lead
+        return y.reshape(*lead, N)
+
+    @staticmethod
+    def backward(ctx, gy):
+        saved = ctx.saved_tensors
+        gx = None
+        if ctx.needs_input_grad[0]:
+            w = ops.NF4Weight.from_tensors(saved, ctx.N, ctx.K, ctx.double_quant)
+            gx = ops.linear_dgrad(gy.reshape(-1, ctx.N).contiguous(), w).reshape(*ctx.lead, ctx.K)
+        return gx, None, None, None, None, None, None, None, None, None, None
+
+
+class NF4GroupedFn(torch.autograd.Function):
+    """Per-expert y = x_e W_e^T over a stacked frozen NF4 weight; grad only for x."""
+
+    @staticmethod
+    def forward(ctx, x, offsets, packed, absmax, absmax_q, nested_absmax, nested_offset, code4,
+                code8, experts: int, N: int, K: int, double_quant: bool):
+        w = ops.NF4Weight.from_tensors(
+            (packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8), N, K,
+            double_quant)
+        y = ops.grouped_fwd(x.contiguous(), offsets, w, experts)
+        ctx.save_for_backward(offsets, packed, absmax, absmax_q, nested_absmax, nested_offset,
+                              code4, code8)
+        ctx.experts, ctx.N, ctx.K, ctx.double_quant = int(experts), int(N), int(K), bool(double_quant)
+        return y
+
+    @staticmethod
+    def backward(ctx, gy):
+        offsets, *rest = ctx.saved_tensors
+        gx = None
+        if ctx.needs_input_grad[0]:
+            w = ops.NF4Weight.from_tensors(tuple(rest), ctx.N, ctx.K, ctx.double_quant)
+            gx = ops.grouped_dgrad(gy.contiguous(), offsets, w, ctx.experts)
+        return (gx,) + (None,) * 12
+
+
+def nf4_linear(x: torch.Tensor, w: ops.NF4Weight) -> torch.Tensor:
+    """Frozen NF4 Linear: the compute dtype is bf16; other input dtypes are cast in
+    and the output is cast back (the casts are ordinary autograd ops)."""
+    dt = x.dtype
+    xb = x if dt == torch.bfloat16 else x.to(torch.bfloat16)
+    y = NF4LinearFn.apply(xb, *w.tensors(), w.N, w.K, w.double_quant)
+    return y if dt == torch.bfloat16 else y.to(dt)
+
+
+def nf4_grouped(x: torch.Tensor, offsets: torch.Tensor, w: ops.NF4Weight, experts: int) -> torch.Tensor:
+    dt = x.dtype
+    xb = x if dt == torch.bfloat16 else x.to(torch.bfloat16)
+    y = NF4GroupedFn.apply(xb, offsets, *w.tensors(), experts, w.N, w.K, w.double_quant)
+    return y if dt == torch.bfloat16 else y.to(dt)
+
+
+class NF4Linear(torch.nn.Module):
+    """A frozen NF4 Linear layer without bias (biases stay in native ops)."""
+
+    def __init__(self, w: ops.NF4Weight):
+        super().__init__()
+        self.w = w
+
+    @classmethod
+    def from_float(cls, weight: torch.Tensor, double_quant: bool = True) -> "NF4Linear":
+        return cls(ops.quantize(weight.detach().contiguous(), double_quant=double_quant))
+
+    def forward(self, x):
+        return nf4_linear(x, self.w)

@@ -1,0 +1,71 @@
+// internal.h -- declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "nf4.h"
+
+namespace nf4 {
+
+// Device status codes written by kernels into the status word (same values as
+// nf4_status).
+constexpr int kStatusTimeout = NF4_ERR_TIMEOUT;
+constexpr int kStatusBadOffsets = NF4_ERR_BAD_OFFSETS;
+
+// Upper bound of experts the grouped kernels accept.
+constexpr int kMaxExperts = 512;
+
+// Tile geometry of the fused products.
+constexpr int kTileW = 128;  // rows of the dequantised operand per tile (MMA M)
+constexpr int kTileK = 64;   // contraction per pipeline stage (one 64-value block)
+
+// Parameters of the fused product kernel (everything but the tensor maps).
+struct GemmArgs {
+  int64_t M;        // activation rows (dense) or T (grouped)
+  int64_t ncols;    // output columns: N (fwd), N_e (grouped fwd), K (dgrad)
+  int64_t N_total;  // rows of the packed weight tensor
+  int64_t K;        // in-features
+  int64_t KB;       // K / 64
+  int64_t N_e;      // rows per expert (grouped); N for dense
+  int ksteps;       // contraction steps of a full item
+  int wtiles;       // tiles over the output columns
+  int ttiles;       // token tiles (dense)
+  int splits;       // contraction splits (dense, small M)
+  int64_t total_items;  // dense only; grouped computes it on the device
+  int grouped;
+  int E;
+  const int32_t* offsets;
+  const float* absmax;
+  const uint8_t* absmax_q;
+  const float* nested_absmax;
+  const float* nested_offset;
+  const float* code4;
+  const float* code8;
+  int dq;
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  float* ws;  // split-K partials [splits][M][ncols]
+  int* status;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_gemm(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
+                        const CUtensorMap& tmap_packed, int grid, cudaStream_t s);
+cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
+                                 __nv_bfloat16* out, int64_t ld, cudaStream_t s);
+int gemm_smem_bytes(int bt);
+
+cudaError_t launch_quantize(const void* W, int w_dtype, int64_t numel, const float* code4,
+                            uint8_t* packed, float* absmax, cudaStream_t s);
+cudaError_t launch_double_quant(const float* absmax, int64_t nblocks, const float* code8,
+                                uint8_t* absmax_q, float* nested_absmax, float* nested_offset,
+                                double* chunk_ws, cudaStream_t s);
+cudaError_t launch_dequantize(const nf4_weight& w, void* out, int out_dtype, cudaStream_t s);
+
+constexpr int kMeanChunk = 1024;    // fixed summation order of the mean offset
+constexpr int kNestedBlock = 256;   // nested blocksize
+
+}  // namespace nf4

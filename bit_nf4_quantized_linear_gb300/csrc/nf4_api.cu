@@ -1,0 +1,416 @@
+// nf4_api.cu -- the extern "C" entry points declared in include/nf4.h: argument
+// validation on the host, tile planning, TMA tensor-map encoding and launches.
+// No allocation, no synchronisation on the hot entry points.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "nf4.h"
+
+namespace {
+
+std::atomic<uint64_t> g_counters[NF4_NUM_PATHS];
+
+// Device status word: kernels record NF4_ERR_TIMEOUT / NF4_ERR_BAD_OFFSETS here.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  bool ok = false;
+  bool supported = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+bool current_device(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+      return false;
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return false;
+    d.status = static_cast<int*>(p);
+    d.ok = true;
+  }
+  *out = d;
+  return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void count(int path) {
+  g_counters[path].fetch_add(1, std::memory_order_relaxed);
+  g_counters[NF4_PATH_TOTAL].fetch_add(1, std::memory_order_relaxed);
+}
+
+nf4_status check_weight(const nf4_weight* w) {
+  if (!w || !w->packed || !w->code4) return NF4_ERR_INVALID_ARG;
+  if (w->N < 1 || w->K < 1) return NF4_ERR_INVALID_ARG;
+  if (w->blocksize != 64) return NF4_ERR_UNSUPPORTED;
+  if (w->double_quant != 0 && w->double_quant != 1) return NF4_ERR_INVALID_ARG;
+  if (w->double_quant) {
+    if (!w->absmax_q || !w->nested_absmax || !w->nested_offset || !w->code8)
+      return NF4_ERR_INVALID_ARG;
+    if (w->nested_blocksize != nf4::kNestedBlock) return NF4_ERR_UNSUPPORTED;
+  } else if (!w->absmax) {
+    return NF4_ERR_INVALID_ARG;
+  }
+  return NF4_OK;
+}
+
+int choose_bt(int64_t M) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  if (M <= 128) return 128;
+  return 256;
+}
+
+struct Plan {
+  int bt, wtiles, ttiles, splits, ksteps;
+  int64_t items;
+  size_t ws_bytes;
+};
+
+// Tile plan of a dense product; a deterministic function of the shape and the SM
+// count.  The contraction is split only when M is small (few tiles) and the
+// fp32 partials stay well below the packed-weight traffic.
+Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
+  Plan p;
+  const int64_t ncols = mode == 0 ? N : K;
+  const int64_t contract = mode == 0 ? K : N;
+  p.bt = choose_bt(M);
+  p.wtiles = static_cast<int>((ncols + nf4::kTileW - 1) / nf4::kTileW);
+  p.ttiles = static_cast<int>((M + p.bt - 1) / p.bt);
+  p.ksteps = static_cast<int>((contract + nf4::kTileK - 1) / nf4::kTileK);
+  const int64_t base = static_cast<int64_t>(p.wtiles) * p.ttiles;
+  int64_t s = 1;
+  if (M > 0 && M <= 32 && base < sms) {
+    s = (sms + base - 1) / base;
+    s = s < p.ksteps / 4 ? s : p.ksteps / 4;
+    const int64_t traffic_cap = contract / (64 * M);
+    s = s < traffic_cap ? s : traffic_cap;
+    s = s < 32 ? s : 32;
+    s = s < 1 ? 1 : s;
+  }
+  p.splits = static_cast<int>(s);
+  p.items = base * p.splits;
+  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * M * ncols * sizeof(float) : 0;
+  return p;
+}
+
+nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const nf4_weight* w,
+                     void* out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream) {
+  nf4_status st = check_weight(w);
+  if (st != NF4_OK) return st;
+  const int64_t N = w->N, K = w->K;
+  if (M < 0) return NF4_ERR_INVALID_ARG;
+  if (K % 64 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  const int64_t act_cols = mode == 0 ? K : N;
+  const int64_t out_cols = mode == 0 ? N : K;
+  if (ld_act < act_cols || ld_out < out_cols) return NF4_ERR_INVALID_ARG;
+  if (M == 0) return NF4_OK;
+  if (!act || !out) return NF4_ERR_INVALID_ARG;
+  if (ld_act % 8 != 0 || !aligned16(act) || !aligned16(w->packed)) return NF4_ERR_ALIGNMENT;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
+  DevInfo dev;
+  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (!dev.supported) return NF4_ERR_UNSUPPORTED;
+  const Plan p = plan_dense(mode, M, N, K, dev.sms);
+  if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
+
+  CUtensorMap tmap_act, tmap_pk;
+  if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, M, ld_act * 2, 64,
+                 p.bt, CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  if (mode == 0) {
+    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 32,
+                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+  } else {
+    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 64,
+                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+  }
+  nf4::GemmArgs a{};
+  a.M = M;
+  a.ncols = out_cols;
+  a.N_total = N;
+  a.K = K;
+  a.KB = K / 64;
+  a.N_e = N;
+  a.ksteps = p.ksteps;
+  a.wtiles = p.wtiles;
+  a.ttiles = p.ttiles;
+  a.splits = p.splits;
+  a.total_items = p.items;
+  a.grouped = 0;
+  a.E = 1;
+  a.offsets = nullptr;
+  a.absmax = w->absmax;
+  a.absmax_q = w->absmax_q;
+  a.nested_absmax = w->nested_absmax;
+  a.nested_offset = w->nested_offset;
+  a.code4 = w->code4;
+  a.code8 = w->code8;
+  a.dq = w->double_quant;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ld_out = ld_out;
+  a.ws = static_cast<float*>(ws);
+  a.status = dev.status;
+  const int grid = static_cast<int>(p.items < dev.sms ? p.items : dev.sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (nf4::launch_gemm(mode, p.bt, a, tmap_act, tmap_pk, grid, s) != cudaSuccess)
+    return NF4_ERR_CUDA;
+  count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
+  if (p.splits > 1) {
+    if (nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols,
+                                  static_cast<__nv_bfloat16*>(out), ld_out, s) != cudaSuccess)
+      return NF4_ERR_CUDA;
+    count(NF4_PATH_SPLITK_REDUCE);
+  }
+  return NF4_OK;
+}
+
+nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_t E, int64_t T,
+                       int64_t ld_act, const nf4_weight* w, int64_t N_e, void* out, int64_t ld_out,
+                       void* stream) {
+  nf4_status st = check_weight(w);
+  if (st != NF4_OK) return st;
+  const int64_t K = w->K;
+  if (E < 1 || E > nf4::kMaxExperts || T < 0 || N_e < 1 || !offsets) return NF4_ERR_INVALID_ARG;
+  if (w->N != static_cast<int64_t>(E) * N_e) return NF4_ERR_INVALID_ARG;
+  if (K % 64 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  const int64_t act_cols = mode == 0 ? K : N_e;
+  const int64_t out_cols = mode == 0 ? N_e : K;
+  if (ld_act < act_cols || ld_out < out_cols) return NF4_ERR_INVALID_ARG;
+  if (T == 0) return NF4_OK;
+  if (!act || !out) return NF4_ERR_INVALID_ARG;
+  if (ld_act % 8 != 0 || !aligned16(act) || !aligned16(w->packed)) return NF4_ERR_ALIGNMENT;
+  if (T > INT32_MAX || w->N > INT32_MAX || K > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
+  DevInfo dev;
+  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (!dev.supported) return NF4_ERR_UNSUPPORTED;
+  // Tokens per tile follow the mean rows per expert.
+  const int bt = choose_bt((T + E - 1) / E);
+  CUtensorMap tmap_act, tmap_pk;
+  if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, T, ld_act * 2, 64, bt,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  if (mode == 0) {
+    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, w->N, K / 2, 32,
+                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+  } else {
+    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, w->N, K / 2, 64,
+                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+  }
+  nf4::GemmArgs a{};
+  a.M = T;
+  a.ncols = out_cols;
+  a.N_total = w->N;
+  a.K = K;
+  a.KB = K / 64;
+  a.N_e = N_e;
+  a.ksteps = static_cast<int>(mode == 0 ? K / 64 : (N_e + 63) / 64);
+  a.wtiles = static_cast<int>((out_cols + nf4::kTileW - 1) / nf4::kTileW);
+  a.ttiles = 0;
+  a.splits = 1;
+  a.total_items = 0;
+  a.grouped = 1;
+  a.E = E;
+  a.offsets = offsets;
+  a.absmax = w->absmax;
+  a.absmax_q = w->absmax_q;
+  a.nested_absmax = w->nested_absmax;
+  a.nested_offset = w->nested_offset;
+  a.code4 = w->code4;
+  a.code8 = w->code8;
+  a.dq = w->double_quant;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ld_out = ld_out;
+  a.ws = nullptr;
+  a.status = dev.status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (nf4::launch_gemm(mode, bt, a, tmap_act, tmap_pk, dev.sms, s) != cudaSuccess)
+    return NF4_ERR_CUDA;
+  count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
+  return NF4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+nf4_status nf4_quantize(const void* W, int32_t w_dtype, int64_t N, int64_t K, int32_t blocksize,
+                        int32_t double_quant, int32_t nested_blocksize, const float* code4,
+                        const float* code8, uint8_t* packed, float* absmax, uint8_t* absmax_q,
+                        float* nested_absmax, float* nested_offset, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!W || !code4 || !packed || !absmax || N < 1 || K < 1) return NF4_ERR_INVALID_ARG;
+  if (w_dtype != NF4_DTYPE_F32 && w_dtype != NF4_DTYPE_BF16) return NF4_ERR_INVALID_ARG;
+  if (blocksize != 64) return NF4_ERR_UNSUPPORTED;
+  if (double_quant != 0 && double_quant != 1) return NF4_ERR_INVALID_ARG;
+  const int64_t numel = N * K;
+  const int64_t nblocks = (numel + 63) / 64;
+  if (double_quant) {
+    if (nested_blocksize != nf4::kNestedBlock) return NF4_ERR_UNSUPPORTED;
+    if (!code8 || !absmax_q || !nested_absmax || !nested_offset) return NF4_ERR_INVALID_ARG;
+    const size_t need = static_cast<size_t>((nblocks + nf4::kMeanChunk - 1) / nf4::kMeanChunk) * 8;
+    if (!ws || ws_bytes < need) return NF4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 7u) != 0) return NF4_ERR_ALIGNMENT;
+  }
+  DevInfo dev;
+  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (nf4::launch_quantize(W, w_dtype, numel, code4, packed, absmax, s) != cudaSuccess)
+    return NF4_ERR_CUDA;
+  count(NF4_PATH_QUANTIZE);
+  if (double_quant) {
+    if (nf4::launch_double_quant(absmax, nblocks, code8, absmax_q, nested_absmax, nested_offset,
+                                 static_cast<double*>(ws), s) != cudaSuccess)
+      return NF4_ERR_CUDA;
+  }
+  return NF4_OK;
+}
+
+nf4_status nf4_dequantize(const nf4_weight* w, void* out, int32_t out_dtype, void* stream) {
+  nf4_status st = check_weight(w);
+  if (st != NF4_OK) return st;
+  if (!out) return NF4_ERR_INVALID_ARG;
+  if (out_dtype != NF4_DTYPE_F32 && out_dtype != NF4_DTYPE_BF16) return NF4_ERR_INVALID_ARG;
+  DevInfo dev;
+  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (nf4::launch_dequantize(*w, out, out_dtype, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return NF4_ERR_CUDA;
+  count(NF4_PATH_DEQUANTIZE);
+  return NF4_OK;
+}
+
+nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
+                          int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(0, x, M, ldx, w, y, ldy, ws, ws_bytes, stream);
+}
+
+nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w, void* gx,
+                            int64_t ldgx, void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(1, gy, M, ldgy, w, gx, ldgx, ws, ws_bytes, stream);
+}
+
+nf4_status nf4_grouped_fwd(const void* x, const int32_t* offsets, int32_t E, int64_t T, int64_t ldx,
+                           const nf4_weight* w, int64_t N_e, void* y, int64_t ldy, void* stream) {
+  return run_grouped(0, x, offsets, E, T, ldx, w, N_e, y, ldy, stream);
+}
+
+nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, int64_t T,
+                             int64_t ldgy, const nf4_weight* w, int64_t N_e, void* gx, int64_t ldgx,
+                             void* stream) {
+  return run_grouped(1, gy, offsets, E, T, ldgy, w, N_e, gx, ldgx, stream);
+}
+
+size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E) {
+  (void)E;
+  if (op == NF4_OP_QUANTIZE) {
+    const int64_t nblocks = (N * K + 63) / 64;
+    return static_cast<size_t>((nblocks + nf4::kMeanChunk - 1) / nf4::kMeanChunk) * 8;
+  }
+  if (op == NF4_OP_LINEAR_FWD || op == NF4_OP_LINEAR_DGRAD) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    DevInfo dev;
+    if (!current_device(&dev)) return 0;
+    return plan_dense(op == NF4_OP_LINEAR_FWD ? 0 : 1, M, N, K, dev.sms).ws_bytes;
+  }
+  return 0;
+}
+
+const char* nf4_status_string(nf4_status s) {
+  switch (s) {
+    case NF4_OK: return "ok";
+    case NF4_ERR_INVALID_ARG: return "invalid argument";
+    case NF4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case NF4_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
+    case NF4_ERR_WORKSPACE: return "workspace too small";
+    case NF4_ERR_CUDA: return "CUDA error";
+    case NF4_ERR_TIMEOUT: return "device wait timed out";
+    case NF4_ERR_UNSUPPORTED: return "unsupported device or parameter";
+    case NF4_ERR_BAD_OFFSETS: return "expert offsets out of contract";
+  }
+  return "unknown status";
+}
+
+void nf4_get_path_counters(uint64_t* out) {
+  if (!out) return;
+  for (int i = 0; i < NF4_NUM_PATHS; ++i) out[i] = g_counters[i].load(std::memory_order_relaxed);
+}
+
+void nf4_reset_path_counters(void) {
+  for (int i = 0; i < NF4_NUM_PATHS; ++i) g_counters[i].store(0, std::memory_order_relaxed);
+}
+
+nf4_status nf4_device_status(int32_t* out, int32_t clear) {
+  if (!out) return NF4_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return NF4_ERR_CUDA;
+  *out = v;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return NF4_ERR_CUDA;
+  }
+  return NF4_OK;
+}
+
+nf4_status nf4_device_check(int32_t* sm_count) {
+  DevInfo dev;
+  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (sm_count) *sm_count = dev.sms;
+  return dev.supported ? NF4_OK : NF4_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+"""Torch-facing wrappers of the C ABI, one per entry point of ``include/nf4.h``.
+
+PyTorch only supplies device memory and the current stream; every step of the
+computation runs in the library's CUDA kernels.  Each wrapper checks that the
+tensors it passes live on a CUDA device and have the layout the ABI expects, then
+forwards raw pointers.  There is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+from . import codebooks
+
+BLOCKSIZE = 64
+NESTED_BLOCKSIZE = 256
+
+
+def _stream() -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(name: str, *ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name}: tensors must be on a CUDA device (no CPU path exists)")
+
+
+@dataclass
+class NF4Weight:
+    """A quantised frozen weight W [N, K]: the device tensors of the pages' quant
+    state (packed codes, absmax or its 8-bit codes with the nested statistics, the
+    codebooks) plus its shape."""
+    packed: torch.Tensor
+    absmax: Optional[torch.Tensor]
+    absmax_q: Optional[torch.Tensor]
+    nested_absmax: Optional[torch.Tensor]
+    nested_offset: Optional[torch.Tensor]
+    code4: torch.Tensor
+    code8: Optional[torch.Tensor]
+    N: int
+    K: int
+    double_quant: bool
+
+    def struct(self) -> _lib.nf4_weight:
+        return _lib.nf4_weight(
+            _ptr(self.packed), _ptr(self.absmax) if not self.double_quant else None,
+            _ptr(self.absmax_q) if self.double_quant else None,
+            _ptr(self.nested_absmax) if self.double_quant else None,
+            _ptr(self.nested_offset) if self.double_quant else None,
+            _ptr(self.code4), _ptr(self.code8) if self.double_quant else None,
+            self.N, self.K, BLOCKSIZE, NESTED_BLOCKSIZE, 1 if self.double_quant else 0)
+
+    def tensors(self) -> tuple:
+        """The tensors a backward needs, in a fixed order (for save_for_backward)."""
+        if self.double_quant:
+            return (self.packed, None, self.absmax_q, self.nested_absmax, self.nested_offset,
+                    self.code4, self.code8)
+        return (self.packed, self.absmax, None, None, None, self.code4, None)
+
+    @staticmethod
+    def from_tensors(t: tuple, N: int, K: int, double_quant: bool) -> "NF4Weight":
+        packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8 = t
+        return NF4Weight(packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8,
+                         N, K, double_quant)
+
+    def nbytes(self) -> int:
+        return sum(x.numel() * x.element_size() for x in self.tensors() if x is not None)
+
+
+def workspace_size(op: int, M: int, N: int, K: int, E: int = 0) -> int:
+    return int(_lib.lib().nf4_workspace_size(op, M, N, K, E))
+
+
+def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.Tensor] = None,
+             code8: Optional[torch.Tensor] = None) -> NF4Weight:
+    """nf4_quantize: blockwise NF4 (+ double quantisation) of a CUDA fp32/bf16 [N, K]."""
+    _need_cuda("quantize", W)
+    if W.dim() != 2 or not W.is_contiguous():
+        raise ValueError("quantize: W must be a contiguous [N, K] tensor")
+    if W.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("quantize: W must be fp32 or bf16")
+    dev = W.device
+    N, K = W.shape
+    numel = N * K
+    nblocks = (numel + BLOCKSIZE - 1) // BLOCKSIZE
+    code4 = (codebooks.nf4_code4() if code4 is None else code4).to(dev, torch.float32).contiguous()
+    code8 = (codebooks.dynamic_code8() if code8 is None else code8).to(dev, torch.float32).contiguous()
+    packed = torch.empty((numel + 1) // 2, dtype=torch.uint8, device=dev)
+    absmax = torch.empty(nblocks, dtype=torch.float32, device=dev)
+    absmax_q = nested = offset = ws = None
+    ws_bytes = 0
+    if double_quant:
+        absmax_q = torch.empty(nblocks, dtype=torch.uint8, device=dev)
+        nested = torch.empty((nblocks + NESTED_BLOCKSIZE - 1) // NESTED_BLOCKSIZE,
+                             dtype=torch.float32, device=dev)
+        offset = torch.empty(1, dtype=torch.float32, device=dev)
+        ws_bytes = workspace_size(_lib.OP_QUANTIZE, 0, N, K)
+        ws = torch.empty(max(ws_bytes, 8), dtype=torch.uint8, device=dev)
+    rc = _lib.lib().nf4_quantize(
+        _ptr(W), _lib.DTYPE_F32 if W.dtype == torch.float32 else _lib.DTYPE_BF16, N, K, BLOCKSIZE,
+        1 if double_quant else 0, NESTED_BLOCKSIZE, _ptr(code4), _ptr(code8) if double_quant else None,
+        _ptr(packed), _ptr(absmax), _ptr(absmax_q), _ptr(nested), _ptr(offset), _ptr(ws), ws_bytes,
+        _stream())
+    _lib.check(rc, "nf4_quantize")
+    return NF4Weight(packed, absmax, absmax_q, nested, offset, code4,
+                     code8 if double_quant else None, N, K, double_quant)
+
+
+def dequantize(w: NF4Weight, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """nf4_dequantize: dense [N, K] copy of the weight (checks only; not the fused path)."""
+    _need_cuda("dequantize", w.packed)
+    out = torch.empty(w.N, w.K, dtype=dtype, device=w.packed.device)
+    code = {torch.float32: _lib.DTYPE_F32, torch.bfloat16: _lib.DTYPE_BF16}[dtype]
+    s = w.struct()
+    _lib.check(_lib.lib().nf4_dequantize(ctypes.byref(s), _ptr(out), code, _stream()),
+               "nf4_dequantize")
+    return out
+
+
+def _check_act(name, a: torch.Tensor, cols: int):
+    _need_cuda(name, a)
+    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.shape[1] != cols or a.stride(1) != 1:
+        raise ValueError(f"{name}: expected a bf16 [rows, {cols}] tensor with unit column stride")
+
+
+def linear_fwd(x: torch.Tensor, w: NF4Weight, out: Optional[torch.Tensor] = None,
+               ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_linear_fwd: y = x W^T, x bf16 [M, K] -> y bf16 [M, N]."""
+    _check_act("linear_fwd", x, w.K)
+    M = x.shape[0]
+    y = torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device) if out is None else out
+    need = workspace_size(_lib.OP_LINEAR_FWD, M, w.N, w.K)
+    if need and (ws is None or ws.numel() * ws.element_size() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    s = w.struct()
+    rc = _lib.lib().nf4_linear_fwd(_ptr(x), M, x.stride(0), ctypes.byref(s), _ptr(y), y.stride(0),
+                                   _ptr(ws) if need else None, need, _stream())
+    _lib.check(rc, "nf4_linear_fwd")
+    return y
+
+
+def linear_dgrad(gy: torch.Tensor, w: NF4Weight, out: Optional[torch.Tensor] = None,
+                 ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_linear_dgrad: grad_x = grad_y W, gy bf16 [M, N] -> gx bf16 [M, K]."""
+    _check_act("linear_dgrad", gy, w.N)
+    M = gy.shape[0]
+    gx = torch.empty(M, w.K, dtype=torch.bfloat16, device=gy.device) if out is None else out
+    need = workspace_size(_lib.OP_LINEAR_DGRAD, M, w.N, w.K)
+    if need and (ws is None or ws.numel() * ws.element_size() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=gy.device)
+    s = w.struct()
+    rc = _lib.lib().nf4_linear_dgrad(_ptr(gy), M, gy.stride(0), ctypes.byref(s), _ptr(gx),
+                                     gx.stride(0), _ptr(ws) if need else None, need, _stream())
+    _lib.check(rc, "nf4_linear_dgrad")
+    return gx
+
+
+def grouped_fwd(x: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: int,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_grouped_fwd: rows offsets[e]..offsets[e+1] of x through expert e.
+    w is the stacked [E*N_e, K] weight; returns bf16 [T, N_e]."""
+    _check_act("grouped_fwd", x, w.K)
+    _need_cuda("grouped_fwd", offsets)
+    if offsets.dtype != torch.int32 or offsets.numel() != experts + 1:
+        raise ValueError("grouped_fwd: offsets must be int32 [E+1]")
+    N_e = w.N // experts
+    T = x.shape[0]
+    y = torch.empty(T, N_e, dtype=torch.bfloat16, device=x.device) if out is None else out
+    s = w.struct()
+    rc = _lib.lib().nf4_grouped_fwd(_ptr(x), _ptr(offsets), experts, T, x.stride(0), ctypes.byref(s),
+                                    N_e, _ptr(y), y.stride(0), _stream())
+    _lib.check(rc, "nf4_grouped_fwd")
+    return y
+
+
+def grouped_dgrad(gy: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: int,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_grouped_dgrad: per-expert grad_x; gy bf16 [T, N_e] -> gx bf16 [T, K]."""
+    N_e = w.N // experts
+    _check_act("grouped_dgrad", gy, N_e)
+    _need_cuda("grouped_dgrad", offsets)
+    if offsets.dtype != torch.int32 or offsets.numel() != experts + 1:
+        raise ValueError("grouped_dgrad: offsets must be int32 [E+1]")
+    T = gy.shape[0]
+    gx = torch.empty(T, w.K, dtype=torch.bfloat16, device=gy.device) if out is None else out
+    s = w.struct()
+    rc = _lib.lib().nf4_grouped_dgrad(_ptr(gy), _ptr(offsets), experts, T, gy.stride(0),
+                                      ctypes.byref(s), N_e, _ptr(gx), gx.stride(0), _stream())
+    _lib.check(rc, "nf4_grouped_dgrad")
+    return gx
+
+
+path_counters = _lib.path_counters
+reset_path_counters = _lib.reset_path_counters
+device_status = _lib.device_status
+device_check = _lib.device_check

@@ -1,0 +1,210 @@
+/*
+ * nf4.h -- C ABI of the GB300 (sm_103a) fused NF4 dequantise-and-multiply library.
+ *
+ * The operations are those of a frozen 4-bit Linear layer as the bitsandbytes
+ * pages describe it:
+ *   - quantize_4bit(w, blocksize=64, quant_type="nf4", compress_statistics=True)
+ *     (bitsandbytes issue "MatMul4Bit keeps B and quant_state on ctx ...",
+ *     section "Minimal reproducer");
+ *   - dequantize_4bit(B, state), and the state's tensors absmax, offset, code,
+ *     nested_absmax, nested_offset (same issue, sections "Root cause" and "Why
+ *     save_for_backward fixes it");
+ *   - the forward y = x W^T and the input gradient grad_x = grad_y W computed with
+ *     no dense weight materialised (Soup issue #842, "Design sketch"; frozen base,
+ *     "Scope"), with a deterministic reduction (same section: no atomics, no
+ *     non-deterministic split-K);
+ *   - a grouped per-expert variant (fork PR "Experts trainability ...", commits 1
+ *     and 2).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless a parameter says otherwise.  The caller
+ *     owns every buffer (inputs, outputs and workspace); the library never
+ *     allocates, frees or synchronises inside these calls.
+ *   - `stream` is a cudaStream_t passed as void*; all work is enqueued on it,
+ *     asynchronously.  NULL means the legacy default stream.
+ *   - Arguments are validated on the host before anything is launched; a failed
+ *     check returns an error status and launches nothing.  A CUDA launch failure
+ *     returns NF4_ERR_CUDA.
+ *   - Every device-side wait inside the kernels is bounded; a wait that runs out
+ *     records NF4_ERR_TIMEOUT in a device status word (nf4_device_status) and the
+ *     kernel returns instead of hanging.
+ *   - Results are bit-identical from run to run for identical inputs, on a given
+ *     device (the tile schedule depends only on the shapes and the SM count).
+ *   - Weight layout: W is [N, K] row-major (out_features x in_features), flattened
+ *     as i = n*K + k.  Blocks are consecutive runs of `blocksize` (64) values of
+ *     the flat array; nested blocks are consecutive runs of `nested_blocksize`
+ *     (256) blocks.  Packed byte j holds value 2j in its HIGH nibble and value 2j+1
+ *     in its LOW nibble.
+ *   - Activations and outputs are bf16, row-major with a leading dimension in
+ *     elements.
+ */
+#ifndef NF4_GB300_H
+#define NF4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NF4_OK = 0,
+  NF4_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum value      */
+  NF4_ERR_UNSUPPORTED_SHAPE = 2, /* e.g. K % 64 != 0 for the products                */
+  NF4_ERR_ALIGNMENT = 3,         /* pointer or leading dimension not 16-byte aligned */
+  NF4_ERR_WORKSPACE = 4,         /* workspace smaller than nf4_workspace_size()      */
+  NF4_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed              */
+  NF4_ERR_TIMEOUT = 6,           /* a bounded device wait ran out (device status)    */
+  NF4_ERR_UNSUPPORTED = 7,       /* no sm_100-family device, or feature not built    */
+  NF4_ERR_BAD_OFFSETS = 8        /* grouped: expert offsets not monotone / in range  */
+} nf4_status;
+
+enum { NF4_DTYPE_F32 = 0, NF4_DTYPE_BF16 = 1 };
+
+enum {
+  NF4_OP_QUANTIZE = 0,
+  NF4_OP_LINEAR_FWD = 1,
+  NF4_OP_LINEAR_DGRAD = 2,
+  NF4_OP_GROUPED_FWD = 3,
+  NF4_OP_GROUPED_DGRAD = 4
+};
+
+/* Path counters (nf4_get_path_counters): how many launches each kernel got.
+ * They prove which path produced a result (Soup issue #842, "Acceptance
+ * criteria": report with a counter proving which path actually ran). */
+enum {
+  NF4_PATH_LINEAR_FWD = 0,   /* fused tcgen05 forward                      */
+  NF4_PATH_LINEAR_DGRAD = 1, /* fused tcgen05 input gradient               */
+  NF4_PATH_SPLITK_REDUCE = 2,/* fixed-order reduction of split-K partials  */
+  NF4_PATH_GROUPED_FWD = 3,
+  NF4_PATH_GROUPED_DGRAD = 4,
+  NF4_PATH_DEQUANTIZE = 5,
+  NF4_PATH_QUANTIZE = 6,
+  NF4_PATH_TOTAL = 7,
+  NF4_NUM_PATHS = 8
+};
+
+/* A quantised weight: the tensors of the pages' QuantState as plain device
+ * pointers.  All are owned by the caller.
+ *   packed         [ceil(N*K/2)] uint8, two 4-bit codes per byte (high = even).
+ *   absmax         [nblocks] fp32 block absmax, nblocks = ceil(N*K/blocksize);
+ *                  used when double_quant == 0 (may be NULL otherwise).
+ *   absmax_q       [nblocks] uint8 8-bit codes of the absmax (double_quant == 1).
+ *   nested_absmax  [ceil(nblocks/nested_blocksize)] fp32 (double_quant == 1).
+ *   nested_offset  [1] fp32, the mean offset (double_quant == 1).
+ *   code4          [16] fp32 4-bit codebook (NF4 levels), strictly increasing.
+ *   code8          [256] fp32 8-bit map of the nested codes (double_quant == 1).
+ * Decoded block scale under double quantisation (two roundings, no FMA):
+ *   absmax'[b] = fp32(fp32(code8[absmax_q[b]] * nested_absmax[b/256]) + offset).
+ * Dequantised value: fp32(code4[q] * absmax'[block]); the products use its bf16
+ * rounding (round to nearest even) as the GEMM operand. */
+typedef struct {
+  const uint8_t* packed;
+  const float* absmax;
+  const uint8_t* absmax_q;
+  const float* nested_absmax;
+  const float* nested_offset;
+  const float* code4;
+  const float* code8;
+  int64_t N;
+  int64_t K;
+  int32_t blocksize;        /* must be 64 */
+  int32_t nested_blocksize; /* must be 256 when double_quant */
+  int32_t double_quant;     /* 0 or 1 */
+} nf4_weight;
+
+/* nf4_quantize -- blockwise NF4 quantisation of W (quantize_4bit of bitsandbytes
+ * issue "MatMul4Bit keeps B and quant_state on ctx", "Minimal reproducer"), with
+ * optional double quantisation of the absmax (compress_statistics=True; "Root
+ * cause").  Offline step, bit-exact with the CPU oracle.
+ *   W        [numel = N*K] device array, fp32 or bf16 (w_dtype).
+ *   blocksize 64.  Any numel >= 1; the last block may be short.
+ *   Per block: a = max|w|; v = w / a (IEEE division); code = nearest level of
+ *   code4 by fp64 midpoints, ties to the lower index; a == 0 -> index of the 0.
+ *   Outputs: packed [ceil(numel/2)], absmax [nblocks] (always written), and when
+ *   double_quant: absmax_q [nblocks], nested_absmax [ceil(nblocks/256)],
+ *   nested_offset [1] (offset = fp32 of the mean of absmax, summed in fp64 over
+ *   chunks of 1024 then over chunk sums; residuals quantised to code8 by nearest
+ *   level, per nested block of 256 scaled by the residuals' max magnitude).
+ *   ws: device workspace of nf4_workspace_size(NF4_OP_QUANTIZE, 0, N, K, 0) bytes
+ *   (fp64 chunk sums; may be NULL when double_quant == 0). */
+nf4_status nf4_quantize(const void* W, int32_t w_dtype, int64_t N, int64_t K, int32_t blocksize,
+                        int32_t double_quant, int32_t nested_blocksize, const float* code4,
+                        const float* code8, uint8_t* packed, float* absmax, uint8_t* absmax_q,
+                        float* nested_absmax, float* nested_offset, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* nf4_dequantize -- dense dequantisation of a quantised weight (dequantize_4bit,
+ * bitsandbytes issue "MatMul4Bit keeps B and quant_state on ctx", "Root cause").
+ * Not on the fused path; provided for checks and for callers that need a dense
+ * copy.  out: [N*K] fp32 (value wf) or bf16 (round-to-nearest-even of wf),
+ * per out_dtype.  Bit-exact with the oracle. */
+nf4_status nf4_dequantize(const nf4_weight* w, void* out, int32_t out_dtype, void* stream);
+
+/* nf4_linear_fwd -- fused forward y = x W^T straight from the packed codes and the
+ * (nested) statistics; the dequantised bf16 tile exists only in shared memory
+ * (Soup issue #842, "Design sketch").
+ *   x  [M, K] bf16, leading dimension ldx (elements, multiple of 8, ldx >= K).
+ *   y  [M, N] bf16, leading dimension ldy (>= N).
+ *   M >= 0 (M == 0 is a no-op); K % 64 == 0; x 16-byte aligned.
+ *   ws: device workspace of nf4_workspace_size(NF4_OP_LINEAR_FWD, M, N, K, 0)
+ *   bytes (split-K partials for small M; may be NULL when that size is 0).
+ *   fp32 accumulation on the tensor cores; split-K partials, when used, are summed
+ *   in a fixed order by a second kernel.  No atomics. */
+nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
+                          int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+
+/* nf4_linear_dgrad -- fused input gradient grad_x = grad_y W (the backward of
+ * MatMul4Bit, bitsandbytes issue "MatMul4Bit keeps B and quant_state on ctx",
+ * "Root cause"; only grad_x since the base is frozen, Soup issue #842 "Scope").
+ *   gy [M, N] bf16, leading dimension ldgy (multiple of 8, >= N).
+ *   gx [M, K] bf16, leading dimension ldgx (>= K).
+ *   Same rules as nf4_linear_fwd; workspace from NF4_OP_LINEAR_DGRAD. */
+nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w, void* gx,
+                            int64_t ldgx, void* ws, size_t ws_bytes, void* stream);
+
+/* nf4_grouped_fwd -- per-expert forward for a stack of E frozen experts quantised
+ * as one tensor (fork PR "Experts trainability ...", commit 1: the fused 3-D
+ * expert stack; commit 2: no dequantised weight is kept).
+ *   w        the stacked weight: w->N == E * N_e rows, expert e owns rows
+ *            [e*N_e, (e+1)*N_e); w->K = K.
+ *   offsets  DEVICE int32 [E+1]: rows offsets[e] .. offsets[e+1]-1 of x belong to
+ *            expert e; offsets[0] == 0, non-decreasing, offsets[E] == T.  Offsets
+ *            outside that contract are detected on the device: the bad expert's
+ *            rows are skipped and NF4_ERR_BAD_OFFSETS is recorded in the device
+ *            status word.
+ *   x [T, K] bf16 (ldx), y [T, N_e] bf16 (ldy).  No workspace is needed. */
+nf4_status nf4_grouped_fwd(const void* x, const int32_t* offsets, int32_t E, int64_t T, int64_t ldx,
+                           const nf4_weight* w, int64_t N_e, void* y, int64_t ldy, void* stream);
+
+/* nf4_grouped_dgrad -- per-expert input gradient gx[rows of e] = gy[rows of e] W_e.
+ *   gy [T, N_e] bf16 (ldgy), gx [T, K] bf16 (ldgx); other arguments as above. */
+nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, int64_t T,
+                             int64_t ldgy, const nf4_weight* w, int64_t N_e, void* gx, int64_t ldgx,
+                             void* stream);
+
+/* Workspace bytes an operation needs for the given shape on the current device
+ * (0 when none).  op is one of NF4_OP_*; E is unused for the dense products. */
+size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E);
+
+/* Static string naming a status code. */
+const char* nf4_status_string(nf4_status s);
+
+/* Copies the NF4_NUM_PATHS host-side launch counters into out (host array). */
+void nf4_get_path_counters(uint64_t* out);
+void nf4_reset_path_counters(void);
+
+/* Reads (and with clear != 0, resets) the device status word of the current
+ * device into *out (host int).  Synchronises with the device; not for hot paths. */
+nf4_status nf4_device_status(int32_t* out, int32_t clear);
+
+/* Library and device information: returns NF4_OK when the current device is an
+ * sm_100-family GPU the kernels were built for; *sm_count receives its SM count. */
+nf4_status nf4_device_check(int32_t* sm_count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NF4_GB300_H */

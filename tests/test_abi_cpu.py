@@ -1,0 +1,76 @@
+"""The C-ABI library builds, loads without a GPU, exports every function that
+include/nf4.h declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+
+import pytest
+
+from bit_nf4_quantized_linear_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return _lib.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = _lib.header_functions()
+    assert {"nf4_quantize", "nf4_dequantize", "nf4_linear_fwd", "nf4_linear_dgrad",
+            "nf4_grouped_fwd", "nf4_grouped_dgrad", "nf4_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(9):
+        s = L.nf4_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert L.nf4_status_string(0) == b"ok"
+
+
+def _weight(N=128, K=128, dq=0, blocksize=64):
+    # Non-null dummy host addresses: validation must fail before anything is read.
+    dummy = ctypes.c_void_p(0x1000)
+    return _lib.nf4_weight(dummy, dummy, dummy, dummy, dummy, dummy, dummy, N, K, blocksize, 256, dq)
+
+
+def test_host_validation_rejects_before_launch(L):
+    w = _weight(K=100)
+    x = ctypes.c_void_p(0x1000)
+    assert L.nf4_linear_fwd(x, 4, 128, ctypes.byref(w), x, 128, None, 0, None) == 2  # K % 64
+    w = _weight(blocksize=32)
+    assert L.nf4_linear_fwd(x, 4, 128, ctypes.byref(w), x, 128, None, 0, None) == 7
+    assert L.nf4_linear_fwd(x, 4, 128, None, x, 128, None, 0, None) == 1
+    w = _weight()
+    assert L.nf4_linear_fwd(x, -1, 128, ctypes.byref(w), x, 128, None, 0, None) == 1
+    assert L.nf4_linear_fwd(x, 4, 64, ctypes.byref(w), x, 128, None, 0, None) == 1  # ldx < K
+    # M == 0 is a no-op that touches nothing
+    assert L.nf4_linear_fwd(None, 0, 128, ctypes.byref(w), None, 128, None, 0, None) == 0
+    assert L.nf4_linear_dgrad(None, 0, 128, ctypes.byref(w), None, 128, None, 0, None) == 0
+    # misaligned activation pointer / leading dimension
+    bad = ctypes.c_void_p(0x1002)
+    assert L.nf4_linear_fwd(bad, 4, 128, ctypes.byref(w), x, 128, None, 0, None) == 3
+    assert L.nf4_linear_fwd(x, 4, 132, ctypes.byref(w), x, 128, None, 0, None) == 3
+    # grouped: N must be E * N_e, E in range, offsets non-null
+    off = ctypes.c_void_p(0x1000)
+    assert L.nf4_grouped_fwd(x, off, 3, 10, 128, ctypes.byref(w), 64, x, 64, None) == 1
+    assert L.nf4_grouped_fwd(x, None, 2, 10, 128, ctypes.byref(w), 64, x, 64, None) == 1
+    assert L.nf4_grouped_fwd(x, off, 0, 10, 128, ctypes.byref(w), 64, x, 64, None) == 1
+    assert L.nf4_grouped_fwd(x, off, 2, 0, 128, ctypes.byref(w), 64, None, 64, None) == 0
+    # double quant without its tensors
+    wd = _lib.nf4_weight(x, None, None, None, None, x, None, 128, 128, 64, 256, 1)
+    assert L.nf4_linear_fwd(x, 4, 128, ctypes.byref(wd), x, 128, None, 0, None) == 1
+    # quantize: bad block size, missing workspace for double quantisation
+    assert L.nf4_quantize(x, 0, 4, 64, 32, 0, 256, x, x, x, x, x, x, x, None, 0, None) == 7
+    assert L.nf4_quantize(x, 0, 4, 64, 64, 1, 256, x, x, x, x, x, x, x, None, 0, None) == 4
+    assert L.nf4_quantize(x, 9, 4, 64, 64, 0, 256, x, x, x, x, x, x, x, None, 0, None) == 1
+
+
+def test_quantize_workspace_size(L):
+    assert L.nf4_workspace_size(0, 0, 4096, 4096, 0) == ((4096 * 4096 // 64 + 1023) // 1024) * 8
+    assert L.nf4_workspace_size(0, 0, 1, 64, 0) == 8
+
+
+def test_path_counters_start_at_zero(L):
+    _lib.reset_path_counters()
+    assert all(v == 0 for v in _lib.path_counters().values())

@@ -1,0 +1,264 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Bit-exact: packed codes, absmax, nested statistics, dense dequantisation, and the
+identity probe (a one-hot activation selects one dequantised weight exactly).
+Within tolerance (relative Frobenius <= 5e-3, per element <= 1e-2 (|ref| + rms)):
+the forward and input-gradient products against the oracle's fp64 sums.
+Bit-identical across reruns.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import codebooks as ocb
+import bit_nf4_quantized_linear_gb300 as nf4
+from bit_nf4_quantized_linear_gb300 import synth
+from tests.helpers import bf16_bits, oracle_state, parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    nf4.device_check()
+    nf4.device_status(clear=True)
+    yield
+    assert nf4.device_status() == 0, "a kernel recorded a device error"
+
+
+def _quant_pair(N, K, dq, seed=0, code8=None, dtype=torch.float32):
+    g = synth.generator(seed)
+    w32 = synth.weight(N, K, g)
+    if dtype == torch.bfloat16:
+        w32 = w32.to(torch.bfloat16).float()
+    w = nf4.quantize(w32.to(DEV, dtype), double_quant=dq,
+                     code8=None if code8 is None else torch.from_numpy(code8))
+    st = oracle_state(w32, dq, code8)
+    return w, st, g
+
+
+def _assert_state_equal(w, st):
+    np.testing.assert_array_equal(w.packed.cpu().numpy(), st.packed)
+    np.testing.assert_array_equal(w.absmax.cpu().numpy().view(np.uint32), st.absmax.view(np.uint32))
+    if st.double_quant:
+        np.testing.assert_array_equal(w.absmax_q.cpu().numpy(), st.absmax_q)
+        np.testing.assert_array_equal(w.nested_absmax.cpu().numpy().view(np.uint32),
+                                      st.nested_absmax.view(np.uint32))
+        np.testing.assert_array_equal(w.nested_offset.cpu().numpy().view(np.uint32),
+                                      st.nested_offset.view(np.uint32))
+
+
+# ------------------------------------------------------- quantise / dequantise --
+
+@pytest.mark.parametrize("N,K,dq", [(64, 64, False), (256, 512, True), (1024, 1024, False),
+                                    (4096, 4096, True), (3, 100, True), (1, 17, False),
+                                    (1000, 1344, True)])
+def test_quantize_bit_exact(N, K, dq):
+    w, st, _ = _quant_pair(N, K, dq)
+    torch.cuda.synchronize()
+    _assert_state_equal(w, st)
+
+
+def test_quantize_bf16_input_and_linear_code8():
+    w, st, _ = _quant_pair(512, 768, True, code8=ocb.linear_code8(), dtype=torch.bfloat16)
+    _assert_state_equal(w, st)
+
+
+@pytest.mark.parametrize("N,K,dq", [(256, 512, True), (1024, 1024, False), (5, 77, True)])
+def test_dequantize_bit_exact(N, K, dq):
+    w, st, _ = _quant_pair(N, K, dq)
+    f32 = nf4.dequantize(w, torch.float32).cpu().numpy().reshape(-1)
+    b16 = bf16_bits(nf4.dequantize(w, torch.bfloat16)).reshape(-1)
+    np.testing.assert_array_equal(f32.view(np.uint32), oracle.dequantize(st, "f32").reshape(-1).view(np.uint32))
+    np.testing.assert_array_equal(b16, oracle.dequantize(st, "bf16").reshape(-1))
+
+
+# ------------------------------------------------------------------ products --
+
+SMALL = [  # (M, N, K): several tiles, ragged tails, every token-tile width
+    (1, 256, 256), (5, 384, 512), (16, 128, 1024), (17, 200, 192), (40, 320, 192),
+    (64, 640, 256), (100, 1000, 640), (128, 256, 128), (129, 384, 320), (300, 200, 256),
+    (700, 640, 1024),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+@pytest.mark.parametrize("dq", [False, True])
+def test_fwd_dgrad_parity_small(M, N, K, dq):
+    w, st, g = _quant_pair(N, K, dq, seed=M + N + K)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"dgrad {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("K,N", [(128, 256), (256, 384), (1024, 512)])
+def test_identity_probe_fwd_exact(K, N):
+    # x = I_K: y[m, n] = Wb[n, m] exactly, so the in-kernel dequantisation is
+    # checked bit for bit (large token tiles), and again with 16 one-hot rows
+    # (the split-contraction path).
+    w, st, _ = _quant_pair(N, K, True, seed=K)
+    wb = oracle.dequantize(st, "bf16")
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    y = nf4.linear_fwd(eye.to(DEV), w)
+    np.testing.assert_array_equal(bf16_bits(y), np.ascontiguousarray(wb.T))
+    y16 = nf4.linear_fwd(eye[:16].contiguous().to(DEV), w)
+    np.testing.assert_array_equal(bf16_bits(y16), np.ascontiguousarray(wb.T[:16]))
+
+
+@pytest.mark.parametrize("N,K", [(128, 256), (384, 256), (1024, 512)])
+def test_identity_probe_dgrad_exact(N, K):
+    w, st, _ = _quant_pair(N, K, True, seed=N)
+    wb = oracle.dequantize(st, "bf16")
+    eye = torch.eye(N, dtype=torch.bfloat16)
+    gx = nf4.linear_dgrad(eye.to(DEV), w)
+    np.testing.assert_array_equal(bf16_bits(gx), wb)
+    gx16 = nf4.linear_dgrad(eye[:16].contiguous().to(DEV), w)
+    np.testing.assert_array_equal(bf16_bits(gx16), wb[:16])
+
+
+@pytest.mark.parametrize("M", [1, 40, 700])
+def test_reruns_bit_identical(M):
+    N, K = 1024, 1024
+    w, st, g = _quant_pair(N, K, True, seed=3)
+    x = synth.activation(M, K, g).to(DEV)
+    gy = synth.activation(M, N, g).to(DEV)
+    y0, gx0 = nf4.linear_fwd(x, w), nf4.linear_dgrad(gy, w)
+    for _ in range(10):
+        assert torch.equal(nf4.linear_fwd(x, w).view(torch.int16), y0.view(torch.int16))
+        assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx0.view(torch.int16))
+
+
+def test_strided_activation_and_output():
+    N, K, M = 256, 320, 33
+    w, st, g = _quant_pair(N, K, False, seed=5)
+    xbig = synth.activation(M, K + 64, g)
+    x = xbig[:, 32:32 + K]
+    ybig = torch.zeros(M, N + 8, dtype=torch.bfloat16, device=DEV)
+    nf4.linear_fwd(xbig.to(DEV)[:, 32:32 + K], w, out=ybig[:, :N])
+    parity(ybig[:, :N], oracle.linear_fwd(bf16_bits(x.contiguous()), oracle.dequantize(st, "bf16")))
+    assert torch.all(ybig[:, N:] == 0)
+
+
+def test_empty_batch_is_noop():
+    w, _, _ = _quant_pair(128, 128, True)
+    y = nf4.linear_fwd(torch.empty(0, 128, dtype=torch.bfloat16, device=DEV), w)
+    assert y.shape == (0, 128)
+
+
+def test_errors_are_reported():
+    w, _, _ = _quant_pair(128, 128, False)
+    x = torch.zeros(4, 129, dtype=torch.bfloat16, device=DEV)[:, 1:]  # 2-byte offset
+    with pytest.raises(nf4.ops._lib.NF4Error) as e:
+        nf4.linear_fwd(x, w)
+    assert e.value.code == 3
+    with pytest.raises(ValueError):
+        nf4.linear_fwd(torch.zeros(4, 128, dtype=torch.bfloat16), w)  # CPU tensor: no CPU path
+
+
+# ----------------------------------------------------------- full-size sampled --
+
+def _sampled_rows(M, n=6, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(M, size=min(n, M), replace=False).tolist())
+    rows |= {0, M - 1}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("M", synth.M_SWEEP)
+def test_m_sweep_4096_sampled(M):
+    N = K = 4096
+    w, st, g = _quant_pair(N, K, True, seed=11)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    rows = _sampled_rows(M)
+    parity(y[torch.from_numpy(rows).to(DEV)], oracle.linear_fwd(bf16_bits(x), wb, rows), f"fwd M={M}")
+    parity(gx[torch.from_numpy(rows).to(DEV)], oracle.linear_dgrad(bf16_bits(gy), wb, rows), f"dgrad M={M}")
+
+
+@pytest.mark.parametrize("name,K,N", synth.LLAMA8B_PROJ)
+def test_llama8b_projection_set_sampled(name, K, N):
+    M = 512
+    w, st, g = _quant_pair(N, K, True, seed=hash(name) % 1000)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    rows = _sampled_rows(M, 4)
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    parity(y[torch.from_numpy(rows).to(DEV)], oracle.linear_fwd(bf16_bits(x), wb, rows), name)
+    parity(gx[torch.from_numpy(rows).to(DEV)], oracle.linear_dgrad(bf16_bits(gy), wb, rows), name)
+
+
+def test_config1_single_linear_full():
+    # x [256, 1024], W [1024, 1024], fp32 absmax: compared in full.
+    w, st, g = _quant_pair(1024, 1024, False, seed=0)
+    x = synth.activation(256, 1024, g)
+    gy = synth.activation(256, 1024, g)
+    wb = oracle.dequantize(st, "bf16")
+    parity(nf4.linear_fwd(x.to(DEV), w), oracle.linear_fwd(bf16_bits(x), wb), "cfg1 fwd")
+    parity(nf4.linear_dgrad(gy.to(DEV), w), oracle.linear_dgrad(bf16_bits(gy), wb), "cfg1 dgrad")
+
+
+# ------------------------------------------------------------------- grouped --
+
+def _grouped_case(E, N_e, K, tokens, topk, dq, seed):
+    g = synth.generator(seed)
+    w32 = synth.weight(E * N_e, K, g)
+    row_token, offsets = synth.routing(tokens, E, topk, g)
+    xt = synth.activation(tokens, K, g)
+    x = xt[row_token].contiguous()
+    T = x.shape[0]
+    gy = synth.activation(T, N_e, g)
+    w = nf4.quantize(w32.to(DEV), double_quant=dq)
+    st = oracle_state(w32, dq)
+    wb = oracle.dequantize(st, "bf16").reshape(E, N_e, K)
+    return w, wb, x, gy, offsets
+
+
+@pytest.mark.parametrize("dq", [False, True])
+def test_grouped_small_ragged(dq):
+    E, N_e, K = 6, 192, 256
+    w, wb, x, gy, offsets = _grouped_case(E, N_e, K, 50, 2, dq, seed=21)
+    offs = offsets.numpy()
+    y = nf4.grouped_fwd(x.to(DEV), offsets.to(DEV), w, E)
+    gx = nf4.grouped_dgrad(gy.to(DEV), offsets.to(DEV), w, E)
+    parity(y, oracle.grouped_fwd(bf16_bits(x), offs, wb), "grouped fwd")
+    parity(gx, oracle.grouped_dgrad(bf16_bits(gy), offs, wb), "grouped dgrad")
+
+
+@pytest.mark.parametrize("proj", ["gate", "down"])
+def test_grouped_olmoe_experts(proj):
+    c = synth.OLMOE
+    E = c["experts"]
+    N_e, K = (c["inter"], c["hidden"]) if proj == "gate" else (c["hidden"], c["inter"])
+    w, wb, x, gy, offsets = _grouped_case(E, N_e, K, c["tokens"], c["topk"], False, seed=31)
+    offs = offsets.numpy()
+    y = nf4.grouped_fwd(x.to(DEV), offsets.to(DEV), w, E)
+    gx = nf4.grouped_dgrad(gy.to(DEV), offsets.to(DEV), w, E)
+    parity(y, oracle.grouped_fwd(bf16_bits(x), offs, wb), f"olmoe {proj} fwd")
+    parity(gx, oracle.grouped_dgrad(bf16_bits(gy), offs, wb), f"olmoe {proj} dgrad")
+
+
+def test_grouped_empty_experts_and_bad_offsets():
+    E, N_e, K = 4, 128, 128
+    w, wb, x, gy, _ = _grouped_case(E, N_e, K, 20, 1, False, seed=41)
+    offs = np.array([0, 0, 20, 20, 20], dtype=np.int32)
+    y = nf4.grouped_fwd(x.to(DEV), torch.from_numpy(offs).to(DEV), w, E)
+    parity(y, oracle.grouped_fwd(bf16_bits(x), offs, wb), "empty experts")
+    nf4.device_status(clear=True)
+    bad = torch.tensor([0, 15, 5, 20, 20], dtype=torch.int32, device=DEV)
+    nf4.grouped_fwd(x.to(DEV), bad, w, E)
+    torch.cuda.synchronize()
+    assert nf4.device_status(clear=True) == 8
