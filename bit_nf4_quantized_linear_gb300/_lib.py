@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "nf4_reset_path_counters": [],
             "nf4_device_status": [P, I32],
             "nf4_device_check": [P],
+            "nf4_last_cuda_error": [],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -93,6 +94,7 @@ def lib() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         L.nf4_workspace_size.restype = ctypes.c_size_t
         L.nf4_status_string.restype = ctypes.c_char_p
+        L.nf4_last_cuda_error.restype = ctypes.c_char_p
         L.nf4_get_path_counters.restype = None
         L.nf4_reset_path_counters.restype = None
         _lib = L
@@ -101,6 +103,8 @@ def lib() -> ctypes.CDLL:
 
 def check(rc: int, what: str):
     if rc != NF4_OK:
+        if rc == 5:
+            what = f"{what} ({lib().nf4_last_cuda_error().decode()})"
         raise NF4Error(what, rc)
 
 

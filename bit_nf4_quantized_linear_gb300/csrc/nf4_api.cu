@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 #include "internal.h"
@@ -15,6 +16,15 @@
 namespace {
 
 std::atomic<uint64_t> g_counters[NF4_NUM_PATHS];
+thread_local char g_last_error[512] = "no error";
+
+// Records a failed CUDA call and maps it to NF4_ERR_CUDA.
+nf4_status cuda_fail(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) e = cudaErrorUnknown;
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorString(e),
+                cudaGetErrorName(e));
+  return NF4_ERR_CUDA;
+}
 
 // Device status word: kernels record NF4_ERR_TIMEOUT / NF4_ERR_BAD_OFFSETS here.
 __device__ int g_device_status;
@@ -31,9 +41,19 @@ struct DevInfo {
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 
+thread_local int t_bound_device = -1;
+
+// The current device's cached properties.  The first call on a thread (and after
+// a device switch) binds the device's primary context to the thread: driver calls
+// such as cuTensorMapEncodeTiled need a current context, and threads the caller
+// did not initialise (e.g. autograd's backward worker) have none yet.
 bool current_device(DevInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (t_bound_device != dev) {
+    if (cudaSetDevice(dev) != cudaSuccess) return false;
+    t_bound_device = dev;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   DevInfo& d = g_dev[dev];
   if (!d.ok) {
@@ -71,7 +91,10 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle sw) {
   auto fn = tensor_map_encoder();
-  if (!fn) return false;
+  if (!fn) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled entry point not found");
+    return false;
+  }
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
@@ -79,6 +102,13 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "cuTensorMapEncodeTiled failed (CUresult %d): base %p dims %llu x %llu stride %llu "
+                  "box %u x %u",
+                  static_cast<int>(r), base, static_cast<unsigned long long>(inner),
+                  static_cast<unsigned long long>(outer), static_cast<unsigned long long>(row_bytes),
+                  box_inner, box_outer);
   return r == CUDA_SUCCESS;
 }
 
@@ -160,7 +190,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   if (ld_act % 8 != 0 || !aligned16(act) || !aligned16(w->packed)) return NF4_ERR_ALIGNMENT;
   if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
   DevInfo dev;
-  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   const Plan p = plan_dense(mode, M, N, K, dev.sms);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
@@ -206,13 +236,13 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.status = dev.status;
   const int grid = static_cast<int>(p.items < dev.sms ? p.items : dev.sms);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (nf4::launch_gemm(mode, p.bt, a, tmap_act, tmap_pk, grid, s) != cudaSuccess)
-    return NF4_ERR_CUDA;
+  cudaError_t le = nf4::launch_gemm(mode, p.bt, a, tmap_act, tmap_pk, grid, s);
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
   if (p.splits > 1) {
-    if (nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols,
-                                  static_cast<__nv_bfloat16*>(out), ld_out, s) != cudaSuccess)
-      return NF4_ERR_CUDA;
+    le = nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols,
+                                   static_cast<__nv_bfloat16*>(out), ld_out, s);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
     count(NF4_PATH_SPLITK_REDUCE);
   }
   return NF4_OK;
@@ -235,7 +265,7 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   if (ld_act % 8 != 0 || !aligned16(act) || !aligned16(w->packed)) return NF4_ERR_ALIGNMENT;
   if (T > INT32_MAX || w->N > INT32_MAX || K > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
   DevInfo dev;
-  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   // Tokens per tile follow the mean rows per expert.
   const int bt = choose_bt((T + E - 1) / E);
@@ -279,8 +309,8 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   a.ws = nullptr;
   a.status = dev.status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (nf4::launch_gemm(mode, bt, a, tmap_act, tmap_pk, dev.sms, s) != cudaSuccess)
-    return NF4_ERR_CUDA;
+  cudaError_t le = nf4::launch_gemm(mode, bt, a, tmap_act, tmap_pk, dev.sms, s);
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
   return NF4_OK;
 }
@@ -308,15 +338,15 @@ nf4_status nf4_quantize(const void* W, int32_t w_dtype, int64_t N, int64_t K, in
     if ((reinterpret_cast<uintptr_t>(ws) & 7u) != 0) return NF4_ERR_ALIGNMENT;
   }
   DevInfo dev;
-  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (nf4::launch_quantize(W, w_dtype, numel, code4, packed, absmax, s) != cudaSuccess)
-    return NF4_ERR_CUDA;
+  cudaError_t le = nf4::launch_quantize(W, w_dtype, numel, code4, packed, absmax, s);
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(NF4_PATH_QUANTIZE);
   if (double_quant) {
-    if (nf4::launch_double_quant(absmax, nblocks, code8, absmax_q, nested_absmax, nested_offset,
-                                 static_cast<double*>(ws), s) != cudaSuccess)
-      return NF4_ERR_CUDA;
+    le = nf4::launch_double_quant(absmax, nblocks, code8, absmax_q, nested_absmax, nested_offset,
+                                  static_cast<double*>(ws), s);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   }
   return NF4_OK;
 }
@@ -327,9 +357,9 @@ nf4_status nf4_dequantize(const nf4_weight* w, void* out, int32_t out_dtype, voi
   if (!out) return NF4_ERR_INVALID_ARG;
   if (out_dtype != NF4_DTYPE_F32 && out_dtype != NF4_DTYPE_BF16) return NF4_ERR_INVALID_ARG;
   DevInfo dev;
-  if (!current_device(&dev)) return NF4_ERR_CUDA;
-  if (nf4::launch_dequantize(*w, out, out_dtype, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return NF4_ERR_CUDA;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
+  cudaError_t le = nf4::launch_dequantize(*w, out, out_dtype, static_cast<cudaStream_t>(stream));
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(NF4_PATH_DEQUANTIZE);
   return NF4_OK;
 }
@@ -397,18 +427,22 @@ void nf4_reset_path_counters(void) {
 nf4_status nf4_device_status(int32_t* out, int32_t clear) {
   if (!out) return NF4_ERR_INVALID_ARG;
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return NF4_ERR_CUDA;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "device status copy");
   *out = v;
   if (clear) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return NF4_ERR_CUDA;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "device status copy");
   }
   return NF4_OK;
 }
 
+const char* nf4_last_cuda_error(void) { return g_last_error; }
+
 nf4_status nf4_device_check(int32_t* sm_count) {
   DevInfo dev;
-  if (!current_device(&dev)) return NF4_ERR_CUDA;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (sm_count) *sm_count = dev.sms;
   return dev.supported ? NF4_OK : NF4_ERR_UNSUPPORTED;
 }

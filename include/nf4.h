@@ -199,6 +199,10 @@ void nf4_reset_path_counters(void);
  * device into *out (host int).  Synchronises with the device; not for hot paths. */
 nf4_status nf4_device_status(int32_t* out, int32_t clear);
 
+/* Human-readable message of the last CUDA error that made a call of this thread
+ * return NF4_ERR_CUDA ("no error" if none).  Static string. */
+const char* nf4_last_cuda_error(void);
+
 /* Library and device information: returns NF4_OK when the current device is an
  * sm_100-family GPU the kernels were built for; *sm_count receives its SM count. */
 nf4_status nf4_device_check(int32_t* sm_count);
