@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(PKG, "libnf4.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "nf4.h")
 
 NF4_OK = 0
+NOALLOC_SCRATCH_BYTES = 4 << 20  # NF4_NOALLOC_SCRATCH_BYTES of include/nf4.h
 STATUS_NAMES = {
     0: "NF4_OK", 1: "NF4_ERR_INVALID_ARG", 2: "NF4_ERR_UNSUPPORTED_SHAPE", 3: "NF4_ERR_ALIGNMENT",
     4: "NF4_ERR_WORKSPACE", 5: "NF4_ERR_CUDA", 6: "NF4_ERR_TIMEOUT", 7: "NF4_ERR_UNSUPPORTED",
@@ -87,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "nf4_device_status": [P, I32],
             "nf4_device_check": [P],
             "nf4_last_cuda_error": [],
+            "nf4_linear_fwd_noalloc": [P, I64, I64, W, P, I64, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)

@@ -448,3 +448,63 @@ nf4_status nf4_device_check(int32_t* sm_count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.
+//
+// For callers that cannot call cudaMalloc -- e.g. code running under an
+// allocator that owns all device memory and forbids direct allocation, or a
+// plugin that is handed only its input and output buffers -- this variant of
+// nf4_linear_fwd takes no workspace.  Its split-contraction partials live in a
+// fixed file-scope device array instead, so the call itself allocates nothing.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NF4_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];  // device address of the array, per device
+
+// Device address of the scratch array on the current device.  Host code cannot
+// use the symbol itself (on the host it names a stand-in, not device memory), so
+// the address is looked up once per device, with that device current.
+nf4_status noalloc_scratch(void** out) {
+  DevInfo dev;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[d]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_addr[d] = p;
+  }
+  *out = g_noalloc_addr[d];
+  return NF4_OK;
+}
+
+}  // namespace
+
+extern "C" nf4_status nf4_linear_fwd_noalloc(const void* x, int64_t M, int64_t ldx,
+                                             const nf4_weight* w, void* y, int64_t ldy,
+                                             void* stream) {
+  nf4_status st = check_weight(w);
+  if (st != NF4_OK) return st;
+  if (M < 0 || ldx < w->K || ldy < w->N) return NF4_ERR_INVALID_ARG;
+  if (w->K % 64 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return NF4_OK;
+  DevInfo dev;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
+  if (!dev.supported) return NF4_ERR_UNSUPPORTED;
+  // Shapes whose partials would not fit the fixed array are rejected up front.
+  if (plan_dense(0, M, w->N, w->K, dev.sms).ws_bytes > NF4_NOALLOC_SCRATCH_BYTES)
+    return NF4_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != NF4_OK) return st;
+  // Every partial the kernel later reads is written first in the same call, so
+  // what a previous call left in the array is never read and needs no clearing.
+  return run_dense(0, x, M, ldx, w, y, ldy, scratch, NF4_NOALLOC_SCRATCH_BYTES, stream);
+}

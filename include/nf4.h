@@ -184,6 +184,28 @@ nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, 
                              int64_t ldgy, const nf4_weight* w, int64_t N_e, void* gx, int64_t ldgx,
                              void* stream);
 
+/* nf4_linear_fwd_noalloc -- the forward of nf4_linear_fwd without a workspace
+ * argument, for callers that cannot allocate device memory themselves (for
+ * instance code running under a framework allocator that owns all device memory,
+ * or a plugin that is handed only its input and output buffers).  The pages
+ * have no counterpart: it is a deployment variant of the same computation.
+ *   Arguments, layouts and results are those of nf4_linear_fwd (same kernels,
+ *   same tile plan, same outputs).
+ *   Scratch: the split-contraction partials go to a fixed file-scope device
+ *   array of NF4_NOALLOC_SCRATCH_BYTES (4 MiB), which every GPU that loads the
+ *   library holds until the process exits.  Shapes whose partials need more
+ *   return NF4_ERR_WORKSPACE and launch nothing; the call never allocates.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (with that device current); make that first call before any stream capture.
+ *   Sharing: all calls use the same array and it keeps the last call's
+ *   contents; a call writes every partial before reading it, so nothing needs
+ *   clearing.  Calls that overlap on the GPU (for instance on two streams of
+ *   one device) race on that device's array: serialise them.  Each device holds
+ *   its own copy. */
+#define NF4_NOALLOC_SCRATCH_BYTES (4u << 20)
+nf4_status nf4_linear_fwd_noalloc(const void* x, int64_t M, int64_t ldx, const nf4_weight* w,
+                                  void* y, int64_t ldy, void* stream);
+
 /* Workspace bytes an operation needs for the given shape on the current device
  * (0 when none).  op is one of NF4_OP_*; E is unused for the dense products. */
 size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E);
