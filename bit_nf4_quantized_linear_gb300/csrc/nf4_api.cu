@@ -148,31 +148,68 @@ struct Plan {
   size_t ws_bytes;
 };
 
-// Tile plan of a dense product; a deterministic function of the shape and the SM
-// count.  The contraction is split only when M is small (few tiles) and the
-// fp32 partials stay well below the packed-weight traffic.
-Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
+Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
   Plan p;
+  p.bt = bt;
+  p.wtiles = static_cast<int>((ncols + nf4::kTileW - 1) / nf4::kTileW);
+  p.ttiles = static_cast<int>((M + bt - 1) / bt);
+  p.ksteps = static_cast<int>((contract + nf4::kTileK - 1) / nf4::kTileK);
+  p.splits = splits;
+  p.items = static_cast<int64_t>(p.wtiles) * p.ttiles * splits;
+  p.ws_bytes = splits > 1 ? static_cast<size_t>(splits) * M * ncols * sizeof(float) : 0;
+  return p;
+}
+
+// Tile plan of a dense product: a deterministic function of the shape and the SM
+// count.  Small M: the narrowest token tile and, when the weight tiles cannot fill
+// the SMs, a split of the contraction while its fp32 partials stay small next to
+// the packed weight.  Larger M: token tile and split chosen by a cost model in SM
+// clocks -- waves of items, each contraction step costing the larger of its MMA
+// time (2*BT clocks for a 128 x BT x 64 step) and its decode time (~480 clocks for
+// a 128 x 64 block of weights), plus the partials' round trip through memory.
+Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
-  p.bt = choose_bt(M);
-  p.wtiles = static_cast<int>((ncols + nf4::kTileW - 1) / nf4::kTileW);
-  p.ttiles = static_cast<int>((M + p.bt - 1) / p.bt);
-  p.ksteps = static_cast<int>((contract + nf4::kTileK - 1) / nf4::kTileK);
-  const int64_t base = static_cast<int64_t>(p.wtiles) * p.ttiles;
-  int64_t s = 1;
-  if (M > 0 && M <= 32 && base < sms) {
-    s = (sms + base - 1) / base;
-    s = s < p.ksteps / 4 ? s : p.ksteps / 4;
-    const int64_t traffic_cap = contract / (64 * M);
-    s = s < traffic_cap ? s : traffic_cap;
-    s = s < 32 ? s : 32;
-    s = s < 1 ? 1 : s;
+  const int64_t ksteps = (contract + nf4::kTileK - 1) / nf4::kTileK;
+  const int64_t wtiles = (ncols + nf4::kTileW - 1) / nf4::kTileW;
+  if (M <= 32) {
+    const int bt = choose_bt(M);
+    int64_t s = 1;
+    if (M > 0 && wtiles < sms) {
+      s = (sms + wtiles - 1) / wtiles;
+      s = s < ksteps / 4 ? s : ksteps / 4;
+      const int64_t traffic_cap = contract / (16 * M);
+      s = s < traffic_cap ? s : traffic_cap;
+      s = s < 32 ? s : 32;
+      s = s < 1 ? 1 : s;
+    }
+    return make_plan(M, ncols, contract, bt, static_cast<int>(s));
   }
-  p.splits = static_cast<int>(s);
-  p.items = base * p.splits;
-  p.ws_bytes = p.splits > 1 ? static_cast<size_t>(p.splits) * M * ncols * sizeof(float) : 0;
-  return p;
+  const int bt_max = choose_bt(M);
+  const int bts[3] = {64, 128, 256};
+  const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
+  double best_t = 1e300;
+  Plan best = make_plan(M, ncols, contract, bt_max, 1);
+  for (int bi = 2; bi >= 0; --bi) {
+    const int bt = bts[bi];
+    if (bt > bt_max) continue;
+    const int64_t ttiles = (M + bt - 1) / bt;
+    for (int si = 0; si < 7; ++si) {
+      const int S = sp[si];
+      if (S > 1 && ksteps / S < 8) break;
+      const int64_t items = wtiles * ttiles * S;
+      const int64_t waves = (items + sms - 1) / sms;
+      const int64_t kps = (ksteps + S - 1) / S;
+      const double step_clk = 2.0 * bt > 480.0 ? 2.0 * bt : 480.0;
+      double t = static_cast<double>(waves) * (kps * step_clk + 3000.0);
+      if (S > 1) t += static_cast<double>(S) * M * ncols * 8.0 / 3500.0;  // write + read partials
+      if (t < best_t * 0.999) {
+        best_t = t;
+        best = make_plan(M, ncols, contract, bt, S);
+      }
+    }
+  }
+  return best;
 }
 
 nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const nf4_weight* w,
@@ -201,11 +238,11 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     return NF4_ERR_CUDA;
   if (mode == 0) {
     if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 32,
-                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_32B))
       return NF4_ERR_CUDA;
   } else {
     if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 64,
-                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_64B))
       return NF4_ERR_CUDA;
   }
   nf4::GemmArgs a{};
@@ -275,11 +312,11 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
     return NF4_ERR_CUDA;
   if (mode == 0) {
     if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, w->N, K / 2, 32,
-                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_32B))
       return NF4_ERR_CUDA;
   } else {
     if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, w->N, K / 2, 64,
-                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_64B))
       return NF4_ERR_CUDA;
   }
   nf4::GemmArgs a{};

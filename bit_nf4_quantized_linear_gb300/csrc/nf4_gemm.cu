@@ -51,7 +51,8 @@ constexpr int kAStage = kTileW * kTileK * 2;  // 16 KB of bf16
 constexpr int kPkStage = kTileW * kTileK / 2;  // 4 KB of packed codes
 constexpr int kStagesA = 4;
 constexpr int kMiscBytes = 8192;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // bound of every wait (2 s)
+constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up to 20 us per try
 
 template <int BT>
 struct Geo {
@@ -104,14 +105,13 @@ __device__ __forceinline__ void record_error(const GemmArgs& a, int code) {
   *reinterpret_cast<volatile int*>(a.status) = code;
 }
 
-// Bounded wait: true once the phase completed; false on abort (another role
-// gave up) or after kTimeoutNs, in which case the timeout is recorded.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Shared& sh,
-                                        const GemmArgs& a) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait, slow path: true once the phase completed; false on abort (another
+// role gave up) or after kTimeoutNs, in which case the timeout is recorded.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, const Shared& sh,
+                                             const GemmArgs& a) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*sh.abort_flag) return false;
     if (globaltimer_ns() - t0 > kTimeoutNs) {
       *sh.abort_flag = 1;
@@ -121,10 +121,18 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Sha
   }
 }
 
+// Bounded wait: an inline non-blocking test first (the common case on a pipelined
+// ring, where the phase has completed already), the sleeping slow path otherwise.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Shared& sh,
+                                           const GemmArgs& a) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, sh, a);
+}
+
 // Wait used while draining on exit: bounded, ignores the abort flag.
 __device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, const GemmArgs& a) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
     if (globaltimer_ns() - t0 > kTimeoutNs) {
       record_error(a, kStatusTimeout);
       return;
@@ -169,29 +177,87 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
   return it;
 }
 
-// Decoded block scale: absmax, or fp32(fp32(code8[q] * nested) + offset).
-__device__ __forceinline__ float load_scale(const GemmArgs& a, const float* code8_s, int64_t n,
-                                            int64_t kb, float offset) {
-  if (n >= a.N_total || kb >= a.KB) return 0.0f;
+// Raw statistics of one block, fetched ahead of use: the fp32 absmax, or the
+// 8-bit code and its nested absmax.  Out-of-range blocks read as scale 0.
+struct RawScale {
+  float v;     // absmax, or nested absmax under double quantisation
+  uint32_t q;  // 8-bit code (double quantisation)
+};
+
+__device__ __forceinline__ RawScale fetch_scale(const GemmArgs& a, int64_t n, int64_t kb) {
+  RawScale r{0.0f, 0u};
+  if (n >= a.N_total || kb >= a.KB) return r;
   const int64_t b = n * a.KB + kb;
-  if (!a.dq) return __ldg(a.absmax + b);
-  const float t = __fmul_rn(code8_s[__ldg(a.absmax_q + b)], __ldg(a.nested_absmax + (b >> 8)));
-  return __fadd_rn(t, offset);
+  if (!a.dq) {
+    r.v = __ldg(a.absmax + b);
+  } else {
+    r.q = __ldg(a.absmax_q + b);
+    r.v = __ldg(a.nested_absmax + (b >> 8));
+  }
+  return r;
+}
+
+// Decoded block scale: absmax, or fp32(fp32(code8[q] * nested) + offset).
+__device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* code8_s,
+                                              const RawScale& r, float offset) {
+  if (!a.dq) return r.v;
+  return __fadd_rn(__fmul_rn(code8_s[r.q], r.v), offset);
+}
+
+// The 16 bf16 values T[q] = bf16(fp32(code4[q] * s)) of one 64-value block,
+// held in registers as byte planes: lo[k] packs the low bytes of T[4k..4k+3],
+// hi[k] the high bytes.  A byte permute (prmt) then looks up four codes at once.
+struct Lut {
+  uint32_t lo[4], hi[4];
+};
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));  // two IEEE products
+  return d;
+}
+
+// code2[i] holds code4[2i] (low word) and code4[2i+1] (high word).
+__device__ __forceinline__ Lut make_lut(const uint64_t (&code2)[8], float s) {
+  const uint64_t s2 = (static_cast<uint64_t>(__float_as_uint(s)) << 32) | __float_as_uint(s);
+  uint32_t p[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t m = mul_f32x2(code2[i], s2);
+    __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(m)),
+                                             __uint_as_float(static_cast<uint32_t>(m >> 32)));
+    p[i] = *reinterpret_cast<uint32_t*>(&b);  // T[2i] low half, T[2i+1] high half
+  }
+  Lut L;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    L.lo[k] = __byte_perm(p[2 * k], p[2 * k + 1], 0x6420u);
+    L.hi[k] = __byte_perm(p[2 * k], p[2 * k + 1], 0x7531u);
+  }
+  return L;
+}
+
+// Four codes (the low 16 bits of v: nibble positions 0..3 = values 1, 0, 3, 2 of a
+// byte pair, even value in the high nibble) to two bf16 pairs, value 0 lowest.
+__device__ __forceinline__ void lookup4(uint32_t v, const Lut& L, uint32_t& out01,
+                                        uint32_t& out23) {
+  const uint32_t sel = v & 0x7777u;                      // low 3 bits of each code
+  const uint32_t s3 = ((v >> 1) & 0x4444u) | 0x3210u;   // code bit 3 picks the upper 8 entries
+  const uint32_t lo = __byte_perm(__byte_perm(L.lo[0], L.lo[1], sel),
+                                  __byte_perm(L.lo[2], L.lo[3], sel), s3);
+  const uint32_t hi = __byte_perm(__byte_perm(L.hi[0], L.hi[1], sel),
+                                  __byte_perm(L.hi[2], L.hi[3], sel), s3);
+  out01 = __byte_perm(lo, hi, 0x4051u);
+  out23 = __byte_perm(lo, hi, 0x6273u);
 }
 
 // Eight packed codes (one 32-bit word; byte j holds value 2j high, 2j+1 low) to
-// eight bf16 values bf16(fp32(code4[q] * s)), packed pairwise, value 0 lowest.
-__device__ __forceinline__ uint4 decode8(uint32_t w, const float* code4_s, float s) {
-  uint32_t o[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t byte = (w >> (8 * j)) & 0xFFu;
-    const float f0 = __fmul_rn(code4_s[byte >> 4], s);
-    const float f1 = __fmul_rn(code4_s[byte & 15u], s);
-    __nv_bfloat162 p = __floats2bfloat162_rn(f0, f1);
-    o[j] = *reinterpret_cast<uint32_t*>(&p);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+// eight bf16 values, packed pairwise, value 0 lowest.
+__device__ __forceinline__ uint4 decode8(uint32_t w, const Lut& L) {
+  uint4 o;
+  lookup4(w, L, o.x, o.y);
+  lookup4(w >> 16, L, o.z, o.w);
+  return o;
 }
 
 template <int MODE, int BT>
@@ -230,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarTmaEmpty + i), 1);
     }
     for (int i = 0; i < kStagesA; ++i) {
-      mbar_init(bar_at(sh, kBarAFull + i), kNumDecWarps);
+      mbar_init(bar_at(sh, kBarAFull + i), kNumDecWarps / 2);
       mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -307,6 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kTileW, BT, MODE == 1, false);
+      // Constant fields of the operand descriptors (address field zero).
+      const uint64_t a_desc_hi = (MODE == 0) ? smem_desc_sw128(0, 16, 1024) : smem_desc_sw128(0, 8192, 1024);
+      const uint64_t b_desc_hi = smem_desc_sw128(0, 16, 1024);
       uint32_t st = 0, ph = 0, sa = 0, pha = 0;
       int acc_i = 0;
       bool ok = true;
@@ -321,13 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_phase(bar_at(sh, kBarTmaFull + st), ph, sh, a)) { ok = false; break; }
           if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_base = sbase + G::kOffA + sa * kAStage;
-          const uint32_t b_base = sbase + G::kOffX + st * G::kXStage;
+          // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
+          const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + sa * kAStage) >> 4);
+          const uint64_t bdesc0 = b_desc_hi | ((sbase + G::kOffX + st * G::kXStage) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk) {
-            const uint64_t adesc = (MODE == 0) ? smem_desc_sw128(a_base + kk * 32, 16, 1024)
-                                               : smem_desc_sw128(a_base + kk * 2048, 8192, 1024);
-            const uint64_t bdesc = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+            const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(kk * 32 >> 4);
             mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(bar_at(sh, kBarTmaEmpty + st));
@@ -382,49 +451,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ decoders --
-    const int d = threadIdx.x - kWarpDec0 * 32;  // 0..255
-    const int rb = d >> 1;                       // row-block 0..127
-    const int h = d & 1;                         // which 32 values of the block
+    // Two groups of four warps take alternate contraction steps; each thread turns
+    // one whole 64-value block (one scale) into bf16.
+    const int dw = warp - kWarpDec0;           // 0..7
+    const uint32_t grp = static_cast<uint32_t>(dw >> 2);
+    const int rb = ((dw & 3) << 5) | lane;     // row-block 0..127
     const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
-    // Geometry of this thread's 128-byte line in the A tile and in the packed tile.
-    int line_off, key, pk_off;
+    uint64_t code2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      code2[i] = (static_cast<uint64_t>(__float_as_uint(sh.code4[2 * i + 1])) << 32) |
+                 __float_as_uint(sh.code4[2 * i]);
+    // Geometry of this thread's 128-byte line in the A tile and of its two 16-byte
+    // chunks of packed codes.  The packed tile arrives with a TMA swizzle (32-byte
+    // rows: 32B mode; 64-byte rows: 64B mode) so that a quarter-warp's chunk loads
+    // fall in distinct banks.
+    int line_off, key, pk0, pk1;
     if (MODE == 0) {
       line_off = (rb >> 3) * 1024 + (rb & 7) * 128;
       key = rb & 7;
-      pk_off = rb * 32 + h * 16;
+      const int x = (rb >> 2) & 1;  // 32B swizzle: chunk bit 0 ^= row bit 2
+      pk0 = rb * 32 + ((0 ^ x) << 4);
+      pk1 = rb * 32 + ((1 ^ x) << 4);
     } else {
       const int nl = rb & 63, j = rb >> 6;
       line_off = j * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
       key = nl & 7;
-      pk_off = nl * 64 + j * 32 + h * 16;
+      const int x = (nl >> 1) & 3;  // 64B swizzle: chunk bits 0-1 ^= row bits 1-2
+      pk0 = nl * 64 + (((2 * j) ^ x) << 4);
+      pk1 = nl * 64 + (((2 * j + 1) ^ x) << 4);
     }
-    uint32_t st = 0, ph = 0, sa = 0, pha = 0;
+    // Contraction step -> (row, block) of this thread's scale.
+    auto block_of = [&](const Item& it, int ks, int64_t& n, int64_t& kb) {
+      if (MODE == 0) {
+        n = it.wrow0 + rb;
+        kb = ks;
+      } else {
+        n = it.wrow0 + static_cast<int64_t>(ks) * kTileK + (rb & 63);
+        kb = (it.col0 >> 6) + (rb >> 6);
+      }
+    };
+    uint32_t st = 0, ph = 0, sa = 0, pha = 0, step = 0;
     bool ok = true;
+    // The statistics of this group's steps are fetched kAhead owned steps (2*kAhead
+    // contraction steps) ahead into a register ring, so their global-memory latency
+    // hides behind the decodes in between.
+    constexpr int kAhead = 4;
+    int64_t nidx = blockIdx.x;
+    Item nit = nidx < total_items ? get_item<MODE, BT>(nidx, a, sh) : Item{};
+    int nks = nit.ks0;
+    auto advance = [&]() {  // next (item, step) in this CTA's sequence
+      if (nidx < total_items && ++nks >= nit.ks1) {
+        nidx += gridDim.x;
+        if (nidx < total_items) {
+          nit = get_item<MODE, BT>(nidx, a, sh);
+          nks = nit.ks0;
+        }
+      }
+    };
+    auto fetch_next = [&]() {
+      RawScale r{0.0f, 0u};
+      if (nidx < total_items) {
+        int64_t n, kb;
+        block_of(nit, nks, n, kb);
+        r = fetch_scale(a, n, kb);
+      }
+      advance();
+      advance();
+      return r;
+    };
+    if (grp == 1) advance();  // this group owns the odd steps
+    RawScale ring[kAhead];
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) ring[i] = fetch_next();
     for (int64_t idx = blockIdx.x; ok && idx < total_items; idx += gridDim.x) {
       const Item it = get_item<MODE, BT>(idx, a, sh);
-      for (int ks = it.ks0; ks < it.ks1; ++ks) {
-        int64_t n, kb;
-        if (MODE == 0) {
-          n = it.wrow0 + rb;
-          kb = ks;
-        } else {
-          n = it.wrow0 + static_cast<int64_t>(ks) * kTileK + (rb & 63);
-          kb = (it.col0 >> 6) + (rb >> 6);
-        }
-        const float s = load_scale(a, sh.code8, n, kb, offset);
-        if (!wait_phase(bar_at(sh, kBarTmaFull + st), ph, sh, a)) { ok = false; break; }
-        if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) { ok = false; break; }
-        const uint4 w4 = *reinterpret_cast<const uint4*>(smem + G::kOffPk + st * kPkStage + pk_off);
-        uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
-        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+      for (int ks = it.ks0; ks < it.ks1; ++ks, ++step) {
+        if ((step & 1u) == grp) {
+          const float s = finish_scale(a, sh.code8, ring[0], offset);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = 4 * h + i;
-          *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[i], sh.code4, s);
+          for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
+          ring[kAhead - 1] = fetch_next();
+          if (!wait_phase(bar_at(sh, kBarTmaFull + st), ph, sh, a)) { ok = false; break; }
+          if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) { ok = false; break; }
+          const uint8_t* pk = smem + G::kOffPk + st * kPkStage;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(pk + pk0);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
+          const Lut L = make_lut(code2, s);
+          uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
+          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[c], L);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_at(sh, kBarAFull + sa));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(sh, kBarAFull + sa));
         if (++st == G::kStagesT) { st = 0; ph ^= 1u; }
         if (++sa == kStagesA) { sa = 0; pha ^= 1u; }
       }
@@ -438,17 +560,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// out[t, c] = bf16(sum over s in order of ws[s, t, c]).
+// out[t, c] = bf16(sum over s in order of ws[s, t, c]); four columns per thread.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ ws, int splits,
                                                             int64_t M, int64_t ncols,
                                                             __nv_bfloat16* __restrict__ out, int64_t ld) {
   const int64_t total = M * ncols;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+  const int64_t nq = (ncols + 3) / 4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * nq;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t t = i / ncols, c = i - t * ncols;
-    float acc = ws[i];
-    for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, ws[static_cast<int64_t>(s) * total + i]);
-    out[t * ld + c] = __float2bfloat16_rn(acc);
+    const int64_t t = i / nq, c0 = (i - t * nq) * 4;
+    const int64_t e = t * ncols + c0;
+    if (c0 + 4 <= ncols && (ncols & 3) == 0 && (ld & 3) == 0) {
+      float4 acc = *reinterpret_cast<const float4*>(ws + e);
+      for (int s = 1; s < splits; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(ws + static_cast<int64_t>(s) * total + e);
+        acc.x = __fadd_rn(acc.x, v.x);
+        acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z);
+        acc.w = __fadd_rn(acc.w, v.w);
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out + t * ld + c0) = pk;
+    } else {
+      for (int64_t c = c0; c < c0 + 4 && c < ncols; ++c) {
+        float acc = ws[t * ncols + c];
+        for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, ws[static_cast<int64_t>(s) * total + t * ncols + c]);
+        out[t * ld + c] = __float2bfloat16_rn(acc);
+      }
+    }
   }
 }
 
@@ -500,9 +643,9 @@ cudaError_t launch_gemm(int mode, int bt, const GemmArgs& a, const CUtensorMap& 
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  __nv_bfloat16* out, int64_t ld, cudaStream_t s) {
-  const int64_t total = M * ncols;
+  const int64_t total = M * ((ncols + 3) / 4);
   int64_t grid = (total + 255) / 256;
-  if (grid > 4096) grid = 4096;
+  if (grid > 8192) grid = 8192;
   if (grid < 1) grid = 1;
   splitk_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(ws, splits, M, ncols, out, ld);
   return cudaGetLastError();
