@@ -176,7 +176,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
     const int bt = choose_bt(M);
     int64_t s = 1;
     if (M > 0 && wtiles < sms) {
-      s = (sms + wtiles - 1) / wtiles;
+      s = sms / wtiles;  // one wave: a second, partial wave would double the time
       s = s < ksteps / 4 ? s : ksteps / 4;
       const int64_t traffic_cap = contract / (16 * M);
       s = s < traffic_cap ? s : traffic_cap;
