@@ -377,30 +377,40 @@ def run_sweep(dev, pk):
                 ops.linear_dgrad(gy, w, out=gx, ws=wsb)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=s):
-            for w in reps:
-                ops.linear_fwd(x, w, out=y, ws=wsb)
-                ops.linear_dgrad(gy, w, out=gx, ws=wsb)
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(10):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            graph.replay()
-            b.record()
-            b.synchronize()
-            times.append(a.elapsed_time(b) / R)
-        t = statistics.median(times) * 1e-3  # seconds per fwd+dgrad pair
+        def timed(ops_list):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                for w in reps:
+                    for op in ops_list:
+                        op(w)
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(10):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                graph.replay()
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b) / R)
+            del graph
+            return statistics.median(times) * 1e-3  # seconds per call group
+        fwd = lambda w: ops.linear_fwd(x, w, out=y, ws=wsb)
+        bwd = lambda w: ops.linear_dgrad(gy, w, out=gx, ws=wsb)
+        t_f = timed([fwd])
+        t_d = timed([bwd])
+        t = t_f + t_d
         tfl = 4.0 * M * N * K / t / 1e12
         gbs = 2.0 * wbytes / t / 1e9
-        res.append({"M": M, "us_per_fwd_dgrad": round(t * 1e6, 2), "tflops": round(tfl, 2),
+        res.append({"M": M, "us_per_fwd_dgrad": round(t * 1e6, 2), "us_fwd": round(t_f * 1e6, 2),
+                    "us_dgrad": round(t_d * 1e6, 2), "tflops": round(tfl, 2),
                     "frac_tc": round(tfl / pk["bf16_tflops"], 4),
                     "weight_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                    "fwd_weight_gbs": round(wbytes / t_f / 1e9, 1),
+                    "dgrad_weight_gbs": round(wbytes / t_d / 1e9, 1),
                     "replicas": R})
-        del graph, reps, x, gy, y, gx, wsb
+        del reps, x, gy, y, gx, wsb
         torch.cuda.empty_cache()
     return res
 

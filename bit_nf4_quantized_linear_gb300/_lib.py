@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(PKG, "libnf4.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "nf4.h")
 
 NF4_OK = 0
-NOALLOC_SCRATCH_BYTES = 4 << 20  # NF4_NOALLOC_SCRATCH_BYTES of include/nf4.h
+NOALLOC_SCRATCH_BYTES = 2 << 20  # NF4_NOALLOC_SCRATCH_BYTES of include/nf4.h
 STATUS_NAMES = {
     0: "NF4_OK", 1: "NF4_ERR_INVALID_ARG", 2: "NF4_ERR_UNSUPPORTED_SHAPE", 3: "NF4_ERR_ALIGNMENT",
     4: "NF4_ERR_WORKSPACE", 5: "NF4_ERR_CUDA", 6: "NF4_ERR_TIMEOUT", 7: "NF4_ERR_UNSUPPORTED",
@@ -24,7 +24,7 @@ STATUS_NAMES = {
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD = range(5)
 PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
-         "dequantize", "quantize", "total"]
+         "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad"]
 
 
 class NF4Error(RuntimeError):
@@ -111,7 +111,7 @@ def check(rc: int, what: str):
 
 
 def path_counters() -> dict:
-    arr = (ctypes.c_uint64 * 8)()
+    arr = (ctypes.c_uint64 * len(PATHS))()
     lib().nf4_get_path_counters(ctypes.cast(arr, ctypes.c_void_p))
     return {name: int(v) for name, v in zip(PATHS, arr)}
 

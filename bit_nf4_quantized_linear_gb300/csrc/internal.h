@@ -51,7 +51,37 @@ struct GemmArgs {
   int* status;
 };
 
+// Parameters of the small-M GEMV kernels.
+struct GemvArgs {
+  const __nv_bfloat16* act;  // x [M, K] (forward) or grad_y [M, N] (input gradient)
+  int64_t ld_act;
+  const uint8_t* packed;
+  int64_t N, K, KB;
+  const float* absmax;
+  const uint8_t* absmax_q;
+  const float* nested_absmax;
+  const float* nested_offset;
+  const float* code4;
+  const float* code8;
+  int dq;
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  float* ws;  // input gradient: per-row-group partials [groups][M][K]
+  int64_t M;
+  int64_t m0;  // first activation row of a launch (set by the launcher)
+  int kseg;    // forward: contraction segments per row group
+  int* status;
+};
+
+// Largest M each product sends to the GEMV kernels.
+constexpr int kGemvMaxMFwd = 4;
+constexpr int kGemvMaxMDgrad = 4;
+
 // Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_gemv_fwd(const GemvArgs& a, cudaStream_t s);
+cudaError_t launch_gemv_dgrad(const GemvArgs& a, cudaStream_t s);
+int gemv_fwd_kseg(int64_t K);
+int64_t gemv_dgrad_row_groups(int64_t N);
 cudaError_t launch_gemm(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
                         const CUtensorMap& tmap_packed, int grid, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,

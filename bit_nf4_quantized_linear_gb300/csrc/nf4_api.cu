@@ -146,6 +146,7 @@ struct Plan {
   int bt, wtiles, ttiles, splits, ksteps;
   int64_t items;
   size_t ws_bytes;
+  bool gemv = false;  // small M: SIMT GEMV kernels
 };
 
 Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
@@ -170,6 +171,14 @@ Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
+  if (M > 0 && M <= (mode == 0 ? nf4::kGemvMaxMFwd : nf4::kGemvMaxMDgrad)) {
+    Plan p = make_plan(M, ncols, contract, 16, 1);
+    p.gemv = true;
+    p.items = 0;
+    const int64_t groups = mode == 0 ? 1 : nf4::gemv_dgrad_row_groups(N);
+    p.ws_bytes = groups > 1 ? static_cast<size_t>(groups) * M * K * sizeof(float) : 0;
+    return p;
+  }
   const int64_t ksteps = (contract + nf4::kTileK - 1) / nf4::kTileK;
   const int64_t wtiles = (ncols + nf4::kTileW - 1) / nf4::kTileW;
   if (M <= 32) {
@@ -232,6 +241,42 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   const Plan p = plan_dense(mode, M, N, K, dev.sms);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
 
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.gemv) {
+    nf4::GemvArgs g{};
+    g.act = static_cast<const __nv_bfloat16*>(act);
+    g.ld_act = ld_act;
+    g.packed = w->packed;
+    g.N = N;
+    g.K = K;
+    g.KB = K / 64;
+    g.absmax = w->absmax;
+    g.absmax_q = w->absmax_q;
+    g.nested_absmax = w->nested_absmax;
+    g.nested_offset = w->nested_offset;
+    g.code4 = w->code4;
+    g.code8 = w->code8;
+    g.dq = w->double_quant;
+    g.out = static_cast<__nv_bfloat16*>(out);
+    g.ld_out = ld_out;
+    g.ws = static_cast<float*>(ws);
+    g.M = M;
+    g.m0 = 0;
+    g.kseg = nf4::gemv_fwd_kseg(K);
+    g.status = dev.status;
+    cudaError_t le = mode == 0 ? nf4::launch_gemv_fwd(g, s) : nf4::launch_gemv_dgrad(g, s);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+    count(mode == 0 ? NF4_PATH_GEMV_FWD : NF4_PATH_GEMV_DGRAD);
+    if (p.ws_bytes > 0) {
+      le = nf4::launch_splitk_reduce(static_cast<const float*>(ws),
+                                     static_cast<int>(nf4::gemv_dgrad_row_groups(N)), M, K,
+                                     static_cast<__nv_bfloat16*>(out), ld_out, s);
+      if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+      count(NF4_PATH_SPLITK_REDUCE);
+    }
+    return NF4_OK;
+  }
+
   CUtensorMap tmap_act, tmap_pk;
   if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, M, ld_act * 2, 64,
                  p.bt, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -272,7 +317,6 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.ws = static_cast<float*>(ws);
   a.status = dev.status;
   const int grid = static_cast<int>(p.items < dev.sms ? p.items : dev.sms);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t le = nf4::launch_gemm(mode, p.bt, a, tmap_act, tmap_pk, grid, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);

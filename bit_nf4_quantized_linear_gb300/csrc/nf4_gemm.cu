@@ -34,6 +34,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "decode.cuh"
 #include "sm100_ptx.cuh"
 
 namespace nf4 {
@@ -204,62 +205,6 @@ __device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* co
                                               const RawScale& r, float offset) {
   if (!a.dq) return r.v;
   return __fadd_rn(__fmul_rn(code8_s[r.q], r.v), offset);
-}
-
-// The 16 bf16 values T[q] = bf16(fp32(code4[q] * s)) of one 64-value block,
-// held in registers as byte planes: lo[k] packs the low bytes of T[4k..4k+3],
-// hi[k] the high bytes.  A byte permute (prmt) then looks up four codes at once.
-struct Lut {
-  uint32_t lo[4], hi[4];
-};
-
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));  // two IEEE products
-  return d;
-}
-
-// code2[i] holds code4[2i] (low word) and code4[2i+1] (high word).
-__device__ __forceinline__ Lut make_lut(const uint64_t (&code2)[8], float s) {
-  const uint64_t s2 = (static_cast<uint64_t>(__float_as_uint(s)) << 32) | __float_as_uint(s);
-  uint32_t p[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint64_t m = mul_f32x2(code2[i], s2);
-    __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(m)),
-                                             __uint_as_float(static_cast<uint32_t>(m >> 32)));
-    p[i] = *reinterpret_cast<uint32_t*>(&b);  // T[2i] low half, T[2i+1] high half
-  }
-  Lut L;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    L.lo[k] = __byte_perm(p[2 * k], p[2 * k + 1], 0x6420u);
-    L.hi[k] = __byte_perm(p[2 * k], p[2 * k + 1], 0x7531u);
-  }
-  return L;
-}
-
-// Four codes (the low 16 bits of v: nibble positions 0..3 = values 1, 0, 3, 2 of a
-// byte pair, even value in the high nibble) to two bf16 pairs, value 0 lowest.
-__device__ __forceinline__ void lookup4(uint32_t v, const Lut& L, uint32_t& out01,
-                                        uint32_t& out23) {
-  const uint32_t sel = v & 0x7777u;                      // low 3 bits of each code
-  const uint32_t s3 = ((v >> 1) & 0x4444u) | 0x3210u;   // code bit 3 picks the upper 8 entries
-  const uint32_t lo = __byte_perm(__byte_perm(L.lo[0], L.lo[1], sel),
-                                  __byte_perm(L.lo[2], L.lo[3], sel), s3);
-  const uint32_t hi = __byte_perm(__byte_perm(L.hi[0], L.hi[1], sel),
-                                  __byte_perm(L.hi[2], L.hi[3], sel), s3);
-  out01 = __byte_perm(lo, hi, 0x4051u);
-  out23 = __byte_perm(lo, hi, 0x6273u);
-}
-
-// Eight packed codes (one 32-bit word; byte j holds value 2j high, 2j+1 low) to
-// eight bf16 values, packed pairwise, value 0 lowest.
-__device__ __forceinline__ uint4 decode8(uint32_t w, const Lut& L) {
-  uint4 o;
-  lookup4(w, L, o.x, o.y);
-  lookup4(w >> 16, L, o.z, o.w);
-  return o;
 }
 
 template <int MODE, int BT>
@@ -559,9 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // out[t, c] = bf16(sum over s in order of ws[s, t, c]); four columns per thread.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ ws, int splits,
-                                                            int64_t M, int64_t ncols,
-                                                            __nv_bfloat16* __restrict__ out, int64_t ld) {
+// Used for few splits (the large-M contraction splits).
+__global__ void __launch_bounds__(256) splitk_reduce_vec_kernel(const float* __restrict__ ws, int splits,
+                                                                int64_t M, int64_t ncols,
+                                                                __nv_bfloat16* __restrict__ out, int64_t ld) {
   const int64_t total = M * ncols;
   const int64_t nq = (ncols + 3) / 4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * nq;
@@ -590,6 +536,36 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
         out[t * ld + c] = __float2bfloat16_rn(acc);
       }
     }
+  }
+}
+
+// out[t, c] = bf16(sum over s of ws[s, t, c]) in a fixed order: a CTA owns 32
+// consecutive elements of one row; its 8 thread groups sum the splits
+// g, g+8, g+16, ... sequentially, then the 8 group sums are added in group order.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ ws, int splits,
+                                                            int64_t M, int64_t ncols,
+                                                            __nv_bfloat16* __restrict__ out, int64_t ld) {
+  __shared__ float part[8][32];
+  const int64_t total = M * ncols;
+  const int64_t slices = (ncols + 31) / 32;
+  const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
+  for (int64_t blk = blockIdx.x; blk < M * slices; blk += gridDim.x) {
+    const int64_t t = blk / slices;
+    const int64_t col = (blk - t * slices) * 32 + c;
+    float v = 0.0f;
+    if (col < ncols) {
+      const float* p = ws + t * ncols + col;
+      if (g < splits) v = p[static_cast<int64_t>(g) * total];
+      for (int s = g + 8; s < splits; s += 8) v = __fadd_rn(v, p[static_cast<int64_t>(s) * total]);
+    }
+    part[g][c] = v;
+    __syncthreads();
+    if (g == 0 && col < ncols) {
+      float acc = part[0][c];
+      for (int q = 1; q < 8 && q < splits; ++q) acc = __fadd_rn(acc, part[q][c]);
+      out[t * ld + col] = __float2bfloat16_rn(acc);
+    }
+    __syncthreads();
   }
 }
 
@@ -641,9 +617,16 @@ cudaError_t launch_gemm(int mode, int bt, const GemmArgs& a, const CUtensorMap& 
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  __nv_bfloat16* out, int64_t ld, cudaStream_t s) {
-  const int64_t total = M * ((ncols + 3) / 4);
-  int64_t grid = (total + 255) / 256;
-  if (grid > 8192) grid = 8192;
+  if (splits <= 8) {
+    int64_t grid = (M * ((ncols + 3) / 4) + 255) / 256;
+    if (grid > 8192) grid = 8192;
+    if (grid < 1) grid = 1;
+    splitk_reduce_vec_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(ws, splits, M, ncols, out, ld);
+    return cudaGetLastError();
+  }
+  // Many splits (the small-M input gradient): one CTA per 32 outputs.
+  int64_t grid = M * ((ncols + 31) / 32);
+  if (grid > 16384) grid = 16384;
   if (grid < 1) grid = 1;
   splitk_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(ws, splits, M, ncols, out, ld);
   return cudaGetLastError();

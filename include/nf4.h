@@ -76,13 +76,15 @@ enum {
 enum {
   NF4_PATH_LINEAR_FWD = 0,   /* fused tcgen05 forward                      */
   NF4_PATH_LINEAR_DGRAD = 1, /* fused tcgen05 input gradient               */
-  NF4_PATH_SPLITK_REDUCE = 2,/* fixed-order reduction of split-K partials  */
+  NF4_PATH_SPLITK_REDUCE = 2,/* fixed-order reduction of split partials    */
   NF4_PATH_GROUPED_FWD = 3,
   NF4_PATH_GROUPED_DGRAD = 4,
   NF4_PATH_DEQUANTIZE = 5,
   NF4_PATH_QUANTIZE = 6,
-  NF4_PATH_TOTAL = 7,
-  NF4_NUM_PATHS = 8
+  NF4_PATH_TOTAL = 7,        /* every launch of the library                */
+  NF4_PATH_GEMV_FWD = 8,     /* small-M SIMT forward                       */
+  NF4_PATH_GEMV_DGRAD = 9,   /* small-M SIMT input gradient                */
+  NF4_NUM_PATHS = 10
 };
 
 /* A quantised weight: the tensors of the pages' QuantState as plain device
@@ -150,8 +152,11 @@ nf4_status nf4_dequantize(const nf4_weight* w, void* out, int32_t out_dtype, voi
  *   M >= 0 (M == 0 is a no-op); K % 64 == 0; x 16-byte aligned.
  *   ws: device workspace of nf4_workspace_size(NF4_OP_LINEAR_FWD, M, N, K, 0)
  *   bytes (split-K partials for small M; may be NULL when that size is 0).
- *   fp32 accumulation on the tensor cores; split-K partials, when used, are summed
- *   in a fixed order by a second kernel.  No atomics. */
+ *   Paths: M <= 4 runs the SIMT GEMV kernels (16-byte code loads, register
+ *   codebook, bf16 x bf16 -> fp32 FMAs, warp-shuffle and in-CTA reductions in a
+ *   fixed order); larger M runs the tcgen05 kernel (fp32 accumulation in tensor
+ *   memory).  Split partials, when used, are summed in a fixed order by a second
+ *   kernel.  No atomics. */
 nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
                           int64_t ldy, void* ws, size_t ws_bytes, void* stream);
 
@@ -160,7 +165,8 @@ nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weigh
  * "Root cause"; only grad_x since the base is frozen, Soup issue #842 "Scope").
  *   gy [M, N] bf16, leading dimension ldgy (multiple of 8, >= N).
  *   gx [M, K] bf16, leading dimension ldgx (>= K).
- *   Same rules as nf4_linear_fwd; workspace from NF4_OP_LINEAR_DGRAD. */
+ *   Same rules as nf4_linear_fwd (the SIMT path serves M <= 4); workspace from
+ *   NF4_OP_LINEAR_DGRAD. */
 nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w, void* gx,
                             int64_t ldgx, void* ws, size_t ws_bytes, void* stream);
 
@@ -192,7 +198,7 @@ nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, 
  *   Arguments, layouts and results are those of nf4_linear_fwd (same kernels,
  *   same tile plan, same outputs).
  *   Scratch: the split-contraction partials go to a fixed file-scope device
- *   array of NF4_NOALLOC_SCRATCH_BYTES (4 MiB), which every GPU that loads the
+ *   array of NF4_NOALLOC_SCRATCH_BYTES (2 MiB), which every GPU that loads the
  *   library holds until the process exits.  Shapes whose partials need more
  *   return NF4_ERR_WORKSPACE and launch nothing; the call never allocates.
  *   Set-up: the first call on a device looks up the array's device address
@@ -202,7 +208,7 @@ nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, 
  *   clearing.  Calls that overlap on the GPU (for instance on two streams of
  *   one device) race on that device's array: serialise them.  Each device holds
  *   its own copy. */
-#define NF4_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define NF4_NOALLOC_SCRATCH_BYTES (2u << 20)
 nf4_status nf4_linear_fwd_noalloc(const void* x, int64_t M, int64_t ldx, const nf4_weight* w,
                                   void* y, int64_t ldy, void* stream);
 
@@ -213,7 +219,8 @@ size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E
 /* Static string naming a status code. */
 const char* nf4_status_string(nf4_status s);
 
-/* Copies the NF4_NUM_PATHS host-side launch counters into out (host array). */
+/* Copies the NF4_NUM_PATHS host-side launch counters into out (host array of
+ * NF4_NUM_PATHS entries). */
 void nf4_get_path_counters(uint64_t* out);
 void nf4_reset_path_counters(void);
 

@@ -262,3 +262,41 @@ def test_grouped_empty_experts_and_bad_offsets():
     nf4.grouped_fwd(x.to(DEV), bad, w, E)
     torch.cuda.synchronize()
     assert nf4.device_status(clear=True) == 8
+
+
+# ------------------------------------------------------------- small-M GEMV --
+
+GEMV = [(1, 64, 64), (2, 104, 128), (3, 136, 1088), (4, 4096, 1024), (5, 296, 2112),
+        (7, 200, 2112), (8, 96, 5120), (1, 4096, 14336), (2, 14336, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMV)
+@pytest.mark.parametrize("dq", [False, True])
+def test_gemv_path_parity(M, N, K, dq):
+    w, st, g = _quant_pair(N, K, dq, seed=7 * M + N + K)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    c = nf4.path_counters()
+    if M <= 4:
+        assert c["gemv_fwd"] == 1 and c["linear_fwd"] == 0
+        assert c["gemv_dgrad"] == 1 and c["linear_dgrad"] == 0
+    else:
+        assert c["gemv_fwd"] == 0 and c["linear_fwd"] == 1
+    parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"gemv fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"gemv dgrad {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("N,K", [(64, 128), (296, 2048)])
+def test_gemv_identity_probe_exact(N, K):
+    w, st, _ = _quant_pair(N, K, True, seed=N + K)
+    wb = oracle.dequantize(st, "bf16")
+    eye = torch.eye(K, dtype=torch.bfloat16)[:4].contiguous()
+    y = nf4.linear_fwd(eye.to(DEV), w)
+    np.testing.assert_array_equal(bf16_bits(y), np.ascontiguousarray(wb.T[:4]))
+    eyen = torch.eye(N, dtype=torch.bfloat16)[:4].contiguous()
+    gx = nf4.linear_dgrad(eyen.to(DEV), w)
+    np.testing.assert_array_equal(bf16_bits(gx), wb[:4])
