@@ -53,6 +53,22 @@ def parse():
     return p.parse_args()
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks (step time of the slowest replica)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: the work of every replica over the slowest replica's time."""
+    return flops_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def flops_per_step(M: int) -> float:
     from bit_nf4_quantized_linear_gb300 import synth
     return sum(2.0 * 2.0 * M * N * K for _, K, N in synth.LLAMA8B_PROJ)
@@ -239,14 +255,10 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     launches = nf4.path_counters()["total"] - c0
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms / args.steps
     flops = flops_per_step(M_HEAD)
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms_step)
 
     # Dominant kernel: the fused tcgen05 product kernel (forward and input-gradient
     # instances); achieved = algorithmic flops per launch / mean launch duration.
@@ -291,12 +303,8 @@ def run_ours(args, rank, world, local_rank):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_val = job_throughput(flops, world, e2e_ms)
 
     sweep = None
     if rank == 0 and world == 1 and not args.no_sweep:
