@@ -12,13 +12,13 @@
 // never materialise W, with a deterministic reduction).
 //
 // Structure (one CTA per SM, persistent over work items):
-//   warp 0      TMA producer: activation tile [BT tokens x 64] (128B swizzle) and
-//               packed-code tile into a ring of stages;
+//   warp 0      TMA producer of packed-code tiles (a deep ring, far ahead);
+//   warp 14     TMA producer of activation tiles [BT tokens x 64] (128B swizzle);
 //   warps 6-13  decoders, two groups of four taking alternate stages: each thread
 //               turns one 64-value block (one absmax) into bf16 through a register
 //               codebook (byte permutes) and stores it in the UMMA canonical
 //               128B-swizzled layout of the A operand (K-major for the forward,
-//               MN-major for the input gradient) in the same stage;
+//               MN-major for the input gradient) in a ring of decoded tiles;
 //   warp 1      MMA issuer: tcgen05.mma M=128 (weight rows / in-features), N=BT
 //               (tokens), K=16, fp32 accumulators in tensor memory, two
 //               accumulator buffers so the epilogue overlaps the next item;
@@ -42,8 +42,9 @@ namespace {
 
 using namespace nf4ptx;
 
-constexpr int kThreads = 14 * 32;
-constexpr int kWarpTma = 0;
+constexpr int kThreads = 15 * 32;
+constexpr int kWarpTma = 0;   // packed-code producer
+constexpr int kWarpTmaX = 14; // activation producer
 constexpr int kWarpMma = 1;
 constexpr int kWarpEpi0 = 2;
 constexpr int kNumEpiWarps = 4;
@@ -58,30 +59,35 @@ constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up t
 template <int BT>
 struct Geo {
   static constexpr int kXStage = BT * 128;  // BT rows of 64 bf16
-  static constexpr int kStageBytes = kXStage + kPkStage + kAStage;
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
-  static constexpr int kStages0 = kBudget / kStageBytes;
-  static constexpr int kStages = kStages0 > 16 ? 16 : kStages0;
+  static constexpr int kStagesA = 3;                // decoded operand tiles
+  static constexpr int kStagesP = BT <= 64 ? 16 : 8; // packed-code tiles (prefetched far ahead)
+  static constexpr int kStagesX0 = (kBudget - kStagesA * kAStage - kStagesP * kPkStage) / kXStage;
+  static constexpr int kStagesX = kStagesX0 > 8 ? 8 : kStagesX0;  // activation tiles
   static constexpr int kOffA = 0;
-  static constexpr int kOffX = kOffA + kStages * kAStage;
-  static constexpr int kOffPk = kOffX + kStages * kXStage;
-  static constexpr int kOffMisc = kOffPk + kStages * kPkStage;
+  static constexpr int kOffX = kOffA + kStagesA * kAStage;
+  static constexpr int kOffPk = kOffX + kStagesX * kXStage;
+  static constexpr int kOffMisc = kOffPk + kStagesP * kPkStage;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;
   static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
-  static_assert(kStages >= 3, "pipeline too shallow");
+  static_assert(kStagesX >= 3, "pipeline too shallow");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
 };
 
-// Barrier slots in the misc region.  One ring of stages: full (TMA landed; the
-// decoders wait on it), dec (decoded tile written; the MMA issuer waits on it),
-// empty (MMAs of the stage done; the producer waits on it).
-constexpr int kBarFull = 0;
-constexpr int kBarDec = 16;
-constexpr int kBarEmpty = 32;
-constexpr int kBarAccFull = 48;
-constexpr int kBarAccEmpty = 50;
-constexpr int kBarDrain = 52;
-constexpr int kNumBars = 53;
+// Barrier slots in the misc region.  Three rings advance one stage per
+// contraction step: packed codes (pfull: TMA landed; pempty: decoders read it),
+// activations (xfull: TMA landed; xempty: MMAs done) and decoded operand tiles
+// (afull: decoders wrote it; aempty: MMAs done).
+constexpr int kBarPFull = 0;
+constexpr int kBarPEmpty = 16;
+constexpr int kBarXFull = 32;
+constexpr int kBarXEmpty = 40;
+constexpr int kBarAFull = 48;
+constexpr int kBarAEmpty = 52;
+constexpr int kBarAccFull = 56;
+constexpr int kBarAccEmpty = 58;
+constexpr int kBarDrain = 60;
+constexpr int kNumBars = 61;
 
 struct Item {
   int64_t tok0, tok_end;
@@ -238,10 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.dq)
     for (int j = threadIdx.x; j < 256; j += kThreads) sh.code8[j] = a.code8[j];
   if (threadIdx.x == 0) {
-    for (int i = 0; i < G::kStages; ++i) {
-      mbar_init(bar_at(sh, kBarFull + i), 1);
-      mbar_init(bar_at(sh, kBarDec + i), kNumDecWarps / 2);
-      mbar_init(bar_at(sh, kBarEmpty + i), 1);
+    for (int i = 0; i < G::kStagesP; ++i) {
+      mbar_init(bar_at(sh, kBarPFull + i), 1);
+      mbar_init(bar_at(sh, kBarPEmpty + i), kNumDecWarps / 2);
+    }
+    for (int i = 0; i < G::kStagesX; ++i) {
+      mbar_init(bar_at(sh, kBarXFull + i), 1);
+      mbar_init(bar_at(sh, kBarXEmpty + i), 1);
+    }
+    for (int i = 0; i < G::kStagesA; ++i) {
+      mbar_init(bar_at(sh, kBarAFull + i), kNumDecWarps / 2);
+      mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_at(sh, kBarAccFull + i), 1);
@@ -269,10 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     *item_count = acc;
     if (bad) record_error(a, kStatusBadOffsets);
   }
-  if (warp == kWarpTma && lane == 0) {
-    prefetch_tensormap(&tmap_act);
-    prefetch_tensormap(&tmap_pk);
-  }
+  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
+  if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
   if (warp == kWarpMma) {
     tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
     tmem_relinquish();
@@ -284,20 +295,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t total_items =
       a.grouped ? static_cast<int64_t>(*item_count) * a.wtiles : a.total_items;
 
-  if (warp == kWarpTma) {
-    // ------------------------------------------------------------ producer --
+  if (warp == kWarpTma || warp == kWarpTmaX) {
+    // ----------------------------------------------------------- producers --
+    // Warp 0 streams packed-code tiles (deep ring, far ahead of the decoders);
+    // warp 14 streams activation tiles for the MMAs.
     if (lane == 0) {
+      const bool is_pk = warp == kWarpTma;
+      const int nst = is_pk ? G::kStagesP : G::kStagesX;
+      const int bar_full = is_pk ? kBarPFull : kBarXFull;
+      const int bar_empty = is_pk ? kBarPEmpty : kBarXEmpty;
+      const uint32_t bytes = is_pk ? kPkStage : G::kXStage;
       uint32_t st = 0, ph = 0, issued = 0, par = 0;
       bool ok = true;
       for (int64_t idx = blockIdx.x; ok && idx < total_items; idx += gridDim.x) {
         const Item it = get_item<MODE, BT>(idx, a, sh);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          if (!wait_phase(bar_at(sh, kBarEmpty + st), ph ^ 1u, sh, a)) { ok = false; break; }
-          const uint32_t full = bar_at(sh, kBarFull + st);
-          mbar_arrive_expect_tx(full, G::kXStage + kPkStage);
-          tma_load_2d(sbase + G::kOffX + st * G::kXStage, &tmap_act, full, ks * kTileK,
-                      static_cast<int32_t>(it.tok0));
-          if (MODE == 0)
+          if (!wait_phase(bar_at(sh, bar_empty + st), ph ^ 1u, sh, a)) { ok = false; break; }
+          const uint32_t full = bar_at(sh, bar_full + st);
+          mbar_arrive_expect_tx(full, bytes);
+          if (!is_pk)
+            tma_load_2d(sbase + G::kOffX + st * G::kXStage, &tmap_act, full, ks * kTileK,
+                        static_cast<int32_t>(it.tok0));
+          else if (MODE == 0)
             tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK / 2),
                         static_cast<int32_t>(it.wrow0));
           else
@@ -306,12 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         static_cast<int32_t>(it.wrow0 + static_cast<int64_t>(ks) * kTileK));
           issued |= 1u << st;
           par = (par & ~(1u << st)) | (ph << st);
-          if (++st == G::kStages) { st = 0; ph ^= 1u; }
+          if (++st == static_cast<uint32_t>(nst)) { st = 0; ph ^= 1u; }
         }
       }
       // Every load issued must have landed before the CTA may exit.
-      for (int s = 0; s < G::kStages; ++s)
-        if (issued & (1u << s)) drain_phase(bar_at(sh, kBarFull + s), (par >> s) & 1u, a);
+      for (int q = 0; q < nst; ++q)
+        if (issued & (1u << q)) drain_phase(bar_at(sh, bar_full + q), (par >> q) & 1u, a);
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issuer --
@@ -320,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Constant fields of the operand descriptors (address field zero).
       const uint64_t a_desc_hi = (MODE == 0) ? smem_desc_sw128(0, 16, 1024) : smem_desc_sw128(0, 8192, 1024);
       const uint64_t b_desc_hi = smem_desc_sw128(0, 16, 1024);
-      uint32_t st = 0, ph = 0;
+      uint32_t sx = 0, phx = 0, sa = 0, pha = 0;
       int acc_i = 0;
       bool ok = true;
       for (int64_t idx = blockIdx.x; ok && idx < total_items; idx += gridDim.x, ++acc_i) {
@@ -331,21 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BT);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          // The decoders signal a stage only after they saw its TMA land, so one
-          // wait covers both operands.
-          if (!wait_phase(bar_at(sh, kBarDec + st), ph, sh, a)) { ok = false; break; }
+          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
+          if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) { ok = false; break; }
           tc_fence_after();
           // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
-          const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + st * kAStage) >> 4);
-          const uint64_t bdesc0 = b_desc_hi | ((sbase + G::kOffX + st * G::kXStage) >> 4);
+          const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + sa * kAStage) >> 4);
+          const uint64_t bdesc0 = b_desc_hi | ((sbase + G::kOffX + sx * G::kXStage) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
             const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(kk * 32 >> 4);
             mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar_at(sh, kBarEmpty + st));
-          if (++st == G::kStages) { st = 0; ph ^= 1u; }
+          mma_commit(bar_at(sh, kBarAEmpty + sa));
+          mma_commit(bar_at(sh, kBarXEmpty + sx));
+          if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
+          if (++sx == G::kStagesX) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
         mma_commit(bar_at(sh, kBarAccFull + ab));
@@ -434,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         kb = (it.col0 >> 6) + (rb >> 6);
       }
     };
-    uint32_t st = 0, ph = 0, step = 0;
+    uint32_t sp = 0, php = 0, sa = 0, pha = 0, step = 0;
     bool ok = true;
     // The statistics of this group's steps are fetched kAhead owned steps (2*kAhead
     // contraction steps) ahead into a register ring, so their global-memory latency
@@ -475,23 +495,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
           ring[kAhead - 1] = fetch_next();
-          // The stage's A slot is free: the producer reused the stage only after its
-          // previous MMAs completed, and this wait follows that reuse.
-          if (!wait_phase(bar_at(sh, kBarFull + st), ph, sh, a)) { ok = false; break; }
-          const uint8_t* pk = smem + G::kOffPk + st * kPkStage;
+          if (!wait_phase(bar_at(sh, kBarPFull + sp), php, sh, a)) { ok = false; break; }
+          const uint8_t* pk = smem + G::kOffPk + sp * kPkStage;
           const uint4 w0 = *reinterpret_cast<const uint4*>(pk + pk0);
           const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
           const Lut L = make_lut(code2, s);
-          uint8_t* A = smem + G::kOffA + st * kAStage + line_off;
+          if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) { ok = false; break; }
+          uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
           const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[c], L);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_at(sh, kBarDec + st));
+          if (lane == 0) {
+            mbar_arrive(bar_at(sh, kBarPEmpty + sp));  // the codes were consumed above
+            mbar_arrive(bar_at(sh, kBarAFull + sa));
+          }
         }
-        if (++st == G::kStages) { st = 0; ph ^= 1u; }
+        if (++sp == G::kStagesP) { sp = 0; php ^= 1u; }
+        if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
       }
     }
   }
