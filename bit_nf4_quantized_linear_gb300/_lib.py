@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
             "nf4_device_check": [P],
             "nf4_last_cuda_error": [],
             "nf4_linear_fwd_noalloc": [P, I64, I64, W, P, I64, P],
+            "nf4_set_cta_pairs": [I32],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
         L.nf4_last_cuda_error.restype = ctypes.c_char_p
         L.nf4_get_path_counters.restype = None
         L.nf4_reset_path_counters.restype = None
+        L.nf4_set_cta_pairs.restype = None
         _lib = L
         return _lib
 
@@ -124,6 +126,10 @@ def device_status(clear: bool = False) -> int:
     v = ctypes.c_int32(0)
     check(lib().nf4_device_status(ctypes.byref(v), 1 if clear else 0), "nf4_device_status")
     return int(v.value)
+
+
+def set_cta_pairs(enabled: bool):
+    lib().nf4_set_cta_pairs(1 if enabled else 0)
 
 
 def device_check() -> int:

@@ -82,11 +82,11 @@ cudaError_t launch_gemv_fwd(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_dgrad(const GemvArgs& a, cudaStream_t s);
 int gemv_fwd_kseg(int64_t K);
 int64_t gemv_dgrad_row_groups(int64_t N);
-cudaError_t launch_gemm(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
+// cg = 2 launches CTA pairs (clusters of two, tcgen05 cta_group::2; bt must be 256).
+cudaError_t launch_gemm(int mode, int bt, int cg, const GemmArgs& a, const CUtensorMap& tmap_act,
                         const CUtensorMap& tmap_packed, int grid, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  __nv_bfloat16* out, int64_t ld, cudaStream_t s);
-int gemm_smem_bytes(int bt);
 
 cudaError_t launch_quantize(const void* W, int w_dtype, int64_t numel, const float* code4,
                             uint8_t* packed, float* absmax, cudaStream_t s);

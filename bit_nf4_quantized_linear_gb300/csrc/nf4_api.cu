@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -143,16 +144,17 @@ int choose_bt(int64_t M) {
 }
 
 struct Plan {
-  int bt, wtiles, ttiles, splits, ksteps;
+  int bt, cg, wtiles, ttiles, splits, ksteps;
   int64_t items;
   size_t ws_bytes;
   bool gemv = false;  // small M: SIMT GEMV kernels
 };
 
-Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
+Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits, int cg = 1) {
   Plan p;
   p.bt = bt;
-  p.wtiles = static_cast<int>((ncols + nf4::kTileW - 1) / nf4::kTileW);
+  p.cg = cg;
+  p.wtiles = static_cast<int>((ncols + nf4::kTileW * cg - 1) / (nf4::kTileW * cg));
   p.ttiles = static_cast<int>((M + bt - 1) / bt);
   p.ksteps = static_cast<int>((contract + nf4::kTileK - 1) / nf4::kTileK);
   p.splits = splits;
@@ -161,13 +163,37 @@ Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
   return p;
 }
 
+// Whether wide tiles may run as CTA pairs: off unless NF4_CTA_PAIR=1 is set or
+// nf4_set_cta_pairs(1) was called (on GB300 the pair's per-stage cross-CTA
+// handshake currently costs more than the shared-memory traffic it saves).
+std::atomic<int> g_cta_pairs{-1};
+
+bool cta_pairs_enabled() {
+  int v = g_cta_pairs.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char* e = std::getenv("NF4_CTA_PAIR");
+    v = (e && e[0] == '1') ? 1 : 0;
+    g_cta_pairs.store(v, std::memory_order_relaxed);
+  }
+  return v != 0;
+}
+
+// Cycles of one 64-deep contraction step of a tile (per SM), as measured on
+// GB300: bound by decode for narrow tiles and by shared-memory traffic (operand
+// tiles written by TMA and the decoders, read by the MMAs) for wide ones; a CTA
+// pair halves each SM's share of the activation tile.
+double step_cycles(int bt, int cg) {
+  if (bt >= 256) return cg == 2 ? 560.0 : 810.0;
+  if (bt >= 128) return 560.0;
+  return 480.0;
+}
+
 // Tile plan of a dense product: a deterministic function of the shape and the SM
 // count.  Small M: the narrowest token tile and, when the weight tiles cannot fill
 // the SMs, a split of the contraction while its fp32 partials stay small next to
-// the packed weight.  Larger M: token tile and split chosen by a cost model in SM
-// clocks -- waves of items, each contraction step costing the larger of its MMA
-// time (2*BT clocks for a 128 x BT x 64 step) and its decode time (~480 clocks for
-// a 128 x 64 block of weights), plus the partials' round trip through memory.
+// the packed weight.  Larger M: token tile, CTA pairing and split chosen by a cost
+// model in SM clocks -- waves of items times contraction steps, plus the split
+// partials' round trip through memory.
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
@@ -195,26 +221,28 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
     return make_plan(M, ncols, contract, bt, static_cast<int>(s));
   }
   const int bt_max = choose_bt(M);
-  const int bts[3] = {64, 128, 256};
+  const int cand_bt[4] = {256, 256, 128, 64};
+  const int cand_cg[4] = {2, 1, 1, 1};
   const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
   double best_t = 1e300;
   Plan best = make_plan(M, ncols, contract, bt_max, 1);
-  for (int bi = 2; bi >= 0; --bi) {
-    const int bt = bts[bi];
-    if (bt > bt_max) continue;
+  for (int ci = 0; ci < 4; ++ci) {
+    const int bt = cand_bt[ci], cg = cand_cg[ci];
+    if (bt > bt_max || (cg == 2 && !cta_pairs_enabled())) continue;
     const int64_t ttiles = (M + bt - 1) / bt;
+    const int64_t wt = (ncols + nf4::kTileW * cg - 1) / (nf4::kTileW * cg);
+    const int64_t units = sms / cg;
     for (int si = 0; si < 7; ++si) {
       const int S = sp[si];
       if (S > 1 && ksteps / S < 8) break;
-      const int64_t items = wtiles * ttiles * S;
-      const int64_t waves = (items + sms - 1) / sms;
+      const int64_t items = wt * ttiles * S;
+      const int64_t waves = (items + units - 1) / units;
       const int64_t kps = (ksteps + S - 1) / S;
-      const double step_clk = 2.0 * bt > 480.0 ? 2.0 * bt : 480.0;
-      double t = static_cast<double>(waves) * (kps * step_clk + 3000.0);
+      double t = static_cast<double>(waves) * (kps * step_cycles(bt, cg) + 3000.0);
       if (S > 1) t += static_cast<double>(S) * M * ncols * 8.0 / 3500.0;  // write + read partials
       if (t < best_t * 0.999) {
         best_t = t;
-        best = make_plan(M, ncols, contract, bt, S);
+        best = make_plan(M, ncols, contract, bt, S, cg);
       }
     }
   }
@@ -279,7 +307,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
 
   CUtensorMap tmap_act, tmap_pk;
   if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, M, ld_act * 2, 64,
-                 p.bt, CU_TENSOR_MAP_SWIZZLE_128B))
+                 p.bt / p.cg, CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   if (mode == 0) {
     if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 32,
@@ -316,8 +344,9 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.ld_out = ld_out;
   a.ws = static_cast<float*>(ws);
   a.status = dev.status;
-  const int grid = static_cast<int>(p.items < dev.sms ? p.items : dev.sms);
-  cudaError_t le = nf4::launch_gemm(mode, p.bt, a, tmap_act, tmap_pk, grid, s);
+  const int64_t units = dev.sms / p.cg;
+  const int grid = static_cast<int>((p.items < units ? p.items : units) * p.cg);
+  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, a, tmap_act, tmap_pk, grid, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
   if (p.splits > 1) {
@@ -390,7 +419,7 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   a.ws = nullptr;
   a.status = dev.status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t le = nf4::launch_gemm(mode, bt, a, tmap_act, tmap_pk, dev.sms, s);
+  cudaError_t le = nf4::launch_gemm(mode, bt, 1, a, tmap_act, tmap_pk, dev.sms, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
   return NF4_OK;
@@ -520,6 +549,8 @@ nf4_status nf4_device_status(int32_t* out, int32_t clear) {
 }
 
 const char* nf4_last_cuda_error(void) { return g_last_error; }
+
+void nf4_set_cta_pairs(int32_t enabled) { g_cta_pairs.store(enabled ? 1 : 0, std::memory_order_relaxed); }
 
 nf4_status nf4_device_check(int32_t* sm_count) {
   DevInfo dev;

@@ -56,9 +56,9 @@ constexpr int kMiscBytes = 8192;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bound of every wait (2 s)
 constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up to 20 us per try
 
-template <int BT>
+template <int BT, int CG>
 struct Geo {
-  static constexpr int kXStage = BT * 128;  // BT rows of 64 bf16
+  static constexpr int kXStage = (BT / CG) * 128;  // this CTA's BT/CG token rows of 64 bf16
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
   static constexpr int kStagesA = 3;                // decoded operand tiles
   static constexpr int kStagesP = BT <= 64 ? 16 : 8; // packed-code tiles (prefetched far ahead)
@@ -72,6 +72,7 @@ struct Geo {
   static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
   static_assert(kStagesX >= 3, "pipeline too shallow");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
+  static_assert(CG == 1 || BT == 256, "CTA pairs are used with 256-token tiles");
 };
 
 // Barrier slots in the misc region.  Three rings advance one stage per
@@ -98,6 +99,7 @@ struct Item {
 };
 
 struct Shared {
+  uint32_t rank;     // CTA rank in its pair (0 without pairs)
   float* code4;
   float* code8;
   uint32_t bars;  // shared address of barrier 0
@@ -116,11 +118,16 @@ __device__ __forceinline__ void record_error(const GemmArgs& a, int code) {
 
 // Bounded wait, slow path: true once the phase completed; false on abort (another
 // role gave up) or after kTimeoutNs, in which case the timeout is recorded.
+// `cluster`: the phase is completed by arrivals from the other CTA of a pair, so
+// the wait acquires at cluster scope (only the leader's waits on the decoded-tile
+// and accumulator-empty barriers need it).
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, const Shared& sh,
-                                             const GemmArgs& a) {
+                                             const GemmArgs& a, bool cluster) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (cluster ? mbar_try_wait_sleep_cluster(bar, parity, kSleepHintNs)
+                : mbar_try_wait_sleep(bar, parity, kSleepHintNs))
+      return true;
     if (*sh.abort_flag) return false;
     if (globaltimer_ns() - t0 > kTimeoutNs) {
       *sh.abort_flag = 1;
@@ -133,9 +140,9 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, cons
 // Bounded wait: an inline non-blocking test first (the common case on a pipelined
 // ring, where the phase has completed already), the sleeping slow path otherwise.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Shared& sh,
-                                           const GemmArgs& a) {
-  if (mbar_test_wait(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, sh, a);
+                                           const GemmArgs& a, bool cluster = false) {
+  if (cluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, sh, a, cluster);
 }
 
 // Wait used while draining on exit: bounded, ignores the abort flag.
@@ -149,8 +156,9 @@ __device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, const Ge
   }
 }
 
-template <int MODE, int BT>
+template <int MODE, int BT, int CG>
 __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const Shared& sh) {
+  constexpr int kW = kTileW * CG;  // weight rows / in-features per (pair) tile
   Item it;
   if (!a.grouped) {
     const int64_t s = idx % a.splits;
@@ -162,8 +170,8 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
     it.ks0 = static_cast<int>((s * a.ksteps) / a.splits);
     it.ks1 = static_cast<int>(((s + 1) * a.ksteps) / a.splits);
     it.split = static_cast<int>(s);
-    it.col0 = wt * kTileW;
-    it.wrow0 = (MODE == 0) ? wt * kTileW : 0;
+    it.col0 = wt * kW + sh.rank * kTileW;
+    it.wrow0 = (MODE == 0) ? it.col0 : 0;
   } else {
     const int64_t g = idx / a.wtiles;
     const int64_t wt = idx % a.wtiles;
@@ -179,8 +187,8 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
     it.ks0 = 0;
     it.ks1 = a.ksteps;
     it.split = 0;
-    it.col0 = wt * kTileW;
-    it.wrow0 = (MODE == 0) ? static_cast<int64_t>(e) * a.N_e + wt * kTileW
+    it.col0 = wt * kW + sh.rank * kTileW;
+    it.wrow0 = (MODE == 0) ? static_cast<int64_t>(e) * a.N_e + it.col0
                            : static_cast<int64_t>(e) * a.N_e;
   }
   return it;
@@ -213,11 +221,11 @@ __device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* co
   return __fadd_rn(__fmul_rn(code8_s[r.q], r.v), offset);
 }
 
-template <int MODE, int BT>
+template <int MODE, int BT, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
                     const __grid_constant__ CUtensorMap tmap_pk, const GemmArgs a) {
-  using G = Geo<BT>;
+  using G = Geo<BT, CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -225,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = raw_addr + pad;
 
   Shared sh;
+  sh.rank = CG == 2 ? cluster_ctarank() : 0u;
+  // Work items are per CTA, or per CTA pair.
+  const int64_t unit = CG == 2 ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t nunits = CG == 2 ? gridDim.x / 2 : gridDim.x;
   sh.code4 = reinterpret_cast<float*>(smem + G::kOffMisc);
   sh.code8 = sh.code4 + 16;
   uint64_t* bars_ptr = reinterpret_cast<uint64_t*>(sh.code8 + 256);
@@ -253,12 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarXEmpty + i), 1);
     }
     for (int i = 0; i < G::kStagesA; ++i) {
-      mbar_init(bar_at(sh, kBarAFull + i), kNumDecWarps / 2);
+      // leader of a pair: its own decoders + one relayed arrival from the peer
+      mbar_init(bar_at(sh, kBarAFull + i), (kNumDecWarps / 2) + (CG == 2 && sh.rank == 0 ? 1 : 0));
       mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_at(sh, kBarAccFull + i), 1);
-      mbar_init(bar_at(sh, kBarAccEmpty + i), kNumEpiWarps);
+      mbar_init(bar_at(sh, kBarAccEmpty + i), kNumEpiWarps * CG);  // both CTAs' epilogues
     }
     mbar_init(bar_at(sh, kBarDrain), 1);
     *sh.abort_flag = 0;
@@ -285,11 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
   if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
   if (warp == kWarpMma) {
-    tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
-    tmem_relinquish();
+    if (CG == 2) {
+      tmem_alloc_pair(smem_addr(sh.tmem_slot), G::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
+      tmem_relinquish();
+    }
     tc_fence_before();
   }
   __syncthreads();
+  if (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *sh.tmem_slot;
   const int64_t total_items =
@@ -307,15 +326,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = is_pk ? kPkStage : G::kXStage;
       uint32_t st = 0, ph = 0, issued = 0, par = 0;
       bool ok = true;
-      for (int64_t idx = blockIdx.x; ok && idx < total_items; idx += gridDim.x) {
-        const Item it = get_item<MODE, BT>(idx, a, sh);
+      for (int64_t idx = unit; ok && idx < total_items; idx += nunits) {
+        const Item it = get_item<MODE, BT, CG>(idx, a, sh);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           if (!wait_phase(bar_at(sh, bar_empty + st), ph ^ 1u, sh, a)) { ok = false; break; }
           const uint32_t full = bar_at(sh, bar_full + st);
           mbar_arrive_expect_tx(full, bytes);
           if (!is_pk)
             tma_load_2d(sbase + G::kOffX + st * G::kXStage, &tmap_act, full, ks * kTileK,
-                        static_cast<int32_t>(it.tok0));
+                        static_cast<int32_t>(it.tok0 + sh.rank * (BT / CG)));
           else if (MODE == 0)
             tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK / 2),
                         static_cast<int32_t>(it.wrow0));
@@ -334,24 +353,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileW, BT, MODE == 1, false);
+    if (CG == 2 && lane == 0 && sh.rank == 1) {
+      // The peer relays "decoded tile and activation half ready" for each stage to
+      // the leader with one cluster-scope arrive, so its decoders only signal
+      // locally.
+      uint32_t sa = 0, pha = 0;
+      bool ok = true;
+      for (int64_t idx = unit; ok && idx < total_items; idx += nunits) {
+        const Item it = get_item<MODE, BT, CG>(idx, a, sh);
+        for (int ks = it.ks0; ks < it.ks1; ++ks) {
+          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
+          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAFull + sa), 0));
+          if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
+        }
+      }
+    }
+    if (lane == 0 && sh.rank == 0) {  // a pair's MMAs are issued by its leader
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileW * CG, BT, MODE == 1, false);
       // Constant fields of the operand descriptors (address field zero).
       const uint64_t a_desc_hi = (MODE == 0) ? smem_desc_sw128(0, 16, 1024) : smem_desc_sw128(0, 8192, 1024);
       const uint64_t b_desc_hi = smem_desc_sw128(0, 16, 1024);
       uint32_t sx = 0, phx = 0, sa = 0, pha = 0;
       int acc_i = 0;
       bool ok = true;
-      for (int64_t idx = blockIdx.x; ok && idx < total_items; idx += gridDim.x, ++acc_i) {
-        const Item it = get_item<MODE, BT>(idx, a, sh);
+      for (int64_t idx = unit; ok && idx < total_items; idx += nunits, ++acc_i) {
+        const Item it = get_item<MODE, BT, CG>(idx, a, sh);
         const int ab = acc_i & 1;
         const uint32_t acc_ph = (acc_i >> 1) & 1;
-        if (!wait_phase(bar_at(sh, kBarAccEmpty + ab), acc_ph ^ 1u, sh, a)) break;
+        if (!wait_phase(bar_at(sh, kBarAccEmpty + ab), acc_ph ^ 1u, sh, a, CG == 2)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BT);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
-          if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) { ok = false; break; }
+          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a, CG == 2)) { ok = false; break; }
+          // A pair's decoders signal a stage only after their own activation half
+          // landed, so the leader waits on its decoded-tile barrier alone.
+          if (CG == 1 && !wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) { ok = false; break; }
           tc_fence_after();
           // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
           const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + sa * kAStage) >> 4);
@@ -360,18 +396,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
             const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(kk * 32 >> 4);
-            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
+            if (CG == 2)
+              mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
+            else
+              mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar_at(sh, kBarAEmpty + sa));
-          mma_commit(bar_at(sh, kBarXEmpty + sx));
+          if (CG == 2) {  // frees the stage in both CTAs
+            mma_commit_pair(bar_at(sh, kBarAEmpty + sa), 0x3);
+            mma_commit_pair(bar_at(sh, kBarXEmpty + sx), 0x3);
+          } else {
+            mma_commit(bar_at(sh, kBarAEmpty + sa));
+            mma_commit(bar_at(sh, kBarXEmpty + sx));
+          }
           if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
           if (++sx == G::kStagesX) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(bar_at(sh, kBarAccFull + ab));
+        if (CG == 2)
+          mma_commit_pair(bar_at(sh, kBarAccFull + ab), 0x3);
+        else
+          mma_commit(bar_at(sh, kBarAccFull + ab));
       }
       // All MMAs issued must be complete before tensor memory is released.
-      mma_commit(bar_at(sh, kBarDrain));
+      if (CG == 2)
+        mma_commit_pair(bar_at(sh, kBarDrain), 0x1);
+      else
+        mma_commit(bar_at(sh, kBarDrain));
       drain_phase(bar_at(sh, kBarDrain), 0, a);
     }
     __syncwarp();
@@ -380,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = 32 * q + lane;
     int acc_i = 0;
-    for (int64_t idx = blockIdx.x; idx < total_items; idx += gridDim.x, ++acc_i) {
-      const Item it = get_item<MODE, BT>(idx, a, sh);
+    for (int64_t idx = unit; idx < total_items; idx += nunits, ++acc_i) {
+      const Item it = get_item<MODE, BT, CG>(idx, a, sh);
       const int ab = acc_i & 1;
       const uint32_t acc_ph = (acc_i >> 1) & 1;
       if (!wait_phase(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)) break;
@@ -410,7 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
+      if (lane == 0) {
+        if (CG == 2)
+          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAccEmpty + ab), 0));
+        else
+          mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
+      }
     }
   } else {
     // ------------------------------------------------------------ decoders --
@@ -454,20 +509,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         kb = (it.col0 >> 6) + (rb >> 6);
       }
     };
-    uint32_t sp = 0, php = 0, sa = 0, pha = 0, step = 0;
+    uint32_t sp = 0, php = 0, sa = 0, pha = 0, sx = 0, phx = 0, step = 0;
     bool ok = true;
     // The statistics of this group's steps are fetched kAhead owned steps (2*kAhead
     // contraction steps) ahead into a register ring, so their global-memory latency
     // hides behind the decodes in between.
     constexpr int kAhead = 4;
-    int64_t nidx = blockIdx.x;
-    Item nit = nidx < total_items ? get_item<MODE, BT>(nidx, a, sh) : Item{};
+    int64_t nidx = unit;
+    Item nit = nidx < total_items ? get_item<MODE, BT, CG>(nidx, a, sh) : Item{};
     int nks = nit.ks0;
     auto advance = [&]() {  // next (item, step) in this CTA's sequence
       if (nidx < total_items && ++nks >= nit.ks1) {
-        nidx += gridDim.x;
+        nidx += nunits;
         if (nidx < total_items) {
-          nit = get_item<MODE, BT>(nidx, a, sh);
+          nit = get_item<MODE, BT, CG>(nidx, a, sh);
           nks = nit.ks0;
         }
       }
@@ -487,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     RawScale ring[kAhead];
 #pragma unroll
     for (int i = 0; i < kAhead; ++i) ring[i] = fetch_next();
-    for (int64_t idx = blockIdx.x; ok && idx < total_items; idx += gridDim.x) {
-      const Item it = get_item<MODE, BT>(idx, a, sh);
+    for (int64_t idx = unit; ok && idx < total_items; idx += nunits) {
+      const Item it = get_item<MODE, BT, CG>(idx, a, sh);
       for (int ks = it.ks0; ks < it.ks1; ++ks, ++step) {
         if ((step & 1u) == grp) {
           const float s = finish_scale(a, sh.code8, ring[0], offset);
@@ -501,6 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
           const Lut L = make_lut(code2, s);
           if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) { ok = false; break; }
+          // In a CTA pair this CTA's activation half must also have landed before
+          // the leader is told the stage is ready.
+          if (CG == 2 && !wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) { ok = false; break; }
           uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
           const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
@@ -515,14 +573,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (++sp == G::kStagesP) { sp = 0; php ^= 1u; }
         if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
+        if (++sx == G::kStagesX) { sx = 0; phx ^= 1u; }
       }
     }
   }
 
+  tc_fence_before();
   __syncthreads();
+  // A pair leaves together: the leader's MMAs (which write the peer's tensor memory)
+  // are drained and no remote arrive can target an exited CTA.
+  if (CG == 2) cluster_sync();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, G::kTmemCols);
+    if (CG == 2)
+      tmem_dealloc_pair(tmem_base, G::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, G::kTmemCols);
   }
 }
 
@@ -592,50 +658,59 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
-template <int MODE, int BT>
+template <int MODE, int BT, int CG>
 cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp, int grid,
                        cudaStream_t s) {
   static bool configured = false;
+  auto kern = nf4_gemm_kernel<MODE, BT, CG>;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(nf4_gemm_kernel<MODE, BT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<BT>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Geo<BT, CG>::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  nf4_gemm_kernel<MODE, BT><<<grid, kThreads, Geo<BT>::kSmem, s>>>(ta, tp, a);
-  return cudaGetLastError();
+  if (CG == 1) {
+    kern<<<grid, kThreads, Geo<BT, CG>::kSmem, s>>>(ta, tp, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Geo<BT, CG>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tp, a);
 }
 
 template <int MODE>
-cudaError_t launch_mode(int bt, const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta,
+                        const CUtensorMap& tp, int grid, cudaStream_t s) {
+  if (cg == 2) {
+    if (bt != 256) return cudaErrorInvalidValue;
+    return launch_one<MODE, 256, 2>(a, ta, tp, grid, s);
+  }
   switch (bt) {
-    case 16: return launch_one<MODE, 16>(a, ta, tp, grid, s);
-    case 32: return launch_one<MODE, 32>(a, ta, tp, grid, s);
-    case 64: return launch_one<MODE, 64>(a, ta, tp, grid, s);
-    case 128: return launch_one<MODE, 128>(a, ta, tp, grid, s);
-    case 256: return launch_one<MODE, 256>(a, ta, tp, grid, s);
+    case 16: return launch_one<MODE, 16, 1>(a, ta, tp, grid, s);
+    case 32: return launch_one<MODE, 32, 1>(a, ta, tp, grid, s);
+    case 64: return launch_one<MODE, 64, 1>(a, ta, tp, grid, s);
+    case 128: return launch_one<MODE, 128, 1>(a, ta, tp, grid, s);
+    case 256: return launch_one<MODE, 256, 1>(a, ta, tp, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-int gemm_smem_bytes(int bt) {
-  switch (bt) {
-    case 16: return Geo<16>::kSmem;
-    case 32: return Geo<32>::kSmem;
-    case 64: return Geo<64>::kSmem;
-    case 128: return Geo<128>::kSmem;
-    case 256: return Geo<256>::kSmem;
-    default: return -1;
-  }
-}
-
-cudaError_t launch_gemm(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
+cudaError_t launch_gemm(int mode, int bt, int cg, const GemmArgs& a, const CUtensorMap& tmap_act,
                         const CUtensorMap& tmap_packed, int grid, cudaStream_t s) {
-  if (mode == 0) return launch_mode<0>(bt, a, tmap_act, tmap_packed, grid, s);
-  return launch_mode<1>(bt, a, tmap_act, tmap_packed, grid, s);
+  if (mode == 0) return launch_mode<0>(bt, cg, a, tmap_act, tmap_packed, grid, s);
+  return launch_mode<1>(bt, cg, a, tmap_act, tmap_packed, grid, s);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,

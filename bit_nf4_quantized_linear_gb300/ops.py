@@ -203,3 +203,4 @@ path_counters = _lib.path_counters
 reset_path_counters = _lib.reset_path_counters
 device_status = _lib.device_status
 device_check = _lib.device_check
+set_cta_pairs = _lib.set_cta_pairs

@@ -228,6 +228,15 @@ void nf4_reset_path_counters(void);
  * device into *out (host int).  Synchronises with the device; not for hot paths. */
 nf4_status nf4_device_status(int32_t* out, int32_t clear);
 
+/* Lets (enabled != 0) or forbids (the default) wide tiles of the dense products
+ * to run as CTA pairs (clusters of two sharing one tcgen05 M=256 MMA, each CTA
+ * holding half of the activation tile).  On GB300 the pairs are currently slower
+ * than single-CTA tiles, so they are off unless asked for.  The choice can change
+ * the fp32 summation grouping, so results may differ in the last bit between the
+ * two settings; each setting is deterministic.  NF4_CTA_PAIR=1 in the environment
+ * sets the initial value to 1. */
+void nf4_set_cta_pairs(int32_t enabled);
+
 /* Human-readable message of the last CUDA error that made a call of this thread
  * return NF4_ERR_CUDA ("no error" if none).  Static string. */
 const char* nf4_last_cuda_error(void);

@@ -300,3 +300,25 @@ def test_gemv_identity_probe_exact(N, K):
     eyen = torch.eye(N, dtype=torch.bfloat16)[:4].contiguous()
     gx = nf4.linear_dgrad(eyen.to(DEV), w)
     np.testing.assert_array_equal(bf16_bits(gx), wb[:4])
+
+
+@pytest.mark.parametrize("M,N,K,mode", [(512, 4096, 4096, 0), (512, 4096, 4096, 1), (1024, 640, 1024, 0),
+                                        (700, 384, 2048, 1), (2048, 14336, 4096, 0)])
+def test_cta_pair_and_single_cta_tiles_both_match_oracle(M, N, K, mode):
+    from bit_nf4_quantized_linear_gb300 import ops
+    w, st, g = _quant_pair(N, K, True, seed=M + N)
+    a = synth.activation(M, K if mode == 0 else N, g)
+    wb = oracle.dequantize(st, "bf16")
+    rows = _sampled_rows(M, 5)
+    ref = (oracle.linear_fwd if mode == 0 else oracle.linear_dgrad)(bf16_bits(a), wb, rows)
+    f = nf4.linear_fwd if mode == 0 else nf4.linear_dgrad
+    outs = []
+    try:
+        for pairs in (True, False):
+            ops.set_cta_pairs(pairs)
+            o = f(a.to(DEV), w)
+            parity(o[torch.from_numpy(rows).to(DEV)], ref, f"pairs={pairs} mode={mode} M={M}")
+            assert torch.equal(f(a.to(DEV), w).view(torch.int16), o.view(torch.int16))
+            outs.append(o)
+    finally:
+        ops.set_cta_pairs(True)
