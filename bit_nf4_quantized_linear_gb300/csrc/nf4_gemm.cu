@@ -439,14 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t col = it.col0 + row;
       const bool col_ok = col < a.ncols;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
+      // 16 columns per load and wait (wider batches measured slower: register pressure).
+      constexpr int kBatch = 16;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BT; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(taddr + c0, v);
+      for (int c0 = 0; c0 < BT; c0 += kBatch) {
+        uint32_t v[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch / 16; ++q)
+          tmem_ld_32x32b_x16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
         tmem_wait_ld();
         if (col_ok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kBatch; ++j) {
             const int64_t tok = it.tok0 + c0 + j;
             if (tok < it.tok_end) {
               const float f = __uint_as_float(v[j]);
