@@ -24,7 +24,8 @@ STATUS_NAMES = {
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD = range(5)
 PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
-         "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad"]
+         "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad", "skinny_fwd",
+         "skinny_dgrad"]
 
 
 class NF4Error(RuntimeError):
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
             "nf4_last_cuda_error": [],
             "nf4_linear_fwd_noalloc": [P, I64, I64, W, P, I64, P],
             "nf4_set_cta_pairs": [I32],
+            "nf4_set_weight_prefetch": [I32],
+            "nf4_set_small_m_path": [I32],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -101,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.nf4_get_path_counters.restype = None
         L.nf4_reset_path_counters.restype = None
         L.nf4_set_cta_pairs.restype = None
+        L.nf4_set_weight_prefetch.restype = None
+        L.nf4_set_small_m_path.restype = None
         _lib = L
         return _lib
 
@@ -130,6 +135,17 @@ def device_status(clear: bool = False) -> int:
 
 def set_cta_pairs(enabled: bool):
     lib().nf4_set_cta_pairs(1 if enabled else 0)
+
+
+SMALL_M_AUTO, SMALL_M_SIMT, SMALL_M_TILES = 0, 1, 2
+
+
+def set_small_m_path(path: int):
+    lib().nf4_set_small_m_path(int(path))
+
+
+def set_weight_prefetch(enabled: bool):
+    lib().nf4_set_weight_prefetch(1 if enabled else 0)
 
 
 def device_check() -> int:

@@ -45,16 +45,21 @@ __device__ __forceinline__ Lut make_lut(const uint64_t (&code2)[8], float s) {
   return L;
 }
 
+// Four codes (the low 16 bits of v) to the byte planes of their bf16 values:
+// byte i of `lo` / `hi` is the low / high byte of T[code in nibble position i].
+__device__ __forceinline__ void planes4(uint32_t v, const Lut& L, uint32_t& lo, uint32_t& hi) {
+  const uint32_t sel = v & 0x7777u;                      // low 3 bits of each code
+  const uint32_t s3 = ((v >> 1) & 0x4444u) | 0x3210u;   // code bit 3 picks the upper 8 entries
+  lo = __byte_perm(__byte_perm(L.lo[0], L.lo[1], sel), __byte_perm(L.lo[2], L.lo[3], sel), s3);
+  hi = __byte_perm(__byte_perm(L.hi[0], L.hi[1], sel), __byte_perm(L.hi[2], L.hi[3], sel), s3);
+}
+
 // Four codes (the low 16 bits of v: nibble positions 0..3 = values 1, 0, 3, 2 of a
 // byte pair, even value in the high nibble) to two bf16 pairs, value 0 lowest.
 __device__ __forceinline__ void lookup4(uint32_t v, const Lut& L, uint32_t& out01,
                                         uint32_t& out23) {
-  const uint32_t sel = v & 0x7777u;                      // low 3 bits of each code
-  const uint32_t s3 = ((v >> 1) & 0x4444u) | 0x3210u;   // code bit 3 picks the upper 8 entries
-  const uint32_t lo = __byte_perm(__byte_perm(L.lo[0], L.lo[1], sel),
-                                  __byte_perm(L.lo[2], L.lo[3], sel), s3);
-  const uint32_t hi = __byte_perm(__byte_perm(L.hi[0], L.hi[1], sel),
-                                  __byte_perm(L.hi[2], L.hi[3], sel), s3);
+  uint32_t lo, hi;
+  planes4(v, L, lo, hi);
   out01 = __byte_perm(lo, hi, 0x4051u);
   out23 = __byte_perm(lo, hi, 0x6273u);
 }

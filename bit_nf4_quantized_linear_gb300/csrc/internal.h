@@ -73,6 +73,45 @@ struct GemvArgs {
   int* status;
 };
 
+// Parameters of the small-M tensor-core kernels (mma.sync m16n8k16).  The grid
+// is C clusters of S CTAs; cluster c owns the output tiles c*T/C .. (c+1)*T/C - 1
+// (forward: 16 weight rows; input gradient: 64 in-features), and CTA rank r of a
+// cluster owns the contraction slice r*cc .. (r+1)*cc - 1; the S partial sums of
+// a tile are reduced through distributed shared memory in rank order.
+struct SkinnyArgs {
+  const __nv_bfloat16* act;  // x [M, K] (forward) or grad_y [M, N] (input gradient)
+  int64_t ld_act;
+  const uint8_t* packed;
+  int64_t N, K, KB;
+  const float* absmax;
+  const uint8_t* absmax_q;
+  const float* nested_absmax;
+  const float* nested_offset;
+  const float* code4;
+  const float* code8;
+  int dq;
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  int64_t M;
+  int S;          // CTAs per cluster (contraction split)
+  int C;          // clusters
+  int64_t T;      // output tiles
+  int64_t cc;     // contraction per CTA (forward: multiple of 64; input gradient: of 16)
+  int prefetch;   // the weight may be read before the preceding grid has finished
+};
+
+constexpr int kSkinnyMaxM = 16;
+
+struct SkinnyPlan {
+  int S = 0, C = 0;
+  int64_t T = 0, cc = 0;
+  size_t smem = 0;
+};
+
+// Plans and launches (S CTAs per cluster along the contraction).
+bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* p);
+cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s);
+
 // Largest M each product sends to the GEMV kernels.
 constexpr int kGemvMaxMFwd = 4;
 constexpr int kGemvMaxMDgrad = 4;

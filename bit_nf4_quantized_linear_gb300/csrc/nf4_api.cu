@@ -148,6 +148,8 @@ struct Plan {
   int64_t items;
   size_t ws_bytes;
   bool gemv = false;  // small M: SIMT GEMV kernels
+  bool skinny = false;  // small M: tensor-core (mma.sync) kernels
+  nf4::SkinnyPlan sk;
 };
 
 Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits, int cg = 1) {
@@ -167,6 +169,13 @@ Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits, i
 // nf4_set_cta_pairs(1) was called (on GB300 the pair's per-stage cross-CTA
 // handshake currently costs more than the shared-memory traffic it saves).
 std::atomic<int> g_cta_pairs{-1};
+
+// Whether the small-M kernels may read the weight before the grid dependency on
+// the previous kernel resolves (nf4_set_weight_prefetch).
+std::atomic<int> g_weight_prefetch{0};
+
+// Kernels for M <= 16 (nf4_set_small_m_path).
+std::atomic<int> g_small_m_path{NF4_SMALL_M_AUTO};
 
 bool cta_pairs_enabled() {
   int v = g_cta_pairs.load(std::memory_order_relaxed);
@@ -197,7 +206,18 @@ double step_cycles(int bt, int cg) {
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
-  if (M > 0 && M <= (mode == 0 ? nf4::kGemvMaxMFwd : nf4::kGemvMaxMDgrad)) {
+  const int small = g_small_m_path.load(std::memory_order_relaxed);
+  nf4::SkinnyPlan sk;
+  if (M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk)) {
+    Plan p = make_plan(M, ncols, contract, 16, 1);
+    p.skinny = true;
+    p.sk = sk;
+    p.items = 0;
+    p.ws_bytes = 0;
+    return p;
+  }
+  if (M > 0 && small != NF4_SMALL_M_TILES &&
+      M <= (mode == 0 ? nf4::kGemvMaxMFwd : nf4::kGemvMaxMDgrad)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.gemv = true;
     p.items = 0;
@@ -270,6 +290,34 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.skinny) {
+    nf4::SkinnyArgs k{};
+    k.act = static_cast<const __nv_bfloat16*>(act);
+    k.ld_act = ld_act;
+    k.packed = w->packed;
+    k.N = N;
+    k.K = K;
+    k.KB = K / 64;
+    k.absmax = w->absmax;
+    k.absmax_q = w->absmax_q;
+    k.nested_absmax = w->nested_absmax;
+    k.nested_offset = w->nested_offset;
+    k.code4 = w->code4;
+    k.code8 = w->code8;
+    k.dq = w->double_quant;
+    k.out = static_cast<__nv_bfloat16*>(out);
+    k.ld_out = ld_out;
+    k.M = M;
+    k.S = p.sk.S;
+    k.C = p.sk.C;
+    k.T = p.sk.T;
+    k.cc = p.sk.cc;
+    k.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+    cudaError_t le = nf4::launch_skinny(mode, k, p.sk, s);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+    count(mode == 0 ? NF4_PATH_SKINNY_FWD : NF4_PATH_SKINNY_DGRAD);
+    return NF4_OK;
+  }
   if (p.gemv) {
     nf4::GemvArgs g{};
     g.act = static_cast<const __nv_bfloat16*>(act);
@@ -551,6 +599,15 @@ nf4_status nf4_device_status(int32_t* out, int32_t clear) {
 const char* nf4_last_cuda_error(void) { return g_last_error; }
 
 void nf4_set_cta_pairs(int32_t enabled) { g_cta_pairs.store(enabled ? 1 : 0, std::memory_order_relaxed); }
+
+void nf4_set_small_m_path(int32_t path) {
+  if (path >= NF4_SMALL_M_AUTO && path <= NF4_SMALL_M_TILES)
+    g_small_m_path.store(path, std::memory_order_relaxed);
+}
+
+void nf4_set_weight_prefetch(int32_t enabled) {
+  g_weight_prefetch.store(enabled ? 1 : 0, std::memory_order_relaxed);
+}
 
 nf4_status nf4_device_check(int32_t* sm_count) {
   DevInfo dev;

@@ -1,0 +1,920 @@
+// nf4_skinny.cu -- small-M tensor-core path of the fused NF4 products: a few
+// activation rows (M <= 16) against a packed NF4 weight, where the work is bound
+// by streaming the packed codes from HBM (Soup issue #842, "Design sketch":
+// forward and transposed backward computed straight from the packed codes,
+// deterministic reduction, no atomics).
+//
+// Decode.  Every CTA holds in shared memory a 256-entry table that maps one
+// byte made of two 4-bit codes to the fp32 pair (code4[high nibble],
+// code4[low nibble]), one copy per lane so that the 32 lookups of a warp touch
+// 32 different 8-byte slots.  A lookup is one byte permute (which also forms the
+// address), one 8-byte shared load, one paired fp32 multiply by the values'
+// block scales and one bf16x2 conversion per two weight values, and yields
+// exactly the dequantised operand bf16(fp32(code4[q] * scale)) in a register of
+// the warp-level bf16 MMA (mma.sync.m16n8k16, fp32 accumulation), which does the
+// multiply-adds for up to 16 activation rows.  The work is spread over the
+// shared-memory, fp32 and integer pipes (a register-resident codebook would load
+// the integer pipe alone, which on this GPU issues at half rate).
+//
+// Work split.  The grid is C clusters of S CTAs (one CTA of 16 warps per SM).
+// Cluster c owns a contiguous range of output tiles, balanced to within one
+// tile; CTA rank r owns one slice of the contraction.  The (tile, contraction
+// step) units of a CTA are dealt to its 16 warps as contiguous ranges, and each
+// warp streams its units' packed codes through its own two-slot ring of
+// shared-memory slots with asynchronous copies (cp.async), one unit ahead of
+// the one it decodes.  The forward decodes each unit's block scales per lane
+// from statistics fetched along with the unit's codes and stages its
+// activation slice in shared memory once; the input gradient decodes the block
+// scales of its slice once into shared memory and carries grad_y in the ring
+// slots next to the codes.  Every sum runs in a fixed order:
+// inside an MMA, over a warp's units in order, over the warps of a CTA in warp
+// order through shared memory, and over the cluster's ranks in rank order
+// through distributed shared memory.  No atomics, no workspace.
+//
+// Launched with programmatic stream serialisation: a kernel may start while its
+// predecessor on the stream drains and waits for it (griddepcontrol.wait)
+// before it reads activations or writes the output.  When the caller declares
+// the weight read-only for the duration (`prefetch`), the codebook table, the
+// block scales and the first units' packed codes are read before that wait.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace nf4 {
+namespace {
+
+using nf4ptx::cluster_sync;
+using nf4ptx::mapa_shared;
+using nf4ptx::smem_addr;
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTableBytes = 256 * 256;    // 256 entries x 32 lanes x 8 bytes
+constexpr size_t kMaxSmem = 227 * 1024;
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// d += a * b: one warp-level 16x8x16 bf16 product, fp32 accumulation.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The byte-pair table: entry e = (code4[e >> 4], code4[e & 15]) as two fp32 (the
+// even value of a packed byte first), copy for lane l at byte offset 256 e + 8 l.
+__device__ __forceinline__ void build_table(uint8_t* smem, const float* code4) {
+  uint4* t = reinterpret_cast<uint4*>(smem);
+  for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
+    const int e = i >> 4;
+    const uint32_t hi = __float_as_uint(__ldg(code4 + (e >> 4)));
+    const uint32_t lo = __float_as_uint(__ldg(code4 + (e & 15)));
+    t[i] = make_uint4(hi, lo, hi, lo);
+  }
+}
+
+// Dequantised bf16 pair of the packed byte that `sel` picks from w:
+// bf16(fp32(code4[q] * s)) for both nibbles, the even value in the low half.
+// The permute puts the byte into bits 8..15 and lane*8 (byte 0 of lane8) into
+// bits 0..7 of the table offset; s2 holds the two values' scales (low word:
+// even value).
+__device__ __forceinline__ uint32_t lookup(const uint8_t* smem, uint32_t w, uint32_t lane8,
+                                           uint32_t sel, uint64_t s2) {
+  const uint2 c = *reinterpret_cast<const uint2*>(smem + __byte_perm(w, lane8, sel));
+  uint64_t p;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(p)
+      : "l"((static_cast<uint64_t>(c.y) << 32) | c.x), "l"(s2));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(p)),
+                                                 __uint_as_float(static_cast<uint32_t>(p >> 32)));
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__device__ __forceinline__ uint64_t pair2(float lo, float hi) {
+  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
+// Selector for byte b of the first operand (see lookup).
+__host__ __device__ constexpr uint32_t lookup_sel(uint32_t b) { return 0x5504u | (b << 4); }
+
+// Raw statistics of one block (absmax, or 8-bit code + nested absmax), fetched
+// ahead; finished into the decoded scale when the block is used.
+struct Raw {
+  float v;
+  uint32_t q;
+};
+
+__device__ __forceinline__ Raw fetch_raw(const SkinnyArgs& a, int64_t b, bool valid) {
+  Raw r{0.0f, 0u};
+  if (valid) {
+    if (!a.dq) {
+      r.v = __ldg(a.absmax + b);
+    } else {
+      r.q = __ldg(a.absmax_q + b);
+      r.v = __ldg(a.nested_absmax + (b >> 8));
+    }
+  }
+  return r;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// A unit's packed codes in a ring slot: 16 rows x 32 bytes, the 16-byte half h
+// of row r at 16-byte unit 2r + (h ^ ((r >> 2) & 1)); the swizzle keeps the
+// forward's 16-byte and the input gradient's 4-byte reads free of bank
+// conflicts.
+__device__ __forceinline__ int code_unit(int r, int h) { return 2 * r + (h ^ ((r >> 2) & 1)); }
+
+// Decoded block scales of `count` blocks into sc[0 .. count): block `block_of(idx)`
+// (-1 for none: scale 0).  The 8-bit codebook is staged in shared memory first
+// (`code8s`, 256 floats) and the statistics of four blocks per thread are
+// fetched together, so the whole decode costs about one memory round trip.
+// Called by all threads of the CTA.
+template <typename BlockOf>
+__device__ __forceinline__ void decode_scales(const SkinnyArgs& a, float* sc, float* code8s,
+                                              int count, BlockOf block_of) {
+  if (a.dq) {
+    for (int i = threadIdx.x; i < 256; i += kThreads) code8s[i] = __ldg(a.code8 + i);
+  }
+  const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
+  __syncthreads();
+  for (int i0 = threadIdx.x; i0 < count; i0 += 4 * kThreads) {
+    Raw r[4];
+    bool ok[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = i0 + j * kThreads;
+      const int64_t b = idx < count ? block_of(idx) : -1;
+      ok[j] = b >= 0;
+      r[j] = fetch_raw(a, ok[j] ? b : 0, ok[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = i0 + j * kThreads;
+      if (idx >= count) break;
+      float v = 0.0f;
+      if (ok[j]) v = a.dq ? __fadd_rn(__fmul_rn(code8s[r[j].q], r[j].v), offset) : r[j].v;
+      sc[idx] = v;
+    }
+  }
+}
+
+// Warp w's contiguous range [lo, hi) of a CTA's U units; per_tile units make
+// one output tile.  A range touches at most two tiles (the plan ensures it).
+struct WarpRange {
+  int lo, hi, t0;
+};
+
+__device__ __forceinline__ WarpRange warp_range(int w, int U, int per_tile) {
+  WarpRange r;
+  r.lo = (w * U) >> 4;
+  r.hi = ((w + 1) * U) >> 4;
+  r.t0 = r.lo < r.hi ? r.lo / per_tile : 0;
+  return r;
+}
+
+// Element e of tile i summed over the warps of the CTA, in warp order.  Warp w
+// keeps its last tile's partial at last + w * last_stride and, when its range
+// started in the tile below its last one, that first tile's partial at
+// first + w * first_stride.  The warps touching tile i form the contiguous run
+// from the warp holding unit i * per_tile to the one holding unit
+// (i + 1) * per_tile - 1.
+__device__ __forceinline__ int warp_of_unit(int u, int U) {
+  const int w = (16 * (u + 1) + U - 1) / U - 1;  // largest w with w * U / 16 <= u
+  return w < kWarps - 1 ? w : kWarps - 1;
+}
+
+__device__ __forceinline__ float cta_sum(int i, int e, int U, int per_tile, const float* first,
+                                         int first_stride, const float* last, int last_stride) {
+  static_assert(kWarps == 16, "warp ranges use w * U / 16");
+  const int a0 = i * per_tile, a1 = a0 + per_tile;
+  const int w0 = warp_of_unit(a0, U), w1 = warp_of_unit(a1 - 1, U);
+  float v = 0.0f;
+  for (int w = w0; w <= w1; ++w) {
+    const int lo = (w * U) >> 4, hi = ((w + 1) * U) >> 4;
+    if (lo >= hi) continue;
+    v = __fadd_rn(v, hi <= a1 ? last[w * last_stride + e] : first[w * first_stride + e]);
+  }
+  return v;
+}
+
+__device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Cluster reduction: element e of `total` is owned by rank e * S / total...; every
+// rank stores its CTA sum of e into the owner's receive buffer, row = its rank,
+// then one cluster barrier, then the owner adds the S rows in rank order.
+struct ClusterShare {
+  int e0, e1, len;  // this rank's elements [e0, e1); row length of the receive buffer
+};
+
+__device__ __forceinline__ ClusterShare cluster_share(int rank, int S, int total) {
+  ClusterShare c;
+  c.e0 = rank * total / S;
+  c.e1 = (rank + 1) * total / S;
+  c.len = (total + S - 1) / S;
+  return c;
+}
+
+// Rank owning element e (the inverse of cluster_share's ranges).
+__device__ __forceinline__ int cluster_owner(int e, int S, int total) {
+  int r = static_cast<int>((static_cast<int64_t>(e) * S) / total);
+  while (r + 1 < S && (r + 1) * total / S <= e) ++r;
+  while (r > 0 && r * total / S > e) --r;
+  return r;
+}
+
+__device__ __forceinline__ void cluster_push(float* recv, int rank, int S, int total, int e,
+                                             float v) {
+  const int owner = cluster_owner(e, S, total);
+  const int len = (total + S - 1) / S;
+  const int local = e - owner * total / S;
+  st_dsmem(mapa_shared(smem_addr(recv + rank * len + local), static_cast<uint32_t>(owner)), v);
+}
+
+template <typename Store>
+__device__ __forceinline__ void cluster_finish(const float* recv, int rank, int S, int total,
+                                               Store store) {
+  cluster_sync();
+  const ClusterShare c = cluster_share(rank, S, total);
+  for (int e = c.e0 + static_cast<int>(threadIdx.x); e < c.e1; e += kThreads) {
+    float v = 0.0f;
+    for (int q = 0; q < S; ++q) v = __fadd_rn(v, recv[q * c.len + (e - c.e0)]);
+    store(e, v);
+  }
+}
+
+constexpr int kFwdQuad = 4;      // 64-value blocks per forward unit (256 values per row)
+constexpr int kFwdUnit = 2048;   // bytes of a forward unit: 16 rows x 128
+constexpr int kFwdDepth = 2;     // ring slots per warp (forward)
+constexpr int kBwdDepth = 2;     // ring slots per warp (input gradient)
+constexpr int kBwdRows = 64;     // weight rows per input-gradient unit
+
+// Shared-memory layout of a CTA (byte offsets), common to the plan and the kernels.
+struct Layout {
+  int table, ring, first, recv, scales, code8, act, total;
+};
+
+__host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t cc, int64_t nt_max) {
+  Layout L;
+  const int slot_elems = mode == 0 ? mt * 8 * 16 : mt * 8 * 64;
+  const int unit = mode == 0 ? kFwdUnit : kBwdRows * 32 + mt * 8 * (kBwdRows * 2 + 16);
+  const int depth = mode == 0 ? kFwdDepth : kBwdDepth;
+  L.table = 0;
+  L.ring = kTableBytes;
+  L.first = L.ring + kWarps * depth * unit;
+  L.recv = L.first + kWarps * slot_elems * 4;
+  const int64_t total = nt_max * slot_elems;
+  const int64_t len = (total + S - 1) / S;
+  L.scales = L.recv + static_cast<int>((S > 1 ? S * len * 4 : 0) + 15) / 16 * 16;
+  // forward: the per-tile warp runs (int2 per tile); input gradient: decoded scales
+  const int64_t nscales = mode == 0 ? nt_max * 2 : nt_max * cc;
+  L.code8 = L.scales + static_cast<int>((nscales * 4 + 15) / 16 * 16);
+  L.act = L.code8 + 256 * 4;
+  const int64_t nch = (cc / 64 + kFwdQuad - 1) / kFwdQuad * kFwdQuad;  // forward: chunks of 64
+  L.total = mode == 0 ? L.act + static_cast<int>(mt * 8 * nch * 128) : L.act;
+  return L;
+}
+
+// ---------------------------------------------------------------- forward --
+//
+// Tile = 16 weight rows; a unit = one tile x four 64-value blocks (256 values
+// per row).  Lane (g, t4) holds rows g and g+8 of the tile and block t4 of the
+// unit: 64 values per row, one block scale per row.  MMA j (0..15) of a
+// unit gives contraction slots (2t4, 2t4+1) the values 4j, 4j+1 of block t4 and
+// slots (2t4+8, 2t4+9) the values 4j+2, 4j+3, for A (the weight) and B (the
+// activations) alike; the sum over the 16 slots is the same whatever order the
+// values take.  A unit's codes (16 rows x 128 bytes) land in a ring slot with
+// the 16-byte chunk c of row r at chunk c ^ (r & 7), which makes the lanes'
+// 16-byte reads conflict-free.  The activation slice of the CTA's contraction
+// sits in shared memory as 64-value chunks per token whose eight 16-byte units
+// are XOR-swizzled by (chunk & 3) | (token & 1) << 2, so the eight lanes of a
+// quarter warp (two tokens, four chunks, one unit index) hit different banks.
+template <int MT>  // 8-token MMA tiles: 1 (M <= 8) or 2 (M <= 16)
+__global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int D = kFwdDepth;
+  static_assert(D == 2, "the statistics rotate through two register sets");
+  constexpr int kSlotElems = MT * 8 * 16;  // [token][row], a power of two
+  constexpr int kSlotShift = MT == 1 ? 7 : 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int S = a.S;
+  const int rank = static_cast<int>(blockIdx.x) % S;
+  const int64_t cl = static_cast<int64_t>(blockIdx.x) / S;
+  const int64_t tile0 = cl * a.T / a.C;
+  const int nt = static_cast<int>((cl + 1) * a.T / a.C - tile0);
+  const int64_t nt_max = (a.T + a.C - 1) / a.C;
+  const int nbs = static_cast<int>(a.cc >> 6);  // blocks per contraction slice
+  const int64_t kb0 = static_cast<int64_t>(rank) * nbs;
+  const int nbr = static_cast<int>(a.KB - kb0 < nbs ? a.KB - kb0 : nbs);  // >= 1 by the plan
+  const int nq = (nbr + kFwdQuad - 1) / kFwdQuad;  // units per tile
+  const int nch = (nbs + kFwdQuad - 1) / kFwdQuad * kFwdQuad;
+  const int U = nt * nq;
+  const WarpRange mine = warp_range(warp, U, nq);
+  const int nunits = mine.hi - mine.lo;
+  const Layout L = make_layout(0, MT, S, a.cc, nt_max);
+  uint8_t* ring = smem + L.ring + warp * D * kFwdUnit;
+  float* first = reinterpret_cast<float*>(smem + L.first);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
+  float* code8s = reinterpret_cast<float*>(smem + L.code8);
+  int2* tile_warps = reinterpret_cast<int2*>(smem + L.scales);  // [tile] first and last warp
+  uint4* xs = reinterpret_cast<uint4*>(smem + L.act);           // [token][chunk][8 units]
+  const int64_t row_bytes = a.K >> 1;
+
+  // Copies: lane moves 16-byte chunk c = lane & 7 of rows r0 + 4j (j < 4) of a
+  // unit; (ii, iq) = (tile, block quad) of the next unit to copy.  The same call
+  // fetches the statistics of the lane's two blocks (rows g and g+8, block t4).
+  const int r0 = lane >> 3, cc8 = lane & 7;
+  const uint32_t ring_s = smem_addr(ring);
+  int issued = 0, ii = mine.t0, iq = mine.lo - mine.t0 * nq;
+  struct Stats {
+    Raw a, b;
+  };
+  auto fetch = [&](int64_t n, int64_t kb, bool ok) -> Raw {
+    Raw r{0.0f, 256u};  // q = 256: no block, scale 0
+    if (ok) {
+      const int64_t bi = n * a.KB + kb;
+      if (!a.dq) {
+        r.v = __ldg(a.absmax + bi);
+        r.q = 0u;
+      } else {
+        r.q = __ldg(a.absmax_q + bi);
+        r.v = __ldg(a.nested_absmax + (bi >> 8));
+      }
+    }
+    return r;
+  };
+  auto issue = [&]() -> Stats {
+    Stats st{Raw{0.0f, 256u}, Raw{0.0f, 256u}};
+    if (issued < nunits) {
+      const uint32_t dst = ring_s + (issued & (D - 1)) * kFwdUnit;
+      const int64_t n16 = (tile0 + ii) * 16;
+      const int64_t kbq = kb0 + kFwdQuad * iq;
+      const bool cok = kFwdQuad * iq + (cc8 >> 1) < nbr;
+      const uint8_t* src = a.packed + (n16 + r0) * row_bytes + kbq * 32 + 16 * cc8;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = r0 + 4 * j;
+        const bool ok = cok && n16 + r < a.N;
+        cp_async16(dst + (r * 8 + (cc8 ^ (r & 7))) * 16, ok ? src + 4 * j * row_bytes : a.packed,
+                   ok);
+      }
+      const bool bok = kFwdQuad * iq + t4 < nbr;
+      st.a = fetch(n16 + g, kbq + t4, bok && n16 + g < a.N);
+      st.b = fetch(n16 + g + 8, kbq + t4, bok && n16 + g + 8 < a.N);
+      if (++iq == nq) {
+        iq = 0;
+        ++ii;
+      }
+    }
+    ++issued;
+    cp_async_commit();
+    return st;
+  };
+  Stats s0, s1;  // statistics of the units in ring slots (q and q+1)
+  auto prologue = [&]() {
+    s0 = issue();
+    s1 = issue();
+    build_table(smem, a.code4);
+    if (a.dq)
+      for (int i = threadIdx.x; i < 256; i += kThreads) code8s[i] = __ldg(a.code8 + i);
+  };
+
+  if (a.prefetch) prologue();
+  grid_dependency_wait();
+  if (!a.prefetch) prologue();
+  allow_dependents();
+  {  // activation slice -> shared memory (asynchronous copies): tokens < M, zero beyond the slice
+    const int units = nch * 8;  // 16-byte units per token
+    const uint32_t xs_s = smem_addr(xs);
+    for (int tok = 0; tok < a.M; ++tok) {
+      const __nv_bfloat16* xrow = a.act + tok * a.ld_act + kb0 * 64;
+      for (int e = threadIdx.x; e < units; e += kThreads) {
+        const int c = e >> 3, q = e & 7;
+        const int slot = ((tok * nch + c) << 3) + (q ^ ((c & 3) | ((tok & 1) << 2)));
+        cp_async16(xs_s + slot * 16, c < nbr ? xrow + 8 * e : a.act, c < nbr);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  if (static_cast<int>(threadIdx.x) < nt) {  // warps touching each tile, for the reduction
+    const int i = threadIdx.x;
+    tile_warps[i] = make_int2(warp_of_unit(i * nq, U), warp_of_unit((i + 1) * nq - 1, U));
+  }
+  const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
+  __syncthreads();
+
+  const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
+  constexpr uint32_t kSel0 = lookup_sel(0), kSel1 = lookup_sel(1), kSel2 = lookup_sel(2),
+                     kSel3 = lookup_sel(3);
+  const int f = t4 | ((g & 1) << 2);  // activation swizzle of this lane's chunks
+  const int sw = g & 7;               // ring swizzle of rows g and g+8
+  auto scale = [&](const Raw& r) -> float {
+    if (!a.dq) return r.q == 256u ? 0.0f : r.v;
+    return r.q == 256u ? 0.0f : __fadd_rn(__fmul_rn(code8s[r.q], r.v), offset);
+  };
+  float acc[MT][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+  int ctile = mine.t0;
+  int ci = mine.t0, cq = mine.lo - mine.t0 * nq;  // (tile, block quad) being decoded
+
+  auto store_acc = [&](float* p) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const int tok = 8 * t + 2 * t4;
+      p[tok * 16 + g] = acc[t][0];
+      p[(tok + 1) * 16 + g] = acc[t][1];
+      p[tok * 16 + g + 8] = acc[t][2];
+      p[(tok + 1) * 16 + g + 8] = acc[t][3];
+      acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    }
+  };
+
+  for (int q = 0; q < nunits; ++q) {
+    cp_async_wait<D - 1>();
+    __syncwarp();
+    const uint8_t* slot = ring + (q & (D - 1)) * kFwdUnit;
+    const int i = ci, kbl = kFwdQuad * cq + t4;
+    if (++cq == nq) {
+      cq = 0;
+      ++ci;
+    }
+    if (i != ctile) {  // first tile done (a range touches at most two)
+      store_acc(first + warp * kSlotElems);
+      ctile = i;
+    }
+    const float sA = scale(s0.a), sB = scale(s0.b);
+    const uint64_t sA2 = pair2(sA, sA), sB2 = pair2(sB, sB);
+    const uint4 ca0 = lds128(slot + (g * 8 + ((2 * t4) ^ sw)) * 16);
+    const uint4 ca1 = lds128(slot + (g * 8 + ((2 * t4 + 1) ^ sw)) * 16);
+    const uint4 cb0 = lds128(slot + ((g + 8) * 8 + ((2 * t4) ^ sw)) * 16);
+    const uint4 cb1 = lds128(slot + ((g + 8) * 8 + ((2 * t4 + 1) ^ sw)) * 16);
+    const uint4* xr[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) xr[t] = xs + (((8 * t + g) * nch + kbl) << 3);
+    const uint32_t wa[8] = {ca0.x, ca0.y, ca0.z, ca0.w, ca1.x, ca1.y, ca1.z, ca1.w};
+    const uint32_t wb[8] = {cb0.x, cb0.y, cb0.z, cb0.w, cb1.x, cb1.y, cb1.z, cb1.w};
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {  // 16-byte activation unit u: MMAs 2u and 2u+1
+      uint4 xv[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) xv[t] = xr[t][u ^ f];
+      // word u holds values 8u .. 8u+7 of the block: bytes 0, 1 feed MMA 2u, bytes 2, 3 MMA 2u+1
+      const uint32_t af[4] = {lookup(smem, wa[u], lane8, kSel0, sA2),
+                              lookup(smem, wb[u], lane8, kSel0, sB2),
+                              lookup(smem, wa[u], lane8, kSel1, sA2),
+                              lookup(smem, wb[u], lane8, kSel1, sB2)};
+#pragma unroll
+      for (int t = 0; t < MT; ++t) mma16816(acc[t], af, xv[t].x, xv[t].y);
+      const uint32_t ag[4] = {lookup(smem, wa[u], lane8, kSel2, sA2),
+                              lookup(smem, wb[u], lane8, kSel2, sB2),
+                              lookup(smem, wa[u], lane8, kSel3, sA2),
+                              lookup(smem, wb[u], lane8, kSel3, sB2)};
+#pragma unroll
+      for (int t = 0; t < MT; ++t) mma16816(acc[t], ag, xv[t].z, xv[t].w);
+    }
+    __syncwarp();
+    s0 = s1;
+    s1 = issue();
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+  if (nunits > 0) store_acc(reinterpret_cast<float*>(ring));  // last tile -> own ring
+  __syncthreads();
+
+  // element e = (tile i, token, row): i = e >> kSlotShift; tokens >= M are skipped
+  const int M = static_cast<int>(a.M);
+  const int total = nt << kSlotShift;
+  const float* last = reinterpret_cast<const float*>(smem + L.ring);
+  auto store = [&](int e, float v) {
+    const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
+    const int64_t n = (tile0 + i) * 16 + (r & 15);
+    if ((r >> 4) < M && n < a.N) a.out[(r >> 4) * a.ld_out + n] = __float2bfloat16_rn(v);
+  };
+  for (int e = threadIdx.x; e < total; e += kThreads) {
+    const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
+    if ((r >> 4) >= M) continue;
+    const int2 tw = tile_warps[i];
+    float v = 0.0f;
+    for (int w = tw.x; w <= tw.y; ++w) {  // warps in order
+      const int lo = (w * U) >> 4, hi = ((w + 1) * U) >> 4;
+      if (lo >= hi) continue;
+      v = __fadd_rn(v, hi <= (i + 1) * nq ? last[w * (D * kFwdUnit / 4) + r]
+                                          : first[w * kSlotElems + r]);
+    }
+    if (S == 1)
+      store(e, v);
+    else
+      cluster_push(recv, rank, S, total, e, v);
+  }
+  if (S > 1) cluster_finish(recv, rank, S, total, store);
+}
+
+// ---------------------------------------------------------- input gradient --
+//
+// grad_x^T = W^T grad_y^T: the MMA's rows are in-features and its contraction
+// runs over weight rows.  Tile = one 64-value block column (64 in-features); a
+// unit = one tile x 64 weight rows, taken as four groups of 16.  In a group,
+// lane (g, t4) holds weight rows {2t4, 2t4+1, 2t4+8, 2t4+9} (contraction slots)
+// at the in-features 8g .. 8g+7 of the block (one 4-byte word per row).  MMA m
+// (0..3) gives output row g the in-feature 8g + 2m (high nibble of byte m) and
+// row g+8 the value 8g + 2m + 1 (low nibble), so the A operand pair of slots
+// (2t4, 2t4+1) at one in-feature is a byte made of one nibble of each of two
+// weight rows, looked up in the same table and scaled by the two rows' block
+// scales; a lane's accumulators stay on its own 16 in-features for the whole
+// column.  The unit's grad_y values travel in the same ring slot as its codes.
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int D = kBwdDepth;
+  constexpr int kRows = kBwdRows;                  // weight rows per unit
+  constexpr int kGyPitch = kRows * 2 + 16;         // bytes per token (padded)
+  constexpr int kUnit = kRows * 32 + MT * 8 * kGyPitch;
+  constexpr int kSlotElems = MT * 8 * 64;          // [token][in-feature]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int S = a.S;
+  const int rank = static_cast<int>(blockIdx.x) % S;
+  const int64_t cl = static_cast<int64_t>(blockIdx.x) / S;
+  const int64_t col0 = cl * a.T / a.C;
+  const int nt = static_cast<int>((cl + 1) * a.T / a.C - col0);
+  const int64_t nt_max = (a.T + a.C - 1) / a.C;
+  const int64_t nr0 = static_cast<int64_t>(rank) * a.cc;
+  const int64_t nr1 = a.N - nr0 < a.cc ? a.N : nr0 + a.cc;  // this CTA's weight rows
+  const int nn = static_cast<int>((nr1 - nr0 + kRows - 1) / kRows);
+  const int U = nt * nn;
+  const WarpRange mine = warp_range(warp, U, nn);
+  const int nunits = mine.hi - mine.lo;
+  const Layout L = make_layout(1, MT, S, a.cc, nt_max);
+  uint8_t* ring = smem + L.ring + warp * D * kUnit;
+  float* first = reinterpret_cast<float*>(smem + L.first);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);
+  float* sc = reinterpret_cast<float*>(smem + L.scales);  // [column][row - nr0]
+  const int64_t row_bytes = a.K >> 1;
+  const int ccs = static_cast<int>(a.cc);
+
+  // Copies of unit (ii, ij): code half (lane & 1) of rows (lane >> 1) + 16 j and
+  // grad_y chunks lane + 32 j (token c >> 3, rows 8 (c & 7) ..); ragged ends and
+  // absent tokens are written directly.
+  const int cr = lane >> 1, ch = lane & 1;
+  const uint32_t ring_s = smem_addr(ring);
+  int issued = 0, ii = mine.t0, ij = mine.lo - mine.t0 * nn;
+  auto gy_edge = [&](uint8_t* d, int tok, int64_t ng) {  // 8 values from row ng, zero-padded
+    uint16_t v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = (tok < a.M && ng + q < nr1)
+                 ? reinterpret_cast<const uint16_t*>(a.act + tok * a.ld_act)[ng + q]
+                 : static_cast<uint16_t>(0);
+    *reinterpret_cast<uint4*>(d) =
+        make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16), v[2] | (static_cast<uint32_t>(v[3]) << 16),
+                   v[4] | (static_cast<uint32_t>(v[5]) << 16), v[6] | (static_cast<uint32_t>(v[7]) << 16));
+  };
+  auto copy_gy = [&](int slot, int64_t n0, bool async) {
+#pragma unroll
+    for (int j = 0; j < MT * 8 * 8 / 32; ++j) {
+      const int c = lane + 32 * j, tok = c >> 3, part = c & 7;
+      const int64_t ng = n0 + 8 * part;
+      const uint32_t off = slot * kUnit + kRows * 32 + tok * kGyPitch + part * 16;
+      if (tok >= a.M) continue;  // absent tokens only feed discarded outputs
+      if (ng + 8 <= nr1) {
+        if (async)
+          cp_async16(ring_s + off, a.act + tok * a.ld_act + ng, true);
+        else
+          *reinterpret_cast<uint4*>(ring + off) =
+              *reinterpret_cast<const uint4*>(a.act + tok * a.ld_act + ng);
+      } else {
+        gy_edge(ring + off, tok, ng);
+      }
+    }
+  };
+  auto issue = [&](bool with_gy) {
+    if (issued < nunits) {
+      const int slot = issued % D;
+      const int64_t kb = col0 + ii;
+      const int64_t n0 = nr0 + static_cast<int64_t>(kRows) * ij;
+#pragma unroll
+      for (int j = 0; j < kRows / 16; ++j) {
+        const int r = cr + 16 * j;
+        const int64_t n = n0 + r;
+        const bool ok = n < nr1;
+        cp_async16(ring_s + slot * kUnit + code_unit(r, ch) * 16,
+                   ok ? a.packed + n * row_bytes + kb * 32 + 16 * ch : a.packed, ok);
+      }
+      if (with_gy) copy_gy(slot, n0, true);
+      if (++ij == nn) {
+        ij = 0;
+        ++ii;
+      }
+    }
+    ++issued;
+    cp_async_commit();
+  };
+  auto prologue = [&](bool with_gy) {
+    for (int j = 0; j < D; ++j) issue(with_gy);
+    build_table(smem, a.code4);
+    // scales [column][row - nr0], whole units; zero beyond the CTA's rows
+    decode_scales(a, sc, reinterpret_cast<float*>(smem + L.code8), nt * ccs,
+                  [&](int idx) -> int64_t {
+                    const int i = idx / ccs, nl = idx - i * ccs;
+                    const int64_t n = nr0 + nl;
+                    return n < nr1 ? n * a.KB + col0 + i : -1;
+                  });
+  };
+
+  if (a.prefetch) prologue(false);
+  grid_dependency_wait();
+  if (!a.prefetch) {
+    prologue(true);
+  } else {  // grad_y of the prefetched units, now that it is final
+    for (int j = 0, gj = mine.lo - mine.t0 * nn; j < D && j < nunits;
+         ++j, gj = gj + 1 == nn ? 0 : gj + 1)
+      copy_gy(j, nr0 + static_cast<int64_t>(kRows) * gj, false);
+  }
+  allow_dependents();
+  __syncthreads();
+
+  const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
+  const int rr[4] = {2 * t4, 2 * t4 + 1, 2 * t4 + 8, 2 * t4 + 9};
+  float acc[MT][4][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[t][m][0] = acc[t][m][1] = acc[t][m][2] = acc[t][m][3] = 0.0f;
+  int ccol = mine.t0;
+  int ci = mine.t0, cj = mine.lo - mine.t0 * nn;  // (column, row unit) being decoded
+
+  auto store_acc = [&](float* p) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int tok = 8 * t + 2 * t4, k = 8 * g + 2 * m;
+        p[tok * 64 + k] = acc[t][m][0];
+        p[(tok + 1) * 64 + k] = acc[t][m][1];
+        p[tok * 64 + k + 1] = acc[t][m][2];
+        p[(tok + 1) * 64 + k + 1] = acc[t][m][3];
+        acc[t][m][0] = acc[t][m][1] = acc[t][m][2] = acc[t][m][3] = 0.0f;
+      }
+  };
+
+  for (int q = 0; q < nunits; ++q) {
+    cp_async_wait<D - 1>();
+    __syncwarp();
+    const uint8_t* slot = ring + (q % D) * kUnit;
+    const int i = ci;
+    const int nl0 = kRows * cj;  // first row of the unit, relative to nr0
+    if (++cj == nn) {
+      cj = 0;
+      ++ci;
+    }
+    if (i != ccol) {  // first column done (a range touches at most two)
+      store_acc(first + warp * kSlotElems);
+      ccol = i;
+    }
+    const float* scol = sc + i * ccs + nl0;
+#pragma unroll
+    for (int rg = 0; rg < kRows / 16; ++rg) {  // 16-row groups of the unit
+      uint32_t w[4];
+      float s[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = 16 * rg + rr[k];
+        w[k] = *reinterpret_cast<const uint32_t*>(slot + code_unit(r, g >> 2) * 16 + (g & 3) * 4);
+        s[k] = scol[r];
+      }
+      const uint64_t s01 = pair2(s[0], s[1]), s23 = pair2(s[2], s[3]);
+      uint32_t b[MT][2];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const uint8_t* gy = slot + kRows * 32 + (8 * t + g) * kGyPitch + (16 * rg + 2 * t4) * 2;
+        b[t][0] = *reinterpret_cast<const uint32_t*>(gy);
+        b[t][1] = *reinterpret_cast<const uint32_t*>(gy + 16);
+      }
+      // table indices: byte m = (code of row 2t4, code of row 2t4+1) at in-feature
+      // 8g + 2m (even) or 8g + 2m + 1 (odd); likewise rows 2t4+8, 2t4+9
+      const uint32_t e01 = (w[0] & 0xf0f0f0f0u) | ((w[1] >> 4) & 0x0f0f0f0fu);
+      const uint32_t o01 = ((w[0] << 4) & 0xf0f0f0f0u) | (w[1] & 0x0f0f0f0fu);
+      const uint32_t e23 = (w[2] & 0xf0f0f0f0u) | ((w[3] >> 4) & 0x0f0f0f0fu);
+      const uint32_t o23 = ((w[2] << 4) & 0xf0f0f0f0u) | (w[3] & 0x0f0f0f0fu);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t sel = lookup_sel(static_cast<uint32_t>(m));
+        const uint32_t af[4] = {lookup(smem, e01, lane8, sel, s01), lookup(smem, o01, lane8, sel, s01),
+                                lookup(smem, e23, lane8, sel, s23), lookup(smem, o23, lane8, sel, s23)};
+#pragma unroll
+        for (int t = 0; t < MT; ++t) mma16816(acc[t][m], af, b[t][0], b[t][1]);
+      }
+    }
+    __syncwarp();
+    issue(true);
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+  if (nunits > 0) store_acc(reinterpret_cast<float*>(ring));  // last column -> own ring
+  __syncthreads();
+
+  const int M = static_cast<int>(a.M);
+  const int total = nt * M * 64;  // (column, token, in-feature)
+  const float* last = reinterpret_cast<const float*>(smem + L.ring);
+  auto store = [&](int e, float v) {
+    const int i = e / (M * 64), r = e - i * M * 64;
+    a.out[(r >> 6) * a.ld_out + (col0 + i) * 64 + (r & 63)] = __float2bfloat16_rn(v);
+  };
+  for (int e = threadIdx.x; e < total; e += kThreads) {
+    const int i = e / (M * 64), r = e - i * M * 64;
+    const float v = cta_sum(i, r, U, nn, first, kSlotElems, last, D * kUnit / 4);
+    if (S == 1)
+      store(e, v);
+    else
+      cluster_push(recv, rank, S, total, e, v);
+  }
+  if (S > 1) cluster_finish(recv, rank, S, total, store);
+}
+
+template <int MODE, int MT>
+cudaError_t configure(void (*&kern)(SkinnyArgs)) {
+  kern = MODE == 0 ? skinny_fwd_kernel<MT> : skinny_dgrad_kernel<MT>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMaxSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return cudaSuccess;
+}
+
+// Clusters of S CTAs (with `smem` bytes each) that can be resident at once.
+template <int MODE, int MT>
+int max_clusters_mt(int S, size_t smem) {
+  void (*kern)(SkinnyArgs) = nullptr;
+  if (configure<MODE, MT>(kern) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(S), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Cached per (mode, tiles, S, shared-memory size).
+int max_clusters(int mode, int mt, int S, size_t smem) {
+  struct Entry {
+    int mode, mt, S;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : cache)
+    if (e.mode == mode && e.mt == mt && e.S == S && e.smem == smem) return e.n;
+  int n;
+  if (mode == 0)
+    n = mt == 1 ? max_clusters_mt<0, 1>(S, smem) : max_clusters_mt<0, 2>(S, smem);
+  else
+    n = mt == 1 ? max_clusters_mt<1, 1>(S, smem) : max_clusters_mt<1, 2>(S, smem);
+  cache.push_back(Entry{mode, mt, S, smem, n});
+  return n;
+}
+
+template <int MODE, int MT>
+cudaError_t launch_mt(const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s) {
+  void (*kern)(SkinnyArgs) = nullptr;
+  cudaError_t ce = configure<MODE, MT>(kern);
+  if (ce != cudaSuccess) return ce;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.C * p.S), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (p.S > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(p.S);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+// Plan: the contraction split S (cluster size) and the number C of clusters
+// (one CTA per SM).  Tiles are dealt to clusters in balanced contiguous ranges;
+// the cost is the busiest CTA's weight values plus a charge per rank for the
+// cluster reduction.  A warp's unit range must touch at most two tiles, and the
+// shared memory must fit.  A deterministic function of the shape and the SM
+// count.
+bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* out) {
+  if (M < 1 || M > kSkinnyMaxM || sms < 1 || K % 64 != 0) return false;
+  const int mt = M <= 8 ? 1 : 2;
+  const int64_t KB = K / 64;
+  const int64_t T = mode == 0 ? (N + 15) / 16 : KB;      // output tiles
+  const int64_t steps = mode == 0 ? KB : (N + kBwdRows - 1) / kBwdRows;  // contraction steps
+  const int64_t gran = mode == 0 ? 64 : kBwdRows;                        // contraction per step
+  double best = 1e300;
+  SkinnyPlan bp;
+  const int ss[4] = {1, 2, 4, 8};
+  for (int si = 0; si < 4; ++si) {
+    const int S = ss[si];
+    const int64_t per = (steps + S - 1) / S;  // steps per rank
+    if ((steps + per - 1) / per != S) continue;
+    int64_t C64 = sms / S;
+    if (C64 > T) C64 = T;
+    if (C64 < 1) continue;
+    int C = static_cast<int>(C64);
+    int64_t nt_max = (T + C - 1) / C;
+    Layout L = make_layout(mode, mt, S, per * gran, nt_max);
+    // clusters must all be resident at once (a GPC holds whole clusters only)
+    for (int it = 0; S > 1 && it < 4; ++it) {
+      const int cmax = max_clusters(mode, mt, S, static_cast<size_t>(L.total));
+      if (cmax >= C) break;
+      C = cmax;
+      if (C < 1) break;
+      nt_max = (T + C - 1) / C;
+      L = make_layout(mode, mt, S, per * gran, nt_max);
+    }
+    if (C < 1) continue;
+    const int64_t upt = mode == 0 ? (per + kFwdQuad - 1) / kFwdQuad : per;  // units per tile
+    if ((nt_max * upt + kWarps - 1) / kWarps > upt) continue;  // ranges span <= 2 tiles
+    if (static_cast<size_t>(L.total) > kMaxSmem) continue;
+    // cycles at ~24 weight values per clock and SM, plus the cluster exchange
+    const double cost = static_cast<double>(nt_max) * per * (mode == 0 ? 1024 : 4096) / 24.0 +
+                        (S > 1 ? 1500.0 : 0.0);
+    if (cost < best * 0.999) {
+      best = cost;
+      bp.S = S;
+      bp.C = C;
+      bp.T = T;
+      bp.cc = per * gran;
+      bp.smem = static_cast<size_t>(L.total);
+    }
+  }
+  if (bp.S == 0) return false;
+  *out = bp;
+  return true;
+}
+
+cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s) {
+  const bool mt1 = a.M <= 8;
+  if (mode == 0) return mt1 ? launch_mt<0, 1>(a, p, s) : launch_mt<0, 2>(a, p, s);
+  return mt1 ? launch_mt<1, 1>(a, p, s) : launch_mt<1, 2>(a, p, s);
+}
+
+}  // namespace nf4

@@ -84,7 +84,9 @@ enum {
   NF4_PATH_TOTAL = 7,        /* every launch of the library                */
   NF4_PATH_GEMV_FWD = 8,     /* small-M SIMT forward                       */
   NF4_PATH_GEMV_DGRAD = 9,   /* small-M SIMT input gradient                */
-  NF4_NUM_PATHS = 10
+  NF4_PATH_SKINNY_FWD = 10,  /* small-M tensor-core (mma.sync) forward     */
+  NF4_PATH_SKINNY_DGRAD = 11,/* small-M tensor-core input gradient         */
+  NF4_NUM_PATHS = 12
 };
 
 /* A quantised weight: the tensors of the pages' QuantState as plain device
@@ -236,6 +238,29 @@ nf4_status nf4_device_status(int32_t* out, int32_t clear);
  * two settings; each setting is deterministic.  NF4_CTA_PAIR=1 in the environment
  * sets the initial value to 1. */
 void nf4_set_cta_pairs(int32_t enabled);
+
+/* Declares (enabled != 0) that no kernel running just before a product call on
+ * the same stream writes that call's weight tensors (packed codes, statistics,
+ * codebooks), as holds for a frozen weight.  The small-M kernels are launched
+ * with programmatic dependent launch: they start while the previous kernel on
+ * the stream drains and wait for it before they read activations or write
+ * outputs.  With this declaration they also read the weight before that wait,
+ * overlapping its HBM stream with the previous kernel's tail.  Off by default
+ * (every read then follows the wait).  Results do not depend on the setting. */
+void nf4_set_weight_prefetch(int32_t enabled);
+
+/* Kernels for the dense products at small M (M <= 16), for comparisons and tests:
+ *   NF4_SMALL_M_AUTO  (default) the tensor-core small-M kernels (warp-level bf16
+ *                     MMA over a shared dequantisation table, contraction split
+ *                     across thread-block clusters) where their plan fits, else
+ *                     as below;
+ *   NF4_SMALL_M_SIMT  the SIMT GEMV kernels for M <= 4, the tiled tcgen05
+ *                     kernels above;
+ *   NF4_SMALL_M_TILES the tiled tcgen05 kernels with a split contraction.
+ * Every choice is deterministic; results may differ in the last bit between
+ * choices (different fp32 summation grouping). */
+enum { NF4_SMALL_M_AUTO = 0, NF4_SMALL_M_SIMT = 1, NF4_SMALL_M_TILES = 2 };
+void nf4_set_small_m_path(int32_t path);
 
 /* Human-readable message of the last CUDA error that made a call of this thread
  * return NF4_ERR_CUDA ("no error" if none).  Static string. */

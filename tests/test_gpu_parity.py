@@ -13,6 +13,7 @@ import torch
 import oracle
 from oracle import codebooks as ocb
 import bit_nf4_quantized_linear_gb300 as nf4
+from bit_nf4_quantized_linear_gb300 import _lib, ops
 from bit_nf4_quantized_linear_gb300 import synth
 from tests.helpers import bf16_bits, oracle_state, parity
 
@@ -264,15 +265,26 @@ def test_grouped_empty_experts_and_bad_offsets():
     assert nf4.device_status(clear=True) == 8
 
 
-# ------------------------------------------------------------- small-M GEMV --
+# ------------------------------------------------------------------ small M --
+# M <= 16: the tensor-core small-M kernels by default (warp-level MMA over a
+# shared dequantisation table, contraction split over thread-block clusters);
+# the SIMT GEMV and the split tcgen05 tiles on request.
 
-GEMV = [(1, 64, 64), (2, 104, 128), (3, 136, 1088), (4, 4096, 1024), (5, 296, 2112),
-        (7, 200, 2112), (8, 96, 5120), (1, 4096, 14336), (2, 14336, 4096)]
+SMALL_M = [(1, 64, 64), (2, 104, 128), (3, 136, 1088), (4, 4096, 1024), (5, 296, 2112),
+           (7, 200, 2112), (8, 96, 5120), (1, 4096, 14336), (2, 14336, 4096), (6, 4096, 14336),
+           (9, 520, 2112), (13, 1000, 4096), (16, 4096, 4096)]
 
 
-@pytest.mark.parametrize("M,N,K", GEMV)
+@pytest.fixture
+def restore_small_m():
+    yield
+    ops.set_small_m_path(_lib.SMALL_M_AUTO)
+    ops.set_weight_prefetch(False)
+
+
+@pytest.mark.parametrize("M,N,K", SMALL_M)
 @pytest.mark.parametrize("dq", [False, True])
-def test_gemv_path_parity(M, N, K, dq):
+def test_small_m_default_path_parity(M, N, K, dq):
     w, st, g = _quant_pair(N, K, dq, seed=7 * M + N + K)
     x = synth.activation(M, K, g)
     gy = synth.activation(M, N, g)
@@ -281,17 +293,44 @@ def test_gemv_path_parity(M, N, K, dq):
     y = nf4.linear_fwd(x.to(DEV), w)
     gx = nf4.linear_dgrad(gy.to(DEV), w)
     c = nf4.path_counters()
-    if M <= 4:
-        assert c["gemv_fwd"] == 1 and c["linear_fwd"] == 0
-        assert c["gemv_dgrad"] == 1 and c["linear_dgrad"] == 0
-    else:
-        assert c["gemv_fwd"] == 0 and c["linear_fwd"] == 1
-    parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"gemv fwd {M}x{N}x{K}")
-    parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"gemv dgrad {M}x{N}x{K}")
+    if M <= 8:
+        assert c["skinny_fwd"] == 1 and c["skinny_dgrad"] == 1, c
+    assert c["skinny_fwd"] + c["gemv_fwd"] + c["linear_fwd"] == 1
+    assert c["skinny_dgrad"] + c["gemv_dgrad"] + c["linear_dgrad"] == 1
+    parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"small-M fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"small-M dgrad {M}x{N}x{K}")
+    assert torch.equal(nf4.linear_fwd(x.to(DEV), w).view(torch.int16), y.view(torch.int16))
+    assert torch.equal(nf4.linear_dgrad(gy.to(DEV), w).view(torch.int16), gx.view(torch.int16))
 
 
-@pytest.mark.parametrize("N,K", [(64, 128), (296, 2048)])
-def test_gemv_identity_probe_exact(N, K):
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (3, 136, 1088), (4, 4096, 1024), (2, 14336, 4096),
+                                   (12, 296, 2112)])
+def test_small_m_simt_and_tile_paths(M, N, K, restore_small_m):
+    w, st, g = _quant_pair(N, K, True, seed=3 * M + N + K)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    for path in (_lib.SMALL_M_SIMT, _lib.SMALL_M_TILES):
+        ops.set_small_m_path(path)
+        nf4.reset_path_counters()
+        y = nf4.linear_fwd(x.to(DEV), w)
+        gx = nf4.linear_dgrad(gy.to(DEV), w)
+        c = nf4.path_counters()
+        assert c["skinny_fwd"] == 0 and c["skinny_dgrad"] == 0
+        if path == _lib.SMALL_M_SIMT and M <= 4:
+            assert c["gemv_fwd"] == 1 and c["gemv_dgrad"] == 1
+        else:
+            assert c["linear_fwd"] == 1 and c["linear_dgrad"] == 1
+        parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"path {path} fwd {M}x{N}x{K}")
+        parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"path {path} dgrad {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("N,K", [(64, 128), (296, 2048), (4096, 4096)])
+@pytest.mark.parametrize("path", [0, 1])
+def test_small_m_identity_probe_exact(N, K, path, restore_small_m):
+    """One-hot activations read single weight values back: the small-M operands
+    are exactly the dequantised bf16 weights."""
+    ops.set_small_m_path(path)
     w, st, _ = _quant_pair(N, K, True, seed=N + K)
     wb = oracle.dequantize(st, "bf16")
     eye = torch.eye(K, dtype=torch.bfloat16)[:4].contiguous()
@@ -300,6 +339,26 @@ def test_gemv_identity_probe_exact(N, K):
     eyen = torch.eye(N, dtype=torch.bfloat16)[:4].contiguous()
     gx = nf4.linear_dgrad(eyen.to(DEV), w)
     np.testing.assert_array_equal(bf16_bits(gx), wb[:4])
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (8, 4096, 14336), (16, 1024, 4096)])
+def test_weight_prefetch_leaves_results_unchanged(M, N, K, restore_small_m):
+    """Reading the frozen weight before the grid dependency resolves changes only
+    timing: outputs are bit-identical with and without it, also back to back."""
+    g = synth.generator(M + K)
+    w = nf4.quantize(synth.weight(N, K, g).to(DEV), double_quant=True)
+    x = synth.activation(M, K, g).to(DEV)
+    gy = synth.activation(M, N, g).to(DEV)
+    outs = []
+    for pf in (False, True):
+        ops.set_weight_prefetch(pf)
+        y1 = nf4.linear_fwd(x, w)
+        g1 = nf4.linear_dgrad(gy, w)
+        y2 = nf4.linear_fwd(x, w)   # starts while the previous kernel drains
+        outs.append((y1, g1, y2))
+    for t in range(3):
+        assert torch.equal(outs[0][t].view(torch.int16), outs[1][t].view(torch.int16))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[0][2].view(torch.int16))
 
 
 @pytest.mark.parametrize("M,N,K,mode", [(512, 4096, 4096, 0), (512, 4096, 4096, 1), (1024, 640, 1024, 0),
@@ -321,4 +380,4 @@ def test_cta_pair_and_single_cta_tiles_both_match_oracle(M, N, K, mode):
             assert torch.equal(f(a.to(DEV), w).view(torch.int16), o.view(torch.int16))
             outs.append(o)
     finally:
-        ops.set_cta_pairs(True)
+        ops.set_cta_pairs(False)
