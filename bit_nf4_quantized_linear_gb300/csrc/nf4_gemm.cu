@@ -116,6 +116,16 @@ __device__ __forceinline__ void record_error(const GemmArgs& a, int code) {
   *reinterpret_cast<volatile int*>(a.status) = code;
 }
 
+// Programmatic dependent launch: wait for the preceding grid on the stream
+// (its results visible), and let the next grid launch early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Bounded wait, slow path: true once the phase completed; false on abort (another
 // role gave up) or after kTimeoutNs, in which case the timeout is recorded.
 // `cluster`: the phase is completed by arrivals from the other CTA of a pair, so
@@ -252,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---------------------------------------------------------------- prologue --
-  if (threadIdx.x < 16) sh.code4[threadIdx.x] = a.code4[threadIdx.x];
-  if (a.dq)
-    for (int j = threadIdx.x; j < 256; j += kThreads) sh.code8[j] = a.code8[j];
+  // Local setup first (barriers, tensor memory, tensor-map prefetch): with
+  // programmatic dependent launch it overlaps the previous kernel's tail.  Global
+  // memory is touched only after the grid dependency has resolved.
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::kStagesP; ++i) {
       mbar_init(bar_at(sh, kBarPFull + i), 1);
@@ -277,6 +287,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     *sh.abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
+  if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
+  if (warp == kWarpMma) {
+    if (CG == 2) {
+      tmem_alloc_pair(smem_addr(sh.tmem_slot), G::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+  }
+  grid_dependency_wait();
+  allow_dependents();
+  if (threadIdx.x < 16) sh.code4[threadIdx.x] = a.code4[threadIdx.x];
+  if (a.dq)
+    for (int j = threadIdx.x; j < 256; j += kThreads) sh.code8[j] = a.code8[j];
   if (a.grouped && threadIdx.x == kWarpEpi0 * 32) {
     // Per-expert token tiles and their prefix; offsets outside the contract are
     // reported and that expert is skipped.
@@ -294,18 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *item_count = acc;
     if (bad) record_error(a, kStatusBadOffsets);
-  }
-  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
-  if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
-  if (warp == kWarpMma) {
-    if (CG == 2) {
-      tmem_alloc_pair(smem_addr(sh.tmem_slot), G::kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
-      tmem_relinquish();
-    }
-    tc_fence_before();
   }
   __syncthreads();
   if (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
@@ -601,6 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) splitk_reduce_vec_kernel(const float* __restrict__ ws, int splits,
                                                                 int64_t M, int64_t ncols,
                                                                 __nv_bfloat16* __restrict__ out, int64_t ld) {
+  grid_dependency_wait();
+  allow_dependents();
   const int64_t total = M * ncols;
   const int64_t nq = (ncols + 3) / 4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < M * nq;
@@ -639,6 +656,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
                                                             int64_t M, int64_t ncols,
                                                             __nv_bfloat16* __restrict__ out, int64_t ld) {
   __shared__ float part[8][32];
+  grid_dependency_wait();
+  allow_dependents();
   const int64_t total = M * ncols;
   const int64_t slices = (ncols + 31) / 32;
   const int c = threadIdx.x & 31, g = threadIdx.x >> 5;
@@ -673,22 +692,20 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (CG == 1) {
-    kern<<<grid, kThreads, Geo<BT, CG>::kSmem, s>>>(ta, tp, a);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Geo<BT, CG>::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CG == 2 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tp, a);
 }
 
@@ -719,19 +736,27 @@ cudaError_t launch_gemm(int mode, int bt, int cg, const GemmArgs& a, const CUten
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  __nv_bfloat16* out, int64_t ld, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (splits <= 8) {
     int64_t grid = (M * ((ncols + 3) / 4) + 255) / 256;
     if (grid > 8192) grid = 8192;
     if (grid < 1) grid = 1;
-    splitk_reduce_vec_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(ws, splits, M, ncols, out, ld);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_vec_kernel, ws, splits, M, ncols, out, ld);
   }
   // Many splits (the small-M input gradient): one CTA per 32 outputs.
   int64_t grid = M * ((ncols + 31) / 32);
   if (grid > 16384) grid = 16384;
   if (grid < 1) grid = 1;
-  splitk_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(ws, splits, M, ncols, out, ld);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, splits, M, ncols, out, ld);
 }
 
 }  // namespace nf4
