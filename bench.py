@@ -307,9 +307,10 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_val = job_throughput(flops, world, e2e_ms)
 
-    sweep = None
+    sweep = grouped = None
     if rank == 0 and world == 1 and not args.no_sweep:
         sweep = run_sweep(dev, pk)
+        grouped = run_grouped(dev, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -352,6 +353,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if sweep is not None:
         out["m_sweep_4096"] = sweep
+    if grouped is not None:
+        out["grouped_olmoe"] = grouped
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
@@ -409,9 +412,52 @@ def run_sweep(dev, pk):
             return statistics.median(times) * 1e-3  # seconds per call group
         fwd = lambda w: ops.linear_fwd(x, w, out=y, ws=wsb)
         bwd = lambda w: ops.linear_dgrad(gy, w, out=gx, ws=wsb)
+        nf4.reset_path_counters()
+        fwd(base)
+        pf = [k for k, v in nf4.path_counters().items() if v and k not in ("total", "splitk_reduce")]
+        nf4.reset_path_counters()
+        bwd(base)
+        pd = [k for k, v in nf4.path_counters().items() if v and k not in ("total", "splitk_reduce")]
         t_f = timed([fwd])
         t_d = timed([bwd])
         t = t_f + t_d
+        # comparison arms in the same session: dense bf16 cuBLAS (same shape, a dense
+        # weight per replica) and dequantise-then-matmul (the unfused design)
+        dense = [nf4.dequantize(w) for w in reps[:max(2, min(R, int(4 * L2_BYTES / (2 * N * K)) + 1))]]
+        Rd = len(dense)
+        def timed_dense(fn):
+            with torch.cuda.stream(s):  # library handles are created outside the capture
+                fn(dense[0])
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                for wd in dense:
+                    fn(wd)
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(10):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                graph.replay()
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b) / Rd)
+            del graph
+            return statistics.median(times) * 1e-3
+        t_cub = timed_dense(lambda wd: (torch.matmul(x, wd.t(), out=y), torch.matmul(gy, wd, out=gx)))
+        wtmp = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+        def deq_linear(w):
+            ops.dequantize(w, out=wtmp)
+            torch.matmul(x, wtmp.t(), out=y)
+            ops.dequantize(w, out=wtmp)
+            torch.matmul(gy, wtmp, out=gx)
+        with torch.cuda.stream(s):
+            deq_linear(base)
+        torch.cuda.synchronize()
+        t_deq = timed([deq_linear])
+        del dense, wtmp
         tfl = 4.0 * M * N * K / t / 1e12
         gbs = 2.0 * wbytes / t / 1e9
         res.append({"M": M, "us_per_fwd_dgrad": round(t * 1e6, 2), "us_fwd": round(t_f * 1e6, 2),
@@ -420,10 +466,79 @@ def run_sweep(dev, pk):
                     "weight_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
                     "fwd_weight_gbs": round(wbytes / t_f / 1e9, 1),
                     "dgrad_weight_gbs": round(wbytes / t_d / 1e9, 1),
-                    "replicas": R})
+                    "replicas": R, "path_fwd": pf, "path_dgrad": pd,
+                    "cublas_dense_bf16_us": round(t_cub * 1e6, 2),
+                    "dequant_then_matmul_us": round(t_deq * 1e6, 2)})
         del reps, x, gy, y, gx, wsb
         torch.cuda.empty_cache()
     return res
+
+
+def run_grouped(dev, pk):
+    """OLMoE-shaped experts (64 experts, hidden 2048, intermediate 1024, 512 tokens,
+    top-8 routing from seeded uniform logits): grouped forward + input gradient of
+    the gate, up and down stacks, each a CUDA graph over weight replicas."""
+    import torch
+    import bit_nf4_quantized_linear_gb300 as nf4
+    from bit_nf4_quantized_linear_gb300 import ops, synth
+    c = synth.OLMOE
+    E, H, I = c["experts"], c["hidden"], c["inter"]
+    g = synth.generator(4)
+    row_token, offsets = synth.routing(c["tokens"], E, c["topk"], g)
+    T = int(offsets[-1])
+    offs = offsets.to(dev)
+    out = {"workload": "olmoe experts: 64 x (gate, up 2048->1024; down 1024->2048), "
+                       "512 tokens top-8 (4096 rows), NF4 double quant, grouped fwd + grad_x",
+           "rows": T}
+    total_t, total_fl, total_b = 0.0, 0.0, 0.0
+    for name, N_e, K in (("gate", I, H), ("up", I, H), ("down", H, I)):
+        base = nf4.quantize(synth.weight(E * N_e, K, g).to(dev), double_quant=True)
+        wbytes = base.nbytes()
+        R = max(2, min(8, int(4 * L2_BYTES / wbytes) + 1))
+        reps = [base] + [nf4.NF4Weight(base.packed.clone(), None, base.absmax_q.clone(),
+                                       base.nested_absmax.clone(), base.nested_offset.clone(),
+                                       base.code4, base.code8, base.N, base.K, True) for _ in range(R - 1)]
+        x = synth.activation(T, K, g).to(dev)
+        gy = synth.activation(T, N_e, g).to(dev)
+        y = torch.empty(T, N_e, dtype=torch.bfloat16, device=dev)
+        gx = torch.empty(T, K, dtype=torch.bfloat16, device=dev)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for w in reps[:2]:
+                ops.grouped_fwd(x, offs, w, E, out=y)
+                ops.grouped_dgrad(gy, offs, w, E, out=gx)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for w in reps:
+                ops.grouped_fwd(x, offs, w, E, out=y)
+                ops.grouped_dgrad(gy, offs, w, E, out=gx)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b) / R)
+        t = statistics.median(times) * 1e-3
+        fl = 4.0 * T * N_e * K
+        out[name] = {"us_fwd_dgrad": round(t * 1e6, 2), "tflops": round(fl / t / 1e12, 2),
+                     "weight_gbs": round(2 * wbytes / t / 1e9, 1)}
+        total_t += t
+        total_fl += fl
+        total_b += 2 * wbytes
+        del graph, reps, x, gy, y, gx
+        torch.cuda.empty_cache()
+    out["tflops"] = round(total_fl / total_t / 1e12, 2)
+    out["frac_tc"] = round(total_fl / total_t / 1e12 / pk["bf16_tflops"], 4)
+    out["weight_gbs"] = round(total_b / total_t / 1e9, 1)
+    return out
 
 
 # ------------------------------------------------------------- CPU oracle --

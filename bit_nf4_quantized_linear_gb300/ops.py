@@ -115,10 +115,15 @@ def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.T
                      code8 if double_quant else None, N, K, double_quant)
 
 
-def dequantize(w: NF4Weight, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
-    """nf4_dequantize: dense [N, K] copy of the weight (checks only; not the fused path)."""
+def dequantize(w: NF4Weight, dtype: torch.dtype = torch.bfloat16,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_dequantize: dense [N, K] copy of the weight (checks and the unfused comparison
+    arm; not the fused path).  `out`, when given, is a contiguous [N, K] tensor of `dtype`."""
     _need_cuda("dequantize", w.packed)
-    out = torch.empty(w.N, w.K, dtype=dtype, device=w.packed.device)
+    if out is None:
+        out = torch.empty(w.N, w.K, dtype=dtype, device=w.packed.device)
+    elif out.shape != (w.N, w.K) or out.dtype != dtype or not out.is_contiguous():
+        raise ValueError("dequantize: out must be a contiguous [N, K] tensor of the requested dtype")
     code = {torch.float32: _lib.DTYPE_F32, torch.bfloat16: _lib.DTYPE_BF16}[dtype]
     s = w.struct()
     _lib.check(_lib.lib().nf4_dequantize(ctypes.byref(s), _ptr(out), code, _stream()),
