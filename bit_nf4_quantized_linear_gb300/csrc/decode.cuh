@@ -65,11 +65,22 @@ __device__ __forceinline__ void lookup4(uint32_t v, const Lut& L, uint32_t& out0
 }
 
 // Eight packed codes (one 32-bit word; byte j holds value 2j high, 2j+1 low) to
-// eight bf16 values, packed pairwise, value 0 lowest.
+// eight bf16 values, packed pairwise, value 0 lowest.  The permute selectors of
+// both halves come from one mask of the whole word (a permute reads only the low
+// 16 bits of its selector).
 __device__ __forceinline__ uint4 decode8(uint32_t w, const Lut& L) {
+  const uint32_t sel = w & 0x77777777u;
+  const uint32_t s3 = ((w >> 1) & 0x44444444u) | 0x32103210u;
+  const uint32_t sel_h = sel >> 16, s3_h = s3 >> 16;
   uint4 o;
-  lookup4(w, L, o.x, o.y);
-  lookup4(w >> 16, L, o.z, o.w);
+  uint32_t lo = __byte_perm(__byte_perm(L.lo[0], L.lo[1], sel), __byte_perm(L.lo[2], L.lo[3], sel), s3);
+  uint32_t hi = __byte_perm(__byte_perm(L.hi[0], L.hi[1], sel), __byte_perm(L.hi[2], L.hi[3], sel), s3);
+  o.x = __byte_perm(lo, hi, 0x4051u);
+  o.y = __byte_perm(lo, hi, 0x6273u);
+  lo = __byte_perm(__byte_perm(L.lo[0], L.lo[1], sel_h), __byte_perm(L.lo[2], L.lo[3], sel_h), s3_h);
+  hi = __byte_perm(__byte_perm(L.hi[0], L.hi[1], sel_h), __byte_perm(L.hi[2], L.hi[3], sel_h), s3_h);
+  o.z = __byte_perm(lo, hi, 0x4051u);
+  o.w = __byte_perm(lo, hi, 0x6273u);
   return o;
 }
 

@@ -42,14 +42,15 @@ namespace {
 
 using namespace nf4ptx;
 
-constexpr int kThreads = 15 * 32;
+constexpr int kDecGroups = 3;                    // decoder groups of four warps
+constexpr int kNumDecWarps = 4 * kDecGroups;
 constexpr int kWarpTma = 0;   // packed-code producer
-constexpr int kWarpTmaX = 14; // activation producer
 constexpr int kWarpMma = 1;
 constexpr int kWarpEpi0 = 2;
 constexpr int kNumEpiWarps = 4;
 constexpr int kWarpDec0 = 6;
-constexpr int kNumDecWarps = 8;
+constexpr int kWarpTmaX = kWarpDec0 + kNumDecWarps;  // activation producer
+constexpr int kThreads = (kWarpTmaX + 1) * 32;
 constexpr int kAStage = kTileW * kTileK * 2;  // 16 KB of bf16
 constexpr int kPkStage = kTileW * kTileK / 2;  // 4 KB of packed codes
 constexpr int kMiscBytes = 8192;
@@ -60,7 +61,9 @@ template <int BT, int CG>
 struct Geo {
   static constexpr int kXStage = (BT / CG) * 128;  // this CTA's BT/CG token rows of 64 bf16
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
-  static constexpr int kStagesA = 3;                // decoded operand tiles
+  // Decoded operand tiles: one slot more than decoder groups where the activation
+  // tiles leave room, so a group never waits on the MMAs of the step just before.
+  static constexpr int kStagesA = BT >= 256 ? kDecGroups : kDecGroups + 1;
   static constexpr int kStagesP = BT <= 64 ? 16 : 8; // packed-code tiles (prefetched far ahead)
   static constexpr int kStagesX0 = (kBudget - kStagesA * kAStage - kStagesP * kPkStage) / kXStage;
   static constexpr int kStagesX = kStagesX0 > 8 ? 8 : kStagesX0;  // activation tiles
@@ -71,6 +74,9 @@ struct Geo {
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;
   static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
   static_assert(kStagesX >= 3, "pipeline too shallow");
+  static_assert(kStagesA <= 4 && kStagesP <= 16 && kStagesX <= 8, "barrier slots");
+  static_assert(kStagesA >= kDecGroups && kStagesP >= kDecGroups && kStagesX >= kDecGroups,
+                "a decoder group advances every ring by kDecGroups slots per step");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
   static_assert(CG == 1 || BT == 256, "CTA pairs are used with 256-token tiles");
 };
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::kStagesP; ++i) {
       mbar_init(bar_at(sh, kBarPFull + i), 1);
-      mbar_init(bar_at(sh, kBarPEmpty + i), kNumDecWarps / 2);
+      mbar_init(bar_at(sh, kBarPEmpty + i), 4);  // the four warps of the owning group
     }
     for (int i = 0; i < G::kStagesX; ++i) {
       mbar_init(bar_at(sh, kBarXFull + i), 1);
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < G::kStagesA; ++i) {
       // leader of a pair: its own decoders + one relayed arrival from the peer
-      mbar_init(bar_at(sh, kBarAFull + i), (kNumDecWarps / 2) + (CG == 2 && sh.rank == 0 ? 1 : 0));
+      mbar_init(bar_at(sh, kBarAFull + i), 4 + (CG == 2 && sh.rank == 0 ? 1 : 0));
       mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -453,27 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t col = it.col0 + row;
       const bool col_ok = col < a.ncols;
+      const int ntok = static_cast<int>(it.tok_end - it.tok0);  // tokens in this tile (<= BT)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
+      // Output pointers advance one token row per element: y / gx in bf16, or this
+      // split's fp32 partials.
+      __nv_bfloat16* op = a.out + it.tok0 * a.ld_out + col;
+      float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
       // 16 columns per load and wait (wider batches measured slower: register pressure).
       constexpr int kBatch = 16;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BT; c0 += kBatch) {
+      for (int c0 = 0; c0 < BT && c0 < ntok; c0 += kBatch) {
         uint32_t v[kBatch];
-#pragma unroll
-        for (int q = 0; q < kBatch / 16; ++q)
-          tmem_ld_32x32b_x16(taddr + c0 + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+        tmem_ld_32x32b_x16(taddr + c0, v);
         tmem_wait_ld();
         if (col_ok) {
+          const int nj = ntok - c0;  // valid tokens in this batch when fewer than kBatch
+          if (a.splits > 1) {
 #pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const int64_t tok = it.tok0 + c0 + j;
-            if (tok < it.tok_end) {
-              const float f = __uint_as_float(v[j]);
-              if (a.splits > 1)
-                a.ws[(static_cast<int64_t>(it.split) * a.M + tok) * a.ncols + col] = f;
-              else
-                a.out[tok * a.ld_out + col] = __float2bfloat16_rn(f);
-            }
+            for (int j = 0; j < kBatch; ++j)
+              if (j < nj) wp[static_cast<int64_t>(c0 + j) * a.ncols] = __uint_as_float(v[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+              if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
         }
       }
@@ -488,10 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ decoders --
-    // Two groups of four warps take alternate contraction steps; each thread turns
-    // one whole 64-value block (one scale) into bf16.
-    const int dw = warp - kWarpDec0;           // 0..7
-    const uint32_t grp = static_cast<uint32_t>(dw >> 2);
+    // kDecGroups groups of four warps: group g decodes the CTA's contraction steps
+    // j = g, g + kDecGroups, g + 2 kDecGroups, ... (j counts the steps of the CTA's
+    // items in order); each thread turns one whole 64-value block (one scale) into
+    // bf16.  The ring slots of step j are j mod (ring depth), kept incrementally.
+    const int dw = warp - kWarpDec0;
+    const int grp = dw >> 2;
     const int rb = ((dw & 3) << 5) | lane;     // row-block 0..127
     const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
     uint64_t code2[8];
@@ -518,85 +528,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       pk0 = nl * 64 + (((2 * j) ^ x) << 4);
       pk1 = nl * 64 + (((2 * j + 1) ^ x) << 4);
     }
-    // Contraction step -> (row, block) of this thread's scale.
-    auto block_of = [&](const Item& it, int ks, int64_t& n, int64_t& kb) {
-      if (MODE == 0) {
-        n = it.wrow0 + rb;
-        kb = ks;
-      } else {
-        n = it.wrow0 + static_cast<int64_t>(ks) * kTileK + (rb & 63);
-        kb = (it.col0 >> 6) + (rb >> 6);
-      }
-    };
-    uint32_t sp = 0, php = 0, sa = 0, pha = 0, sx = 0, phx = 0, step = 0;
-    bool ok = true;
-    // The statistics of this group's steps are fetched kAhead owned steps (2*kAhead
-    // contraction steps) ahead into a register ring, so their global-memory latency
-    // hides behind the decodes in between.
-    constexpr int kAhead = 4;
-    int64_t nidx = unit;
-    Item nit = nidx < total_items ? get_item<MODE, BT, CG>(nidx, a, sh) : Item{};
-    int nks = nit.ks0;
-    auto advance = [&]() {  // next (item, step) in this CTA's sequence
-      if (nidx < total_items && ++nks >= nit.ks1) {
-        nidx += nunits;
-        if (nidx < total_items) {
-          nit = get_item<MODE, BT, CG>(nidx, a, sh);
-          nks = nit.ks0;
+    // The statistics of this group's steps are fetched kAhead owned steps ahead
+    // into a register ring (global-memory latency hides behind the decodes in
+    // between).  A walker over (item, step) supplies them; q == kNoStep marks the
+    // end of the CTA's sequence.
+    constexpr uint32_t kNoStep = 0xffffffffu;
+    constexpr int kAhead = 2;
+    int64_t fidx = unit;
+    Item fit = fidx < total_items ? get_item<MODE, BT, CG>(fidx, a, sh) : Item{};
+    int fks = fit.ks0;
+    auto walk = [&](int n) {  // advance the walker n steps
+      fks += n;
+      while (fidx < total_items && fks >= fit.ks1) {
+        const int over = fks - fit.ks1;
+        fidx += nunits;
+        if (fidx < total_items) {
+          fit = get_item<MODE, BT, CG>(fidx, a, sh);
+          fks = fit.ks0 + over;
         }
       }
     };
     auto fetch_next = [&]() {
-      RawScale r{0.0f, 0u};
-      if (nidx < total_items) {
+      RawScale r{0.0f, kNoStep};
+      if (fidx < total_items) {
         int64_t n, kb;
-        block_of(nit, nks, n, kb);
+        if (MODE == 0) {
+          n = fit.wrow0 + rb;
+          kb = fks;
+        } else {
+          n = fit.wrow0 + static_cast<int64_t>(fks) * kTileK + (rb & 63);
+          kb = (fit.col0 >> 6) + (rb >> 6);
+        }
         r = fetch_scale(a, n, kb);
+        walk(kDecGroups);
       }
-      advance();
-      advance();
       return r;
     };
-    if (grp == 1) advance();  // this group owns the odd steps
+    walk(grp);
     RawScale ring[kAhead];
 #pragma unroll
     for (int i = 0; i < kAhead; ++i) ring[i] = fetch_next();
-    for (int64_t idx = unit; ok && idx < total_items; idx += nunits) {
-      const Item it = get_item<MODE, BT, CG>(idx, a, sh);
-      for (int ks = it.ks0; ks < it.ks1; ++ks, ++step) {
-        if ((step & 1u) == grp) {
-          const float s = finish_scale(a, sh.code8, ring[0], offset);
+    uint32_t sp = grp, php = 0, sa = grp, pha = 0, sx = grp, phx = 0;
+    while (ring[0].q != kNoStep) {
+      const float s = finish_scale(a, sh.code8, ring[0], offset);
 #pragma unroll
-          for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
-          ring[kAhead - 1] = fetch_next();
-          if (!wait_phase(bar_at(sh, kBarPFull + sp), php, sh, a)) { ok = false; break; }
-          const uint8_t* pk = smem + G::kOffPk + sp * kPkStage;
-          const uint4 w0 = *reinterpret_cast<const uint4*>(pk + pk0);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
-          const Lut L = make_lut(code2, s);
-          if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) { ok = false; break; }
-          // In a CTA pair this CTA's activation half must also have landed before
-          // the leader is told the stage is ready.
-          if (CG == 2 && !wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) { ok = false; break; }
-          uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
-          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
+      ring[kAhead - 1] = fetch_next();
+      if (!wait_phase(bar_at(sh, kBarPFull + sp), php, sh, a)) break;
+      const uint8_t* pk = smem + G::kOffPk + sp * kPkStage;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(pk + pk0);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
+      const Lut L = make_lut(code2, s);
+      if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) break;
+      // In a CTA pair this CTA's activation half must also have landed before
+      // the leader is told the stage is ready.
+      if (CG == 2 && !wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
+      uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
+      const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[c], L);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bar_at(sh, kBarPEmpty + sp));  // the codes were consumed above
-            mbar_arrive(bar_at(sh, kBarAFull + sa));
-          }
-        }
-        if (++sp == G::kStagesP) { sp = 0; php ^= 1u; }
-        if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
-        if (++sx == G::kStagesX) { sx = 0; phx ^= 1u; }
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[c], L);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar_at(sh, kBarPEmpty + sp));  // the codes were consumed above
+        mbar_arrive(bar_at(sh, kBarAFull + sa));
+      }
+      sp += kDecGroups;
+      if (sp >= static_cast<uint32_t>(G::kStagesP)) { sp -= G::kStagesP; php ^= 1u; }
+      sa += kDecGroups;
+      if (sa >= static_cast<uint32_t>(G::kStagesA)) { sa -= G::kStagesA; pha ^= 1u; }
+      if (CG == 2) {
+        sx += kDecGroups;
+        if (sx >= static_cast<uint32_t>(G::kStagesX)) { sx -= G::kStagesX; phx ^= 1u; }
       }
     }
   }
-
   tc_fence_before();
   __syncthreads();
   // A pair leaves together: the leader's MMAs (which write the peer's tensor memory)
