@@ -75,6 +75,9 @@ struct Geo {
   static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
   static_assert(kStagesX >= 3, "pipeline too shallow");
   static_assert(kStagesA <= 4 && kStagesP <= 16 && kStagesX <= 8, "barrier slots");
+  // A decoded slot waits on the "stage done" ring for the step kStagesA back; that
+  // ring slot must not be able to complete again first.
+  static_assert(kStagesX >= kStagesA, "stage-done ring shallower than the decoded ring");
   static_assert(kStagesA >= kDecGroups && kStagesP >= kDecGroups && kStagesX >= kDecGroups,
                 "a decoder group advances every ring by kDecGroups slots per step");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
@@ -120,6 +123,11 @@ __device__ __forceinline__ uint32_t bar_at(const Shared& sh, int i) { return sh.
 
 __device__ __forceinline__ void record_error(const GemmArgs& a, int code) {
   *reinterpret_cast<volatile int*>(a.status) = code;
+}
+
+// Barrier among `count` threads (a multiple of 32) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Programmatic dependent launch: wait for the preceding grid on the stream
@@ -307,9 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   grid_dependency_wait();
   allow_dependents();
-  if (threadIdx.x < 16) sh.code4[threadIdx.x] = a.code4[threadIdx.x];
-  if (a.dq)
-    for (int j = threadIdx.x; j < 256; j += kThreads) sh.code8[j] = a.code8[j];
+  // The codebooks are loaded by the decoders alone (below), so the producers start
+  // their first copies without waiting on those loads.
   if (a.grouped && threadIdx.x == kWarpEpi0 * 32) {
     // Per-expert token tiles and their prefix; offsets outside the contract are
     // reported and that expert is skipped.
@@ -405,10 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BT);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
+          // The decoders signal a stage only after its activation tile landed, so
+          // one wait per step covers both operands (every barrier operation of this
+          // thread is serialised with its MMA issue).
           if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a, CG == 2)) { ok = false; break; }
-          // A pair's decoders signal a stage only after their own activation half
-          // landed, so the leader waits on its decoded-tile barrier alone.
-          if (CG == 1 && !wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) { ok = false; break; }
           tc_fence_after();
           // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
           const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + sa * kAStage) >> 4);
@@ -425,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (CG == 2) {  // frees the stage in both CTAs
             mma_commit_pair(bar_at(sh, kBarAEmpty + sa), 0x3);
             mma_commit_pair(bar_at(sh, kBarXEmpty + sx), 0x3);
-          } else {
-            mma_commit(bar_at(sh, kBarAEmpty + sa));
+          } else {  // one "stage done" ring frees the activation and decoded slots
             mma_commit(bar_at(sh, kBarXEmpty + sx));
           }
           if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
@@ -507,8 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t code2[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      code2[i] = (static_cast<uint64_t>(__float_as_uint(sh.code4[2 * i + 1])) << 32) |
-                 __float_as_uint(sh.code4[2 * i]);
+      code2[i] = (static_cast<uint64_t>(__float_as_uint(__ldg(a.code4 + 2 * i + 1))) << 32) |
+                 __float_as_uint(__ldg(a.code4 + 2 * i));
+    // The 8-bit map of the block statistics goes to shared memory for the random
+    // lookups; the decoder warps alone synchronise on it (named barrier 1).
+    const int dtid = dw * 32 + lane;
+    if (a.dq && dtid < 256) sh.code8[dtid] = __ldg(a.code8 + dtid);
+    static_assert(kNumDecWarps * 32 >= 256, "one code8 entry per decoder thread");
     // Geometry of this thread's 128-byte line in the A tile and of its two 16-byte
     // chunks of packed codes.  The packed tile arrives with a TMA swizzle (32-byte
     // rows: 32B mode; 64-byte rows: 64B mode) so that a quarter-warp's chunk loads
@@ -568,7 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     RawScale ring[kAhead];
 #pragma unroll
     for (int i = 0; i < kAhead; ++i) ring[i] = fetch_next();
+    named_barrier_sync(1, kNumDecWarps * 32);  // code8 in shared memory
     uint32_t sp = grp, php = 0, sa = grp, pha = 0, sx = grp, phx = 0;
+    // Without pairs, decoded slot j mod kStagesA is free once the MMAs of step
+    // m = j - kStagesA are done, which the "stage done" ring (depth kStagesX)
+    // records in slot ms with phase parity mph.
+    int m = grp - G::kStagesA;
+    uint32_t ms = 0, mph = 0;
     while (ring[0].q != kNoStep) {
       const float s = finish_scale(a, sh.code8, ring[0], offset);
 #pragma unroll
@@ -579,10 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint4 w0 = *reinterpret_cast<const uint4*>(pk + pk0);
       const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
       const Lut L = make_lut(code2, s);
-      if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) break;
-      // In a CTA pair this CTA's activation half must also have landed before
-      // the leader is told the stage is ready.
-      if (CG == 2 && !wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
+      if (CG == 2) {
+        if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) break;
+      } else if (m >= 0) {
+        if (!wait_phase(bar_at(sh, kBarXEmpty + ms), mph, sh, a)) break;
+      }
+      // The stage's activation tile (this CTA's half in a pair) must have landed
+      // before the MMA issuer is told the stage is ready.
+      if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
       uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
       const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
@@ -598,9 +619,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sp >= static_cast<uint32_t>(G::kStagesP)) { sp -= G::kStagesP; php ^= 1u; }
       sa += kDecGroups;
       if (sa >= static_cast<uint32_t>(G::kStagesA)) { sa -= G::kStagesA; pha ^= 1u; }
-      if (CG == 2) {
-        sx += kDecGroups;
-        if (sx >= static_cast<uint32_t>(G::kStagesX)) { sx -= G::kStagesX; phx ^= 1u; }
+      sx += kDecGroups;
+      if (sx >= static_cast<uint32_t>(G::kStagesX)) { sx -= G::kStagesX; phx ^= 1u; }
+      m += kDecGroups;
+      if (m >= kDecGroups) {
+        ms += kDecGroups;
+        if (ms >= static_cast<uint32_t>(G::kStagesX)) { ms -= G::kStagesX; mph ^= 1u; }
+      } else if (m >= 0) {  // first step with a predecessor in this slot (m < kDecGroups <= kStagesX)
+        ms = static_cast<uint32_t>(m);
+        mph = 0;
       }
     }
   }
