@@ -25,7 +25,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD = range(5)
 PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
          "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad", "skinny_fwd",
-         "skinny_dgrad"]
+         "skinny_dgrad", "stream_k"]
 
 
 class NF4Error(RuntimeError):
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "nf4_set_cta_pairs": [I32],
             "nf4_set_weight_prefetch": [I32],
             "nf4_set_small_m_path": [I32],
+            "nf4_set_stream_k": [I32],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -106,6 +107,7 @@ def lib() -> ctypes.CDLL:
         L.nf4_set_cta_pairs.restype = None
         L.nf4_set_weight_prefetch.restype = None
         L.nf4_set_small_m_path.restype = None
+        L.nf4_set_stream_k.restype = None
         _lib = L
         return _lib
 
@@ -142,6 +144,13 @@ SMALL_M_AUTO, SMALL_M_SIMT, SMALL_M_TILES = 0, 1, 2
 
 def set_small_m_path(path: int):
     lib().nf4_set_small_m_path(int(path))
+
+
+STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_FORCE = 0, 1, 2
+
+
+def set_stream_k(mode: int):
+    lib().nf4_set_stream_k(int(mode))
 
 
 def set_weight_prefetch(enabled: bool):

@@ -95,8 +95,10 @@ class NF4Linear(torch.nn.Module):
         self.w = w
 
     @classmethod
-    def from_float(cls, weight: torch.Tensor, double_quant: bool = True) -> "NF4Linear":
-        return cls(ops.quantize(weight.detach().contiguous(), double_quant=double_quant))
+    def from_float(cls, weight: torch.Tensor, double_quant: bool = True,
+                   quant_type: str = "nf4") -> "NF4Linear":
+        return cls(ops.quantize(weight.detach().contiguous(), double_quant=double_quant,
+                                quant_type=quant_type))
 
     def forward(self, x):
         return nf4_linear(x, self.w)

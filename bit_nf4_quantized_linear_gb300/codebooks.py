@@ -9,6 +9,12 @@ delta = (1/30 + 1/32) / 2.  The pages name the type ("nf4", bitsandbytes issue
 "MatMul4Bit keeps B and quant_state on ctx", "Minimal reproducer") without
 printing it.
 
+``fp4_code4``: the "fp4" quant_type that the pages list beside nf4 for the same
+packed 4-bit path (fork PR "Experts trainability", commit 1, quant_type table),
+read as the E2M1 4-bit float (sign, 2-bit exponent with bias 1, 1-bit mantissa,
+subnormals at exponent 0) scaled by 1/6 so its extremes are +-1, in ascending
+order with -0 before +0.
+
 ``dynamic_code8``: the signed 8-bit dynamic tree map (Dettmers et al. 2022,
 "8-bit Optimizers via Block-wise Quantization") for the nested absmax codes:
 decimal exponent groups 10**(e-6), e = 0..6, holding 2**e linear fraction values
@@ -29,6 +35,29 @@ def nf4_code4() -> torch.Tensor:
                         torch.zeros(1, dtype=torch.float64)])
     levels, _ = torch.sort(levels)
     return (levels / levels.max()).to(torch.float32)
+
+
+def fp4_code4() -> torch.Tensor:
+    bits = torch.arange(16, dtype=torch.int64)
+    sign = torch.where(bits >= 8, -1.0, 1.0).to(torch.float64)
+    exp = (bits >> 1) & 3
+    man = (bits & 1).to(torch.float64)
+    mag = torch.where(exp == 0, man * 0.5,
+                      (1.0 + man * 0.5) * torch.pow(2.0, (exp - 1).to(torch.float64)))
+    vals = sign * mag / 6.0
+    # The magnitude grows with the low three bits, so ascending order (-0 before
+    # +0) is codes 15 down to 8, then 0 up to 7.
+    order = torch.cat([torch.arange(15, 7, -1), torch.arange(0, 8)])
+    return vals[order].to(torch.float32)
+
+
+def code4_for(quant_type: str) -> torch.Tensor:
+    """The 16-entry codebook of a 4-bit quant_type ("nf4" or "fp4")."""
+    if quant_type == "nf4":
+        return nf4_code4()
+    if quant_type == "fp4":
+        return fp4_code4()
+    raise ValueError(f"unknown 4-bit quant_type {quant_type!r} (expected 'nf4' or 'fp4')")
 
 
 def dynamic_code8() -> torch.Tensor:

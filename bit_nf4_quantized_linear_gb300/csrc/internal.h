@@ -49,7 +49,25 @@ struct GemmArgs {
   int64_t ld_out;
   float* ws;  // split-K partials [splits][M][ncols]
   int* status;
+  int tma_out;  // dense bf16 output written by bulk tensor stores (aligned out and ld_out)
+  // Stream-K schedule (dense, no pairs, splits == 1): the items * ksteps
+  // contraction steps are cut into sk_ctas equal contiguous runs, one per CTA.  A
+  // tile cut between CTAs is finished by the CTA holding its first steps, which
+  // adds the later runs' fp32 partials in CTA order.
+  int sk;
+  int64_t sk_units;     // items * ksteps
+  int sk_ctas;          // CTAs (= grid)
+  float* sk_ws;         // partial tiles [sk_ctas][4 row quarters][bt tokens][32 rows] fp32
+  uint32_t* sk_flags;   // [sk_ctas][4]: partial of (CTA, row quarter) published
+  uint32_t sk_epoch;    // value this launch publishes (never 0)
 };
+
+// Stream-K bookkeeping: ready flags live in a device array of kSkSlots launch
+// slots of kSkMaxCtas * 4 words (slot = epoch % kSkSlots), so that flags need no
+// clearing and launches in flight on other streams use other slots.
+constexpr int kSkSlots = 64;
+constexpr int kSkMaxCtas = 256;
+uint32_t* stream_k_flags(uint32_t epoch);  // device address of the epoch's slot
 
 // Parameters of the small-M GEMV kernels.
 struct GemvArgs {
@@ -122,8 +140,10 @@ cudaError_t launch_gemv_dgrad(const GemvArgs& a, cudaStream_t s);
 int gemv_fwd_kseg(int64_t K);
 int64_t gemv_dgrad_row_groups(int64_t N);
 // cg = 2 launches CTA pairs (clusters of two, tcgen05 cta_group::2; bt must be 256).
+// tmap_out: bf16 output [M, ncols] with a 32 x 32 box, used when a.tma_out is set.
 cudaError_t launch_gemm(int mode, int bt, int cg, const GemmArgs& a, const CUtensorMap& tmap_act,
-                        const CUtensorMap& tmap_packed, int grid, cudaStream_t s);
+                        const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
+                        cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  __nv_bfloat16* out, int64_t ld, cudaStream_t s);
 

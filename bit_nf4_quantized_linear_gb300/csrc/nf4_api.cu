@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <cstdlib>
 #include <mutex>
 
@@ -150,6 +151,8 @@ struct Plan {
   bool gemv = false;  // small M: SIMT GEMV kernels
   bool skinny = false;  // small M: tensor-core (mma.sync) kernels
   nf4::SkinnyPlan sk;
+  bool stream_k = false;  // fused kernel with the stream-K schedule
+  int sk_ctas = 0;
 };
 
 Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits, int cg = 1) {
@@ -177,6 +180,18 @@ std::atomic<int> g_weight_prefetch{0};
 // Kernels for M <= 16 (nf4_set_small_m_path).
 std::atomic<int> g_small_m_path{NF4_SMALL_M_AUTO};
 
+// Stream-K schedule of the fused kernel (nf4_set_stream_k).
+std::atomic<int> g_stream_k{NF4_STREAM_K_AUTO};
+
+// Epoch a stream-K launch publishes in its ready flags: unique per launch, never 0.
+std::atomic<uint32_t> g_sk_epoch{0};
+
+uint32_t next_sk_epoch() {
+  uint32_t e = g_sk_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  while (e == 0) e = g_sk_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
+
 bool cta_pairs_enabled() {
   int v = g_cta_pairs.load(std::memory_order_relaxed);
   if (v < 0) {
@@ -192,9 +207,8 @@ bool cta_pairs_enabled() {
 // tiles written by TMA and the decoders, read by the MMAs) for wide ones; a CTA
 // pair halves each SM's share of the activation tile.
 double step_cycles(int bt, int cg) {
-  if (bt >= 256) return cg == 2 ? 560.0 : 810.0;
-  if (bt >= 128) return 560.0;
-  return 480.0;
+  if (bt >= 256) return cg == 2 ? 1600.0 : 950.0;
+  return 830.0;
 }
 
 // Tile plan of a dense product: a deterministic function of the shape and the SM
@@ -203,7 +217,7 @@ double step_cycles(int bt, int cg) {
 // the packed weight.  Larger M: token tile, CTA pairing and split chosen by a cost
 // model in SM clocks -- waves of items times contraction steps, plus the split
 // partials' round trip through memory.
-Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
+Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
   const int small = g_small_m_path.load(std::memory_order_relaxed);
@@ -244,8 +258,10 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
   const int cand_bt[4] = {256, 256, 128, 64};
   const int cand_cg[4] = {2, 1, 1, 1};
   const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
-  double best_t = 1e300;
+  const int skm = allow_sk ? g_stream_k.load(std::memory_order_relaxed) : NF4_STREAM_K_OFF;
+  double best_t = 1e300, sk_t = 1e300;
   Plan best = make_plan(M, ncols, contract, bt_max, 1);
+  Plan sk_best = best;
   for (int ci = 0; ci < 4; ++ci) {
     const int bt = cand_bt[ci], cg = cand_cg[ci];
     if (bt > bt_max || (cg == 2 && !cta_pairs_enabled())) continue;
@@ -265,12 +281,31 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms) {
         best = make_plan(M, ncols, contract, bt, S, cg);
       }
     }
+    if (cg == 1 && skm != NF4_STREAM_K_OFF && sms <= nf4::kSkMaxCtas) {
+      // Stream-K: equal runs of the items' contraction steps, one per CTA (each at
+      // least one step), plus the split tiles' partials through L2: the CTA
+      // finishing a split tile waits about one L2 round trip per 16-token batch
+      // (measured on GB300: about 25000 cycles of fixed cost at 256-token tiles).
+      const int64_t U = wt * ttiles * ksteps;
+      const int64_t G = U < sms ? U : sms;
+      const double t = static_cast<double>((U + G - 1) / G) * step_cycles(bt, 1) + 5000.0 +
+                       20000.0 * bt / 256.0;
+      if (G >= 1 && t < sk_t * 0.999) {
+        sk_t = t;
+        sk_best = make_plan(M, ncols, contract, bt, 1, 1);
+        sk_best.stream_k = true;
+        sk_best.sk_ctas = static_cast<int>(G);
+        sk_best.ws_bytes = static_cast<size_t>(G) * nf4::kTileW * bt * sizeof(float);
+      }
+    }
   }
+  if (sk_best.stream_k && (skm == NF4_STREAM_K_FORCE || sk_t < best_t * 0.97)) return sk_best;
   return best;
 }
 
 nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const nf4_weight* w,
-                     void* out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream) {
+                     void* out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream,
+                     bool allow_sk = true) {
   nf4_status st = check_weight(w);
   if (st != NF4_OK) return st;
   const int64_t N = w->N, K = w->K;
@@ -286,7 +321,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   DevInfo dev;
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
-  const Plan p = plan_dense(mode, M, N, K, dev.sms);
+  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -393,10 +428,32 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.ws = static_cast<float*>(ws);
   a.status = dev.status;
   const int64_t units = dev.sms / p.cg;
-  const int grid = static_cast<int>((p.items < units ? p.items : units) * p.cg);
-  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, a, tmap_act, tmap_pk, grid, s);
+  int grid = static_cast<int>((p.items < units ? p.items : units) * p.cg);
+  if (p.stream_k) {
+    a.sk = 1;
+    a.sk_units = p.items * p.ksteps;
+    a.sk_ctas = p.sk_ctas;
+    a.sk_ws = static_cast<float*>(ws);
+    a.sk_epoch = next_sk_epoch();
+    a.sk_flags = nf4::stream_k_flags(a.sk_epoch);
+    if (!a.sk_flags) return cuda_fail(cudaGetLastError(), "stream-K flags");
+    grid = p.sk_ctas;
+  }
+  // The bf16 output goes out through bulk tensor stores when its base and row pitch
+  // meet the 16-byte rule; otherwise through direct stores.
+  CUtensorMap tmap_out;
+  std::memset(&tmap_out, 0, sizeof(tmap_out));
+  if (p.splits == 1 && aligned16(out) && ld_out % 8 == 0) {
+    if (!encode_2d(&tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, out_cols, M, ld_out * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+    a.tma_out = 1;
+  }
+  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, a, tmap_act, tmap_pk, tmap_out, grid, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
+  if (p.stream_k)  // a property of the launch just counted, not a launch of its own
+    g_counters[NF4_PATH_STREAM_K].fetch_add(1, std::memory_order_relaxed);
   if (p.splits > 1) {
     le = nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols,
                                    static_cast<__nv_bfloat16*>(out), ld_out, s);
@@ -467,7 +524,10 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   a.ws = nullptr;
   a.status = dev.status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t le = nf4::launch_gemm(mode, bt, 1, a, tmap_act, tmap_pk, dev.sms, s);
+  CUtensorMap tmap_out;  // unused: expert row ranges end inside tiles (direct stores)
+  std::memset(&tmap_out, 0, sizeof(tmap_out));
+  a.tma_out = 0;
+  cudaError_t le = nf4::launch_gemm(mode, bt, 1, a, tmap_act, tmap_pk, tmap_out, dev.sms, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
   return NF4_OK;
@@ -605,6 +665,11 @@ void nf4_set_small_m_path(int32_t path) {
     g_small_m_path.store(path, std::memory_order_relaxed);
 }
 
+void nf4_set_stream_k(int32_t mode) {
+  if (mode >= NF4_STREAM_K_OFF && mode <= NF4_STREAM_K_FORCE)
+    g_stream_k.store(mode, std::memory_order_relaxed);
+}
+
 void nf4_set_weight_prefetch(int32_t enabled) {
   g_weight_prefetch.store(enabled ? 1 : 0, std::memory_order_relaxed);
 }
@@ -667,13 +732,14 @@ extern "C" nf4_status nf4_linear_fwd_noalloc(const void* x, int64_t M, int64_t l
   DevInfo dev;
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
-  // Shapes whose partials would not fit the fixed array are rejected up front.
-  if (plan_dense(0, M, w->N, w->K, dev.sms).ws_bytes > NF4_NOALLOC_SCRATCH_BYTES)
+  // The stream-K schedule is not used here (its partial tiles outgrow the array);
+  // shapes whose split partials would not fit are rejected up front.
+  if (plan_dense(0, M, w->N, w->K, dev.sms, false).ws_bytes > NF4_NOALLOC_SCRATCH_BYTES)
     return NF4_ERR_WORKSPACE;
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != NF4_OK) return st;
   // Every partial the kernel later reads is written first in the same call, so
   // what a previous call left in the array is never read and needs no clearing.
-  return run_dense(0, x, M, ldx, w, y, ldy, scratch, NF4_NOALLOC_SCRATCH_BYTES, stream);
+  return run_dense(0, x, M, ldx, w, y, ldy, scratch, NF4_NOALLOC_SCRATCH_BYTES, stream, false);
 }

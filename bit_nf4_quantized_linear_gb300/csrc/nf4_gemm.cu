@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -54,6 +55,8 @@ constexpr int kThreads = (kWarpTmaX + 1) * 32;
 constexpr int kAStage = kTileW * kTileK * 2;  // 16 KB of bf16
 constexpr int kPkStage = kTileW * kTileK / 2;  // 4 KB of packed codes
 constexpr int kMiscBytes = 8192;
+constexpr int kOutWarpBytes = 32 * 32 * 2;        // epilogue staging: 32 tokens x 32 bf16 per warp
+constexpr int kOutBytes = 4 * kOutWarpBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bound of every wait (2 s)
 constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up to 20 us per try
 
@@ -65,12 +68,14 @@ struct Geo {
   // tiles leave room, so a group never waits on the MMAs of the step just before.
   static constexpr int kStagesA = BT >= 256 ? kDecGroups : kDecGroups + 1;
   static constexpr int kStagesP = BT <= 64 ? 16 : 8; // packed-code tiles (prefetched far ahead)
-  static constexpr int kStagesX0 = (kBudget - kStagesA * kAStage - kStagesP * kPkStage) / kXStage;
+  static constexpr int kStagesX0 =
+      (kBudget - kStagesA * kAStage - kStagesP * kPkStage - kOutBytes) / kXStage;
   static constexpr int kStagesX = kStagesX0 > 8 ? 8 : kStagesX0;  // activation tiles
   static constexpr int kOffA = 0;
   static constexpr int kOffX = kOffA + kStagesA * kAStage;
   static constexpr int kOffPk = kOffX + kStagesX * kXStage;
-  static constexpr int kOffMisc = kOffPk + kStagesP * kPkStage;
+  static constexpr int kOffOut = kOffPk + kStagesP * kPkStage;  // output staging
+  static constexpr int kOffMisc = kOffOut + kOutBytes;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;
   static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
   static_assert(kStagesX >= 3, "pipeline too shallow");
@@ -100,10 +105,11 @@ constexpr int kBarDrain = 60;
 constexpr int kNumBars = 61;
 
 struct Item {
+  int64_t idx;    // item (tile) index
   int64_t tok0, tok_end;
   int64_t wrow0;  // forward: first weight row of the tile; input gradient: first row of the expert
   int64_t col0;   // first output column of the tile
-  int ks0, ks1;
+  int ks0, ks1;   // contraction steps of this segment of the item
   int split;
 };
 
@@ -180,10 +186,39 @@ __device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, const Ge
   }
 }
 
+// Stream-K partial-tile flags: publish with release semantics after the partial's
+// stores; wait (bounded) with acquire semantics before reading it.
+__device__ __forceinline__ void flag_publish(uint32_t* f, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t flag_read(const uint32_t* f) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+
+__device__ __noinline__ bool flag_wait(const uint32_t* f, uint32_t v, const Shared& sh,
+                                       const GemmArgs& a) {
+  if (flag_read(f) == v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (flag_read(f) == v) return true;
+    if (*sh.abort_flag) return false;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      *sh.abort_flag = 1;
+      record_error(a, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 template <int MODE, int BT, int CG>
 __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const Shared& sh) {
   constexpr int kW = kTileW * CG;  // weight rows / in-features per (pair) tile
   Item it;
+  it.idx = idx;
   if (!a.grouped) {
     const int64_t s = idx % a.splits;
     const int64_t r = idx / a.splits;
@@ -218,6 +253,44 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
   return it;
 }
 
+// The CTA's sequence of item segments.  Classic: whole items unit, unit + nunits,
+// ... (their contraction split fixed by the plan).  Stream-K: the contiguous run
+// of contraction steps [unit * U / G, (unit + 1) * U / G) over items in order,
+// cut at item boundaries.  Every role of the CTA walks the same sequence.
+struct Cursor {
+  int64_t pos, end;
+};
+
+__device__ __forceinline__ int64_t sk_first_unit(const GemmArgs& a, int64_t cta) {
+  return cta * a.sk_units / a.sk_ctas;
+}
+
+__device__ __forceinline__ Cursor cursor_begin(const GemmArgs& a, int64_t unit,
+                                               int64_t total_items) {
+  if (a.sk) return Cursor{sk_first_unit(a, unit), sk_first_unit(a, unit + 1)};
+  return Cursor{unit, total_items};
+}
+
+template <int MODE, int BT, int CG>
+__device__ __forceinline__ bool cursor_next(Cursor& c, const GemmArgs& a, const Shared& sh,
+                                            int64_t nunits, Item& it) {
+  if (c.pos >= c.end) return false;
+  if (!a.sk) {
+    it = get_item<MODE, BT, CG>(c.pos, a, sh);
+    c.pos += nunits;
+    return true;
+  }
+  const int64_t idx = c.pos / a.ksteps;
+  const int ks0 = static_cast<int>(c.pos - idx * a.ksteps);
+  const int64_t left = c.end - c.pos;
+  const int ks1 = left < a.ksteps - ks0 ? ks0 + static_cast<int>(left) : a.ksteps;
+  it = get_item<MODE, BT, CG>(idx, a, sh);
+  it.ks0 = ks0;
+  it.ks1 = ks1;
+  c.pos += ks1 - ks0;
+  return true;
+}
+
 // Raw statistics of one block, fetched ahead of use: the fp32 absmax, or the
 // 8-bit code and its nested absmax.  Out-of-range blocks read as scale 0.
 struct RawScale {
@@ -248,7 +321,8 @@ __device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* co
 template <int MODE, int BT, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
-                    const __grid_constant__ CUtensorMap tmap_pk, const GemmArgs a) {
+                    const __grid_constant__ CUtensorMap tmap_pk,
+                    const __grid_constant__ CUtensorMap tmap_out, const GemmArgs a) {
   using G = Geo<BT, CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -354,8 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = is_pk ? kPkStage : G::kXStage;
       uint32_t st = 0, ph = 0, issued = 0, par = 0;
       bool ok = true;
-      for (int64_t idx = unit; ok && idx < total_items; idx += nunits) {
-        const Item it = get_item<MODE, BT, CG>(idx, a, sh);
+      Cursor cur = cursor_begin(a, unit, total_items);
+      Item it;
+      while (ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it)) {
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           if (!wait_phase(bar_at(sh, bar_empty + st), ph ^ 1u, sh, a)) { ok = false; break; }
           const uint32_t full = bar_at(sh, bar_full + st);
@@ -387,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // locally.
       uint32_t sa = 0, pha = 0;
       bool ok = true;
-      for (int64_t idx = unit; ok && idx < total_items; idx += nunits) {
-        const Item it = get_item<MODE, BT, CG>(idx, a, sh);
+      Cursor cur = cursor_begin(a, unit, total_items);
+      Item it;
+      while (ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it)) {
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
           mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAFull + sa), 0));
@@ -404,8 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sx = 0, phx = 0, sa = 0, pha = 0;
       int acc_i = 0;
       bool ok = true;
-      for (int64_t idx = unit; ok && idx < total_items; idx += nunits, ++acc_i) {
-        const Item it = get_item<MODE, BT, CG>(idx, a, sh);
+      Cursor cur = cursor_begin(a, unit, total_items);
+      Item it;
+      for (; ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it); ++acc_i) {
         const int ab = acc_i & 1;
         const uint32_t acc_ph = (acc_i >> 1) & 1;
         if (!wait_phase(bar_at(sh, kBarAccEmpty + ab), acc_ph ^ 1u, sh, a, CG == 2)) break;
@@ -457,8 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = 32 * q + lane;
     int acc_i = 0;
-    for (int64_t idx = unit; idx < total_items; idx += nunits, ++acc_i) {
-      const Item it = get_item<MODE, BT, CG>(idx, a, sh);
+    Cursor cur = cursor_begin(a, unit, total_items);
+    Item it;
+    for (; cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it); ++acc_i) {
       const int ab = acc_i & 1;
       const uint32_t acc_ph = (acc_i >> 1) & 1;
       if (!wait_phase(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)) break;
@@ -466,30 +544,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t col = it.col0 + row;
       const bool col_ok = col < a.ncols;
       const int ntok = static_cast<int>(it.tok_end - it.tok0);  // tokens in this tile (<= BT)
+      // Stream-K: a segment after the tile's first steps publishes its fp32 partial
+      // (this warp's quarter of the rows, lane-contiguous per token) in this CTA's
+      // slot; the segment holding the first steps of a tile cut between CTAs adds
+      // the partials of the following CTAs, in CTA order, before rounding.
+      const bool sk_part = a.sk && it.ks0 > 0;
+      const bool sk_own = a.sk && it.ks0 == 0 && it.ks1 < a.ksteps;
+      int64_t own_last = unit;  // last CTA holding steps of an owned split tile
+      if (sk_own) {
+        const int64_t tile_end = (it.idx + 1) * a.ksteps;
+        while (own_last + 1 < a.sk_ctas && sk_first_unit(a, own_last + 1) < tile_end) ++own_last;
+        for (int64_t c = unit + 1; c <= own_last; ++c)
+          if (!flag_wait(a.sk_flags + c * 4 + q, a.sk_epoch, sh, a)) break;
+      }
+      auto sk_slot = [&](int64_t c) {  // partial of CTA c, this quarter, token 0, this lane
+        return a.sk_ws + ((c * 4 + q) * BT) * 32 + lane;
+      };
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
-      // Output pointers advance one token row per element: y / gx in bf16, or this
-      // split's fp32 partials.
-      __nv_bfloat16* op = a.out + it.tok0 * a.ld_out + col;
-      float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
-      // 16 columns per load and wait (wider batches measured slower: register pressure).
+      // One 16-token batch: tensor-memory load, plus the following CTAs' partials.
       constexpr int kBatch = 16;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BT && c0 < ntok; c0 += kBatch) {
-        uint32_t v[kBatch];
+      auto load_batch = [&](int c0, uint32_t (&v)[kBatch]) {
         tmem_ld_32x32b_x16(taddr + c0, v);
         tmem_wait_ld();
-        if (col_ok) {
-          const int nj = ntok - c0;  // valid tokens in this batch when fewer than kBatch
-          if (a.splits > 1) {
+        if (sk_own)
+          for (int64_t c = unit + 1; c <= own_last; ++c) {
+            const float* src = sk_slot(c) + c0 * 32;
 #pragma unroll
             for (int j = 0; j < kBatch; ++j)
-              if (j < nj) wp[static_cast<int64_t>(c0 + j) * a.ncols] = __uint_as_float(v[j]);
-          } else {
+              v[j] = __float_as_uint(__fadd_rn(__uint_as_float(v[j]), src[j * 32]));
+          }
+      };
+      if (sk_part) {
+        float* dst = sk_slot(unit);
+#pragma unroll 1
+        for (int c0 = 0; c0 < ntok; c0 += kBatch) {
+          uint32_t v[kBatch];
+          tmem_ld_32x32b_x16(taddr + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j)
+            if (c0 + j < ntok) dst[(c0 + j) * 32] = __uint_as_float(v[j]);
+        }
+        __threadfence();  // every lane's partial stores, then the quarter's flag
+        __syncwarp();
+        if (lane == 0) flag_publish(a.sk_flags + unit * 4 + q, a.sk_epoch);
+      } else if (a.tma_out && a.splits == 1) {
+        // bf16 tile through shared memory: per 32-token chunk this warp writes its
+        // 32 columns x 32 tokens and one lane stores them with a bulk tensor copy
+        // (rows past M and columns past the output width are not written).
+        uint16_t* stg = reinterpret_cast<uint16_t*>(smem + G::kOffOut + q * kOutWarpBytes);
+        const uint32_t stg_addr = sbase + G::kOffOut + q * kOutWarpBytes;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ntok; c0 += 32) {
+          if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
+          __syncwarp();
+#pragma unroll 1
+          for (int h = 0; h < 32 && c0 + h < ntok; h += kBatch) {
+            uint32_t v[kBatch];
+            load_batch(c0 + h, v);
 #pragma unroll
             for (int j = 0; j < kBatch; ++j)
-              if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = __float2bfloat16_rn(__uint_as_float(v[j]));
+              stg[(h + j) * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_out, stg_addr, static_cast<int32_t>(it.col0 + 32 * q),
+                         static_cast<int32_t>(it.tok0 + c0));
+            bulk_commit_group();
           }
         }
+      } else {
+        // Direct stores, one token row per element: y / gx in bf16, or this split's
+        // fp32 partials.
+        __nv_bfloat16* op = a.out + it.tok0 * a.ld_out + col;
+        float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ntok; c0 += kBatch) {
+          uint32_t v[kBatch];
+          load_batch(c0, v);
+          if (col_ok) {
+            const int nj = ntok - c0;  // valid tokens in this batch when fewer than kBatch
+            if (a.splits > 1) {
+#pragma unroll
+              for (int j = 0; j < kBatch; ++j)
+                if (j < nj) wp[static_cast<int64_t>(c0 + j) * a.ncols] = __uint_as_float(v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kBatch; ++j)
+                if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            }
+          }
+        }
+      }
+      if (sk_own) {  // the partials are consumed: clear their flags for the next launch
+        __syncwarp();
+        if (lane == 0)
+          for (int64_t c = unit + 1; c <= own_last; ++c) a.sk_flags[c * 4 + q] = 0u;
       }
       tc_fence_before();
       __syncwarp();
@@ -500,6 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
       }
     }
+    if (lane == 0) bulk_wait_all();  // output tiles written before the CTA exits
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ decoders --
     // kDecGroups groups of four warps: group g decodes the CTA's contraction steps
@@ -545,23 +698,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // end of the CTA's sequence.
     constexpr uint32_t kNoStep = 0xffffffffu;
     constexpr int kAhead = 2;
-    int64_t fidx = unit;
-    Item fit = fidx < total_items ? get_item<MODE, BT, CG>(fidx, a, sh) : Item{};
+    Cursor fcur = cursor_begin(a, unit, total_items);
+    Item fit{};
+    bool fvalid = cursor_next<MODE, BT, CG>(fcur, a, sh, nunits, fit);
     int fks = fit.ks0;
     auto walk = [&](int n) {  // advance the walker n steps
       fks += n;
-      while (fidx < total_items && fks >= fit.ks1) {
+      while (fvalid && fks >= fit.ks1) {
         const int over = fks - fit.ks1;
-        fidx += nunits;
-        if (fidx < total_items) {
-          fit = get_item<MODE, BT, CG>(fidx, a, sh);
-          fks = fit.ks0 + over;
-        }
+        fvalid = cursor_next<MODE, BT, CG>(fcur, a, sh, nunits, fit);
+        if (fvalid) fks = fit.ks0 + over;
       }
     };
     auto fetch_next = [&]() {
       RawScale r{0.0f, kNoStep};
-      if (fidx < total_items) {
+      if (fvalid) {
         int64_t n, kb;
         if (MODE == 0) {
           n = fit.wrow0 + rb;
@@ -716,7 +867,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 }
 
 template <int MODE, int BT, int CG>
-cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp, int grid,
+cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
+                       const CUtensorMap& to, int grid,
                        cudaStream_t s) {
   static bool configured = false;
   auto kern = nf4_gemm_kernel<MODE, BT, CG>;
@@ -740,32 +892,51 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CG == 2 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tp, a);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tp, to, a);
 }
 
 template <int MODE>
 cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta,
-                        const CUtensorMap& tp, int grid, cudaStream_t s) {
+                        const CUtensorMap& tp, const CUtensorMap& to, int grid, cudaStream_t s) {
   if (cg == 2) {
     if (bt != 256) return cudaErrorInvalidValue;
-    return launch_one<MODE, 256, 2>(a, ta, tp, grid, s);
+    return launch_one<MODE, 256, 2>(a, ta, tp, to, grid, s);
   }
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1>(a, ta, tp, grid, s);
-    case 32: return launch_one<MODE, 32, 1>(a, ta, tp, grid, s);
-    case 64: return launch_one<MODE, 64, 1>(a, ta, tp, grid, s);
-    case 128: return launch_one<MODE, 128, 1>(a, ta, tp, grid, s);
-    case 256: return launch_one<MODE, 256, 1>(a, ta, tp, grid, s);
+    case 16: return launch_one<MODE, 16, 1>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 1>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 1>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 1>(a, ta, tp, to, grid, s);
+    case 256: return launch_one<MODE, 256, 1>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
+// Stream-K ready flags (zero at module load; a launch publishes its epoch).
+__device__ uint32_t g_stream_k_flags[kSkSlots * kSkMaxCtas * 4];
+
+uint32_t* stream_k_flags(uint32_t epoch) {
+  constexpr int kDevices = 64;
+  static std::atomic<uint32_t*> cache[kDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return nullptr;
+  uint32_t* base = cache[dev].load(std::memory_order_acquire);
+  if (!base) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_stream_k_flags) != cudaSuccess) return nullptr;
+    base = static_cast<uint32_t*>(p);
+    cache[dev].store(base, std::memory_order_release);
+  }
+  return base + static_cast<size_t>(epoch % kSkSlots) * kSkMaxCtas * 4;
+}
+
 cudaError_t launch_gemm(int mode, int bt, int cg, const GemmArgs& a, const CUtensorMap& tmap_act,
-                        const CUtensorMap& tmap_packed, int grid, cudaStream_t s) {
-  if (mode == 0) return launch_mode<0>(bt, cg, a, tmap_act, tmap_packed, grid, s);
-  return launch_mode<1>(bt, cg, a, tmap_act, tmap_packed, grid, s);
+                        const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
+                        cudaStream_t s) {
+  if (mode == 0) return launch_mode<0>(bt, cg, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  return launch_mode<1>(bt, cg, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,

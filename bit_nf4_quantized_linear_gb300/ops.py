@@ -81,8 +81,9 @@ def workspace_size(op: int, M: int, N: int, K: int, E: int = 0) -> int:
 
 
 def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.Tensor] = None,
-             code8: Optional[torch.Tensor] = None) -> NF4Weight:
-    """nf4_quantize: blockwise NF4 (+ double quantisation) of a CUDA fp32/bf16 [N, K]."""
+             code8: Optional[torch.Tensor] = None, quant_type: str = "nf4") -> NF4Weight:
+    """nf4_quantize: blockwise 4-bit (+ double quantisation) of a CUDA fp32/bf16 [N, K].
+    `quant_type` ("nf4" or "fp4") picks the default codebook when `code4` is None."""
     _need_cuda("quantize", W)
     if W.dim() != 2 or not W.is_contiguous():
         raise ValueError("quantize: W must be a contiguous [N, K] tensor")
@@ -92,7 +93,7 @@ def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.T
     N, K = W.shape
     numel = N * K
     nblocks = (numel + BLOCKSIZE - 1) // BLOCKSIZE
-    code4 = (codebooks.nf4_code4() if code4 is None else code4).to(dev, torch.float32).contiguous()
+    code4 = (codebooks.code4_for(quant_type) if code4 is None else code4).to(dev, torch.float32).contiguous()
     code8 = (codebooks.dynamic_code8() if code8 is None else code8).to(dev, torch.float32).contiguous()
     packed = torch.empty((numel + 1) // 2, dtype=torch.uint8, device=dev)
     absmax = torch.empty(nblocks, dtype=torch.float32, device=dev)
@@ -211,3 +212,4 @@ device_check = _lib.device_check
 set_cta_pairs = _lib.set_cta_pairs
 set_weight_prefetch = _lib.set_weight_prefetch
 set_small_m_path = _lib.set_small_m_path
+set_stream_k = _lib.set_stream_k

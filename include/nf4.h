@@ -86,7 +86,8 @@ enum {
   NF4_PATH_GEMV_DGRAD = 9,   /* small-M SIMT input gradient                */
   NF4_PATH_SKINNY_FWD = 10,  /* small-M tensor-core (mma.sync) forward     */
   NF4_PATH_SKINNY_DGRAD = 11,/* small-M tensor-core input gradient         */
-  NF4_NUM_PATHS = 12
+  NF4_PATH_STREAM_K = 12,    /* fused launch with the stream-K schedule     */
+  NF4_NUM_PATHS = 13
 };
 
 /* A quantised weight: the tensors of the pages' QuantState as plain device
@@ -97,7 +98,10 @@ enum {
  *   absmax_q       [nblocks] uint8 8-bit codes of the absmax (double_quant == 1).
  *   nested_absmax  [ceil(nblocks/nested_blocksize)] fp32 (double_quant == 1).
  *   nested_offset  [1] fp32, the mean offset (double_quant == 1).
- *   code4          [16] fp32 4-bit codebook (NF4 levels), strictly increasing.
+ *   code4          [16] fp32 4-bit codebook in ascending order with an exact zero:
+ *                  the NF4 levels, or the E2M1 ("fp4") levels scaled to +-1 (whose
+ *                  -0, +0 pair is the one repeated value).  Quantisation picks the
+ *                  nearest level, ties to the lower index.
  *   code8          [256] fp32 8-bit map of the nested codes (double_quant == 1).
  * Decoded block scale under double quantisation (two roundings, no FMA):
  *   absmax'[b] = fp32(fp32(code8[absmax_q[b]] * nested_absmax[b/256]) + offset).
@@ -261,6 +265,23 @@ void nf4_set_weight_prefetch(int32_t enabled);
  * choices (different fp32 summation grouping). */
 enum { NF4_SMALL_M_AUTO = 0, NF4_SMALL_M_SIMT = 1, NF4_SMALL_M_TILES = 2 };
 void nf4_set_small_m_path(int32_t path);
+
+/* Schedule of the fused tcgen05 kernel for the dense products (process-wide;
+ * host only).  Classic: every CTA takes whole tiles (with a fixed contraction
+ * split at small M), leaving the last wave partly idle when the tile count is not
+ * a multiple of the SM count.  Stream-K: the tiles' 64-deep contraction steps are
+ * cut into one equal contiguous run per CTA; a tile cut between CTAs is finished
+ * by the CTA holding its first steps, which adds the following CTAs' fp32
+ * partial tiles in CTA order (deterministic for a given shape and SM count; the
+ * partials live in the workspace, which then holds SMs x 128 x tile-tokens fp32).
+ *   NF4_STREAM_K_OFF   classic only.
+ *   NF4_STREAM_K_AUTO  (default) stream-K where the planner's cost model prefers it.
+ *   NF4_STREAM_K_FORCE stream-K for every product on the fused kernel (tests).
+ * The CTA finishing a split tile waits (bounded, NF4_ERR_TIMEOUT on expiry) for
+ * the others' partials, so the grid (at most one CTA per SM) must be resident at
+ * once, as it is on a device this process does not share. */
+enum { NF4_STREAM_K_OFF = 0, NF4_STREAM_K_AUTO = 1, NF4_STREAM_K_FORCE = 2 };
+void nf4_set_stream_k(int32_t mode);
 
 /* Human-readable message of the last CUDA error that made a call of this thread
  * return NF4_ERR_CUDA ("no error" if none).  Static string. */

@@ -15,6 +15,16 @@ negative levels mirrored from ``linspace(1 - delta, 1/2, 8)`` without the last
 point, plus 0 -- and the whole set divided by its largest value so that both
 extremes are exactly +-1.  ``delta = (1/30 + 1/32) / 2``.
 
+``fp4_code4`` -- the "fp4" quant_type, which the pages list beside nf4 as the
+same packed 4-bit path (fork PR "Experts trainability", commit 1, quant_type
+table, row "nf4 / fp4") without giving its levels.  Reading: the 16 codes of the
+E2M1 4-bit float (1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit;
+exponent 0 holds the subnormals 0 and 0.5), whose magnitudes are 0, 0.5, 1, 1.5,
+2, 3, 4 and 6, divided by the largest (6) so that the extremes are exactly +-1,
+and listed in ascending order with -0 before +0.  Because of that signed-zero
+pair the table is non-decreasing rather than strictly increasing; quantisation
+then never yields index 8 (+0), and an all-zero block uses index 7 (-0).
+
 ``dynamic_code8`` -- the signed 8-bit dynamic ("tree") map used for the nested
 absmax codes.  The pages name only "blockwise dynamic map" (fork PR "Experts
 trainability", commit 1 table, int8 row) and BASELINE fixes "8-bit blockwise".
@@ -44,6 +54,20 @@ def nf4_code4_f64() -> np.ndarray:
 def nf4_code4() -> np.ndarray:
     """16 strictly increasing fp32 levels, code4[0] = -1, code4[7] = 0, code4[15] = 1."""
     return nf4_code4_f64().astype(np.float32)
+
+
+def fp4_code4_f64() -> np.ndarray:
+    mags = []
+    for e in range(4):          # exponent field, bias 1
+        for m in range(2):      # mantissa bit
+            mags.append(m * 0.5 if e == 0 else (1.0 + 0.5 * m) * 2.0 ** (e - 1))
+    mags = np.array(mags) / max(mags)  # 0, 1/12, 1/6, 1/4, 1/3, 1/2, 2/3, 1
+    return np.concatenate([-mags[::-1], mags])  # -1 ... -1/12, -0, +0, 1/12 ... 1
+
+
+def fp4_code4() -> np.ndarray:
+    """16 non-decreasing fp32 levels: -1 ... -1/12, -0, +0, 1/12 ... 1."""
+    return fp4_code4_f64().astype(np.float32)
 
 
 def dynamic_code8_f64() -> np.ndarray:

@@ -70,10 +70,13 @@ float oracle_f32_from_bf16(uint16_t h) {
 
 /* ------------------------------------------------------------ codebooks ---- */
 
-/* A codebook must be strictly increasing (nearest-level search relies on it). */
+/* A codebook must be in ascending order (nearest-level search relies on it):
+ * non-decreasing, so that the signed-zero pair of the E2M1
+ * ("fp4") levels, -0 then +0, is accepted; every other level is distinct in the
+ * tables used. */
 static int codebook_sorted(const float* code, int n) {
   for (int j = 0; j + 1 < n; ++j)
-    if (!(code[j] < code[j + 1])) return 0;
+    if (!(code[j] <= code[j + 1])) return 0;
   return 1;
 }
 

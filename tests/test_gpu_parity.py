@@ -381,3 +381,100 @@ def test_cta_pair_and_single_cta_tiles_both_match_oracle(M, N, K, mode):
             outs.append(o)
     finally:
         ops.set_cta_pairs(False)
+
+
+# --------------------------------------------------------------- fp4 codebook --
+# The "fp4" quant_type runs the same kernels with the E2M1 levels as code4.
+
+def _quant_pair_fp4(N, K, dq, seed=0):
+    g = synth.generator(seed)
+    w32 = synth.weight(N, K, g)
+    w = nf4.quantize(w32.to(DEV), double_quant=dq, quant_type="fp4")
+    st = oracle.quantize(w32.numpy(), ocb.fp4_code4(), 64, dq, ocb.dynamic_code8(), 256)
+    return w, st, g
+
+
+@pytest.mark.parametrize("N,K,dq", [(256, 512, True), (1000, 1344, False), (4096, 4096, True)])
+def test_fp4_quantize_dequantize_bit_exact(N, K, dq):
+    w, st, _ = _quant_pair_fp4(N, K, dq, seed=N)
+    torch.cuda.synchronize()
+    _assert_state_equal(w, st)
+    f32 = nf4.dequantize(w, torch.float32).cpu().numpy().reshape(-1)
+    b16 = bf16_bits(nf4.dequantize(w, torch.bfloat16)).reshape(-1)
+    np.testing.assert_array_equal(f32.view(np.uint32), oracle.dequantize(st, "f32").reshape(-1).view(np.uint32))
+    np.testing.assert_array_equal(b16, oracle.dequantize(st, "bf16").reshape(-1))
+
+
+@pytest.mark.parametrize("M", [1, 8, 40, 300])
+def test_fp4_fwd_dgrad_parity(M):
+    N, K = 640, 1024
+    w, st, g = _quant_pair_fp4(N, K, True, seed=M)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    parity(nf4.linear_fwd(x.to(DEV), w), oracle.linear_fwd(bf16_bits(x), wb), f"fp4 fwd M={M}")
+    parity(nf4.linear_dgrad(gy.to(DEV), w), oracle.linear_dgrad(bf16_bits(gy), wb), f"fp4 dgrad M={M}")
+
+
+def test_fp4_identity_probe_exact():
+    # One-hot rows select single dequantised weights; values compare exactly (a
+    # -0 weight sums to +0 with the other products, so values, not bits).
+    K, N = 256, 384
+    w, st, _ = _quant_pair_fp4(N, K, True, seed=5)
+    wb = oracle.dequantize(st, "bf16")
+    wbf = torch.from_numpy(wb.view(np.int16)).view(torch.bfloat16).float().numpy()
+    for rows in (K, 16):
+        eye = torch.eye(K, dtype=torch.bfloat16)[:rows].contiguous()
+        y = nf4.linear_fwd(eye.to(DEV), w).float().cpu().numpy()
+        np.testing.assert_array_equal(y, np.ascontiguousarray(wbf.T[:rows]))
+
+
+# ------------------------------------------------------------------- stream-K --
+# Forced on small shapes, tiles are cut between many CTAs (a tile's first segment
+# adds up to several following partials), which exercises every case of the
+# schedule; the default planner picks it for the large-M sweep points above.
+
+@pytest.fixture
+def restore_stream_k():
+    yield
+    ops.set_stream_k(_lib.STREAM_K_AUTO)
+
+
+@pytest.mark.parametrize("M,N,K", [(40, 320, 192), (64, 1000, 640), (129, 384, 320),
+                                   (300, 640, 1024), (700, 640, 1024)])
+def test_stream_k_forced_parity_and_reruns(M, N, K, restore_stream_k):
+    ops.set_stream_k(_lib.STREAM_K_FORCE)
+    w, st, g = _quant_pair(N, K, True, seed=7 * M + N)
+    x = synth.activation(M, K, g).to(DEV)
+    gy = synth.activation(M, N, g).to(DEV)
+    wb = oracle.dequantize(st, "bf16")
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x, w)
+    gx = nf4.linear_dgrad(gy, w)
+    c = nf4.path_counters()
+    assert c["stream_k"] == 2 and c["splitk_reduce"] == 0, c
+    parity(y, oracle.linear_fwd(bf16_bits(x.cpu()), wb), f"stream-K fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy.cpu()), wb), f"stream-K dgrad {M}x{N}x{K}")
+    for _ in range(5):
+        assert torch.equal(nf4.linear_fwd(x, w).view(torch.int16), y.view(torch.int16))
+        assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx.view(torch.int16))
+
+
+def test_stream_k_off_and_on_agree_within_tolerance(restore_stream_k):
+    M, N, K = 1536, 1024, 1024
+    w, st, g = _quant_pair(N, K, True, seed=11)
+    x = synth.activation(M, K, g).to(DEV)
+    ys = []
+    for mode in (_lib.STREAM_K_OFF, _lib.STREAM_K_FORCE):
+        ops.set_stream_k(mode)
+        ys.append(nf4.linear_fwd(x, w).float())
+    # Only the fp32 summation order differs (the split tiles add partials), so the
+    # bf16 results agree except where that order flips a rounding: one bf16 ulp,
+    # plus the fp32 sums' own difference (about sqrt(K) 2^-24 of the terms, far
+    # below 1e-4 rms) where cancellation leaves a small result.
+    rel = (torch.linalg.norm(ys[0] - ys[1]) / torch.linalg.norm(ys[0])).item()
+    assert rel < 1e-3, rel
+    assert (ys[0] == ys[1]).float().mean().item() > 0.9
+    rms = ys[0].pow(2).mean().sqrt()
+    bound = torch.maximum(ys[0].abs(), ys[1].abs()) * 2.0 ** -7 + 1e-4 * rms
+    assert bool(((ys[0] - ys[1]).abs() <= bound).all())

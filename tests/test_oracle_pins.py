@@ -58,6 +58,53 @@ def test_code4_levels_are_normal_quantiles():
         assert abs(_phi(-float(CODE4[j]) * z_top) - p) < 2e-7, j
 
 
+FP4 = codebooks.fp4_code4()
+
+
+def test_fp4_levels_are_e2m1_scaled_to_unit():
+    # E2M1: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (exponent bias 1, one mantissa
+    # bit, subnormals at exponent 0), divided by the largest; ascending with -0
+    # before +0.
+    assert FP4.dtype == np.float32 and FP4.shape == (16,)
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for i, m in enumerate(e2m1):
+        assert abs(float(FP4[8 + i]) * 6.0 - m) <= 4e-7 * max(m, 1.0), i
+        assert abs(float(FP4[7 - i]) * 6.0 + m) <= 4e-7 * max(m, 1.0), i
+    # levels that are dyadic are exact; the rest are the nearest fp32
+    assert FP4[15] == 1.0 and FP4[0] == -1.0 and FP4[13] == 0.5 and FP4[11] == 0.25
+    assert FP4[14] == np.float32(2.0 / 3.0) and FP4[9] == np.float32(1.0 / 12.0)
+    # signed zero pair; every other neighbour strictly increasing; mirror symmetry
+    assert FP4[7] == 0.0 and np.signbit(FP4[7]) and FP4[8] == 0.0 and not np.signbit(FP4[8])
+    d = np.diff(FP4.astype(np.float64))
+    assert np.all(d[np.arange(15) != 7] > 0) and d[7] == 0
+    np.testing.assert_array_equal(FP4[::-1].view(np.uint32), (-FP4).view(np.uint32))
+
+
+def test_fp4_round_trip_ties_and_zero_block():
+    # Codebook-aligned blocks come back exactly (index 8, +0, is never produced:
+    # an exact zero maps to index 7, -0, the first level equal to it).
+    rng = np.random.default_rng(11)
+    idx = rng.choice([j for j in range(16) if j != 8], size=(64, 64))
+    idx[:, 0] = 15
+    a = np.float32(0.75)
+    w = (FP4[idx] * a).astype(np.float32)
+    packed, absmax = oracle.quantize_nf4(w, FP4, 64)
+    assert np.all(absmax == a)
+    q = np.stack([packed >> 4, packed & 15], axis=1).reshape(-1)
+    np.testing.assert_array_equal(q, idx.reshape(-1))
+    st = oracle.QuantState(w.shape, 64, packed, absmax, FP4)
+    np.testing.assert_array_equal(oracle.dequantize(st, "f32"), w)
+    # Midpoint of 0 and 1/12 (exact: half an fp32) goes to the lower index (+0);
+    # just above goes to 1/12; a small negative value to -0; 0 itself to -0.
+    mid = np.float32(FP4[9] / np.float32(2))
+    w = np.array([1.0, mid, np.nextafter(mid, np.float32(1)), np.float32(-1e-3), 0.0, 0.0],
+                 np.float32)
+    packed, _ = oracle.quantize_nf4(w, FP4, blocksize=6)
+    assert packed.tolist() == [(15 << 4) | 8, (9 << 4) | 7, (7 << 4) | 7]
+    packed, absmax = oracle.quantize_nf4(np.zeros(64, np.float32), FP4)
+    assert absmax.tolist() == [0.0] and packed.tolist() == [0x77] * 32
+
+
 def test_code8_dynamic_map_structure():
     assert CODE8.shape == (256,) and np.all(np.diff(CODE8) > 0)
     assert 0.0 in CODE8 and CODE8.max() == 1.0
