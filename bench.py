@@ -50,6 +50,8 @@ def parse():
                    help="profiling case: one projection of the workload (q,k,v,o,gate,up,down)")
     p.add_argument("--m", type=int, default=M_HEAD, help="tokens of the --single case")
     p.add_argument("--reps", type=int, default=3, help="fwd+dgrad pairs of the --single case")
+    p.add_argument("--stream-k", choices=["auto", "off", "force"], default="auto",
+                   help="schedule of the fused kernel (library default: auto)")
     return p.parse_args()
 
 
@@ -213,6 +215,7 @@ def run_ours(args, rank, world, local_rank):
     nf4.device_check()
     nf4.device_status(clear=True)
     ops.set_weight_prefetch(True)  # frozen weights: the small-M kernels may read them early
+    ops.set_stream_k({"off": 0, "auto": 1, "force": 2}[args.stream_k])
     sets, g = make_weights(dev, REPLICAS)
     xs, gys, xs_host, gys_host = make_acts(g, M_HEAD, dev)
     ys = [torch.empty(M_HEAD, w.N, dtype=torch.bfloat16, device=dev) for w in sets[0]]
@@ -337,6 +340,7 @@ def run_ours(args, rank, world, local_rank):
             "parallelism": f"replicas x{world}",
             "weight_prefetch": "on (frozen weights; small-M kernels read them before the "
                                "dependency on the previous kernel resolves)",
+            "stream_k": args.stream_k,
         },
         "roofline": {
             "kernel": "nf4_gemm_kernel (fused tcgen05 fwd + dgrad, BT=256)",
@@ -593,6 +597,7 @@ def run_single(args):
     import bit_nf4_quantized_linear_gb300 as nf4
     from bit_nf4_quantized_linear_gb300 import ops, synth
     dev = torch.device("cuda", 0)
+    ops.set_stream_k({"off": 0, "auto": 1, "force": 2}[args.stream_k])
     shapes = {n: (K, N) for n, K, N in synth.LLAMA8B_PROJ}
     K, N = shapes[args.single]
     g = synth.generator(0)
