@@ -591,21 +591,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (a.tma_out && a.splits == 1) {
         // bf16 tile through shared memory: per 32-token chunk this warp writes its
         // 32 columns x 32 tokens and one lane stores them with a bulk tensor copy
-        // (rows past M and columns past the output width are not written).
+        // (rows past M and columns past the output width are not written).  A chunk
+        // is one tensor-memory wait, and its partial loads (stream-K) are all in
+        // flight together.
         uint16_t* stg = reinterpret_cast<uint16_t*>(smem + G::kOffOut + q * kOutWarpBytes);
         const uint32_t stg_addr = sbase + G::kOffOut + q * kOutWarpBytes;
 #pragma unroll 1
         for (int c0 = 0; c0 < ntok; c0 += 32) {
           if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
           __syncwarp();
-#pragma unroll 1
-          for (int h = 0; h < 32 && c0 + h < ntok; h += kBatch) {
-            uint32_t v[kBatch];
-            load_batch(c0 + h, v);
+          uint32_t v[32];
+          tmem_ld_32x32b_x16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
+          if (BT > 16) tmem_ld_32x32b_x16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          tmem_wait_ld();
+          if (sk_own)
+            for (int64_t c = unit + 1; c <= own_last; ++c) {
+              const float* src = sk_slot(c) + c0 * 32;
+              float p[32];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-              stg[(h + j) * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
-          }
+              for (int j = 0; j < 32; ++j) p[j] = (BT > 16 || j < 16) ? src[j * 32] : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = __float_as_uint(__fadd_rn(__uint_as_float(v[j]), p[j]));
+            }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (BT > 16 || j < 16)
+              stg[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
