@@ -60,13 +60,16 @@ def lib():
             L.oracle_double_quant.argtypes = [P, i64, i32, i32, P, P, P, P]
             L.oracle_decode_absmax.argtypes = [P, P, ctypes.c_float, i64, i32, P, P]
             L.oracle_dequantize_nf4.argtypes = [P, P, i64, i32, P, P, P]
+            L.oracle_quantize_8bit.argtypes = [P, i64, i32, P, P, P]
+            L.oracle_dequantize_8bit.argtypes = [P, P, i64, i32, P, P, P]
             L.oracle_linear_fwd.argtypes = [P, i64, i64, P, i64, P, i64, P]
             L.oracle_linear_dgrad.argtypes = [P, i64, i64, P, i64, P, i64, P]
             L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
             L.oracle_bf16_from_f32.restype = ctypes.c_uint16
             L.oracle_num_threads.restype = ctypes.c_int
             for name in ("oracle_quantize_nf4", "oracle_double_quant", "oracle_decode_absmax",
-                         "oracle_dequantize_nf4", "oracle_linear_fwd", "oracle_linear_dgrad"):
+                         "oracle_dequantize_nf4", "oracle_linear_fwd", "oracle_linear_dgrad",
+                         "oracle_quantize_8bit", "oracle_dequantize_8bit"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -112,7 +115,8 @@ class QuantState:
 
     def __init__(self, shape, blocksize, packed, absmax, code4, double_quant=False,
                  absmax_q=None, nested_absmax=None, nested_offset=None, code8=None,
-                 nested_blocksize=256):
+                 nested_blocksize=256, bits=4):
+        self.bits = bits  # 4: two codes per byte, 16-level code4; 8: one code per byte, 256 levels
         self.shape = tuple(shape)
         self.blocksize = blocksize
         self.packed = packed
@@ -145,6 +149,20 @@ def quantize_nf4(w: np.ndarray, code4: np.ndarray, blocksize: int = 64):
     return packed, absmax
 
 
+def quantize_8bit(w: np.ndarray, code: np.ndarray, blocksize: int = 64):
+    """Blockwise 8-bit quantisation of a flat view of w (fp32) with a 256-level
+    codebook.  Returns (codes uint8 [numel], absmax)."""
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    code = np.ascontiguousarray(code, dtype=np.float32)
+    assert code.size == 256
+    numel = w.size
+    q = np.zeros(numel, dtype=np.uint8)
+    absmax = np.zeros((numel + blocksize - 1) // blocksize, dtype=np.float32)
+    _check(lib().oracle_quantize_8bit(_p(w), numel, blocksize, _p(code), _p(q), _p(absmax)),
+           "quantize_8bit")
+    return q, absmax
+
+
 def double_quant(absmax: np.ndarray, code8: np.ndarray, nested_blocksize: int = 256):
     """8-bit blockwise quantisation of the absmax array.  Returns (absmax_q, nested_absmax, offset)."""
     absmax = np.ascontiguousarray(absmax, dtype=np.float32).reshape(-1)
@@ -172,8 +190,15 @@ def decode_absmax(absmax_q, nested_absmax, offset, code8, nested_blocksize: int 
 
 def quantize(w: np.ndarray, code4, blocksize: int = 64, double_quant_: bool = False,
              code8=None, nested_blocksize: int = 256) -> QuantState:
-    packed, absmax = quantize_nf4(w, code4, blocksize)
-    st = QuantState(np.shape(w), blocksize, packed, absmax, np.asarray(code4, np.float32))
+    """Blockwise quantisation with the value codebook `code4`: 16 levels give the
+    packed 4-bit format, 256 levels the 8-bit format (one code per byte)."""
+    code4 = np.asarray(code4, np.float32)
+    if code4.size == 256:
+        packed, absmax = quantize_8bit(w, code4, blocksize)
+        st = QuantState(np.shape(w), blocksize, packed, absmax, code4, bits=8)
+    else:
+        packed, absmax = quantize_nf4(w, code4, blocksize)
+        st = QuantState(np.shape(w), blocksize, packed, absmax, code4)
     if double_quant_:
         aq, nested, off = double_quant(absmax, code8, nested_blocksize)
         st.double_quant = True
@@ -196,14 +221,15 @@ def dequantize(st: QuantState, dtype: str = "bf16") -> np.ndarray:
     """Dense dequantised weight: fp32 values, or bf16 bit patterns (uint16)."""
     scale = np.ascontiguousarray(block_scale(st), dtype=np.float32)
     n = st.numel
+    fn = lib().oracle_dequantize_8bit if st.bits == 8 else lib().oracle_dequantize_nf4
     if dtype == "f32":
         out = np.zeros(n, dtype=np.float32)
-        _check(lib().oracle_dequantize_nf4(_p(st.packed), _p(scale), n, st.blocksize,
-                                           _p(st.code4), _p(out), None), "dequantize")
+        _check(fn(_p(st.packed), _p(scale), n, st.blocksize, _p(st.code4), _p(out), None),
+               "dequantize")
     elif dtype == "bf16":
         out = np.zeros(n, dtype=np.uint16)
-        _check(lib().oracle_dequantize_nf4(_p(st.packed), _p(scale), n, st.blocksize,
-                                           _p(st.code4), None, _p(out)), "dequantize")
+        _check(fn(_p(st.packed), _p(scale), n, st.blocksize, _p(st.code4), None, _p(out)),
+               "dequantize")
     else:
         raise ValueError(dtype)
     return out.reshape(st.shape)

@@ -25,6 +25,16 @@ and listed in ascending order with -0 before +0.  Because of that signed-zero
 pair the table is non-decreasing rather than strictly increasing; quantisation
 then never yields index 8 (+0), and an all-zero block uses index 7 (-0).
 
+``e4m3_code8`` -- the "fp8" 8-bit weight storage, which the pages describe as an
+"e4m3 codebook" on the same blockwise path (fork PR "Experts trainability",
+commit 1, quant_type table, row "fp8").  Reading: the 256 codes of a float with
+1 sign bit, 4 exponent bits (bias 7) and 3 mantissa bits, exponent 0 holding the
+subnormals, no code set aside for NaN or infinity; magnitudes m/8 * 2**-6 (e = 0)
+and (1 + m/8) * 2**(e - 7) (e = 1..15), divided by the largest (480) so the
+extremes are +-1, ascending with -0 before +0 (non-decreasing, as for fp4).  The
+"int8" storage of the same table row uses ``dynamic_code8`` below as its 256
+levels ("blockwise dynamic map").
+
 ``dynamic_code8`` -- the signed 8-bit dynamic ("tree") map used for the nested
 absmax codes.  The pages name only "blockwise dynamic map" (fork PR "Experts
 trainability", commit 1 table, int8 row) and BASELINE fixes "8-bit blockwise".
@@ -68,6 +78,20 @@ def fp4_code4_f64() -> np.ndarray:
 def fp4_code4() -> np.ndarray:
     """16 non-decreasing fp32 levels: -1 ... -1/12, -0, +0, 1/12 ... 1."""
     return fp4_code4_f64().astype(np.float32)
+
+
+def e4m3_code8_f64() -> np.ndarray:
+    mags = []
+    for e in range(16):        # exponent field, bias 7
+        for m in range(8):     # mantissa field
+            mags.append(m / 8.0 * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    mags = np.array(mags) / max(mags)
+    return np.concatenate([-mags[::-1], mags])
+
+
+def e4m3_code8() -> np.ndarray:
+    """256 non-decreasing fp32 levels: -1 ... -0, +0 ... 1."""
+    return e4m3_code8_f64().astype(np.float32)
 
 
 def dynamic_code8_f64() -> np.ndarray:

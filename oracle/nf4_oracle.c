@@ -144,6 +144,54 @@ int oracle_quantize_nf4(const float* w, int64_t numel, int32_t blocksize, const 
   return ORACLE_OK;
 }
 
+/* --------------------------------------------------- 8-bit quantisation ---- */
+
+/* Blockwise 8-bit quantisation (fork PR "Experts trainability", commit 1 table:
+ * "int8: blockwise dynamic map, 1 byte/value"; "fp8: e4m3 codebook, same
+ * blockwise path").  Same steps as the 4-bit case with a 256-level codebook and
+ * one code per byte: q[i] = nearest level of fp32(w[i] / absmax) (ties to the
+ * lower index), an all-zero block using the index of the first exact zero. */
+int oracle_quantize_8bit(const float* w, int64_t numel, int32_t blocksize, const float* code,
+                         uint8_t* q, float* absmax) {
+  if (numel < 0 || blocksize <= 0 || !w || !code || !q || !absmax) return ORACLE_ERR_ARG;
+  if (!codebook_sorted(code, 256)) return ORACLE_ERR_CODEBOOK;
+  int zero = codebook_zero(code, 256);
+  if (zero < 0) return ORACLE_ERR_CODEBOOK;
+  int64_t nblocks = (numel + blocksize - 1) / blocksize;
+  for (int64_t b = 0; b < nblocks; ++b) {
+    int64_t start = b * blocksize;
+    int64_t len = numel - start < blocksize ? numel - start : blocksize;
+    float a = 0.0f;
+    for (int64_t i = 0; i < len; ++i) {
+      float m = fabsf(w[start + i]);
+      if (m > a) a = m;
+    }
+    absmax[b] = a;
+    for (int64_t i = 0; i < len; ++i) {
+      if (a == 0.0f) {
+        q[start + i] = (uint8_t)zero;
+      } else {
+        float v = w[start + i] / a; /* one IEEE single-precision division */
+        q[start + i] = (uint8_t)nearest_level(code, 256, v);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* wf[i] = fp32(code[q[i]] * scale[block(i)]), one code per byte. */
+int oracle_dequantize_8bit(const uint8_t* q, const float* scale, int64_t numel,
+                           int32_t blocksize, const float* code, float* out_f32,
+                           uint16_t* out_bf16) {
+  if (numel < 0 || blocksize <= 0 || !q || !scale || !code) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < numel; ++i) {
+    float wf = code[q[i]] * scale[i / blocksize];
+    if (out_f32) out_f32[i] = wf;
+    if (out_bf16) out_bf16[i] = oracle_bf16_from_f32(wf);
+  }
+  return ORACLE_OK;
+}
+
 /* ------------------------------------------------- double quantisation ---- */
 
 /* 8-bit blockwise quantisation of the fp32 absmax array (nested statistics).
