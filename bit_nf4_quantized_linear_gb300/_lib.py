@@ -48,6 +48,7 @@ class nf4_weight(ctypes.Structure):
         ("blocksize", ctypes.c_int32),
         ("nested_blocksize", ctypes.c_int32),
         ("double_quant", ctypes.c_int32),
+        ("bits", ctypes.c_int32),
     ]
 
 
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
         W = ctypes.POINTER(nf4_weight)
         sig = {
             "nf4_quantize": [P, I32, I64, I64, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
+            "nf4_quantize_8bit": [P, I32, I64, I64, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
             "nf4_dequantize": [W, P, I32, P],
             "nf4_linear_fwd": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_linear_dgrad": [P, I64, I64, W, P, I64, P, SZ, P],

@@ -15,6 +15,12 @@ read as the E2M1 4-bit float (sign, 2-bit exponent with bias 1, 1-bit mantissa,
 subnormals at exponent 0) scaled by 1/6 so its extremes are +-1, in ascending
 order with -0 before +0.
 
+``e4m3_code8``: the "fp8" 8-bit weight storage ("e4m3 codebook", fork PR
+"Experts trainability", commit 1, quant_type table), read as all 256 codes of a
+1-4-3 float (exponent bias 7, subnormals at exponent 0, no special codes) scaled
+by 1/480 so its extremes are +-1, ascending with -0 before +0.  The "int8"
+storage of the same row uses ``dynamic_code8`` as its 256 levels.
+
 ``dynamic_code8``: the signed 8-bit dynamic tree map (Dettmers et al. 2022,
 "8-bit Optimizers via Block-wise Quantization") for the nested absmax codes:
 decimal exponent groups 10**(e-6), e = 0..6, holding 2**e linear fraction values
@@ -51,13 +57,42 @@ def fp4_code4() -> torch.Tensor:
     return vals[order].to(torch.float32)
 
 
-def code4_for(quant_type: str) -> torch.Tensor:
-    """The 16-entry codebook of a 4-bit quant_type ("nf4" or "fp4")."""
+def e4m3_code8() -> torch.Tensor:
+    bits = torch.arange(256, dtype=torch.int64)
+    sign = torch.where(bits >= 128, -1.0, 1.0).to(torch.float64)
+    exp = (bits >> 3) & 15
+    man = (bits & 7).to(torch.float64)
+    mag = torch.where(exp == 0, man / 8.0 * 2.0 ** -6,
+                      (1.0 + man / 8.0) * torch.pow(2.0, (exp - 7).to(torch.float64)))
+    vals = sign * mag / 480.0
+    # The magnitude grows with the low seven bits, so ascending order (-0 before
+    # +0) is codes 255 down to 128, then 0 up to 127.
+    order = torch.cat([torch.arange(255, 127, -1), torch.arange(0, 128)])
+    return vals[order].to(torch.float32)
+
+
+QUANT_TYPES = {"nf4": 4, "fp4": 4, "int8": 8, "fp8": 8}
+
+
+def code_for(quant_type: str) -> torch.Tensor:
+    """The value codebook of a quant_type: 16 levels for the packed 4-bit types
+    ("nf4", "fp4"), 256 for the one-byte types ("int8": dynamic map, "fp8": e4m3)."""
     if quant_type == "nf4":
         return nf4_code4()
     if quant_type == "fp4":
         return fp4_code4()
-    raise ValueError(f"unknown 4-bit quant_type {quant_type!r} (expected 'nf4' or 'fp4')")
+    if quant_type == "int8":
+        return dynamic_code8()
+    if quant_type == "fp8":
+        return e4m3_code8()
+    raise ValueError(f"unknown quant_type {quant_type!r} (expected one of {sorted(QUANT_TYPES)})")
+
+
+def code4_for(quant_type: str) -> torch.Tensor:
+    """The 16-entry codebook of a 4-bit quant_type ("nf4" or "fp4")."""
+    if QUANT_TYPES.get(quant_type) != 4:
+        raise ValueError(f"unknown 4-bit quant_type {quant_type!r} (expected 'nf4' or 'fp4')")
+    return code_for(quant_type)
 
 
 def dynamic_code8() -> torch.Tensor:

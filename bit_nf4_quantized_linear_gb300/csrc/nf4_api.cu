@@ -116,6 +116,23 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tensor map of the codes for one contraction step: the forward reads 128 weight
+// rows x 64 values, the input gradient 64 rows x 128 values.  4-bit codes: 32-byte
+// rows (32B swizzle) / 64-byte rows (64B swizzle); 8-bit codes: 64-byte rows (64B
+// swizzle) / 128-byte rows (128B swizzle).  The swizzles keep the decoders'
+// 16-byte loads bank-conflict free.
+bool encode_codes(CUtensorMap* m, const nf4_weight* w, int mode) {
+  const int bits = w->bits == 8 ? 8 : 4;
+  const uint64_t row_bytes = static_cast<uint64_t>(w->K) * bits / 8;
+  if (mode == 0)
+    return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, row_bytes, w->N, row_bytes,
+                     nf4::kTileK * bits / 8, nf4::kTileW,
+                     bits == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, row_bytes, w->N, row_bytes,
+                   nf4::kTileW * bits / 8, nf4::kTileK,
+                   bits == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 void count(int path) {
   g_counters[path].fetch_add(1, std::memory_order_relaxed);
   g_counters[NF4_PATH_TOTAL].fetch_add(1, std::memory_order_relaxed);
@@ -123,6 +140,7 @@ void count(int path) {
 
 nf4_status check_weight(const nf4_weight* w) {
   if (!w || !w->packed || !w->code4) return NF4_ERR_INVALID_ARG;
+  if (w->bits != 0 && w->bits != 4 && w->bits != 8) return NF4_ERR_INVALID_ARG;
   if (w->N < 1 || w->K < 1) return NF4_ERR_INVALID_ARG;
   if (w->blocksize != 64) return NF4_ERR_UNSUPPORTED;
   if (w->double_quant != 0 && w->double_quant != 1) return NF4_ERR_INVALID_ARG;
@@ -218,12 +236,14 @@ double step_cycles(int bt, int cg) {
 // the packed weight.  Larger M: token tile, CTA pairing and split chosen by a cost
 // model in SM clocks -- waves of items times contraction steps, plus the split
 // partials' round trip through memory.
-Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true) {
+Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true,
+                int bits = 4) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
   const int small = g_small_m_path.load(std::memory_order_relaxed);
   nf4::SkinnyPlan sk;
-  if (M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk)) {
+  // 8-bit codes run the fused tcgen05 kernel at every M (tiles of <= 128 tokens).
+  if (bits == 4 && M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.skinny = true;
     p.sk = sk;
@@ -231,7 +251,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     p.ws_bytes = 0;
     return p;
   }
-  if (M > 0 && small != NF4_SMALL_M_TILES &&
+  if (bits == 4 && M > 0 && small != NF4_SMALL_M_TILES &&
       M <= (mode == 0 ? nf4::kGemvMaxMFwd : nf4::kGemvMaxMDgrad)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.gemv = true;
@@ -255,7 +275,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     }
     return make_plan(M, ncols, contract, bt, static_cast<int>(s));
   }
-  const int bt_max = choose_bt(M);
+  const int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : choose_bt(M);
   const int cand_bt[4] = {256, 256, 128, 64};
   const int cand_cg[4] = {2, 1, 1, 1};
   const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
@@ -322,7 +342,8 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   DevInfo dev;
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
-  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk);
+  const int bits = w->bits == 8 ? 8 : 4;
+  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk, bits);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -393,15 +414,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, M, ld_act * 2, 64,
                  p.bt / p.cg, CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
-  if (mode == 0) {
-    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 32,
-                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_32B))
-      return NF4_ERR_CUDA;
-  } else {
-    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2, 64,
-                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_64B))
-      return NF4_ERR_CUDA;
-  }
+  if (!encode_codes(&tmap_pk, w, mode)) return NF4_ERR_CUDA;
   nf4::GemmArgs a{};
   a.M = M;
   a.ncols = out_cols;
@@ -450,7 +463,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
       return NF4_ERR_CUDA;
     a.tma_out = 1;
   }
-  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, a, tmap_act, tmap_pk, tmap_out, grid, s);
+  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, bits, a, tmap_act, tmap_pk, tmap_out, grid, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
   if (p.stream_k)  // a property of the launch just counted, not a launch of its own
@@ -484,20 +497,13 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   // Tokens per tile follow the mean rows per expert.
-  const int bt = choose_bt((T + E - 1) / E);
+  int bt = choose_bt((T + E - 1) / E);
+  if (w->bits == 8 && bt > 128) bt = 128;  // 8-bit codes: tiles of <= 128 tokens
   CUtensorMap tmap_act, tmap_pk;
   if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, T, ld_act * 2, 64, bt,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
-  if (mode == 0) {
-    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, w->N, K / 2, 32,
-                   nf4::kTileW, CU_TENSOR_MAP_SWIZZLE_32B))
-      return NF4_ERR_CUDA;
-  } else {
-    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, w->N, K / 2, 64,
-                   nf4::kTileK, CU_TENSOR_MAP_SWIZZLE_64B))
-      return NF4_ERR_CUDA;
-  }
+  if (!encode_codes(&tmap_pk, w, mode)) return NF4_ERR_CUDA;
   nf4::GemmArgs a{};
   a.M = T;
   a.ncols = out_cols;
@@ -528,7 +534,8 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   CUtensorMap tmap_out;  // unused: expert row ranges end inside tiles (direct stores)
   std::memset(&tmap_out, 0, sizeof(tmap_out));
   a.tma_out = 0;
-  cudaError_t le = nf4::launch_gemm(mode, bt, 1, a, tmap_act, tmap_pk, tmap_out, dev.sms, s);
+  cudaError_t le = nf4::launch_gemm(mode, bt, 1, w->bits == 8 ? 8 : 4, a, tmap_act, tmap_pk,
+                                    tmap_out, dev.sms, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
   return NF4_OK;
@@ -560,6 +567,38 @@ nf4_status nf4_quantize(const void* W, int32_t w_dtype, int64_t N, int64_t K, in
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t le = nf4::launch_quantize(W, w_dtype, numel, code4, packed, absmax, s);
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+  count(NF4_PATH_QUANTIZE);
+  if (double_quant) {
+    le = nf4::launch_double_quant(absmax, nblocks, code8, absmax_q, nested_absmax, nested_offset,
+                                  static_cast<double*>(ws), s);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+  }
+  return NF4_OK;
+}
+
+nf4_status nf4_quantize_8bit(const void* W, int32_t w_dtype, int64_t N, int64_t K,
+                             int32_t blocksize, int32_t double_quant, int32_t nested_blocksize,
+                             const float* code, const float* code8, uint8_t* codes,
+                             float* absmax, uint8_t* absmax_q, float* nested_absmax,
+                             float* nested_offset, void* ws, size_t ws_bytes, void* stream) {
+  if (!W || !code || !codes || !absmax || N < 1 || K < 1) return NF4_ERR_INVALID_ARG;
+  if (w_dtype != NF4_DTYPE_F32 && w_dtype != NF4_DTYPE_BF16) return NF4_ERR_INVALID_ARG;
+  if (blocksize != 64) return NF4_ERR_UNSUPPORTED;
+  if (double_quant != 0 && double_quant != 1) return NF4_ERR_INVALID_ARG;
+  const int64_t numel = N * K;
+  const int64_t nblocks = (numel + 63) / 64;
+  if (double_quant) {
+    if (nested_blocksize != nf4::kNestedBlock) return NF4_ERR_UNSUPPORTED;
+    if (!code8 || !absmax_q || !nested_absmax || !nested_offset) return NF4_ERR_INVALID_ARG;
+    const size_t need = static_cast<size_t>((nblocks + nf4::kMeanChunk - 1) / nf4::kMeanChunk) * 8;
+    if (!ws || ws_bytes < need) return NF4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 7u) != 0) return NF4_ERR_ALIGNMENT;
+  }
+  DevInfo dev;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t le = nf4::launch_quantize8(W, w_dtype, numel, code, codes, absmax, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(NF4_PATH_QUANTIZE);
   if (double_quant) {
@@ -614,7 +653,11 @@ size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     DevInfo dev;
     if (!current_device(&dev)) return 0;
-    return plan_dense(op == NF4_OP_LINEAR_FWD ? 0 : 1, M, N, K, dev.sms).ws_bytes;
+    // Enough for either code width (the plan depends on it).
+    const int mode = op == NF4_OP_LINEAR_FWD ? 0 : 1;
+    const size_t w4 = plan_dense(mode, M, N, K, dev.sms, true, 4).ws_bytes;
+    const size_t w8 = plan_dense(mode, M, N, K, dev.sms, true, 8).ws_bytes;
+    return w4 > w8 ? w4 : w8;
   }
   return 0;
 }
@@ -735,7 +778,8 @@ extern "C" nf4_status nf4_linear_fwd_noalloc(const void* x, int64_t M, int64_t l
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   // The stream-K schedule is not used here (its partial tiles outgrow the array);
   // shapes whose split partials would not fit are rejected up front.
-  if (plan_dense(0, M, w->N, w->K, dev.sms, false).ws_bytes > NF4_NOALLOC_SCRATCH_BYTES)
+  if (plan_dense(0, M, w->N, w->K, dev.sms, false, w->bits == 8 ? 8 : 4).ws_bytes >
+      NF4_NOALLOC_SCRATCH_BYTES)
     return NF4_ERR_WORKSPACE;
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);

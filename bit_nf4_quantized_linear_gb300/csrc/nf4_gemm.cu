@@ -38,6 +38,12 @@
 #include "decode.cuh"
 #include "sm100_ptx.cuh"
 
+// Code width of the kernel instances this translation unit launches: 4 here,
+// 8 when nf4_gemm8.cu compiles this file a second time.
+#ifndef NF4_GEMM_BITS
+#define NF4_GEMM_BITS 4
+#endif
+
 namespace nf4 {
 namespace {
 
@@ -53,21 +59,25 @@ constexpr int kWarpDec0 = 6;
 constexpr int kWarpTmaX = kWarpDec0 + kNumDecWarps;  // activation producer
 constexpr int kThreads = (kWarpTmaX + 1) * 32;
 constexpr int kAStage = kTileW * kTileK * 2;  // 16 KB of bf16
-constexpr int kPkStage = kTileW * kTileK / 2;  // 4 KB of packed codes
-constexpr int kMiscBytes = 8192;
+constexpr int kMiscBase = 8192;  // codebooks, barriers, expert tables
 constexpr int kOutWarpBytes = 32 * 32 * 2;        // epilogue staging: 32 tokens x 32 bf16 per warp
 constexpr int kOutBytes = 4 * kOutWarpBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bound of every wait (2 s)
 constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up to 20 us per try
 
-template <int BT, int CG>
+// BITS = 4: two codes per byte (packed nibbles, 16-level codebook in registers);
+// BITS = 8: one code per byte (256-level codebook in shared memory, after the
+// base misc region).
+template <int BT, int CG, int BITS>
 struct Geo {
+  static constexpr int kPkStage = kTileW * kTileK * BITS / 8;  // codes of one step: 4 or 8 KB
+  static constexpr int kMiscBytes = kMiscBase + (BITS == 8 ? 1024 : 0);
   static constexpr int kXStage = (BT / CG) * 128;  // this CTA's BT/CG token rows of 64 bf16
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
   // Decoded operand tiles: one slot more than decoder groups where the activation
   // tiles leave room, so a group never waits on the MMAs of the step just before.
   static constexpr int kStagesA = BT >= 256 ? kDecGroups : kDecGroups + 1;
-  static constexpr int kStagesP = BT <= 64 ? 16 : 8; // packed-code tiles (prefetched far ahead)
+  static constexpr int kStagesP = (BT <= 64 ? 16 : 8) / (BITS / 4);  // code tiles, prefetched far ahead
   static constexpr int kStagesX0 =
       (kBudget - kStagesA * kAStage - kStagesP * kPkStage - kOutBytes) / kXStage;
   static constexpr int kStagesX = kStagesX0 > 8 ? 8 : kStagesX0;  // activation tiles
@@ -87,6 +97,7 @@ struct Geo {
                 "a decoder group advances every ring by kDecGroups slots per step");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
   static_assert(CG == 1 || BT == 256, "CTA pairs are used with 256-token tiles");
+  static_assert(BITS == 4 || (BITS == 8 && CG == 1 && BT <= 128), "8-bit codes: tiles of <= 128 tokens");
 };
 
 // Barrier slots in the misc region.  Three rings advance one stage per
@@ -318,12 +329,13 @@ __device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* co
   return __fadd_rn(__fmul_rn(code8_s[r.q], r.v), offset);
 }
 
-template <int MODE, int BT, int CG>
+template <int MODE, int BT, int CG, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
                     const __grid_constant__ CUtensorMap tmap_pk,
                     const __grid_constant__ CUtensorMap tmap_out, const GemmArgs a) {
-  using G = Geo<BT, CG>;
+  using G = Geo<BT, CG, BITS>;
+  constexpr int kPkStage = G::kPkStage;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -439,11 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sbase + G::kOffX + st * G::kXStage, &tmap_act, full, ks * kTileK,
                         static_cast<int32_t>(it.tok0 + sh.rank * (BT / CG)));
           else if (MODE == 0)
-            tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK / 2),
+            tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK * BITS / 8),
                         static_cast<int32_t>(it.wrow0));
           else
             tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full,
-                        static_cast<int32_t>(it.col0 / 2),
+                        static_cast<int32_t>(it.col0 * BITS / 8),
                         static_cast<int32_t>(it.wrow0 + static_cast<int64_t>(ks) * kTileK));
           issued |= 1u << st;
           par = (par & ~(1u << st)) | (ph << st);
@@ -676,26 +688,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rb = ((dw & 3) << 5) | lane;     // row-block 0..127
     const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
     uint64_t code2[8];
+    if (BITS == 4) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      code2[i] = (static_cast<uint64_t>(__float_as_uint(__ldg(a.code4 + 2 * i + 1))) << 32) |
-                 __float_as_uint(__ldg(a.code4 + 2 * i));
-    // The 8-bit map of the block statistics goes to shared memory for the random
-    // lookups; the decoder warps alone synchronise on it (named barrier 1).
+      for (int i = 0; i < 8; ++i)
+        code2[i] = (static_cast<uint64_t>(__float_as_uint(__ldg(a.code4 + 2 * i + 1))) << 32) |
+                   __float_as_uint(__ldg(a.code4 + 2 * i));
+    }
+    // The 8-bit map of the block statistics (and, for 8-bit codes, the 256-level
+    // value codebook) go to shared memory for the random lookups; the decoder
+    // warps alone synchronise on them (named barrier 1).
+    float* valtab = reinterpret_cast<float*>(smem + G::kOffMisc + kMiscBase);
     const int dtid = dw * 32 + lane;
     if (a.dq && dtid < 256) sh.code8[dtid] = __ldg(a.code8 + dtid);
+    if (BITS == 8 && dtid < 256) valtab[dtid] = __ldg(a.code4 + dtid);
     static_assert(kNumDecWarps * 32 >= 256, "one code8 entry per decoder thread");
     // Geometry of this thread's 128-byte line in the A tile and of its two 16-byte
     // chunks of packed codes.  The packed tile arrives with a TMA swizzle (32-byte
     // rows: 32B mode; 64-byte rows: 64B mode) so that a quarter-warp's chunk loads
     // fall in distinct banks.
-    int line_off, key, pk0, pk1;
+    // 8-bit codes: 64-byte rows (64B swizzle) in the forward, 128-byte rows (128B
+    // swizzle) in the input gradient; four 16-byte chunks per thread.
+    int line_off, key, pk0, pk1, pkc[4];
     if (MODE == 0) {
       line_off = (rb >> 3) * 1024 + (rb & 7) * 128;
       key = rb & 7;
       const int x = (rb >> 2) & 1;  // 32B swizzle: chunk bit 0 ^= row bit 2
       pk0 = rb * 32 + ((0 ^ x) << 4);
       pk1 = rb * 32 + ((1 ^ x) << 4);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pkc[c] = rb * 64 + ((c ^ ((rb >> 1) & 3)) << 4);
     } else {
       const int nl = rb & 63, j = rb >> 6;
       line_off = j * 8192 + (nl >> 3) * 1024 + (nl & 7) * 128;
@@ -703,6 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int x = (nl >> 1) & 3;  // 64B swizzle: chunk bits 0-1 ^= row bits 1-2
       pk0 = nl * 64 + (((2 * j) ^ x) << 4);
       pk1 = nl * 64 + (((2 * j + 1) ^ x) << 4);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pkc[c] = nl * 128 + (((4 * j + c) ^ (nl & 7)) << 4);
     }
     // The statistics of this group's steps are fetched kAhead owned steps ahead
     // into a register ring (global-memory latency hides behind the decodes in
@@ -756,9 +779,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ring[kAhead - 1] = fetch_next();
       if (!wait_phase(bar_at(sh, kBarPFull + sp), php, sh, a)) break;
       const uint8_t* pk = smem + G::kOffPk + sp * kPkStage;
-      const uint4 w0 = *reinterpret_cast<const uint4*>(pk + pk0);
-      const uint4 w1 = *reinterpret_cast<const uint4*>(pk + pk1);
-      const Lut L = make_lut(code2, s);
+      uint4 wc[4];
+      Lut L;
+      if (BITS == 4) {
+        wc[0] = *reinterpret_cast<const uint4*>(pk + pk0);
+        wc[1] = *reinterpret_cast<const uint4*>(pk + pk1);
+        L = make_lut(code2, s);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) wc[c] = *reinterpret_cast<const uint4*>(pk + pkc[c]);
+      }
       if (CG == 2) {
         if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) break;
       } else if (m >= 0) {
@@ -768,10 +798,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the MMA issuer is told the stage is ready.
       if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
       uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
-      const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      if (BITS == 4) {
+        const uint32_t wv[8] = {wc[0].x, wc[0].y, wc[0].z, wc[0].w, wc[1].x, wc[1].y, wc[1].z, wc[1].w};
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[c], L);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = decode8(wv[c], L);
+      } else {
+        // One code per byte: value = bf16(fp32(code[q] * s)) from the shared table.
+        const uint64_t s2 = (static_cast<uint64_t>(__float_as_uint(s)) << 32) | __float_as_uint(s);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // eight codes -> one 16-byte chunk of the A line
+          const uint4 w = wc[c >> 1];
+          const uint32_t lo = (c & 1) ? w.z : w.x, hi = (c & 1) ? w.w : w.y;
+          uint32_t o[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t word = p < 2 ? lo : hi;
+            const int sft = (p & 1) * 16;
+            const float f0 = valtab[(word >> sft) & 0xffu];
+            const float f1 = valtab[(word >> (sft + 8)) & 0xffu];
+            const uint64_t m = mul_f32x2(
+                (static_cast<uint64_t>(__float_as_uint(f1)) << 32) | __float_as_uint(f0), s2);
+            __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(m)),
+                                                     __uint_as_float(static_cast<uint32_t>(m >> 32)));
+            o[p] = *reinterpret_cast<uint32_t*>(&b);
+          }
+          *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -878,22 +932,22 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
-template <int MODE, int BT, int CG>
+template <int MODE, int BT, int CG, int BITS>
 cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
                        const CUtensorMap& to, int grid,
                        cudaStream_t s) {
   static bool configured = false;
-  auto kern = nf4_gemm_kernel<MODE, BT, CG>;
+  auto kern = nf4_gemm_kernel<MODE, BT, CG, BITS>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Geo<BT, CG>::kSmem);
+                                         Geo<BT, CG, BITS>::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Geo<BT, CG>::kSmem;
+  cfg.dynamicSmemBytes = Geo<BT, CG, BITS>::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -910,21 +964,42 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
 template <int MODE>
 cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta,
                         const CUtensorMap& tp, const CUtensorMap& to, int grid, cudaStream_t s) {
+#if NF4_GEMM_BITS == 4
   if (cg == 2) {
     if (bt != 256) return cudaErrorInvalidValue;
-    return launch_one<MODE, 256, 2>(a, ta, tp, to, grid, s);
+    return launch_one<MODE, 256, 2, 4>(a, ta, tp, to, grid, s);
   }
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1>(a, ta, tp, to, grid, s);
-    case 32: return launch_one<MODE, 32, 1>(a, ta, tp, to, grid, s);
-    case 64: return launch_one<MODE, 64, 1>(a, ta, tp, to, grid, s);
-    case 128: return launch_one<MODE, 128, 1>(a, ta, tp, to, grid, s);
-    case 256: return launch_one<MODE, 256, 1>(a, ta, tp, to, grid, s);
+    case 16: return launch_one<MODE, 16, 1, 4>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 1, 4>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 1, 4>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 1, 4>(a, ta, tp, to, grid, s);
+    case 256: return launch_one<MODE, 256, 1, 4>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
+#else
+  if (cg != 1) return cudaErrorInvalidValue;
+  switch (bt) {
+    case 16: return launch_one<MODE, 16, 1, 8>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 1, 8>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 1, 8>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 1, 8>(a, ta, tp, to, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+#endif
 }
 
 }  // namespace
+
+#if NF4_GEMM_BITS == 8
+// The 8-bit-code instances (this file compiled a second time, from nf4_gemm8.cu).
+cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
+                             const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
+                             cudaStream_t s) {
+  if (mode == 0) return launch_mode<0>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  return launch_mode<1>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
+}
+#else
 
 // Stream-K ready flags (zero at module load; a launch publishes its epoch).
 __device__ uint32_t g_stream_k_flags[kSkSlots * kSkMaxCtas * 4];
@@ -944,9 +1019,13 @@ uint32_t* stream_k_flags(uint32_t epoch) {
   return base + static_cast<size_t>(epoch % kSkSlots) * kSkMaxCtas * 4;
 }
 
-cudaError_t launch_gemm(int mode, int bt, int cg, const GemmArgs& a, const CUtensorMap& tmap_act,
-                        const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(int mode, int bt, int cg, int bits, const GemmArgs& a,
+                        const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,
+                        const CUtensorMap& tmap_out, int grid, cudaStream_t s) {
+  if (bits == 8) {
+    if (cg != 1) return cudaErrorInvalidValue;
+    return launch_gemm_8bit(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  }
   if (mode == 0) return launch_mode<0>(bt, cg, a, tmap_act, tmap_packed, tmap_out, grid, s);
   return launch_mode<1>(bt, cg, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
@@ -975,5 +1054,7 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, splits, M, ncols, out, ld);
 }
+
+#endif  // NF4_GEMM_BITS
 
 }  // namespace nf4

@@ -1,5 +1,5 @@
-// nf4_quant.cu -- blockwise NF4 quantisation (with double quantisation of the
-// absmax statistics) and dense dequantisation.
+// nf4_quant.cu -- blockwise NF4 (and 8-bit) quantisation, with double
+// quantisation of the absmax statistics, and dense dequantisation.
 //
 // quantize_4bit(w, blocksize=64, quant_type="nf4", compress_statistics=True) and
 // dequantize_4bit(B, state) of bitsandbytes issue "MatMul4Bit keeps B and
@@ -84,6 +84,45 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(const T* __restric
       q1 = has1 ? count_below(mid, 15, __fdiv_rn(v1, a)) : 0;
     }
     if (has0) packed[e0 >> 1] = static_cast<uint8_t>((q0 << 4) | q1);
+  }
+}
+
+// 8-bit storage (one code per byte, 256-level codebook): the same block steps as
+// above.  One warp per block of 64 values; lane l owns values 2l and 2l+1.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize8_blocks_kernel(const T* __restrict__ W, int64_t numel,
+                                                                const float* __restrict__ code,
+                                                                uint8_t* __restrict__ codes,
+                                                                float* __restrict__ absmax) {
+  __shared__ double mid[255];
+  __shared__ int zero_idx;
+  for (int j = threadIdx.x; j < 255; j += blockDim.x)
+    mid[j] = __dmul_rn(__dadd_rn(static_cast<double>(code[j]), static_cast<double>(code[j + 1])), 0.5);
+  if (threadIdx.x == 0) {
+    int z = 0;
+    for (int j = 255; j >= 0; --j)
+      if (code[j] == 0.0f) z = j;
+    zero_idx = z;
+  }
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int64_t nblocks = (numel + 63) / 64;
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t blk = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       blk < nblocks; blk += warps_total) {
+    const int64_t e0 = blk * 64 + 2 * lane;
+    const bool has0 = e0 < numel, has1 = e0 + 1 < numel;
+    const float v0 = has0 ? load_as_f32(W, e0) : 0.0f;
+    const float v1 = has1 ? load_as_f32(W, e0 + 1) : 0.0f;
+    float a = fmaxf(has0 ? fabsf(v0) : 0.0f, has1 ? fabsf(v1) : 0.0f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) absmax[blk] = a;
+    const int q0 = a == 0.0f ? zero_idx : count_below(mid, 255, __fdiv_rn(v0, a));
+    const int q1 = a == 0.0f ? zero_idx : count_below(mid, 255, __fdiv_rn(v1, a));
+    if (has0) codes[e0] = static_cast<uint8_t>(q0);
+    if (has1) codes[e0 + 1] = static_cast<uint8_t>(q1);
   }
 }
 
@@ -180,6 +219,24 @@ __global__ void __launch_bounds__(256) dequantize_kernel(nf4_weight w, int64_t n
   }
 }
 
+// 8-bit storage: one thread per value.
+template <typename OutT>
+__global__ void __launch_bounds__(256) dequantize8_kernel(nf4_weight w, int64_t numel, OutT* __restrict__ out) {
+  __shared__ float code_s[256];
+  __shared__ float code8_s[256];
+  for (int j = threadIdx.x; j < 256; j += blockDim.x) {
+    code_s[j] = w.code4[j];
+    if (w.double_quant) code8_s[j] = w.code8[j];
+  }
+  __syncthreads();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < numel;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float f = __fmul_rn(code_s[w.packed[i]], block_scale(w, i / w.blocksize, code8_s));
+    if constexpr (sizeof(OutT) == 4) out[i] = f;
+    else out[i] = __float2bfloat16_rn(f);
+  }
+}
+
 int grid_for(int64_t work, int per_block) {
   int64_t g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -202,6 +259,19 @@ cudaError_t launch_quantize(const void* W, int w_dtype, int64_t numel, const flo
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize8(const void* W, int w_dtype, int64_t numel, const float* code,
+                             uint8_t* codes, float* absmax, cudaStream_t s) {
+  const int64_t nblocks = (numel + 63) / 64;
+  const int grid = grid_for(nblocks, 8);
+  if (w_dtype == NF4_DTYPE_F32)
+    quantize8_blocks_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(W), numel, code,
+                                                         codes, absmax);
+  else
+    quantize8_blocks_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(W), numel, code, codes, absmax);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_double_quant(const float* absmax, int64_t nblocks, const float* code8,
                                 uint8_t* absmax_q, float* nested_absmax, float* nested_offset,
                                 double* chunk_ws, cudaStream_t s) {
@@ -220,6 +290,14 @@ cudaError_t launch_double_quant(const float* absmax, int64_t nblocks, const floa
 
 cudaError_t launch_dequantize(const nf4_weight& w, void* out, int out_dtype, cudaStream_t s) {
   const int64_t numel = w.N * w.K;
+  if (w.bits == 8) {
+    const int grid8 = grid_for(numel, 256 * 4);
+    if (out_dtype == NF4_DTYPE_F32)
+      dequantize8_kernel<float><<<grid8, 256, 0, s>>>(w, numel, static_cast<float*>(out));
+    else
+      dequantize8_kernel<__nv_bfloat16><<<grid8, 256, 0, s>>>(w, numel, static_cast<__nv_bfloat16*>(out));
+    return cudaGetLastError();
+  }
   const int grid = grid_for((numel + 1) / 2, 256 * 4);
   if (out_dtype == NF4_DTYPE_F32)
     dequantize_kernel<float><<<grid, 256, 0, s>>>(w, numel, static_cast<float*>(out));

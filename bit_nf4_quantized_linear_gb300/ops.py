@@ -50,6 +50,12 @@ class NF4Weight:
     K: int
     double_quant: bool
 
+    @property
+    def bits(self) -> int:
+        """Code width: 4 (packed nibbles, 16-level code4) or 8 (one code per byte,
+        256-level code4)."""
+        return 8 if self.code4.numel() == 256 else 4
+
     def struct(self) -> _lib.nf4_weight:
         return _lib.nf4_weight(
             _ptr(self.packed), _ptr(self.absmax) if not self.double_quant else None,
@@ -57,7 +63,8 @@ class NF4Weight:
             _ptr(self.nested_absmax) if self.double_quant else None,
             _ptr(self.nested_offset) if self.double_quant else None,
             _ptr(self.code4), _ptr(self.code8) if self.double_quant else None,
-            self.N, self.K, BLOCKSIZE, NESTED_BLOCKSIZE, 1 if self.double_quant else 0)
+            self.N, self.K, BLOCKSIZE, NESTED_BLOCKSIZE, 1 if self.double_quant else 0,
+            self.bits)
 
     def tensors(self) -> tuple:
         """The tensors a backward needs, in a fixed order (for save_for_backward)."""
@@ -82,8 +89,10 @@ def workspace_size(op: int, M: int, N: int, K: int, E: int = 0) -> int:
 
 def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.Tensor] = None,
              code8: Optional[torch.Tensor] = None, quant_type: str = "nf4") -> NF4Weight:
-    """nf4_quantize: blockwise 4-bit (+ double quantisation) of a CUDA fp32/bf16 [N, K].
-    `quant_type` ("nf4" or "fp4") picks the default codebook when `code4` is None."""
+    """nf4_quantize / nf4_quantize_8bit: blockwise quantisation (+ double quantisation
+    of the absmax) of a CUDA fp32/bf16 [N, K].  `quant_type` picks the storage and the
+    default codebook: "nf4", "fp4" (packed 4-bit), "int8", "fp8" (one byte per
+    value).  A given `code4` (16 or 256 levels) overrides the codebook."""
     _need_cuda("quantize", W)
     if W.dim() != 2 or not W.is_contiguous():
         raise ValueError("quantize: W must be a contiguous [N, K] tensor")
@@ -93,9 +102,12 @@ def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.T
     N, K = W.shape
     numel = N * K
     nblocks = (numel + BLOCKSIZE - 1) // BLOCKSIZE
-    code4 = (codebooks.code4_for(quant_type) if code4 is None else code4).to(dev, torch.float32).contiguous()
+    code4 = (codebooks.code_for(quant_type) if code4 is None else code4).to(dev, torch.float32).contiguous()
+    if code4.numel() not in (16, 256):
+        raise ValueError("quantize: the value codebook must have 16 or 256 levels")
+    bits = 8 if code4.numel() == 256 else 4
     code8 = (codebooks.dynamic_code8() if code8 is None else code8).to(dev, torch.float32).contiguous()
-    packed = torch.empty((numel + 1) // 2, dtype=torch.uint8, device=dev)
+    packed = torch.empty(numel if bits == 8 else (numel + 1) // 2, dtype=torch.uint8, device=dev)
     absmax = torch.empty(nblocks, dtype=torch.float32, device=dev)
     absmax_q = nested = offset = ws = None
     ws_bytes = 0
@@ -106,7 +118,8 @@ def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.T
         offset = torch.empty(1, dtype=torch.float32, device=dev)
         ws_bytes = workspace_size(_lib.OP_QUANTIZE, 0, N, K)
         ws = torch.empty(max(ws_bytes, 8), dtype=torch.uint8, device=dev)
-    rc = _lib.lib().nf4_quantize(
+    fn = _lib.lib().nf4_quantize_8bit if bits == 8 else _lib.lib().nf4_quantize
+    rc = fn(
         _ptr(W), _lib.DTYPE_F32 if W.dtype == torch.float32 else _lib.DTYPE_BF16, N, K, BLOCKSIZE,
         1 if double_quant else 0, NESTED_BLOCKSIZE, _ptr(code4), _ptr(code8) if double_quant else None,
         _ptr(packed), _ptr(absmax), _ptr(absmax_q), _ptr(nested), _ptr(offset), _ptr(ws), ws_bytes,

@@ -120,6 +120,10 @@ typedef struct {
   int32_t blocksize;        /* must be 64 */
   int32_t nested_blocksize; /* must be 256 when double_quant */
   int32_t double_quant;     /* 0 or 1 */
+  int32_t bits;             /* code width: 4 (or 0, meaning 4) or 8.  With 8 the
+                             * codes are one byte per value, packed [N*K], and
+                             * code4 is the [256] value codebook (blockwise int8
+                             * dynamic map or e4m3 levels) */
 } nf4_weight;
 
 /* nf4_quantize -- blockwise NF4 quantisation of W (quantize_4bit of bitsandbytes
@@ -142,6 +146,20 @@ nf4_status nf4_quantize(const void* W, int32_t w_dtype, int64_t N, int64_t K, in
                         const float* code8, uint8_t* packed, float* absmax, uint8_t* absmax_q,
                         float* nested_absmax, float* nested_offset, void* ws, size_t ws_bytes,
                         void* stream);
+
+/* nf4_quantize_8bit -- blockwise 8-bit storage of W, one code per byte (fork PR
+ * "Experts trainability", commit 1, quant_type table: "int8: blockwise dynamic
+ * map, 1 byte/value"; "fp8: e4m3 codebook, same blockwise path").  The same steps
+ * and outputs as nf4_quantize with a 256-level codebook `code` (ascending, with
+ * an exact zero; the e4m3 levels repeat only the signed zero) and codes [N*K]
+ * instead of packed nibbles; double quantisation of the absmax as there.  The
+ * products, dequantisation and grouped calls take the result as an nf4_weight
+ * with bits = 8, packed = codes and code4 = code. */
+nf4_status nf4_quantize_8bit(const void* W, int32_t w_dtype, int64_t N, int64_t K,
+                             int32_t blocksize, int32_t double_quant, int32_t nested_blocksize,
+                             const float* code, const float* code8, uint8_t* codes,
+                             float* absmax, uint8_t* absmax_q, float* nested_absmax,
+                             float* nested_offset, void* ws, size_t ws_bytes, void* stream);
 
 /* nf4_dequantize -- dense dequantisation of a quantised weight (dequantize_4bit,
  * bitsandbytes issue "MatMul4Bit keeps B and quant_state on ctx", "Root cause").

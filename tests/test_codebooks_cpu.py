@@ -7,7 +7,7 @@ from oracle import codebooks as ocb
 import bit_nf4_quantized_linear_gb300 as nf4
 
 
-@pytest.mark.parametrize("name", ["nf4_code4", "fp4_code4", "dynamic_code8"])
+@pytest.mark.parametrize("name", ["nf4_code4", "fp4_code4", "dynamic_code8", "e4m3_code8"])
 def test_library_codebooks_equal_oracle_bits(name):
     lib = getattr(nf4, name)().numpy()
     ref = getattr(ocb, name)()
@@ -21,3 +21,11 @@ def test_code4_for_quant_type():
                                   ocb.fp4_code4().view(np.uint32))
     with pytest.raises(ValueError):
         nf4.code4_for("int4")
+
+
+def test_code_for_every_quant_type():
+    for qt, ref in (("nf4", ocb.nf4_code4()), ("fp4", ocb.fp4_code4()),
+                    ("int8", ocb.dynamic_code8()), ("fp8", ocb.e4m3_code8())):
+        np.testing.assert_array_equal(nf4.code_for(qt).numpy().view(np.uint32), ref.view(np.uint32))
+    with pytest.raises(ValueError):
+        nf4.code_for("nf8")

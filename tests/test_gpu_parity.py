@@ -478,3 +478,97 @@ def test_stream_k_off_and_on_agree_within_tolerance(restore_stream_k):
     rms = ys[0].pow(2).mean().sqrt()
     bound = torch.maximum(ys[0].abs(), ys[1].abs()) * 2.0 ** -7 + 1e-4 * rms
     assert bool(((ys[0] - ys[1]).abs() <= bound).all())
+
+
+# ------------------------------------------------------- 8-bit weight storage --
+# "int8" (blockwise dynamic map) and "fp8" (e4m3 levels): one code per byte, the
+# same blockwise statistics, the fused tcgen05 kernel at every M.
+
+def _quant_pair_8bit(N, K, dq, quant_type, seed=0):
+    g = synth.generator(seed)
+    w32 = synth.weight(N, K, g)
+    w = nf4.quantize(w32.to(DEV), double_quant=dq, quant_type=quant_type)
+    code = ocb.dynamic_code8() if quant_type == "int8" else ocb.e4m3_code8()
+    st = oracle.quantize(w32.numpy(), code, 64, dq, ocb.dynamic_code8(), 256)
+    return w, st, g
+
+
+@pytest.mark.parametrize("quant_type", ["int8", "fp8"])
+@pytest.mark.parametrize("N,K,dq", [(256, 512, True), (1000, 1344, False), (3, 100, True)])
+def test_8bit_quantize_dequantize_bit_exact(quant_type, N, K, dq):
+    w, st, _ = _quant_pair_8bit(N, K, dq, quant_type, seed=N + K)
+    assert w.bits == 8 and w.packed.numel() == N * K
+    torch.cuda.synchronize()
+    _assert_state_equal(w, st)
+    f32 = nf4.dequantize(w, torch.float32).cpu().numpy().reshape(-1)
+    b16 = bf16_bits(nf4.dequantize(w, torch.bfloat16)).reshape(-1)
+    np.testing.assert_array_equal(f32.view(np.uint32), oracle.dequantize(st, "f32").reshape(-1).view(np.uint32))
+    np.testing.assert_array_equal(b16, oracle.dequantize(st, "bf16").reshape(-1))
+
+
+@pytest.mark.parametrize("quant_type", ["int8", "fp8"])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (16, 384, 512), (40, 320, 192), (129, 384, 320),
+                                   (300, 640, 1024), (700, 640, 1024)])
+def test_8bit_fwd_dgrad_parity_and_reruns(quant_type, M, N, K):
+    w, st, g = _quant_pair_8bit(N, K, True, quant_type, seed=M + N + K)
+    x = synth.activation(M, K, g).to(DEV)
+    gy = synth.activation(M, N, g).to(DEV)
+    wb = oracle.dequantize(st, "bf16")
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x, w)
+    gx = nf4.linear_dgrad(gy, w)
+    c = nf4.path_counters()
+    assert c["linear_fwd"] == 1 and c["linear_dgrad"] == 1, c
+    parity(y, oracle.linear_fwd(bf16_bits(x.cpu()), wb), f"{quant_type} fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy.cpu()), wb), f"{quant_type} dgrad {M}x{N}x{K}")
+    for _ in range(3):
+        assert torch.equal(nf4.linear_fwd(x, w).view(torch.int16), y.view(torch.int16))
+        assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx.view(torch.int16))
+
+
+@pytest.mark.parametrize("quant_type", ["int8", "fp8"])
+def test_8bit_identity_probes_exact(quant_type):
+    # One-hot rows select single dequantised weights (values; a -0 weight of the
+    # e4m3 table sums to +0): the in-kernel 8-bit decode, both operand layouts.
+    N, K = 384, 256
+    w, st, _ = _quant_pair_8bit(N, K, True, quant_type, seed=9)
+    wbf = torch.from_numpy(oracle.dequantize(st, "bf16").view(np.int16)).view(torch.bfloat16).float().numpy()
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    y = nf4.linear_fwd(eye.to(DEV), w).float().cpu().numpy()
+    np.testing.assert_array_equal(y, np.ascontiguousarray(wbf.T))
+    eyeN = torch.eye(N, dtype=torch.bfloat16)
+    gx = nf4.linear_dgrad(eyeN.to(DEV), w).float().cpu().numpy()
+    np.testing.assert_array_equal(gx, wbf)
+
+
+def test_8bit_stream_k_and_grouped(restore_stream_k):
+    ops.set_stream_k(_lib.STREAM_K_FORCE)
+    M, N, K = 300, 640, 1024
+    w, st, g = _quant_pair_8bit(N, K, True, "int8", seed=21)
+    x = synth.activation(M, K, g).to(DEV)
+    wb = oracle.dequantize(st, "bf16")
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x, w)
+    assert nf4.path_counters()["stream_k"] == 1
+    parity(y, oracle.linear_fwd(bf16_bits(x.cpu()), wb), "int8 stream-K fwd")
+    ops.set_stream_k(_lib.STREAM_K_AUTO)
+    # grouped: 4 experts of 128 rows over one stacked weight, ragged token counts
+    E, Ne = 4, 128
+    wg, stg, g = _quant_pair_8bit(E * Ne, 256, True, "fp8", seed=22)
+    counts = [5, 0, 40, 19]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    T = int(offs[-1])
+    xg = synth.activation(T, 256, g)
+    gyg = synth.activation(T, Ne, g)
+    wbg = oracle.dequantize(stg, "bf16")
+    yg = nf4.grouped_fwd(xg.to(DEV), torch.from_numpy(offs).to(DEV), wg, E)
+    gxg = nf4.grouped_dgrad(gyg.to(DEV), torch.from_numpy(offs).to(DEV), wg, E)
+    xb, gyb = bf16_bits(xg), bf16_bits(gyg)
+    yref = np.zeros((T, Ne)); gref = np.zeros((T, 256))
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        if r1 > r0:
+            yref[r0:r1] = oracle.linear_fwd(xb[r0:r1], wbg[e * Ne:(e + 1) * Ne])
+            gref[r0:r1] = oracle.linear_dgrad(gyb[r0:r1], wbg[e * Ne:(e + 1) * Ne])
+    parity(yg, yref, "fp8 grouped fwd")
+    parity(gxg, gref, "fp8 grouped dgrad")

@@ -49,9 +49,10 @@ def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
         after = nf4.path_counters()
         assert after["total"] > before["total"]
         parity(y, ref.double().cpu().numpy(), f"noalloc call {call} M={M}")
-    # the small-M cases really exercise the scratch (split contraction)
-    if ops.workspace_size(_lib.OP_LINEAR_FWD, M, N, K) > 0:
-        assert nf4.path_counters()["splitk_reduce"] > 0
+        # a small-M call on the tiled kernel really exercises the scratch (split
+        # contraction, summed by the reduction kernel)
+        if M <= 32 and after["linear_fwd"] > before["linear_fwd"]:
+            assert after["splitk_reduce"] > before["splitk_reduce"]
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
