@@ -310,10 +310,11 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_val = job_throughput(flops, world, e2e_ms)
 
-    sweep = grouped = None
+    sweep = grouped = storage8 = None
     if rank == 0 and world == 1 and not args.no_sweep:
         sweep = run_sweep(dev, pk)
         grouped = run_grouped(dev, pk)
+        storage8 = run_storage8(dev, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -359,6 +360,8 @@ def run_ours(args, rank, world, local_rank):
         out["m_sweep_4096"] = sweep
     if grouped is not None:
         out["grouped_olmoe"] = grouped
+    if storage8 is not None:
+        out["storage_8bit_4096"] = storage8
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
@@ -476,6 +479,70 @@ def run_sweep(dev, pk):
         del reps, x, gy, y, gx, wsb
         torch.cuda.empty_cache()
     return res
+
+
+def run_storage8(dev, pk):
+    """One-byte storage ("int8" dynamic map, "fp8" e4m3 levels) at K = N = 4096,
+    double-quant statistics: fwd + dgrad through the fused kernel, each point a CUDA
+    graph of back-to-back calls over weight replicas (>= 4 x L2 at small M)."""
+    import torch
+    import bit_nf4_quantized_linear_gb300 as nf4
+    from bit_nf4_quantized_linear_gb300 import ops, synth
+    N = K = 4096
+    out = {}
+    for qt in ("int8", "fp8"):
+        g = synth.generator(2)
+        base = nf4.quantize(synth.weight(N, K, g).to(dev), double_quant=True, quant_type=qt)
+        wbytes = base.nbytes()
+        rows = []
+        for M in (1, 16, 512, 4096):
+            R = max(2, min(32, int(4 * L2_BYTES / wbytes) + 1)) if M <= 16 else 4
+            reps = [base] + [nf4.NF4Weight(base.packed.clone(), None, base.absmax_q.clone(),
+                                           base.nested_absmax.clone(), base.nested_offset.clone(),
+                                           base.code4, base.code8, N, K, True) for _ in range(R - 1)]
+            x = synth.activation(M, K, g).to(dev)
+            gy = synth.activation(M, N, g).to(dev)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            gx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+            wsz = max(ops.workspace_size(1, M, N, K), ops.workspace_size(2, M, N, K), 16)
+            wsb = torch.empty(wsz, dtype=torch.uint8, device=dev)
+            s = torch.cuda.Stream(dev)
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for w in reps[:2]:
+                    ops.linear_fwd(x, w, out=y, ws=wsb)
+                    ops.linear_dgrad(gy, w, out=gx, ws=wsb)
+            torch.cuda.synchronize()
+            ts = []
+            for op in (lambda w: ops.linear_fwd(x, w, out=y, ws=wsb),
+                       lambda w: ops.linear_dgrad(gy, w, out=gx, ws=wsb)):
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=s):
+                    for w in reps:
+                        op(w)
+                for _ in range(3):
+                    graph.replay()
+                torch.cuda.synchronize()
+                times = []
+                for _ in range(10):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    graph.replay()
+                    b.record()
+                    b.synchronize()
+                    times.append(a.elapsed_time(b) / R)
+                ts.append(statistics.median(times) * 1e-3)
+                del graph
+            t = ts[0] + ts[1]
+            tfl = 4.0 * M * N * K / t / 1e12
+            gbs = 2.0 * wbytes / t / 1e9
+            rows.append({"M": M, "us_fwd": round(ts[0] * 1e6, 2), "us_dgrad": round(ts[1] * 1e6, 2),
+                         "tflops": round(tfl, 2), "frac_tc": round(tfl / pk["bf16_tflops"], 4),
+                         "weight_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
+            del reps, x, gy, y, gx, wsb
+            torch.cuda.empty_cache()
+        out[qt] = {"weight_bytes": wbytes, "rows": rows}
+    return out
 
 
 def run_grouped(dev, pk):
