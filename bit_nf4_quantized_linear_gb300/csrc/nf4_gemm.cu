@@ -66,12 +66,13 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // bound of every wait (2 s)
 constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up to 20 us per try
 
 // BITS = 4: two codes per byte (packed nibbles, 16-level codebook in registers);
-// BITS = 8: one code per byte (256-level codebook in shared memory, after the
-// base misc region).
+// BITS = 8: one code per byte (256-level codebook in shared memory after the base
+// misc region, one copy per lane: entry e of lane l in word 32 e + l, so the
+// lookups of a warp never share a bank).
 template <int BT, int CG, int BITS>
 struct Geo {
   static constexpr int kPkStage = kTileW * kTileK * BITS / 8;  // codes of one step: 4 or 8 KB
-  static constexpr int kMiscBytes = kMiscBase + (BITS == 8 ? 1024 : 0);
+  static constexpr int kMiscBytes = kMiscBase + (BITS == 8 ? 256 * 32 * 4 : 0);
   static constexpr int kXStage = (BT / CG) * 128;  // this CTA's BT/CG token rows of 64 bf16
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
   // Decoded operand tiles: one slot more than decoder groups where the activation
@@ -700,7 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* valtab = reinterpret_cast<float*>(smem + G::kOffMisc + kMiscBase);
     const int dtid = dw * 32 + lane;
     if (a.dq && dtid < 256) sh.code8[dtid] = __ldg(a.code8 + dtid);
-    if (BITS == 8 && dtid < 256) valtab[dtid] = __ldg(a.code4 + dtid);
+    if (BITS == 8)
+      for (int i = dtid; i < 256 * 32; i += kNumDecWarps * 32) valtab[i] = __ldg(a.code4 + (i >> 5));
+    const float* vt = valtab + lane;  // this lane's copy: entry e at vt[32 e]
     static_assert(kNumDecWarps * 32 >= 256, "one code8 entry per decoder thread");
     // Geometry of this thread's 128-byte line in the A tile and of its two 16-byte
     // chunks of packed codes.  The packed tile arrives with a TMA swizzle (32-byte
@@ -815,8 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int p = 0; p < 4; ++p) {
             const uint32_t word = p < 2 ? lo : hi;
             const int sft = (p & 1) * 16;
-            const float f0 = valtab[(word >> sft) & 0xffu];
-            const float f1 = valtab[(word >> (sft + 8)) & 0xffu];
+            const float f0 = vt[((word >> sft) & 0xffu) * 32];
+            const float f1 = vt[((word >> (sft + 8)) & 0xffu) * 32];
             const uint64_t m = mul_f32x2(
                 (static_cast<uint64_t>(__float_as_uint(f1)) << 32) | __float_as_uint(f0), s2);
             __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(m)),
