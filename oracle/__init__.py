@@ -66,10 +66,18 @@ def lib():
             L.oracle_linear_dgrad.argtypes = [P, i64, i64, P, i64, P, i64, P]
             L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
             L.oracle_bf16_from_f32.restype = ctypes.c_uint16
+            L.oracle_f16_from_f32.argtypes = [ctypes.c_float]
+            L.oracle_f16_from_f32.restype = ctypes.c_uint16
+            L.oracle_f32_from_f16.argtypes = [ctypes.c_uint16]
+            L.oracle_f32_from_f16.restype = ctypes.c_float
+            L.oracle_f16_array.argtypes = [P, i64, P]
+            L.oracle_linear_fwd_f16.argtypes = [P, i64, i64, P, i64, P, i64, P]
+            L.oracle_linear_dgrad_f16.argtypes = [P, i64, i64, P, i64, P, i64, P]
             L.oracle_num_threads.restype = ctypes.c_int
             for name in ("oracle_quantize_nf4", "oracle_double_quant", "oracle_decode_absmax",
                          "oracle_dequantize_nf4", "oracle_linear_fwd", "oracle_linear_dgrad",
-                         "oracle_quantize_8bit", "oracle_dequantize_8bit"):
+                         "oracle_quantize_8bit", "oracle_dequantize_8bit", "oracle_f16_array",
+                         "oracle_linear_fwd_f16", "oracle_linear_dgrad_f16"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -237,9 +245,23 @@ def dequantize(st: QuantState, dtype: str = "bf16") -> np.ndarray:
 
 # ------------------------------------------------------------- products ----
 
-def linear_fwd(x_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None) -> np.ndarray:
-    """y = x W^T in fp64 from bf16 bit patterns x [M,K] and Wb [N,K]; only `rows` of y
-    when given."""
+def f16_bits(f: np.ndarray) -> np.ndarray:
+    """fp32 values -> IEEE binary16 bit patterns (round to nearest, ties to even)."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.zeros(f.shape, dtype=np.uint16)
+    _check(lib().oracle_f16_array(_p(f), f.size, _p(out)), "f16_array")
+    return out
+
+
+def dequantize_f16(st: QuantState) -> np.ndarray:
+    """Dense dequantised weight rounded to fp16 (bit patterns): the operand of the
+    fp16 compute dtype."""
+    return f16_bits(dequantize(st, "f32"))
+
+
+def linear_fwd(x_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None, dtype: str = "bf16") -> np.ndarray:
+    """y = x W^T in fp64 from 16-bit patterns x [M,K] and Wb [N,K] (bf16, or fp16 with
+    dtype="f16"); only `rows` of y when given."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     wb = np.ascontiguousarray(wb_bf16, dtype=np.uint16)
     M, K = x.shape
@@ -248,12 +270,14 @@ def linear_fwd(x_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None) -> np.ndarray
     r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     nrows = M if r is None else r.size
     y = np.zeros((nrows, N), dtype=np.float64)
-    _check(lib().oracle_linear_fwd(_p(x), M, K, _p(wb), N, _p(r), nrows, _p(y)), "linear_fwd")
+    fn = lib().oracle_linear_fwd_f16 if dtype == "f16" else lib().oracle_linear_fwd
+    _check(fn(_p(x), M, K, _p(wb), N, _p(r), nrows, _p(y)), "linear_fwd")
     return y
 
 
-def linear_dgrad(gy_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None) -> np.ndarray:
-    """grad_x = grad_y W in fp64 from bf16 bit patterns gy [M,N] and Wb [N,K]."""
+def linear_dgrad(gy_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None, dtype: str = "bf16") -> np.ndarray:
+    """grad_x = grad_y W in fp64 from 16-bit patterns gy [M,N] and Wb [N,K] (bf16, or
+    fp16 with dtype="f16")."""
     gy = np.ascontiguousarray(gy_bf16, dtype=np.uint16)
     wb = np.ascontiguousarray(wb_bf16, dtype=np.uint16)
     M, N = gy.shape
@@ -262,7 +286,8 @@ def linear_dgrad(gy_bf16: np.ndarray, wb_bf16: np.ndarray, rows=None) -> np.ndar
     r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     nrows = M if r is None else r.size
     gx = np.zeros((nrows, K), dtype=np.float64)
-    _check(lib().oracle_linear_dgrad(_p(gy), M, N, _p(wb), K, _p(r), nrows, _p(gx)), "linear_dgrad")
+    fn = lib().oracle_linear_dgrad_f16 if dtype == "f16" else lib().oracle_linear_dgrad
+    _check(fn(_p(gy), M, N, _p(wb), K, _p(r), nrows, _p(gx)), "linear_dgrad")
     return gx
 
 

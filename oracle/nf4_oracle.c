@@ -68,6 +68,50 @@ float oracle_f32_from_bf16(uint16_t h) {
   return f;
 }
 
+/* ---------------------------------------------------------------- fp16 ---- */
+
+/* Round an fp32 value to IEEE binary16 (round to nearest, ties to even), with
+ * subnormals and overflow to infinity: the fp16 compute dtype's operand and
+ * output rounding.  Worked in fp64, where every step below is exact except the
+ * final rint (ties to even in the default rounding mode). */
+uint16_t oracle_f16_from_f32(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)(sign | 0x7e00u); /* quiet NaN */
+  double a = fabs((double)f);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+  e -= 1;       /* a = m' * 2^e, m' in [1, 2) */
+  if (e < -14) {  /* subnormal range: multiples of 2^-24 */
+    double q = rint(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)q);  /* q == 1024 is the smallest normal */
+  }
+  double mant = rint((ldexp(a, -e) - 1.0) * 1024.0);
+  if (mant == 1024.0) {
+    mant = 0.0;
+    e += 1;
+  }
+  if (e > 15) return (uint16_t)(sign | 0x7c00u); /* infinity */
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)mant);
+}
+
+float oracle_f32_from_f16(uint16_t h) {
+  int e = (h >> 10) & 31, m = h & 1023;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp(1.0 + m / 1024.0, e - 15);
+  return (float)((h & 0x8000u) ? -v : v);
+}
+
+int oracle_f16_array(const float* in, int64_t n, uint16_t* out) {
+  if (n < 0 || (n > 0 && (!in || !out))) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_from_f32(in[i]);
+  return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------ codebooks ---- */
 
 /* A codebook must be in ascending order (nearest-level search relies on it):
@@ -275,12 +319,14 @@ int oracle_dequantize_nf4(const uint8_t* packed, const float* scale, int64_t num
 
 /* ------------------------------------------------------------- products ---- */
 
+typedef float (*decode16_fn)(uint16_t);
+
 /* Forward y[m][n] = sum_k x[m][k] * Wb[n][k], for the rows listed in `rows`
- * (all rows when rows == NULL, nrows == M).  x: bf16 [M][K]; Wb: bf16 [N][K];
- * y: fp64 [nrows][N].  Each product of two bf16 values is exact in fp64; the sum
- * runs sequentially over k. */
-int oracle_linear_fwd(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wb, int64_t N,
-                      const int64_t* rows, int64_t nrows, double* y) {
+ * (all rows when rows == NULL, nrows == M).  x: [M][K] and Wb: [N][K] as 16-bit
+ * patterns (bf16, or fp16 for the fp16 compute dtype); y: fp64 [nrows][N].  Each
+ * product of two 16-bit floats is exact in fp64; the sum runs sequentially over k. */
+static int linear_fwd_16(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wb, int64_t N,
+                         const int64_t* rows, int64_t nrows, double* y, decode16_fn dec) {
   if (M < 0 || K < 0 || N < 0 || nrows < 0 || !y) return ORACLE_ERR_ARG;
   if (!rows && nrows != M) return ORACLE_ERR_ARG;
   for (int64_t r = 0; r < nrows; ++r) {
@@ -292,18 +338,17 @@ int oracle_linear_fwd(const uint16_t* x, int64_t M, int64_t K, const uint16_t* w
     int64_t m = rows ? rows[r] : r;
     for (int64_t n = 0; n < N; ++n) {
       double s = 0.0;
-      for (int64_t k = 0; k < K; ++k)
-        s += (double)oracle_f32_from_bf16(x[m * K + k]) * (double)oracle_f32_from_bf16(wb[n * K + k]);
+      for (int64_t k = 0; k < K; ++k) s += (double)dec(x[m * K + k]) * (double)dec(wb[n * K + k]);
       y[r * N + n] = s;
     }
   }
   return ORACLE_OK;
 }
 
-/* Input gradient gx[m][k] = sum_n gy[m][n] * Wb[n][k] for the listed rows.
- * gy: bf16 [M][N]; Wb: bf16 [N][K]; gx: fp64 [nrows][K].  Sequential sum over n. */
-int oracle_linear_dgrad(const uint16_t* gy, int64_t M, int64_t N, const uint16_t* wb, int64_t K,
-                        const int64_t* rows, int64_t nrows, double* gx) {
+/* Input gradient gx[m][k] = sum_n gy[m][n] * Wb[n][k] (rows of gx as above);
+ * gy: [M][N], Wb: [N][K] 16-bit patterns; gx: fp64 [nrows][K]; sequential over n. */
+static int linear_dgrad_16(const uint16_t* gy, int64_t M, int64_t N, const uint16_t* wb, int64_t K,
+                           const int64_t* rows, int64_t nrows, double* gx, decode16_fn dec) {
   if (M < 0 || K < 0 || N < 0 || nrows < 0 || !gx) return ORACLE_ERR_ARG;
   if (!rows && nrows != M) return ORACLE_ERR_ARG;
   for (int64_t r = 0; r < nrows; ++r) {
@@ -315,12 +360,31 @@ int oracle_linear_dgrad(const uint16_t* gy, int64_t M, int64_t N, const uint16_t
     int64_t m = rows ? rows[r] : r;
     for (int64_t k = 0; k < K; ++k) {
       double s = 0.0;
-      for (int64_t n = 0; n < N; ++n)
-        s += (double)oracle_f32_from_bf16(gy[m * N + n]) * (double)oracle_f32_from_bf16(wb[n * K + k]);
+      for (int64_t n = 0; n < N; ++n) s += (double)dec(gy[m * N + n]) * (double)dec(wb[n * K + k]);
       gx[r * K + k] = s;
     }
   }
   return ORACLE_OK;
+}
+
+int oracle_linear_fwd(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wb, int64_t N,
+                      const int64_t* rows, int64_t nrows, double* y) {
+  return linear_fwd_16(x, M, K, wb, N, rows, nrows, y, oracle_f32_from_bf16);
+}
+
+int oracle_linear_dgrad(const uint16_t* gy, int64_t M, int64_t N, const uint16_t* wb, int64_t K,
+                        const int64_t* rows, int64_t nrows, double* gx) {
+  return linear_dgrad_16(gy, M, N, wb, K, rows, nrows, gx, oracle_f32_from_bf16);
+}
+
+int oracle_linear_fwd_f16(const uint16_t* x, int64_t M, int64_t K, const uint16_t* wb, int64_t N,
+                          const int64_t* rows, int64_t nrows, double* y) {
+  return linear_fwd_16(x, M, K, wb, N, rows, nrows, y, oracle_f32_from_f16);
+}
+
+int oracle_linear_dgrad_f16(const uint16_t* gy, int64_t M, int64_t N, const uint16_t* wb, int64_t K,
+                            const int64_t* rows, int64_t nrows, double* gx) {
+  return linear_dgrad_16(gy, M, N, wb, K, rows, nrows, gx, oracle_f32_from_f16);
 }
 
 /* Number of OpenMP threads the products above run on. */

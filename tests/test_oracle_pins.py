@@ -494,3 +494,41 @@ def test_mean_offset_sums_in_fp64():
     absmax = np.array([2.0 ** 24] + [1.0] * 1023, np.float32)
     _, _, off = oracle.double_quant(absmax, LIN8)
     assert off.tolist() == [16385.0]
+
+
+# ------------------------------------------------------------- fp16 dtype ----
+
+@pytest.mark.parametrize("value,bits", [
+    (1.0, 0x3C00), (65504.0, 0x7BFF), (65520.0, 0x7C00), (65519.996, 0x7BFF),
+    (2.0 ** -24, 0x0001), (2.0 ** -25, 0x0000), (1.5 * 2.0 ** -25, 0x0001), (3 * 2.0 ** -25, 0x0002),
+    (1 + 2.0 ** -11, 0x3C00), (1 + 3 * 2.0 ** -11, 0x3C02), (-2.5, 0xC100), (0.1, 0x2E66),
+    (6.1e-5, 0x03FF), (1e-8, 0x0000)])
+def test_f16_round_to_nearest_even_literals(value, bits):
+    # ties to even at the subnormal and normal boundaries, overflow at the half-ulp
+    # above 65504, subnormals down to 2^-24
+    assert int(oracle.f16_bits(np.array([value], np.float32))[0]) == bits
+
+
+def test_f16_rounding_matches_numpy_and_decodes_every_pattern():
+    rng = np.random.default_rng(14)
+    r = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 12, 200000))).astype(np.float32)
+    with np.errstate(over="ignore"):
+        ref = r.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(oracle.f16_bits(r), ref)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = (pats & 0x7C00) != 0x7C00
+    dec = np.array([oracle.lib().oracle_f32_from_f16(int(h)) for h in pats[finite]], np.float32)
+    np.testing.assert_array_equal(dec, pats[finite].view(np.float16).astype(np.float32))
+    np.testing.assert_array_equal(oracle.f16_bits(dec), pats[finite])
+
+
+def test_f16_products_brute_force_vs_numpy():
+    rng = np.random.default_rng(15)
+    x = rng.standard_normal((5, 40)).astype(np.float16)
+    w = (rng.standard_normal((7, 40)) * 0.05).astype(np.float16)
+    gy = rng.standard_normal((5, 7)).astype(np.float16)
+    xb, wb, gb = x.view(np.uint16), w.view(np.uint16), gy.view(np.uint16)
+    np.testing.assert_allclose(oracle.linear_fwd(xb, wb, dtype="f16"),
+                               x.astype(np.float64) @ w.astype(np.float64).T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle.linear_dgrad(gb, wb, dtype="f16"),
+                               gy.astype(np.float64) @ w.astype(np.float64), rtol=1e-13, atol=1e-13)
