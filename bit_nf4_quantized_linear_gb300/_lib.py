@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
             "nf4_dequantize": [W, P, I32, P],
             "nf4_linear_fwd": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_linear_dgrad": [P, I64, I64, W, P, I64, P, SZ, P],
+            "nf4_linear_fwd_f16": [P, I64, I64, W, P, I64, P, SZ, P],
+            "nf4_linear_dgrad_f16": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_grouped_fwd": [P, P, I32, I64, I64, W, I64, P, I64, P],
             "nf4_grouped_dgrad": [P, P, I32, I64, I64, W, I64, P, I64, P],
             "nf4_workspace_size": [I32, I64, I64, I64, I32],

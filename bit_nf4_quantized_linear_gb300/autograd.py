@@ -72,9 +72,13 @@ class NF4GroupedFn(torch.autograd.Function):
 
 
 def nf4_linear(x: torch.Tensor, w: ops.NF4Weight) -> torch.Tensor:
-    """Frozen NF4 Linear: the compute dtype is bf16; other input dtypes are cast in
-    and the output is cast back (the casts are ordinary autograd ops)."""
+    """Frozen NF4 Linear: the compute dtype is the activations' half-precision type,
+    bf16 or fp16 (the dtype handling of Linear4bit, which Soup issue #842's "Design
+    sketch" keeps); other input dtypes are cast to bf16 and the output cast back (the
+    casts are ordinary autograd ops)."""
     dt = x.dtype
+    if dt == torch.float16 and w.bits == 4:
+        return NF4LinearFn.apply(x, *w.tensors(), w.N, w.K, w.double_quant)
     xb = x if dt == torch.bfloat16 else x.to(torch.bfloat16)
     y = NF4LinearFn.apply(xb, *w.tensors(), w.N, w.K, w.double_quant)
     return y if dt == torch.bfloat16 else y.to(dt)

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libnf4.so")
-SOURCES = ["nf4_api.cu", "nf4_gemm.cu", "nf4_gemm8.cu", "nf4_gemv.cu", "nf4_quant.cu", "nf4_skinny.cu"]
+SOURCES = ["nf4_api.cu", "nf4_gemm.cu", "nf4_gemm8.cu", "nf4_gemm_f16.cu", "nf4_gemv.cu", "nf4_quant.cu", "nf4_skinny.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

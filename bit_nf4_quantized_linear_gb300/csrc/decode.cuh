@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace nf4 {
@@ -25,16 +26,30 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// code2[i] holds code4[2i] (low word) and code4[2i+1] (high word).
+// Two fp32 values to a pair of 16-bit floats (the first in the low half), round to
+// nearest even: bf16, or IEEE fp16 when F16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+  }
+}
+
+// code2[i] holds code4[2i] (low word) and code4[2i+1] (high word).  Entries are
+// bf16 (or fp16 when F16) of fp32(code4[q] * s).
+template <bool F16 = false>
 __device__ __forceinline__ Lut make_lut(const uint64_t (&code2)[8], float s) {
   const uint64_t s2 = (static_cast<uint64_t>(__float_as_uint(s)) << 32) | __float_as_uint(s);
   uint32_t p[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint64_t m = mul_f32x2(code2[i], s2);
-    __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(m)),
-                                             __uint_as_float(static_cast<uint32_t>(m >> 32)));
-    p[i] = *reinterpret_cast<uint32_t*>(&b);  // T[2i] low half, T[2i+1] high half
+    p[i] = pack16x2<F16>(__uint_as_float(static_cast<uint32_t>(m)),  // T[2i] low half,
+                         __uint_as_float(static_cast<uint32_t>(m >> 32)));  // T[2i+1] high half
   }
   Lut L;
 #pragma unroll

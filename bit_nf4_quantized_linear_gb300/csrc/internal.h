@@ -140,16 +140,20 @@ cudaError_t launch_gemv_dgrad(const GemvArgs& a, cudaStream_t s);
 int gemv_fwd_kseg(int64_t K);
 int64_t gemv_dgrad_row_groups(int64_t N);
 // cg = 2 launches CTA pairs (clusters of two, tcgen05 cta_group::2; bt must be 256).
-// tmap_out: bf16 output [M, ncols] with a 32 x 32 box, used when a.tma_out is set.
-// bits: code width of the weight (4, or 8 with cg == 1 and bt <= 128).
-cudaError_t launch_gemm(int mode, int bt, int cg, int bits, const GemmArgs& a,
+// tmap_out: 16-bit output [M, ncols] with a 32 x 32 box, used when a.tma_out is set.
+// bits: code width of the weight (4, or 8 with cg == 1 and bt <= 128).  f16: fp16
+// activations, operand and output instead of bf16 (4-bit codes, cg == 1).
+cudaError_t launch_gemm(int mode, int bt, int cg, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,
                         const CUtensorMap& tmap_out, int grid, cudaStream_t s);
 cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
                              const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
                              cudaStream_t s);
+cudaError_t launch_gemm_f16(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
+                            const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
+                            cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
-                                 __nv_bfloat16* out, int64_t ld, cudaStream_t s);
+                                 void* out, int64_t ld, bool f16, cudaStream_t s);
 
 cudaError_t launch_quantize(const void* W, int w_dtype, int64_t numel, const float* code4,
                             uint8_t* packed, float* absmax, cudaStream_t s);

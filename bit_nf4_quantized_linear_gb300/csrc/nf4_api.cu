@@ -237,13 +237,15 @@ double step_cycles(int bt, int cg) {
 // model in SM clocks -- waves of items times contraction steps, plus the split
 // partials' round trip through memory.
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true,
-                int bits = 4) {
+                int bits = 4, bool f16 = false) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
   const int small = g_small_m_path.load(std::memory_order_relaxed);
   nf4::SkinnyPlan sk;
-  // 8-bit codes run the fused tcgen05 kernel at every M (tiles of <= 128 tokens).
-  if (bits == 4 && M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk)) {
+  // 8-bit codes (tiles of <= 128 tokens) and the fp16 dtype run the fused tcgen05
+  // kernel at every M.
+  const bool fused_only = bits == 8 || f16;
+  if (!fused_only && M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.skinny = true;
     p.sk = sk;
@@ -251,7 +253,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     p.ws_bytes = 0;
     return p;
   }
-  if (bits == 4 && M > 0 && small != NF4_SMALL_M_TILES &&
+  if (!fused_only && M > 0 && small != NF4_SMALL_M_TILES &&
       M <= (mode == 0 ? nf4::kGemvMaxMFwd : nf4::kGemvMaxMDgrad)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.gemv = true;
@@ -285,7 +287,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
   Plan sk_best = best;
   for (int ci = 0; ci < 4; ++ci) {
     const int bt = cand_bt[ci], cg = cand_cg[ci];
-    if (bt > bt_max || (cg == 2 && !cta_pairs_enabled())) continue;
+    if (bt > bt_max || (cg == 2 && (fused_only || !cta_pairs_enabled()))) continue;
     const int64_t ttiles = (M + bt - 1) / bt;
     const int64_t wt = (ncols + nf4::kTileW * cg - 1) / (nf4::kTileW * cg);
     const int64_t units = sms / cg;
@@ -326,7 +328,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
 
 nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const nf4_weight* w,
                      void* out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream,
-                     bool allow_sk = true) {
+                     bool allow_sk = true, bool f16 = false) {
   nf4_status st = check_weight(w);
   if (st != NF4_OK) return st;
   const int64_t N = w->N, K = w->K;
@@ -343,7 +345,8 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   const int bits = w->bits == 8 ? 8 : 4;
-  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk, bits);
+  if (f16 && bits == 8) return NF4_ERR_UNSUPPORTED;  // fp16 dtype: 4-bit codes
+  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk, bits, f16);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -403,7 +406,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     if (p.ws_bytes > 0) {
       le = nf4::launch_splitk_reduce(static_cast<const float*>(ws),
                                      static_cast<int>(nf4::gemv_dgrad_row_groups(N)), M, K,
-                                     static_cast<__nv_bfloat16*>(out), ld_out, s);
+                                     out, ld_out, false, s);
       if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
       count(NF4_PATH_SPLITK_REDUCE);
     }
@@ -411,7 +414,8 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   }
 
   CUtensorMap tmap_act, tmap_pk;
-  if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, M, ld_act * 2, 64,
+  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_2d(&tmap_act, dt16, act, act_cols, M, ld_act * 2, 64,
                  p.bt / p.cg, CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   if (!encode_codes(&tmap_pk, w, mode)) return NF4_ERR_CUDA;
@@ -458,19 +462,19 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   CUtensorMap tmap_out;
   std::memset(&tmap_out, 0, sizeof(tmap_out));
   if (p.splits == 1 && aligned16(out) && ld_out % 8 == 0) {
-    if (!encode_2d(&tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, out_cols, M, ld_out * 2, 32, 32,
+    if (!encode_2d(&tmap_out, dt16, out, out_cols, M, ld_out * 2, 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return NF4_ERR_CUDA;
     a.tma_out = 1;
   }
-  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, bits, a, tmap_act, tmap_pk, tmap_out, grid, s);
+  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, bits, f16, a, tmap_act, tmap_pk, tmap_out, grid, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
   if (p.stream_k)  // a property of the launch just counted, not a launch of its own
     g_counters[NF4_PATH_STREAM_K].fetch_add(1, std::memory_order_relaxed);
   if (p.splits > 1) {
-    le = nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols,
-                                   static_cast<__nv_bfloat16*>(out), ld_out, s);
+    le = nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols, out,
+                                   ld_out, f16, s);
     if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
     count(NF4_PATH_SPLITK_REDUCE);
   }
@@ -534,8 +538,8 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   CUtensorMap tmap_out;  // unused: expert row ranges end inside tiles (direct stores)
   std::memset(&tmap_out, 0, sizeof(tmap_out));
   a.tma_out = 0;
-  cudaError_t le = nf4::launch_gemm(mode, bt, 1, w->bits == 8 ? 8 : 4, a, tmap_act, tmap_pk,
-                                    tmap_out, dev.sms, s);
+  cudaError_t le = nf4::launch_gemm(mode, bt, 1, w->bits == 8 ? 8 : 4, false, a, tmap_act,
+                                    tmap_pk, tmap_out, dev.sms, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
   return NF4_OK;
@@ -632,6 +636,16 @@ nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_w
   return run_dense(1, gy, M, ldgy, w, gx, ldgx, ws, ws_bytes, stream);
 }
 
+nf4_status nf4_linear_fwd_f16(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
+                              int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(0, x, M, ldx, w, y, ldy, ws, ws_bytes, stream, true, true);
+}
+
+nf4_status nf4_linear_dgrad_f16(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w,
+                                void* gx, int64_t ldgx, void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(1, gy, M, ldgy, w, gx, ldgx, ws, ws_bytes, stream, true, true);
+}
+
 nf4_status nf4_grouped_fwd(const void* x, const int32_t* offsets, int32_t E, int64_t T, int64_t ldx,
                            const nf4_weight* w, int64_t N_e, void* y, int64_t ldy, void* stream) {
   return run_grouped(0, x, offsets, E, T, ldx, w, N_e, y, ldy, stream);
@@ -655,9 +669,12 @@ size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E
     if (!current_device(&dev)) return 0;
     // Enough for either code width (the plan depends on it).
     const int mode = op == NF4_OP_LINEAR_FWD ? 0 : 1;
-    const size_t w4 = plan_dense(mode, M, N, K, dev.sms, true, 4).ws_bytes;
-    const size_t w8 = plan_dense(mode, M, N, K, dev.sms, true, 8).ws_bytes;
-    return w4 > w8 ? w4 : w8;
+    size_t need = 0;
+    for (int v = 0; v < 3; ++v) {  // 4-bit bf16, 8-bit bf16, 4-bit fp16
+      const size_t b = plan_dense(mode, M, N, K, dev.sms, true, v == 1 ? 8 : 4, v == 2).ws_bytes;
+      need = b > need ? b : need;
+    }
+    return need;
   }
   return 0;
 }

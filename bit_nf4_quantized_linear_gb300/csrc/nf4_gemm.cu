@@ -38,11 +38,16 @@
 #include "decode.cuh"
 #include "sm100_ptx.cuh"
 
-// Code width of the kernel instances this translation unit launches: 4 here,
-// 8 when nf4_gemm8.cu compiles this file a second time.
+// Code width and operand type of the kernel instances this translation unit
+// launches: 4-bit codes with bf16 operands here, 8-bit codes when nf4_gemm8.cu
+// compiles this file again, fp16 operands when nf4_gemm_f16.cu does.
 #ifndef NF4_GEMM_BITS
 #define NF4_GEMM_BITS 4
 #endif
+#ifndef NF4_GEMM_F16
+#define NF4_GEMM_F16 0
+#endif
+#define NF4_GEMM_MAIN_TU (NF4_GEMM_BITS == 4 && NF4_GEMM_F16 == 0)
 
 namespace nf4 {
 namespace {
@@ -330,7 +335,14 @@ __device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* co
   return __fadd_rn(__fmul_rn(code8_s[r.q], r.v), offset);
 }
 
-template <int MODE, int BT, int CG, int BITS>
+// fp32 to the output / operand 16-bit type (bf16, or IEEE fp16 when F16), RNE.
+template <bool F16>
+__device__ __forceinline__ uint16_t to16(float f) {
+  if constexpr (F16) return __half_as_ushort(__float2half_rn(f));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <int MODE, int BT, int CG, int BITS, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
                     const __grid_constant__ CUtensorMap tmap_pk,
@@ -486,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0 && sh.rank == 0) {  // a pair's MMAs are issued by its leader
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileW * CG, BT, MODE == 1, false);
+      constexpr uint32_t idesc = F16 ? idesc_f16_f32(kTileW * CG, BT, MODE == 1, false)
+                                     : idesc_bf16_f32(kTileW * CG, BT, MODE == 1, false);
       // Constant fields of the operand descriptors (address field zero).
       const uint64_t a_desc_hi = (MODE == 0) ? smem_desc_sw128(0, 16, 1024) : smem_desc_sw128(0, 8192, 1024);
       const uint64_t b_desc_hi = smem_desc_sw128(0, 16, 1024);
@@ -630,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (BT > 16 || j < 16)
-              stg[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+              stg[j * 32 + lane] = to16<F16>(__uint_as_float(v[j]));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -642,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // Direct stores, one token row per element: y / gx in bf16, or this split's
         // fp32 partials.
-        __nv_bfloat16* op = a.out + it.tok0 * a.ld_out + col;
+        uint16_t* op = reinterpret_cast<uint16_t*>(a.out) + it.tok0 * a.ld_out + col;
         float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
 #pragma unroll 1
         for (int c0 = 0; c0 < ntok; c0 += kBatch) {
@@ -657,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int j = 0; j < kBatch; ++j)
-                if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = to16<F16>(__uint_as_float(v[j]));
             }
           }
         }
@@ -787,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (BITS == 4) {
         wc[0] = *reinterpret_cast<const uint4*>(pk + pk0);
         wc[1] = *reinterpret_cast<const uint4*>(pk + pk1);
-        L = make_lut(code2, s);
+        L = make_lut<F16>(code2, s);
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) wc[c] = *reinterpret_cast<const uint4*>(pk + pkc[c]);
@@ -822,9 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float f1 = vt[((word >> (sft + 8)) & 0xffu) * 32];
             const uint64_t m = mul_f32x2(
                 (static_cast<uint64_t>(__float_as_uint(f1)) << 32) | __float_as_uint(f0), s2);
-            __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(m)),
-                                                     __uint_as_float(static_cast<uint32_t>(m >> 32)));
-            o[p] = *reinterpret_cast<uint32_t*>(&b);
+            o[p] = pack16x2<F16>(__uint_as_float(static_cast<uint32_t>(m)),
+                                 __uint_as_float(static_cast<uint32_t>(m >> 32)));
           }
           *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
@@ -865,11 +877,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// out[t, c] = bf16(sum over s in order of ws[s, t, c]); four columns per thread.
-// Used for few splits (the large-M contraction splits).
+// out[t, c] = bf16 (fp16 when F16) of the sum over s in order of ws[s, t, c]; four
+// columns per thread.  Used for few splits (the large-M contraction splits).
+template <bool F16>
 __global__ void __launch_bounds__(256) splitk_reduce_vec_kernel(const float* __restrict__ ws, int splits,
                                                                 int64_t M, int64_t ncols,
-                                                                __nv_bfloat16* __restrict__ out, int64_t ld) {
+                                                                uint16_t* __restrict__ out, int64_t ld) {
   grid_dependency_wait();
   allow_dependents();
   const int64_t total = M * ncols;
@@ -887,28 +900,28 @@ __global__ void __launch_bounds__(256) splitk_reduce_vec_kernel(const float* __r
         acc.z = __fadd_rn(acc.z, v.z);
         acc.w = __fadd_rn(acc.w, v.w);
       }
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
       uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      pk.x = pack16x2<F16>(acc.x, acc.y);
+      pk.y = pack16x2<F16>(acc.z, acc.w);
       *reinterpret_cast<uint2*>(out + t * ld + c0) = pk;
     } else {
       for (int64_t c = c0; c < c0 + 4 && c < ncols; ++c) {
         float acc = ws[t * ncols + c];
         for (int s = 1; s < splits; ++s) acc = __fadd_rn(acc, ws[static_cast<int64_t>(s) * total + t * ncols + c]);
-        out[t * ld + c] = __float2bfloat16_rn(acc);
+        out[t * ld + c] = to16<F16>(acc);
       }
     }
   }
 }
 
-// out[t, c] = bf16(sum over s of ws[s, t, c]) in a fixed order: a CTA owns 32
-// consecutive elements of one row; its 8 thread groups sum the splits
-// g, g+8, g+16, ... sequentially, then the 8 group sums are added in group order.
+// out[t, c] = bf16 (fp16 when F16) of the sum over s of ws[s, t, c] in a fixed
+// order: a CTA owns 32 consecutive elements of one row; its 8 thread groups sum the
+// splits g, g+8, g+16, ... sequentially, then the 8 group sums are added in group
+// order.
+template <bool F16>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ ws, int splits,
                                                             int64_t M, int64_t ncols,
-                                                            __nv_bfloat16* __restrict__ out, int64_t ld) {
+                                                            uint16_t* __restrict__ out, int64_t ld) {
   __shared__ float part[8][32];
   grid_dependency_wait();
   allow_dependents();
@@ -929,18 +942,18 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
     if (g == 0 && col < ncols) {
       float acc = part[0][c];
       for (int q = 1; q < 8 && q < splits; ++q) acc = __fadd_rn(acc, part[q][c]);
-      out[t * ld + col] = __float2bfloat16_rn(acc);
+      out[t * ld + col] = to16<F16>(acc);
     }
     __syncthreads();
   }
 }
 
-template <int MODE, int BT, int CG, int BITS>
+template <int MODE, int BT, int CG, int BITS, bool F16>
 cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
                        const CUtensorMap& to, int grid,
                        cudaStream_t s) {
   static bool configured = false;
-  auto kern = nf4_gemm_kernel<MODE, BT, CG, BITS>;
+  auto kern = nf4_gemm_kernel<MODE, BT, CG, BITS, F16>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Geo<BT, CG, BITS>::kSmem);
@@ -967,26 +980,36 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
 template <int MODE>
 cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta,
                         const CUtensorMap& tp, const CUtensorMap& to, int grid, cudaStream_t s) {
-#if NF4_GEMM_BITS == 4
+#if NF4_GEMM_MAIN_TU
   if (cg == 2) {
     if (bt != 256) return cudaErrorInvalidValue;
-    return launch_one<MODE, 256, 2, 4>(a, ta, tp, to, grid, s);
+    return launch_one<MODE, 256, 2, 4, false>(a, ta, tp, to, grid, s);
   }
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1, 4>(a, ta, tp, to, grid, s);
-    case 32: return launch_one<MODE, 32, 1, 4>(a, ta, tp, to, grid, s);
-    case 64: return launch_one<MODE, 64, 1, 4>(a, ta, tp, to, grid, s);
-    case 128: return launch_one<MODE, 128, 1, 4>(a, ta, tp, to, grid, s);
-    case 256: return launch_one<MODE, 256, 1, 4>(a, ta, tp, to, grid, s);
+    case 16: return launch_one<MODE, 16, 1, 4, false>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 1, 4, false>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 1, 4, false>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 1, 4, false>(a, ta, tp, to, grid, s);
+    case 256: return launch_one<MODE, 256, 1, 4, false>(a, ta, tp, to, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+#elif NF4_GEMM_F16
+  if (cg != 1) return cudaErrorInvalidValue;
+  switch (bt) {
+    case 16: return launch_one<MODE, 16, 1, 4, true>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 1, 4, true>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 1, 4, true>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 1, 4, true>(a, ta, tp, to, grid, s);
+    case 256: return launch_one<MODE, 256, 1, 4, true>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #else
   if (cg != 1) return cudaErrorInvalidValue;
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1, 8>(a, ta, tp, to, grid, s);
-    case 32: return launch_one<MODE, 32, 1, 8>(a, ta, tp, to, grid, s);
-    case 64: return launch_one<MODE, 64, 1, 8>(a, ta, tp, to, grid, s);
-    case 128: return launch_one<MODE, 128, 1, 8>(a, ta, tp, to, grid, s);
+    case 16: return launch_one<MODE, 16, 1, 8, false>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 1, 8, false>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 1, 8, false>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 1, 8, false>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #endif
@@ -994,7 +1017,15 @@ cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta
 
 }  // namespace
 
-#if NF4_GEMM_BITS == 8
+#if NF4_GEMM_F16
+// The fp16-operand instances (this file compiled again, from nf4_gemm_f16.cu).
+cudaError_t launch_gemm_f16(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
+                            const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
+                            cudaStream_t s) {
+  if (mode == 0) return launch_mode<0>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  return launch_mode<1>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
+}
+#elif NF4_GEMM_BITS == 8
 // The 8-bit-code instances (this file compiled a second time, from nf4_gemm8.cu).
 cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
                              const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
@@ -1022,9 +1053,13 @@ uint32_t* stream_k_flags(uint32_t epoch) {
   return base + static_cast<size_t>(epoch % kSkSlots) * kSkMaxCtas * 4;
 }
 
-cudaError_t launch_gemm(int mode, int bt, int cg, int bits, const GemmArgs& a,
+cudaError_t launch_gemm(int mode, int bt, int cg, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,
                         const CUtensorMap& tmap_out, int grid, cudaStream_t s) {
+  if (f16) {
+    if (cg != 1 || bits != 4) return cudaErrorInvalidValue;
+    return launch_gemm_f16(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  }
   if (bits == 8) {
     if (cg != 1) return cudaErrorInvalidValue;
     return launch_gemm_8bit(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
@@ -1034,7 +1069,8 @@ cudaError_t launch_gemm(int mode, int bt, int cg, int bits, const GemmArgs& a,
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
-                                 __nv_bfloat16* out, int64_t ld, cudaStream_t s) {
+                                 void* out_, int64_t ld, bool f16, cudaStream_t s) {
+  uint16_t* out = static_cast<uint16_t*>(out_);
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = s;
@@ -1048,14 +1084,16 @@ cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t
     if (grid > 8192) grid = 8192;
     if (grid < 1) grid = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_vec_kernel, ws, splits, M, ncols, out, ld);
+    return f16 ? cudaLaunchKernelEx(&cfg, splitk_reduce_vec_kernel<true>, ws, splits, M, ncols, out, ld)
+               : cudaLaunchKernelEx(&cfg, splitk_reduce_vec_kernel<false>, ws, splits, M, ncols, out, ld);
   }
   // Many splits (the small-M input gradient): one CTA per 32 outputs.
   int64_t grid = M * ((ncols + 31) / 32);
   if (grid > 16384) grid = 16384;
   if (grid < 1) grid = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, splits, M, ncols, out, ld);
+  return f16 ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true>, ws, splits, M, ncols, out, ld)
+             : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false>, ws, splits, M, ncols, out, ld);
 }
 
 #endif  // NF4_GEMM_BITS

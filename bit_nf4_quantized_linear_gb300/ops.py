@@ -145,40 +145,50 @@ def dequantize(w: NF4Weight, dtype: torch.dtype = torch.bfloat16,
     return out
 
 
-def _check_act(name, a: torch.Tensor, cols: int):
+def _check_act(name, a: torch.Tensor, cols: int, f16_ok: bool = False):
     _need_cuda(name, a)
-    if a.dtype != torch.bfloat16 or a.dim() != 2 or a.shape[1] != cols or a.stride(1) != 1:
-        raise ValueError(f"{name}: expected a bf16 [rows, {cols}] tensor with unit column stride")
+    dts = (torch.bfloat16, torch.float16) if f16_ok else (torch.bfloat16,)
+    if a.dtype not in dts or a.dim() != 2 or a.shape[1] != cols or a.stride(1) != 1:
+        kinds = "bf16 or fp16" if f16_ok else "bf16"
+        raise ValueError(f"{name}: expected a {kinds} [rows, {cols}] tensor with unit column stride")
 
 
 def linear_fwd(x: torch.Tensor, w: NF4Weight, out: Optional[torch.Tensor] = None,
                ws: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """nf4_linear_fwd: y = x W^T, x bf16 [M, K] -> y bf16 [M, N]."""
-    _check_act("linear_fwd", x, w.K)
+    """nf4_linear_fwd (bf16) / nf4_linear_fwd_f16 (fp16): y = x W^T, x [M, K] -> y [M, N]
+    in the activations' dtype."""
+    _check_act("linear_fwd", x, w.K, f16_ok=True)
     M = x.shape[0]
-    y = torch.empty(M, w.N, dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = torch.empty(M, w.N, dtype=x.dtype, device=x.device) if out is None else out
     need = workspace_size(_lib.OP_LINEAR_FWD, M, w.N, w.K)
     if need and (ws is None or ws.numel() * ws.element_size() < need):
         ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if y.dtype != x.dtype:
+        raise ValueError("linear_fwd: out must have the activations' dtype")
     s = w.struct()
-    rc = _lib.lib().nf4_linear_fwd(_ptr(x), M, x.stride(0), ctypes.byref(s), _ptr(y), y.stride(0),
-                                   _ptr(ws) if need else None, need, _stream())
+    fn = _lib.lib().nf4_linear_fwd_f16 if x.dtype == torch.float16 else _lib.lib().nf4_linear_fwd
+    rc = fn(_ptr(x), M, x.stride(0), ctypes.byref(s), _ptr(y), y.stride(0),
+            _ptr(ws) if need else None, need, _stream())
     _lib.check(rc, "nf4_linear_fwd")
     return y
 
 
 def linear_dgrad(gy: torch.Tensor, w: NF4Weight, out: Optional[torch.Tensor] = None,
                  ws: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """nf4_linear_dgrad: grad_x = grad_y W, gy bf16 [M, N] -> gx bf16 [M, K]."""
-    _check_act("linear_dgrad", gy, w.N)
+    """nf4_linear_dgrad (bf16) / nf4_linear_dgrad_f16 (fp16): grad_x = grad_y W,
+    gy [M, N] -> gx [M, K] in grad_y's dtype."""
+    _check_act("linear_dgrad", gy, w.N, f16_ok=True)
     M = gy.shape[0]
-    gx = torch.empty(M, w.K, dtype=torch.bfloat16, device=gy.device) if out is None else out
+    gx = torch.empty(M, w.K, dtype=gy.dtype, device=gy.device) if out is None else out
     need = workspace_size(_lib.OP_LINEAR_DGRAD, M, w.N, w.K)
     if need and (ws is None or ws.numel() * ws.element_size() < need):
         ws = torch.empty(need, dtype=torch.uint8, device=gy.device)
+    if gx.dtype != gy.dtype:
+        raise ValueError("linear_dgrad: out must have grad_y's dtype")
     s = w.struct()
-    rc = _lib.lib().nf4_linear_dgrad(_ptr(gy), M, gy.stride(0), ctypes.byref(s), _ptr(gx),
-                                     gx.stride(0), _ptr(ws) if need else None, need, _stream())
+    fn = _lib.lib().nf4_linear_dgrad_f16 if gy.dtype == torch.float16 else _lib.lib().nf4_linear_dgrad
+    rc = fn(_ptr(gy), M, gy.stride(0), ctypes.byref(s), _ptr(gx),
+            gx.stride(0), _ptr(ws) if need else None, need, _stream())
     _lib.check(rc, "nf4_linear_dgrad")
     return gx
 

@@ -194,6 +194,19 @@ nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weigh
 nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w, void* gx,
                             int64_t ldgx, void* ws, size_t ws_bytes, void* stream);
 
+/* nf4_linear_fwd_f16 / nf4_linear_dgrad_f16 -- the same products for the fp16
+ * compute dtype (Soup issue #842, "Design sketch": keep the dtype handling of
+ * Linear4bit, which computes in the activations' half-precision type): x / grad_y
+ * and y / grad_x are IEEE fp16, and the operand is fp16(fp32(code4[q] * absmax'))
+ * (round to nearest even) instead of bf16.  Same arguments, workspace and
+ * determinism as nf4_linear_fwd / nf4_linear_dgrad; every M runs the fused tcgen05
+ * kernel (fp16 tcgen05 MMAs, fp32 accumulation).  4-bit codes only (bits == 8 ->
+ * NF4_ERR_UNSUPPORTED). */
+nf4_status nf4_linear_fwd_f16(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
+                              int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+nf4_status nf4_linear_dgrad_f16(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w,
+                                void* gx, int64_t ldgx, void* ws, size_t ws_bytes, void* stream);
+
 /* nf4_grouped_fwd -- per-expert forward for a stack of E frozen experts quantised
  * as one tensor (fork PR "Experts trainability ...", commit 1: the fused 3-D
  * expert stack; commit 2: no dequantised weight is kept).

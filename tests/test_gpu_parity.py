@@ -572,3 +572,60 @@ def test_8bit_stream_k_and_grouped(restore_stream_k):
             gref[r0:r1] = oracle.linear_dgrad(gyb[r0:r1], wbg[e * Ne:(e + 1) * Ne])
     parity(yg, yref, "fp8 grouped fwd")
     parity(gxg, gref, "fp8 grouped dgrad")
+
+
+# ------------------------------------------------------------- fp16 dtype --
+# fp16 activations, operand fp16(fp32(code4[q] * scale)) and fp16 outputs: the
+# fused kernel at every M.
+
+def _f16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (16, 384, 512), (40, 320, 192), (129, 384, 320),
+                                   (300, 640, 1024), (700, 640, 1024)])
+def test_f16_fwd_dgrad_parity_and_reruns(M, N, K):
+    w, st, g = _quant_pair(N, K, True, seed=M + 2 * N + K)
+    x = synth.activation(M, K, g).float().half().to(DEV)
+    gy = synth.activation(M, N, g).float().half().to(DEV)
+    wf = oracle.dequantize_f16(st)
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x, w)
+    gx = nf4.linear_dgrad(gy, w)
+    c = nf4.path_counters()
+    assert y.dtype == torch.float16 and gx.dtype == torch.float16
+    assert c["linear_fwd"] == 1 and c["linear_dgrad"] == 1, c
+    parity(y, oracle.linear_fwd(_f16_bits(x), wf, dtype="f16"), f"f16 fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(_f16_bits(gy), wf, dtype="f16"), f"f16 dgrad {M}x{N}x{K}")
+    for _ in range(3):
+        assert torch.equal(nf4.linear_fwd(x, w).view(torch.int16), y.view(torch.int16))
+        assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx.view(torch.int16))
+
+
+def test_f16_identity_probes_exact():
+    N, K = 384, 256
+    w, st, _ = _quant_pair(N, K, True, seed=31)
+    wf = torch.from_numpy(oracle.dequantize_f16(st).view(np.int16)).view(torch.float16).float().numpy()
+    y = nf4.linear_fwd(torch.eye(K, dtype=torch.float16, device=DEV), w).float().cpu().numpy()
+    np.testing.assert_array_equal(y, np.ascontiguousarray(wf.T))
+    gx = nf4.linear_dgrad(torch.eye(N, dtype=torch.float16, device=DEV), w).float().cpu().numpy()
+    np.testing.assert_array_equal(gx, wf)
+
+
+def test_f16_autograd_and_stream_k(restore_stream_k):
+    from bit_nf4_quantized_linear_gb300 import autograd
+    M, N, K = 300, 640, 1024
+    w, st, g = _quant_pair(N, K, True, seed=32)
+    wf = oracle.dequantize_f16(st)
+    x = synth.activation(M, K, g).float().half().to(DEV).requires_grad_(True)
+    gy = synth.activation(M, N, g).float().half().to(DEV)
+    y = autograd.nf4_linear(x, w)
+    y.backward(gy)
+    assert y.dtype == torch.float16 and x.grad.dtype == torch.float16
+    parity(y, oracle.linear_fwd(_f16_bits(x), wf, dtype="f16"), "f16 autograd fwd")
+    parity(x.grad, oracle.linear_dgrad(_f16_bits(gy), wf, dtype="f16"), "f16 autograd dgrad")
+    ops.set_stream_k(_lib.STREAM_K_FORCE)
+    nf4.reset_path_counters()
+    y2 = nf4.linear_fwd(x.detach(), w)
+    assert nf4.path_counters()["stream_k"] == 1
+    parity(y2, oracle.linear_fwd(_f16_bits(x), wf, dtype="f16"), "f16 stream-K fwd")
