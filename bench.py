@@ -310,11 +310,12 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_val = job_throughput(flops, world, e2e_ms)
 
-    sweep = grouped = storage8 = None
+    sweep = grouped = storage8 = f16 = None
     if rank == 0 and world == 1 and not args.no_sweep:
         sweep = run_sweep(dev, pk)
         grouped = run_grouped(dev, pk)
         storage8 = run_storage8(dev, pk)
+        f16 = run_storage8(dev, pk, (("nf4_f16", "nf4", "f16"),))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -362,6 +363,8 @@ def run_ours(args, rank, world, local_rank):
         out["grouped_olmoe"] = grouped
     if storage8 is not None:
         out["storage_8bit_4096"] = storage8
+    if f16 is not None:
+        out["f16_compute_4096"] = f16
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
@@ -481,16 +484,18 @@ def run_sweep(dev, pk):
     return res
 
 
-def run_storage8(dev, pk):
-    """One-byte storage ("int8" dynamic map, "fp8" e4m3 levels) at K = N = 4096,
-    double-quant statistics: fwd + dgrad through the fused kernel, each point a CUDA
-    graph of back-to-back calls over weight replicas (>= 4 x L2 at small M)."""
+def run_storage8(dev, pk, variants=(("int8", "int8", "bf16"), ("fp8", "fp8", "bf16"))):
+    """Storage / dtype variants at K = N = 4096, double-quant statistics: one-byte
+    storage ("int8" dynamic map, "fp8" e4m3 levels) and the fp16 compute dtype; fwd +
+    dgrad through the fused kernel, each point a CUDA graph of back-to-back calls over
+    weight replicas (>= 4 x L2 at small M)."""
     import torch
     import bit_nf4_quantized_linear_gb300 as nf4
     from bit_nf4_quantized_linear_gb300 import ops, synth
     N = K = 4096
     out = {}
-    for qt in ("int8", "fp8"):
+    for name, qt, adt in variants:
+        adt = torch.float16 if adt == "f16" else torch.bfloat16
         g = synth.generator(2)
         base = nf4.quantize(synth.weight(N, K, g).to(dev), double_quant=True, quant_type=qt)
         wbytes = base.nbytes()
@@ -500,10 +505,10 @@ def run_storage8(dev, pk):
             reps = [base] + [nf4.NF4Weight(base.packed.clone(), None, base.absmax_q.clone(),
                                            base.nested_absmax.clone(), base.nested_offset.clone(),
                                            base.code4, base.code8, N, K, True) for _ in range(R - 1)]
-            x = synth.activation(M, K, g).to(dev)
-            gy = synth.activation(M, N, g).to(dev)
-            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            gx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+            x = synth.activation(M, K, g).float().to(adt).to(dev)
+            gy = synth.activation(M, N, g).float().to(adt).to(dev)
+            y = torch.empty(M, N, dtype=adt, device=dev)
+            gx = torch.empty(M, K, dtype=adt, device=dev)
             wsz = max(ops.workspace_size(1, M, N, K), ops.workspace_size(2, M, N, K), 16)
             wsb = torch.empty(wsz, dtype=torch.uint8, device=dev)
             s = torch.cuda.Stream(dev)
@@ -541,7 +546,7 @@ def run_storage8(dev, pk):
                          "weight_gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
             del reps, x, gy, y, gx, wsb
             torch.cuda.empty_cache()
-        out[qt] = {"weight_bytes": wbytes, "rows": rows}
+        out[name] = {"weight_bytes": wbytes, "rows": rows}
     return out
 
 
