@@ -304,6 +304,42 @@ def grouped_fwd(x_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray) -> np.nd
     return y
 
 
+def interleave_gate_up(gate: np.ndarray, up: np.ndarray, experts: int) -> np.ndarray:
+    """Stack the gate and up projections of each expert ([E*H, K] each, H a multiple
+    of 64) into one [E*2H, K] weight whose 128-row groups hold 64 gate rows then the
+    64 up rows of the same output columns (the layout the fused SwiGLU epilogue reads)."""
+    EH, K = gate.shape
+    H = EH // experts
+    g = gate.reshape(experts, H // 64, 64, K)
+    u = up.reshape(experts, H // 64, 64, K)
+    return np.stack([g, u], axis=2).reshape(experts * 2 * H, K)
+
+
+def grouped_fwd_epilogue(x_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray, bias=None,
+                         row_scale=None, swiglu: bool = False) -> np.ndarray:
+    """The grouped forward followed by the expert epilogue, in fp64 (Soup issue #842's
+    expert path / fork PR "Experts trainability": the SwiGLU of gate and up, the
+    routing-weight scaling and a bias that otherwise run in torch around the products):
+      a = x_e W_e^T (+ bias[e, :], fp32 per weight row);
+      swiglu: each 128-column group of a is (gate[64], up[64]) of 64 output columns,
+              h = silu(gate) * up with silu(g) = g / (1 + exp(-g));
+      row_scale: every output row times row_scale[t] (routing weights, sorted order)."""
+    E, N, K = wb_stack_bf16.shape
+    a = grouped_fwd(x_bf16, offsets, wb_stack_bf16)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float32).astype(np.float64).reshape(E, N)
+        for e in range(E):
+            a[int(offsets[e]):int(offsets[e + 1])] += b[e]
+    if swiglu:
+        T = a.shape[0]
+        grp = a.reshape(T, N // 128, 2, 64)
+        g, u = grp[:, :, 0, :], grp[:, :, 1, :]
+        a = (g / (1.0 + np.exp(-g)) * u).reshape(T, N // 2)
+    if row_scale is not None:
+        a = a * np.asarray(row_scale, dtype=np.float32).astype(np.float64)[:, None]
+    return a
+
+
 def grouped_dgrad(gy_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray) -> np.ndarray:
     E, N, K = wb_stack_bf16.shape
     T = gy_bf16.shape[0]

@@ -532,3 +532,44 @@ def test_f16_products_brute_force_vs_numpy():
                                x.astype(np.float64) @ w.astype(np.float64).T, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(oracle.linear_dgrad(gb, wb, dtype="f16"),
                                gy.astype(np.float64) @ w.astype(np.float64), rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------- expert epilogues ----
+
+def test_interleave_gate_up_layout():
+    E, H, K = 2, 128, 3
+    gate = np.arange(E * H * K, dtype=np.float32).reshape(E * H, K)
+    up = -gate - 1
+    w = oracle.interleave_gate_up(gate, up, E)
+    assert w.shape == (E * 2 * H, K)
+    for e in range(E):
+        for c in range(H):  # output column c of expert e
+            r = e * 2 * H + 128 * (c // 64) + c % 64
+            np.testing.assert_array_equal(w[r], gate[e * H + c])
+            np.testing.assert_array_equal(w[r + 64], up[e * H + c])
+
+
+def test_swiglu_bias_and_row_scale_literals():
+    # One expert, N = 128 (64 gate + 64 up rows), K = 64, one-hot weights: the
+    # accumulator of row t, column n is x[t, n % 64], so g and u are chosen by x.
+    N, K = 128, 64
+    w = np.zeros((1, N, K), np.float32)
+    for n in range(N):
+        w[0, n, n % 64] = 1.0
+    wb = _bf16(w)
+    x = np.zeros((2, K), np.float32)
+    x[0, :4] = [0.0, 1.0, -1.0, 20.0]
+    x[1, :4] = [2.0, 2.0, 2.0, 2.0]
+    xb = _bf16(x)
+    off = np.array([0, 2])
+    bias = np.zeros(N, np.float32)
+    bias[64:68] = 1.0              # up = x + 1
+    h = oracle.grouped_fwd_epilogue(xb, off, wb, bias=bias, row_scale=np.array([1.0, 0.5], np.float32),
+                                    swiglu=True)
+    assert h.shape == (2, 64)
+    # row 0: g = (0, 1, -1, 20), u = g + 1; silu(1) = 0.7310585786300049
+    np.testing.assert_allclose(h[0, :4], [0.0, 0.7310585786300049 * 2.0, -0.2689414213699951 * 0.0,
+                                          20.0 / (1 + math.exp(-20.0)) * 21.0], rtol=1e-12)
+    # row 1: g = 2, u = 3, scaled by 0.5; silu(2) = 1.7615941559557649
+    np.testing.assert_allclose(h[1, :4], [1.7615941559557649 * 3 * 0.5] * 4, rtol=1e-12)
+    assert np.all(h[:, 4:] == 0.0)
