@@ -52,6 +52,14 @@ class nf4_weight(ctypes.Structure):
     ]
 
 
+class nf4_epilogue(ctypes.Structure):
+    _fields_ = [
+        ("bias", ctypes.c_void_p),
+        ("row_scale", ctypes.c_void_p),
+        ("swiglu", ctypes.c_int32),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -86,6 +94,7 @@ def lib() -> ctypes.CDLL:
             "nf4_linear_dgrad_f16": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_grouped_fwd": [P, P, I32, I64, I64, W, I64, P, I64, P],
             "nf4_grouped_dgrad": [P, P, I32, I64, I64, W, I64, P, I64, P],
+            "nf4_grouped_fwd_ep": [P, P, I32, I64, I64, W, I64, ctypes.POINTER(nf4_epilogue), P, I64, P],
             "nf4_workspace_size": [I32, I64, I64, I64, I32],
             "nf4_status_string": [I32],
             "nf4_get_path_counters": [P],

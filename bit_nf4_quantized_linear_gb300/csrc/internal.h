@@ -50,6 +50,11 @@ struct GemmArgs {
   float* ws;  // split-K partials [splits][M][ncols]
   int* status;
   int tma_out;  // dense bf16 output written by bulk tensor stores (aligned out and ld_out)
+  // Grouped forward epilogue (nf4_grouped_fwd_ep): fp32 bias per weight row, fp32
+  // scale per output row (routing weights), SwiGLU of interleaved gate/up rows.
+  const float* ep_bias;
+  const float* ep_scale;
+  int ep_swiglu;
   // Stream-K schedule (dense, no pairs, splits == 1): the items * ksteps
   // contraction steps are cut into sk_ctas equal contiguous runs, one per CTA.  A
   // tile cut between CTAs is finished by the CTA holding its first steps, which

@@ -483,16 +483,20 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
 
 nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_t E, int64_t T,
                        int64_t ld_act, const nf4_weight* w, int64_t N_e, void* out, int64_t ld_out,
-                       void* stream) {
+                       void* stream, const nf4_epilogue* ep = nullptr) {
   nf4_status st = check_weight(w);
   if (st != NF4_OK) return st;
   const int64_t K = w->K;
   if (E < 1 || E > nf4::kMaxExperts || T < 0 || N_e < 1 || !offsets) return NF4_ERR_INVALID_ARG;
   if (w->N != static_cast<int64_t>(E) * N_e) return NF4_ERR_INVALID_ARG;
   if (K % 64 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  const bool swiglu = ep && ep->swiglu;
+  if (ep && (ep->swiglu != 0 && ep->swiglu != 1)) return NF4_ERR_INVALID_ARG;
+  if (swiglu && N_e % 128 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
   const int64_t act_cols = mode == 0 ? K : N_e;
   const int64_t out_cols = mode == 0 ? N_e : K;
-  if (ld_act < act_cols || ld_out < out_cols) return NF4_ERR_INVALID_ARG;
+  const int64_t out_width = swiglu ? N_e / 2 : out_cols;
+  if (ld_act < act_cols || ld_out < out_width) return NF4_ERR_INVALID_ARG;
   if (T == 0) return NF4_OK;
   if (!act || !out) return NF4_ERR_INVALID_ARG;
   if (ld_act % 8 != 0 || !aligned16(act) || !aligned16(w->packed)) return NF4_ERR_ALIGNMENT;
@@ -534,6 +538,11 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   a.ld_out = ld_out;
   a.ws = nullptr;
   a.status = dev.status;
+  if (ep) {
+    a.ep_bias = ep->bias;
+    a.ep_scale = ep->row_scale;
+    a.ep_swiglu = ep->swiglu;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tmap_out;  // unused: expert row ranges end inside tiles (direct stores)
   std::memset(&tmap_out, 0, sizeof(tmap_out));
@@ -649,6 +658,13 @@ nf4_status nf4_linear_dgrad_f16(const void* gy, int64_t M, int64_t ldgy, const n
 nf4_status nf4_grouped_fwd(const void* x, const int32_t* offsets, int32_t E, int64_t T, int64_t ldx,
                            const nf4_weight* w, int64_t N_e, void* y, int64_t ldy, void* stream) {
   return run_grouped(0, x, offsets, E, T, ldx, w, N_e, y, ldy, stream);
+}
+
+nf4_status nf4_grouped_fwd_ep(const void* x, const int32_t* offsets, int32_t E, int64_t T,
+                              int64_t ldx, const nf4_weight* w, int64_t N_e, const nf4_epilogue* ep,
+                              void* y, int64_t ldy, void* stream) {
+  if (!ep) return NF4_ERR_INVALID_ARG;
+  return run_grouped(0, x, offsets, E, T, ldx, w, N_e, y, ldy, stream, ep);
 }
 
 nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, int64_t T,

@@ -119,7 +119,9 @@ constexpr int kBarAEmpty = 52;
 constexpr int kBarAccFull = 56;
 constexpr int kBarAccEmpty = 58;
 constexpr int kBarDrain = 60;
-constexpr int kNumBars = 61;
+constexpr int kBarEpFull = 61;   // SwiGLU epilogue: up values of a batch written (2 warp pairs)
+constexpr int kBarEpEmpty = 63;  // ... and read by the gate warp
+constexpr int kNumBars = 65;
 
 struct Item {
   int64_t idx;    // item (tile) index
@@ -397,6 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarAccEmpty + i), kNumEpiWarps * CG);  // both CTAs' epilogues
     }
     mbar_init(bar_at(sh, kBarDrain), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_at(sh, kBarEpFull + i), 1);
+      mbar_init(bar_at(sh, kBarEpEmpty + i), 1);
+    }
     *sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -560,9 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = 32 * q + lane;
     int acc_i = 0;
+    uint32_t xb = 0;    // SwiGLU exchange batches so far (barrier phases)
+    bool ep_ok = true;  // false once an exchange wait gave up
     Cursor cur = cursor_begin(a, unit, total_items);
     Item it;
-    for (; cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it); ++acc_i) {
+    for (; ep_ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it); ++acc_i) {
       const int ab = acc_i & 1;
       const uint32_t acc_ph = (acc_i >> 1) & 1;
       if (!wait_phase(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)) break;
@@ -652,15 +660,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
+      } else if (MODE == 0 && a.ep_swiglu) {
+        // Grouped SwiGLU: the tile's rows 0-63 are gate rows and rows 64-127 the up
+        // rows of the same 64 output columns, held by other TMEM lane quarters, so the
+        // up warp (quarter p + 2) passes each 16-token batch to the gate warp
+        // (quarter p) through shared memory (32 rows x 16 fp32, conflict-free), with
+        // a full / empty barrier pair per warp pair.  h = silu(g) * u, times the row
+        // scale; biases are added to g and u first.
+        const int p = q & 1;
+        float* xch = reinterpret_cast<float*>(smem + G::kOffOut) + p * (32 * kBatch);
+        const float bias = a.ep_bias ? __ldg(a.ep_bias + it.wrow0 + row) : 0.0f;
+        uint16_t* op = reinterpret_cast<uint16_t*>(a.out) + it.tok0 * a.ld_out + it.col0 / 2 + row;
+        const bool gate_ok = q < 2 && it.col0 / 2 + row < a.ncols / 2;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ntok && ep_ok; c0 += kBatch, ++xb) {
+          uint32_t v[kBatch];
+          tmem_ld_32x32b_x16(taddr + c0, v);
+          tmem_wait_ld();
+          if (q >= 2) {  // up rows: hand the batch to the gate warp
+            if (!wait_phase(bar_at(sh, kBarEpEmpty + p), (xb & 1u) ^ 1u, sh, a)) { ep_ok = false; break; }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+              xch[j * 32 + lane] = __fadd_rn(__uint_as_float(v[j]), bias);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(sh, kBarEpFull + p));
+          } else {
+            if (!wait_phase(bar_at(sh, kBarEpFull + p), xb & 1u, sh, a)) { ep_ok = false; break; }
+            const int nj = ntok - c0;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+              const float g = __fadd_rn(__uint_as_float(v[j]), bias);
+              const float u = xch[j * 32 + lane];
+              float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+              if (a.ep_scale && j < nj) h = __fmul_rn(h, __ldg(a.ep_scale + it.tok0 + c0 + j));
+              if (gate_ok && j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = to16<F16>(h);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(sh, kBarEpEmpty + p));
+          }
+        }
       } else {
         // Direct stores, one token row per element: y / gx in bf16, or this split's
-        // fp32 partials.
+        // fp32 partials.  Grouped forward epilogue: bias per weight row, scale per
+        // output row.
         uint16_t* op = reinterpret_cast<uint16_t*>(a.out) + it.tok0 * a.ld_out + col;
         float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
+        const float bias = MODE == 0 && a.ep_bias && col_ok ? __ldg(a.ep_bias + it.wrow0 + row) : 0.0f;
 #pragma unroll 1
         for (int c0 = 0; c0 < ntok; c0 += kBatch) {
           uint32_t v[kBatch];
           load_batch(c0, v);
+          if (MODE == 0 && (a.ep_bias || a.ep_scale)) {
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+              float f = __fadd_rn(__uint_as_float(v[j]), bias);
+              if (a.ep_scale && c0 + j < ntok) f = __fmul_rn(f, __ldg(a.ep_scale + it.tok0 + c0 + j));
+              v[j] = __float_as_uint(f);
+            }
+          }
           if (col_ok) {
             const int nj = ntok - c0;  // valid tokens in this batch when fewer than kBatch
             if (a.splits > 1) {

@@ -194,21 +194,50 @@ def linear_dgrad(gy: torch.Tensor, w: NF4Weight, out: Optional[torch.Tensor] = N
 
 
 def grouped_fwd(x: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: int,
-                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                out: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                row_scale: Optional[torch.Tensor] = None, swiglu: bool = False) -> torch.Tensor:
     """nf4_grouped_fwd: rows offsets[e]..offsets[e+1] of x through expert e.
-    w is the stacked [E*N_e, K] weight; returns bf16 [T, N_e]."""
+    w is the stacked [E*N_e, K] weight; returns bf16 [T, N_e].
+    With an epilogue (nf4_grouped_fwd_ep): `bias` fp32 [E*N_e] per weight row,
+    `row_scale` fp32 [T] per output row (routing weights), `swiglu` for a weight whose
+    expert rows interleave gate and up in groups of 64 (see `interleave_gate_up`):
+    then y = silu(gate) * up, [T, N_e / 2]."""
     _check_act("grouped_fwd", x, w.K)
-    _need_cuda("grouped_fwd", offsets)
+    _need_cuda("grouped_fwd", offsets, bias, row_scale)
     if offsets.dtype != torch.int32 or offsets.numel() != experts + 1:
         raise ValueError("grouped_fwd: offsets must be int32 [E+1]")
     N_e = w.N // experts
     T = x.shape[0]
-    y = torch.empty(T, N_e, dtype=torch.bfloat16, device=x.device) if out is None else out
+    width = N_e // 2 if swiglu else N_e
+    y = torch.empty(T, width, dtype=torch.bfloat16, device=x.device) if out is None else out
     s = w.struct()
-    rc = _lib.lib().nf4_grouped_fwd(_ptr(x), _ptr(offsets), experts, T, x.stride(0), ctypes.byref(s),
-                                    N_e, _ptr(y), y.stride(0), _stream())
+    if bias is None and row_scale is None and not swiglu:
+        rc = _lib.lib().nf4_grouped_fwd(_ptr(x), _ptr(offsets), experts, T, x.stride(0),
+                                        ctypes.byref(s), N_e, _ptr(y), y.stride(0), _stream())
+    else:
+        for name, t, n in (("bias", bias, w.N), ("row_scale", row_scale, T)):
+            if t is not None and (t.dtype != torch.float32 or t.numel() != n or not t.is_contiguous()):
+                raise ValueError(f"grouped_fwd: {name} must be a contiguous fp32 tensor of {n} values")
+        ep = _lib.nf4_epilogue(_ptr(bias), _ptr(row_scale), 1 if swiglu else 0)
+        rc = _lib.lib().nf4_grouped_fwd_ep(_ptr(x), _ptr(offsets), experts, T, x.stride(0),
+                                           ctypes.byref(s), N_e, ctypes.byref(ep), _ptr(y),
+                                           y.stride(0), _stream())
     _lib.check(rc, "nf4_grouped_fwd")
     return y
+
+
+def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor, experts: int) -> torch.Tensor:
+    """Stack per-expert gate and up weights ([E*H, K] each, H a multiple of 64) into
+    the [E*2H, K] layout of the fused SwiGLU epilogue: each 128-row group holds 64
+    gate rows, then the up rows of the same 64 output columns.  Done on the dense
+    weight before quantisation."""
+    EH, K = gate.shape
+    H = EH // experts
+    if up.shape != gate.shape or EH != experts * H or H % 64 != 0:
+        raise ValueError("interleave_gate_up: gate and up must be [E*H, K] with H % 64 == 0")
+    g = gate.reshape(experts, H // 64, 1, 64, K)
+    u = up.reshape(experts, H // 64, 1, 64, K)
+    return torch.cat([g, u], dim=2).reshape(experts * 2 * H, K).contiguous()
 
 
 def grouped_dgrad(gy: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: int,

@@ -221,6 +221,27 @@ nf4_status nf4_linear_dgrad_f16(const void* gy, int64_t M, int64_t ldgy, const n
 nf4_status nf4_grouped_fwd(const void* x, const int32_t* offsets, int32_t E, int64_t T, int64_t ldx,
                            const nf4_weight* w, int64_t N_e, void* y, int64_t ldy, void* stream);
 
+/* nf4_grouped_fwd_ep -- nf4_grouped_fwd with the expert epilogue fused into the
+ * kernel (fork PR "Experts trainability" and Soup issue #842 run these in torch
+ * around the products): with a = x_e W_e^T per expert,
+ *   bias       [E*N_e] fp32 added per weight row (NULL: none);
+ *   swiglu     1: the weight rows of each expert are interleaved in groups of 128,
+ *              64 gate rows then the 64 up rows of the same output columns (N_e a
+ *              multiple of 128); y has N_e/2 columns, y = silu(g) * u with
+ *              silu(g) = g / (1 + exp(-g)), g and u including their biases;
+ *              0: y = a (+ bias), N_e columns;
+ *   row_scale  [T] fp32 multiplying each output row last (the tokens' routing
+ *              weights in the expert-sorted order; NULL: none).
+ * fp32 arithmetic, one bf16 rounding at the end; otherwise as nf4_grouped_fwd. */
+typedef struct {
+  const float* bias;
+  const float* row_scale;
+  int32_t swiglu;
+} nf4_epilogue;
+nf4_status nf4_grouped_fwd_ep(const void* x, const int32_t* offsets, int32_t E, int64_t T,
+                              int64_t ldx, const nf4_weight* w, int64_t N_e, const nf4_epilogue* ep,
+                              void* y, int64_t ldy, void* stream);
+
 /* nf4_grouped_dgrad -- per-expert input gradient gx[rows of e] = gy[rows of e] W_e.
  *   gy [T, N_e] bf16 (ldgy), gx [T, K] bf16 (ldgx); other arguments as above. */
 nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, int64_t T,

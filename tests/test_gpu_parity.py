@@ -629,3 +629,66 @@ def test_f16_autograd_and_stream_k(restore_stream_k):
     y2 = nf4.linear_fwd(x.detach(), w)
     assert nf4.path_counters()["stream_k"] == 1
     parity(y2, oracle.linear_fwd(_f16_bits(x), wf, dtype="f16"), "f16 stream-K fwd")
+
+
+# ------------------------------------------------------ expert epilogues --
+# nf4_grouped_fwd_ep: bias, routing-weight row scale and the SwiGLU of interleaved
+# gate/up weights fused into the grouped forward, against the oracle's fp64 steps.
+
+def _grouped_ep_case(E, N_e, K, counts, seed, interleave=False):
+    g = synth.generator(seed)
+    if interleave:
+        gate = synth.weight(E * N_e // 2, K, g)
+        up = synth.weight(E * N_e // 2, K, g)
+        w32 = nf4.interleave_gate_up(gate, up, E)
+    else:
+        w32 = synth.weight(E * N_e, K, g)
+    w = nf4.quantize(w32.to(DEV), double_quant=True)
+    st = oracle.quantize(w32.numpy(), ocb.nf4_code4(), 64, True, ocb.dynamic_code8(), 256)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = synth.activation(int(offs[-1]), K, g)
+    return w, st, offs, x, g
+
+
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_grouped_epilogue_bias_scale_swiglu(swiglu):
+    E, N_e, K = 4, 256, 320
+    counts = [5, 0, 70, 19]
+    w, st, offs, x, g = _grouped_ep_case(E, N_e, K, counts, seed=41 + swiglu, interleave=swiglu)
+    T = int(offs[-1])
+    bias = (torch.randn(E * N_e, generator=g) * 0.1).float()
+    scale = torch.rand(T, generator=g).float()
+    wb = oracle.dequantize(st, "bf16").reshape(E, N_e, K)
+    y = nf4.grouped_fwd(x.to(DEV), torch.from_numpy(offs).to(DEV), w, E, bias=bias.to(DEV),
+                        row_scale=scale.to(DEV), swiglu=swiglu)
+    ref = oracle.grouped_fwd_epilogue(bf16_bits(x), offs, wb, bias=bias.numpy(),
+                                      row_scale=scale.numpy(), swiglu=swiglu)
+    assert y.shape == (T, N_e // 2 if swiglu else N_e)
+    parity(y, ref, f"grouped epilogue swiglu={swiglu}")
+    # without the optional parts
+    y2 = nf4.grouped_fwd(x.to(DEV), torch.from_numpy(offs).to(DEV), w, E, swiglu=swiglu,
+                         bias=None, row_scale=None) if swiglu else None
+    if swiglu:
+        parity(y2, oracle.grouped_fwd_epilogue(bf16_bits(x), offs, wb, swiglu=True), "grouped swiglu only")
+
+
+def test_olmoe_fused_swiglu_and_routing_scale():
+    # OLMoE-shaped: 64 experts, hidden 2048, intermediate 1024 (gate and up
+    # interleaved: 2048 rows per expert), 512 tokens top-8 (4096 rows).
+    E, H, K = 64, 1024, 2048
+    g = synth.generator(43)
+    _, offs_t = synth.routing(512, E, 8, g)
+    offs = offs_t.numpy().astype(np.int32)
+    gate = synth.weight(E * H, K, g)
+    up = synth.weight(E * H, K, g)
+    w32 = nf4.interleave_gate_up(gate, up, E)
+    w = nf4.quantize(w32.to(DEV), double_quant=True)
+    st = oracle.quantize(w32.numpy(), ocb.nf4_code4(), 64, True, ocb.dynamic_code8(), 256)
+    T = int(offs[-1])
+    x = synth.activation(T, K, g)
+    scale = torch.rand(T, generator=g).float()
+    y = nf4.grouped_fwd(x.to(DEV), torch.from_numpy(offs).to(DEV), w, E, row_scale=scale.to(DEV),
+                        swiglu=True)
+    wb = oracle.dequantize(st, "bf16").reshape(E, 2 * H, K)
+    ref = oracle.grouped_fwd_epilogue(bf16_bits(x), offs, wb, row_scale=scale.numpy(), swiglu=True)
+    parity(y, ref, "olmoe fused swiglu")
