@@ -614,6 +614,53 @@ def run_grouped(dev, pk):
     out["tflops"] = round(total_fl / total_t / 1e12, 2)
     out["frac_tc"] = round(total_fl / total_t / 1e12 / pk["bf16_tflops"], 4)
     out["weight_gbs"] = round(total_b / total_t / 1e9, 1)
+
+    # Forward of the expert MLP's first half, h = silu(x Wg^T) * (x Wu^T) * routing
+    # weight: the fused epilogue over the interleaved gate/up weight, against two
+    # grouped products and the same steps in torch (the unfused form).
+    gate = synth.weight(E * I, H, g)
+    up = synth.weight(E * I, H, g)
+    wgu = nf4.quantize(nf4.interleave_gate_up(gate, up, E).to(dev), double_quant=True)
+    wg = nf4.quantize(gate.to(dev), double_quant=True)
+    wu = nf4.quantize(up.to(dev), double_quant=True)
+    x = synth.activation(T, H, g).to(dev)
+    rw = torch.rand(T, generator=g).to(dev)
+    h = torch.empty(T, I, dtype=torch.bfloat16, device=dev)
+    yg = torch.empty(T, I, dtype=torch.bfloat16, device=dev)
+    yu = torch.empty(T, I, dtype=torch.bfloat16, device=dev)
+    def fused():
+        ops.grouped_fwd(x, offs, wgu, E, out=h, row_scale=rw, swiglu=True)
+    def unfused():
+        ops.grouped_fwd(x, offs, wg, E, out=yg)
+        ops.grouped_fwd(x, offs, wu, E, out=yu)
+        h.copy_(torch.nn.functional.silu(yg.float()) * yu.float() * rw[:, None])
+    def time_graph(fn, reps=8):
+        s2 = torch.cuda.Stream(dev)
+        s2.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s2):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s2):
+            for _ in range(reps):
+                fn()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / reps)
+        del graph
+        return statistics.median(ts) * 1e-3
+    t_f, t_u = time_graph(fused), time_graph(unfused)
+    out["swiglu_gate_up_fwd"] = {"us_fused_epilogue": round(t_f * 1e6, 2),
+                                 "us_unfused_torch_glue": round(t_u * 1e6, 2),
+                                 "tflops_fused": round(2.0 * T * 2 * I * H / t_f / 1e12, 2)}
     return out
 
 
