@@ -4,7 +4,8 @@ The compute lives in ``libnf4.so`` (hand-written CUDA, C ABI in ``include/nf4.h`
 this package is its thin binding plus the autograd Functions.  Importing it does
 not load the library; the first call does, and fails loudly if it is not built.
 """
-from .autograd import NF4GroupedFn, NF4Linear, NF4LinearFn, nf4_grouped, nf4_linear
+from .autograd import (NF4GroupedFn, NF4GroupedSwiGLUFn, NF4Linear, NF4LinearFn, nf4_grouped,
+                       nf4_grouped_swiglu, nf4_linear)
 from .codebooks import code4_for, code_for, dynamic_code8, e4m3_code8, fp4_code4, nf4_code4
 from .ops import (NF4Weight, dequantize, device_check, device_status, grouped_dgrad, grouped_fwd,
                   interleave_gate_up,
@@ -23,7 +24,8 @@ nf4_grouped_dgrad = grouped_dgrad
 nf4_workspace_size = workspace_size
 
 __all__ = [
-    "NF4Weight", "NF4Linear", "NF4LinearFn", "NF4GroupedFn", "nf4_linear", "nf4_grouped",
+    "NF4Weight", "NF4Linear", "NF4LinearFn", "NF4GroupedFn", "NF4GroupedSwiGLUFn", "nf4_linear",
+    "nf4_grouped", "nf4_grouped_swiglu",
     "nf4_code4", "fp4_code4", "e4m3_code8", "code4_for", "code_for", "dynamic_code8", "quantize", "dequantize", "linear_fwd", "linear_dgrad",
     "grouped_fwd", "grouped_dgrad", "interleave_gate_up", "workspace_size", "path_counters", "reset_path_counters",
     "device_status", "device_check", "nf4_quantize", "nf4_dequantize", "nf4_linear_fwd",

@@ -71,6 +71,55 @@ class NF4GroupedFn(torch.autograd.Function):
         return (gx,) + (None,) * 12
 
 
+class NF4GroupedSwiGLUFn(torch.autograd.Function):
+    """h = silu(x_e Wg_e^T) * (x_e Wu_e^T) * rw for grouped experts whose gate and up
+    weights are interleaved (ops.interleave_gate_up) in one frozen 4-bit weight; the
+    forward is one fused kernel (nf4_grouped_fwd_ep).  The backward recomputes gate
+    and up with one grouped product, forms their gradients elementwise and returns
+    grad_x with one grouped input-gradient product over the interleaved weight; only
+    the quantised weight (through save_for_backward), x and rw are kept."""
+
+    @staticmethod
+    def forward(ctx, x, offsets, row_scale, packed, absmax, absmax_q, nested_absmax,
+                nested_offset, code4, code8, experts: int, N: int, K: int, double_quant: bool):
+        w = ops.NF4Weight.from_tensors(
+            (packed, absmax, absmax_q, nested_absmax, nested_offset, code4, code8), N, K,
+            double_quant)
+        h = ops.grouped_fwd(x.contiguous(), offsets, w, experts, row_scale=row_scale, swiglu=True)
+        ctx.save_for_backward(x, offsets, row_scale, packed, absmax, absmax_q, nested_absmax,
+                              nested_offset, code4, code8)
+        ctx.experts, ctx.N, ctx.K, ctx.double_quant = int(experts), int(N), int(K), bool(double_quant)
+        return h
+
+    @staticmethod
+    def backward(ctx, gh):
+        x, offsets, rw, *wt = ctx.saved_tensors
+        gx = None
+        if ctx.needs_input_grad[0]:
+            E = ctx.experts
+            w = ops.NF4Weight.from_tensors(tuple(wt), ctx.N, ctx.K, ctx.double_quant)
+            a = ops.grouped_fwd(x.contiguous(), offsets, w, E).float()  # [T, N_e] interleaved
+            T = a.shape[0]
+            grp = a.reshape(T, -1, 2, 64)
+            g, u = grp[:, :, 0, :], grp[:, :, 1, :]
+            d = gh.float().reshape(T, -1, 64)
+            if rw is not None:
+                d = d * rw[:, None, None]
+            sg = torch.sigmoid(g)
+            dg = d * u * (sg * (1.0 + g * (1.0 - sg)))   # d/dg of g * sigmoid(g)
+            du = d * g * sg
+            dgu = torch.stack([dg, du], dim=2).reshape(T, -1).to(torch.bfloat16).contiguous()
+            gx = ops.grouped_dgrad(dgu, offsets, w, E)
+        return (gx,) + (None,) * 13
+
+
+def nf4_grouped_swiglu(x: torch.Tensor, offsets: torch.Tensor, w: ops.NF4Weight, experts: int,
+                       row_scale: torch.Tensor = None) -> torch.Tensor:
+    """Fused expert SwiGLU over an interleaved gate/up weight (bf16 activations)."""
+    return NF4GroupedSwiGLUFn.apply(x, offsets, row_scale, *w.tensors(), experts, w.N, w.K,
+                                    w.double_quant)
+
+
 def nf4_linear(x: torch.Tensor, w: ops.NF4Weight) -> torch.Tensor:
     """Frozen NF4 Linear: the compute dtype is the activations' half-precision type,
     bf16 or fp16 (the dtype handling of Linear4bit, which Soup issue #842's "Design

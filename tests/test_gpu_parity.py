@@ -692,3 +692,30 @@ def test_olmoe_fused_swiglu_and_routing_scale():
     wb = oracle.dequantize(st, "bf16").reshape(E, 2 * H, K)
     ref = oracle.grouped_fwd_epilogue(bf16_bits(x), offs, wb, row_scale=scale.numpy(), swiglu=True)
     parity(y, ref, "olmoe fused swiglu")
+
+
+def test_grouped_swiglu_autograd_against_oracle():
+    # Gradient of sum(h * gh) w.r.t. x, following the backward's steps: gate and up
+    # recomputed by the grouped product (bf16 outputs), the SiLU derivative and the
+    # products in fp64, dg and du rounded to bf16 (the input-gradient operand).
+    E, N_e, K = 4, 256, 192
+    counts = [9, 40, 0, 23]
+    w, st, offs, x, g = _grouped_ep_case(E, N_e, K, counts, seed=44, interleave=True)
+    T = int(offs[-1])
+    rw = torch.rand(T, generator=g).float()
+    gh = synth.activation(T, N_e // 2, g)
+    xd = x.to(DEV).requires_grad_(True)
+    h = nf4.nf4_grouped_swiglu(xd, torch.from_numpy(offs).to(DEV), w, E, row_scale=rw.to(DEV))
+    h.backward(gh.to(DEV))
+    wb = oracle.dequantize(st, "bf16").reshape(E, N_e, K)
+    parity(h, oracle.grouped_fwd_epilogue(bf16_bits(x), offs, wb, row_scale=rw.numpy(), swiglu=True),
+           "swiglu autograd fwd")
+    a = oracle.grouped_fwd(bf16_bits(x), offs, wb)
+    a = oracle.bf16_bits_to_f32(oracle.f32_to_bf16_bits(a.astype(np.float32))).astype(np.float64)
+    a = a.reshape(T, -1, 2, 64)
+    gg, uu = a[:, :, 0, :], a[:, :, 1, :]
+    d = oracle.bf16_bits_to_f32(bf16_bits(gh)).astype(np.float64).reshape(T, -1, 64) * rw.numpy()[:, None, None]
+    sg = 1.0 / (1.0 + np.exp(-gg))
+    dgu = np.stack([d * uu * sg * (1 + gg * (1 - sg)), d * gg * sg], axis=2).reshape(T, -1)
+    ref = oracle.grouped_dgrad(oracle.f32_to_bf16_bits(dgu.astype(np.float32)), offs, wb)
+    parity(xd.grad, ref, "swiglu autograd dgrad")
