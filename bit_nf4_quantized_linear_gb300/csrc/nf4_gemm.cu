@@ -391,7 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < G::kStagesA; ++i) {
       // leader of a pair: its own decoders + one relayed arrival from the peer
-      mbar_init(bar_at(sh, kBarAFull + i), 4 + (CG == 2 && sh.rank == 0 ? 1 : 0));
+      // the leader of a pair also counts the peer's four decoder warps (they arrive
+      // remotely, with cluster-scope release)
+      mbar_init(bar_at(sh, kBarAFull + i), CG == 2 && sh.rank == 0 ? 8 : 4);
       mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -487,22 +489,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issuer --
-    if (CG == 2 && lane == 0 && sh.rank == 1) {
-      // The peer relays "decoded tile and activation half ready" for each stage to
-      // the leader with one cluster-scope arrive, so its decoders only signal
-      // locally.
-      uint32_t sa = 0, pha = 0;
-      bool ok = true;
-      Cursor cur = cursor_begin(a, unit, total_items);
-      Item it;
-      while (ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it)) {
-        for (int ks = it.ks0; ks < it.ks1; ++ks) {
-          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
-          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAFull + sa), 0));
-          if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
-        }
-      }
-    }
     if (lane == 0 && sh.rank == 0) {  // a pair's MMAs are issued by its leader
       constexpr uint32_t idesc = F16 ? idesc_f16_f32(kTileW * CG, BT, MODE == 1, false)
                                      : idesc_bf16_f32(kTileW * CG, BT, MODE == 1, false);
@@ -902,7 +888,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar_at(sh, kBarPEmpty + sp));  // the codes were consumed above
-        mbar_arrive(bar_at(sh, kBarAFull + sa));
+        if (CG == 2 && sh.rank == 1)
+          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAFull + sa), 0));
+        else
+          mbar_arrive(bar_at(sh, kBarAFull + sa));
       }
       sp += kDecGroups;
       if (sp >= static_cast<uint32_t>(G::kStagesP)) { sp -= G::kStagesP; php ^= 1u; }
