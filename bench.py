@@ -431,6 +431,18 @@ def run_sweep(dev, pk):
         t_f = timed([fwd])
         t_d = timed([bwd])
         t = t_f + t_d
+        # single-launch latency: one forward call between events on an idle stream
+        # (launch overhead included; the graphs above hide it)
+        singles = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record()
+                fwd(base)
+                b.record()
+            b.synchronize()
+            singles.append(a.elapsed_time(b) * 1e3)
+        t_single = statistics.median(singles)
         # comparison arms in the same session: dense bf16 cuBLAS (same shape, a dense
         # weight per replica) and dequantise-then-matmul (the unfused design)
         dense = [nf4.dequantize(w) for w in reps[:max(2, min(R, int(4 * L2_BYTES / (2 * N * K)) + 1))]]
@@ -477,6 +489,7 @@ def run_sweep(dev, pk):
                     "fwd_weight_gbs": round(wbytes / t_f / 1e9, 1),
                     "dgrad_weight_gbs": round(wbytes / t_d / 1e9, 1),
                     "replicas": R, "path_fwd": pf, "path_dgrad": pd,
+                    "single_launch_fwd_us": round(t_single, 2),
                     "cublas_dense_bf16_us": round(t_cub * 1e6, 2),
                     "dequant_then_matmul_us": round(t_deq * 1e6, 2)})
         del reps, x, gy, y, gx, wsb
