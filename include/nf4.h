@@ -176,11 +176,13 @@ nf4_status nf4_dequantize(const nf4_weight* w, void* out, int32_t out_dtype, voi
  *   M >= 0 (M == 0 is a no-op); K % 64 == 0; x 16-byte aligned.
  *   ws: device workspace of nf4_workspace_size(NF4_OP_LINEAR_FWD, M, N, K, 0)
  *   bytes (split-K partials for small M; may be NULL when that size is 0).
- *   Paths: M <= 4 runs the SIMT GEMV kernels (16-byte code loads, register
- *   codebook, bf16 x bf16 -> fp32 FMAs, warp-shuffle and in-CTA reductions in a
- *   fixed order); larger M runs the tcgen05 kernel (fp32 accumulation in tensor
- *   memory).  Split partials, when used, are summed in a fixed order by a second
- *   kernel.  No atomics. */
+ *   Paths (nf4_get_path_counters tells which ran): M <= 16 runs the warp-MMA
+ *   small-M kernels (mma.sync bf16, fixed-order cluster reduction; see
+ *   nf4_set_small_m_path for the SIMT GEMV and tiled alternatives); larger M, and
+ *   every M for 8-bit codes and the fp16 dtype, runs the tcgen05 kernel (fp32
+ *   accumulation in tensor memory) with the classic or stream-K schedule
+ *   (nf4_set_stream_k).  Split partials are summed in a fixed order, by a second
+ *   kernel (classic) or by the CTA finishing the tile (stream-K).  No atomics. */
 nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
                           int64_t ldy, void* ws, size_t ws_bytes, void* stream);
 
