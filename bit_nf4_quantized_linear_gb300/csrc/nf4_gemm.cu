@@ -11,21 +11,25 @@
 // #842, "Design sketch": a fused forward and a transposed fused backward that
 // never materialise W, with a deterministic reduction).
 //
-// Structure (one CTA per SM, persistent over work items):
-//   warp 0      TMA producer of packed-code tiles (a deep ring, far ahead);
-//   warp 14     TMA producer of activation tiles [BT tokens x 64] (128B swizzle);
-//   warps 6-13  decoders, two groups of four taking alternate stages: each thread
-//               turns one 64-value block (one absmax) into bf16 through a register
-//               codebook (byte permutes) and stores it in the UMMA canonical
-//               128B-swizzled layout of the A operand (K-major for the forward,
-//               MN-major for the input gradient) in a ring of decoded tiles;
+// Structure (one CTA per SM, persistent over its work; 19 warps):
+//   warp 0      TMA producer of code tiles (a deep ring, far ahead);
+//   warp 18     TMA producer of activation tiles [BT tokens x 64] (128B swizzle);
+//   warps 6-17  decoders, three groups of four, group g taking contraction steps
+//               j = g mod 3: each thread turns one 64-value block (one scale) into
+//               the 16-bit operand -- 4-bit codes through a register codebook (byte
+//               permutes), 8-bit codes through a per-lane shared codebook -- and
+//               stores it in the UMMA canonical 128B-swizzled layout of the A
+//               operand (K-major for the forward, MN-major for the input gradient);
 //   warp 1      MMA issuer: tcgen05.mma M=128 (weight rows / in-features), N=BT
 //               (tokens), K=16, fp32 accumulators in tensor memory, two
-//               accumulator buffers so the epilogue overlaps the next item;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, bf16 rounding, store.
-// Every output element is produced by exactly one CTA with a fixed order of MMAs;
-// when the contraction is split (small M only) the fp32 partials go to a
-// workspace and a second kernel adds them in split order.  No atomics anywhere.
+//               accumulator buffers so the epilogue overlaps the next item; one
+//               barrier wait and one commit per contraction step;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, rounding, bulk tensor
+//               stores through shared memory (or direct stores), the grouped
+//               expert epilogue (bias, row scale, SwiGLU), stream-K partials.
+// Every output element gets a fixed order of MMAs and, when its tile is split
+// (small-M contraction split, or stream-K), partials added in a fixed order: by a
+// second kernel, or by the CTA holding the tile's first steps.  No atomics.
 // Every wait is bounded; on timeout the kernel records the error and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
