@@ -64,6 +64,24 @@ def test_host_validation_rejects_before_launch(L):
     assert L.nf4_quantize(x, 0, 4, 64, 32, 0, 256, x, x, x, x, x, x, x, None, 0, None) == 7
     assert L.nf4_quantize(x, 0, 4, 64, 64, 1, 256, x, x, x, x, x, x, x, None, 0, None) == 4
     assert L.nf4_quantize(x, 9, 4, 64, 64, 0, 256, x, x, x, x, x, x, x, None, 0, None) == 1
+    assert L.nf4_quantize_8bit(x, 0, 4, 64, 32, 0, 256, x, x, x, x, x, x, x, None, 0, None) == 7
+    assert L.nf4_quantize_8bit(x, 0, 4, 64, 64, 1, 256, x, x, x, x, x, x, x, None, 0, None) == 4
+    # code width other than 4 or 8
+    w3 = _lib.nf4_weight(x, x, None, None, None, x, None, 128, 128, 64, 256, 0, 3)
+    assert L.nf4_linear_fwd(x, 4, 128, ctypes.byref(w3), x, 128, None, 0, None) == 1
+    # fp16 entry points share the host checks
+    w = _weight(K=100)
+    assert L.nf4_linear_fwd_f16(x, 4, 128, ctypes.byref(w), x, 128, None, 0, None) == 2
+    w = _weight()
+    assert L.nf4_linear_dgrad_f16(None, 0, 128, ctypes.byref(w), None, 128, None, 0, None) == 0
+    # grouped epilogue: required struct, SwiGLU needs N_e % 128 == 0 and N_e/2 output columns
+    ep = _lib.nf4_epilogue(None, None, 1)
+    assert L.nf4_grouped_fwd_ep(x, off, 2, 10, 128, ctypes.byref(w), 64, None, x, 64, None) == 1
+    assert L.nf4_grouped_fwd_ep(x, off, 2, 10, 128, ctypes.byref(w), 64, ctypes.byref(ep), x, 64, None) == 2
+    ep_bad = _lib.nf4_epilogue(None, None, 2)
+    assert L.nf4_grouped_fwd_ep(x, off, 1, 10, 128, ctypes.byref(w), 128, ctypes.byref(ep_bad), x, 64, None) == 1
+    assert L.nf4_grouped_fwd_ep(x, off, 1, 10, 128, ctypes.byref(w), 128, ctypes.byref(ep), x, 32, None) == 1
+    assert L.nf4_grouped_fwd_ep(x, off, 1, 0, 128, ctypes.byref(w), 128, ctypes.byref(ep), x, 64, None) == 0
 
 
 def test_quantize_workspace_size(L):
