@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--reps", type=int, default=3, help="fwd+dgrad pairs of the --single case")
     p.add_argument("--stream-k", choices=["auto", "off", "force"], default="auto",
                    help="schedule of the fused kernel (library default: auto)")
+    p.add_argument("--weight-prefetch", choices=["on", "off"], default="on",
+                   help="declare the weights frozen so kernels may read them before the "
+                        "previous kernel on the stream has finished (library default: off)")
     return p.parse_args()
 
 
@@ -214,7 +217,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     nf4.device_check()
     nf4.device_status(clear=True)
-    ops.set_weight_prefetch(True)  # frozen weights: the small-M kernels may read them early
+    ops.set_weight_prefetch(args.weight_prefetch == "on")  # frozen weights may be read early
     ops.set_stream_k({"off": 0, "auto": 1, "force": 2}[args.stream_k])
     sets, g = make_weights(dev, REPLICAS)
     xs, gys, xs_host, gys_host = make_acts(g, M_HEAD, dev)
@@ -340,8 +343,9 @@ def run_ours(args, rank, world, local_rank):
             "l2": f"inputs larger than L2: {REPLICAS} rotating weight replicas, "
                   f"{REPLICAS * weight_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB",
             "parallelism": f"replicas x{world}",
-            "weight_prefetch": "on (frozen weights; small-M kernels read them before the "
-                               "dependency on the previous kernel resolves)",
+            "weight_prefetch": ("on (frozen weights: kernels read them before the dependency "
+                                "on the previous kernel resolves)") if args.weight_prefetch == "on"
+                               else "off",
             "stream_k": args.stream_k,
         },
         "roofline": {

@@ -49,6 +49,7 @@ struct GemmArgs {
   int64_t ld_out;
   float* ws;  // split-K partials [splits][M][ncols]
   int* status;
+  int prefetch;  // dense: the weight may be read before the preceding grid has finished
   int tma_out;  // dense bf16 output written by bulk tensor stores (aligned out and ld_out)
   // Grouped forward epilogue (nf4_grouped_fwd_ep): fp32 bias per weight row, fp32
   // scale per output row (routing weights), SwiGLU of interleaved gate/up rows.

@@ -445,6 +445,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.ld_out = ld_out;
   a.ws = static_cast<float*>(ws);
   a.status = dev.status;
+  a.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
   const int64_t units = dev.sms / p.cg;
   int grid = static_cast<int>((p.items < units ? p.items : units) * p.cg);
   if (p.stream_k) {

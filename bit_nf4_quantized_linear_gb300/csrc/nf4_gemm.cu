@@ -150,6 +150,12 @@ struct Shared {
 
 __device__ __forceinline__ uint32_t bar_at(const Shared& sh, int i) { return sh.bars + 8u * i; }
 
+// 0 until the grid dependency has resolved (set when the weight-side roles start
+// early), then 1; the word after the tensor-memory slot, abort flag and item count.
+__device__ __forceinline__ volatile int* dep_done(const Shared& sh) {
+  return reinterpret_cast<volatile int*>(sh.tmem_slot + 3);
+}
+
 __device__ __forceinline__ void record_error(const GemmArgs& a, int code) {
   *reinterpret_cast<volatile int*>(a.status) = code;
 }
@@ -170,19 +176,24 @@ __device__ __forceinline__ void allow_dependents() {
 }
 
 // Bounded wait, slow path: true once the phase completed; false on abort (another
-// role gave up) or after kTimeoutNs, in which case the timeout is recorded.
+// role gave up) or after kTimeoutNs, in which case the timeout is recorded.  The
+// bound runs from the later of the wait's start and the resolution of the grid
+// dependency: the roles that start early wait on phases that follow it.
 // `cluster`: the phase is completed by arrivals from the other CTA of a pair, so
 // the wait acquires at cluster scope (only the leader's waits on the decoded-tile
 // and accumulator-empty barriers need it).
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, const Shared& sh,
                                              const GemmArgs& a, bool cluster) {
-  const uint64_t t0 = globaltimer_ns();
+  uint64_t t0 = globaltimer_ns();
   while (true) {
     if (cluster ? mbar_try_wait_sleep_cluster(bar, parity, kSleepHintNs)
                 : mbar_try_wait_sleep(bar, parity, kSleepHintNs))
       return true;
     if (*sh.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
+    const uint64_t now = globaltimer_ns();
+    if (!*dep_done(sh)) {
+      t0 = now;
+    } else if (now - t0 > kTimeoutNs) {
       *sh.abort_flag = 1;
       record_error(a, kStatusTimeout);
       return false;
@@ -383,7 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- prologue --
   // Local setup first (barriers, tensor memory, tensor-map prefetch): with
   // programmatic dependent launch it overlaps the previous kernel's tail.  Global
-  // memory is touched only after the grid dependency has resolved.
+  // memory is touched only after the grid dependency has resolved -- except, for a
+  // dense product whose weight the caller declared frozen (`early`), by the
+  // weight-side roles: the code producer and the decoders then stream and decode
+  // the first steps while the previous kernel drains, and only the activation
+  // producer and the epilogue (the readers of activations, the writers of
+  // outputs and partials) wait.
+  const bool early = a.prefetch != 0 && !a.grouped;
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::kStagesP; ++i) {
       mbar_init(bar_at(sh, kBarPFull + i), 1);
@@ -410,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarEpEmpty + i), 1);
     }
     *sh.abort_flag = 0;
+    *dep_done(sh) = early ? 0 : 1;
     fence_mbar_init();
   }
   if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
@@ -424,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
   }
-  grid_dependency_wait();
+  if (!early) grid_dependency_wait();
   allow_dependents();
   // The codebooks are loaded by the decoders alone (below), so the producers start
   // their first copies without waiting on those loads.
@@ -456,7 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma || warp == kWarpTmaX) {
     // ----------------------------------------------------------- producers --
     // Warp 0 streams packed-code tiles (deep ring, far ahead of the decoders);
-    // warp 14 streams activation tiles for the MMAs.
+    // warp 18 streams activation tiles for the MMAs.
+    if (early && warp == kWarpTmaX) {
+      grid_dependency_wait();
+      if (lane == 0) *dep_done(sh) = 1;
+    }
     if (lane == 0) {
       const bool is_pk = warp == kWarpTma;
       const int nst = is_pk ? G::kStagesP : G::kStagesX;
@@ -553,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kWarpDec0) {
     // ------------------------------------------------------------ epilogue --
+    if (early) grid_dependency_wait();
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
     const int row = 32 * q + lane;
     int acc_i = 0;
@@ -857,9 +880,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (m >= 0) {
         if (!wait_phase(bar_at(sh, kBarXEmpty + ms), mph, sh, a)) break;
       }
-      // The stage's activation tile (this CTA's half in a pair) must have landed
-      // before the MMA issuer is told the stage is ready.
-      if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
       uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
       if (BITS == 4) {
         const uint32_t wv[8] = {wc[0].x, wc[0].y, wc[0].z, wc[0].w, wc[1].x, wc[1].y, wc[1].z, wc[1].w};
@@ -888,6 +908,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
+      // The stage's activation tile (this CTA's half in a pair) must have landed
+      // before the MMA issuer is told the stage is ready; the decode above does not
+      // need it, so it may run before the activations exist.
+      if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {

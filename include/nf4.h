@@ -299,12 +299,14 @@ void nf4_set_cta_pairs(int32_t enabled);
 
 /* Declares (enabled != 0) that no kernel running just before a product call on
  * the same stream writes that call's weight tensors (packed codes, statistics,
- * codebooks), as holds for a frozen weight.  The small-M kernels are launched
+ * codebooks), as holds for a frozen weight.  The product kernels are launched
  * with programmatic dependent launch: they start while the previous kernel on
  * the stream drains and wait for it before they read activations or write
- * outputs.  With this declaration they also read the weight before that wait,
- * overlapping its HBM stream with the previous kernel's tail.  Off by default
- * (every read then follows the wait).  Results do not depend on the setting. */
+ * outputs.  With this declaration the small-M kernels and the dense fused
+ * kernel also read the weight before that wait (the fused kernel's code stream
+ * and decode of its first steps then overlap the previous kernel's tail; the
+ * grouped products keep every read after the wait).  Off by default (every read
+ * then follows the wait).  Results do not depend on the setting. */
 void nf4_set_weight_prefetch(int32_t enabled);
 
 /* Kernels for the dense products at small M (M <= 16), for comparisons and tests:

@@ -341,10 +341,13 @@ def test_small_m_identity_probe_exact(N, K, path, restore_small_m):
     np.testing.assert_array_equal(bf16_bits(gx), wb[:4])
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (8, 4096, 14336), (16, 1024, 4096)])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (8, 4096, 14336), (16, 1024, 4096),
+                                   (64, 4096, 4096), (512, 1024, 4096), (1536, 4096, 4096)])
 def test_weight_prefetch_leaves_results_unchanged(M, N, K, restore_small_m):
     """Reading the frozen weight before the grid dependency resolves changes only
-    timing: outputs are bit-identical with and without it, also back to back."""
+    timing: outputs are bit-identical with and without it, also back to back
+    (small-M kernels; the fused kernel with a contraction split, classic and
+    stream-K schedules)."""
     g = synth.generator(M + K)
     w = nf4.quantize(synth.weight(N, K, g).to(DEV), double_quant=True)
     x = synth.activation(M, K, g).to(DEV)
