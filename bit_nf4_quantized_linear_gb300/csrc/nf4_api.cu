@@ -306,13 +306,14 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     }
     if (cg == 1 && skm != NF4_STREAM_K_OFF && sms <= nf4::kSkMaxCtas) {
       // Stream-K: equal runs of the items' contraction steps, one per CTA (each at
-      // least one step), plus the split tiles' partials through L2: the CTA
-      // finishing a split tile waits about one L2 round trip per 16-token batch
-      // (measured on GB300: about 25000 cycles of fixed cost at 256-token tiles).
+      // least one step), whose steps measured about 2% slower than those of whole
+      // tiles, plus a fixed cost for the split tiles' partials (the CTA finishing a
+      // split tile brings the next CTA's partial into shared memory with one bulk
+      // copy; measured on GB300: about 19000 cycles at 256-token tiles).
       const int64_t U = wt * ttiles * ksteps;
       const int64_t G = U < sms ? U : sms;
-      const double t = static_cast<double>((U + G - 1) / G) * step_cycles(bt, 1) + 5000.0 +
-                       20000.0 * bt / 256.0;
+      const double t = static_cast<double>((U + G - 1) / G) * step_cycles(bt, 1) * 1.02 + 5000.0 +
+                       14000.0 * bt / 256.0;
       if (G >= 1 && t < sk_t * 0.999) {
         sk_t = t;
         sk_best = make_plan(M, ncols, contract, bt, 1, 1);

@@ -125,7 +125,12 @@ constexpr int kBarAccEmpty = 58;
 constexpr int kBarDrain = 60;
 constexpr int kBarEpFull = 61;   // SwiGLU epilogue: up values of a batch written (2 warp pairs)
 constexpr int kBarEpEmpty = 63;  // ... and read by the gate warp
-constexpr int kNumBars = 65;
+constexpr int kBarSkPart = 65;   // stream-K: a following CTA's partial landed (one per epilogue warp)
+constexpr int kNumBars = 69;
+// Misc region: codebooks (16 + 256 fp32), barriers, four words (tensor-memory
+// slot, abort flag, item count, dependency flag), three expert tables.
+static_assert((16 + 256) * 4 + kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * 4 <= kMiscBase,
+              "misc region overflow");
 
 struct Item {
   int64_t idx;    // item (tile) index
@@ -426,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarEpFull + i), 1);
       mbar_init(bar_at(sh, kBarEpEmpty + i), 1);
     }
+    for (int i = 0; i < kNumEpiWarps; ++i) mbar_init(bar_at(sh, kBarSkPart + i), 1);
     *sh.abort_flag = 0;
     *dep_done(sh) = early ? 0 : 1;
     fence_mbar_init();
@@ -607,6 +613,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto sk_slot = [&](int64_t c) {  // partial of CTA c, this quarter, token 0, this lane
         return a.sk_ws + ((c * 4 + q) * BT) * 32 + lane;
       };
+      // The owned segment is the CTA's last item, so when its accumulator is full
+      // the activation ring is idle (every tile loaded into it has been consumed by
+      // the MMAs).  The next CTA's partial of this warp's quarter (ntok x 128 bytes)
+      // then comes into the warp's part of that ring with one bulk copy, and the
+      // chunks below read it from shared memory instead of waiting on L2 per chunk;
+      // further CTAs' partials (tiles cut three or more ways) are read from global
+      // memory.  The sum order is the same either way.
+      const float* p_first = nullptr;  // partial of CTA unit + 1 in shared memory
+      if (CG == 1 && sk_own && own_last > unit &&
+          (reinterpret_cast<uintptr_t>(a.sk_ws) & 15u) == 0) {
+        static_assert(CG != 1 || G::kStagesX * G::kXStage >= kNumEpiWarps * BT * 128,
+                      "stream-K partials of the four row quarters fit in the activation ring");
+        float* land = reinterpret_cast<float*>(smem + G::kOffX) + q * (BT * 32);
+        const uint32_t bar = bar_at(sh, kBarSkPart + q);
+        if (lane == 0) {
+          fence_proxy_async_global();  // the flag acquired above, then the async-proxy read
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ntok) * 128u);
+          bulk_load_g2s(smem_addr(land), sk_slot(unit + 1) - lane, static_cast<uint32_t>(ntok) * 128u, bar);
+        }
+        __syncwarp();
+        if (!wait_phase(bar, 0, sh, a)) break;  // completes once: the owned tile is the last item
+        p_first = land + lane;
+      }
+      auto part_src = [&](int64_t c, int c0) -> const float* {
+        return (c == unit + 1 && p_first) ? p_first + c0 * 32 : sk_slot(c) + c0 * 32;
+      };
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
       // One 16-token batch: tensor-memory load, plus the following CTAs' partials.
       constexpr int kBatch = 16;
@@ -615,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (sk_own)
           for (int64_t c = unit + 1; c <= own_last; ++c) {
-            const float* src = sk_slot(c) + c0 * 32;
+            const float* src = part_src(c, c0);
 #pragma unroll
             for (int j = 0; j < kBatch; ++j)
               v[j] = __float_as_uint(__fadd_rn(__uint_as_float(v[j]), src[j * 32]));
@@ -632,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kBatch; ++j)
             if (c0 + j < ntok) dst[(c0 + j) * 32] = __uint_as_float(v[j]);
         }
+        fence_proxy_async_global();  // the owner may read the partial with a bulk copy
         __threadfence();  // every lane's partial stores, then the quarter's flag
         __syncwarp();
         if (lane == 0) flag_publish(a.sk_flags + unit * 4 + q, a.sk_epoch);
@@ -653,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           if (sk_own)
             for (int64_t c = unit + 1; c <= own_last; ++c) {
-              const float* src = sk_slot(c) + c0 * 32;
+              const float* src = part_src(c, c0);
               float p[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) p[j] = (BT > 16 || j < 16) ? src[j * 32] : 0.0f;
