@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
             "nf4_set_weight_prefetch": [I32],
             "nf4_set_small_m_path": [I32],
             "nf4_set_stream_k": [I32],
+            "nf4_inject_stream_k_timeout": [],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -121,6 +122,7 @@ def lib() -> ctypes.CDLL:
         L.nf4_set_weight_prefetch.restype = None
         L.nf4_set_small_m_path.restype = None
         L.nf4_set_stream_k.restype = None
+        L.nf4_inject_stream_k_timeout.restype = None
         _lib = L
         return _lib
 
@@ -164,6 +166,12 @@ STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_FORCE = 0, 1, 2
 
 def set_stream_k(mode: int):
     lib().nf4_set_stream_k(int(mode))
+
+
+def inject_stream_k_timeout():
+    """Failure-path test hook: the next stream-K launch's bounded waits run out
+    (NF4_ERR_TIMEOUT in the device status word); see nf4_inject_stream_k_timeout."""
+    lib().nf4_inject_stream_k_timeout()
 
 
 def set_weight_prefetch(enabled: bool):

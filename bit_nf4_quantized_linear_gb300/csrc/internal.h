@@ -66,6 +66,8 @@ struct GemmArgs {
   float* sk_ws;         // partial tiles [sk_ctas][4 row quarters][bt tokens][32 rows] fp32
   uint32_t* sk_flags;   // [sk_ctas][4]: partial of (CTA, row quarter) published
   uint32_t sk_epoch;    // value this launch publishes (never 0)
+  uint32_t sk_wait_xor; // the finishing CTA waits for sk_epoch ^ sk_wait_xor (0; the
+                        // failure-path test sets a bit no contributor publishes)
 };
 
 // Stream-K bookkeeping: ready flags live in a device array of kSkSlots launch

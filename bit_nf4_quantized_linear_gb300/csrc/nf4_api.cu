@@ -198,6 +198,9 @@ std::atomic<int> g_weight_prefetch{0};
 // Kernels for M <= 16 (nf4_set_small_m_path).
 std::atomic<int> g_small_m_path{NF4_SMALL_M_AUTO};
 
+// One-shot failure-path test hook (nf4_inject_stream_k_timeout).
+std::atomic<int> g_inject_sk_timeout{0};
+
 // Stream-K schedule of the fused kernel (nf4_set_stream_k).
 std::atomic<int> g_stream_k{NF4_STREAM_K_AUTO};
 
@@ -455,6 +458,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     a.sk_ctas = p.sk_ctas;
     a.sk_ws = static_cast<float*>(ws);
     a.sk_epoch = next_sk_epoch();
+    if (g_inject_sk_timeout.exchange(0, std::memory_order_relaxed)) a.sk_wait_xor = 0x80000000u;
     a.sk_flags = nf4::stream_k_flags(a.sk_epoch);
     if (!a.sk_flags) return cuda_fail(cudaGetLastError(), "stream-K flags");
     grid = p.sk_ctas;
@@ -748,6 +752,8 @@ void nf4_set_stream_k(int32_t mode) {
   if (mode >= NF4_STREAM_K_OFF && mode <= NF4_STREAM_K_FORCE)
     g_stream_k.store(mode, std::memory_order_relaxed);
 }
+
+void nf4_inject_stream_k_timeout(void) { g_inject_sk_timeout.store(1, std::memory_order_relaxed); }
 
 void nf4_set_weight_prefetch(int32_t enabled) {
   g_weight_prefetch.store(enabled ? 1 : 0, std::memory_order_relaxed);

@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t tile_end = (it.idx + 1) * a.ksteps;
         while (own_last + 1 < a.sk_ctas && sk_first_unit(a, own_last + 1) < tile_end) ++own_last;
         for (int64_t c = unit + 1; c <= own_last; ++c)
-          if (!flag_wait(a.sk_flags + c * 4 + q, a.sk_epoch, sh, a)) break;
+          if (!flag_wait(a.sk_flags + c * 4 + q, a.sk_epoch ^ a.sk_wait_xor, sh, a)) break;
       }
       auto sk_slot = [&](int64_t c) {  // partial of CTA c, this quarter, token 0, this lane
         return a.sk_ws + ((c * 4 + q) * BT) * 32 + lane;
@@ -633,7 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load_g2s(smem_addr(land), sk_slot(unit + 1) - lane, static_cast<uint32_t>(ntok) * 128u, bar);
         }
         __syncwarp();
-        if (!wait_phase(bar, 0, sh, a)) break;  // completes once: the owned tile is the last item
+        // Completes once (the owned tile is the last item).  Waited for even after
+        // another role gave up: the copy must land before the CTA may exit.
+        drain_phase(bar, 0, a);
         p_first = land + lane;
       }
       auto part_src = [&](int64_t c, int c0) -> const float* {

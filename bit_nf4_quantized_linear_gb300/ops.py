@@ -265,3 +265,4 @@ set_cta_pairs = _lib.set_cta_pairs
 set_weight_prefetch = _lib.set_weight_prefetch
 set_small_m_path = _lib.set_small_m_path
 set_stream_k = _lib.set_stream_k
+inject_stream_k_timeout = _lib.inject_stream_k_timeout

@@ -339,6 +339,15 @@ void nf4_set_small_m_path(int32_t path);
 enum { NF4_STREAM_K_OFF = 0, NF4_STREAM_K_AUTO = 1, NF4_STREAM_K_FORCE = 2 };
 void nf4_set_stream_k(int32_t mode);
 
+/* Failure-path test hook (host-side injection; no fault of any kind): arms a
+ * one-shot for the next stream-K launch of this process, whose finishing CTAs
+ * then wait for a flag value that no CTA publishes.  Their bounded waits run out
+ * (2 s), the kernel records NF4_ERR_TIMEOUT in the device status word
+ * (nf4_device_status), finishes its remaining work with whatever the partials
+ * hold, and exits normally; the device stays usable and later launches are
+ * unaffected.  The affected call's output is unspecified. */
+void nf4_inject_stream_k_timeout(void);
+
 /* Human-readable message of the last CUDA error that made a call of this thread
  * return NF4_ERR_CUDA ("no error" if none).  Static string. */
 const char* nf4_last_cuda_error(void);

@@ -463,6 +463,28 @@ def test_stream_k_forced_parity_and_reruns(M, N, K, restore_stream_k):
         assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx.view(torch.int16))
 
 
+def test_stream_k_wait_that_runs_out_reports_timeout(restore_stream_k):
+    """Failure detection without a fault: the injected launch's finishing CTAs wait
+    for a flag value no CTA publishes; the bounded waits (2 s) run out, the kernel
+    records NF4_ERR_TIMEOUT and exits, and the next launch is normal and correct."""
+    ops.set_stream_k(_lib.STREAM_K_FORCE)
+    M, N, K = 300, 640, 1024
+    w, st, g = _quant_pair(N, K, True, seed=5)
+    x = synth.activation(M, K, g).to(DEV)
+    nf4.device_status(clear=True)
+    nf4.reset_path_counters()
+    ops.inject_stream_k_timeout()
+    nf4.linear_fwd(x, w)
+    torch.cuda.synchronize()
+    assert nf4.path_counters()["stream_k"] == 1
+    assert nf4.device_status(clear=True) == 6  # NF4_ERR_TIMEOUT
+    y = nf4.linear_fwd(x, w)
+    torch.cuda.synchronize()
+    assert nf4.device_status() == 0
+    parity(y, oracle.linear_fwd(bf16_bits(x.cpu()), oracle.dequantize(st, "bf16")),
+           "stream-K launch after a timed-out one")
+
+
 def test_stream_k_off_and_on_agree_within_tolerance(restore_stream_k):
     M, N, K = 1536, 1024, 1024
     w, st, g = _quant_pair(N, K, True, seed=11)
