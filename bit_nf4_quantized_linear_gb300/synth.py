@@ -4,7 +4,7 @@ arithmetic (no quantisation, no dequantisation, no products): it only draws
 random tensors and routing patterns, so that the GPU path and the CPU oracle can
 be fed the very same inputs.
 
-Distributions (BASELINE configurations): weights ~ N(0, 0.02) fp32, activations
+Distributions (those of the benchmark workloads): weights ~ N(0, 0.02) fp32, activations
 and output gradients ~ N(0, 1) rounded to bf16, MoE router logits ~ U(0, 1).
 Everything is drawn from a CPU ``torch.Generator`` in a fixed order, then moved
 to the device by the caller.

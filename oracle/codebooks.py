@@ -37,7 +37,7 @@ levels ("blockwise dynamic map").
 
 ``dynamic_code8`` -- the signed 8-bit dynamic ("tree") map used for the nested
 absmax codes.  The pages name only "blockwise dynamic map" (fork PR "Experts
-trainability", commit 1 table, int8 row) and BASELINE fixes "8-bit blockwise".
+trainability", commit 1 table, int8 row); the nested statistics are 8-bit blockwise.
 Reading: the dynamic tree quantisation of Dettmers et al., 2022 ("8-bit
 Optimizers via Block-wise Quantization"): a sign, a run of leading zero bits that
 sets a decimal exponent, an indicator bit, and the remaining bits a linear

@@ -6,7 +6,7 @@ import torch
 import oracle
 from oracle import codebooks as ocb
 
-REL_FRO = 5e-3      # relative Frobenius error bound (BASELINE the benchmark spec)
+REL_FRO = 5e-3      # relative Frobenius error bound of the fused products
 ELEM = 1e-2         # per-element bound: |err| <= ELEM * (|ref| + rms(ref))
 
 

@@ -22,7 +22,7 @@ LIN8 = codebooks.linear_code8()
 # --------------------------------------------------------------- codebooks ----
 
 def test_code4_shape_endpoints_zero():
-    # BASELINE north star: "the 16-level codebook with an exact zero and +-1 endpoints".
+    # The NF4 codebook: 16 levels, an exact zero, endpoints -1 and +1.
     assert CODE4.dtype == np.float32 and CODE4.shape == (16,)
     assert np.all(np.diff(CODE4) > 0)
     assert CODE4[0] == -1.0 and CODE4[15] == 1.0 and CODE4[7] == 0.0
