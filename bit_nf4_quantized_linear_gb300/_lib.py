@@ -60,6 +60,21 @@ class nf4_epilogue(ctypes.Structure):
     ]
 
 
+class nf4_plan_info(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int32),
+        ("token_tile", ctypes.c_int32),
+        ("ctas_per_tile", ctypes.c_int32),
+        ("splits", ctypes.c_int32),
+        ("stream_k", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("items", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_uint64),
+    ]
+
+
+PLAN_KERNELS = {0: "fused", 1: "small_m_mma", 2: "simt_gemv"}
+
 _lock = threading.Lock()
 _lib = None
 
@@ -108,6 +123,7 @@ def lib() -> ctypes.CDLL:
             "nf4_set_small_m_path": [I32],
             "nf4_set_stream_k": [I32],
             "nf4_inject_stream_k_timeout": [],
+            "nf4_plan_query": [I32, I64, I64, I64, I32, I32, I32, ctypes.POINTER(nf4_plan_info)],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -166,6 +182,16 @@ STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_FORCE = 0, 1, 2
 
 def set_stream_k(mode: int):
     lib().nf4_set_stream_k(int(mode))
+
+
+def plan_query(op: int, M: int, N: int, K: int, sms: int, bits: int = 4, f16: bool = False) -> dict:
+    """The launch plan of a dense product (host only, no device needed)."""
+    r = nf4_plan_info()
+    check(lib().nf4_plan_query(int(op), int(M), int(N), int(K), int(sms), int(bits),
+                               1 if f16 else 0, ctypes.byref(r)), "nf4_plan_query")
+    d = {name: getattr(r, name) for name, _ in nf4_plan_info._fields_}
+    d["kernel"] = PLAN_KERNELS[d["kernel"]]
+    return d
 
 
 def inject_stream_k_timeout():

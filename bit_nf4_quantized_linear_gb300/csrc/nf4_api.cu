@@ -755,6 +755,31 @@ void nf4_set_stream_k(int32_t mode) {
 
 void nf4_inject_stream_k_timeout(void) { g_inject_sk_timeout.store(1, std::memory_order_relaxed); }
 
+nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t sms, int32_t bits,
+                          int32_t f16, nf4_plan_info* out) {
+  if (!out || (op != NF4_OP_LINEAR_FWD && op != NF4_OP_LINEAR_DGRAD) || sms < 1 ||
+      (bits != 4 && bits != 8) || (f16 && bits == 8) || M <= 0 || N <= 0 || K <= 0)
+    return NF4_ERR_INVALID_ARG;
+  const int mode = op == NF4_OP_LINEAR_FWD ? 0 : 1;
+  const Plan p = plan_dense(mode, M, N, K, sms, true, bits, f16 != 0);
+  nf4_plan_info r{};
+  r.kernel = p.skinny ? NF4_PLAN_SMALL_M_MMA : p.gemv ? NF4_PLAN_SIMT_GEMV : NF4_PLAN_FUSED;
+  r.token_tile = p.bt;
+  r.ctas_per_tile = p.cg;
+  r.splits = p.splits;
+  r.stream_k = p.stream_k ? 1 : 0;
+  if (p.skinny) {
+    r.grid = p.sk.S * p.sk.C;
+  } else if (!p.gemv) {
+    const int64_t units = sms / p.cg;
+    r.grid = p.stream_k ? p.sk_ctas : static_cast<int32_t>((p.items < units ? p.items : units) * p.cg);
+  }
+  r.items = p.items;
+  r.workspace_bytes = p.ws_bytes;
+  *out = r;
+  return NF4_OK;
+}
+
 void nf4_set_weight_prefetch(int32_t enabled) {
   g_weight_prefetch.store(enabled ? 1 : 0, std::memory_order_relaxed);
 }

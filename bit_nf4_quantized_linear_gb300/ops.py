@@ -266,3 +266,4 @@ set_weight_prefetch = _lib.set_weight_prefetch
 set_small_m_path = _lib.set_small_m_path
 set_stream_k = _lib.set_stream_k
 inject_stream_k_timeout = _lib.inject_stream_k_timeout
+plan_query = _lib.plan_query

@@ -339,6 +339,29 @@ void nf4_set_small_m_path(int32_t path);
 enum { NF4_STREAM_K_OFF = 0, NF4_STREAM_K_AUTO = 1, NF4_STREAM_K_FORCE = 2 };
 void nf4_set_stream_k(int32_t mode);
 
+/* The launch plan a dense product (NF4_OP_LINEAR_FWD / NF4_OP_LINEAR_DGRAD)
+ * takes, computed on the host without a device: a deterministic function of the
+ * shape, the SM count `sms`, the code width `bits` (4 or 8), the compute dtype
+ * (`f16` != 0: fp16) and the process-wide launch options (nf4_set_stream_k,
+ * nf4_set_small_m_path, nf4_set_cta_pairs).  For diagnostics and tests; the
+ * product calls compute the same plan with the current device's SM count.
+ * Returns NF4_ERR_INVALID_ARG for a null `out`, an unknown op, sms < 1,
+ * bits other than 4 / 8, fp16 with 8-bit codes or a non-positive dimension. */
+enum { NF4_PLAN_FUSED = 0, NF4_PLAN_SMALL_M_MMA = 1, NF4_PLAN_SIMT_GEMV = 2 };
+typedef struct nf4_plan_info {
+  int32_t kernel;          /* NF4_PLAN_*: tcgen05 tiles, warp-MMA small-M, SIMT GEMV   */
+  int32_t token_tile;      /* fused: tokens per tile (16 .. 256)                        */
+  int32_t ctas_per_tile;   /* fused: 2 when a CTA pair shares a 256-row tile, else 1    */
+  int32_t splits;          /* fused classic: contraction splits (1 = none)              */
+  int32_t stream_k;        /* fused: 1 for the stream-K schedule                        */
+  int32_t grid;            /* fused: CTAs launched; small-M MMA: clusters x CTAs per    */
+                           /* cluster; 0 for the GEMV kernels (sized at launch)         */
+  int64_t items;           /* fused: work items (tiles x splits)                        */
+  uint64_t workspace_bytes;/* workspace this plan needs                                */
+} nf4_plan_info;
+nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t sms, int32_t bits,
+                          int32_t f16, nf4_plan_info* out);
+
 /* Failure-path test hook (host-side injection; no fault of any kind): arms a
  * one-shot for the next stream-K launch of this process, whose finishing CTAs
  * then wait for a flag value that no CTA publishes.  Their bounded waits run out

@@ -1,0 +1,138 @@
+"""Host logic of the launch planner (nf4_plan_query: no device needed).
+
+The planner is a deterministic function of the shape, the SM count and the
+launch options.  These tests pin its decisions on the measured workloads
+(GB300: 152 SMs) and check invariants every plan must satisfy: the workspace
+it asks for covers what its kernels write, the grid fits the device, stream-K
+and CTA pairs only where the fused kernel supports them, the launch options
+take effect.
+"""
+import itertools
+
+import pytest
+
+from bit_nf4_quantized_linear_gb300 import _lib, build
+
+SMS = 152
+FWD, DGRAD = _lib.OP_LINEAR_FWD, _lib.OP_LINEAR_DGRAD
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    build.build()
+    _lib.lib()
+
+
+@pytest.fixture(autouse=True)
+def _default_options():
+    _lib.set_stream_k(_lib.STREAM_K_AUTO)
+    _lib.set_small_m_path(_lib.SMALL_M_AUTO)
+    _lib.set_cta_pairs(False)
+    yield
+    _lib.set_stream_k(_lib.STREAM_K_AUTO)
+    _lib.set_small_m_path(_lib.SMALL_M_AUTO)
+    _lib.set_cta_pairs(False)
+
+
+def q(op, M, N, K, sms=SMS, **kw):
+    return _lib.plan_query(op, M, N, K, sms, **kw)
+
+
+def test_plans_of_the_measured_workloads():
+    # K = N = 4096 sweep: stream-K where one wave leaves SMs idle and the cost
+    # model prefers it; whole tiles at M = 8192; a 2-way split at M = 512.
+    for M, sk in [(1536, 1), (2048, 1), (4096, 1), (8192, 0)]:
+        for op in (FWD, DGRAD):
+            p = q(op, M, 4096, 4096)
+            assert (p["kernel"], p["token_tile"], p["stream_k"]) == ("fused", 256, sk), (M, p)
+    p = q(FWD, 512, 4096, 4096)
+    assert (p["token_tile"], p["splits"], p["stream_k"], p["grid"]) == (256, 2, 0, 128)
+    # Llama-3.1-8B set at M = 512: k/v forward split 8 ways, k/v input gradient on
+    # 128-token tiles, gate/up/down on stream-K.
+    assert q(FWD, 512, 1024, 4096)["splits"] == 8
+    p = q(DGRAD, 512, 1024, 4096)
+    assert (p["token_tile"], p["splits"], p["stream_k"]) == (128, 1, 0)
+    for N, K in [(14336, 4096), (4096, 14336)]:
+        for op in (FWD, DGRAD):
+            assert q(op, 512, N, K)["stream_k"] == 1
+    # Small M: the warp-MMA kernels for a 4-bit bf16 product; fp16 compute and
+    # one-byte codes always take the fused kernel.
+    assert q(FWD, 1, 4096, 4096)["kernel"] == "small_m_mma"
+    assert q(DGRAD, 8, 4096, 4096)["kernel"] == "small_m_mma"
+    assert q(FWD, 1, 4096, 4096, f16=True)["kernel"] == "fused"
+    assert q(FWD, 1, 4096, 4096, bits=8)["kernel"] == "fused"
+
+
+SHAPES = list(itertools.product([1, 3, 16, 17, 32, 33, 100, 129, 300, 512, 700, 2048, 5000],
+                                [64, 320, 1000, 4096], [64, 1024, 4096]))
+
+
+@pytest.mark.parametrize("bits,f16", [(4, False), (8, False), (4, True)])
+def test_plan_invariants(bits, f16):
+    for (M, N, K), op in itertools.product(SHAPES, (FWD, DGRAD)):
+        p = q(op, M, N, K, bits=bits, f16=f16)
+        assert p == q(op, M, N, K, bits=bits, f16=f16)  # deterministic
+        ncols, contract = (N, K) if op == FWD else (K, N)
+        if bits == 8 or f16:
+            assert p["kernel"] == "fused"
+        if p["kernel"] != "fused":
+            assert M <= 16 and p["workspace_bytes"] >= 0
+            continue
+        bt = p["token_tile"]
+        assert bt in (16, 32, 64, 128, 256) and (bits == 4 or bt <= 128)
+        assert 1 <= p["grid"] <= SMS
+        ttiles = -(-M // bt)
+        wtiles = -(-ncols // (128 * p["ctas_per_tile"]))
+        assert p["items"] == wtiles * ttiles * p["splits"]
+        assert p["splits"] <= max(1, -(-contract // 64))
+        if p["stream_k"]:
+            assert p["splits"] == 1 and p["ctas_per_tile"] == 1
+            # one partial tile [4 row quarters][bt tokens][32 rows] fp32 per CTA
+            assert p["workspace_bytes"] == p["grid"] * 128 * bt * 4
+            assert p["grid"] == min(SMS, p["items"] * -(-contract // 64))
+        elif p["splits"] > 1:
+            assert p["workspace_bytes"] == p["splits"] * M * ncols * 4
+        else:
+            assert p["workspace_bytes"] == 0
+
+
+def test_launch_options_take_effect():
+    _lib.set_stream_k(_lib.STREAM_K_OFF)
+    assert all(q(op, M, 4096, 4096)["stream_k"] == 0
+               for op in (FWD, DGRAD) for M in (512, 1536, 2048, 4096))
+    _lib.set_stream_k(_lib.STREAM_K_FORCE)
+    for M in (33, 129, 700, 8192):
+        p = q(FWD, M, 1000, 1024)
+        assert p["stream_k"] == 1 and p["splits"] == 1, (M, p)
+    _lib.set_stream_k(_lib.STREAM_K_AUTO)
+    _lib.set_small_m_path(_lib.SMALL_M_SIMT)
+    assert q(FWD, 4, 4096, 4096)["kernel"] == "simt_gemv"
+    _lib.set_small_m_path(_lib.SMALL_M_TILES)
+    assert q(FWD, 4, 4096, 4096)["kernel"] == "fused"
+    _lib.set_small_m_path(_lib.SMALL_M_AUTO)
+    _lib.set_cta_pairs(True)
+    assert any(q(FWD, M, 4096, 4096)["ctas_per_tile"] == 2 for M in (2048, 4096, 8192))
+    _lib.set_cta_pairs(False)
+    assert all(q(FWD, M, 4096, 4096)["ctas_per_tile"] == 1 for M in (2048, 4096, 8192))
+
+
+def test_sm_count_changes_the_schedule_not_the_contract():
+    # Fewer SMs: more waves; the plan stays within the device and keeps its
+    # workspace rules (checked above); it never needs a GPU to compute.
+    for sms in (1, 8, 76, 148, 152, 160):
+        for M in (64, 2048):
+            p = q(FWD, M, 4096, 4096, sms=sms)
+            assert 1 <= p["grid"] <= sms
+
+
+@pytest.mark.parametrize("args", [
+    (0, 8, 64, 64, SMS, 4, 0),            # not a dense product
+    (FWD, 0, 64, 64, SMS, 4, 0),          # empty M
+    (FWD, 8, 64, 64, 0, 4, 0),            # no SMs
+    (FWD, 8, 64, 64, SMS, 6, 0),          # code width
+    (FWD, 8, 64, 64, SMS, 8, 1),          # fp16 with one-byte codes
+])
+def test_plan_query_rejects_bad_arguments(args):
+    op, M, N, K, sms, bits, f16 = args
+    with pytest.raises(_lib.NF4Error):
+        _lib.plan_query(op, M, N, K, sms, bits=bits, f16=bool(f16))
