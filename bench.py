@@ -683,12 +683,9 @@ def run_grouped(dev, pk):
 
 # ------------------------------------------------------------- CPU oracle --
 
-def cpu_baseline(target_s: float = 12.0):
-    """The CPU oracle as it stands, on a bounded sample of the headline workload:
-    all seven projections quantised and dequantised by the oracle, then S token rows
-    of the forward and S rows of the input gradient; the step time is scaled to
-    M = 512 rows as t_dequant + (512 / S) * t_rows."""
-    import numpy as np
+def oracle_workload():
+    """The headline workload for the CPU oracle (untimed setup): the seven
+    projections quantised by the oracle, and the activations / output gradients."""
     import oracle
     from oracle import codebooks as ocb
     from bit_nf4_quantized_linear_gb300 import synth
@@ -699,6 +696,17 @@ def cpu_baseline(target_s: float = 12.0):
         states.append(oracle.quantize(synth.weight(N, K, g).numpy(), code4, 64, True, code8, 256))
     xs = [synth.activation(M_HEAD, K, g) for _, K, N in synth.LLAMA8B_PROJ]
     gys = [synth.activation(M_HEAD, N, g) for _, K, N in synth.LLAMA8B_PROJ]
+    return states, xs, gys
+
+
+def cpu_baseline(target_s: float = 12.0, workload=None):
+    """The CPU oracle as it stands, on a bounded sample of the headline workload:
+    all seven projections dequantised by the oracle, then S token rows of the
+    forward and S rows of the input gradient; the step time is scaled to M = 512
+    rows as t_dequant + (512 / S) * t_rows."""
+    import numpy as np
+    import oracle
+    states, xs, gys = workload if workload is not None else oracle_workload()
     bits = lambda t: t.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
     wbs = [oracle.dequantize(st, "bf16") for st in states]
@@ -758,20 +766,30 @@ def run_single(args):
 
 
 def run_reference(args, rank, world):
+    """The oracle timed on the host cores (rank 0 only): up to three warm-up and
+    three timed steps, each a bounded sample of the headline workload, about a
+    minute in all whatever --steps / --warmup ask for; the line reports the steps
+    actually run."""
     if rank != 0:
         return None
-    steps = max(1, args.steps if args.steps <= 3 else 1)
+    steps = max(1, min(args.steps, 3))
+    warm = max(0, min(args.warmup, 3))
+    target = max(2.0, min(8.0, 48.0 / (steps + warm)))
+    wl = oracle_workload()
+    for _ in range(warm):
+        cpu_baseline(target_s=target, workload=wl)
     vals = []
     last = None
     for _ in range(steps):
-        last = cpu_baseline(target_s=8.0)
+        last = cpu_baseline(target_s=target, workload=wl)
         vals.append(last["value"])
     v = statistics.median(vals)
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": steps, "warmup": 0, "ms_per_step": last["s_per_step_scaled"] * 1e3,
+        "steps": steps, "warmup": warm, "ms_per_step": last["s_per_step_scaled"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "M": M_HEAD},
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_HEAD, "flops_per_step": flops_per_step(M_HEAD)},
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
