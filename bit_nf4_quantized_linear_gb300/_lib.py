@@ -64,7 +64,6 @@ class nf4_plan_info(ctypes.Structure):
     _fields_ = [
         ("kernel", ctypes.c_int32),
         ("token_tile", ctypes.c_int32),
-        ("ctas_per_tile", ctypes.c_int32),
         ("splits", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
         ("grid", ctypes.c_int32),
@@ -118,7 +117,6 @@ def lib() -> ctypes.CDLL:
             "nf4_device_check": [P],
             "nf4_last_cuda_error": [],
             "nf4_linear_fwd_noalloc": [P, I64, I64, W, P, I64, P],
-            "nf4_set_cta_pairs": [I32],
             "nf4_set_weight_prefetch": [I32],
             "nf4_set_small_m_path": [I32],
             "nf4_set_stream_k": [I32],
@@ -134,7 +132,6 @@ def lib() -> ctypes.CDLL:
         L.nf4_last_cuda_error.restype = ctypes.c_char_p
         L.nf4_get_path_counters.restype = None
         L.nf4_reset_path_counters.restype = None
-        L.nf4_set_cta_pairs.restype = None
         L.nf4_set_weight_prefetch.restype = None
         L.nf4_set_small_m_path.restype = None
         L.nf4_set_stream_k.restype = None
@@ -164,10 +161,6 @@ def device_status(clear: bool = False) -> int:
     v = ctypes.c_int32(0)
     check(lib().nf4_device_status(ctypes.byref(v), 1 if clear else 0), "nf4_device_status")
     return int(v.value)
-
-
-def set_cta_pairs(enabled: bool):
-    lib().nf4_set_cta_pairs(1 if enabled else 0)
 
 
 SMALL_M_AUTO, SMALL_M_SIMT, SMALL_M_TILES = 0, 1, 2

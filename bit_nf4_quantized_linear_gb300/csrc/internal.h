@@ -56,7 +56,7 @@ struct GemmArgs {
   const float* ep_bias;
   const float* ep_scale;
   int ep_swiglu;
-  // Stream-K schedule (dense, no pairs, splits == 1): the items * ksteps
+  // Stream-K schedule (dense, splits == 1): the items * ksteps
   // contraction steps are cut into sk_ctas equal contiguous runs, one per CTA.  A
   // tile cut between CTAs is finished by the CTA holding its first steps, which
   // adds the later runs' fp32 partials in CTA order.
@@ -147,11 +147,10 @@ cudaError_t launch_gemv_fwd(const GemvArgs& a, cudaStream_t s);
 cudaError_t launch_gemv_dgrad(const GemvArgs& a, cudaStream_t s);
 int gemv_fwd_kseg(int64_t K);
 int64_t gemv_dgrad_row_groups(int64_t N);
-// cg = 2 launches CTA pairs (clusters of two, tcgen05 cta_group::2; bt must be 256).
 // tmap_out: 16-bit output [M, ncols] with a 32 x 32 box, used when a.tma_out is set.
-// bits: code width of the weight (4, or 8 with cg == 1 and bt <= 128).  f16: fp16
-// activations, operand and output instead of bf16 (4-bit codes, cg == 1).
-cudaError_t launch_gemm(int mode, int bt, int cg, int bits, bool f16, const GemmArgs& a,
+// bits: code width of the weight (4, or 8 with bt <= 128).  f16: fp16 activations,
+// operand and output instead of bf16 (4-bit codes).
+cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,
                         const CUtensorMap& tmap_out, int grid, cudaStream_t s);
 cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,

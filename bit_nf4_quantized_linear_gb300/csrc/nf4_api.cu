@@ -163,7 +163,7 @@ int choose_bt(int64_t M) {
 }
 
 struct Plan {
-  int bt, cg, wtiles, ttiles, splits, ksteps;
+  int bt, wtiles, ttiles, splits, ksteps;
   int64_t items;
   size_t ws_bytes;
   bool gemv = false;  // small M: SIMT GEMV kernels
@@ -173,11 +173,10 @@ struct Plan {
   int sk_ctas = 0;
 };
 
-Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits, int cg = 1) {
+Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
   Plan p;
   p.bt = bt;
-  p.cg = cg;
-  p.wtiles = static_cast<int>((ncols + nf4::kTileW * cg - 1) / (nf4::kTileW * cg));
+  p.wtiles = static_cast<int>((ncols + nf4::kTileW - 1) / nf4::kTileW);
   p.ttiles = static_cast<int>((M + bt - 1) / bt);
   p.ksteps = static_cast<int>((contract + nf4::kTileK - 1) / nf4::kTileK);
   p.splits = splits;
@@ -185,11 +184,6 @@ Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits, i
   p.ws_bytes = splits > 1 ? static_cast<size_t>(splits) * M * ncols * sizeof(float) : 0;
   return p;
 }
-
-// Whether wide tiles may run as CTA pairs: off unless NF4_CTA_PAIR=1 is set or
-// nf4_set_cta_pairs(1) was called (on GB300 the pair's per-stage cross-CTA
-// handshake currently costs more than the shared-memory traffic it saves).
-std::atomic<int> g_cta_pairs{-1};
 
 // Whether the small-M kernels may read the weight before the grid dependency on
 // the previous kernel resolves (nf4_set_weight_prefetch).
@@ -213,22 +207,11 @@ uint32_t next_sk_epoch() {
   return e;
 }
 
-bool cta_pairs_enabled() {
-  int v = g_cta_pairs.load(std::memory_order_relaxed);
-  if (v < 0) {
-    const char* e = std::getenv("NF4_CTA_PAIR");
-    v = (e && e[0] == '1') ? 1 : 0;
-    g_cta_pairs.store(v, std::memory_order_relaxed);
-  }
-  return v != 0;
-}
-
 // Cycles of one 64-deep contraction step of a tile (per SM), as measured on
 // GB300 with the timeline probes: about 0.40 us for tiles of up to 128 tokens
 // (bound by the MMA issuer's barrier round trips), about 0.46 us for 256 tokens
 // (MMA time plus activation-ring stalls).
-double step_cycles(int bt, int cg) {
-  (void)cg;  // pairs are opt-in; when enabled they take 256-token tiles at equal cost
+double step_cycles(int bt) {
   if (bt >= 256) return 950.0;
   return 830.0;
 }
@@ -236,7 +219,7 @@ double step_cycles(int bt, int cg) {
 // Tile plan of a dense product: a deterministic function of the shape and the SM
 // count.  Small M: the narrowest token tile and, when the weight tiles cannot fill
 // the SMs, a split of the contraction while its fp32 partials stay small next to
-// the packed weight.  Larger M: token tile, CTA pairing and split chosen by a cost
+// the packed weight.  Larger M: token tile and split chosen by a cost
 // model in SM clocks -- waves of items times contraction steps, plus the split
 // partials' round trip through memory.
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true,
@@ -281,33 +264,32 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     return make_plan(M, ncols, contract, bt, static_cast<int>(s));
   }
   const int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : choose_bt(M);
-  const int cand_bt[4] = {256, 256, 128, 64};
-  const int cand_cg[4] = {2, 1, 1, 1};
+  const int cand_bt[3] = {256, 128, 64};
   const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
   const int skm = allow_sk ? g_stream_k.load(std::memory_order_relaxed) : NF4_STREAM_K_OFF;
   double best_t = 1e300, sk_t = 1e300;
   Plan best = make_plan(M, ncols, contract, bt_max, 1);
   Plan sk_best = best;
-  for (int ci = 0; ci < 4; ++ci) {
-    const int bt = cand_bt[ci], cg = cand_cg[ci];
-    if (bt > bt_max || (cg == 2 && (fused_only || !cta_pairs_enabled()))) continue;
+  for (int ci = 0; ci < 3; ++ci) {
+    const int bt = cand_bt[ci];
+    if (bt > bt_max) continue;
     const int64_t ttiles = (M + bt - 1) / bt;
-    const int64_t wt = (ncols + nf4::kTileW * cg - 1) / (nf4::kTileW * cg);
-    const int64_t units = sms / cg;
+    const int64_t wt = (ncols + nf4::kTileW - 1) / nf4::kTileW;
+    const int64_t units = sms;
     for (int si = 0; si < 7; ++si) {
       const int S = sp[si];
       if (S > 1 && ksteps / S < 8) break;
       const int64_t items = wt * ttiles * S;
       const int64_t waves = (items + units - 1) / units;
       const int64_t kps = (ksteps + S - 1) / S;
-      double t = static_cast<double>(waves) * (kps * step_cycles(bt, cg) + 3000.0);
+      double t = static_cast<double>(waves) * (kps * step_cycles(bt) + 3000.0);
       if (S > 1) t += static_cast<double>(S) * M * ncols * 8.0 / 3500.0;  // write + read partials
       if (t < best_t * 0.999) {
         best_t = t;
-        best = make_plan(M, ncols, contract, bt, S, cg);
+        best = make_plan(M, ncols, contract, bt, S);
       }
     }
-    if (cg == 1 && skm != NF4_STREAM_K_OFF && sms <= nf4::kSkMaxCtas) {
+    if (skm != NF4_STREAM_K_OFF && sms <= nf4::kSkMaxCtas) {
       // Stream-K: equal runs of the items' contraction steps, one per CTA (each at
       // least one step), whose steps measured about 2% slower than those of whole
       // tiles, plus a fixed cost for the split tiles' partials (the CTA finishing a
@@ -315,11 +297,11 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
       // copy; measured on GB300: about 19000 cycles at 256-token tiles).
       const int64_t U = wt * ttiles * ksteps;
       const int64_t G = U < sms ? U : sms;
-      const double t = static_cast<double>((U + G - 1) / G) * step_cycles(bt, 1) * 1.02 + 5000.0 +
+      const double t = static_cast<double>((U + G - 1) / G) * step_cycles(bt) * 1.02 + 5000.0 +
                        14000.0 * bt / 256.0;
       if (G >= 1 && t < sk_t * 0.999) {
         sk_t = t;
-        sk_best = make_plan(M, ncols, contract, bt, 1, 1);
+        sk_best = make_plan(M, ncols, contract, bt, 1);
         sk_best.stream_k = true;
         sk_best.sk_ctas = static_cast<int>(G);
         sk_best.ws_bytes = static_cast<size_t>(G) * nf4::kTileW * bt * sizeof(float);
@@ -420,7 +402,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   CUtensorMap tmap_act, tmap_pk;
   const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!encode_2d(&tmap_act, dt16, act, act_cols, M, ld_act * 2, 64,
-                 p.bt / p.cg, CU_TENSOR_MAP_SWIZZLE_128B))
+                 p.bt, CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   if (!encode_codes(&tmap_pk, w, mode)) return NF4_ERR_CUDA;
   nf4::GemmArgs a{};
@@ -450,8 +432,8 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.ws = static_cast<float*>(ws);
   a.status = dev.status;
   a.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
-  const int64_t units = dev.sms / p.cg;
-  int grid = static_cast<int>((p.items < units ? p.items : units) * p.cg);
+  const int64_t units = dev.sms;
+  int grid = static_cast<int>(p.items < units ? p.items : units);
   if (p.stream_k) {
     a.sk = 1;
     a.sk_units = p.items * p.ksteps;
@@ -473,7 +455,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
       return NF4_ERR_CUDA;
     a.tma_out = 1;
   }
-  cudaError_t le = nf4::launch_gemm(mode, p.bt, p.cg, bits, f16, a, tmap_act, tmap_pk, tmap_out, grid, s);
+  cudaError_t le = nf4::launch_gemm(mode, p.bt, bits, f16, a, tmap_act, tmap_pk, tmap_out, grid, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
   if (p.stream_k)  // a property of the launch just counted, not a launch of its own
@@ -553,7 +535,7 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   CUtensorMap tmap_out;  // unused: expert row ranges end inside tiles (direct stores)
   std::memset(&tmap_out, 0, sizeof(tmap_out));
   a.tma_out = 0;
-  cudaError_t le = nf4::launch_gemm(mode, bt, 1, w->bits == 8 ? 8 : 4, false, a, tmap_act,
+  cudaError_t le = nf4::launch_gemm(mode, bt, w->bits == 8 ? 8 : 4, false, a, tmap_act,
                                     tmap_pk, tmap_out, dev.sms, s);
   if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   count(mode == 0 ? NF4_PATH_GROUPED_FWD : NF4_PATH_GROUPED_DGRAD);
@@ -741,8 +723,6 @@ nf4_status nf4_device_status(int32_t* out, int32_t clear) {
 
 const char* nf4_last_cuda_error(void) { return g_last_error; }
 
-void nf4_set_cta_pairs(int32_t enabled) { g_cta_pairs.store(enabled ? 1 : 0, std::memory_order_relaxed); }
-
 void nf4_set_small_m_path(int32_t path) {
   if (path >= NF4_SMALL_M_AUTO && path <= NF4_SMALL_M_TILES)
     g_small_m_path.store(path, std::memory_order_relaxed);
@@ -765,14 +745,13 @@ nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t s
   nf4_plan_info r{};
   r.kernel = p.skinny ? NF4_PLAN_SMALL_M_MMA : p.gemv ? NF4_PLAN_SIMT_GEMV : NF4_PLAN_FUSED;
   r.token_tile = p.bt;
-  r.ctas_per_tile = p.cg;
   r.splits = p.splits;
   r.stream_k = p.stream_k ? 1 : 0;
   if (p.skinny) {
     r.grid = p.sk.S * p.sk.C;
   } else if (!p.gemv) {
-    const int64_t units = sms / p.cg;
-    r.grid = p.stream_k ? p.sk_ctas : static_cast<int32_t>((p.items < units ? p.items : units) * p.cg);
+    const int64_t units = sms;
+    r.grid = p.stream_k ? p.sk_ctas : static_cast<int32_t>(p.items < units ? p.items : units);
   }
   r.items = p.items;
   r.workspace_bytes = p.ws_bytes;

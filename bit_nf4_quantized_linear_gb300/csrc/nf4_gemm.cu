@@ -78,11 +78,11 @@ constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up t
 // BITS = 8: one code per byte (256-level codebook in shared memory after the base
 // misc region, one copy per lane: entry e of lane l in word 32 e + l, so the
 // lookups of a warp never share a bank).
-template <int BT, int CG, int BITS>
+template <int BT, int BITS>
 struct Geo {
   static constexpr int kPkStage = kTileW * kTileK * BITS / 8;  // codes of one step: 4 or 8 KB
   static constexpr int kMiscBytes = kMiscBase + (BITS == 8 ? 256 * 32 * 4 : 0);
-  static constexpr int kXStage = (BT / CG) * 128;  // this CTA's BT/CG token rows of 64 bf16
+  static constexpr int kXStage = BT * 128;  // BT token rows of 64 bf16
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
   // Decoded operand tiles: one slot more than decoder groups where the activation
   // tiles leave room, so a group never waits on the MMAs of the step just before.
@@ -106,8 +106,7 @@ struct Geo {
   static_assert(kStagesA >= kDecGroups && kStagesP >= kDecGroups && kStagesX >= kDecGroups,
                 "a decoder group advances every ring by kDecGroups slots per step");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
-  static_assert(CG == 1 || BT == 256, "CTA pairs are used with 256-token tiles");
-  static_assert(BITS == 4 || (BITS == 8 && CG == 1 && BT <= 128), "8-bit codes: tiles of <= 128 tokens");
+  static_assert(BITS == 4 || (BITS == 8 && BT <= 128), "8-bit codes: tiles of <= 128 tokens");
 };
 
 // Barrier slots in the misc region.  Three rings advance one stage per
@@ -142,7 +141,6 @@ struct Item {
 };
 
 struct Shared {
-  uint32_t rank;     // CTA rank in its pair (0 without pairs)
   float* code4;
   float* code8;
   uint32_t bars;  // shared address of barrier 0
@@ -184,16 +182,11 @@ __device__ __forceinline__ void allow_dependents() {
 // role gave up) or after kTimeoutNs, in which case the timeout is recorded.  The
 // bound runs from the later of the wait's start and the resolution of the grid
 // dependency: the roles that start early wait on phases that follow it.
-// `cluster`: the phase is completed by arrivals from the other CTA of a pair, so
-// the wait acquires at cluster scope (only the leader's waits on the decoded-tile
-// and accumulator-empty barriers need it).
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, const Shared& sh,
-                                             const GemmArgs& a, bool cluster) {
+                                             const GemmArgs& a) {
   uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (cluster ? mbar_try_wait_sleep_cluster(bar, parity, kSleepHintNs)
-                : mbar_try_wait_sleep(bar, parity, kSleepHintNs))
-      return true;
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*sh.abort_flag) return false;
     const uint64_t now = globaltimer_ns();
     if (!*dep_done(sh)) {
@@ -209,9 +202,9 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, cons
 // Bounded wait: an inline non-blocking test first (the common case on a pipelined
 // ring, where the phase has completed already), the sleeping slow path otherwise.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Shared& sh,
-                                           const GemmArgs& a, bool cluster = false) {
-  if (cluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, sh, a, cluster);
+                                           const GemmArgs& a) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, sh, a);
 }
 
 // Wait used while draining on exit: bounded, ignores the abort flag.
@@ -253,9 +246,8 @@ __device__ __noinline__ bool flag_wait(const uint32_t* f, uint32_t v, const Shar
   }
 }
 
-template <int MODE, int BT, int CG>
+template <int MODE, int BT>
 __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const Shared& sh) {
-  constexpr int kW = kTileW * CG;  // weight rows / in-features per (pair) tile
   Item it;
   it.idx = idx;
   if (!a.grouped) {
@@ -268,7 +260,7 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
     it.ks0 = static_cast<int>((s * a.ksteps) / a.splits);
     it.ks1 = static_cast<int>(((s + 1) * a.ksteps) / a.splits);
     it.split = static_cast<int>(s);
-    it.col0 = wt * kW + sh.rank * kTileW;
+    it.col0 = wt * kTileW;
     it.wrow0 = (MODE == 0) ? it.col0 : 0;
   } else {
     const int64_t g = idx / a.wtiles;
@@ -285,7 +277,7 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
     it.ks0 = 0;
     it.ks1 = a.ksteps;
     it.split = 0;
-    it.col0 = wt * kW + sh.rank * kTileW;
+    it.col0 = wt * kTileW;
     it.wrow0 = (MODE == 0) ? static_cast<int64_t>(e) * a.N_e + it.col0
                            : static_cast<int64_t>(e) * a.N_e;
   }
@@ -310,12 +302,12 @@ __device__ __forceinline__ Cursor cursor_begin(const GemmArgs& a, int64_t unit,
   return Cursor{unit, total_items};
 }
 
-template <int MODE, int BT, int CG>
+template <int MODE, int BT>
 __device__ __forceinline__ bool cursor_next(Cursor& c, const GemmArgs& a, const Shared& sh,
                                             int64_t nunits, Item& it) {
   if (c.pos >= c.end) return false;
   if (!a.sk) {
-    it = get_item<MODE, BT, CG>(c.pos, a, sh);
+    it = get_item<MODE, BT>(c.pos, a, sh);
     c.pos += nunits;
     return true;
   }
@@ -323,7 +315,7 @@ __device__ __forceinline__ bool cursor_next(Cursor& c, const GemmArgs& a, const 
   const int ks0 = static_cast<int>(c.pos - idx * a.ksteps);
   const int64_t left = c.end - c.pos;
   const int ks1 = left < a.ksteps - ks0 ? ks0 + static_cast<int>(left) : a.ksteps;
-  it = get_item<MODE, BT, CG>(idx, a, sh);
+  it = get_item<MODE, BT>(idx, a, sh);
   it.ks0 = ks0;
   it.ks1 = ks1;
   c.pos += ks1 - ks0;
@@ -364,12 +356,12 @@ __device__ __forceinline__ uint16_t to16(float f) {
   else return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-template <int MODE, int BT, int CG, int BITS, bool F16>
+template <int MODE, int BT, int BITS, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
                     const __grid_constant__ CUtensorMap tmap_pk,
                     const __grid_constant__ CUtensorMap tmap_out, const GemmArgs a) {
-  using G = Geo<BT, CG, BITS>;
+  using G = Geo<BT, BITS>;
   constexpr int kPkStage = G::kPkStage;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -378,10 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = raw_addr + pad;
 
   Shared sh;
-  sh.rank = CG == 2 ? cluster_ctarank() : 0u;
-  // Work items are per CTA, or per CTA pair.
-  const int64_t unit = CG == 2 ? blockIdx.x / 2 : blockIdx.x;
-  const int64_t nunits = CG == 2 ? gridDim.x / 2 : gridDim.x;
+  const int64_t unit = blockIdx.x;  // work items are per CTA
+  const int64_t nunits = gridDim.x;
   sh.code4 = reinterpret_cast<float*>(smem + G::kOffMisc);
   sh.code8 = sh.code4 + 16;
   uint64_t* bars_ptr = reinterpret_cast<uint64_t*>(sh.code8 + 256);
@@ -416,15 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarXEmpty + i), 1);
     }
     for (int i = 0; i < G::kStagesA; ++i) {
-      // leader of a pair: its own decoders + one relayed arrival from the peer
-      // the leader of a pair also counts the peer's four decoder warps (they arrive
-      // remotely, with cluster-scope release)
-      mbar_init(bar_at(sh, kBarAFull + i), CG == 2 && sh.rank == 0 ? 8 : 4);
+      mbar_init(bar_at(sh, kBarAFull + i), 4);  // the four decoder warps of the step's group
       mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_at(sh, kBarAccFull + i), 1);
-      mbar_init(bar_at(sh, kBarAccEmpty + i), kNumEpiWarps * CG);  // both CTAs' epilogues
+      mbar_init(bar_at(sh, kBarAccEmpty + i), kNumEpiWarps);
     }
     mbar_init(bar_at(sh, kBarDrain), 1);
     for (int i = 0; i < 2; ++i) {
@@ -439,13 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
   if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
   if (warp == kWarpMma) {
-    if (CG == 2) {
-      tmem_alloc_pair(smem_addr(sh.tmem_slot), G::kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
-      tmem_relinquish();
-    }
+    tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
+    tmem_relinquish();
     tc_fence_before();
   }
   if (!early) grid_dependency_wait();
@@ -471,7 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad) record_error(a, kStatusBadOffsets);
   }
   __syncthreads();
-  if (CG == 2) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *sh.tmem_slot;
   const int64_t total_items =
@@ -495,14 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       Cursor cur = cursor_begin(a, unit, total_items);
       Item it;
-      while (ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it)) {
+      while (ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it)) {
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           if (!wait_phase(bar_at(sh, bar_empty + st), ph ^ 1u, sh, a)) { ok = false; break; }
           const uint32_t full = bar_at(sh, bar_full + st);
           mbar_arrive_expect_tx(full, bytes);
           if (!is_pk)
             tma_load_2d(sbase + G::kOffX + st * G::kXStage, &tmap_act, full, ks * kTileK,
-                        static_cast<int32_t>(it.tok0 + sh.rank * (BT / CG)));
+                        static_cast<int32_t>(it.tok0));
           else if (MODE == 0)
             tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK * BITS / 8),
                         static_cast<int32_t>(it.wrow0));
@@ -521,9 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0 && sh.rank == 0) {  // a pair's MMAs are issued by its leader
-      constexpr uint32_t idesc = F16 ? idesc_f16_f32(kTileW * CG, BT, MODE == 1, false)
-                                     : idesc_bf16_f32(kTileW * CG, BT, MODE == 1, false);
+    if (lane == 0) {
+      constexpr uint32_t idesc = F16 ? idesc_f16_f32(kTileW, BT, MODE == 1, false)
+                                     : idesc_bf16_f32(kTileW, BT, MODE == 1, false);
       // Constant fields of the operand descriptors (address field zero).
       const uint64_t a_desc_hi = (MODE == 0) ? smem_desc_sw128(0, 16, 1024) : smem_desc_sw128(0, 8192, 1024);
       const uint64_t b_desc_hi = smem_desc_sw128(0, 16, 1024);
@@ -532,17 +513,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       Cursor cur = cursor_begin(a, unit, total_items);
       Item it;
-      for (; ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it); ++acc_i) {
+      for (; ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it); ++acc_i) {
         const int ab = acc_i & 1;
         const uint32_t acc_ph = (acc_i >> 1) & 1;
-        if (!wait_phase(bar_at(sh, kBarAccEmpty + ab), acc_ph ^ 1u, sh, a, CG == 2)) break;
+        if (!wait_phase(bar_at(sh, kBarAccEmpty + ab), acc_ph ^ 1u, sh, a)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BT);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           // The decoders signal a stage only after its activation tile landed, so
           // one wait per step covers both operands (every barrier operation of this
           // thread is serialised with its MMA issue).
-          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a, CG == 2)) { ok = false; break; }
+          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
           tc_fence_after();
           // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
           const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + sa * kAStage) >> 4);
@@ -551,31 +532,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
             const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(kk * 32 >> 4);
-            if (CG == 2)
-              mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
-            else
-              mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
           }
-          if (CG == 2) {  // frees the stage in both CTAs
-            mma_commit_pair(bar_at(sh, kBarAEmpty + sa), 0x3);
-            mma_commit_pair(bar_at(sh, kBarXEmpty + sx), 0x3);
-          } else {  // one "stage done" ring frees the activation and decoded slots
-            mma_commit(bar_at(sh, kBarXEmpty + sx));
-          }
+          // one "stage done" ring frees the activation and decoded slots
+          mma_commit(bar_at(sh, kBarXEmpty + sx));
           if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
           if (++sx == G::kStagesX) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
-        if (CG == 2)
-          mma_commit_pair(bar_at(sh, kBarAccFull + ab), 0x3);
-        else
-          mma_commit(bar_at(sh, kBarAccFull + ab));
+        mma_commit(bar_at(sh, kBarAccFull + ab));
       }
       // All MMAs issued must be complete before tensor memory is released.
-      if (CG == 2)
-        mma_commit_pair(bar_at(sh, kBarDrain), 0x1);
-      else
-        mma_commit(bar_at(sh, kBarDrain));
+      mma_commit(bar_at(sh, kBarDrain));
       drain_phase(bar_at(sh, kBarDrain), 0, a);
     }
     __syncwarp();
@@ -589,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ep_ok = true;  // false once an exchange wait gave up
     Cursor cur = cursor_begin(a, unit, total_items);
     Item it;
-    for (; ep_ok && cursor_next<MODE, BT, CG>(cur, a, sh, nunits, it); ++acc_i) {
+    for (; ep_ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it); ++acc_i) {
       const int ab = acc_i & 1;
       const uint32_t acc_ph = (acc_i >> 1) & 1;
       if (!wait_phase(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)) break;
@@ -621,9 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // further CTAs' partials (tiles cut three or more ways) are read from global
       // memory.  The sum order is the same either way.
       const float* p_first = nullptr;  // partial of CTA unit + 1 in shared memory
-      if (CG == 1 && sk_own && own_last > unit &&
+      if (sk_own && own_last > unit &&
           (reinterpret_cast<uintptr_t>(a.sk_ws) & 15u) == 0) {
-        static_assert(CG != 1 || G::kStagesX * G::kXStage >= kNumEpiWarps * BT * 128,
+        static_assert(G::kStagesX * G::kXStage >= kNumEpiWarps * BT * 128,
                       "stream-K partials of the four row quarters fit in the activation ring");
         float* land = reinterpret_cast<float*>(smem + G::kOffX) + q * (BT * 32);
         const uint32_t bar = bar_at(sh, kBarSkPart + q);
@@ -787,12 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if (CG == 2)
-          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAccEmpty + ab), 0));
-        else
-          mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
-      }
+      if (lane == 0) mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
     }
     if (lane == 0) bulk_wait_all();  // output tiles written before the CTA exits
     __syncwarp();
@@ -856,13 +819,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kAhead = 2;
     Cursor fcur = cursor_begin(a, unit, total_items);
     Item fit{};
-    bool fvalid = cursor_next<MODE, BT, CG>(fcur, a, sh, nunits, fit);
+    bool fvalid = cursor_next<MODE, BT>(fcur, a, sh, nunits, fit);
     int fks = fit.ks0;
     auto walk = [&](int n) {  // advance the walker n steps
       fks += n;
       while (fvalid && fks >= fit.ks1) {
         const int over = fks - fit.ks1;
-        fvalid = cursor_next<MODE, BT, CG>(fcur, a, sh, nunits, fit);
+        fvalid = cursor_next<MODE, BT>(fcur, a, sh, nunits, fit);
         if (fvalid) fks = fit.ks0 + over;
       }
     };
@@ -888,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kAhead; ++i) ring[i] = fetch_next();
     named_barrier_sync(1, kNumDecWarps * 32);  // code8 in shared memory
     uint32_t sp = grp, php = 0, sa = grp, pha = 0, sx = grp, phx = 0;
-    // Without pairs, decoded slot j mod kStagesA is free once the MMAs of step
+    // Decoded slot j mod kStagesA is free once the MMAs of step
     // m = j - kStagesA are done, which the "stage done" ring (depth kStagesX)
     // records in slot ms with phase parity mph.
     int m = grp - G::kStagesA;
@@ -910,9 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) wc[c] = *reinterpret_cast<const uint4*>(pk + pkc[c]);
       }
-      if (CG == 2) {
-        if (!wait_phase(bar_at(sh, kBarAEmpty + sa), pha ^ 1u, sh, a)) break;
-      } else if (m >= 0) {
+      if (m >= 0) {
         if (!wait_phase(bar_at(sh, kBarXEmpty + ms), mph, sh, a)) break;
       }
       uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
@@ -943,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(A + ((c ^ key) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      // The stage's activation tile (this CTA's half in a pair) must have landed
+      // The stage's activation tile must have landed
       // before the MMA issuer is told the stage is ready; the decode above does not
       // need it, so it may run before the activations exist.
       if (!wait_phase(bar_at(sh, kBarXFull + sx), phx, sh, a)) break;
@@ -951,10 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar_at(sh, kBarPEmpty + sp));  // the codes were consumed above
-        if (CG == 2 && sh.rank == 1)
-          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAFull + sa), 0));
-        else
-          mbar_arrive(bar_at(sh, kBarAFull + sa));
+        mbar_arrive(bar_at(sh, kBarAFull + sa));
       }
       sp += kDecGroups;
       if (sp >= static_cast<uint32_t>(G::kStagesP)) { sp -= G::kStagesP; php ^= 1u; }
@@ -974,15 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // A pair leaves together: the leader's MMAs (which write the peer's tensor memory)
-  // are drained and no remote arrive can target an exited CTA.
-  if (CG == 2) cluster_sync();
   if (warp == kWarpMma) {
     tc_fence_after();
-    if (CG == 2)
-      tmem_dealloc_pair(tmem_base, G::kTmemCols);
-    else
-      tmem_dealloc(tmem_base, G::kTmemCols);
+    tmem_dealloc(tmem_base, G::kTmemCols);
   }
 }
 
@@ -1057,68 +1009,58 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
-template <int MODE, int BT, int CG, int BITS, bool F16>
+template <int MODE, int BT, int BITS, bool F16>
 cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
                        const CUtensorMap& to, int grid,
                        cudaStream_t s) {
   static bool configured = false;
-  auto kern = nf4_gemm_kernel<MODE, BT, CG, BITS, F16>;
+  auto kern = nf4_gemm_kernel<MODE, BT, BITS, F16>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Geo<BT, CG, BITS>::kSmem);
+                                         Geo<BT, BITS>::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Geo<BT, CG, BITS>::kSmem;
+  cfg.dynamicSmemBytes = Geo<BT, BITS>::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CG == 2 ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tp, to, a);
 }
 
 template <int MODE>
-cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta,
-                        const CUtensorMap& tp, const CUtensorMap& to, int grid, cudaStream_t s) {
+cudaError_t launch_mode(int bt, const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
+                        const CUtensorMap& to, int grid, cudaStream_t s) {
 #if NF4_GEMM_MAIN_TU
-  if (cg == 2) {
-    if (bt != 256) return cudaErrorInvalidValue;
-    return launch_one<MODE, 256, 2, 4, false>(a, ta, tp, to, grid, s);
-  }
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1, 4, false>(a, ta, tp, to, grid, s);
-    case 32: return launch_one<MODE, 32, 1, 4, false>(a, ta, tp, to, grid, s);
-    case 64: return launch_one<MODE, 64, 1, 4, false>(a, ta, tp, to, grid, s);
-    case 128: return launch_one<MODE, 128, 1, 4, false>(a, ta, tp, to, grid, s);
-    case 256: return launch_one<MODE, 256, 1, 4, false>(a, ta, tp, to, grid, s);
+    case 16: return launch_one<MODE, 16, 4, false>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 4, false>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 4, false>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 4, false>(a, ta, tp, to, grid, s);
+    case 256: return launch_one<MODE, 256, 4, false>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #elif NF4_GEMM_F16
-  if (cg != 1) return cudaErrorInvalidValue;
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1, 4, true>(a, ta, tp, to, grid, s);
-    case 32: return launch_one<MODE, 32, 1, 4, true>(a, ta, tp, to, grid, s);
-    case 64: return launch_one<MODE, 64, 1, 4, true>(a, ta, tp, to, grid, s);
-    case 128: return launch_one<MODE, 128, 1, 4, true>(a, ta, tp, to, grid, s);
-    case 256: return launch_one<MODE, 256, 1, 4, true>(a, ta, tp, to, grid, s);
+    case 16: return launch_one<MODE, 16, 4, true>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 4, true>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 4, true>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 4, true>(a, ta, tp, to, grid, s);
+    case 256: return launch_one<MODE, 256, 4, true>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #else
-  if (cg != 1) return cudaErrorInvalidValue;
   switch (bt) {
-    case 16: return launch_one<MODE, 16, 1, 8, false>(a, ta, tp, to, grid, s);
-    case 32: return launch_one<MODE, 32, 1, 8, false>(a, ta, tp, to, grid, s);
-    case 64: return launch_one<MODE, 64, 1, 8, false>(a, ta, tp, to, grid, s);
-    case 128: return launch_one<MODE, 128, 1, 8, false>(a, ta, tp, to, grid, s);
+    case 16: return launch_one<MODE, 16, 8, false>(a, ta, tp, to, grid, s);
+    case 32: return launch_one<MODE, 32, 8, false>(a, ta, tp, to, grid, s);
+    case 64: return launch_one<MODE, 64, 8, false>(a, ta, tp, to, grid, s);
+    case 128: return launch_one<MODE, 128, 8, false>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #endif
@@ -1131,16 +1073,16 @@ cudaError_t launch_mode(int bt, int cg, const GemmArgs& a, const CUtensorMap& ta
 cudaError_t launch_gemm_f16(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
                             const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
                             cudaStream_t s) {
-  if (mode == 0) return launch_mode<0>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
-  return launch_mode<1>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  if (mode == 0) return launch_mode<0>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  return launch_mode<1>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
 #elif NF4_GEMM_BITS == 8
 // The 8-bit-code instances (this file compiled a second time, from nf4_gemm8.cu).
 cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensorMap& tmap_act,
                              const CUtensorMap& tmap_packed, const CUtensorMap& tmap_out, int grid,
                              cudaStream_t s) {
-  if (mode == 0) return launch_mode<0>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
-  return launch_mode<1>(bt, 1, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  if (mode == 0) return launch_mode<0>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  return launch_mode<1>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
 #else
 
@@ -1162,19 +1104,16 @@ uint32_t* stream_k_flags(uint32_t epoch) {
   return base + static_cast<size_t>(epoch % kSkSlots) * kSkMaxCtas * 4;
 }
 
-cudaError_t launch_gemm(int mode, int bt, int cg, int bits, bool f16, const GemmArgs& a,
+cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,
                         const CUtensorMap& tmap_out, int grid, cudaStream_t s) {
   if (f16) {
-    if (cg != 1 || bits != 4) return cudaErrorInvalidValue;
+    if (bits != 4) return cudaErrorInvalidValue;
     return launch_gemm_f16(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
   }
-  if (bits == 8) {
-    if (cg != 1) return cudaErrorInvalidValue;
-    return launch_gemm_8bit(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
-  }
-  if (mode == 0) return launch_mode<0>(bt, cg, a, tmap_act, tmap_packed, tmap_out, grid, s);
-  return launch_mode<1>(bt, cg, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  if (bits == 8) return launch_gemm_8bit(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  if (mode == 0) return launch_mode<0>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+  return launch_mode<1>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,

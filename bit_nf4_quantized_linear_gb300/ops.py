@@ -261,7 +261,6 @@ path_counters = _lib.path_counters
 reset_path_counters = _lib.reset_path_counters
 device_status = _lib.device_status
 device_check = _lib.device_check
-set_cta_pairs = _lib.set_cta_pairs
 set_weight_prefetch = _lib.set_weight_prefetch
 set_small_m_path = _lib.set_small_m_path
 set_stream_k = _lib.set_stream_k

@@ -288,15 +288,6 @@ void nf4_reset_path_counters(void);
  * device into *out (host int).  Synchronises with the device; not for hot paths. */
 nf4_status nf4_device_status(int32_t* out, int32_t clear);
 
-/* Lets (enabled != 0) or forbids (the default) wide tiles of the dense products
- * to run as CTA pairs (clusters of two sharing one tcgen05 M=256 MMA, each CTA
- * holding half of the activation tile).  On GB300 the pairs are currently slower
- * than single-CTA tiles, so they are off unless asked for.  The choice can change
- * the fp32 summation grouping, so results may differ in the last bit between the
- * two settings; each setting is deterministic.  NF4_CTA_PAIR=1 in the environment
- * sets the initial value to 1. */
-void nf4_set_cta_pairs(int32_t enabled);
-
 /* Declares (enabled != 0) that no kernel running just before a product call on
  * the same stream writes that call's weight tensors (packed codes, statistics,
  * codebooks), as holds for a frozen weight.  The product kernels are launched
@@ -343,7 +334,7 @@ void nf4_set_stream_k(int32_t mode);
  * takes, computed on the host without a device: a deterministic function of the
  * shape, the SM count `sms`, the code width `bits` (4 or 8), the compute dtype
  * (`f16` != 0: fp16) and the process-wide launch options (nf4_set_stream_k,
- * nf4_set_small_m_path, nf4_set_cta_pairs).  For diagnostics and tests; the
+ * nf4_set_small_m_path).  For diagnostics and tests; the
  * product calls compute the same plan with the current device's SM count.
  * Returns NF4_ERR_INVALID_ARG for a null `out`, an unknown op, sms < 1,
  * bits other than 4 / 8, fp16 with 8-bit codes or a non-positive dimension. */
@@ -351,7 +342,6 @@ enum { NF4_PLAN_FUSED = 0, NF4_PLAN_SMALL_M_MMA = 1, NF4_PLAN_SIMT_GEMV = 2 };
 typedef struct nf4_plan_info {
   int32_t kernel;          /* NF4_PLAN_*: tcgen05 tiles, warp-MMA small-M, SIMT GEMV   */
   int32_t token_tile;      /* fused: tokens per tile (16 .. 256)                        */
-  int32_t ctas_per_tile;   /* fused: 2 when a CTA pair shares a 256-row tile, else 1    */
   int32_t splits;          /* fused classic: contraction splits (1 = none)              */
   int32_t stream_k;        /* fused: 1 for the stream-K schedule                        */
   int32_t grid;            /* fused: CTAs launched; small-M MMA: clusters x CTAs per    */

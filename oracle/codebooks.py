@@ -22,8 +22,10 @@ E2M1 4-bit float (1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit;
 exponent 0 holds the subnormals 0 and 0.5), whose magnitudes are 0, 0.5, 1, 1.5,
 2, 3, 4 and 6, divided by the largest (6) so that the extremes are exactly +-1,
 and listed in ascending order with -0 before +0.  Because of that signed-zero
-pair the table is non-decreasing rather than strictly increasing; quantisation
-then never yields index 8 (+0), and an all-zero block uses index 7 (-0).
+pair the table is non-decreasing rather than strictly increasing.  The midpoint
+of the pair is 0, so a normalised value v quantises to index 7 (-0) when
+-1/24 <= v <= 0 (an all-zero block included) and to index 8 (+0) when
+0 < v <= 1/24 (the midpoint with 1/12 goes to the lower index).
 
 ``e4m3_code8`` -- the "fp8" 8-bit weight storage, which the pages describe as an
 "e4m3 codebook" on the same blockwise path (fork PR "Experts trainability",

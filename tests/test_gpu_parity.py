@@ -366,24 +366,20 @@ def test_weight_prefetch_leaves_results_unchanged(M, N, K, restore_small_m):
 
 @pytest.mark.parametrize("M,N,K,mode", [(512, 4096, 4096, 0), (512, 4096, 4096, 1), (1024, 640, 1024, 0),
                                         (700, 384, 2048, 1), (2048, 14336, 4096, 0)])
-def test_cta_pair_and_single_cta_tiles_both_match_oracle(M, N, K, mode):
-    from bit_nf4_quantized_linear_gb300 import ops
+def test_wide_tiles_classic_and_stream_k_match_oracle(M, N, K, mode, restore_stream_k):
+    # 256-token tiles on both schedules of the fused kernel: sampled rows against
+    # the oracle, each schedule bit-identical on a rerun.
     w, st, g = _quant_pair(N, K, True, seed=M + N)
     a = synth.activation(M, K if mode == 0 else N, g)
     wb = oracle.dequantize(st, "bf16")
     rows = _sampled_rows(M, 5)
     ref = (oracle.linear_fwd if mode == 0 else oracle.linear_dgrad)(bf16_bits(a), wb, rows)
     f = nf4.linear_fwd if mode == 0 else nf4.linear_dgrad
-    outs = []
-    try:
-        for pairs in (True, False):
-            ops.set_cta_pairs(pairs)
-            o = f(a.to(DEV), w)
-            parity(o[torch.from_numpy(rows).to(DEV)], ref, f"pairs={pairs} mode={mode} M={M}")
-            assert torch.equal(f(a.to(DEV), w).view(torch.int16), o.view(torch.int16))
-            outs.append(o)
-    finally:
-        ops.set_cta_pairs(False)
+    for sk in (_lib.STREAM_K_OFF, _lib.STREAM_K_FORCE):
+        ops.set_stream_k(sk)
+        o = f(a.to(DEV), w)
+        parity(o[torch.from_numpy(rows).to(DEV)], ref, f"stream_k={sk} mode={mode} M={M}")
+        assert torch.equal(f(a.to(DEV), w).view(torch.int16), o.view(torch.int16))
 
 
 # --------------------------------------------------------------- fp4 codebook --

@@ -4,8 +4,7 @@ The planner is a deterministic function of the shape, the SM count and the
 launch options.  These tests pin its decisions on the measured workloads
 (GB300: 152 SMs) and check invariants every plan must satisfy: the workspace
 it asks for covers what its kernels write, the grid fits the device, stream-K
-and CTA pairs only where the fused kernel supports them, the launch options
-take effect.
+only where the fused kernel supports it, the launch options take effect.
 """
 import itertools
 
@@ -27,11 +26,9 @@ def _library():
 def _default_options():
     _lib.set_stream_k(_lib.STREAM_K_AUTO)
     _lib.set_small_m_path(_lib.SMALL_M_AUTO)
-    _lib.set_cta_pairs(False)
     yield
     _lib.set_stream_k(_lib.STREAM_K_AUTO)
     _lib.set_small_m_path(_lib.SMALL_M_AUTO)
-    _lib.set_cta_pairs(False)
 
 
 def q(op, M, N, K, sms=SMS, **kw):
@@ -82,11 +79,11 @@ def test_plan_invariants(bits, f16):
         assert bt in (16, 32, 64, 128, 256) and (bits == 4 or bt <= 128)
         assert 1 <= p["grid"] <= SMS
         ttiles = -(-M // bt)
-        wtiles = -(-ncols // (128 * p["ctas_per_tile"]))
+        wtiles = -(-ncols // 128)
         assert p["items"] == wtiles * ttiles * p["splits"]
         assert p["splits"] <= max(1, -(-contract // 64))
         if p["stream_k"]:
-            assert p["splits"] == 1 and p["ctas_per_tile"] == 1
+            assert p["splits"] == 1
             # one partial tile [4 row quarters][bt tokens][32 rows] fp32 per CTA
             assert p["workspace_bytes"] == p["grid"] * 128 * bt * 4
             assert p["grid"] == min(SMS, p["items"] * -(-contract // 64))
@@ -110,10 +107,6 @@ def test_launch_options_take_effect():
     _lib.set_small_m_path(_lib.SMALL_M_TILES)
     assert q(FWD, 4, 4096, 4096)["kernel"] == "fused"
     _lib.set_small_m_path(_lib.SMALL_M_AUTO)
-    _lib.set_cta_pairs(True)
-    assert any(q(FWD, M, 4096, 4096)["ctas_per_tile"] == 2 for M in (2048, 4096, 8192))
-    _lib.set_cta_pairs(False)
-    assert all(q(FWD, M, 4096, 4096)["ctas_per_tile"] == 1 for M in (2048, 4096, 8192))
 
 
 def test_sm_count_changes_the_schedule_not_the_contract():
