@@ -8,7 +8,7 @@ from .autograd import (NF4GroupedFn, NF4GroupedSwiGLUFn, NF4Linear, NF4LinearFn,
                        nf4_grouped_swiglu, nf4_linear)
 from .codebooks import code4_for, code_for, dynamic_code8, e4m3_code8, fp4_code4, nf4_code4
 from .ops import (NF4Weight, dequantize, device_check, device_status, grouped_dgrad, grouped_fwd,
-                  interleave_gate_up,
+                  grouped_swiglu_bwd, interleave_gate_up,
                   linear_dgrad, linear_fwd, path_counters, quantize, reset_path_counters,
                   workspace_size)
 
@@ -21,13 +21,15 @@ nf4_linear_dgrad = linear_dgrad
 nf4_grouped_fwd = grouped_fwd
 nf4_grouped_fwd_ep = grouped_fwd
 nf4_grouped_dgrad = grouped_dgrad
+nf4_grouped_swiglu_bwd = grouped_swiglu_bwd
 nf4_workspace_size = workspace_size
 
 __all__ = [
     "NF4Weight", "NF4Linear", "NF4LinearFn", "NF4GroupedFn", "NF4GroupedSwiGLUFn", "nf4_linear",
     "nf4_grouped", "nf4_grouped_swiglu",
     "nf4_code4", "fp4_code4", "e4m3_code8", "code4_for", "code_for", "dynamic_code8", "quantize", "dequantize", "linear_fwd", "linear_dgrad",
-    "grouped_fwd", "grouped_dgrad", "interleave_gate_up", "workspace_size", "path_counters", "reset_path_counters",
+    "grouped_fwd", "grouped_dgrad", "grouped_swiglu_bwd", "interleave_gate_up", "workspace_size", "path_counters", "reset_path_counters",
     "device_status", "device_check", "nf4_quantize", "nf4_dequantize", "nf4_linear_fwd",
-    "nf4_linear_dgrad", "nf4_grouped_fwd", "nf4_grouped_dgrad", "nf4_workspace_size",
+    "nf4_linear_dgrad", "nf4_grouped_fwd", "nf4_grouped_dgrad", "nf4_grouped_swiglu_bwd",
+    "nf4_workspace_size",
 ]

@@ -22,7 +22,7 @@ STATUS_NAMES = {
     8: "NF4_ERR_BAD_OFFSETS",
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
-OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD = range(5)
+OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD, OP_GROUPED_SWIGLU_BWD = range(6)
 PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
          "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad", "skinny_fwd",
          "skinny_dgrad", "stream_k"]
@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
             "nf4_grouped_fwd": [P, P, I32, I64, I64, W, I64, P, I64, P],
             "nf4_grouped_dgrad": [P, P, I32, I64, I64, W, I64, P, I64, P],
             "nf4_grouped_fwd_ep": [P, P, I32, I64, I64, W, I64, ctypes.POINTER(nf4_epilogue), P, I64, P],
+            "nf4_grouped_swiglu_bwd": [P, P, I32, I64, I64, W, I64, ctypes.POINTER(nf4_epilogue), P, I64,
+                                       P, I64, P, P, SZ, P],
             "nf4_workspace_size": [I32, I64, I64, I64, I32],
             "nf4_status_string": [I32],
             "nf4_get_path_counters": [P],

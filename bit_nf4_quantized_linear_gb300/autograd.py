@@ -74,10 +74,12 @@ class NF4GroupedFn(torch.autograd.Function):
 class NF4GroupedSwiGLUFn(torch.autograd.Function):
     """h = silu(x_e Wg_e^T) * (x_e Wu_e^T) * rw for grouped experts whose gate and up
     weights are interleaved (ops.interleave_gate_up) in one frozen 4-bit weight; the
-    forward is one fused kernel (nf4_grouped_fwd_ep).  The backward recomputes gate
-    and up with one grouped product, forms their gradients elementwise and returns
-    grad_x with one grouped input-gradient product over the interleaved weight; only
-    the quantised weight (through save_for_backward), x and rw are kept."""
+    forward is one fused kernel (nf4_grouped_fwd_ep).  The backward is one library
+    call (nf4_grouped_swiglu_bwd): the kernel recomputes gate and up, forms their
+    gradients in its epilogue, and one grouped input-gradient product gives grad_x;
+    the routing weights get their gradient (sum over the row of silu(g) u dh) when
+    they require it.  Only the quantised weight (through save_for_backward), x and
+    rw are kept."""
 
     @staticmethod
     def forward(ctx, x, offsets, row_scale, packed, absmax, absmax_q, nested_absmax,
@@ -94,23 +96,16 @@ class NF4GroupedSwiGLUFn(torch.autograd.Function):
     @staticmethod
     def backward(ctx, gh):
         x, offsets, rw, *wt = ctx.saved_tensors
-        gx = None
-        if ctx.needs_input_grad[0]:
-            E = ctx.experts
+        gx = grw = None
+        need_rw = rw is not None and ctx.needs_input_grad[2]
+        if ctx.needs_input_grad[0] or need_rw:
             w = ops.NF4Weight.from_tensors(tuple(wt), ctx.N, ctx.K, ctx.double_quant)
-            a = ops.grouped_fwd(x.contiguous(), offsets, w, E).float()  # [T, N_e] interleaved
-            T = a.shape[0]
-            grp = a.reshape(T, -1, 2, 64)
-            g, u = grp[:, :, 0, :], grp[:, :, 1, :]
-            d = gh.float().reshape(T, -1, 64)
-            if rw is not None:
-                d = d * rw[:, None, None]
-            sg = torch.sigmoid(g)
-            dg = d * u * (sg * (1.0 + g * (1.0 - sg)))   # d/dg of g * sigmoid(g)
-            du = d * g * sg
-            dgu = torch.stack([dg, du], dim=2).reshape(T, -1).to(torch.bfloat16).contiguous()
-            gx = ops.grouped_dgrad(dgu, offsets, w, E)
-        return (gx,) + (None,) * 13
+            gx, grw = ops.grouped_swiglu_bwd(x.contiguous(), offsets, w, ctx.experts,
+                                             gh.contiguous(), row_scale=rw,
+                                             need_row_scale_grad=need_rw)
+            if not ctx.needs_input_grad[0]:
+                gx = None
+        return (gx, None, grw) + (None,) * 11
 
 
 def nf4_grouped_swiglu(x: torch.Tensor, offsets: torch.Tensor, w: ops.NF4Weight, experts: int,

@@ -56,6 +56,16 @@ struct GemmArgs {
   const float* ep_bias;
   const float* ep_scale;
   int ep_swiglu;
+  // Backward of the SwiGLU epilogue (ep_swiglu and ep_bwd set): the recomputed
+  // gate g and up u meet the upstream gradient dh [T, N_e / 2] (bf16, row pitch
+  // ep_ld_dh) and, instead of h, the kernel writes dg = dh r u silu'(g) and
+  // du = dh r silu(g) in bf16 at the weight rows' own columns of `out` ([T, N_e]),
+  // and, when ep_drw is set, per 32 gate columns the fp32 partial sum over those
+  // columns of silu(g) u dh into ep_drw[(N_e / 64) partials][T].
+  int ep_bwd;
+  const __nv_bfloat16* ep_dh;
+  int64_t ep_ld_dh;
+  float* ep_drw;
   // Stream-K schedule (dense, splits == 1): the items * ksteps
   // contraction steps are cut into sk_ctas equal contiguous runs, one per CTA.  A
   // tile cut between CTAs is finished by the CTA holding its first steps, which
@@ -161,6 +171,10 @@ cudaError_t launch_gemm_f16(int mode, int bt, const GemmArgs& a, const CUtensorM
                             cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  void* out, int64_t ld, bool f16, cudaStream_t s);
+// out[t] = sum over p = 0 .. P-1 in order of part[p][t] for rows inside the expert
+// ranges (offsets[0] <= t < offsets[E]), 0 for the other rows of [0, T).
+cudaError_t launch_row_partial_sum(const float* part, int P, int64_t T, const int32_t* offsets,
+                                   int E, float* out, cudaStream_t s);
 
 cudaError_t launch_quantize(const void* W, int w_dtype, int64_t numel, const float* code4,
                             uint8_t* packed, float* absmax, cudaStream_t s);

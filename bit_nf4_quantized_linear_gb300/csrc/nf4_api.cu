@@ -469,9 +469,25 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   return NF4_OK;
 }
 
+// Backward of the SwiGLU epilogue (nf4_grouped_swiglu_bwd): the grouped forward
+// kernel writes dg / du instead of h; `bwd` carries the upstream gradient and the
+// routing-weight partials.
+struct SwigluBwd {
+  const void* dh;
+  int64_t ld_dh;
+  float* drw;  // [N_e / 64][T] partials, or null
+};
+
+// Workspace of nf4_grouped_swiglu_bwd: dg / du in bf16 [T, N_e] (the whole block
+// padded to 256 bytes), then the routing-weight partials fp32 [N_e / 64][T].
+size_t swiglu_bwd_dgu_bytes(int64_t T, int64_t N_e) {
+  return (static_cast<size_t>(T) * N_e * 2 + 255) / 256 * 256;
+}
+
 nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_t E, int64_t T,
                        int64_t ld_act, const nf4_weight* w, int64_t N_e, void* out, int64_t ld_out,
-                       void* stream, const nf4_epilogue* ep = nullptr) {
+                       void* stream, const nf4_epilogue* ep = nullptr,
+                       const SwigluBwd* bwd = nullptr) {
   nf4_status st = check_weight(w);
   if (st != NF4_OK) return st;
   const int64_t K = w->K;
@@ -481,9 +497,10 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   const bool swiglu = ep && ep->swiglu;
   if (ep && (ep->swiglu != 0 && ep->swiglu != 1)) return NF4_ERR_INVALID_ARG;
   if (swiglu && N_e % 128 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  if (bwd && (mode != 0 || !swiglu)) return NF4_ERR_INVALID_ARG;
   const int64_t act_cols = mode == 0 ? K : N_e;
   const int64_t out_cols = mode == 0 ? N_e : K;
-  const int64_t out_width = swiglu ? N_e / 2 : out_cols;
+  const int64_t out_width = swiglu && !bwd ? N_e / 2 : out_cols;
   if (ld_act < act_cols || ld_out < out_width) return NF4_ERR_INVALID_ARG;
   if (T == 0) return NF4_OK;
   if (!act || !out) return NF4_ERR_INVALID_ARG;
@@ -530,6 +547,12 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
     a.ep_bias = ep->bias;
     a.ep_scale = ep->row_scale;
     a.ep_swiglu = ep->swiglu;
+  }
+  if (bwd) {
+    a.ep_bwd = 1;
+    a.ep_dh = static_cast<const __nv_bfloat16*>(bwd->dh);
+    a.ep_ld_dh = bwd->ld_dh;
+    a.ep_drw = bwd->drw;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tmap_out;  // unused: expert row ranges end inside tiles (direct stores)
@@ -661,8 +684,43 @@ nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, 
   return run_grouped(1, gy, offsets, E, T, ldgy, w, N_e, gx, ldgx, stream);
 }
 
+nf4_status nf4_grouped_swiglu_bwd(const void* x, const int32_t* offsets, int32_t E, int64_t T,
+                                  int64_t ldx, const nf4_weight* w, int64_t N_e,
+                                  const nf4_epilogue* ep, const void* gh, int64_t ldgh, void* gx,
+                                  int64_t ldgx, float* grad_row_scale, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!ep || ep->swiglu != 1) return NF4_ERR_INVALID_ARG;
+  if (grad_row_scale && !ep->row_scale) return NF4_ERR_INVALID_ARG;
+  if (T < 0 || N_e < 1 || ldgh < N_e / 2) return NF4_ERR_INVALID_ARG;
+  if (T == 0) return NF4_OK;
+  if (!gh || !gx) return NF4_ERR_INVALID_ARG;
+  if (ldgh % 8 != 0 || (reinterpret_cast<uintptr_t>(gh) & 15u) != 0) return NF4_ERR_ALIGNMENT;
+  const size_t need = nf4_workspace_size(NF4_OP_GROUPED_SWIGLU_BWD, T, N_e, w ? w->K : 0, E);
+  if (!ws || ws_bytes < need) return NF4_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NF4_ERR_ALIGNMENT;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* dgu = base;  // bf16 [T, N_e]
+  float* part = grad_row_scale ? reinterpret_cast<float*>(base + swiglu_bwd_dgu_bytes(T, N_e)) : nullptr;
+  SwigluBwd b{gh, ldgh, part};
+  nf4_status st = run_grouped(0, x, offsets, E, T, ldx, w, N_e, dgu, N_e, stream, ep, &b);
+  if (st != NF4_OK) return st;
+  st = run_grouped(1, dgu, offsets, E, T, N_e, w, N_e, gx, ldgx, stream);
+  if (st != NF4_OK) return st;
+  if (grad_row_scale) {
+    cudaError_t le = nf4::launch_row_partial_sum(part, static_cast<int>(N_e / 64), T, offsets, E,
+                                                 grad_row_scale, static_cast<cudaStream_t>(stream));
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+    count(NF4_PATH_SPLITK_REDUCE);
+  }
+  return NF4_OK;
+}
+
 size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E) {
   (void)E;
+  if (op == NF4_OP_GROUPED_SWIGLU_BWD) {
+    if (M <= 0 || N <= 0) return 0;
+    return swiglu_bwd_dgu_bytes(M, N) + static_cast<size_t>(N / 64) * M * sizeof(float);
+  }
   if (op == NF4_OP_QUANTIZE) {
     const int64_t nblocks = (N * K + 63) / 64;
     return static_cast<size_t>((nblocks + nf4::kMeanChunk - 1) / nf4::kMeanChunk) * 8;

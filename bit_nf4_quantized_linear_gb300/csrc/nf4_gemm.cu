@@ -681,12 +681,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows of the same 64 output columns, held by other TMEM lane quarters, so the
         // up warp (quarter p + 2) passes each 16-token batch to the gate warp
         // (quarter p) through shared memory (32 rows x 16 fp32, conflict-free), with
-        // a full / empty barrier pair per warp pair.  h = silu(g) * u, times the row
-        // scale; biases are added to g and u first.
+        // a full / empty barrier pair per warp pair.  Biases are added to g and u
+        // first.  Forward: h = silu(g) * u, times the row scale.  Backward (ep_bwd):
+        // with d = dh * r, dg = d u silu'(g) and du = d silu(g) go to the gate and up
+        // rows' columns, and the warp's 32 values of silu(g) u dh per token are summed
+        // (fixed butterfly) into its routing-weight partial.
         const int p = q & 1;
         float* xch = reinterpret_cast<float*>(smem + G::kOffOut) + p * (32 * kBatch);
         const float bias = a.ep_bias ? __ldg(a.ep_bias + it.wrow0 + row) : 0.0f;
-        uint16_t* op = reinterpret_cast<uint16_t*>(a.out) + it.tok0 * a.ld_out + it.col0 / 2 + row;
+        const bool bwd = a.ep_bwd != 0;
+        uint16_t* op = reinterpret_cast<uint16_t*>(a.out) + it.tok0 * a.ld_out +
+                       (bwd ? it.col0 + row : it.col0 / 2 + row);
+        const uint16_t* dhp = bwd ? reinterpret_cast<const uint16_t*>(a.ep_dh) + it.tok0 * a.ep_ld_dh +
+                                        it.col0 / 2 + row
+                                  : nullptr;
+        float* drw = (bwd && a.ep_drw) ? a.ep_drw + ((it.col0 >> 7) * 2 + q) * a.M + it.tok0 : nullptr;
         const bool gate_ok = q < 2 && it.col0 / 2 + row < a.ncols / 2;
 #pragma unroll 1
         for (int c0 = 0; c0 < ntok && ep_ok; c0 += kBatch, ++xb) {
@@ -707,9 +716,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kBatch; ++j) {
               const float g = __fadd_rn(__uint_as_float(v[j]), bias);
               const float u = xch[j * 32 + lane];
-              float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
-              if (a.ep_scale && j < nj) h = __fmul_rn(h, __ldg(a.ep_scale + it.tok0 + c0 + j));
-              if (gate_ok && j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = to16<F16>(h);
+              const bool tok_ok = j < nj;
+              const float r = (a.ep_scale && tok_ok) ? __ldg(a.ep_scale + it.tok0 + c0 + j) : 1.0f;
+              if (!bwd) {
+                float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                if (a.ep_scale) h = __fmul_rn(h, r);
+                if (gate_ok && tok_ok) op[static_cast<int64_t>(c0 + j) * a.ld_out] = to16<F16>(h);
+              } else {
+                const int64_t tj = static_cast<int64_t>(c0 + j);
+                const float dh = (gate_ok && tok_ok)
+                                     ? __uint_as_float(static_cast<uint32_t>(dhp[tj * a.ep_ld_dh]) << 16)
+                                     : 0.0f;
+                const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));  // sigmoid(g)
+                const float silu = __fmul_rn(g, sg);
+                const float d = __fmul_rn(dh, r);
+                // silu'(g) = s (1 + g (1 - s))
+                const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg))));
+                const float dg = __fmul_rn(__fmul_rn(d, u), dsilu);
+                const float du = __fmul_rn(d, silu);
+                if (gate_ok && tok_ok) {
+                  op[tj * a.ld_out] = to16<F16>(dg);
+                  op[tj * a.ld_out + 64] = to16<F16>(du);
+                }
+                if (drw) {  // routing-weight partial over this warp's 32 gate columns
+                  float t = __fmul_rn(__fmul_rn(silu, u), dh);
+#pragma unroll
+                  for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+                  if (lane == 0 && tok_ok) drw[tj] = t;
+                }
+              }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_at(sh, kBarEpEmpty + p));
@@ -1009,6 +1044,26 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
+#if NF4_GEMM_MAIN_TU
+// out[t] = sum over p in order of part[p * T + t] for rows inside the expert ranges
+// (offsets[0] <= t < offsets[E]), 0 elsewhere: the routing-weight gradient of the
+// SwiGLU backward from its per-32-column partials.
+__global__ void __launch_bounds__(256) row_partial_sum_kernel(const float* __restrict__ part, int P,
+                                                              int64_t T, const int32_t* __restrict__ offsets,
+                                                              int E, float* __restrict__ out) {
+  grid_dependency_wait();
+  allow_dependents();
+  const int64_t lo = offsets[0], hi = offsets[E];
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float acc = 0.0f;
+    if (t >= lo && t < hi)
+      for (int p = 0; p < P; ++p) acc = (p == 0) ? part[t] : __fadd_rn(acc, part[static_cast<int64_t>(p) * T + t]);
+    out[t] = acc;
+  }
+}
+#endif
+
 template <int MODE, int BT, int BITS, bool F16>
 cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
                        const CUtensorMap& to, int grid,
@@ -1114,6 +1169,23 @@ cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,
   if (bits == 8) return launch_gemm_8bit(mode, bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
   if (mode == 0) return launch_mode<0>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
   return launch_mode<1>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
+}
+
+cudaError_t launch_row_partial_sum(const float* part, int P, int64_t T, const int32_t* offsets,
+                                   int E, float* out, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  int64_t grid = (T + 255) / 256;
+  if (grid > 4096) grid = 4096;
+  if (grid < 1) grid = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, row_partial_sum_kernel, part, P, T, offsets, E, out);
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,

@@ -226,6 +226,40 @@ def grouped_fwd(x: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: i
     return y
 
 
+def grouped_swiglu_bwd(x: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: int,
+                       gh: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                       row_scale: Optional[torch.Tensor] = None, need_row_scale_grad: bool = False,
+                       ws: Optional[torch.Tensor] = None):
+    """nf4_grouped_swiglu_bwd: the backward of grouped_fwd(..., swiglu=True) over an
+    interleaved gate/up weight.  x bf16 [T, K] (the forward input), gh bf16
+    [T, N_e / 2].  Returns (grad_x bf16 [T, K], grad_row_scale fp32 [T] or None);
+    the second needs `row_scale` and `need_row_scale_grad`."""
+    _check_act("grouped_swiglu_bwd", x, w.K)
+    N_e = w.N // experts
+    _check_act("grouped_swiglu_bwd", gh, N_e // 2)
+    _need_cuda("grouped_swiglu_bwd", offsets, bias, row_scale)
+    if offsets.dtype != torch.int32 or offsets.numel() != experts + 1:
+        raise ValueError("grouped_swiglu_bwd: offsets must be int32 [E+1]")
+    T = x.shape[0]
+    for name, t, n in (("bias", bias, w.N), ("row_scale", row_scale, T)):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != n or not t.is_contiguous()):
+            raise ValueError(f"grouped_swiglu_bwd: {name} must be a contiguous fp32 tensor of {n} values")
+    gx = torch.empty(T, w.K, dtype=torch.bfloat16, device=x.device)
+    drw = (torch.empty(T, dtype=torch.float32, device=x.device)
+           if need_row_scale_grad and row_scale is not None else None)
+    need = workspace_size(_lib.OP_GROUPED_SWIGLU_BWD, T, N_e, w.K, experts)
+    if ws is None or ws.numel() * ws.element_size() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    ep = _lib.nf4_epilogue(_ptr(bias), _ptr(row_scale), 1)
+    s = w.struct()
+    rc = _lib.lib().nf4_grouped_swiglu_bwd(_ptr(x), _ptr(offsets), experts, T, x.stride(0),
+                                           ctypes.byref(s), N_e, ctypes.byref(ep), _ptr(gh),
+                                           gh.stride(0), _ptr(gx), gx.stride(0), _ptr(drw), _ptr(ws),
+                                           need, _stream())
+    _lib.check(rc, "nf4_grouped_swiglu_bwd")
+    return gx, drw
+
+
 def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor, experts: int) -> torch.Tensor:
     """Stack per-expert gate and up weights ([E*H, K] each, H a multiple of 64) into
     the [E*2H, K] layout of the fused SwiGLU epilogue: each 128-row group holds 64

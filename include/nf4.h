@@ -67,7 +67,8 @@ enum {
   NF4_OP_LINEAR_FWD = 1,
   NF4_OP_LINEAR_DGRAD = 2,
   NF4_OP_GROUPED_FWD = 3,
-  NF4_OP_GROUPED_DGRAD = 4
+  NF4_OP_GROUPED_DGRAD = 4,
+  NF4_OP_GROUPED_SWIGLU_BWD = 5  /* M = T rows, N = N_e, K; E experts */
 };
 
 /* Path counters (nf4_get_path_counters): how many launches each kernel got.
@@ -249,6 +250,34 @@ nf4_status nf4_grouped_fwd_ep(const void* x, const int32_t* offsets, int32_t E, 
 nf4_status nf4_grouped_dgrad(const void* gy, const int32_t* offsets, int32_t E, int64_t T,
                              int64_t ldgy, const nf4_weight* w, int64_t N_e, void* gx, int64_t ldgx,
                              void* stream);
+
+/* nf4_grouped_swiglu_bwd -- backward of nf4_grouped_fwd_ep with swiglu = 1 (fork
+ * PR "Experts trainability ...", commit 2: the backward recomputes the expert
+ * products from the frozen 4-bit weight and keeps no dequantised weight).  With
+ * h = silu(g) * u * r (r = row_scale[t], or 1), given the upstream gradient gh:
+ *   1. the grouped forward product is recomputed over the interleaved gate/up
+ *      weight and its epilogue forms, in fp32, s = 1 / (1 + exp(-g)),
+ *      dg = gh r u s (1 + g (1 - s)) and du = gh r g s, rounded to bf16 into the
+ *      workspace at the gate and up rows' own columns ([T, N_e]);
+ *   2. one grouped input-gradient product over the same weight turns them into
+ *      gx = [dg du]_e W_e for each expert's rows;
+ *   3. with grad_row_scale (needs ep->row_scale): grad_row_scale[t] = sum over
+ *      the row's N_e/2 outputs of silu(g) u gh, as fp32 partials per 32 gate
+ *      columns added in a fixed order (rows outside the expert ranges get 0).
+ *   x [T, K] bf16 (ldx), the forward's input; w, offsets, E, N_e, ep (swiglu must
+ *   be 1; bias and row_scale as in the forward) as in nf4_grouped_fwd_ep.
+ *   gh [T, N_e/2] bf16 (ldgh, a multiple of 8, 16-byte aligned); gx [T, K] bf16
+ *   (ldgx); grad_row_scale DEVICE fp32 [T] or NULL.
+ *   ws: device workspace of nf4_workspace_size(NF4_OP_GROUPED_SWIGLU_BWD, T, N_e,
+ *   K, E) bytes, 256-byte aligned (NF4_ERR_WORKSPACE / NF4_ERR_ALIGNMENT).
+ * Deterministic: no atomics; every output has a fixed summation order.  Returns
+ * NF4_ERR_INVALID_ARG for swiglu != 1, grad_row_scale without row_scale, or the
+ * argument errors of the grouped products. */
+nf4_status nf4_grouped_swiglu_bwd(const void* x, const int32_t* offsets, int32_t E, int64_t T,
+                                  int64_t ldx, const nf4_weight* w, int64_t N_e,
+                                  const nf4_epilogue* ep, const void* gh, int64_t ldgh, void* gx,
+                                  int64_t ldgx, float* grad_row_scale, void* ws, size_t ws_bytes,
+                                  void* stream);
 
 /* nf4_linear_fwd_noalloc -- the forward of nf4_linear_fwd without a workspace
  * argument, for callers that cannot allocate device memory themselves (for

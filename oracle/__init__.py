@@ -71,12 +71,14 @@ def lib():
             L.oracle_f32_from_f16.argtypes = [ctypes.c_uint16]
             L.oracle_f32_from_f16.restype = ctypes.c_float
             L.oracle_f16_array.argtypes = [P, i64, P]
+            L.oracle_bf16_array.argtypes = [P, i64, P]
             L.oracle_linear_fwd_f16.argtypes = [P, i64, i64, P, i64, P, i64, P]
             L.oracle_linear_dgrad_f16.argtypes = [P, i64, i64, P, i64, P, i64, P]
             L.oracle_num_threads.restype = ctypes.c_int
             for name in ("oracle_quantize_nf4", "oracle_double_quant", "oracle_decode_absmax",
                          "oracle_dequantize_nf4", "oracle_linear_fwd", "oracle_linear_dgrad",
                          "oracle_quantize_8bit", "oracle_dequantize_8bit", "oracle_f16_array",
+                         "oracle_bf16_array",
                          "oracle_linear_fwd_f16", "oracle_linear_dgrad_f16"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -106,12 +108,9 @@ def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
 def f32_to_bf16_bits(f: np.ndarray) -> np.ndarray:
     """fp32 -> bf16 bit patterns by round-to-nearest-even (the C oracle's rule)."""
     f = np.ascontiguousarray(f, dtype=np.float32)
-    flat = f.reshape(-1)
-    out = np.empty(flat.shape, dtype=np.uint16)
-    fn = lib().oracle_bf16_from_f32
-    for i, v in enumerate(flat.tolist()):
-        out[i] = fn(v)
-    return out.reshape(f.shape)
+    out = np.zeros(f.shape, dtype=np.uint16)
+    _check(lib().oracle_bf16_array(_p(f), f.size, _p(out)), "bf16_array")
+    return out
 
 
 # --------------------------------------------------------- quantisation ----
@@ -331,13 +330,76 @@ def grouped_fwd_epilogue(x_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray,
         for e in range(E):
             a[int(offsets[e]):int(offsets[e + 1])] += b[e]
     if swiglu:
-        T = a.shape[0]
-        grp = a.reshape(T, N // 128, 2, 64)
-        g, u = grp[:, :, 0, :], grp[:, :, 1, :]
-        a = (g / (1.0 + np.exp(-g)) * u).reshape(T, N // 2)
+        return swiglu_forward(a, row_scale)
     if row_scale is not None:
         a = a * np.asarray(row_scale, dtype=np.float32).astype(np.float64)[:, None]
     return a
+
+
+def _gate_up(a: np.ndarray):
+    """Views of the gate and up columns of an interleaved [T, N] array (each 128-column
+    group holds 64 gate columns, then the 64 up columns of the same outputs)."""
+    T, N = a.shape
+    grp = a.reshape(T, N // 128, 2, 64)
+    return grp[:, :, 0, :], grp[:, :, 1, :]
+
+
+def swiglu_forward(a: np.ndarray, row_scale=None) -> np.ndarray:
+    """h = silu(g) * u (* row_scale[t]) in fp64 from interleaved pre-activations a
+    [T, N]; silu(g) = g / (1 + exp(-g)).  Returns [T, N / 2]."""
+    g, u = _gate_up(np.asarray(a, dtype=np.float64))
+    h = (g / (1.0 + np.exp(-g)) * u).reshape(a.shape[0], a.shape[1] // 2)
+    if row_scale is not None:
+        h = h * np.asarray(row_scale, dtype=np.float32).astype(np.float64)[:, None]
+    return h
+
+
+def swiglu_backward(a: np.ndarray, dh: np.ndarray, row_scale=None):
+    """Gradients of h = silu(g) * u * r (r = row_scale[t], or 1) in fp64, the chain
+    rule of the fused expert SwiGLU written out (fork PR "Experts trainability",
+    commit 2: the backward recomputes the expert products and needs no saved dense
+    weight):
+      s = 1 / (1 + exp(-g)),  silu(g) = g s,  silu'(g) = s (1 + g (1 - s));
+      dg = dh r u silu'(g);   du = dh r silu(g);
+      dr = sum over the row's outputs of silu(g) u dh.
+    a: interleaved pre-activations [T, N] (bias included); dh: [T, N / 2].
+    Returns (dgu [T, N] in the same interleaved layout, dr [T] or None)."""
+    a = np.asarray(a, dtype=np.float64)
+    T, N = a.shape
+    g, u = _gate_up(a)
+    d = np.asarray(dh, dtype=np.float64).reshape(T, N // 128, 64)
+    r = None if row_scale is None else np.asarray(row_scale, dtype=np.float32).astype(np.float64)
+    s = 1.0 / (1.0 + np.exp(-g))
+    silu = g * s
+    dr = None if r is None else (silu * u * d).reshape(T, -1).sum(axis=1)
+    dd = d if r is None else d * r[:, None, None]
+    dgu = np.empty((T, N // 128, 2, 64), dtype=np.float64)
+    dgu[:, :, 0, :] = dd * u * (s * (1.0 + g * (1.0 - s)))
+    dgu[:, :, 1, :] = dd * silu
+    return dgu.reshape(T, N), dr
+
+
+def grouped_swiglu_dgrad(x_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray,
+                         dh_bf16: np.ndarray, bias=None, row_scale=None):
+    """Input gradient (and routing-weight gradient) of the fused expert SwiGLU over an
+    interleaved gate/up weight, in the order the backward takes its steps:
+      1. a = x_e W_e^T (+ bias), the exact fp64 product (grouped_fwd);
+      2. (dgu, dr) = swiglu_backward(a, dh, row_scale);
+      3. the gate/up gradient becomes an activation-dtype tensor: bf16(fp32(dgu)),
+         round to nearest even (the operand of the frozen input-gradient product,
+         as the activations are for the forward);
+      4. gx = grouped_dgrad(that operand) in fp64.
+    dh_bf16: bf16 bit patterns [T, N / 2].  Returns (gx fp64 [T, K], dr fp64 [T] or None)."""
+    E, N, K = wb_stack_bf16.shape
+    a = grouped_fwd(x_bf16, offsets, wb_stack_bf16)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float32).astype(np.float64).reshape(E, N)
+        for e in range(E):
+            a[int(offsets[e]):int(offsets[e + 1])] += b[e]
+    dh = bf16_bits_to_f32(dh_bf16).astype(np.float64)
+    dgu, dr = swiglu_backward(a, dh, row_scale)
+    op = f32_to_bf16_bits(dgu.astype(np.float32))
+    return grouped_dgrad(op, offsets, wb_stack_bf16), dr
 
 
 def grouped_dgrad(gy_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray) -> np.ndarray:

@@ -106,6 +106,13 @@ float oracle_f32_from_f16(uint16_t h) {
   return (float)((h & 0x8000u) ? -v : v);
 }
 
+/* oracle_bf16_from_f32 over an array. */
+int oracle_bf16_array(const float* in, int64_t n, uint16_t* out) {
+  if (n < 0 || (n > 0 && (!in || !out))) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_from_f32(in[i]);
+  return ORACLE_OK;
+}
+
 int oracle_f16_array(const float* in, int64_t n, uint16_t* out) {
   if (n < 0 || (n > 0 && (!in || !out))) return ORACLE_ERR_ARG;
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_from_f32(in[i]);

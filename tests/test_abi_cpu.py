@@ -92,3 +92,30 @@ def test_quantize_workspace_size(L):
 def test_path_counters_start_at_zero(L):
     _lib.reset_path_counters()
     assert all(v == 0 for v in _lib.path_counters().values())
+
+
+def test_swiglu_backward_host_validation(L):
+    x = ctypes.c_void_p(0x1000)
+    off = ctypes.c_void_p(0x1000)
+    w = _weight(N=256, K=128)
+    ep = _lib.nf4_epilogue(None, x, 1)
+    T, N_e = 10, 256
+    need = L.nf4_workspace_size(_lib.OP_GROUPED_SWIGLU_BWD, T, N_e, 128, 1)
+    # dg / du in bf16 (padded to 256 bytes), then N_e / 64 fp32 partials per row
+    assert need == (T * N_e * 2 + 255) // 256 * 256 + (N_e // 64) * T * 4
+    ws = ctypes.c_void_p(0x10000)
+    call = lambda ep_, drw, ws_, nbytes, ldgh=128, gh=x: L.nf4_grouped_swiglu_bwd(
+        x, off, 1, T, 128, ctypes.byref(w), N_e, ep_, gh, ldgh, x, 128, drw, ws_, nbytes, None)
+    assert call(None, None, ws, need) == 1                                   # epilogue required
+    assert call(ctypes.byref(_lib.nf4_epilogue(None, x, 0)), None, ws, need) == 1  # swiglu must be 1
+    no_scale = _lib.nf4_epilogue(None, None, 1)
+    assert call(ctypes.byref(no_scale), x, ws, need) == 1   # routing-weight grad without weights
+    assert call(ctypes.byref(ep), x, None, 0) == 4          # workspace missing
+    assert call(ctypes.byref(ep), x, ws, need - 4) == 4     # workspace too small
+    assert call(ctypes.byref(ep), x, ctypes.c_void_p(0x10010), need) == 3  # not 256-byte aligned
+    assert call(ctypes.byref(ep), x, ws, need, ldgh=64) == 1              # ldgh < N_e / 2
+    assert call(ctypes.byref(ep), x, ws, need, ldgh=132) == 3             # ldgh % 8
+    assert call(ctypes.byref(ep), x, ws, need, gh=ctypes.c_void_p(0x1008)) == 3
+    # T == 0 is a no-op
+    assert L.nf4_grouped_swiglu_bwd(x, off, 1, 0, 128, ctypes.byref(w), N_e, ctypes.byref(ep), None,
+                                    128, None, 128, None, None, 0, None) == 0

@@ -128,3 +128,56 @@ def test_checkpoint_recycled_slots_exact_and_ctx_control_wrong(cpu_products):
         assert torch.equal(got[i], ref[i]), i
     wrong = [i for i in range(L) if not torch.equal(ctl[i], ref[i])]
     assert wrong[:L - 2] == list(range(L - 2)), wrong
+
+
+def test_swiglu_function_returns_input_and_routing_weight_gradients(monkeypatch):
+    # NF4GroupedSwiGLUFn with the two library calls replaced by oracle-backed test
+    # doubles: the Function passes the saved x, offsets and routing weights to the
+    # backward call, and returns its grad_x and routing-weight gradient.
+    E, H, K = 2, 64, 64
+    rng = np.random.default_rng(5)
+    gate = (rng.standard_normal((E * H, K)) * 0.1).astype(np.float32)
+    up = (rng.standard_normal((E * H, K)) * 0.1).astype(np.float32)
+    w32 = oracle.interleave_gate_up(gate, up, E)
+    w = _weight_from(w32)
+    wb = oracle.dequantize(oracle.quantize(w32, ocb.nf4_code4(), 64, False), "bf16").reshape(E, 2 * H, K)
+    offs = np.array([0, 3, 7], np.int32)
+    bits = lambda t: t.detach().contiguous().view(torch.int16).numpy().view(np.uint16)
+    calls = {}
+
+    def fwd(x, offsets, w_, experts, out=None, bias=None, row_scale=None, swiglu=False):
+        h = oracle.grouped_fwd_epilogue(bits(x), offsets.numpy(), wb,
+                                        row_scale=None if row_scale is None else row_scale.numpy(),
+                                        swiglu=swiglu)
+        return torch.from_numpy(h).to(torch.bfloat16)
+
+    def bwd(x, offsets, w_, experts, gh, bias=None, row_scale=None, need_row_scale_grad=False, ws=None):
+        calls["need_rw"] = need_row_scale_grad
+        gx, dr = oracle.grouped_swiglu_dgrad(bits(x), offsets.numpy(), wb, bits(gh),
+                                             row_scale=None if row_scale is None else row_scale.numpy())
+        return (torch.from_numpy(gx).to(torch.bfloat16),
+                torch.from_numpy(dr).float() if need_row_scale_grad else None)
+
+    monkeypatch.setattr(ops, "grouped_fwd", fwd)
+    monkeypatch.setattr(ops, "grouped_swiglu_bwd", bwd)
+    x = torch.from_numpy(rng.standard_normal((7, K)).astype(np.float32)).to(torch.bfloat16)
+    rw = torch.from_numpy(rng.random(7).astype(np.float32))
+    gh = torch.from_numpy(rng.standard_normal((7, H)).astype(np.float32)).to(torch.bfloat16)
+    xr, rwr = x.clone().requires_grad_(True), rw.clone().requires_grad_(True)
+    h = nf4.nf4_grouped_swiglu(xr, torch.from_numpy(offs), w, E, row_scale=rwr)
+    h.backward(gh)
+    assert calls["need_rw"] is True
+    gx_ref, dr_ref = oracle.grouped_swiglu_dgrad(bits(x), offs, wb, bits(gh), row_scale=rw.numpy())
+    assert torch.equal(xr.grad, torch.from_numpy(gx_ref).to(torch.bfloat16))
+    assert torch.equal(rwr.grad, torch.from_numpy(dr_ref).float())
+    # routing weights that need no gradient are not asked for one
+    xr2 = x.clone().requires_grad_(True)
+    nf4.nf4_grouped_swiglu(xr2, torch.from_numpy(offs), w, E, row_scale=rw).backward(gh)
+    assert calls["need_rw"] is False and torch.equal(xr2.grad, xr.grad)
+
+
+def _weight_from(w32):
+    st = oracle.quantize(w32, ocb.nf4_code4(), 64, False)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    return ops.NF4Weight(t(st.packed), t(st.absmax), None, None, None, t(ocb.nf4_code4()), None,
+                         w32.shape[0], w32.shape[1], False)

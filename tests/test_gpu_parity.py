@@ -716,9 +716,8 @@ def test_olmoe_fused_swiglu_and_routing_scale():
 
 
 def test_grouped_swiglu_autograd_against_oracle():
-    # Gradient of sum(h * gh) w.r.t. x, following the backward's steps: gate and up
-    # recomputed by the grouped product (bf16 outputs), the SiLU derivative and the
-    # products in fp64, dg and du rounded to bf16 (the input-gradient operand).
+    # The backward is one library call; its input gradient and routing-weight
+    # gradient are compared with the oracle's grouped_swiglu_dgrad (fp64 steps).
     E, N_e, K = 4, 256, 192
     counts = [9, 40, 0, 23]
     w, st, offs, x, g = _grouped_ep_case(E, N_e, K, counts, seed=44, interleave=True)
@@ -726,17 +725,54 @@ def test_grouped_swiglu_autograd_against_oracle():
     rw = torch.rand(T, generator=g).float()
     gh = synth.activation(T, N_e // 2, g)
     xd = x.to(DEV).requires_grad_(True)
-    h = nf4.nf4_grouped_swiglu(xd, torch.from_numpy(offs).to(DEV), w, E, row_scale=rw.to(DEV))
+    rwd = rw.to(DEV).requires_grad_(True)
+    nf4.reset_path_counters()
+    h = nf4.nf4_grouped_swiglu(xd, torch.from_numpy(offs).to(DEV), w, E, row_scale=rwd)
     h.backward(gh.to(DEV))
+    c = nf4.path_counters()
+    assert c["grouped_fwd"] == 2 and c["grouped_dgrad"] == 1, c
     wb = oracle.dequantize(st, "bf16").reshape(E, N_e, K)
     parity(h, oracle.grouped_fwd_epilogue(bf16_bits(x), offs, wb, row_scale=rw.numpy(), swiglu=True),
            "swiglu autograd fwd")
-    a = oracle.grouped_fwd(bf16_bits(x), offs, wb)
-    a = oracle.bf16_bits_to_f32(oracle.f32_to_bf16_bits(a.astype(np.float32))).astype(np.float64)
-    a = a.reshape(T, -1, 2, 64)
-    gg, uu = a[:, :, 0, :], a[:, :, 1, :]
-    d = oracle.bf16_bits_to_f32(bf16_bits(gh)).astype(np.float64).reshape(T, -1, 64) * rw.numpy()[:, None, None]
-    sg = 1.0 / (1.0 + np.exp(-gg))
-    dgu = np.stack([d * uu * sg * (1 + gg * (1 - sg)), d * gg * sg], axis=2).reshape(T, -1)
-    ref = oracle.grouped_dgrad(oracle.f32_to_bf16_bits(dgu.astype(np.float32)), offs, wb)
-    parity(xd.grad, ref, "swiglu autograd dgrad")
+    gx_ref, drw_ref = oracle.grouped_swiglu_dgrad(bf16_bits(x), offs, wb, bf16_bits(gh),
+                                                  row_scale=rw.numpy())
+    parity(xd.grad, gx_ref, "swiglu autograd dgrad")
+    parity(rwd.grad, drw_ref, "swiglu routing-weight grad")
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_grouped_swiglu_bwd_entry_point(with_bias):
+    # nf4_grouped_swiglu_bwd through the C ABI: ragged experts (one empty), bias,
+    # rows past the last expert untouched in grad_x and zero in the routing-weight
+    # gradient, bit-identical reruns.
+    E, N_e, K = 3, 384, 256
+    counts = [33, 0, 150]
+    w, st, offs, x, g = _grouped_ep_case(E, N_e, K, counts, seed=45 + with_bias, interleave=True)
+    T = int(offs[-1])
+    Tpad = T + 5
+    xp = torch.cat([x, synth.activation(5, K, g)])
+    rw = torch.rand(Tpad, generator=g).float()
+    gh = synth.activation(Tpad, N_e // 2, g)
+    bias = (torch.randn(E * N_e, generator=g) * 0.1).float() if with_bias else None
+    offs_d = torch.from_numpy(offs).to(DEV)
+    outs = []
+    for _ in range(2):
+        gx, drw = ops.grouped_swiglu_bwd(xp.to(DEV), offs_d, w, E, gh.to(DEV),
+                                         bias=None if bias is None else bias.to(DEV),
+                                         row_scale=rw.to(DEV), need_row_scale_grad=True)
+        outs.append((gx, drw))
+    assert torch.equal(outs[0][0].view(torch.int16)[:T], outs[1][0].view(torch.int16)[:T])
+    assert torch.equal(outs[0][1], outs[1][1])
+    wb = oracle.dequantize(st, "bf16").reshape(E, N_e, K)
+    gx_ref, drw_ref = oracle.grouped_swiglu_dgrad(bf16_bits(x), offs, wb, bf16_bits(gh[:T]),
+                                                  bias=None if bias is None else bias.numpy(),
+                                                  row_scale=rw[:T].numpy())
+    gx, drw = outs[0]
+    parity(gx[:T], gx_ref, f"swiglu bwd gx bias={with_bias}")
+    parity(drw[:T], drw_ref, f"swiglu bwd drw bias={with_bias}")
+    assert torch.count_nonzero(drw[T:]) == 0
+    # without the routing-weight gradient, grad_x is the same
+    gx2, none = ops.grouped_swiglu_bwd(xp.to(DEV), offs_d, w, E, gh.to(DEV),
+                                       bias=None if bias is None else bias.to(DEV),
+                                       row_scale=rw.to(DEV))
+    assert none is None and torch.equal(gx2.view(torch.int16)[:T], gx.view(torch.int16)[:T])

@@ -573,3 +573,101 @@ def test_swiglu_bias_and_row_scale_literals():
     # row 1: g = 2, u = 3, scaled by 0.5; silu(2) = 1.7615941559557649
     np.testing.assert_allclose(h[1, :4], [1.7615941559557649 * 3 * 0.5] * 4, rtol=1e-12)
     assert np.all(h[:, 4:] == 0.0)
+
+
+# -------------------------------------------------- expert SwiGLU backward --
+# h = silu(g) u r: gradients with respect to the gate and up pre-activations and
+# the routing weight r, pinned by literal derivative values, by central
+# differences of the (separately pinned) forward, and through the whole
+# input-gradient composition with one-hot weights.
+
+# silu(g) and silu'(g) = d/dg [g / (1 + exp(-g))] to 17 digits (computed
+# symbolically, independent of the oracle's formula).
+SILU = {0.0: 0.0, 1.0: 0.73105857863000488, -2.0: -0.23840584404423511, 4.0: 3.9280551601516338,
+        0.5: 0.31122966560092728}
+DSILU = {0.0: 0.5, 1.0: 0.92767051187148673, -2.0: -0.090784248784895479, 4.0: 1.0526646148910729,
+         0.5: 0.73996118730265181}
+
+
+def test_swiglu_backward_literals():
+    gs = [0.0, 1.0, -2.0, 4.0, 0.5]
+    a = np.zeros((2, 128))
+    a[0, :5] = gs                 # gate columns
+    a[0, 64:69] = [3.0, 2.0, -1.0, 0.25, 5.0]   # up columns of the same outputs
+    a[1, :5] = gs
+    a[1, 64:69] = 1.0
+    dh = np.zeros((2, 64))
+    dh[0, :5] = [1.0, 1.0, 2.0, -1.0, 0.5]
+    dh[1, :5] = 1.0
+    r = np.array([0.5, 2.0], np.float32)
+    dgu, dr = oracle.swiglu_backward(a, dh, r)
+    up0 = [3.0, 2.0, -1.0, 0.25, 5.0]
+    for j, g in enumerate(gs):
+        assert dgu[0, j] == pytest.approx(0.5 * dh[0, j] * up0[j] * DSILU[g], rel=1e-14, abs=1e-300)
+        assert dgu[0, 64 + j] == pytest.approx(0.5 * dh[0, j] * SILU[g], rel=1e-14, abs=1e-300)
+        assert dgu[1, j] == pytest.approx(2.0 * DSILU[g], rel=1e-14)
+        assert dgu[1, 64 + j] == pytest.approx(2.0 * SILU[g], rel=1e-14, abs=1e-300)
+    assert np.all(dgu[:, 5:64] == 0.0) and np.all(dgu[:, 69:] == 0.0)
+    assert dr[0] == pytest.approx(sum(SILU[g] * u * d for g, u, d in zip(gs, up0, dh[0, :5])), rel=1e-14)
+    assert dr[1] == pytest.approx(sum(SILU[g] for g in gs), rel=1e-14)
+    # no routing weight: the same as r = 1, and no routing-weight gradient
+    dgu1, dr1 = oracle.swiglu_backward(a, dh)
+    assert dr1 is None
+    np.testing.assert_array_equal(dgu1, oracle.swiglu_backward(a, dh, np.ones(2, np.float32))[0])
+
+
+def test_swiglu_backward_matches_central_differences_of_the_forward():
+    rng = np.random.default_rng(3)
+    T, N = 3, 256
+    a = rng.standard_normal((T, N)) * 2.0
+    dh = rng.standard_normal((T, N // 2))
+    r = rng.random(T).astype(np.float32)
+    dgu, dr = oracle.swiglu_backward(a, dh, r)
+    loss = lambda aa, rr: float(np.sum(oracle.swiglu_forward(aa, rr) * dh))
+    eps = 1e-6
+    for t in range(T):
+        for c in list(range(0, N, 7)) + [63, 64, 127, 128, 255]:
+            ap, am = a.copy(), a.copy()
+            ap[t, c] += eps
+            am[t, c] -= eps
+            num = (loss(ap, r) - loss(am, r)) / (2 * eps)
+            assert dgu[t, c] == pytest.approx(num, rel=1e-6, abs=1e-7), (t, c)
+    # routing weight: the loss is linear in r (fp32 scales, so perturb in fp64 by hand)
+    h1 = oracle.swiglu_forward(a)
+    np.testing.assert_allclose(dr, np.sum(h1 * dh, axis=1), rtol=1e-12)
+
+
+def test_grouped_swiglu_dgrad_one_hot_literals():
+    # E = 1, N = 128 (64 gate + 64 up rows), K = 128, W = I: a[t, c] = x[t, c], and
+    # grad_x[t, k] = bf16(dgu[t, k]).  Row 0: g = 1, u = 2, dh = 1, r = 0.5, so
+    # dg = 0.5 * 2 * silu'(1) = 0.92767... -> bf16 0.92578125 and
+    # du = 0.5 * silu(1) = 0.36552... -> bf16 0.365234375.
+    N = K = 128
+    w = np.eye(N, K, dtype=np.float32)[None]
+    wb = _bf16(w)
+    x = np.zeros((2, K), np.float32)
+    x[0, 0], x[0, 64] = 1.0, 2.0
+    x[1, 3], x[1, 67] = -2.0, 4.0
+    dh = np.zeros((2, 64), np.float32)
+    dh[0, 0] = 1.0
+    dh[1, 3] = -0.5
+    r = np.array([0.5, 1.0], np.float32)
+    gx, dr = oracle.grouped_swiglu_dgrad(_bf16(x), np.array([0, 2]), wb, _bf16(dh), row_scale=r)
+    assert gx.shape == (2, K) and dr.shape == (2,)
+    assert gx[0, 0] == 0.92578125 and gx[0, 64] == 0.365234375
+    # row 1: g = -2, u = 4, dh = -0.5: dg = -0.5 * 4 * silu'(-2) = 0.18156... -> 0.181640625,
+    # du = -0.5 * silu(-2) = 0.11920... -> 0.119140625
+    assert gx[1, 3] == 0.181640625 and gx[1, 67] == 0.119140625
+    others = np.ones_like(gx, bool)
+    others[0, [0, 64]] = others[1, [3, 67]] = False
+    assert np.all(gx[others] == 0.0)
+    assert dr[0] == pytest.approx(SILU[1.0] * 2.0, rel=1e-14)
+    assert dr[1] == pytest.approx(SILU[-2.0] * 4.0 * -0.5, rel=1e-14)
+    # a bias is added to the pre-activations before the derivative
+    bias = np.zeros(N, np.float32)
+    bias[0] = 1.0   # g of row 0 becomes 2
+    gxb, _ = oracle.grouped_swiglu_dgrad(_bf16(x), np.array([0, 2]), wb, _bf16(dh), bias=bias,
+                                         row_scale=r)
+    s2 = 1.0 / (1.0 + math.exp(-2.0))
+    assert gxb[0, 0] == oracle.bf16_bits_to_f32(oracle.f32_to_bf16_bits(
+        np.float32(0.5 * 2.0 * s2 * (1 + 2.0 * (1 - s2)))))
