@@ -431,12 +431,13 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_val = job_throughput(flops, world, e2e_ms)
 
-    sweep = grouped = storage8 = f16 = None
+    sweep = grouped = storage8 = f16 = stack = None
     if rank == 0 and world == 1 and not args.no_sweep:
         sweep = run_sweep(dev, pk)
         grouped = run_grouped(dev, pk)
         storage8 = run_storage8(dev, pk)
         f16 = run_storage8(dev, pk, (("nf4_f16", "nf4", "f16"),))
+        stack = run_stack(dev, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -491,16 +492,24 @@ def run_ours(args, rank, world, local_rank):
         out["storage_8bit_4096"] = storage8
     if f16 is not None:
         out["f16_compute_4096"] = f16
+    if stack is not None:
+        out["config5_stack"] = stack
     if cpu is not None:
         out["cpu_baseline"] = cpu
     if sweep is not None:
-        # Compact K = N = 4096 curve last on the line, where a truncated log keeps it:
-        # [M, us fwd, us dgrad, TFLOP/s, fraction of the burst tensor peak, fraction of
-        # HBM on weight bytes].
-        out["m_sweep_4096_summary"] = {
-            "cols": ["M", "us_fwd", "us_dgrad", "tflops", "frac_tc", "frac_hbm"],
-            "rows": [[r["M"], r["us_fwd"], r["us_dgrad"], r["tflops"], r["frac_tc"], r["frac_hbm"]]
-                     for r in sweep]}
+        # Compact summaries last on the line, where a truncated log keeps them: the
+        # K = N = 4096 curve as [M, us fwd, us dgrad, TFLOP/s, fraction of the burst
+        # tensor peak, fraction of HBM on weight bytes], then the expert and stack rows.
+        summ = {"cols": ["M", "us_fwd", "us_dgrad", "tflops", "frac_tc", "frac_hbm"],
+                "rows": [[r["M"], r["us_fwd"], r["us_dgrad"], r["tflops"], r["frac_tc"], r["frac_hbm"]]
+                         for r in sweep]}
+        if grouped is not None:
+            summ["grouped_olmoe_tflops"] = grouped["tflops"]
+            summ["grouped_olmoe_weight_gbs"] = grouped["weight_gbs"]
+        if stack is not None:
+            summ["config5_stack_ms"] = stack["ms_per_step"]
+            summ["config5_stack_tflops"] = stack["tflops_products"]
+        out["m_sweep_4096_summary"] = summ
     return out
 
 
@@ -809,6 +818,91 @@ def run_grouped(dev, pk):
                                  "us_unfused_torch_glue": round(t_u * 1e6, 2),
                                  "tflops_fused": round(2.0 * T * 2 * I * H / t_f / 1e12, 2)}
     return out
+
+
+def run_stack(dev, pk, layers_n: int = 8, M: int = 4096, reps: int = 3):
+    """The 32B-class layer stack (hidden 5120, intermediate 27648, k/v 1024, M = 4096,
+    eight layers of NF4 double-quant weights) under non-reentrant checkpointing with
+    each layer's quantised tensors copied into one of two recycled slot sets inside
+    its checkpointed region; one step = forward, recompute and input gradients of the
+    whole stack (h = x / rms(x) s; a = h + o(q(h)); kv = mean(k(h) v(h));
+    z = silu(gate(a)) up(a); out = a + down(z)).  TFLOP/s counts the products only: three passes of 2 M N K
+    per projection (forward, recompute, input gradient)."""
+    import itertools
+    import torch
+    import torch.nn.functional as F
+    from torch.utils.checkpoint import checkpoint
+    import bit_nf4_quantized_linear_gb300 as nf4
+    from bit_nf4_quantized_linear_gb300 import ops, synth
+    g = torch.Generator(device=dev)
+    g.manual_seed(60)
+    layers = []
+    for _ in range(layers_n):
+        layer = {}
+        for name, K, N in synth.QWEN32B_PROJ:
+            layer[name] = nf4.quantize(torch.randn(N, K, generator=g, device=dev) * synth.WEIGHT_STD,
+                                       double_quant=True)
+        layers.append(layer)
+    torch.cuda.empty_cache()
+    slot_sets = [{n: [None if t is None else torch.empty_like(t) for t in w.tensors()]
+                  for n, w in layers[0].items()} for _ in range(2)]
+    turn = itertools.cycle(range(2))
+
+    def load(layer):
+        dst = slot_sets[next(turn)]
+        out = {}
+        for n, w in layer.items():
+            for b, t in zip(dst[n], w.tensors()):
+                if b is not None:
+                    b.copy_(t)
+            out[n] = ops.NF4Weight.from_tensors(tuple(dst[n]), w.N, w.K, w.double_quant)
+        return out
+
+    H = synth.QWEN32B_PROJ[0][1]
+    x0 = torch.randn(M, H, generator=g, device=dev).to(torch.bfloat16)
+    scales = [(1 + 0.01 * torch.randn(H, generator=g, device=dev)).to(torch.bfloat16)
+              .requires_grad_(True) for _ in range(layers_n)]
+
+    def block(i):
+        def run(x, s):
+            w = load(layers[i])
+            p = lambda t, n: nf4.nf4_linear(t, w[n])
+            xf = x.float()
+            h = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + 1e-6) * s.float()).to(torch.bfloat16)
+            a = h + p(p(h, "q"), "o")
+            kv = (p(h, "k").float() * p(h, "v").float()).mean()
+            z = F.silu(p(a, "gate")) * p(a, "up")
+            return a + p(z, "down"), kv
+        return run
+
+    def step():
+        x = x0.clone().requires_grad_(True)
+        h, kvs = x, 0.0
+        for i in range(layers_n):
+            h, kv = checkpoint(block(i), h, scales[i], use_reentrant=False)
+            kvs = kvs + kv
+        (h.float().pow(2).mean() + kvs).backward()
+
+    step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    t = statistics.median(times)
+    flops = 3.0 * layers_n * sum(2.0 * M * N * K for _, K, N in synth.QWEN32B_PROJ)
+    per_layer = sum(w.nbytes() for w in layers[0].values())
+    del layers, slot_sets
+    torch.cuda.empty_cache()
+    return {"workload": "qwen2.5-32b-shaped stack: 8 layers x (q,o 5120^2; k,v 1024x5120; gate,up "
+                        "27648x5120; down 5120x27648), M=4096, checkpointed, 2 recycled slot sets",
+            "nf4_bytes_per_layer": per_layer, "ms_per_step": round(t * 1e3, 3),
+            "tflops_products": round(flops / t / 1e12, 1),
+            "frac_tc": round(flops / t / 1e12 / pk["bf16_tflops"], 4)}
 
 
 # ------------------------------------------------------------- CPU oracle --

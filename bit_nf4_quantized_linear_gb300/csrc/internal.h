@@ -67,25 +67,28 @@ struct GemmArgs {
   int64_t ep_ld_dh;
   float* ep_drw;
   // Stream-K schedule (dense, splits == 1): the items * ksteps
-  // contraction steps are cut into sk_ctas equal contiguous runs, one per CTA.  A
-  // tile cut between CTAs is finished by the CTA holding its first steps, which
-  // adds the later runs' fp32 partials in CTA order.
+  // contraction steps are cut into sk_ctas equal contiguous runs, one per CTA, and
+  // each CTA walks the tiles of its run in reverse.  A tile cut between CTAs is
+  // finished by the highest-index CTA holding part of it (the one with its last
+  // steps), which adds the lower CTAs' fp32 partials in a fixed order; a CTA thus
+  // only ever waits for CTAs of lower index, which are dispatched before it.
   int sk;
   int64_t sk_units;     // items * ksteps
   int sk_ctas;          // CTAs (= grid)
   float* sk_ws;         // partial tiles [sk_ctas][4 row quarters][bt tokens][32 rows] fp32
-  uint32_t* sk_flags;   // [sk_ctas][4]: partial of (CTA, row quarter) published
-  uint32_t sk_epoch;    // value this launch publishes (never 0)
-  uint32_t sk_wait_xor; // the finishing CTA waits for sk_epoch ^ sk_wait_xor (0; the
+  uint64_t* sk_flags;   // [sk_ctas][4] in the caller's workspace: partial of (CTA,
+                        // row quarter) published; cleared by the finishing CTA
+  uint64_t sk_epoch;    // value this launch publishes (never 0)
+  uint64_t sk_wait_xor; // the finishing CTA waits for sk_epoch ^ sk_wait_xor (0; the
                         // failure-path test sets a bit no contributor publishes)
 };
 
-// Stream-K bookkeeping: ready flags live in a device array of kSkSlots launch
-// slots of kSkMaxCtas * 4 words (slot = epoch % kSkSlots), so that flags need no
-// clearing and launches in flight on other streams use other slots.
-constexpr int kSkSlots = 64;
-constexpr int kSkMaxCtas = 256;
-uint32_t* stream_k_flags(uint32_t epoch);  // device address of the epoch's slot
+// Stream-K workspace: partial tiles, then the ready flags (8 bytes per CTA and row
+// quarter).
+constexpr int kSkMaxCtas = 1024;
+inline size_t stream_k_ws_bytes(int ctas, int bt) {
+  return static_cast<size_t>(ctas) * kTileW * bt * sizeof(float) + static_cast<size_t>(ctas) * 4 * 8;
+}
 
 // Parameters of the small-M GEMV kernels.
 struct GemvArgs {

@@ -198,13 +198,16 @@ std::atomic<int> g_inject_sk_timeout{0};
 // Stream-K schedule of the fused kernel (nf4_set_stream_k).
 std::atomic<int> g_stream_k{NF4_STREAM_K_AUTO};
 
-// Epoch a stream-K launch publishes in its ready flags: unique per launch, never 0.
-std::atomic<uint32_t> g_sk_epoch{0};
+// Epoch a stream-K launch publishes in its ready flags: unique per launch of the
+// process, never 0.  The flags live in the caller's workspace and the CTA that
+// finishes a tile clears them, so a launch replayed from a CUDA graph (same epoch)
+// finds them cleared by its previous replay.
+std::atomic<uint64_t> g_sk_epoch{0};
 
-uint32_t next_sk_epoch() {
-  uint32_t e = g_sk_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+uint64_t next_sk_epoch() {
+  uint64_t e = g_sk_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
   while (e == 0) e = g_sk_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  return e;
+  return e ^ 0x5a17c0de00000000ull;  // unlikely to match what a fresh buffer holds
 }
 
 // Cycles of one 64-deep contraction step of a tile (per SM), as measured on
@@ -304,7 +307,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
         sk_best = make_plan(M, ncols, contract, bt, 1);
         sk_best.stream_k = true;
         sk_best.sk_ctas = static_cast<int>(G);
-        sk_best.ws_bytes = static_cast<size_t>(G) * nf4::kTileW * bt * sizeof(float);
+        sk_best.ws_bytes = nf4::stream_k_ws_bytes(static_cast<int>(G), bt);
       }
     }
   }
@@ -439,10 +442,11 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     a.sk_units = p.items * p.ksteps;
     a.sk_ctas = p.sk_ctas;
     a.sk_ws = static_cast<float*>(ws);
+    a.sk_flags = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) +
+                                             static_cast<size_t>(p.sk_ctas) * nf4::kTileW * p.bt * sizeof(float));
+    if ((reinterpret_cast<uintptr_t>(a.sk_flags) & 7u) != 0) return NF4_ERR_ALIGNMENT;
     a.sk_epoch = next_sk_epoch();
-    if (g_inject_sk_timeout.exchange(0, std::memory_order_relaxed)) a.sk_wait_xor = 0x80000000u;
-    a.sk_flags = nf4::stream_k_flags(a.sk_epoch);
-    if (!a.sk_flags) return cuda_fail(cudaGetLastError(), "stream-K flags");
+    if (g_inject_sk_timeout.exchange(0, std::memory_order_relaxed)) a.sk_wait_xor = 1ull << 62;
     grid = p.sk_ctas;
   }
   // The bf16 output goes out through bulk tensor stores when its base and row pitch

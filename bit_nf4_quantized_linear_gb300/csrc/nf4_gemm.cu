@@ -220,17 +220,17 @@ __device__ __noinline__ void drain_phase(uint32_t bar, uint32_t parity, const Ge
 
 // Stream-K partial-tile flags: publish with release semantics after the partial's
 // stores; wait (bounded) with acquire semantics before reading it.
-__device__ __forceinline__ void flag_publish(uint32_t* f, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+__device__ __forceinline__ void flag_publish(uint64_t* f, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t flag_read(const uint32_t* f) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+__device__ __forceinline__ uint64_t flag_read(const uint64_t* f) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
   return v;
 }
 
-__device__ __noinline__ bool flag_wait(const uint32_t* f, uint32_t v, const Shared& sh,
+__device__ __noinline__ bool flag_wait(const uint64_t* f, uint64_t v, const Shared& sh,
                                        const GemmArgs& a) {
   if (flag_read(f) == v) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -286,10 +286,14 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
 
 // The CTA's sequence of item segments.  Classic: whole items unit, unit + nunits,
 // ... (their contraction split fixed by the plan).  Stream-K: the contiguous run
-// of contraction steps [unit * U / G, (unit + 1) * U / G) over items in order,
-// cut at item boundaries.  Every role of the CTA walks the same sequence.
+// of contraction steps [unit * U / G, (unit + 1) * U / G) over items in order, cut
+// at item boundaries and walked from its last item back to its first (the steps
+// of each segment still in increasing order): the segment a CTA contributes to a
+// tile finished elsewhere (its run's last item) comes first, the segment it
+// finishes itself (its run's first item, when cut) comes last.  Every role of the
+// CTA walks the same sequence.
 struct Cursor {
-  int64_t pos, end;
+  int64_t pos, end;  // stream-K: the run's first step and the end of what is left
 };
 
 __device__ __forceinline__ int64_t sk_first_unit(const GemmArgs& a, int64_t cta) {
@@ -311,14 +315,13 @@ __device__ __forceinline__ bool cursor_next(Cursor& c, const GemmArgs& a, const 
     c.pos += nunits;
     return true;
   }
-  const int64_t idx = c.pos / a.ksteps;
-  const int ks0 = static_cast<int>(c.pos - idx * a.ksteps);
-  const int64_t left = c.end - c.pos;
-  const int ks1 = left < a.ksteps - ks0 ? ks0 + static_cast<int>(left) : a.ksteps;
+  const int64_t idx = (c.end - 1) / a.ksteps;  // last item with steps left
+  const int64_t tile0 = idx * a.ksteps;
+  const int64_t seg0 = c.pos > tile0 ? c.pos : tile0;
   it = get_item<MODE, BT>(idx, a, sh);
-  it.ks0 = ks0;
-  it.ks1 = ks1;
-  c.pos += ks1 - ks0;
+  it.ks0 = static_cast<int>(seg0 - tile0);
+  it.ks1 = static_cast<int>(c.end - tile0);
+  c.end = seg0;
   return true;
 }
 
@@ -565,17 +568,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t col = it.col0 + row;
       const bool col_ok = col < a.ncols;
       const int ntok = static_cast<int>(it.tok_end - it.tok0);  // tokens in this tile (<= BT)
-      // Stream-K: a segment after the tile's first steps publishes its fp32 partial
-      // (this warp's quarter of the rows, lane-contiguous per token) in this CTA's
-      // slot; the segment holding the first steps of a tile cut between CTAs adds
-      // the partials of the following CTAs, in CTA order, before rounding.
-      const bool sk_part = a.sk && it.ks0 > 0;
-      const bool sk_own = a.sk && it.ks0 == 0 && it.ks1 < a.ksteps;
-      int64_t own_last = unit;  // last CTA holding steps of an owned split tile
+      // Stream-K: a segment that stops before the tile's last step publishes its
+      // fp32 partial (this warp's quarter of the rows, lane-contiguous per token) in
+      // this CTA's slot; the segment holding the last steps of a tile cut between
+      // CTAs (always the highest-index CTA on it) adds the partials of the lower
+      // CTAs, from the nearest down, before rounding.  Waits only go to lower CTAs,
+      // which are dispatched first, so the grid needs no co-residency.
+      const bool sk_part = a.sk && it.ks1 < a.ksteps;
+      const bool sk_own = a.sk && it.ks1 == a.ksteps && it.ks0 > 0;
+      int64_t own_first = unit;  // lowest CTA holding steps of an owned split tile
       if (sk_own) {
-        const int64_t tile_end = (it.idx + 1) * a.ksteps;
-        while (own_last + 1 < a.sk_ctas && sk_first_unit(a, own_last + 1) < tile_end) ++own_last;
-        for (int64_t c = unit + 1; c <= own_last; ++c)
+        const int64_t tile0 = it.idx * a.ksteps;
+        while (own_first > 0 && sk_first_unit(a, own_first) > tile0) --own_first;
+        for (int64_t c = unit - 1; c >= own_first; --c)
           if (!flag_wait(a.sk_flags + c * 4 + q, a.sk_epoch ^ a.sk_wait_xor, sh, a)) break;
       }
       auto sk_slot = [&](int64_t c) {  // partial of CTA c, this quarter, token 0, this lane
@@ -583,13 +588,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // The owned segment is the CTA's last item, so when its accumulator is full
       // the activation ring is idle (every tile loaded into it has been consumed by
-      // the MMAs).  The next CTA's partial of this warp's quarter (ntok x 128 bytes)
-      // then comes into the warp's part of that ring with one bulk copy, and the
-      // chunks below read it from shared memory instead of waiting on L2 per chunk;
-      // further CTAs' partials (tiles cut three or more ways) are read from global
-      // memory.  The sum order is the same either way.
-      const float* p_first = nullptr;  // partial of CTA unit + 1 in shared memory
-      if (sk_own && own_last > unit &&
+      // the MMAs).  The previous CTA's partial of this warp's quarter (ntok x 128
+      // bytes) then comes into the warp's part of that ring with one bulk copy, and
+      // the chunks below read it from shared memory instead of waiting on L2 per
+      // chunk; further CTAs' partials (tiles cut three or more ways) are read from
+      // global memory.  The sum order is the same either way.
+      const float* p_first = nullptr;  // partial of CTA unit - 1 in shared memory
+      if (sk_own && own_first < unit &&
           (reinterpret_cast<uintptr_t>(a.sk_ws) & 15u) == 0) {
         static_assert(G::kStagesX * G::kXStage >= kNumEpiWarps * BT * 128,
                       "stream-K partials of the four row quarters fit in the activation ring");
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           fence_proxy_async_global();  // the flag acquired above, then the async-proxy read
           mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ntok) * 128u);
-          bulk_load_g2s(smem_addr(land), sk_slot(unit + 1) - lane, static_cast<uint32_t>(ntok) * 128u, bar);
+          bulk_load_g2s(smem_addr(land), sk_slot(unit - 1) - lane, static_cast<uint32_t>(ntok) * 128u, bar);
         }
         __syncwarp();
         // Completes once (the owned tile is the last item).  Waited for even after
@@ -607,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p_first = land + lane;
       }
       auto part_src = [&](int64_t c, int c0) -> const float* {
-        return (c == unit + 1 && p_first) ? p_first + c0 * 32 : sk_slot(c) + c0 * 32;
+        return (c == unit - 1 && p_first) ? p_first + c0 * 32 : sk_slot(c) + c0 * 32;
       };
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
       // One 16-token batch: tensor-memory load, plus the following CTAs' partials.
@@ -616,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x16(taddr + c0, v);
         tmem_wait_ld();
         if (sk_own)
-          for (int64_t c = unit + 1; c <= own_last; ++c) {
+          for (int64_t c = unit - 1; c >= own_first; --c) {
             const float* src = part_src(c, c0);
 #pragma unroll
             for (int j = 0; j < kBatch; ++j)
@@ -655,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (BT > 16) tmem_ld_32x32b_x16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
           tmem_wait_ld();
           if (sk_own)
-            for (int64_t c = unit + 1; c <= own_last; ++c) {
+            for (int64_t c = unit - 1; c >= own_first; --c) {
               const float* src = part_src(c, c0);
               float p[32];
 #pragma unroll
@@ -786,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sk_own) {  // the partials are consumed: clear their flags for the next launch
         __syncwarp();
         if (lane == 0)
-          for (int64_t c = unit + 1; c <= own_last; ++c) a.sk_flags[c * 4 + q] = 0u;
+          for (int64_t c = unit - 1; c >= own_first; --c) a.sk_flags[c * 4 + q] = 0ull;
       }
       tc_fence_before();
       __syncwarp();
@@ -1140,24 +1145,6 @@ cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensor
   return launch_mode<1>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
 #else
-
-// Stream-K ready flags (zero at module load; a launch publishes its epoch).
-__device__ uint32_t g_stream_k_flags[kSkSlots * kSkMaxCtas * 4];
-
-uint32_t* stream_k_flags(uint32_t epoch) {
-  constexpr int kDevices = 64;
-  static std::atomic<uint32_t*> cache[kDevices];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return nullptr;
-  uint32_t* base = cache[dev].load(std::memory_order_acquire);
-  if (!base) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_stream_k_flags) != cudaSuccess) return nullptr;
-    base = static_cast<uint32_t*>(p);
-    cache[dev].store(base, std::memory_order_release);
-  }
-  return base + static_cast<size_t>(epoch % kSkSlots) * kSkMaxCtas * 4;
-}
 
 cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,

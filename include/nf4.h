@@ -347,15 +347,18 @@ void nf4_set_small_m_path(int32_t path);
  * split at small M), leaving the last wave partly idle when the tile count is not
  * a multiple of the SM count.  Stream-K: the tiles' 64-deep contraction steps are
  * cut into one equal contiguous run per CTA; a tile cut between CTAs is finished
- * by the CTA holding its first steps, which adds the following CTAs' fp32
- * partial tiles in CTA order (deterministic for a given shape and SM count; the
- * partials live in the workspace, which then holds SMs x 128 x tile-tokens fp32).
+ * by the highest-index CTA holding part of it, which adds the lower CTAs' fp32
+ * partial tiles in a fixed order (deterministic for a given shape and SM count).
+ * The workspace then holds the partials (CTAs x 128 x tile-tokens fp32) and one
+ * 8-byte ready flag per CTA and row quarter; concurrent calls need workspaces of
+ * their own, as for the split partials.
  *   NF4_STREAM_K_OFF   classic only.
  *   NF4_STREAM_K_AUTO  (default) stream-K where the planner's cost model prefers it.
  *   NF4_STREAM_K_FORCE stream-K for every product on the fused kernel (tests).
- * The CTA finishing a split tile waits (bounded, NF4_ERR_TIMEOUT on expiry) for
- * the others' partials, so the grid (at most one CTA per SM) must be resident at
- * once, as it is on a device this process does not share. */
+ * A CTA waits (bounded, NF4_ERR_TIMEOUT on expiry) only for partials of CTAs of
+ * lower index, which the device dispatches before it, so the grid need not be
+ * resident at once: other kernels may share the device (for instance a second
+ * stream-K product on another stream). */
 enum { NF4_STREAM_K_OFF = 0, NF4_STREAM_K_AUTO = 1, NF4_STREAM_K_FORCE = 2 };
 void nf4_set_stream_k(int32_t mode);
 

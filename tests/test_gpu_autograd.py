@@ -1,19 +1,15 @@
 """The autograd Functions on the GPU: gradients through the fused kernels match
-the oracle, only save_for_backward carries the weight (no dense weight saved), an
-in-place change of the saved packed weight is caught by autograd's version
-counter, and under non-reentrant activation checkpointing with recycled weight
-buffers the gradients equal the private-buffer run bit for bit while a control
-that keeps the weight as a ctx attribute gets them wrong (bitsandbytes issue
-"MatMul4Bit keeps B and quant_state on ctx", "Minimal reproducer" and "What it
-prints"; Soup issue #842, "Acceptance criteria": aliasing control)."""
-import numpy as np
+the oracle, only save_for_backward carries the weight (no dense weight saved), and
+an in-place change of the saved packed weight is caught by autograd's version
+counter (bitsandbytes issue "MatMul4Bit keeps B and quant_state on ctx", "Why
+save_for_backward fixes it").  The checkpointed stack with recycled weight slots
+and its ctx-attribute control run at full size in test_gpu_stack.py."""
 import pytest
 import torch
-from torch.utils.checkpoint import checkpoint
 
 import oracle
 import bit_nf4_quantized_linear_gb300 as nf4
-from bit_nf4_quantized_linear_gb300 import ops, synth
+from bit_nf4_quantized_linear_gb300 import synth
 from tests.helpers import bf16_bits, oracle_state, parity
 
 pytestmark = pytest.mark.gpu
@@ -86,73 +82,6 @@ def test_inplace_change_of_saved_weight_is_caught():
     w.packed.add_(1)
     with pytest.raises(RuntimeError, match="modified by an inplace operation"):
         y.float().sum().backward()
-
-
-class _CtxAttrFn(torch.autograd.Function):
-    """Negative control: the packed weight is kept as a ctx attribute (the
-    MatMul4Bit pattern), invisible to checkpointing."""
-
-    @staticmethod
-    def forward(ctx, x, w_tensors, N, K, dq):
-        w = ops.NF4Weight.from_tensors(w_tensors, N, K, dq)
-        ctx.w = w
-        return ops.linear_fwd(x.contiguous(), w)
-
-    @staticmethod
-    def backward(ctx, gy):
-        return ops.linear_dgrad(gy.contiguous(), ctx.w), None, None, None, None
-
-
-class SlotPool:
-    def __init__(self, n, like):
-        self.slots = [torch.empty_like(like) for _ in range(n)]
-        self.cursor = 0
-
-    def acquire(self, src):
-        s = self.slots[self.cursor % len(self.slots)]
-        self.cursor += 1
-        s.copy_(src)
-        return s
-
-
-def _aliasing_run(layers, x0, scales, arm):
-    recycle = arm in ("recycled", "control")
-    pool = SlotPool(2, layers[0].packed) if recycle else None
-    params = [s.clone().requires_grad_(True) for s in scales]
-
-    def body(i):
-        def fn(h, scale):
-            h = h * scale
-            packed = pool.acquire(layers[i].packed) if recycle else layers[i].packed
-            wt = list(layers[i].tensors())
-            wt[0] = packed
-            if arm == "control":
-                return _CtxAttrFn.apply(h, tuple(wt), layers[i].N, layers[i].K, layers[i].double_quant)
-            return nf4.NF4LinearFn.apply(h, *wt, layers[i].N, layers[i].K, layers[i].double_quant)
-        return fn
-
-    h = x0.clone().requires_grad_(True)
-    for i in range(len(layers)):
-        h = checkpoint(body(i), h, params[i], use_reentrant=False)
-    h.float().pow(2).mean().backward()
-    return [p.grad.float().clone() for p in params]
-
-
-def test_checkpoint_recycled_buffers_exact_and_control_wrong():
-    # 8 layers of 4096 x 4096 NF4 (double quant), M = 256, two recycled slots.
-    g = synth.generator(12)
-    D, L, M = 4096, 8, 256
-    layers = [nf4.quantize((torch.randn(D, D, generator=g) / 32).to(DEV), double_quant=True)
-              for _ in range(L)]
-    x0 = synth.activation(M, D, g).to(DEV)
-    scales = [(1 + 0.01 * torch.randn(D, generator=g)).to(DEV, torch.bfloat16) for _ in range(L)]
-    ref = _aliasing_run(layers, x0, scales, "private")
-    got = _aliasing_run(layers, x0, scales, "recycled")
-    ctl = _aliasing_run(layers, x0, scales, "control")
-    for i in range(L):
-        assert torch.equal(got[i], ref[i]), f"layer {i}: recycled != private"
-    wrong = [i for i in range(L) if not torch.equal(ctl[i], ref[i])]
-    assert wrong[:L - 2] == list(range(L - 2)), f"control arm should be wrong on early layers: {wrong}"
 
 
 def test_grouped_function_grad():

@@ -481,6 +481,73 @@ def test_stream_k_wait_that_runs_out_reports_timeout(restore_stream_k):
            "stream-K launch after a timed-out one")
 
 
+def test_stream_k_concurrent_products_on_two_streams(restore_stream_k):
+    """Two stream-K products at once on two streams, each with its own workspace:
+    one launch's CTAs can find SMs held by the other's.  A CTA waits only for CTAs
+    of lower index of its own launch, so both finish without a timeout, match the
+    oracle and repeat bit for bit."""
+    ops.set_stream_k(_lib.STREAM_K_FORCE)
+    M, N, K = 2048, 4096, 4096
+    w1, st1, g1 = _quant_pair(N, K, True, seed=61)
+    w2, st2, g2 = _quant_pair(N, K, True, seed=62)
+    x1 = synth.activation(M, K, g1)
+    gy2 = synth.activation(M, N, g2)
+    x1d, gy2d = x1.to(DEV), gy2.to(DEV)
+    nf4.device_status(clear=True)
+    s1, s2 = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    ys, gxs = [], []
+    for _ in range(4):
+        with torch.cuda.stream(s1):
+            ys.append(nf4.linear_fwd(x1d, w1))
+        with torch.cuda.stream(s2):
+            gxs.append(nf4.linear_dgrad(gy2d, w2))
+    torch.cuda.synchronize()
+    assert nf4.device_status() == 0
+    rows = _sampled_rows(M, 5)
+    r = torch.from_numpy(rows).to(DEV)
+    parity(ys[0][r], oracle.linear_fwd(bf16_bits(x1), oracle.dequantize(st1, "bf16"), rows), "concurrent fwd")
+    parity(gxs[0][r], oracle.linear_dgrad(bf16_bits(gy2), oracle.dequantize(st2, "bf16"), rows),
+           "concurrent dgrad")
+    for i in range(1, 4):
+        assert torch.equal(ys[i].view(torch.int16), ys[0].view(torch.int16))
+        assert torch.equal(gxs[i].view(torch.int16), gxs[0].view(torch.int16))
+
+
+def test_stream_k_graph_replays_between_eager_launches(restore_stream_k):
+    """A stream-K product captured in a CUDA graph keeps its launch epoch on every
+    replay; its ready flags sit in the graph's own workspace and are cleared by the
+    CTAs that finish the tiles, so replays interleaved with eager launches of the
+    same shape (other workspaces, new epochs) all give the same bits."""
+    ops.set_stream_k(_lib.STREAM_K_FORCE)
+    M, N, K = 700, 1024, 2048
+    w, st, g = _quant_pair(N, K, True, seed=63)
+    x = synth.activation(M, K, g).to(DEV)
+    ref = nf4.linear_fwd(x, w)
+    y = torch.empty_like(ref)
+    ws = torch.empty(max(ops.workspace_size(_lib.OP_LINEAR_FWD, M, N, K), 16), dtype=torch.uint8,
+                     device=DEV)
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ops.linear_fwd(x, w, out=y, ws=ws)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        ops.linear_fwd(x, w, out=y, ws=ws)
+    nf4.device_status(clear=True)
+    for _ in range(4):
+        y.zero_()
+        graph.replay()
+        eager = nf4.linear_fwd(x, w)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(eager.view(torch.int16), ref.view(torch.int16))
+    assert nf4.device_status() == 0
+    parity(ref, oracle.linear_fwd(bf16_bits(x.cpu()), oracle.dequantize(st, "bf16")), "graph stream-K")
+
+
 def test_stream_k_off_and_on_agree_within_tolerance(restore_stream_k):
     M, N, K = 1536, 1024, 1024
     w, st, g = _quant_pair(N, K, True, seed=11)

@@ -84,8 +84,9 @@ def test_plan_invariants(bits, f16):
         assert p["splits"] <= max(1, -(-contract // 64))
         if p["stream_k"]:
             assert p["splits"] == 1
-            # one partial tile [4 row quarters][bt tokens][32 rows] fp32 per CTA
-            assert p["workspace_bytes"] == p["grid"] * 128 * bt * 4
+            # one partial tile [4 row quarters][bt tokens][32 rows] fp32 per CTA, then
+            # one 8-byte ready flag per CTA and row quarter
+            assert p["workspace_bytes"] == p["grid"] * 128 * bt * 4 + p["grid"] * 4 * 8
             assert p["grid"] == min(SMS, p["items"] * -(-contract // 64))
         elif p["splits"] > 1:
             assert p["workspace_bytes"] == p["splits"] * M * ncols * 4
