@@ -78,13 +78,23 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 
 // The byte-pair table: entry e = (code4[e >> 4], code4[e & 15]) as two fp32 (the
 // even value of a packed byte first), copy for lane l at byte offset 256 e + 8 l.
+// Written as 8 rounds of one 16-byte store per thread (16-byte unit
+// i = 512 k + thread, entry i / 16, so a warp's stores are contiguous); every
+// codebook value a thread needs is loaded up front, so the whole build costs one
+// global-memory round trip.
 __device__ __forceinline__ void build_table(uint8_t* smem, const float* code4) {
+  static_assert(kThreads == 512, "the table is 8 rounds of 512 16-byte units");
   uint4* t = reinterpret_cast<uint4*>(smem);
-  for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
-    const int e = i >> 4;
-    const uint32_t hi = __float_as_uint(__ldg(code4 + (e >> 4)));
-    const uint32_t lo = __float_as_uint(__ldg(code4 + (e & 15)));
-    t[i] = make_uint4(hi, lo, hi, lo);
+  const int tid = static_cast<int>(threadIdx.x);
+  const bool odd = ((tid >> 8) & 1) != 0;  // unit 512 k + tid holds entry 32 k + tid / 16,
+  const uint32_t lo = __float_as_uint(__ldg(code4 + ((tid >> 4) & 15)));  // whose low code is fixed
+  float c[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) c[i] = __ldg(code4 + i);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // high code of entry 32 k + tid / 16: 2 k + tid / 256
+    const uint32_t hi = __float_as_uint(odd ? c[2 * k + 1] : c[2 * k]);
+    t[k * kThreads + tid] = make_uint4(hi, lo, hi, lo);
   }
 }
 
