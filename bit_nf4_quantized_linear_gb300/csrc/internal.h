@@ -137,6 +137,7 @@ struct SkinnyArgs {
   int64_t T;      // output tiles
   int64_t cc;     // contraction per CTA (forward: multiple of 64; input gradient: of 16)
   int prefetch;   // the weight may be read before the preceding grid has finished
+  int* status;    // device status word (NF4_ERR_TIMEOUT from a bounded wait)
 };
 
 constexpr int kSkinnyMaxM = 16;
@@ -149,7 +150,11 @@ struct SkinnyPlan {
 
 // Plans and launches (S CTAs per cluster along the contraction).
 bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* p);
-cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s);
+// tmap: the packed codes [N rows, K/2 bytes] as a uint8 tensor with a box of
+// 128 bytes x 16 rows and 128B swizzle (forward) or 32 bytes x 64 rows and 32B
+// swizzle (input gradient).
+cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, const CUtensorMap& tmap,
+                          cudaStream_t s);
 
 // Largest M each product sends to the GEMV kernels.
 constexpr int kGemvMaxMFwd = 4;

@@ -362,7 +362,15 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     k.T = p.sk.T;
     k.cc = p.sk.cc;
     k.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
-    cudaError_t le = nf4::launch_skinny(mode, k, p.sk, s);
+    k.status = dev.status;
+    // The packed codes as [N rows, K/2 bytes]: the forward copies 16 rows x 128
+    // bytes per unit (128B swizzle), the input gradient 64 rows x 32 bytes (32B).
+    CUtensorMap tmap_pk;
+    if (!encode_2d(&tmap_pk, CU_TENSOR_MAP_DATA_TYPE_UINT8, w->packed, K / 2, N, K / 2,
+                   mode == 0 ? 128 : 32, mode == 0 ? 16 : 64,
+                   mode == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B))
+      return NF4_ERR_CUDA;
+    cudaError_t le = nf4::launch_skinny(mode, k, p.sk, tmap_pk, s);
     if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
     count(mode == 0 ? NF4_PATH_SKINNY_FWD : NF4_PATH_SKINNY_DGRAD);
     return NF4_OK;

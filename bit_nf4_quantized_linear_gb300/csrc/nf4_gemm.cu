@@ -99,7 +99,7 @@ struct Geo {
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;
   static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
   static_assert(kStagesX >= 3, "pipeline too shallow");
-  static_assert(kStagesA <= 4 && kStagesP <= 16 && kStagesX <= 8, "barrier slots");
+  static_assert(kStagesA <= 8 && kStagesP <= 16 && kStagesX <= 8, "barrier slots");
   // A decoded slot waits on the "stage done" ring for the step kStagesA back; that
   // ring slot must not be able to complete again first.
   static_assert(kStagesX >= kStagesA, "stage-done ring shallower than the decoded ring");
@@ -111,20 +111,20 @@ struct Geo {
 
 // Barrier slots in the misc region.  Three rings advance one stage per
 // contraction step: packed codes (pfull: TMA landed; pempty: decoders read it),
-// activations (xfull: TMA landed; xempty: MMAs done) and decoded operand tiles
-// (afull: decoders wrote it; aempty: MMAs done).
+// activations (xfull: TMA landed; xempty: MMAs done, the "stage done" signal
+// that also frees the decoded slot of the same step) and decoded operand tiles
+// (afull: decoders wrote it).
 constexpr int kBarPFull = 0;
 constexpr int kBarPEmpty = 16;
 constexpr int kBarXFull = 32;
 constexpr int kBarXEmpty = 40;
 constexpr int kBarAFull = 48;
-constexpr int kBarAEmpty = 52;
 constexpr int kBarAccFull = 56;
 constexpr int kBarAccEmpty = 58;
 constexpr int kBarDrain = 60;
 constexpr int kBarEpFull = 61;   // SwiGLU epilogue: up values of a batch written (2 warp pairs)
 constexpr int kBarEpEmpty = 63;  // ... and read by the gate warp
-constexpr int kBarSkPart = 65;   // stream-K: a following CTA's partial landed (one per epilogue warp)
+constexpr int kBarSkPart = 65;   // stream-K: a lower CTA's partial landed (one per epilogue warp)
 constexpr int kNumBars = 69;
 // Misc region: codebooks (16 + 256 fp32), barriers, four words (tensor-memory
 // slot, abort flag, item count, dependency flag), three expert tables.
@@ -332,15 +332,30 @@ struct RawScale {
   uint32_t q;  // 8-bit code (double quantisation)
 };
 
+// Read-only global loads kept where the program puts them (volatile asm is not
+// moved past the barrier waits around it), so that a fetch issued steps ahead of
+// its use stays ahead instead of being scheduled next to the use.
+__device__ __forceinline__ float ldg_keep_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_keep_u8(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ RawScale fetch_scale(const GemmArgs& a, int64_t n, int64_t kb) {
   RawScale r{0.0f, 0u};
   if (n >= a.N_total || kb >= a.KB) return r;
   const int64_t b = n * a.KB + kb;
   if (!a.dq) {
-    r.v = __ldg(a.absmax + b);
+    r.v = ldg_keep_f32(a.absmax + b);
   } else {
-    r.q = __ldg(a.absmax_q + b);
-    r.v = __ldg(a.nested_absmax + (b >> 8));
+    r.q = ldg_keep_u8(a.absmax_q + b);
+    r.v = ldg_keep_f32(a.nested_absmax + (b >> 8));
   }
   return r;
 }
@@ -410,7 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < G::kStagesA; ++i) {
       mbar_init(bar_at(sh, kBarAFull + i), 4);  // the four decoder warps of the step's group
-      mbar_init(bar_at(sh, kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_at(sh, kBarAccFull + i), 1);
@@ -615,28 +629,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         return (c == unit - 1 && p_first) ? p_first + c0 * 32 : sk_slot(c) + c0 * 32;
       };
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
-      // One 16-token batch: tensor-memory load, plus the following CTAs' partials.
+      // Tensor-memory loads are issued kWide columns (tokens) at a time with one wait:
+      // the load latency, not the stores, bounds a narrow batch.
       constexpr int kBatch = 16;
-      auto load_batch = [&](int c0, uint32_t (&v)[kBatch]) {
-        tmem_ld_32x32b_x16(taddr + c0, v);
-        tmem_wait_ld();
-        if (sk_own)
-          for (int64_t c = unit - 1; c >= own_first; --c) {
-            const float* src = part_src(c, c0);
+      constexpr int kWide = BT < 32 ? BT : 32;
+      auto load_wide = [&](int c0, uint32_t (&v)[kWide]) {
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-              v[j] = __float_as_uint(__fadd_rn(__uint_as_float(v[j]), src[j * 32]));
+        for (int b = 0; b < kWide / 16; ++b)
+          tmem_ld_32x32b_x16(taddr + c0 + 16 * b, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * b));
+        tmem_wait_ld();
+      };
+      // Adds the lower CTAs' partials (stream-K owner) to kWide tokens from c0.
+      auto add_partials = [&](int c0, uint32_t (&v)[kWide]) {
+        for (int64_t c = unit - 1; c >= own_first; --c)
+#pragma unroll
+          for (int sb = 0; sb < kWide; sb += 16) {
+            const float* src = part_src(c, c0 + sb);
+            float p[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) p[j] = src[j * 32];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              v[sb + j] = __float_as_uint(__fadd_rn(__uint_as_float(v[sb + j]), p[j]));
           }
       };
       if (sk_part) {
         float* dst = sk_slot(unit);
 #pragma unroll 1
-        for (int c0 = 0; c0 < ntok; c0 += kBatch) {
-          uint32_t v[kBatch];
-          tmem_ld_32x32b_x16(taddr + c0, v);
-          tmem_wait_ld();
+        for (int c0 = 0; c0 < ntok; c0 += kWide) {
+          uint32_t v[kWide];
+          load_wide(c0, v);
 #pragma unroll
-          for (int j = 0; j < kBatch; ++j)
+          for (int j = 0; j < kWide; ++j)
             if (c0 + j < ntok) dst[(c0 + j) * 32] = __uint_as_float(v[j]);
         }
         fence_proxy_async_global();  // the owner may read the partial with a bulk copy
@@ -651,13 +675,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // flight together.
         uint16_t* stg = reinterpret_cast<uint16_t*>(smem + G::kOffOut + q * kOutWarpBytes);
         const uint32_t stg_addr = sbase + G::kOffOut + q * kOutWarpBytes;
-#pragma unroll 1
-        for (int c0 = 0; c0 < ntok; c0 += 32) {
-          if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
-          __syncwarp();
-          uint32_t v[32];
+        uint32_t v[32];
+        auto load_chunk = [&](int c0) {
           tmem_ld_32x32b_x16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
           if (BT > 16) tmem_ld_32x32b_x16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        };
+        load_chunk(0);
+#pragma unroll 1
+        for (int c0 = 0; c0 < ntok; c0 += 32) {
           tmem_wait_ld();
           if (sk_own)
             for (int64_t c = unit - 1; c >= own_first; --c) {
@@ -669,10 +694,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 32; ++j)
                 v[j] = __float_as_uint(__fadd_rn(__uint_as_float(v[j]), p[j]));
             }
+          if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (BT > 16 || j < 16)
               stg[j * 32 + lane] = to16<F16>(__uint_as_float(v[j]));
+          // The next chunk's loads go out now, in flight during this chunk's store.
+          if (c0 + 32 < ntok) load_chunk(c0 + 32);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -763,26 +792,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
         const float bias = MODE == 0 && a.ep_bias && col_ok ? __ldg(a.ep_bias + it.wrow0 + row) : 0.0f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < ntok; c0 += kBatch) {
-          uint32_t v[kBatch];
-          load_batch(c0, v);
+        for (int c0 = 0; c0 < ntok; c0 += kWide) {
+          uint32_t v[kWide];
+          load_wide(c0, v);
+          if (sk_own) add_partials(c0, v);
           if (MODE == 0 && (a.ep_bias || a.ep_scale)) {
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
+            for (int j = 0; j < kWide; ++j) {
               float f = __fadd_rn(__uint_as_float(v[j]), bias);
               if (a.ep_scale && c0 + j < ntok) f = __fmul_rn(f, __ldg(a.ep_scale + it.tok0 + c0 + j));
               v[j] = __float_as_uint(f);
             }
           }
           if (col_ok) {
-            const int nj = ntok - c0;  // valid tokens in this batch when fewer than kBatch
+            const int nj = ntok - c0;  // valid tokens in this batch when fewer than kWide
             if (a.splits > 1) {
 #pragma unroll
-              for (int j = 0; j < kBatch; ++j)
+              for (int j = 0; j < kWide; ++j)
                 if (j < nj) wp[static_cast<int64_t>(c0 + j) * a.ncols] = __uint_as_float(v[j]);
             } else {
 #pragma unroll
-              for (int j = 0; j < kBatch; ++j)
+              for (int j = 0; j < kWide; ++j)
                 if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = to16<F16>(__uint_as_float(v[j]));
             }
           }
@@ -856,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // between).  A walker over (item, step) supplies them; q == kNoStep marks the
     // end of the CTA's sequence.
     constexpr uint32_t kNoStep = 0xffffffffu;
-    constexpr int kAhead = 2;
+    constexpr int kAhead = 3;
     Cursor fcur = cursor_begin(a, unit, total_items);
     Item fit{};
     bool fvalid = cursor_next<MODE, BT>(fcur, a, sh, nunits, fit);

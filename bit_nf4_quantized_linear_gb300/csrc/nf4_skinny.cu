@@ -21,8 +21,12 @@
 // tile; CTA rank r owns one slice of the contraction.  The (tile, contraction
 // step) units of a CTA are dealt to its 16 warps as contiguous ranges, and each
 // warp streams its units' packed codes through its own two-slot ring of
-// shared-memory slots with asynchronous copies (cp.async), one unit ahead of
-// the one it decodes.  The forward decodes each unit's block scales per lane
+// shared-memory slots: one tensor (TMA) tile copy per unit, issued by lane 0 and
+// completing on the slot's barrier, one unit ahead of the one it decodes (the
+// copy engine keeps the slices of all 16 warps in flight at once, which 16-byte
+// copies from every lane could not).  The tile copies write the codes in the
+// swizzled layouts the decode reads conflict-free (128B swizzle for the forward's
+// 128-byte rows, 32B swizzle for the input gradient's 32-byte rows).  The forward decodes each unit's block scales per lane
 // from statistics fetched along with the unit's codes and stages its
 // activation slice in shared memory once; the input gradient decodes the block
 // scales of its slice once into shared memory and carries grad_y in the ring
@@ -53,6 +57,24 @@ namespace {
 using nf4ptx::cluster_sync;
 using nf4ptx::mapa_shared;
 using nf4ptx::smem_addr;
+
+// Bounded wait (2 s) for the phase of `parity` of a ring barrier; false after
+// recording NF4_ERR_TIMEOUT in the status word.
+__device__ __noinline__ bool ring_wait_slow(uint32_t bar, uint32_t parity, int* status) {
+  const uint64_t t0 = nf4ptx::globaltimer_ns();
+  while (!nf4ptx::mbar_try_wait(bar, parity)) {
+    if (nf4ptx::globaltimer_ns() - t0 > 2000000000ull) {
+      if (status) *reinterpret_cast<volatile int*>(status) = kStatusTimeout;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, int* status) {
+  if (nf4ptx::mbar_test_wait(bar, parity)) return true;
+  return ring_wait_slow(bar, parity, status);
+}
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
@@ -293,19 +315,26 @@ constexpr int kFwdDepth = 2;     // ring slots per warp (forward)
 constexpr int kBwdDepth = 2;     // ring slots per warp (input gradient)
 constexpr int kBwdRows = 64;     // weight rows per input-gradient unit
 
+// Input-gradient ring slots: 64 rows x 32 bytes of codes (a whole number of
+// 256-byte swizzle atoms) in one ring, the unit's grad_y (padded rows per token)
+// in a second ring.
+constexpr int kBwdCodeUnit = kBwdRows * 32;
+__host__ __device__ constexpr int bwd_gy_unit_bytes(int mt) { return mt * 8 * (kBwdRows * 2 + 16); }
+
 // Shared-memory layout of a CTA (byte offsets), common to the plan and the kernels.
 struct Layout {
-  int table, ring, first, recv, scales, code8, act, total;
+  int table, ring, gy, first, recv, scales, code8, bars, act, total;
 };
 
 __host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t cc, int64_t nt_max) {
   Layout L;
   const int slot_elems = mode == 0 ? mt * 8 * 16 : mt * 8 * 64;
-  const int unit = mode == 0 ? kFwdUnit : kBwdRows * 32 + mt * 8 * (kBwdRows * 2 + 16);
+  const int unit = mode == 0 ? kFwdUnit : kBwdCodeUnit;
   const int depth = mode == 0 ? kFwdDepth : kBwdDepth;
   L.table = 0;
   L.ring = kTableBytes;
-  L.first = L.ring + kWarps * depth * unit;
+  L.gy = L.ring + kWarps * depth * unit;
+  L.first = L.gy + (mode == 0 ? 0 : kWarps * depth * bwd_gy_unit_bytes(mt));
   L.recv = L.first + kWarps * slot_elems * 4;
   const int64_t total = nt_max * slot_elems;
   const int64_t len = (total + S - 1) / S;
@@ -313,7 +342,10 @@ __host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t c
   // forward: the per-tile warp runs (int2 per tile); input gradient: decoded scales
   const int64_t nscales = mode == 0 ? nt_max * 2 : nt_max * cc;
   L.code8 = L.scales + static_cast<int>((nscales * 4 + 15) / 16 * 16);
-  L.act = L.code8 + 256 * 4;
+  // Forward: one ring barrier per warp and slot here.  The input gradient keeps its
+  // two per warp in the unused padding of its first grad_y row (bytes 128-143).
+  L.bars = L.code8 + 256 * 4;
+  L.act = L.bars + (mode == 0 ? kWarps * kFwdDepth * 8 : 0);
   const int64_t nch = (cc / 64 + kFwdQuad - 1) / kFwdQuad * kFwdQuad;  // forward: chunks of 64
   L.total = mode == 0 ? L.act + static_cast<int>(mt * 8 * nch * 128) : L.act;
   return L;
@@ -334,8 +366,16 @@ __host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t c
 // are XOR-swizzled by (chunk & 3) | (token & 1) << 2, so the eight lanes of a
 // quarter warp (two tokens, four chunks, one unit index) hit different banks.
 template <int MT>  // 8-token MMA tiles: 1 (M <= 8) or 2 (M <= 16)
-__global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_fwd_kernel(const __grid_constant__ CUtensorMap tmap, const SkinnyArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  // The tile copies' swizzle follows absolute shared-memory address bits: the
+  // ring must start on a 1024-byte boundary (it does, after the 64 KB table, when
+  // the dynamic shared memory does).
+  if ((smem_addr(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0 && a.status) *reinterpret_cast<volatile int*>(a.status) = NF4_ERR_UNSUPPORTED;
+    return;
+  }
   constexpr int D = kFwdDepth;
   static_assert(D == 2, "the statistics rotate through two register sets");
   constexpr int kSlotElems = MT * 8 * 16;  // [token][row], a power of two
@@ -363,12 +403,18 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArg
   float* code8s = reinterpret_cast<float*>(smem + L.code8);
   int2* tile_warps = reinterpret_cast<int2*>(smem + L.scales);  // [tile] first and last warp
   uint4* xs = reinterpret_cast<uint4*>(smem + L.act);           // [token][chunk][8 units]
-  const int64_t row_bytes = a.K >> 1;
+  // The warp's ring barriers (one per slot), initialised by its lane 0.
+  const uint32_t bars_s = smem_addr(smem + L.bars) + warp * D * 8;
+  if (lane == 0) {
+    for (int j = 0; j < D; ++j) nf4ptx::mbar_init(bars_s + 8 * j, 1);
+    nf4ptx::fence_mbar_init();
+  }
+  __syncwarp();
 
-  // Copies: lane moves 16-byte chunk c = lane & 7 of rows r0 + 4j (j < 4) of a
-  // unit; (ii, iq) = (tile, block quad) of the next unit to copy.  The same call
-  // fetches the statistics of the lane's two blocks (rows g and g+8, block t4).
-  const int r0 = lane >> 3, cc8 = lane & 7;
+  // Copies: lane 0 issues one tile copy of a unit's 16 rows x 128 bytes (rows
+  // past N and bytes past the row read as zeros); (ii, iq) = (tile, block quad) of
+  // the next unit to copy.  The same call fetches, per lane, the statistics of the
+  // lane's two blocks (rows g and g+8, block t4).
   const uint32_t ring_s = smem_addr(ring);
   int issued = 0, ii = mine.t0, iq = mine.lo - mine.t0 * nq;
   struct Stats {
@@ -391,17 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArg
   auto issue = [&]() -> Stats {
     Stats st{Raw{0.0f, 256u}, Raw{0.0f, 256u}};
     if (issued < nunits) {
-      const uint32_t dst = ring_s + (issued & (D - 1)) * kFwdUnit;
+      const int slot = issued & (D - 1);
       const int64_t n16 = (tile0 + ii) * 16;
       const int64_t kbq = kb0 + kFwdQuad * iq;
-      const bool cok = kFwdQuad * iq + (cc8 >> 1) < nbr;
-      const uint8_t* src = a.packed + (n16 + r0) * row_bytes + kbq * 32 + 16 * cc8;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = r0 + 4 * j;
-        const bool ok = cok && n16 + r < a.N;
-        cp_async16(dst + (r * 8 + (cc8 ^ (r & 7))) * 16, ok ? src + 4 * j * row_bytes : a.packed,
-                   ok);
+      // Blocks of the quad past this rank's slice come in too; their scales (and
+      // activations) are zero, so they add nothing.
+      if (lane == 0) {
+        const uint32_t bar = bars_s + 8 * slot;
+        nf4ptx::mbar_arrive_expect_tx(bar, kFwdUnit);
+        nf4ptx::tma_load_2d(ring_s + slot * kFwdUnit, &tmap, bar, static_cast<int32_t>(kbq * 32),
+                            static_cast<int32_t>(n16));
       }
       const bool bok = kFwdQuad * iq + t4 < nbr;
       st.a = fetch(n16 + g, kbq + t4, bok && n16 + g < a.N);
@@ -412,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArg
       }
     }
     ++issued;
-    cp_async_commit();
     return st;
   };
   Stats s0, s1;  // statistics of the units in ring slots (q and q+1)
@@ -476,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArg
     }
   };
 
-  for (int q = 0; q < nunits; ++q) {
-    cp_async_wait<D - 1>();
-    __syncwarp();
+  int q = 0;
+  for (; q < nunits; ++q) {
+    if (!ring_wait(bars_s + 8 * (q & (D - 1)), static_cast<uint32_t>(q / D) & 1u, a.status)) break;
     const uint8_t* slot = ring + (q & (D - 1)) * kFwdUnit;
     const int i = ci, kbl = kFwdQuad * cq + t4;
     if (++cq == nq) {
@@ -523,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArg
     s0 = s1;
     s1 = issue();
   }
-  cp_async_wait<0>();
+  // After a wait that ran out, the copies still in flight land before the ring is
+  // reused or the CTA exits.
+  for (; q < issued && q < nunits; ++q)
+    ring_wait(bars_s + 8 * (q & (D - 1)), static_cast<uint32_t>(q / D) & 1u, nullptr);
   __syncwarp();
   if (nunits > 0) store_acc(reinterpret_cast<float*>(ring));  // last tile -> own ring
   __syncthreads();
@@ -570,12 +617,21 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_fwd_kernel(const SkinnyArg
 // scales; a lane's accumulators stay on its own 16 in-features for the whole
 // column.  The unit's grad_y values travel in the same ring slot as its codes.
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    skinny_dgrad_kernel(const __grid_constant__ CUtensorMap tmap, const SkinnyArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  // The tile copies' swizzle follows absolute shared-memory address bits: the
+  // ring must start on a 1024-byte boundary (it does, after the 64 KB table, when
+  // the dynamic shared memory does).
+  if ((smem_addr(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0 && a.status) *reinterpret_cast<volatile int*>(a.status) = NF4_ERR_UNSUPPORTED;
+    return;
+  }
   constexpr int D = kBwdDepth;
   constexpr int kRows = kBwdRows;                  // weight rows per unit
   constexpr int kGyPitch = kRows * 2 + 16;         // bytes per token (padded)
-  constexpr int kUnit = kRows * 32 + MT * 8 * kGyPitch;
+  constexpr int kUnit = kBwdCodeUnit;              // code ring slot
+  constexpr int kGyUnit = bwd_gy_unit_bytes(MT);   // grad_y ring slot
   constexpr int kSlotElems = MT * 8 * 64;          // [token][in-feature]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -593,16 +649,27 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
   const int nunits = mine.hi - mine.lo;
   const Layout L = make_layout(1, MT, S, a.cc, nt_max);
   uint8_t* ring = smem + L.ring + warp * D * kUnit;
+  uint8_t* gyring = smem + L.gy + warp * D * kGyUnit;
   float* first = reinterpret_cast<float*>(smem + L.first);
   float* recv = reinterpret_cast<float*>(smem + L.recv);
   float* sc = reinterpret_cast<float*>(smem + L.scales);  // [column][row - nr0]
-  const int64_t row_bytes = a.K >> 1;
   const int ccs = static_cast<int>(a.cc);
+  // The warp's ring barriers (one per slot, for the code tiles), initialised by
+  // its lane 0: the padding bytes 128-143 of grad_y slot 0's first token row,
+  // which no copy writes and no lookup reads.
+  static_assert(kGyPitch >= kRows * 2 + 8 * D, "barriers in the grad_y row padding");
+  const uint32_t bars_s = smem_addr(gyring) + kRows * 2;
+  if (lane == 0) {
+    for (int j = 0; j < D; ++j) nf4ptx::mbar_init(bars_s + 8 * j, 1);
+    nf4ptx::fence_mbar_init();
+  }
+  __syncwarp();
 
-  // Copies of unit (ii, ij): code half (lane & 1) of rows (lane >> 1) + 16 j and
-  // grad_y chunks lane + 32 j (token c >> 3, rows 8 (c & 7) ..); ragged ends and
-  // absent tokens are written directly.
-  const int cr = lane >> 1, ch = lane & 1;
+  // Copies of unit (ii, ij): one tile copy by lane 0 of the codes of rows n0 ..
+  // n0 + 63 of block column kb (rows past N read as zeros; rows of the next rank
+  // come in too and meet zero scales and zero grad_y), and grad_y chunks lane +
+  // 32 j (token c >> 3, rows 8 (c & 7) ..) by every lane; ragged ends and absent
+  // tokens are written directly.
   const uint32_t ring_s = smem_addr(ring);
   int issued = 0, ii = mine.t0, ij = mine.lo - mine.t0 * nn;
   auto gy_edge = [&](uint8_t* d, int tok, int64_t ng) {  // 8 values from row ng, zero-padded
@@ -621,16 +688,16 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
     for (int j = 0; j < MT * 8 * 8 / 32; ++j) {
       const int c = lane + 32 * j, tok = c >> 3, part = c & 7;
       const int64_t ng = n0 + 8 * part;
-      const uint32_t off = slot * kUnit + kRows * 32 + tok * kGyPitch + part * 16;
+      const uint32_t off = slot * kGyUnit + tok * kGyPitch + part * 16;
       if (tok >= a.M) continue;  // absent tokens only feed discarded outputs
       if (ng + 8 <= nr1) {
         if (async)
-          cp_async16(ring_s + off, a.act + tok * a.ld_act + ng, true);
+          cp_async16(smem_addr(gyring) + off, a.act + tok * a.ld_act + ng, true);
         else
-          *reinterpret_cast<uint4*>(ring + off) =
+          *reinterpret_cast<uint4*>(gyring + off) =
               *reinterpret_cast<const uint4*>(a.act + tok * a.ld_act + ng);
       } else {
-        gy_edge(ring + off, tok, ng);
+        gy_edge(gyring + off, tok, ng);
       }
     }
   };
@@ -639,13 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
       const int slot = issued % D;
       const int64_t kb = col0 + ii;
       const int64_t n0 = nr0 + static_cast<int64_t>(kRows) * ij;
-#pragma unroll
-      for (int j = 0; j < kRows / 16; ++j) {
-        const int r = cr + 16 * j;
-        const int64_t n = n0 + r;
-        const bool ok = n < nr1;
-        cp_async16(ring_s + slot * kUnit + code_unit(r, ch) * 16,
-                   ok ? a.packed + n * row_bytes + kb * 32 + 16 * ch : a.packed, ok);
+      if (lane == 0) {
+        const uint32_t bar = bars_s + 8 * slot;
+        nf4ptx::mbar_arrive_expect_tx(bar, kRows * 32);
+        nf4ptx::tma_load_2d(ring_s + slot * kUnit, &tmap, bar, static_cast<int32_t>(kb * 32),
+                            static_cast<int32_t>(n0));
       }
       if (with_gy) copy_gy(slot, n0, true);
       if (++ij == nn) {
@@ -704,10 +769,13 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
       }
   };
 
-  for (int q = 0; q < nunits; ++q) {
-    cp_async_wait<D - 1>();
+  int q = 0;
+  for (; q < nunits; ++q) {
+    cp_async_wait<D - 1>();  // this unit's grad_y
     __syncwarp();
+    if (!ring_wait(bars_s + 8 * (q % D), static_cast<uint32_t>(q / D) & 1u, a.status)) break;
     const uint8_t* slot = ring + (q % D) * kUnit;
+    const uint8_t* gslot = gyring + (q % D) * kGyUnit;
     const int i = ci;
     const int nl0 = kRows * cj;  // first row of the unit, relative to nr0
     if (++cj == nn) {
@@ -733,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
       uint32_t b[MT][2];
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
-        const uint8_t* gy = slot + kRows * 32 + (8 * t + g) * kGyPitch + (16 * rg + 2 * t4) * 2;
+        const uint8_t* gy = gslot + (8 * t + g) * kGyPitch + (16 * rg + 2 * t4) * 2;
         b[t][0] = *reinterpret_cast<const uint32_t*>(gy);
         b[t][1] = *reinterpret_cast<const uint32_t*>(gy + 16);
       }
@@ -755,6 +823,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
     __syncwarp();
     issue(true);
   }
+  // After a wait that ran out, the copies still in flight land before the ring is
+  // reused or the CTA exits.
+  for (; q < issued && q < nunits; ++q)
+    ring_wait(bars_s + 8 * (q % D), static_cast<uint32_t>(q / D) & 1u, nullptr);
   cp_async_wait<0>();
   __syncwarp();
   if (nunits > 0) store_acc(reinterpret_cast<float*>(ring));  // last column -> own ring
@@ -778,8 +850,10 @@ __global__ void __launch_bounds__(kThreads, 1) skinny_dgrad_kernel(const SkinnyA
   if (S > 1) cluster_finish(recv, rank, S, total, store);
 }
 
+using SkinnyKernel = void (*)(CUtensorMap, SkinnyArgs);
+
 template <int MODE, int MT>
-cudaError_t configure(void (*&kern)(SkinnyArgs)) {
+cudaError_t configure(SkinnyKernel& kern) {
   kern = MODE == 0 ? skinny_fwd_kernel<MT> : skinny_dgrad_kernel<MT>;
   static bool configured = false;
   if (!configured) {
@@ -794,7 +868,7 @@ cudaError_t configure(void (*&kern)(SkinnyArgs)) {
 // Clusters of S CTAs (with `smem` bytes each) that can be resident at once.
 template <int MODE, int MT>
 int max_clusters_mt(int S, size_t smem) {
-  void (*kern)(SkinnyArgs) = nullptr;
+  SkinnyKernel kern = nullptr;
   if (configure<MODE, MT>(kern) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(S), 1, 1);
@@ -837,8 +911,9 @@ int max_clusters(int mode, int mt, int S, size_t smem) {
 }
 
 template <int MODE, int MT>
-cudaError_t launch_mt(const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s) {
-  void (*kern)(SkinnyArgs) = nullptr;
+cudaError_t launch_mt(const SkinnyArgs& a, const SkinnyPlan& p, const CUtensorMap& tmap,
+                      cudaStream_t s) {
+  SkinnyKernel kern = nullptr;
   cudaError_t ce = configure<MODE, MT>(kern);
   if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
@@ -860,7 +935,7 @@ cudaError_t launch_mt(const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s) 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, a);
 }
 
 }  // namespace
@@ -921,10 +996,11 @@ bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan*
   return true;
 }
 
-cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, cudaStream_t s) {
+cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, const CUtensorMap& tmap,
+                          cudaStream_t s) {
   const bool mt1 = a.M <= 8;
-  if (mode == 0) return mt1 ? launch_mt<0, 1>(a, p, s) : launch_mt<0, 2>(a, p, s);
-  return mt1 ? launch_mt<1, 1>(a, p, s) : launch_mt<1, 2>(a, p, s);
+  if (mode == 0) return mt1 ? launch_mt<0, 1>(a, p, tmap, s) : launch_mt<0, 2>(a, p, tmap, s);
+  return mt1 ? launch_mt<1, 1>(a, p, tmap, s) : launch_mt<1, 2>(a, p, tmap, s);
 }
 
 }  // namespace nf4
