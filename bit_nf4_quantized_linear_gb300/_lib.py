@@ -25,7 +25,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD, OP_GROUPED_SWIGLU_BWD = range(6)
 PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
          "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad", "skinny_fwd",
-         "skinny_dgrad", "stream_k"]
+         "skinny_dgrad", "stream_k", "cluster_split"]
 
 
 class NF4Error(RuntimeError):
@@ -69,6 +69,7 @@ class nf4_plan_info(ctypes.Structure):
         ("grid", ctypes.c_int32),
         ("items", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64),
+        ("cluster_split", ctypes.c_int32),
     ]
 
 
@@ -122,6 +123,7 @@ def lib() -> ctypes.CDLL:
             "nf4_set_weight_prefetch": [I32],
             "nf4_set_small_m_path": [I32],
             "nf4_set_stream_k": [I32],
+            "nf4_set_cluster_split": [I32],
             "nf4_inject_stream_k_timeout": [],
             "nf4_plan_query": [I32, I64, I64, I64, I32, I32, I32, ctypes.POINTER(nf4_plan_info)],
         }
@@ -137,6 +139,7 @@ def lib() -> ctypes.CDLL:
         L.nf4_set_weight_prefetch.restype = None
         L.nf4_set_small_m_path.restype = None
         L.nf4_set_stream_k.restype = None
+        L.nf4_set_cluster_split.restype = None
         L.nf4_inject_stream_k_timeout.restype = None
         _lib = L
         return _lib
@@ -177,6 +180,13 @@ STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_FORCE = 0, 1, 2
 
 def set_stream_k(mode: int):
     lib().nf4_set_stream_k(int(mode))
+
+
+CLUSTER_SPLIT_OFF, CLUSTER_SPLIT_AUTO, CLUSTER_SPLIT_FORCE = 0, 1, 2
+
+
+def set_cluster_split(mode: int):
+    lib().nf4_set_cluster_split(int(mode))
 
 
 def plan_query(op: int, M: int, N: int, K: int, sms: int, bits: int = 4, f16: bool = False) -> dict:

@@ -51,6 +51,11 @@ struct GemmArgs {
   int* status;
   int prefetch;  // dense: the weight may be read before the preceding grid has finished
   int tma_out;  // dense bf16 output written by bulk tensor stores (aligned out and ld_out)
+  // Cluster split (dense, tma_out): cs > 1 CTAs, one cluster, share each tile, one
+  // contraction slice each (items = tiles x cs, one per CTA, splits == cs); token
+  // slice p of the tile (bt / cs tokens) is summed and stored by cluster rank p from
+  // the partials the other ranks write into its activation ring.
+  int cs;
   // Grouped forward epilogue (nf4_grouped_fwd_ep): fp32 bias per weight row, fp32
   // scale per output row (routing weights), SwiGLU of interleaved gate/up rows.
   const float* ep_bias;
@@ -179,6 +184,12 @@ cudaError_t launch_gemm_f16(int mode, int bt, const GemmArgs& a, const CUtensorM
                             cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  void* out, int64_t ld, bool f16, cudaStream_t s);
+// Bytes of the fused kernel's activation ring for a token tile and code width (the
+// receive area of a cluster split).
+size_t gemm_ring_bytes(int bt, int bits);
+// Clusters of `cs` CTAs of the fused kernel (4-bit bf16 instance of `bt`) that can
+// be resident at once on the current device; 0 when it cannot be queried.
+int gemm_cluster_capacity(int mode, int bt, int cs);
 // out[t] = sum over p = 0 .. P-1 in order of part[p][t] for rows inside the expert
 // ranges (offsets[0] <= t < offsets[E]), 0 for the other rows of [0, T).
 cudaError_t launch_row_partial_sum(const float* part, int P, int64_t T, const int32_t* offsets,

@@ -171,6 +171,7 @@ struct Plan {
   nf4::SkinnyPlan sk;
   bool stream_k = false;  // fused kernel with the stream-K schedule
   int sk_ctas = 0;
+  int cs = 0;  // cluster split: CTAs per tile (one cluster), 0 for none
 };
 
 Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
@@ -197,6 +198,19 @@ std::atomic<int> g_inject_sk_timeout{0};
 
 // Stream-K schedule of the fused kernel (nf4_set_stream_k).
 std::atomic<int> g_stream_k{NF4_STREAM_K_AUTO};
+
+// Cluster split of the fused kernel (nf4_set_cluster_split).
+std::atomic<int> g_cluster_split{NF4_CLUSTER_SPLIT_AUTO};
+
+// Clusters of cs CTAs that can be resident at once: the device's answer when one is
+// current, else the SM count's bound (host-only plan queries).
+int cluster_capacity(int mode, int bt, int cs, int sms, bool query_device) {
+  if (query_device) {
+    const int n = nf4::gemm_cluster_capacity(mode, bt, cs);
+    if (n > 0) return n;
+  }
+  return sms / cs;
+}
 
 // Epoch a stream-K launch publishes in its ready flags: unique per launch of the
 // process, never 0.  The flags live in the caller's workspace and the CTA that
@@ -226,7 +240,7 @@ double step_cycles(int bt) {
 // model in SM clocks -- waves of items times contraction steps, plus the split
 // partials' round trip through memory.
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true,
-                int bits = 4, bool f16 = false) {
+                int bits = 4, bool f16 = false, bool allow_cs = true, bool query_device = false) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
   const int small = g_small_m_path.load(std::memory_order_relaxed);
@@ -311,8 +325,50 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
       }
     }
   }
-  if (sk_best.stream_k && (skm == NF4_STREAM_K_FORCE || sk_t < best_t * 0.97)) return sk_best;
-  return best;
+  // Cluster split: when every tile, cut into cs contraction slices (2..8, at least
+  // 32 tokens of the tile per slice), fits the device in one wave of clusters, the
+  // slices of a tile run on the cs CTAs of one cluster and meet in shared memory:
+  // no fp32 partials in global memory and no reduction kernel.  Cost: the slice's
+  // steps, plus a fixed cost and the exchange (each rank writes (cs - 1) / cs of
+  // its partial tile through distributed shared memory).
+  const int csm = allow_cs && bits == 4 ? g_cluster_split.load(std::memory_order_relaxed)
+                                        : NF4_CLUSTER_SPLIT_OFF;
+  Plan cs_best;
+  double cs_t = 1e300;
+  if (csm != NF4_CLUSTER_SPLIT_OFF) {
+    const int cand_cs[3] = {2, 4, 8};
+    for (int ci = 0; ci < 3; ++ci) {
+      const int bt = cand_bt[ci];
+      if (bt > bt_max) continue;
+      const int64_t ttiles = (M + bt - 1) / bt;
+      const int64_t tiles = ((ncols + nf4::kTileW - 1) / nf4::kTileW) * ttiles;
+      for (int si = 0; si < 3; ++si) {
+        const int cs = cand_cs[si];
+        if (bt / cs < 32 || ksteps < cs) continue;
+        const size_t recv = static_cast<size_t>(cs - 1) * 4 * 32 * (bt / cs + 4) * 4;
+        if (recv > nf4::gemm_ring_bytes(bt, 4)) continue;
+        if (tiles > cluster_capacity(mode, bt, cs, sms, query_device)) continue;
+        const double t = static_cast<double>((ksteps + cs - 1) / cs) * step_cycles(bt) + 3000.0 +
+                         1500.0 + 8.0 * bt * (cs - 1) / cs;
+        if (t < cs_t * 0.999) {
+          cs_t = t;
+          cs_best = make_plan(M, ncols, contract, bt, cs);
+          cs_best.cs = cs;
+          cs_best.ws_bytes = 0;
+        }
+      }
+    }
+  }
+  double best_any = best_t;
+  Plan chosen = best;
+  if (sk_best.stream_k && (skm == NF4_STREAM_K_FORCE || sk_t < best_t * 0.97)) {
+    chosen = sk_best;
+    best_any = sk_t;
+  }
+  if (cs_best.cs > 1 && (csm == NF4_CLUSTER_SPLIT_FORCE ||
+                         (skm != NF4_STREAM_K_FORCE && cs_t < best_any * 0.97)))
+    return cs_best;
+  return chosen;
 }
 
 nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const nf4_weight* w,
@@ -335,7 +391,10 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   const int bits = w->bits == 8 ? 8 : 4;
   if (f16 && bits == 8) return NF4_ERR_UNSUPPORTED;  // fp16 dtype: 4-bit codes
-  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk, bits, f16);
+  // A cluster split stores its bf16 tile with bulk tensor stores, which need a
+  // 16-byte aligned output and row pitch.
+  const bool out_tma_ok = aligned16(out) && ld_out % 8 == 0;
+  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk, bits, f16, out_tma_ok, true);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -445,6 +504,10 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
   const int64_t units = dev.sms;
   int grid = static_cast<int>(p.items < units ? p.items : units);
+  if (p.cs > 1) {
+    a.cs = p.cs;  // items = tiles x cs, one per CTA, the clusters in one wave
+    grid = static_cast<int>(p.items);
+  }
   if (p.stream_k) {
     a.sk = 1;
     a.sk_units = p.items * p.ksteps;
@@ -461,7 +524,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   // meet the 16-byte rule; otherwise through direct stores.
   CUtensorMap tmap_out;
   std::memset(&tmap_out, 0, sizeof(tmap_out));
-  if (p.splits == 1 && aligned16(out) && ld_out % 8 == 0) {
+  if ((p.splits == 1 || p.cs > 1) && out_tma_ok) {
     if (!encode_2d(&tmap_out, dt16, out, out_cols, M, ld_out * 2, 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return NF4_ERR_CUDA;
@@ -472,7 +535,8 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   count(mode == 0 ? NF4_PATH_LINEAR_FWD : NF4_PATH_LINEAR_DGRAD);
   if (p.stream_k)  // a property of the launch just counted, not a launch of its own
     g_counters[NF4_PATH_STREAM_K].fetch_add(1, std::memory_order_relaxed);
-  if (p.splits > 1) {
+  if (p.cs > 1) g_counters[NF4_PATH_CLUSTER_SPLIT].fetch_add(1, std::memory_order_relaxed);
+  if (p.splits > 1 && p.cs == 0) {
     le = nf4::launch_splitk_reduce(static_cast<const float*>(ws), p.splits, M, out_cols, out,
                                    ld_out, f16, s);
     if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
@@ -744,8 +808,9 @@ size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E
     // Enough for either code width (the plan depends on it).
     const int mode = op == NF4_OP_LINEAR_FWD ? 0 : 1;
     size_t need = 0;
-    for (int v = 0; v < 3; ++v) {  // 4-bit bf16, 8-bit bf16, 4-bit fp16
-      const size_t b = plan_dense(mode, M, N, K, dev.sms, true, v == 1 ? 8 : 4, v == 2).ws_bytes;
+    for (int v = 0; v < 6; ++v) {  // 4-bit bf16, 8-bit bf16, 4-bit fp16; aligned output or not
+      const size_t b = plan_dense(mode, M, N, K, dev.sms, true, v % 3 == 1 ? 8 : 4, v % 3 == 2, v < 3,
+                                  true).ws_bytes;
       need = b > need ? b : need;
     }
     return need;
@@ -803,6 +868,11 @@ void nf4_set_stream_k(int32_t mode) {
     g_stream_k.store(mode, std::memory_order_relaxed);
 }
 
+void nf4_set_cluster_split(int32_t mode) {
+  if (mode >= NF4_CLUSTER_SPLIT_OFF && mode <= NF4_CLUSTER_SPLIT_FORCE)
+    g_cluster_split.store(mode, std::memory_order_relaxed);
+}
+
 void nf4_inject_stream_k_timeout(void) { g_inject_sk_timeout.store(1, std::memory_order_relaxed); }
 
 nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t sms, int32_t bits,
@@ -811,7 +881,7 @@ nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t s
       (bits != 4 && bits != 8) || (f16 && bits == 8) || M <= 0 || N <= 0 || K <= 0)
     return NF4_ERR_INVALID_ARG;
   const int mode = op == NF4_OP_LINEAR_FWD ? 0 : 1;
-  const Plan p = plan_dense(mode, M, N, K, sms, true, bits, f16 != 0);
+  const Plan p = plan_dense(mode, M, N, K, sms, true, bits, f16 != 0, true, true);
   nf4_plan_info r{};
   r.kernel = p.skinny ? NF4_PLAN_SMALL_M_MMA : p.gemv ? NF4_PLAN_SIMT_GEMV : NF4_PLAN_FUSED;
   r.token_tile = p.bt;
@@ -825,6 +895,7 @@ nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t s
   }
   r.items = p.items;
   r.workspace_bytes = p.ws_bytes;
+  r.cluster_split = p.cs;
   *out = r;
   return NF4_OK;
 }
@@ -893,8 +964,8 @@ extern "C" nf4_status nf4_linear_fwd_noalloc(const void* x, int64_t M, int64_t l
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
   // The stream-K schedule is not used here (its partial tiles outgrow the array);
   // shapes whose split partials would not fit are rejected up front.
-  if (plan_dense(0, M, w->N, w->K, dev.sms, false, w->bits == 8 ? 8 : 4).ws_bytes >
-      NF4_NOALLOC_SCRATCH_BYTES)
+  if (plan_dense(0, M, w->N, w->K, dev.sms, false, w->bits == 8 ? 8 : 4, false,
+                 aligned16(y) && ldy % 8 == 0, true).ws_bytes > NF4_NOALLOC_SCRATCH_BYTES)
     return NF4_ERR_WORKSPACE;
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);

@@ -37,6 +37,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "decode.cuh"
@@ -125,7 +126,9 @@ constexpr int kBarDrain = 60;
 constexpr int kBarEpFull = 61;   // SwiGLU epilogue: up values of a batch written (2 warp pairs)
 constexpr int kBarEpEmpty = 63;  // ... and read by the gate warp
 constexpr int kBarSkPart = 65;   // stream-K: a lower CTA's partial landed (one per epilogue warp)
-constexpr int kNumBars = 69;
+constexpr int kBarCsFree = 69;   // cluster split: every other rank's ring is free (their arrivals)
+constexpr int kBarCsRecv = 70;   // cluster split: the other ranks' partials of this rank's slice landed
+constexpr int kNumBars = 71;
 // Misc region: codebooks (16 + 256 fp32), barriers, four words (tensor-memory
 // slot, abort flag, item count, dependency flag), three expert tables.
 static_assert((16 + 256) * 4 + kNumBars * 8 + 16 + 3 * (kMaxExperts + 1) * 4 <= kMiscBase,
@@ -205,6 +208,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
                                            const GemmArgs& a) {
   if (mbar_test_wait(bar, parity)) return true;
   return wait_phase_slow(bar, parity, sh, a);
+}
+
+// Bounded wait on a phase completed by arrivals of other CTAs of the cluster
+// (acquire at cluster scope); as wait_phase otherwise.
+__device__ __noinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Shared& sh,
+                                                const GemmArgs& a) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep_cluster(bar, parity, kSleepHintNs)) return true;
+    if (*sh.abort_flag) return false;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      *sh.abort_flag = 1;
+      record_error(a, kStatusTimeout);
+      return false;
+    }
+  }
 }
 
 // Wait used while draining on exit: bounded, ignores the abort flag.
@@ -436,6 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarEpEmpty + i), 1);
     }
     for (int i = 0; i < kNumEpiWarps; ++i) mbar_init(bar_at(sh, kBarSkPart + i), 1);
+    const int cs_peers = a.cs > 1 ? a.cs - 1 : 1;
+    mbar_init(bar_at(sh, kBarCsFree), cs_peers);                  // one arrival per other rank
+    mbar_init(bar_at(sh, kBarCsRecv), cs_peers * kNumEpiWarps);   // each of their epilogue warps
     *sh.abort_flag = 0;
     *dep_done(sh) = early ? 0 : 1;
     fence_mbar_init();
@@ -470,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad) record_error(a, kStatusBadOffsets);
   }
   __syncthreads();
+  if (a.cs > 1) cluster_sync();  // every rank's barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *sh.tmem_slot;
   const int64_t total_items =
@@ -543,8 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
           tc_fence_after();
           // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
-          const uint64_t adesc0 = a_desc_hi | ((sbase + G::kOffA + sa * kAStage) >> 4);
-          const uint64_t bdesc0 = b_desc_hi | ((sbase + G::kOffX + sx * G::kXStage) >> 4);
+          // Only the CTA-local offset goes there: in a cluster launch the shared
+          // addresses of ranks above 0 carry the rank in higher bits, which would
+          // otherwise spill into the leading-byte-offset field (used by the
+          // MN-major operand of the input gradient).
+          const uint64_t adesc0 = a_desc_hi | (((sbase + G::kOffA + sa * kAStage) & 0x3FFFFu) >> 4);
+          const uint64_t bdesc0 = b_desc_hi | (((sbase + G::kOffX + sx * G::kXStage) & 0x3FFFFu) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk) {
             const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
@@ -653,7 +681,102 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[sb + j] = __float_as_uint(__fadd_rn(__uint_as_float(v[sb + j]), p[j]));
           }
       };
-      if (sk_part) {
+      if (a.cs > 1) {
+        // Cluster split: the cs CTAs of this cluster hold one contraction slice each
+        // of the same tile, and rank p finishes token slice p (W = BT / cs tokens).
+        // Each rank writes its fp32 partial of the other slices into their owners'
+        // activation rings (idle once the tile's MMAs are done) through distributed
+        // shared memory, then adds the partials of its own slice in rank order and
+        // stores it in bf16.  In rank p's ring, the block of (sending rank, with p
+        // itself skipped, row quarter) holds 32 rows x W tokens fp32 at a row pitch of
+        // W + 4 floats, so that the owner's 16-byte row reads are conflict-free.
+        const int S = a.cs;
+        const int rank = static_cast<int>(cluster_ctarank());
+        const int W = BT / S;
+        const int pitch = W + 4;
+        auto recv_off = [&](int slot, int qq) {  // byte offset of a block in the ring
+          return ((slot * kNumEpiWarps + qq) * 32) * pitch * 4;
+        };
+        bool cs_ok = (S - 1) * kNumEpiWarps * 32 * pitch * 4 <= G::kStagesX * G::kXStage && W % 32 == 0;
+        if (!cs_ok) record_error(a, NF4_ERR_UNSUPPORTED_SHAPE);
+        // 1. This rank's ring is free (its MMAs are done): tell every other rank.
+        if (cs_ok && q == 0 && lane == 0)
+          for (int p = 0; p < S; ++p)
+            if (p != rank) mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarCsFree), static_cast<uint32_t>(p)));
+        // 2. Once every other rank's ring is free, send each its slice of this partial.
+        if (cs_ok) cs_ok = wait_phase_cluster(bar_at(sh, kBarCsFree), 0, sh, a);
+        if (cs_ok) {
+          for (int p = 0; p < S; ++p) {
+            if (p == rank) continue;
+            const int slot = rank < p ? rank : rank - 1;
+            const uint32_t dst = mapa_shared(sbase + G::kOffX + static_cast<uint32_t>(recv_off(slot, q) + lane * pitch * 4),
+                                             static_cast<uint32_t>(p));
+            for (int c0 = 0; c0 < W && p * W + c0 < ntok; c0 += 16) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(taddr + p * W + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 16; k += 4)
+                st_cluster_v4(dst + static_cast<uint32_t>((c0 + k) * 4), v[k], v[k + 1], v[k + 2], v[k + 3]);
+            }
+          }
+          asm volatile("fence.acq_rel.cluster;" ::: "memory");  // this lane's stores, then the arrival
+          __syncwarp();
+          if (lane == 0)
+            for (int p = 0; p < S; ++p)
+              if (p != rank) mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarCsRecv), static_cast<uint32_t>(p)));
+        }
+        // 3. This rank's slice: the ranks' partials added in rank order, to bf16,
+        // through shared-memory staging and bulk tensor stores (tokens past M are not
+        // written).
+        if (cs_ok) cs_ok = wait_phase_cluster(bar_at(sh, kBarCsRecv), 0, sh, a);
+        if (cs_ok) {
+          const int t0 = rank * W;
+          uint16_t* stg = reinterpret_cast<uint16_t*>(smem + G::kOffOut + q * kOutWarpBytes);
+          const uint32_t stg_addr = sbase + G::kOffOut + q * kOutWarpBytes;
+#pragma unroll 1
+          for (int c0 = 0; c0 < W && t0 + c0 < ntok; c0 += 32) {
+            if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
+            __syncwarp();
+#pragma unroll 1
+            for (int h = 0; h < 32; h += 16) {  // two 16-token halves of the chunk
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(taddr + t0 + c0 + h, v);
+              tmem_wait_ld();
+              float acc[16];
+#pragma unroll 1
+              for (int r = 0; r < S; ++r) {
+                if (r == rank) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    acc[j] = r == 0 ? __uint_as_float(v[j]) : __fadd_rn(acc[j], __uint_as_float(v[j]));
+                } else {
+                  const int slot = r < rank ? r : r - 1;
+                  const float* src = reinterpret_cast<const float*>(smem + G::kOffX + recv_off(slot, q) +
+                                                                    lane * pitch * 4) + c0 + h;
+#pragma unroll
+                  for (int j = 0; j < 16; j += 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(src + j);
+                    acc[j] = r == 0 ? f.x : __fadd_rn(acc[j], f.x);
+                    acc[j + 1] = r == 0 ? f.y : __fadd_rn(acc[j + 1], f.y);
+                    acc[j + 2] = r == 0 ? f.z : __fadd_rn(acc[j + 2], f.z);
+                    acc[j + 3] = r == 0 ? f.w : __fadd_rn(acc[j + 3], f.w);
+                  }
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) stg[(h + j) * 32 + lane] = to16<F16>(acc[j]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_out, stg_addr, static_cast<int32_t>(it.col0 + 32 * q),
+                           static_cast<int32_t>(it.tok0 + t0 + c0));
+              bulk_commit_group();
+            }
+          }
+        }
+      } else if (sk_part) {
         float* dst = sk_slot(unit);
 #pragma unroll 1
         for (int c0 = 0; c0 < ntok; c0 += kWide) {
@@ -1002,6 +1125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // A cluster leaves together: no rank exits while another may still write into its
+  // shared memory or arrive on its barriers.
+  if (a.cs > 1) cluster_sync();
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem_base, G::kTmemCols);
@@ -1116,11 +1242,15 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Geo<BT, BITS>::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // cluster split: one tile per cluster
+  attr[1].val.clusterDim.x = a.cs > 1 ? static_cast<unsigned>(a.cs) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.cs > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tp, to, a);
 }
 
@@ -1175,6 +1305,75 @@ cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensor
   return launch_mode<1>(bt, a, tmap_act, tmap_packed, tmap_out, grid, s);
 }
 #else
+
+size_t gemm_ring_bytes(int bt, int bits) {
+  switch (bits == 8 ? bt + 1 : bt) {
+    case 16: return size_t(Geo<16, 4>::kStagesX) * Geo<16, 4>::kXStage;
+    case 32: return size_t(Geo<32, 4>::kStagesX) * Geo<32, 4>::kXStage;
+    case 64: return size_t(Geo<64, 4>::kStagesX) * Geo<64, 4>::kXStage;
+    case 128: return size_t(Geo<128, 4>::kStagesX) * Geo<128, 4>::kXStage;
+    case 256: return size_t(Geo<256, 4>::kStagesX) * Geo<256, 4>::kXStage;
+    case 17: return size_t(Geo<16, 8>::kStagesX) * Geo<16, 8>::kXStage;
+    case 33: return size_t(Geo<32, 8>::kStagesX) * Geo<32, 8>::kXStage;
+    case 65: return size_t(Geo<64, 8>::kStagesX) * Geo<64, 8>::kXStage;
+    case 129: return size_t(Geo<128, 8>::kStagesX) * Geo<128, 8>::kXStage;
+    default: return 0;
+  }
+}
+
+template <int MODE, int BT>
+int cluster_capacity_bt(int cs) {
+  auto kern = nf4_gemm_kernel<MODE, BT, 4, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<BT, 4>::kSmem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Geo<BT, 4>::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int gemm_cluster_capacity(int mode, int bt, int cs) {
+  struct Entry {
+    int dev, mode, bt, cs, n;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int used = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].mode == mode && cache[i].bt == bt && cache[i].cs == cs)
+      return cache[i].n;
+  int n = 0;
+  switch (bt) {
+    case 64: n = mode == 0 ? cluster_capacity_bt<0, 64>(cs) : cluster_capacity_bt<1, 64>(cs); break;
+    case 128: n = mode == 0 ? cluster_capacity_bt<0, 128>(cs) : cluster_capacity_bt<1, 128>(cs); break;
+    case 256: n = mode == 0 ? cluster_capacity_bt<0, 256>(cs) : cluster_capacity_bt<1, 256>(cs); break;
+    default: n = 0;
+  }
+  if (used < 64) cache[used++] = Entry{dev, mode, bt, cs, n};
+  return n;
+}
 
 cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,

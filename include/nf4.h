@@ -88,7 +88,8 @@ enum {
   NF4_PATH_SKINNY_FWD = 10,  /* small-M tensor-core (mma.sync) forward     */
   NF4_PATH_SKINNY_DGRAD = 11,/* small-M tensor-core input gradient         */
   NF4_PATH_STREAM_K = 12,    /* fused launch with the stream-K schedule     */
-  NF4_NUM_PATHS = 13
+  NF4_PATH_CLUSTER_SPLIT = 13,/* fused launch with the cluster split         */
+  NF4_NUM_PATHS = 14
 };
 
 /* A quantised weight: the tensors of the pages' QuantState as plain device
@@ -362,11 +363,28 @@ void nf4_set_small_m_path(int32_t path);
 enum { NF4_STREAM_K_OFF = 0, NF4_STREAM_K_AUTO = 1, NF4_STREAM_K_FORCE = 2 };
 void nf4_set_stream_k(int32_t mode);
 
+/* Cluster split of the fused tcgen05 kernel for the dense products (process-wide;
+ * host only): when every tile of a product, cut into S contraction slices (S = 2,
+ * 4 or 8, at least 32 tokens of the tile per slice), fits the device in one wave
+ * of thread-block clusters of S CTAs, the S slices of a tile run on the CTAs of
+ * one cluster.  Cluster rank p then finishes token slice p of the tile: every rank
+ * writes its fp32 partial of the other slices into their owners' shared memory
+ * (distributed shared memory), and the owner adds the S partials in rank order
+ * and stores bf16.  No workspace, no partials in global memory, no reduction
+ * kernel; deterministic for a given shape and device.  Needs a 16-byte aligned
+ * output and row pitch; 4-bit codes.
+ *   NF4_CLUSTER_SPLIT_OFF   never.
+ *   NF4_CLUSTER_SPLIT_AUTO  (default) where the planner's cost model prefers it.
+ *   NF4_CLUSTER_SPLIT_FORCE wherever it applies (tests). */
+enum { NF4_CLUSTER_SPLIT_OFF = 0, NF4_CLUSTER_SPLIT_AUTO = 1, NF4_CLUSTER_SPLIT_FORCE = 2 };
+void nf4_set_cluster_split(int32_t mode);
+
 /* The launch plan a dense product (NF4_OP_LINEAR_FWD / NF4_OP_LINEAR_DGRAD)
  * takes, computed on the host without a device: a deterministic function of the
  * shape, the SM count `sms`, the code width `bits` (4 or 8), the compute dtype
  * (`f16` != 0: fp16) and the process-wide launch options (nf4_set_stream_k,
- * nf4_set_small_m_path).  For diagnostics and tests; the
+ * nf4_set_small_m_path, nf4_set_cluster_split).  With a current device the
+ * cluster split also takes the device's cluster residency into account.  For diagnostics and tests; the
  * product calls compute the same plan with the current device's SM count.
  * Returns NF4_ERR_INVALID_ARG for a null `out`, an unknown op, sms < 1,
  * bits other than 4 / 8, fp16 with 8-bit codes or a non-positive dimension. */
@@ -380,6 +398,7 @@ typedef struct nf4_plan_info {
                            /* cluster; 0 for the GEMV kernels (sized at launch)         */
   int64_t items;           /* fused: work items (tiles x splits)                        */
   uint64_t workspace_bytes;/* workspace this plan needs                                */
+  int32_t cluster_split;   /* fused: CTAs of a cluster sharing each tile (splits), or 0 */
 } nf4_plan_info;
 nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t sms, int32_t bits,
                           int32_t f16, nf4_plan_info* out);

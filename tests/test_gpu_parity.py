@@ -548,6 +548,68 @@ def test_stream_k_graph_replays_between_eager_launches(restore_stream_k):
     parity(ref, oracle.linear_fwd(bf16_bits(x.cpu()), oracle.dequantize(st, "bf16")), "graph stream-K")
 
 
+@pytest.fixture
+def restore_cluster_split():
+    yield
+    ops.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 4096, 4096), (512, 1024, 4096), (129, 384, 320), (64, 4096, 1024),
+                                   (700, 640, 1024), (300, 200, 256), (256, 2048, 2048)])
+def test_cluster_split_parity_and_reruns(M, N, K, restore_cluster_split):
+    """Cluster split forced: the contraction slices of a tile run on the CTAs of one
+    cluster and the owners add the partials they receive through distributed shared
+    memory in rank order.  Both products against the oracle, bit-identical reruns."""
+    ops.set_cluster_split(_lib.CLUSTER_SPLIT_FORCE)
+    w, st, g = _quant_pair(N, K, True, seed=5 * M + N + K)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    sms = nf4.device_check()
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    c = nf4.path_counters()
+    expect = sum(ops.plan_query(op, M, N, K, sms)["cluster_split"] > 1
+                 for op in (_lib.OP_LINEAR_FWD, _lib.OP_LINEAR_DGRAD))
+    assert expect >= 1 and c["cluster_split"] == expect and c["splitk_reduce"] == 0, c
+    parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"cluster split fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"cluster split dgrad {M}x{N}x{K}")
+    for _ in range(3):
+        assert torch.equal(nf4.linear_fwd(x.to(DEV), w).view(torch.int16), y.view(torch.int16))
+        assert torch.equal(nf4.linear_dgrad(gy.to(DEV), w).view(torch.int16), gx.view(torch.int16))
+    assert nf4.device_status() == 0
+
+
+def test_cluster_split_fp16_and_identity_probe(restore_cluster_split):
+    ops.set_cluster_split(_lib.CLUSTER_SPLIT_FORCE)
+    N, K = 384, 256
+    w, st, g = _quant_pair(N, K, True, seed=71)
+    wb = oracle.dequantize(st, "bf16")
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(torch.eye(K, dtype=torch.bfloat16, device=DEV), w)
+    gx = nf4.linear_dgrad(torch.eye(N, dtype=torch.bfloat16, device=DEV), w)
+    assert nf4.path_counters()["cluster_split"] == 2
+    np.testing.assert_array_equal(bf16_bits(y), np.ascontiguousarray(wb.T))
+    np.testing.assert_array_equal(bf16_bits(gx), wb)
+    M = 200
+    x = synth.activation(M, K, g).float().half()
+    yh = nf4.linear_fwd(x.to(DEV), w)
+    parity(yh, oracle.linear_fwd(_f16_bits(x), oracle.dequantize_f16(st), dtype="f16"), "cluster split f16")
+
+
+def test_cluster_split_off_and_on_agree_within_tolerance(restore_cluster_split):
+    M, N, K = 512, 4096, 4096
+    w, st, g = _quant_pair(N, K, True, seed=72)
+    x = synth.activation(M, K, g).to(DEV)
+    ys = []
+    for mode in (_lib.CLUSTER_SPLIT_OFF, _lib.CLUSTER_SPLIT_FORCE):
+        ops.set_cluster_split(mode)
+        ys.append(nf4.linear_fwd(x, w).float())
+    rel = (torch.linalg.norm(ys[0] - ys[1]) / torch.linalg.norm(ys[0])).item()
+    assert rel < 1e-3, rel
+
+
 def test_stream_k_off_and_on_agree_within_tolerance(restore_stream_k):
     M, N, K = 1536, 1024, 1024
     w, st, g = _quant_pair(N, K, True, seed=11)

@@ -26,9 +26,11 @@ def _library():
 def _default_options():
     _lib.set_stream_k(_lib.STREAM_K_AUTO)
     _lib.set_small_m_path(_lib.SMALL_M_AUTO)
+    _lib.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
     yield
     _lib.set_stream_k(_lib.STREAM_K_AUTO)
     _lib.set_small_m_path(_lib.SMALL_M_AUTO)
+    _lib.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
 
 
 def q(op, M, N, K, sms=SMS, **kw):
@@ -37,18 +39,21 @@ def q(op, M, N, K, sms=SMS, **kw):
 
 def test_plans_of_the_measured_workloads():
     # K = N = 4096 sweep: stream-K where one wave leaves SMs idle and the cost
-    # model prefers it; whole tiles at M = 8192; a 2-way split at M = 512.
+    # model prefers it; whole tiles at M = 8192; at M = 512 a 2-way cluster split
+    # (the two halves of a tile on one cluster, no workspace).
     for M, sk in [(1536, 1), (2048, 1), (4096, 1), (8192, 0)]:
         for op in (FWD, DGRAD):
             p = q(op, M, 4096, 4096)
             assert (p["kernel"], p["token_tile"], p["stream_k"]) == ("fused", 256, sk), (M, p)
-    p = q(FWD, 512, 4096, 4096)
-    assert (p["token_tile"], p["splits"], p["stream_k"], p["grid"]) == (256, 2, 0, 128)
-    # Llama-3.1-8B set at M = 512: k/v forward split 8 ways, k/v input gradient on
-    # 128-token tiles, gate/up/down on stream-K.
-    assert q(FWD, 512, 1024, 4096)["splits"] == 8
+    for op in (FWD, DGRAD):
+        p = q(op, 512, 4096, 4096)
+        assert (p["token_tile"], p["splits"], p["cluster_split"], p["grid"], p["workspace_bytes"]) == \
+            (256, 2, 2, 128, 0), p
+    # Llama-3.1-8B set at M = 512: k/v forward as 8-way cluster splits, k/v input
+    # gradient as 2-way cluster splits, gate/up/down on stream-K.
+    assert q(FWD, 512, 1024, 4096)["cluster_split"] == 8
     p = q(DGRAD, 512, 1024, 4096)
-    assert (p["token_tile"], p["splits"], p["stream_k"]) == (128, 1, 0)
+    assert (p["token_tile"], p["cluster_split"], p["stream_k"]) == (256, 2, 0)
     for N, K in [(14336, 4096), (4096, 14336)]:
         for op in (FWD, DGRAD):
             assert q(op, 512, N, K)["stream_k"] == 1
@@ -82,7 +87,13 @@ def test_plan_invariants(bits, f16):
         wtiles = -(-ncols // 128)
         assert p["items"] == wtiles * ttiles * p["splits"]
         assert p["splits"] <= max(1, -(-contract // 64))
-        if p["stream_k"]:
+        if p["cluster_split"]:
+            cs = p["cluster_split"]
+            # one tile per cluster of cs CTAs, in one wave, no workspace
+            assert cs in (2, 4, 8) and p["splits"] == cs and bits == 4 and bt // cs >= 32
+            assert p["grid"] == p["items"] and p["grid"] % cs == 0 and p["workspace_bytes"] == 0
+            assert not p["stream_k"]
+        elif p["stream_k"]:
             assert p["splits"] == 1
             # one partial tile [4 row quarters][bt tokens][32 rows] fp32 per CTA, then
             # one 8-byte ready flag per CTA and row quarter
@@ -108,6 +119,15 @@ def test_launch_options_take_effect():
     _lib.set_small_m_path(_lib.SMALL_M_TILES)
     assert q(FWD, 4, 4096, 4096)["kernel"] == "fused"
     _lib.set_small_m_path(_lib.SMALL_M_AUTO)
+    _lib.set_cluster_split(_lib.CLUSTER_SPLIT_OFF)
+    assert all(q(op, M, N, 4096)["cluster_split"] == 0
+               for op in (FWD, DGRAD) for M in (128, 512) for N in (1024, 4096))
+    _lib.set_cluster_split(_lib.CLUSTER_SPLIT_FORCE)
+    for M, N, K in [(64, 4096, 4096), (300, 200, 256), (512, 14336, 4096)]:
+        p = q(FWD, M, N, K)
+        tiles = -(-N // 128) * -(-M // p["token_tile"])
+        assert p["cluster_split"] > 1 or tiles * 2 > SMS, (M, N, K, p)
+    _lib.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
 
 
 def test_sm_count_changes_the_schedule_not_the_contract():

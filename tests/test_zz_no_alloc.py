@@ -55,8 +55,11 @@ def test_noalloc_matches_workspace_entry_point_and_oracle_twice(M, N, K, force_t
     wb = oracle.dequantize(oracle_state(w32, True), "bf16")
     try:
         # The allocation-free call never takes the stream-K schedule (its partial
-        # tiles outgrow the array); the reference call is given the same plan.
+        # tiles outgrow the array); the reference call is given the same plan, and
+        # both skip the cluster split, whose partials never leave shared memory, so
+        # that the split partials go through the array.
         ops.set_stream_k(_lib.STREAM_K_OFF)
+        ops.set_cluster_split(_lib.CLUSTER_SPLIT_OFF)
         ops.set_small_m_path(_lib.SMALL_M_TILES if force_tiles else _lib.SMALL_M_AUTO)
         plan = ops.plan_query(_lib.OP_LINEAR_FWD, M, N, K, nf4.device_check())
         assert plan["kernel"] == "fused" and plan["splits"] > 1 and not plan["stream_k"], plan
@@ -78,6 +81,7 @@ def test_noalloc_matches_workspace_entry_point_and_oracle_twice(M, N, K, force_t
     finally:
         ops.set_small_m_path(_lib.SMALL_M_AUTO)
         ops.set_stream_k(_lib.STREAM_K_AUTO)
+        ops.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
 
 
 def test_noalloc_small_m_kernels_need_no_scratch():
@@ -99,18 +103,21 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     M, N, K = 32, 9728, 8192
     try:
         ops.set_stream_k(_lib.STREAM_K_OFF)
+        ops.set_cluster_split(_lib.CLUSTER_SPLIT_OFF)
         plan = ops.plan_query(_lib.OP_LINEAR_FWD, M, N, K, nf4.device_check())
+        g = synth.generator(5)
+        w = nf4.quantize(synth.weight(N, K, g).to(DEV), double_quant=False)
+        x = synth.activation(M, K, g).to(DEV)
+        y = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+        rc = _noalloc(x, w, y)
+        torch.cuda.synchronize()
+        ref = ops.linear_fwd(x, w)
     finally:
         ops.set_stream_k(_lib.STREAM_K_AUTO)
-    g = synth.generator(5)
-    w = nf4.quantize(synth.weight(N, K, g).to(DEV), double_quant=False)
-    x = synth.activation(M, K, g).to(DEV)
-    y = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
-    rc = _noalloc(x, w, y)
-    torch.cuda.synchronize()
+        ops.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
     if plan["workspace_bytes"] > _lib.NOALLOC_SCRATCH_BYTES:
         assert rc == 4  # NF4_ERR_WORKSPACE, nothing launched
         assert torch.count_nonzero(y) == 0
     else:
         assert rc == 0
-        parity(y, ops.linear_fwd(x, w).double().cpu().numpy(), "noalloc large")
+        parity(y, ref.double().cpu().numpy(), "noalloc large")
