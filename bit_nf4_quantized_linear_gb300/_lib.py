@@ -124,6 +124,7 @@ def lib() -> ctypes.CDLL:
             "nf4_set_small_m_path": [I32],
             "nf4_set_stream_k": [I32],
             "nf4_set_cluster_split": [I32],
+            "nf4_set_token_tile": [I32],
             "nf4_inject_stream_k_timeout": [],
             "nf4_plan_query": [I32, I64, I64, I64, I32, I32, I32, ctypes.POINTER(nf4_plan_info)],
         }
@@ -140,6 +141,7 @@ def lib() -> ctypes.CDLL:
         L.nf4_set_small_m_path.restype = None
         L.nf4_set_stream_k.restype = None
         L.nf4_set_cluster_split.restype = None
+        L.nf4_set_token_tile.restype = None
         L.nf4_inject_stream_k_timeout.restype = None
         _lib = L
         return _lib
@@ -187,6 +189,11 @@ CLUSTER_SPLIT_OFF, CLUSTER_SPLIT_AUTO, CLUSTER_SPLIT_FORCE = 0, 1, 2
 
 def set_cluster_split(mode: int):
     lib().nf4_set_cluster_split(int(mode))
+
+
+def set_token_tile(tokens: int):
+    """Fixed token tile of the fused kernel (64, 128 or 256), 0 for the planner's."""
+    lib().nf4_set_token_tile(int(tokens))
 
 
 def plan_query(op: int, M: int, N: int, K: int, sms: int, bits: int = 4, f16: bool = False) -> dict:

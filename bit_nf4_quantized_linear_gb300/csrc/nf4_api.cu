@@ -202,6 +202,9 @@ std::atomic<int> g_stream_k{NF4_STREAM_K_AUTO};
 // Cluster split of the fused kernel (nf4_set_cluster_split).
 std::atomic<int> g_cluster_split{NF4_CLUSTER_SPLIT_AUTO};
 
+// Fixed token tile of the fused kernel, 0 for the planner's choice (nf4_set_token_tile).
+std::atomic<int> g_token_tile{0};
+
 // Clusters of cs CTAs that can be resident at once: the device's answer when one is
 // current, else the SM count's bound (host-only plan queries).
 int cluster_capacity(int mode, int bt, int cs, int sms, bool query_device) {
@@ -280,7 +283,11 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     }
     return make_plan(M, ncols, contract, bt, static_cast<int>(s));
   }
-  const int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : choose_bt(M);
+  // A fixed tile (nf4_set_token_tile) is the only candidate.
+  const int fixed_bt = g_token_tile.load(std::memory_order_relaxed);
+  int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : choose_bt(M);
+  if (fixed_bt > 0) bt_max = bits == 8 && fixed_bt > 128 ? 128 : fixed_bt;
+  const int bt_min = fixed_bt > 0 ? bt_max : 0;
   const int cand_bt[3] = {256, 128, 64};
   const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
   const int skm = allow_sk ? g_stream_k.load(std::memory_order_relaxed) : NF4_STREAM_K_OFF;
@@ -289,7 +296,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
   Plan sk_best = best;
   for (int ci = 0; ci < 3; ++ci) {
     const int bt = cand_bt[ci];
-    if (bt > bt_max) continue;
+    if (bt > bt_max || bt < bt_min) continue;
     const int64_t ttiles = (M + bt - 1) / bt;
     const int64_t wt = (ncols + nf4::kTileW - 1) / nf4::kTileW;
     const int64_t units = sms;
@@ -339,7 +346,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     const int cand_cs[3] = {2, 4, 8};
     for (int ci = 0; ci < 3; ++ci) {
       const int bt = cand_bt[ci];
-      if (bt > bt_max) continue;
+      if (bt > bt_max || bt < bt_min) continue;
       const int64_t ttiles = (M + bt - 1) / bt;
       const int64_t tiles = ((ncols + nf4::kTileW - 1) / nf4::kTileW) * ttiles;
       for (int si = 0; si < 3; ++si) {
@@ -585,8 +592,11 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   DevInfo dev;
   if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
   if (!dev.supported) return NF4_ERR_UNSUPPORTED;
-  // Tokens per tile follow the mean rows per expert.
-  int bt = choose_bt((T + E - 1) / E);
+  // Tokens per tile: the tile that holds twice the mean rows per expert, so that
+  // an expert near the mean takes one token tile, not a full one and a ragged one
+  // (the steps of a tile cost about the same from 16 to 128 tokens: the weight
+  // decode bounds them).
+  int bt = choose_bt(2 * ((T + E - 1) / E));
   if (w->bits == 8 && bt > 128) bt = 128;  // 8-bit codes: tiles of <= 128 tokens
   CUtensorMap tmap_act, tmap_pk;
   if (!encode_2d(&tmap_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act, act_cols, T, ld_act * 2, 64, bt,
@@ -871,6 +881,11 @@ void nf4_set_stream_k(int32_t mode) {
 void nf4_set_cluster_split(int32_t mode) {
   if (mode >= NF4_CLUSTER_SPLIT_OFF && mode <= NF4_CLUSTER_SPLIT_FORCE)
     g_cluster_split.store(mode, std::memory_order_relaxed);
+}
+
+void nf4_set_token_tile(int32_t tokens) {
+  if (tokens == 0 || tokens == 64 || tokens == 128 || tokens == 256)
+    g_token_tile.store(tokens, std::memory_order_relaxed);
 }
 
 void nf4_inject_stream_k_timeout(void) { g_inject_sk_timeout.store(1, std::memory_order_relaxed); }

@@ -299,5 +299,6 @@ set_weight_prefetch = _lib.set_weight_prefetch
 set_small_m_path = _lib.set_small_m_path
 set_stream_k = _lib.set_stream_k
 set_cluster_split = _lib.set_cluster_split
+set_token_tile = _lib.set_token_tile
 inject_stream_k_timeout = _lib.inject_stream_k_timeout
 plan_query = _lib.plan_query

@@ -379,11 +379,17 @@ void nf4_set_stream_k(int32_t mode);
 enum { NF4_CLUSTER_SPLIT_OFF = 0, NF4_CLUSTER_SPLIT_AUTO = 1, NF4_CLUSTER_SPLIT_FORCE = 2 };
 void nf4_set_cluster_split(int32_t mode);
 
+/* Token tile of the fused tcgen05 kernel for the dense products (process-wide;
+ * host only): 0 (default) lets the planner choose; 64, 128 or 256 fixes it for
+ * every product with M > 32 that runs on the fused kernel (8-bit codes: at most
+ * 128).  For tests and measurements.  Other values are ignored. */
+void nf4_set_token_tile(int32_t tokens);
+
 /* The launch plan a dense product (NF4_OP_LINEAR_FWD / NF4_OP_LINEAR_DGRAD)
  * takes, computed on the host without a device: a deterministic function of the
  * shape, the SM count `sms`, the code width `bits` (4 or 8), the compute dtype
  * (`f16` != 0: fp16) and the process-wide launch options (nf4_set_stream_k,
- * nf4_set_small_m_path, nf4_set_cluster_split).  With a current device the
+ * nf4_set_small_m_path, nf4_set_cluster_split, nf4_set_token_tile).  With a current device the
  * cluster split also takes the device's cluster residency into account.  For diagnostics and tests; the
  * product calls compute the same plan with the current device's SM count.
  * Returns NF4_ERR_INVALID_ARG for a null `out`, an unknown op, sms < 1,

@@ -87,6 +87,29 @@ def test_dense_products_stay_inside_their_output(M, N, K, sk, small):
     parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"guarded dgrad {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("bt,M,N,K", [(64, 1100, 648, 1024), (128, 700, 136, 8192)])
+def test_fixed_token_tiles_stay_inside_their_output(bt, M, N, K):
+    g = synth.generator(M + N)
+    w32 = synth.weight(N, K, g)
+    w = nf4.quantize(w32.to(DEV), double_quant=True)
+    wb = oracle.dequantize(oracle_state(w32, True), "bf16")
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    try:
+        ops.set_token_tile(bt)
+        ybuf, y = guarded(M, N)
+        ops.linear_fwd(x.to(DEV), w, out=y)
+        gbuf, gx = guarded(M, K)
+        ops.linear_dgrad(gy.to(DEV), w, out=gx)
+        torch.cuda.synchronize()
+    finally:
+        ops.set_token_tile(0)
+    check_guard(ybuf, M, N, f"tile {bt} fwd {M}x{N}x{K}")
+    check_guard(gbuf, M, K, f"tile {bt} dgrad {M}x{N}x{K}")
+    parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"guarded tile {bt} fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"guarded tile {bt} dgrad {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("M", [3, 200])
 def test_one_byte_codes_and_fp16_stay_inside_their_output(M):
     N, K = 264, 320

@@ -905,3 +905,36 @@ def test_grouped_swiglu_bwd_entry_point(with_bias):
                                        bias=None if bias is None else bias.to(DEV),
                                        row_scale=rw.to(DEV))
     assert none is None and torch.equal(gx2.view(torch.int16)[:T], gx.view(torch.int16)[:T])
+
+
+# ------------------------------------------------------------ fixed token tile --
+# The narrower tiles on shapes whose default plan takes 256 tokens (and the
+# reverse), through nf4_set_token_tile.
+
+@pytest.fixture
+def restore_token_tile():
+    yield
+    ops.set_token_tile(0)
+
+
+@pytest.mark.parametrize("bt,M,N,K", [(64, 1100, 640, 1024), (128, 600, 384, 2048), (256, 40, 320, 192),
+                                      (64, 513, 256, 8192), (128, 2048, 4096, 4096)])
+def test_fixed_token_tile_parity_and_reruns(bt, M, N, K, restore_token_tile):
+    ops.set_token_tile(bt)
+    sms = nf4.device_check()
+    plans = [ops.plan_query(op, M, N, K, sms) for op in (_lib.OP_LINEAR_FWD, _lib.OP_LINEAR_DGRAD)]
+    assert all(p["token_tile"] == bt and p["kernel"] == "fused" for p in plans), plans
+    w, st, g = _quant_pair(N, K, True, seed=7 * M + N + K)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    rows = _sampled_rows(M, 8) if M * N * K > 2e9 else np.arange(M)
+    r = torch.from_numpy(rows).to(DEV)
+    parity(y[r], oracle.linear_fwd(bf16_bits(x), wb, rows), f"tile {bt} fwd {M}x{N}x{K}")
+    parity(gx[r], oracle.linear_dgrad(bf16_bits(gy), wb, rows), f"tile {bt} dgrad {M}x{N}x{K}")
+    for _ in range(2):
+        assert torch.equal(nf4.linear_fwd(x.to(DEV), w).view(torch.int16), y.view(torch.int16))
+        assert torch.equal(nf4.linear_dgrad(gy.to(DEV), w).view(torch.int16), gx.view(torch.int16))
+    assert nf4.device_status() == 0

@@ -39,9 +39,9 @@ def q(op, M, N, K, sms=SMS, **kw):
 
 def test_plans_of_the_measured_workloads():
     # K = N = 4096 sweep: stream-K where one wave leaves SMs idle and the cost
-    # model prefers it; whole tiles at M = 8192; at M = 512 a 2-way cluster split
-    # (the two halves of a tile on one cluster, no workspace).
-    for M, sk in [(1536, 1), (2048, 1), (4096, 1), (8192, 0)]:
+    # model prefers it; whole tiles at M = 1024 and 8192; at M = 512 a 2-way
+    # cluster split (the two halves of a tile on one cluster, no workspace).
+    for M, sk in [(1024, 0), (1536, 1), (2048, 1), (4096, 1), (8192, 0)]:
         for op in (FWD, DGRAD):
             p = q(op, M, 4096, 4096)
             assert (p["kernel"], p["token_tile"], p["stream_k"]) == ("fused", 256, sk), (M, p)
@@ -128,6 +128,34 @@ def test_launch_options_take_effect():
         tiles = -(-N // 128) * -(-M // p["token_tile"])
         assert p["cluster_split"] > 1 or tiles * 2 > SMS, (M, N, K, p)
     _lib.set_cluster_split(_lib.CLUSTER_SPLIT_AUTO)
+
+
+def test_fixed_token_tile_option():
+    # A fixed tile is the only candidate for M > 32 (one-byte codes: at most 128),
+    # on every schedule; other values are ignored; 0 restores the planner's choice.
+    try:
+        for bt in (64, 128, 256):
+            _lib.set_token_tile(bt)
+            for M, N, K in [(33, 256, 512), (700, 640, 1024), (4096, 4096, 4096)]:
+                for op in (FWD, DGRAD):
+                    p = q(op, M, N, K)
+                    assert p["token_tile"] == bt, (bt, M, p)
+                    assert p["items"] == -(-(N if op == FWD else K) // 128) * -(-M // bt) * p["splits"]
+            assert q(FWD, 700, 640, 1024, bits=8)["token_tile"] == min(bt, 128)
+            assert q(FWD, 20, 640, 1024)["token_tile"] == 32  # M <= 32 keeps its own tile
+        _lib.set_stream_k(_lib.STREAM_K_FORCE)
+        _lib.set_token_tile(128)
+        p = q(FWD, 4096, 4096, 4096)
+        assert p["stream_k"] and p["token_tile"] == 128
+        _lib.set_stream_k(_lib.STREAM_K_AUTO)
+        _lib.set_token_tile(96)  # ignored
+        assert q(FWD, 4096, 4096, 4096)["token_tile"] == 128
+        _lib.set_token_tile(512)  # ignored
+        assert q(FWD, 4096, 4096, 4096)["token_tile"] == 128
+    finally:
+        _lib.set_token_tile(0)
+        _lib.set_stream_k(_lib.STREAM_K_AUTO)
+    assert q(FWD, 4096, 4096, 4096)["token_tile"] == 256
 
 
 def test_sm_count_changes_the_schedule_not_the_contract():
