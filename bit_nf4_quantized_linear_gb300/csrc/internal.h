@@ -122,6 +122,11 @@ struct GemvArgs {
 // (forward: 16 weight rows; input gradient: 64 in-features), and CTA rank r of a
 // cluster owns the contraction slice r*cc .. (r+1)*cc - 1; the S partial sums of
 // a tile are reduced through distributed shared memory in rank order.
+// Shared-memory layout of a small-M CTA (byte offsets).
+struct SkinnyLayout {
+  int table, ring, gy, first, recv, scales, code8, bars, act, total;
+};
+
 struct SkinnyArgs {
   const __nv_bfloat16* act;  // x [M, K] (forward) or grad_y [M, N] (input gradient)
   int64_t ld_act;
@@ -143,6 +148,12 @@ struct SkinnyArgs {
   int64_t cc;     // contraction per CTA (forward: multiple of 64; input gradient: of 16)
   int prefetch;   // the weight may be read before the preceding grid has finished
   int* status;    // device status word (NF4_ERR_TIMEOUT from a bounded wait)
+  // Derived on the host by launch_skinny (no 64-bit divisions in the kernels):
+  SkinnyLayout lay;  // the CTA's shared-memory layout
+  int64_t nt_max;    // most tiles of a cluster, ceil(T / C)
+  int64_t tq;        // T / C
+  int tr;            // T % C
+  int log2S;         // S = 1 << log2S
 };
 
 constexpr int kSkinnyMaxM = 16;

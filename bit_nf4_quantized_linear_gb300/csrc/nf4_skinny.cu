@@ -101,23 +101,30 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // The byte-pair table: entry e = (code4[e >> 4], code4[e & 15]) as two fp32 (the
 // even value of a packed byte first), copy for lane l at byte offset 256 e + 8 l.
 // Written as 8 rounds of one 16-byte store per thread (16-byte unit
-// i = 512 k + thread, entry i / 16, so a warp's stores are contiguous); every
-// codebook value a thread needs is loaded up front, so the whole build costs one
-// global-memory round trip.
-__device__ __forceinline__ void build_table(uint8_t* smem, const float* code4) {
+// i = 512 k + thread, entry i / 16, so a warp's stores are contiguous).  The
+// codebook values a thread needs are loaded first (table_src), so that their round
+// trip overlaps the kernel's other first loads, and stored later (store_table).
+struct TableSrc {
+  uint32_t lo;      // low code of the thread's entries (fixed per thread)
+  uint32_t hi[8];   // high code of entry 32 k + thread / 16 in round k
+};
+
+__device__ __forceinline__ TableSrc table_src(const float* code4) {
   static_assert(kThreads == 512, "the table is 8 rounds of 512 16-byte units");
+  const int tid = static_cast<int>(threadIdx.x);
+  const int odd = (tid >> 8) & 1;  // unit 512 k + tid holds entry 32 k + tid / 16
+  TableSrc t;
+  t.lo = __float_as_uint(__ldg(code4 + ((tid >> 4) & 15)));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t.hi[k] = __float_as_uint(__ldg(code4 + 2 * k + odd));  // code 2 k + tid / 256
+  return t;
+}
+
+__device__ __forceinline__ void store_table(uint8_t* smem, const TableSrc& src) {
   uint4* t = reinterpret_cast<uint4*>(smem);
   const int tid = static_cast<int>(threadIdx.x);
-  const bool odd = ((tid >> 8) & 1) != 0;  // unit 512 k + tid holds entry 32 k + tid / 16,
-  const uint32_t lo = __float_as_uint(__ldg(code4 + ((tid >> 4) & 15)));  // whose low code is fixed
-  float c[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) c[i] = __ldg(code4 + i);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {  // high code of entry 32 k + tid / 16: 2 k + tid / 256
-    const uint32_t hi = __float_as_uint(odd ? c[2 * k + 1] : c[2 * k]);
-    t[k * kThreads + tid] = make_uint4(hi, lo, hi, lo);
-  }
+  for (int k = 0; k < 8; ++k) t[k * kThreads + tid] = make_uint4(src.hi[k], src.lo, src.hi[k], src.lo);
 }
 
 // Dequantised bf16 pair of the packed byte that `sel` picks from w:
@@ -145,21 +152,26 @@ __device__ __forceinline__ uint64_t pair2(float lo, float hi) {
 __host__ __device__ constexpr uint32_t lookup_sel(uint32_t b) { return 0x5504u | (b << 4); }
 
 // Raw statistics of one block (absmax, or 8-bit code + nested absmax), fetched
-// ahead; finished into the decoded scale when the block is used.
+// ahead; finished into the decoded scale when the block is used.  The loads are
+// unconditional (a block that does not exist reads block 0 and is marked invalid)
+// so that nothing merges their values at fetch time: the thread runs on until the
+// values are used.
 struct Raw {
   float v;
   uint32_t q;
+  bool ok;
 };
 
 __device__ __forceinline__ Raw fetch_raw(const SkinnyArgs& a, int64_t b, bool valid) {
-  Raw r{0.0f, 0u};
-  if (valid) {
-    if (!a.dq) {
-      r.v = __ldg(a.absmax + b);
-    } else {
-      r.q = __ldg(a.absmax_q + b);
-      r.v = __ldg(a.nested_absmax + (b >> 8));
-    }
+  Raw r;
+  const int64_t bi = valid ? b : 0;
+  r.ok = valid;
+  if (!a.dq) {
+    r.v = __ldg(a.absmax + bi);
+    r.q = 0u;
+  } else {
+    r.q = __ldg(a.absmax_q + bi);
+    r.v = __ldg(a.nested_absmax + (bi >> 8));
   }
   return r;
 }
@@ -190,36 +202,36 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 __device__ __forceinline__ int code_unit(int r, int h) { return 2 * r + (h ^ ((r >> 2) & 1)); }
 
 // Decoded block scales of `count` blocks into sc[0 .. count): block `block_of(idx)`
-// (-1 for none: scale 0).  The 8-bit codebook is staged in shared memory first
-// (`code8s`, 256 floats) and the statistics of four blocks per thread are
-// fetched together, so the whole decode costs about one memory round trip.
-// Called by all threads of the CTA.
+// (-1 for none: scale 0), four blocks per thread per batch (idx = i0 + j kThreads).
+// A batch's statistics are fetched together (fetch_scales), then decoded with the
+// 8-bit codebook staged in shared memory (`code8s`, 256 floats; finish_scales), so
+// the first batch can be fetched along with the kernel's other first loads.
+struct ScaleBatch {
+  Raw r[4];
+};
+
 template <typename BlockOf>
-__device__ __forceinline__ void decode_scales(const SkinnyArgs& a, float* sc, float* code8s,
-                                              int count, BlockOf block_of) {
-  if (a.dq) {
-    for (int i = threadIdx.x; i < 256; i += kThreads) code8s[i] = __ldg(a.code8 + i);
+__device__ __forceinline__ ScaleBatch fetch_scales(const SkinnyArgs& a, int i0, int count,
+                                                   BlockOf block_of) {
+  ScaleBatch s;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int idx = i0 + j * kThreads;
+    const int64_t b = idx < count ? block_of(idx) : -1;
+    s.r[j] = fetch_raw(a, b, b >= 0);
   }
-  const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
-  __syncthreads();
-  for (int i0 = threadIdx.x; i0 < count; i0 += 4 * kThreads) {
-    Raw r[4];
-    bool ok[4];
+  return s;
+}
+
+__device__ __forceinline__ void finish_scales(const SkinnyArgs& a, float* sc, const float* code8s,
+                                              float offset, int i0, int count, const ScaleBatch& s) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int idx = i0 + j * kThreads;
-      const int64_t b = idx < count ? block_of(idx) : -1;
-      ok[j] = b >= 0;
-      r[j] = fetch_raw(a, ok[j] ? b : 0, ok[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int idx = i0 + j * kThreads;
-      if (idx >= count) break;
-      float v = 0.0f;
-      if (ok[j]) v = a.dq ? __fadd_rn(__fmul_rn(code8s[r[j].q], r[j].v), offset) : r[j].v;
-      sc[idx] = v;
-    }
+  for (int j = 0; j < 4; ++j) {
+    const int idx = i0 + j * kThreads;
+    if (idx >= count) break;
+    float v = 0.0f;
+    if (s.r[j].ok) v = a.dq ? __fadd_rn(__fmul_rn(code8s[s.r[j].q], s.r[j].v), offset) : s.r[j].v;
+    sc[idx] = v;
   }
 }
 
@@ -240,25 +252,26 @@ __device__ __forceinline__ WarpRange warp_range(int w, int U, int per_tile) {
 // Element e of tile i summed over the warps of the CTA, in warp order.  Warp w
 // keeps its last tile's partial at last + w * last_stride and, when its range
 // started in the tile below its last one, that first tile's partial at
-// first + w * first_stride.  The warps touching tile i form the contiguous run
-// from the warp holding unit i * per_tile to the one holding unit
-// (i + 1) * per_tile - 1.
-__device__ __forceinline__ int warp_of_unit(int u, int U) {
-  const int w = (16 * (u + 1) + U - 1) / U - 1;  // largest w with w * U / 16 <= u
-  return w < kWarps - 1 ? w : kWarps - 1;
-}
-
+// first + w * first_stride.  The warps touching tile i are those whose unit
+// range [w U / 16, (w + 1) U / 16) meets [i per_tile, (i + 1) per_tile); all
+// sixteen candidates' loads go out before the adds (shifts and compares only, no
+// division), and the adds run in warp order.
 __device__ __forceinline__ float cta_sum(int i, int e, int U, int per_tile, const float* first,
                                          int first_stride, const float* last, int last_stride) {
   static_assert(kWarps == 16, "warp ranges use w * U / 16");
   const int a0 = i * per_tile, a1 = a0 + per_tile;
-  const int w0 = warp_of_unit(a0, U), w1 = warp_of_unit(a1 - 1, U);
-  float v = 0.0f;
-  for (int w = w0; w <= w1; ++w) {
+  float p[kWarps];
+  bool use[kWarps];
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
     const int lo = (w * U) >> 4, hi = ((w + 1) * U) >> 4;
-    if (lo >= hi) continue;
-    v = __fadd_rn(v, hi <= a1 ? last[w * last_stride + e] : first[w * first_stride + e]);
+    use[w] = lo < hi && lo < a1 && hi > a0;
+    p[w] = use[w] ? (hi <= a1 ? last[w * last_stride + e] : first[w * first_stride + e]) : 0.0f;
   }
+  float v = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w)
+    if (use[w]) v = __fadd_rn(v, p[w]);
   return v;
 }
 
@@ -266,34 +279,27 @@ __device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Cluster reduction: element e of `total` is owned by rank e * S / total...; every
-// rank stores its CTA sum of e into the owner's receive buffer, row = its rank,
-// then one cluster barrier, then the owner adds the S rows in rank order.
+// Cluster reduction: the `total` elements are cut into S chunks of
+// len = ceil(total / S); rank r owns chunk r.  Every rank stores its CTA sum of
+// element e into the owner's receive buffer (row = the sending rank), then one
+// cluster barrier, then the owner adds the S rows in rank order.
 struct ClusterShare {
   int e0, e1, len;  // this rank's elements [e0, e1); row length of the receive buffer
 };
 
 __device__ __forceinline__ ClusterShare cluster_share(int rank, int S, int total) {
   ClusterShare c;
-  c.e0 = rank * total / S;
-  c.e1 = (rank + 1) * total / S;
   c.len = (total + S - 1) / S;
+  c.e0 = rank * c.len < total ? rank * c.len : total;
+  c.e1 = c.e0 + c.len < total ? c.e0 + c.len : total;
   return c;
-}
-
-// Rank owning element e (the inverse of cluster_share's ranges).
-__device__ __forceinline__ int cluster_owner(int e, int S, int total) {
-  int r = static_cast<int>((static_cast<int64_t>(e) * S) / total);
-  while (r + 1 < S && (r + 1) * total / S <= e) ++r;
-  while (r > 0 && r * total / S > e) --r;
-  return r;
 }
 
 __device__ __forceinline__ void cluster_push(float* recv, int rank, int S, int total, int e,
                                              float v) {
-  const int owner = cluster_owner(e, S, total);
   const int len = (total + S - 1) / S;
-  const int local = e - owner * total / S;
+  const int owner = e / len;
+  const int local = e - owner * len;
   st_dsmem(mapa_shared(smem_addr(recv + rank * len + local), static_cast<uint32_t>(owner)), v);
 }
 
@@ -322,9 +328,7 @@ constexpr int kBwdCodeUnit = kBwdRows * 32;
 __host__ __device__ constexpr int bwd_gy_unit_bytes(int mt) { return mt * 8 * (kBwdRows * 2 + 16); }
 
 // Shared-memory layout of a CTA (byte offsets), common to the plan and the kernels.
-struct Layout {
-  int table, ring, gy, first, recv, scales, code8, bars, act, total;
-};
+using Layout = SkinnyLayout;
 
 __host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t cc, int64_t nt_max) {
   Layout L;
@@ -339,8 +343,8 @@ __host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t c
   const int64_t total = nt_max * slot_elems;
   const int64_t len = (total + S - 1) / S;
   L.scales = L.recv + static_cast<int>((S > 1 ? S * len * 4 : 0) + 15) / 16 * 16;
-  // forward: the per-tile warp runs (int2 per tile); input gradient: decoded scales
-  const int64_t nscales = mode == 0 ? nt_max * 2 : nt_max * cc;
+  // input gradient: the decoded block scales of the CTA's slice (forward: none)
+  const int64_t nscales = mode == 0 ? 0 : nt_max * cc;
   L.code8 = L.scales + static_cast<int>((nscales * 4 + 15) / 16 * 16);
   // Forward: one ring barrier per warp and slot here.  The input gradient keeps its
   // two per warp in the unused padding of its first grad_y row (bytes 128-143).
@@ -383,11 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int S = a.S;
-  const int rank = static_cast<int>(blockIdx.x) % S;
-  const int64_t cl = static_cast<int64_t>(blockIdx.x) / S;
-  const int64_t tile0 = cl * a.T / a.C;
-  const int nt = static_cast<int>((cl + 1) * a.T / a.C - tile0);
-  const int64_t nt_max = (a.T + a.C - 1) / a.C;
+  const int rank = static_cast<int>(blockIdx.x) & (S - 1);
+  const int cl = static_cast<int>(blockIdx.x) >> a.log2S;
+  // cl * T / C and (cl + 1) * T / C from T = tq C + tr (32-bit divisions only)
+  const int64_t tile0 = cl * a.tq + (cl * a.tr) / a.C;
+  const int nt = static_cast<int>((cl + 1) * a.tq + ((cl + 1) * a.tr) / a.C - tile0);
+  const int64_t nt_max = a.nt_max;
   const int nbs = static_cast<int>(a.cc >> 6);  // blocks per contraction slice
   const int64_t kb0 = static_cast<int64_t>(rank) * nbs;
   const int nbr = static_cast<int>(a.KB - kb0 < nbs ? a.KB - kb0 : nbs);  // >= 1 by the plan
@@ -396,12 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int U = nt * nq;
   const WarpRange mine = warp_range(warp, U, nq);
   const int nunits = mine.hi - mine.lo;
-  const Layout L = make_layout(0, MT, S, a.cc, nt_max);
+  const Layout L = a.lay;
   uint8_t* ring = smem + L.ring + warp * D * kFwdUnit;
   float* first = reinterpret_cast<float*>(smem + L.first);
   float* recv = reinterpret_cast<float*>(smem + L.recv);
   float* code8s = reinterpret_cast<float*>(smem + L.code8);
-  int2* tile_warps = reinterpret_cast<int2*>(smem + L.scales);  // [tile] first and last warp
   uint4* xs = reinterpret_cast<uint4*>(smem + L.act);           // [token][chunk][8 units]
   // The warp's ring barriers (one per slot), initialised by its lane 0.
   const uint32_t bars_s = smem_addr(smem + L.bars) + warp * D * 8;
@@ -420,22 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   struct Stats {
     Raw a, b;
   };
-  auto fetch = [&](int64_t n, int64_t kb, bool ok) -> Raw {
-    Raw r{0.0f, 256u};  // q = 256: no block, scale 0
-    if (ok) {
-      const int64_t bi = n * a.KB + kb;
-      if (!a.dq) {
-        r.v = __ldg(a.absmax + bi);
-        r.q = 0u;
-      } else {
-        r.q = __ldg(a.absmax_q + bi);
-        r.v = __ldg(a.nested_absmax + (bi >> 8));
-      }
-    }
-    return r;
-  };
+  auto fetch = [&](int64_t n, int64_t kb, bool ok) -> Raw { return fetch_raw(a, n * a.KB + kb, ok); };
   auto issue = [&]() -> Stats {
-    Stats st{Raw{0.0f, 256u}, Raw{0.0f, 256u}};
+    Stats st{Raw{0.0f, 0u, false}, Raw{0.0f, 0u, false}};
     if (issued < nunits) {
       const int slot = issued & (D - 1);
       const int64_t n16 = (tile0 + ii) * 16;
@@ -459,19 +450,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++issued;
     return st;
   };
+  // The first loads all go out together, so that the kernel start costs about one
+  // memory round trip: the first two units' tile copies and statistics, the
+  // codebook values of the byte-pair table, the 8-bit codebook entry and the nested
+  // offset (the weight side, read before the grid dependency resolves when the
+  // weight is declared frozen), then the activation slice; the table and codebook
+  // stores wait for their values after that.
   Stats s0, s1;  // statistics of the units in ring slots (q and q+1)
-  auto prologue = [&]() {
+  TableSrc tsrc;
+  float c8, offset;  // 8-bit codebook entry, nested offset (double quantisation)
+  auto weight_side = [&]() {
     s0 = issue();
     s1 = issue();
-    build_table(smem, a.code4);
-    if (a.dq)
-      for (int i = threadIdx.x; i < 256; i += kThreads) code8s[i] = __ldg(a.code8 + i);
+    tsrc = table_src(a.code4);
+    // unconditional loads from valid addresses (used only under double quantisation)
+    c8 = __ldg(a.dq ? a.code8 + (threadIdx.x & 255) : a.code4);
+    offset = __ldg(a.dq ? a.nested_offset : a.code4);
   };
 
-  if (a.prefetch) prologue();
-  grid_dependency_wait();
-  if (!a.prefetch) prologue();
-  allow_dependents();
+  // One call site for the weight side (the dependency wait goes before or after
+  // it), so that no branch merge makes the thread wait for the loaded values here.
+  if (!a.prefetch) grid_dependency_wait();
+  weight_side();
+  if (a.prefetch) grid_dependency_wait();
   {  // activation slice -> shared memory (asynchronous copies): tokens < M, zero beyond the slice
     const int units = nch * 8;  // 16-byte units per token
     const uint32_t xs_s = smem_addr(xs);
@@ -484,13 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_commit();
-    cp_async_wait<0>();
   }
-  if (static_cast<int>(threadIdx.x) < nt) {  // warps touching each tile, for the reduction
-    const int i = threadIdx.x;
-    tile_warps[i] = make_int2(warp_of_unit(i * nq, U), warp_of_unit((i + 1) * nq - 1, U));
-  }
-  const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
+  allow_dependents();
+  store_table(smem, tsrc);
+  static_assert(kThreads >= 256, "one 8-bit codebook entry per thread");
+  if (a.dq && threadIdx.x < 256) code8s[threadIdx.x] = c8;
+  cp_async_wait<0>();
   __syncthreads();
 
   const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
@@ -499,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int f = t4 | ((g & 1) << 2);  // activation swizzle of this lane's chunks
   const int sw = g & 7;               // ring swizzle of rows g and g+8
   auto scale = [&](const Raw& r) -> float {
-    if (!a.dq) return r.q == 256u ? 0.0f : r.v;
-    return r.q == 256u ? 0.0f : __fadd_rn(__fmul_rn(code8s[r.q], r.v), offset);
+    if (!a.dq) return r.ok ? r.v : 0.0f;
+    return r.ok ? __fadd_rn(__fmul_rn(code8s[r.q], r.v), offset) : 0.0f;
   };
   float acc[MT][4];
 #pragma unroll
@@ -587,14 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int e = threadIdx.x; e < total; e += kThreads) {
     const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
     if ((r >> 4) >= M) continue;
-    const int2 tw = tile_warps[i];
-    float v = 0.0f;
-    for (int w = tw.x; w <= tw.y; ++w) {  // warps in order
-      const int lo = (w * U) >> 4, hi = ((w + 1) * U) >> 4;
-      if (lo >= hi) continue;
-      v = __fadd_rn(v, hi <= (i + 1) * nq ? last[w * (D * kFwdUnit / 4) + r]
-                                          : first[w * kSlotElems + r]);
-    }
+    const float v = cta_sum(i, r, U, nq, first, kSlotElems, last, D * kFwdUnit / 4);
     if (S == 1)
       store(e, v);
     else
@@ -636,18 +629,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int S = a.S;
-  const int rank = static_cast<int>(blockIdx.x) % S;
-  const int64_t cl = static_cast<int64_t>(blockIdx.x) / S;
-  const int64_t col0 = cl * a.T / a.C;
-  const int nt = static_cast<int>((cl + 1) * a.T / a.C - col0);
-  const int64_t nt_max = (a.T + a.C - 1) / a.C;
+  const int rank = static_cast<int>(blockIdx.x) & (S - 1);
+  const int cl = static_cast<int>(blockIdx.x) >> a.log2S;
+  // cl * T / C and (cl + 1) * T / C from T = tq C + tr (32-bit divisions only)
+  const int64_t col0 = cl * a.tq + (cl * a.tr) / a.C;
+  const int nt = static_cast<int>((cl + 1) * a.tq + ((cl + 1) * a.tr) / a.C - col0);
   const int64_t nr0 = static_cast<int64_t>(rank) * a.cc;
   const int64_t nr1 = a.N - nr0 < a.cc ? a.N : nr0 + a.cc;  // this CTA's weight rows
   const int nn = static_cast<int>((nr1 - nr0 + kRows - 1) / kRows);
   const int U = nt * nn;
   const WarpRange mine = warp_range(warp, U, nn);
   const int nunits = mine.hi - mine.lo;
-  const Layout L = make_layout(1, MT, S, a.cc, nt_max);
+  const Layout L = a.lay;
   uint8_t* ring = smem + L.ring + warp * D * kUnit;
   uint8_t* gyring = smem + L.gy + warp * D * kGyUnit;
   float* first = reinterpret_cast<float*>(smem + L.first);
@@ -721,28 +714,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++issued;
     cp_async_commit();
   };
-  auto prologue = [&](bool with_gy) {
+  // The first loads all go out together, so that the kernel start costs about one
+  // memory round trip: the first units' tile copies (and their grad_y, once the
+  // grid dependency has resolved), the codebook values of the byte-pair table, the
+  // 8-bit codebook entry, the nested offset and the first batch of block
+  // statistics; the stores that need those values follow.
+  // Scales: [column][row - nr0], whole units; zero beyond the CTA's rows.
+  const int nsc = nt * ccs;
+  auto block_of = [&](int idx) -> int64_t {
+    const int i = idx / ccs, nl = idx - i * ccs;
+    const int64_t n = nr0 + nl;
+    return n < nr1 ? n * a.KB + col0 + i : -1;
+  };
+  float* code8s = reinterpret_cast<float*>(smem + L.code8);
+  TableSrc tsrc;
+  ScaleBatch sb0;
+  float c8, offset;  // 8-bit codebook entry, nested offset (double quantisation)
+  auto weight_side = [&](bool with_gy) {
     for (int j = 0; j < D; ++j) issue(with_gy);
-    build_table(smem, a.code4);
-    // scales [column][row - nr0], whole units; zero beyond the CTA's rows
-    decode_scales(a, sc, reinterpret_cast<float*>(smem + L.code8), nt * ccs,
-                  [&](int idx) -> int64_t {
-                    const int i = idx / ccs, nl = idx - i * ccs;
-                    const int64_t n = nr0 + nl;
-                    return n < nr1 ? n * a.KB + col0 + i : -1;
-                  });
+    tsrc = table_src(a.code4);
+    // unconditional loads from valid addresses (used only under double quantisation)
+    c8 = __ldg(a.dq ? a.code8 + (threadIdx.x & 255) : a.code4);
+    offset = __ldg(a.dq ? a.nested_offset : a.code4);
+    sb0 = fetch_scales(a, threadIdx.x, nsc, block_of);
   };
 
-  if (a.prefetch) prologue(false);
-  grid_dependency_wait();
-  if (!a.prefetch) {
-    prologue(true);
-  } else {  // grad_y of the prefetched units, now that it is final
-    for (int j = 0, gj = mine.lo - mine.t0 * nn; j < D && j < nunits;
-         ++j, gj = gj + 1 == nn ? 0 : gj + 1)
-      copy_gy(j, nr0 + static_cast<int64_t>(kRows) * gj, false);
+  // One call site for the weight side (the dependency wait goes before or after
+  // it), so that no branch merge makes the thread wait for the loaded values here.
+  if (!a.prefetch) grid_dependency_wait();
+  weight_side(!a.prefetch);
+  if (a.prefetch) {
+    grid_dependency_wait();
+    // grad_y of the prefetched units, now that it is final: one group per unit, in order
+    for (int j = 0, gj = mine.lo - mine.t0 * nn; j < D; ++j, gj = gj + 1 == nn ? 0 : gj + 1) {
+      if (j < nunits) copy_gy(j, nr0 + static_cast<int64_t>(kRows) * gj, true);
+      cp_async_commit();
+    }
   }
   allow_dependents();
+  store_table(smem, tsrc);
+  static_assert(kThreads >= 256, "one 8-bit codebook entry per thread");
+  if (a.dq && threadIdx.x < 256) code8s[threadIdx.x] = c8;
+  __syncthreads();  // code8s
+  finish_scales(a, sc, code8s, offset, threadIdx.x, nsc, sb0);
+  for (int i0 = threadIdx.x + 4 * kThreads; i0 < nsc; i0 += 4 * kThreads)
+    finish_scales(a, sc, code8s, offset, i0, nsc, fetch_scales(a, i0, nsc, block_of));
   __syncthreads();
 
   const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
@@ -996,9 +1012,15 @@ bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan*
   return true;
 }
 
-cudaError_t launch_skinny(int mode, const SkinnyArgs& a, const SkinnyPlan& p, const CUtensorMap& tmap,
+cudaError_t launch_skinny(int mode, const SkinnyArgs& args, const SkinnyPlan& p, const CUtensorMap& tmap,
                           cudaStream_t s) {
+  SkinnyArgs a = args;
   const bool mt1 = a.M <= 8;
+  a.nt_max = (p.T + p.C - 1) / p.C;
+  a.tq = p.T / p.C;
+  a.tr = static_cast<int>(p.T % p.C);
+  a.log2S = p.S == 1 ? 0 : p.S == 2 ? 1 : p.S == 4 ? 2 : 3;
+  a.lay = make_layout(mode, mt1 ? 1 : 2, p.S, p.cc, a.nt_max);
   if (mode == 0) return mt1 ? launch_mt<0, 1>(a, p, tmap, s) : launch_mt<0, 2>(a, p, tmap, s);
   return mt1 ? launch_mt<1, 1>(a, p, tmap, s) : launch_mt<1, 2>(a, p, tmap, s);
 }
