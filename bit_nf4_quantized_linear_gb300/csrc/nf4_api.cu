@@ -177,7 +177,8 @@ struct Plan {
 Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
   Plan p;
   p.bt = bt;
-  p.wtiles = static_cast<int>((ncols + nf4::kTileW - 1) / nf4::kTileW);
+  const int64_t tw = bt == 512 ? 2 * nf4::kTileW : nf4::kTileW;  // CTA pairs: 256-row weight tiles
+  p.wtiles = static_cast<int>((ncols + tw - 1) / tw);
   p.ttiles = static_cast<int>((M + bt - 1) / bt);
   p.ksteps = static_cast<int>((contract + nf4::kTileK - 1) / nf4::kTileK);
   p.splits = splits;
@@ -231,7 +232,10 @@ uint64_t next_sk_epoch() {
 // GB300 with the timeline probes: about 0.40 us for tiles of up to 128 tokens
 // (bound by the MMA issuer's barrier round trips), about 0.46 us for 256 tokens
 // (MMA time plus activation-ring stalls).
+// CTA pairs (512-token tiles): two MMAs of M = 256, N = 256 per step on one decoded
+// weight tile per CTA.
 double step_cycles(int bt) {
+  if (bt >= 512) return 1650.0;
   if (bt >= 256) return 950.0;
   return 830.0;
 }
@@ -283,37 +287,44 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     }
     return make_plan(M, ncols, contract, bt, static_cast<int>(s));
   }
-  // A fixed tile (nf4_set_token_tile) is the only candidate.
+  // A fixed tile (nf4_set_token_tile) is the only candidate.  512-token tiles are
+  // CTA-pair tiles (4-bit codes, from M = 1024).
   const int fixed_bt = g_token_tile.load(std::memory_order_relaxed);
-  int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : choose_bt(M);
+  int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : (bits == 4 && M >= 1024 ? 512 : choose_bt(M));
   if (fixed_bt > 0) bt_max = bits == 8 && fixed_bt > 128 ? 128 : fixed_bt;
   const int bt_min = fixed_bt > 0 ? bt_max : 0;
-  const int cand_bt[3] = {256, 128, 64};
+  const int cand_bt[4] = {512, 256, 128, 64};
   const int sp[7] = {1, 2, 3, 4, 5, 6, 8};
   const int skm = allow_sk ? g_stream_k.load(std::memory_order_relaxed) : NF4_STREAM_K_OFF;
   double best_t = 1e300, sk_t = 1e300;
   Plan best = make_plan(M, ncols, contract, bt_max, 1);
   Plan sk_best = best;
-  for (int ci = 0; ci < 3; ++ci) {
+  for (int ci = 0; ci < 4; ++ci) {
     const int bt = cand_bt[ci];
     if (bt > bt_max || bt < bt_min) continue;
+    const bool pair = bt == 512;
     const int64_t ttiles = (M + bt - 1) / bt;
-    const int64_t wt = (ncols + nf4::kTileW - 1) / nf4::kTileW;
-    const int64_t units = sms;
+    const int64_t tw = pair ? 2 * nf4::kTileW : nf4::kTileW;
+    const int64_t wt = (ncols + tw - 1) / tw;
+    // pairs: the clusters of two that can be resident at once
+    const int64_t units = pair ? cluster_capacity(mode, bt, 2, sms, query_device) : sms;
+    if (units < 1) continue;
     for (int si = 0; si < 7; ++si) {
       const int S = sp[si];
       if (S > 1 && ksteps / S < 8) break;
       const int64_t items = wt * ttiles * S;
       const int64_t waves = (items + units - 1) / units;
       const int64_t kps = (ksteps + S - 1) / S;
-      double t = static_cast<double>(waves) * (kps * step_cycles(bt) + 3000.0);
+      // per wave: the steps and the epilogue (pairs: one accumulator, so the next
+      // tile's MMAs wait for it)
+      double t = static_cast<double>(waves) * (kps * step_cycles(bt) + (pair ? 6000.0 : 3000.0));
       if (S > 1) t += static_cast<double>(S) * M * ncols * 8.0 / 3500.0;  // write + read partials
       if (t < best_t * 0.999) {
         best_t = t;
         best = make_plan(M, ncols, contract, bt, S);
       }
     }
-    if (skm != NF4_STREAM_K_OFF && sms <= nf4::kSkMaxCtas) {
+    if (skm != NF4_STREAM_K_OFF && sms <= nf4::kSkMaxCtas && !pair) {
       // Stream-K: equal runs of the items' contraction steps, one per CTA (each at
       // least one step), whose steps measured about 2% slower than those of whole
       // tiles, plus a fixed cost for the split tiles' partials (the CTA finishing a
@@ -344,9 +355,9 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
   double cs_t = 1e300;
   if (csm != NF4_CLUSTER_SPLIT_OFF) {
     const int cand_cs[3] = {2, 4, 8};
-    for (int ci = 0; ci < 3; ++ci) {
+    for (int ci = 0; ci < 4; ++ci) {
       const int bt = cand_bt[ci];
-      if (bt > bt_max || bt < bt_min) continue;
+      if (bt > bt_max || bt < bt_min || bt > 256) continue;
       const int64_t ttiles = (M + bt - 1) / bt;
       const int64_t tiles = ((ncols + nf4::kTileW - 1) / nf4::kTileW) * ttiles;
       for (int si = 0; si < 3; ++si) {
@@ -478,8 +489,9 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
 
   CUtensorMap tmap_act, tmap_pk;
   const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // (CTA pairs: each CTA copies 128-token quarters of the 512-token tile)
   if (!encode_2d(&tmap_act, dt16, act, act_cols, M, ld_act * 2, 64,
-                 p.bt, CU_TENSOR_MAP_SWIZZLE_128B))
+                 p.bt == 512 ? 128 : p.bt, CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   if (!encode_codes(&tmap_pk, w, mode)) return NF4_ERR_CUDA;
   nf4::GemmArgs a{};
@@ -511,6 +523,10 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   a.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
   const int64_t units = dev.sms;
   int grid = static_cast<int>(p.items < units ? p.items : units);
+  if (p.bt == 512) {  // CTA pairs: two CTAs per item, as many pairs as can be resident
+    const int64_t pairs = cluster_capacity(mode, 512, 2, dev.sms, true);
+    grid = 2 * static_cast<int>(p.items < pairs ? p.items : pairs);
+  }
   if (p.cs > 1) {
     a.cs = p.cs;  // items = tiles x cs, one per CTA, the clusters in one wave
     grid = static_cast<int>(p.items);
@@ -884,7 +900,7 @@ void nf4_set_cluster_split(int32_t mode) {
 }
 
 void nf4_set_token_tile(int32_t tokens) {
-  if (tokens == 0 || tokens == 64 || tokens == 128 || tokens == 256)
+  if (tokens == 0 || tokens == 64 || tokens == 128 || tokens == 256 || tokens == 512)
     g_token_tile.store(tokens, std::memory_order_relaxed);
 }
 
@@ -907,6 +923,10 @@ nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t s
   } else if (!p.gemv) {
     const int64_t units = sms;
     r.grid = p.stream_k ? p.sk_ctas : static_cast<int32_t>(p.items < units ? p.items : units);
+    if (p.bt == 512) {  // CTA pairs: two CTAs per item
+      const int64_t pairs = cluster_capacity(op == NF4_OP_LINEAR_FWD ? 0 : 1, 512, 2, sms, true);
+      r.grid = 2 * static_cast<int32_t>(p.items < pairs ? p.items : pairs);
+    }
   }
   r.items = p.items;
   r.workspace_bytes = p.ws_bytes;

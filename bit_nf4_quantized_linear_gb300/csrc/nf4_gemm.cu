@@ -79,16 +79,30 @@ constexpr uint32_t kSleepHintNs = 20000;         // a waiting thread sleeps up t
 // BITS = 8: one code per byte (256-level codebook in shared memory after the base
 // misc region, one copy per lane: entry e of lane l in word 32 e + l, so the
 // lookups of a warp never share a bank).
+//
+// BT = 512 is the CTA-pair tile: the two CTAs of a cluster share each MMA of
+// M = 256 weight rows (each decodes its own 128 rows) and N = 256 tokens (each
+// holds 128 of them), two such MMAs per step for the tile's two 256-token halves,
+// into one 512-column accumulator per CTA.  A decoded weight tile then serves 512
+// tokens, and each CTA's activation stage is 256 token rows (two 128-row copies).
 template <int BT, int BITS>
 struct Geo {
+  static constexpr bool kPair = BT == 512;
   static constexpr int kPkStage = kTileW * kTileK * BITS / 8;  // codes of one step: 4 or 8 KB
   static constexpr int kMiscBytes = kMiscBase + (BITS == 8 ? 256 * 32 * 4 : 0);
-  static constexpr int kXStage = BT * 128;  // BT token rows of 64 bf16
+  static constexpr int kXRows = kPair ? BT / 2 : BT;  // token rows of a step's activation tile here
+  static constexpr int kXStage = kXRows * 128;        // of 64 bf16 each
+  static constexpr int kXParts = kPair ? 2 : 1;       // bulk tensor copies per stage
+  static constexpr int kXPartRows = kXRows / kXParts;
+  static constexpr int kMmaN = kPair ? 256 : BT;      // tokens per MMA
+  static constexpr int kAccCols = kPair ? 512 : BT;   // accumulator columns of a tile
+  static constexpr int kAccBufs = kPair ? 1 : 2;      // accumulators in tensor memory
   static constexpr int kBudget = 225 * 1024 - kMiscBytes - 1024;
-  // Decoded operand tiles: one slot more than decoder groups where the activation
-  // tiles leave room, so a group never waits on the MMAs of the step just before.
-  static constexpr int kStagesA = BT >= 256 ? kDecGroups : kDecGroups + 1;
-  static constexpr int kStagesP = (BT <= 64 ? 16 : 8) / (BITS / 4);  // code tiles, prefetched far ahead
+  // Decoded operand tiles: one slot more than decoder groups, so a group never
+  // waits on the MMAs of the step just before -- except at 256 tokens, where the
+  // activation tiles take the room (pairs make room with a shallower code ring).
+  static constexpr int kStagesA = BT == 256 ? kDecGroups : kDecGroups + 1;
+  static constexpr int kStagesP = (BT <= 64 ? 16 : (kPair ? 4 : 8)) / (BITS / 4);  // code tiles, prefetched far ahead
   static constexpr int kStagesX0 =
       (kBudget - kStagesA * kAStage - kStagesP * kPkStage - kOutBytes) / kXStage;
   static constexpr int kStagesX = kStagesX0 > 8 ? 8 : kStagesX0;  // activation tiles
@@ -98,7 +112,9 @@ struct Geo {
   static constexpr int kOffOut = kOffPk + kStagesP * kPkStage;  // output staging
   static constexpr int kOffMisc = kOffOut + kOutBytes;
   static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;
-  static constexpr uint32_t kTmemCols = (2 * BT < 32) ? 32u : static_cast<uint32_t>(2 * BT);
+  static constexpr uint32_t kTmemCols =
+      (kAccBufs * kAccCols < 32) ? 32u : static_cast<uint32_t>(kAccBufs * kAccCols);
+  static_assert(kTmemCols <= 512, "tensor memory columns");
   static_assert(kStagesX >= 3, "pipeline too shallow");
   static_assert(kStagesA <= 8 && kStagesP <= 16 && kStagesX <= 8, "barrier slots");
   // A decoded slot waits on the "stage done" ring for the step kStagesA back; that
@@ -108,6 +124,7 @@ struct Geo {
                 "a decoder group advances every ring by kDecGroups slots per step");
   static_assert(kXStage % 1024 == 0, "activation stage must keep 1024-byte alignment");
   static_assert(BITS == 4 || (BITS == 8 && BT <= 128), "8-bit codes: tiles of <= 128 tokens");
+  static_assert(kXPartRows <= 256, "a bulk tensor copy box is at most 256 rows");
 };
 
 // Barrier slots in the misc region.  Three rings advance one stage per
@@ -152,6 +169,7 @@ struct Shared {
   int* starts;
   int* ends;
   int* pref;
+  uint32_t rank;  // CTA pairs: rank in the cluster (0 otherwise)
 };
 
 __device__ __forceinline__ uint32_t bar_at(const Shared& sh, int i) { return sh.bars + 8u * i; }
@@ -212,19 +230,27 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 
 // Bounded wait on a phase completed by arrivals of other CTAs of the cluster
 // (acquire at cluster scope); as wait_phase otherwise.
-__device__ __noinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Shared& sh,
-                                                const GemmArgs& a) {
-  if (mbar_test_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+__device__ __noinline__ bool wait_phase_cluster_slow(uint32_t bar, uint32_t parity, const Shared& sh,
+                                                     const GemmArgs& a) {
+  uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait_sleep_cluster(bar, parity, kSleepHintNs)) return true;
     if (*sh.abort_flag) return false;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
+    const uint64_t now = globaltimer_ns();
+    if (!*dep_done(sh)) {
+      t0 = now;
+    } else if (now - t0 > kTimeoutNs) {
       *sh.abort_flag = 1;
       record_error(a, kStatusTimeout);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, const Shared& sh,
+                                                   const GemmArgs& a) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  return wait_phase_cluster_slow(bar, parity, sh, a);
 }
 
 // Wait used while draining on exit: bounded, ignores the abort flag.
@@ -280,7 +306,9 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
     it.ks0 = static_cast<int>((s * a.ksteps) / a.splits);
     it.ks1 = static_cast<int>(((s + 1) * a.ksteps) / a.splits);
     it.split = static_cast<int>(s);
-    it.col0 = wt * kTileW;
+    // CTA pairs: a weight tile is 256 rows (or in-features), of which this CTA
+    // holds the 128 of its rank.
+    it.col0 = BT == 512 ? wt * 2 * kTileW + kTileW * static_cast<int64_t>(sh.rank) : wt * kTileW;
     it.wrow0 = (MODE == 0) ? it.col0 : 0;
   } else {
     const int64_t g = idx / a.wtiles;
@@ -408,8 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = raw_addr + pad;
 
   Shared sh;
-  const int64_t unit = blockIdx.x;  // work items are per CTA
-  const int64_t nunits = gridDim.x;
+  constexpr bool kPair = G::kPair;
+  sh.rank = kPair ? cluster_ctarank() : 0u;
+  // Work items are per CTA, or per CTA pair (both CTAs of a cluster walk the same
+  // items).
+  const int64_t unit = kPair ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t nunits = kPair ? gridDim.x / 2 : gridDim.x;
   sh.code4 = reinterpret_cast<float*>(smem + G::kOffMisc);
   sh.code8 = sh.code4 + 16;
   uint64_t* bars_ptr = reinterpret_cast<uint64_t*>(sh.code8 + 256);
@@ -443,12 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_at(sh, kBarXFull + i), 1);
       mbar_init(bar_at(sh, kBarXEmpty + i), 1);
     }
-    for (int i = 0; i < G::kStagesA; ++i) {
-      mbar_init(bar_at(sh, kBarAFull + i), 4);  // the four decoder warps of the step's group
-    }
+    // Pairs: the leader's full / accumulator-empty barriers also count the peer's
+    // four decoder / epilogue warps (remote arrivals); the leader's MMA commits
+    // arrive on the empty and accumulator-full barriers of both CTAs.
+    for (int i = 0; i < G::kStagesA; ++i)
+      mbar_init(bar_at(sh, kBarAFull + i), kPair ? 8 : 4);  // the decoder warps of the step's group
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_at(sh, kBarAccFull + i), 1);
-      mbar_init(bar_at(sh, kBarAccEmpty + i), kNumEpiWarps);
+      mbar_init(bar_at(sh, kBarAccEmpty + i), kPair ? 2 * kNumEpiWarps : kNumEpiWarps);
     }
     mbar_init(bar_at(sh, kBarDrain), 1);
     for (int i = 0; i < 2; ++i) {
@@ -466,8 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
   if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
   if (warp == kWarpMma) {
-    tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_addr(sh.tmem_slot), G::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(sh.tmem_slot), G::kTmemCols);
+      tmem_relinquish();
+    }
     tc_fence_before();
   }
   if (!early) grid_dependency_wait();
@@ -493,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad) record_error(a, kStatusBadOffsets);
   }
   __syncthreads();
-  if (a.cs > 1) cluster_sync();  // every rank's barriers exist before any remote arrival
+  if (a.cs > 1 || kPair) cluster_sync();  // every rank's barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *sh.tmem_slot;
   const int64_t total_items =
@@ -522,10 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_phase(bar_at(sh, bar_empty + st), ph ^ 1u, sh, a)) { ok = false; break; }
           const uint32_t full = bar_at(sh, bar_full + st);
           mbar_arrive_expect_tx(full, bytes);
-          if (!is_pk)
-            tma_load_2d(sbase + G::kOffX + st * G::kXStage, &tmap_act, full, ks * kTileK,
-                        static_cast<int32_t>(it.tok0));
-          else if (MODE == 0)
+          if (!is_pk) {
+            // Pairs: this CTA's 128 tokens of each 256-token half of the tile.
+#pragma unroll
+            for (int h = 0; h < G::kXParts; ++h)
+              tma_load_2d(sbase + G::kOffX + st * G::kXStage + h * (G::kXStage / G::kXParts), &tmap_act,
+                          full, ks * kTileK,
+                          static_cast<int32_t>(it.tok0 + (kPair ? 256 * h + 128 * static_cast<int>(sh.rank) : 0)));
+          } else if (MODE == 0)
             tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK * BITS / 8),
                         static_cast<int32_t>(it.wrow0));
           else
@@ -543,28 +586,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      constexpr uint32_t idesc = F16 ? idesc_f16_f32(kTileW, BT, MODE == 1, false)
-                                     : idesc_bf16_f32(kTileW, BT, MODE == 1, false);
+    // Pairs: rank 0 issues the pair's MMAs (M = 256) and commits them to the
+    // barriers of both CTAs; rank 1's issuer warp has nothing to do.
+    if (lane == 0 && sh.rank == 0) {
+      constexpr int kMmaM = kPair ? 2 * kTileW : kTileW;
+      constexpr uint32_t idesc = F16 ? idesc_f16_f32(kMmaM, G::kMmaN, MODE == 1, false)
+                                     : idesc_bf16_f32(kMmaM, G::kMmaN, MODE == 1, false);
       // Constant fields of the operand descriptors (address field zero).
       const uint64_t a_desc_hi = (MODE == 0) ? smem_desc_sw128(0, 16, 1024) : smem_desc_sw128(0, 8192, 1024);
       const uint64_t b_desc_hi = smem_desc_sw128(0, 16, 1024);
+      // A commit that frees a slot: the barrier in this CTA, or in both CTAs of a pair.
+      auto commit_both = [&](int bar) {
+        if (kPair) {
+          mma_commit_pair(mapa_shared(bar_at(sh, bar), 0u));
+          mma_commit_pair(mapa_shared(bar_at(sh, bar), 1u));
+        } else {
+          mma_commit(bar_at(sh, bar));
+        }
+      };
+      // Waits on barriers that remote arrivals complete (pairs) acquire at cluster scope.
+      auto wait_in = [&](int bar, uint32_t parity) {
+        return kPair ? wait_phase_cluster(bar_at(sh, bar), parity, sh, a) : wait_phase(bar_at(sh, bar), parity, sh, a);
+      };
       uint32_t sx = 0, phx = 0, sa = 0, pha = 0;
       int acc_i = 0;
       bool ok = true;
       Cursor cur = cursor_begin(a, unit, total_items);
       Item it;
       for (; ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it); ++acc_i) {
-        const int ab = acc_i & 1;
-        const uint32_t acc_ph = (acc_i >> 1) & 1;
-        if (!wait_phase(bar_at(sh, kBarAccEmpty + ab), acc_ph ^ 1u, sh, a)) break;
+        const int ab = acc_i % G::kAccBufs;
+        const uint32_t acc_ph = (acc_i / G::kAccBufs) & 1;
+        if (!wait_in(kBarAccEmpty + ab, acc_ph ^ 1u)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * BT);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * G::kAccCols);
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           // The decoders signal a stage only after its activation tile landed, so
           // one wait per step covers both operands (every barrier operation of this
           // thread is serialised with its MMA issue).
-          if (!wait_phase(bar_at(sh, kBarAFull + sa), pha, sh, a)) { ok = false; break; }
+          if (!wait_in(kBarAFull + sa, pha)) { ok = false; break; }
           tc_fence_after();
           // Descriptors differ only in the start-address field (bits 0-13, address >> 4).
           // Only the CTA-local offset goes there: in a cluster launch the shared
@@ -572,23 +631,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           // otherwise spill into the leading-byte-offset field (used by the
           // MN-major operand of the input gradient).
           const uint64_t adesc0 = a_desc_hi | (((sbase + G::kOffA + sa * kAStage) & 0x3FFFFu) >> 4);
-          const uint64_t bdesc0 = b_desc_hi | (((sbase + G::kOffX + sx * G::kXStage) & 0x3FFFFu) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
-            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(kk * 32 >> 4);
-            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (ks > it.ks0 || kk > 0) ? 1u : 0u);
+          for (int h = 0; h < G::kXParts; ++h) {  // pairs: the tile's two 256-token halves
+            const uint32_t xoff = G::kOffX + sx * G::kXStage + h * (G::kXStage / G::kXParts);
+            const uint64_t bdesc0 = b_desc_hi | (((sbase + xoff) & 0x3FFFFu) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              const uint64_t adesc = adesc0 + static_cast<uint64_t>(kk * (MODE == 0 ? 32 : 2048) >> 4);
+              const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(kk * 32 >> 4);
+              const uint32_t acc = (ks > it.ks0 || kk > 0) ? 1u : 0u;
+              if (kPair)
+                mma_bf16_ss_pair(d_tmem + static_cast<uint32_t>(h * G::kMmaN), adesc, bdesc, idesc, acc);
+              else
+                mma_bf16_ss(d_tmem, adesc, bdesc, idesc, acc);
+            }
           }
           // one "stage done" ring frees the activation and decoded slots
-          mma_commit(bar_at(sh, kBarXEmpty + sx));
+          commit_both(kBarXEmpty + sx);
           if (++sa == G::kStagesA) { sa = 0; pha ^= 1u; }
           if (++sx == G::kStagesX) { sx = 0; phx ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(bar_at(sh, kBarAccFull + ab));
+        commit_both(kBarAccFull + ab);
       }
       // All MMAs issued must be complete before tensor memory is released.
-      mma_commit(bar_at(sh, kBarDrain));
+      if (kPair)
+        mma_commit_pair(mapa_shared(bar_at(sh, kBarDrain), 0u));
+      else
+        mma_commit(bar_at(sh, kBarDrain));
       drain_phase(bar_at(sh, kBarDrain), 0, a);
     }
     __syncwarp();
@@ -603,9 +673,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor cur = cursor_begin(a, unit, total_items);
     Item it;
     for (; ep_ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it); ++acc_i) {
-      const int ab = acc_i & 1;
-      const uint32_t acc_ph = (acc_i >> 1) & 1;
-      if (!wait_phase(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)) break;
+      const int ab = acc_i % G::kAccBufs;
+      const uint32_t acc_ph = (acc_i / G::kAccBufs) & 1;
+      if (kPair ? !wait_phase_cluster(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)
+                : !wait_phase(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a))
+        break;
       tc_fence_after();
       const int64_t col = it.col0 + row;
       const bool col_ok = col < a.ncols;
@@ -636,10 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // chunk; further CTAs' partials (tiles cut three or more ways) are read from
       // global memory.  The sum order is the same either way.
       const float* p_first = nullptr;  // partial of CTA unit - 1 in shared memory
-      if (sk_own && own_first < unit &&
+      // (Stream-K does not run on CTA pairs, whose 512-token partials would not fit.)
+      constexpr bool kPartFits = G::kStagesX * G::kXStage >= kNumEpiWarps * BT * 128;
+      static_assert(kPartFits || kPair, "stream-K partials of the four row quarters fit in the activation ring");
+      if (kPartFits && sk_own && own_first < unit &&
           (reinterpret_cast<uintptr_t>(a.sk_ws) & 15u) == 0) {
-        static_assert(G::kStagesX * G::kXStage >= kNumEpiWarps * BT * 128,
-                      "stream-K partials of the four row quarters fit in the activation ring");
         float* land = reinterpret_cast<float*>(smem + G::kOffX) + q * (BT * 32);
         const uint32_t bar = bar_at(sh, kBarSkPart + q);
         if (lane == 0) {
@@ -656,7 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto part_src = [&](int64_t c, int c0) -> const float* {
         return (c == unit - 1 && p_first) ? p_first + c0 * 32 : sk_slot(c) + c0 * 32;
       };
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * BT);
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab * G::kAccCols);
       // Tensor-memory loads are issued kWide columns (tokens) at a time with one wait:
       // the load latency, not the stores, bounds a narrow batch.
       constexpr int kBatch = 16;
@@ -948,7 +1022,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
+      if (lane == 0) {  // pairs: on the leader's barrier
+        if (kPair && sh.rank != 0)
+          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAccEmpty + ab), 0u));
+        else
+          mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
+      }
     }
     if (lane == 0) bulk_wait_all();  // output tiles written before the CTA exits
     __syncwarp();
@@ -1066,8 +1145,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) wc[c] = *reinterpret_cast<const uint4*>(pk + pkc[c]);
       }
-      if (m >= 0) {
-        if (!wait_phase(bar_at(sh, kBarXEmpty + ms), mph, sh, a)) break;
+      if (m >= 0) {  // pairs: the leader's commit arrives from the other CTA
+        if (kPair ? !wait_phase_cluster(bar_at(sh, kBarXEmpty + ms), mph, sh, a)
+                  : !wait_phase(bar_at(sh, kBarXEmpty + ms), mph, sh, a))
+          break;
       }
       uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
       if (BITS == 4) {
@@ -1105,7 +1186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar_at(sh, kBarPEmpty + sp));  // the codes were consumed above
-        mbar_arrive(bar_at(sh, kBarAFull + sa));
+        if (kPair && sh.rank != 0)  // pairs: the leader issues the MMAs
+          mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarAFull + sa), 0u));
+        else
+          mbar_arrive(bar_at(sh, kBarAFull + sa));
       }
       sp += kDecGroups;
       if (sp >= static_cast<uint32_t>(G::kStagesP)) { sp -= G::kStagesP; php ^= 1u; }
@@ -1127,10 +1211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // A cluster leaves together: no rank exits while another may still write into its
   // shared memory or arrive on its barriers.
-  if (a.cs > 1) cluster_sync();
+  if (a.cs > 1 || kPair) cluster_sync();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, G::kTmemCols);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, G::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, G::kTmemCols);
   }
 }
 
@@ -1245,12 +1332,14 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;  // cluster split: one tile per cluster
-  attr[1].val.clusterDim.x = a.cs > 1 ? static_cast<unsigned>(a.cs) : 1u;
+  // Clusters: a cluster split (one tile per cluster of cs CTAs) or a CTA pair.
+  const unsigned cluster = Geo<BT, BITS>::kPair ? 2u : (a.cs > 1 ? static_cast<unsigned>(a.cs) : 1u);
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = a.cs > 1 ? 2 : 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, ta, tp, to, a);
 }
 
@@ -1264,6 +1353,7 @@ cudaError_t launch_mode(int bt, const GemmArgs& a, const CUtensorMap& ta, const 
     case 64: return launch_one<MODE, 64, 4, false>(a, ta, tp, to, grid, s);
     case 128: return launch_one<MODE, 128, 4, false>(a, ta, tp, to, grid, s);
     case 256: return launch_one<MODE, 256, 4, false>(a, ta, tp, to, grid, s);
+    case 512: return launch_one<MODE, 512, 4, false>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #elif NF4_GEMM_F16
@@ -1273,6 +1363,7 @@ cudaError_t launch_mode(int bt, const GemmArgs& a, const CUtensorMap& ta, const 
     case 64: return launch_one<MODE, 64, 4, true>(a, ta, tp, to, grid, s);
     case 128: return launch_one<MODE, 128, 4, true>(a, ta, tp, to, grid, s);
     case 256: return launch_one<MODE, 256, 4, true>(a, ta, tp, to, grid, s);
+    case 512: return launch_one<MODE, 512, 4, true>(a, ta, tp, to, grid, s);
     default: return cudaErrorInvalidValue;
   }
 #else
@@ -1369,6 +1460,7 @@ int gemm_cluster_capacity(int mode, int bt, int cs) {
     case 64: n = mode == 0 ? cluster_capacity_bt<0, 64>(cs) : cluster_capacity_bt<1, 64>(cs); break;
     case 128: n = mode == 0 ? cluster_capacity_bt<0, 128>(cs) : cluster_capacity_bt<1, 128>(cs); break;
     case 256: n = mode == 0 ? cluster_capacity_bt<0, 256>(cs) : cluster_capacity_bt<1, 256>(cs); break;
+    case 512: n = mode == 0 ? cluster_capacity_bt<0, 512>(cs) : cluster_capacity_bt<1, 512>(cs); break;
     default: n = 0;
   }
   if (used < 64) cache[used++] = Entry{dev, mode, bt, cs, n};

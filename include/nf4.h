@@ -380,9 +380,14 @@ enum { NF4_CLUSTER_SPLIT_OFF = 0, NF4_CLUSTER_SPLIT_AUTO = 1, NF4_CLUSTER_SPLIT_
 void nf4_set_cluster_split(int32_t mode);
 
 /* Token tile of the fused tcgen05 kernel for the dense products (process-wide;
- * host only): 0 (default) lets the planner choose; 64, 128 or 256 fixes it for
- * every product with M > 32 that runs on the fused kernel (8-bit codes: at most
- * 128).  For tests and measurements.  Other values are ignored. */
+ * host only): 0 (default) lets the planner choose; 64, 128, 256 or 512 fixes it
+ * for every product with M > 32 that runs on the fused kernel (8-bit codes: at
+ * most 128).  512 is the CTA-pair tile: the two CTAs of a thread-block cluster
+ * share each 256-row MMA (cta_group::2), each decoding its 128 weight rows and
+ * holding 128 tokens of each 256-token half, two MMAs per contraction step into
+ * a 512-column accumulator per CTA (classic schedule only; the planner takes it
+ * from M = 1024 where its cost model prefers it).  For tests and measurements.
+ * Other values are ignored. */
 void nf4_set_token_tile(int32_t tokens);
 
 /* The launch plan a dense product (NF4_OP_LINEAR_FWD / NF4_OP_LINEAR_DGRAD)
@@ -397,7 +402,7 @@ void nf4_set_token_tile(int32_t tokens);
 enum { NF4_PLAN_FUSED = 0, NF4_PLAN_SMALL_M_MMA = 1, NF4_PLAN_SIMT_GEMV = 2 };
 typedef struct nf4_plan_info {
   int32_t kernel;          /* NF4_PLAN_*: tcgen05 tiles, warp-MMA small-M, SIMT GEMV   */
-  int32_t token_tile;      /* fused: tokens per tile (16 .. 256)                        */
+  int32_t token_tile;      /* fused: tokens per tile (16 .. 256; 512: CTA-pair tile)    */
   int32_t splits;          /* fused classic: contraction splits (1 = none)              */
   int32_t stream_k;        /* fused: 1 for the stream-K schedule                        */
   int32_t grid;            /* fused: CTAs launched; small-M MMA: clusters x CTAs per    */

@@ -87,7 +87,8 @@ def test_dense_products_stay_inside_their_output(M, N, K, sk, small):
     parity(gx, oracle.linear_dgrad(bf16_bits(gy), wb), f"guarded dgrad {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("bt,M,N,K", [(64, 1100, 648, 1024), (128, 700, 136, 8192)])
+@pytest.mark.parametrize("bt,M,N,K", [(64, 1100, 648, 1024), (128, 700, 136, 8192),
+                                      (512, 1100, 648, 1024), (512, 700, 136, 8192)])
 def test_fixed_token_tiles_stay_inside_their_output(bt, M, N, K):
     g = synth.generator(M + N)
     w32 = synth.weight(N, K, g)

@@ -909,7 +909,8 @@ def test_grouped_swiglu_bwd_entry_point(with_bias):
 
 # ------------------------------------------------------------ fixed token tile --
 # The narrower tiles on shapes whose default plan takes 256 tokens (and the
-# reverse), through nf4_set_token_tile.
+# reverse), and the CTA-pair tile (512 tokens x 256 weight rows on two CTAs, with
+# ragged token and column tails and classic splits), through nf4_set_token_tile.
 
 @pytest.fixture
 def restore_token_tile():
@@ -918,7 +919,9 @@ def restore_token_tile():
 
 
 @pytest.mark.parametrize("bt,M,N,K", [(64, 1100, 640, 1024), (128, 600, 384, 2048), (256, 40, 320, 192),
-                                      (64, 513, 256, 8192), (128, 2048, 4096, 4096)])
+                                      (64, 513, 256, 8192), (128, 2048, 4096, 4096),
+                                      (512, 1100, 640, 1024), (512, 600, 384, 2048), (512, 513, 256, 8192),
+                                      (512, 1536, 4096, 4096), (512, 40, 320, 192)])
 def test_fixed_token_tile_parity_and_reruns(bt, M, N, K, restore_token_tile):
     ops.set_token_tile(bt)
     sms = nf4.device_check()
@@ -937,4 +940,27 @@ def test_fixed_token_tile_parity_and_reruns(bt, M, N, K, restore_token_tile):
     for _ in range(2):
         assert torch.equal(nf4.linear_fwd(x.to(DEV), w).view(torch.int16), y.view(torch.int16))
         assert torch.equal(nf4.linear_dgrad(gy.to(DEV), w).view(torch.int16), gx.view(torch.int16))
+    assert nf4.device_status() == 0
+
+
+def test_pair_tiles_identity_probe_and_f16(restore_token_tile):
+    # One-hot activations select dequantised weights exactly on CTA-pair tiles
+    # (both token halves and both CTAs' rows of every tile); the fp16 dtype on the
+    # same tiles within tolerance.
+    ops.set_token_tile(512)
+    N, K = 384, 1024
+    w, st, g = _quant_pair(N, K, True, seed=81)
+    wb = oracle.dequantize(st, "bf16")
+    y = nf4.linear_fwd(torch.eye(K, dtype=torch.bfloat16, device=DEV), w)
+    gx = nf4.linear_dgrad(torch.eye(N, dtype=torch.bfloat16, device=DEV), w)
+    np.testing.assert_array_equal(bf16_bits(y), np.ascontiguousarray(wb.T))
+    np.testing.assert_array_equal(bf16_bits(gx), wb)
+    M = 700
+    x = synth.activation(M, K, g).float().half()
+    gy = synth.activation(M, N, g).float().half()
+    yh = nf4.linear_fwd(x.to(DEV), w)
+    gxh = nf4.linear_dgrad(gy.to(DEV), w)
+    wh = oracle.dequantize_f16(st)
+    parity(yh, oracle.linear_fwd(_f16_bits(x), wh, dtype="f16"), "pair f16 fwd")
+    parity(gxh, oracle.linear_dgrad(_f16_bits(gy), wh, dtype="f16"), "pair f16 dgrad")
     assert nf4.device_status() == 0

@@ -38,13 +38,13 @@ def q(op, M, N, K, sms=SMS, **kw):
 
 
 def test_plans_of_the_measured_workloads():
-    # K = N = 4096 sweep: stream-K where one wave leaves SMs idle and the cost
-    # model prefers it; whole tiles at M = 1024 and 8192; at M = 512 a 2-way
+    # K = N = 4096 sweep: CTA-pair tiles (512 tokens x 256 rows on two CTAs) from
+    # M = 2048, stream-K at 1536, whole 256-token tiles at 1024; at M = 512 a 2-way
     # cluster split (the two halves of a tile on one cluster, no workspace).
-    for M, sk in [(1024, 0), (1536, 1), (2048, 1), (4096, 1), (8192, 0)]:
+    for M, bt, sk in [(1024, 256, 0), (1536, 256, 1), (2048, 512, 0), (4096, 512, 0), (8192, 512, 0)]:
         for op in (FWD, DGRAD):
             p = q(op, M, 4096, 4096)
-            assert (p["kernel"], p["token_tile"], p["stream_k"]) == ("fused", 256, sk), (M, p)
+            assert (p["kernel"], p["token_tile"], p["stream_k"]) == ("fused", bt, sk), (M, p)
     for op in (FWD, DGRAD):
         p = q(op, 512, 4096, 4096)
         assert (p["token_tile"], p["splits"], p["cluster_split"], p["grid"], p["workspace_bytes"]) == \
@@ -81,10 +81,12 @@ def test_plan_invariants(bits, f16):
             assert M <= 16 and p["workspace_bytes"] >= 0
             continue
         bt = p["token_tile"]
-        assert bt in (16, 32, 64, 128, 256) and (bits == 4 or bt <= 128)
+        assert bt in (16, 32, 64, 128, 256, 512) and (bits == 4 or bt <= 128)
         assert 1 <= p["grid"] <= SMS
         ttiles = -(-M // bt)
-        wtiles = -(-ncols // 128)
+        wtiles = -(-ncols // (256 if bt == 512 else 128))  # CTA pairs: 256-row weight tiles
+        if bt == 512:
+            assert M >= 1024 and p["grid"] % 2 == 0 and not p["stream_k"] and not p["cluster_split"]
         assert p["items"] == wtiles * ttiles * p["splits"]
         assert p["splits"] <= max(1, -(-contract // 64))
         if p["cluster_split"]:
@@ -134,13 +136,14 @@ def test_fixed_token_tile_option():
     # A fixed tile is the only candidate for M > 32 (one-byte codes: at most 128),
     # on every schedule; other values are ignored; 0 restores the planner's choice.
     try:
-        for bt in (64, 128, 256):
+        for bt in (64, 128, 256, 512):
             _lib.set_token_tile(bt)
+            tw = 256 if bt == 512 else 128
             for M, N, K in [(33, 256, 512), (700, 640, 1024), (4096, 4096, 4096)]:
                 for op in (FWD, DGRAD):
                     p = q(op, M, N, K)
                     assert p["token_tile"] == bt, (bt, M, p)
-                    assert p["items"] == -(-(N if op == FWD else K) // 128) * -(-M // bt) * p["splits"]
+                    assert p["items"] == -(-(N if op == FWD else K) // tw) * -(-M // bt) * p["splits"]
             assert q(FWD, 700, 640, 1024, bits=8)["token_tile"] == min(bt, 128)
             assert q(FWD, 20, 640, 1024)["token_tile"] == 32  # M <= 32 keeps its own tile
         _lib.set_stream_k(_lib.STREAM_K_FORCE)
@@ -150,12 +153,15 @@ def test_fixed_token_tile_option():
         _lib.set_stream_k(_lib.STREAM_K_AUTO)
         _lib.set_token_tile(96)  # ignored
         assert q(FWD, 4096, 4096, 4096)["token_tile"] == 128
-        _lib.set_token_tile(512)  # ignored
-        assert q(FWD, 4096, 4096, 4096)["token_tile"] == 128
+        _lib.set_token_tile(512)  # CTA-pair tiles: 256-row weight tiles, two CTAs per item
+        p = q(FWD, 700, 640, 1024)
+        assert p["token_tile"] == 512 and p["items"] == 3 * 2 * p["splits"] and not p["stream_k"]
+        assert p["grid"] % 2 == 0 and p["grid"] <= SMS
+        assert q(FWD, 700, 640, 1024, bits=8)["token_tile"] == 128
     finally:
         _lib.set_token_tile(0)
         _lib.set_stream_k(_lib.STREAM_K_AUTO)
-    assert q(FWD, 4096, 4096, 4096)["token_tile"] == 256
+    assert q(FWD, 4096, 4096, 4096)["token_tile"] == 512
 
 
 def test_sm_count_changes_the_schedule_not_the_contract():
