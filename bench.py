@@ -371,51 +371,66 @@ def run_ours(args, rank, world, local_rank):
     status = nf4.device_status()
 
     # End to end through the public API: each step copies that step's inputs from
-    # pinned host memory and reads its results back.  The copies run on two copy
-    # streams (host to device, device to host) ordered with events, so projection
-    # j + 1's inputs arrive and projection j - 1's results leave while j computes;
-    # two sets of device buffers alternate between steps.
+    # pinned host memory and reads its results back.  All inputs of a step (x and
+    # grad_y of the seven projections) sit in one pinned buffer and go over in one
+    # copy, the results in one copy back (few host calls per step, so the host does
+    # not bound it); the copies run on two copy streams ordered with events, so
+    # step i + 1's inputs arrive and step i - 1's results leave while step i
+    # computes, and two device buffer sets alternate between steps.
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    xh = [x.pin_memory() for x in xs_host]
-    gyh = [y.pin_memory() for y in gys_host]
-    yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
-    gxh = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in gxs]
-    h2d = sum(t.numel() * 2 for t in xh + gyh)
-    d2h = sum(t.numel() * 2 for t in yh + gxh)
-    bufs = [(xs, gys, ys, gxs),
-            ([torch.empty_like(t) for t in xs], [torch.empty_like(t) for t in gys],
-             [torch.empty_like(t) for t in ys], [torch.empty_like(t) for t in gxs])]
-    up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_shapes = [tuple(t.shape) for t in xs_host] + [tuple(t.shape) for t in gys_host]
+    out_shapes = [tuple(y.shape) for y in ys] + [tuple(x.shape) for x in gxs]
+    n_in = sum(a * b for a, b in in_shapes)
+    n_out = sum(a * b for a, b in out_shapes)
+    in_h = torch.empty(n_in, dtype=torch.bfloat16).pin_memory()
+    off = 0
+    for t in list(xs_host) + list(gys_host):
+        in_h[off:off + t.numel()].copy_(t.reshape(-1))
+        off += t.numel()
+    out_h = torch.empty(n_out, dtype=torch.bfloat16).pin_memory()
+    h2d, d2h = n_in * 2, n_out * 2
+
+    def views(flat, shapes):
+        vs, o = [], 0
+        for a, b in shapes:
+            vs.append(flat[o:o + a * b].view(a, b))
+            o += a * b
+        return vs
+
     nproj = len(sets[0])
-    ev_in = [[torch.cuda.Event() for _ in range(nproj)] for _ in range(2)]
-    ev_done = [[torch.cuda.Event() for _ in range(nproj)] for _ in range(2)]
-    ev_out = [[torch.cuda.Event() for _ in range(nproj)] for _ in range(2)]
-    used = [[False] * nproj for _ in range(2)]
+    bufs = []
+    for _ in range(2):
+        fin = torch.empty(n_in, dtype=torch.bfloat16, device=dev)
+        fout = torch.empty(n_out, dtype=torch.bfloat16, device=dev)
+        vin, vout = views(fin, in_shapes), views(fout, out_shapes)
+        bufs.append((fin, fout, vin[:nproj], vin[nproj:], vout[:nproj], vout[nproj:]))
+    up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
     def e2e_step(i):
         b = i & 1
-        xb, gyb, yb, gxb = bufs[b]
+        fin, fout, xb, gyb, yb, gxb = bufs[b]
         ws = sets[i % REPLICAS]
+        with torch.cuda.stream(up_s):
+            if used[b]:
+                up_s.wait_event(ev_done[b])  # the last step on this set read its inputs
+            fin.copy_(in_h, non_blocking=True)
+            ev_in[b].record(up_s)
+        stream.wait_event(ev_in[b])
+        if used[b]:
+            stream.wait_event(ev_out[b])  # the last step's results on this set have left
         for j in range(nproj):
-            with torch.cuda.stream(up_s):
-                if used[b][j]:
-                    up_s.wait_event(ev_done[b][j])  # the last step on this set read them
-                xb[j].copy_(xh[j], non_blocking=True)
-                gyb[j].copy_(gyh[j], non_blocking=True)
-                ev_in[b][j].record(up_s)
-        for j in range(nproj):
-            stream.wait_event(ev_in[b][j])
-            if used[b][j]:
-                stream.wait_event(ev_out[b][j])  # results of the last use have left
             ops.linear_fwd(xb[j], ws[j], out=yb[j])
             ops.linear_dgrad(gyb[j], ws[j], out=gxb[j])
-            ev_done[b][j].record(stream)
-            with torch.cuda.stream(down_s):
-                down_s.wait_event(ev_done[b][j])
-                yh[j].copy_(yb[j], non_blocking=True)
-                gxh[j].copy_(gxb[j], non_blocking=True)
-                ev_out[b][j].record(down_s)
-            used[b][j] = True
+        ev_done[b].record(stream)
+        with torch.cuda.stream(down_s):
+            down_s.wait_event(ev_done[b])
+            out_h.copy_(fout, non_blocking=True)
+            ev_out[b].record(down_s)
+        used[b] = True
 
     for i in range(3):
         e2e_step(i)
@@ -424,8 +439,7 @@ def run_ours(args, rank, world, local_rank):
     e0.record(stream)
     for i in range(e2e_steps):
         e2e_step(i)
-    for j in range(nproj):  # the last results are on the host before the clock stops
-        stream.wait_event(ev_out[(e2e_steps - 1) & 1][j])
+    stream.wait_event(ev_out[(e2e_steps - 1) & 1])  # the last results are on the host before the clock stops
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
@@ -478,8 +492,9 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "copies": "pinned host buffers; H2D and D2H on two copy streams overlapping "
-                          "the products (event-ordered, two device buffer sets)"},
+                "copies": "one pinned host buffer of the step's inputs and one of its results, "
+                          "one H2D and one D2H copy per step on two copy streams overlapping the "
+                          "products of the neighbouring steps (event-ordered, two device buffer sets)"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "device_status": status,
