@@ -50,13 +50,18 @@ def test_plans_of_the_measured_workloads():
         assert (p["token_tile"], p["splits"], p["cluster_split"], p["grid"], p["workspace_bytes"]) == \
             (256, 2, 2, 128, 0), p
     # Llama-3.1-8B set at M = 512: k/v forward as 8-way cluster splits, k/v input
-    # gradient as 2-way cluster splits, gate/up/down on stream-K.
+    # gradient as 2-way cluster splits.
     assert q(FWD, 512, 1024, 4096)["cluster_split"] == 8
     p = q(DGRAD, 512, 1024, 4096)
     assert (p["token_tile"], p["cluster_split"], p["stream_k"]) == (256, 2, 0)
-    for N, K in [(14336, 4096), (4096, 14336)]:
-        for op in (FWD, DGRAD):
-            assert q(op, 512, N, K)["stream_k"] == 1
+    # gate / up forward and down input gradient (224 tiles of 64 steps) on
+    # stream-K; their 224-step contractions over 64 tiles (gate / up input
+    # gradient, down forward) as 2-way cluster splits.
+    for op, N, K in [(FWD, 14336, 4096), (DGRAD, 4096, 14336)]:
+        assert q(op, 512, N, K)["stream_k"] == 1
+    for op, N, K in [(DGRAD, 14336, 4096), (FWD, 4096, 14336)]:
+        p = q(op, 512, N, K)
+        assert (p["cluster_split"], p["stream_k"], p["workspace_bytes"]) == (2, 0, 0), p
     # Small M: the warp-MMA kernels for a 4-bit bf16 product; fp16 compute and
     # one-byte codes always take the fused kernel.
     assert q(FWD, 1, 4096, 4096)["kernel"] == "small_m_mma"
