@@ -195,9 +195,10 @@ cudaError_t launch_gemm_f16(int mode, int bt, const GemmArgs& a, const CUtensorM
                             cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* ws, int splits, int64_t M, int64_t ncols,
                                  void* out, int64_t ld, bool f16, cudaStream_t s);
-// Bytes of the fused kernel's activation ring for a token tile and code width (the
-// receive area of a cluster split).
-size_t gemm_ring_bytes(int bt, int bits);
+// Bytes of the fused kernel's rings (decoded, activation and code tiles) for a
+// token tile and code width: the exchange area of a cluster split (receive and
+// outgoing blocks), idle once a CTA's single tile is done.
+size_t gemm_exchange_bytes(int bt, int bits);
 // Clusters of `cs` CTAs of the fused kernel (4-bit bf16 instance of `bt`) that can
 // be resident at once on the current device; 0 when it cannot be queried.
 int gemm_cluster_capacity(int mode, int bt, int cs);

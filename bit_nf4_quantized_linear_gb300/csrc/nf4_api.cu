@@ -363,8 +363,9 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
       for (int si = 0; si < 3; ++si) {
         const int cs = cand_cs[si];
         if (bt / cs < 32 || ksteps < cs) continue;
-        const size_t recv = static_cast<size_t>(cs - 1) * 4 * 32 * (bt / cs + 4) * 4;
-        if (recv > nf4::gemm_ring_bytes(bt, 4)) continue;
+        // receive and outgoing blocks of the partials fit the idle rings
+        const size_t xchg = 2 * static_cast<size_t>(cs - 1) * 4 * 32 * (bt / cs + 4) * 4;
+        if (xchg > nf4::gemm_exchange_bytes(bt, 4)) continue;
         if (tiles > cluster_capacity(mode, bt, cs, sms, query_device)) continue;
         const double t = static_cast<double>((ksteps + cs - 1) / cs) * step_cycles(bt) + 3000.0 +
                          1500.0 + 8.0 * bt * (cs - 1) / cs;

@@ -422,6 +422,118 @@ __device__ __forceinline__ uint16_t to16(float f) {
   else return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Cluster-split epilogue of the CTA's tile (one epilogue warp per TMEM row
+// quarter q).  The cs CTAs of this cluster hold one contraction slice each of the
+// same tile, and rank p finishes token slice p (W = BT / cs tokens).  The CTA's
+// rings [0, kOffOut) are idle once its single tile's MMAs are done; they hold a
+// receive block and an outgoing block per (other rank, row quarter), each 32 rows
+// x W tokens fp32 at a row pitch of W + 4 floats (so that the 16-byte row reads
+// and writes are conflict-free).  Each warp stages its fp32 partial of every other
+// slice in its outgoing blocks, and once every other rank's rings are idle one
+// lane sends each block to its owner with one bulk copy (shared memory to the
+// other CTA's shared memory), completing on the owner's receive barrier.  The owner
+// then adds the partials of its own slice in rank order (its own from tensor
+// memory) and stores bf16 through its 2 KB staging slice and bulk tensor stores
+// (tokens past M are not written).
+template <int BT, int BITS, bool F16>
+__device__ __forceinline__ void cs_epilogue(const GemmArgs& a, const Shared& sh, uint8_t* smem, uint32_t sbase,
+                                            const CUtensorMap* tmap_out, const Item& it, uint32_t taddr,
+                                            int q, int ntok) {
+  using G = Geo<BT, BITS>;
+  const int lane = threadIdx.x & 31;
+  const int S = a.cs;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int W = BT / S;
+  const int pitch = W + 4;
+  const int blk = 32 * pitch * 4;  // bytes of a block
+  auto recv_off = [&](int slot, int qq) { return (slot * kNumEpiWarps + qq) * blk; };
+  auto out_off = [&](int slot, int qq) { return ((S - 1 + slot) * kNumEpiWarps + qq) * blk; };
+  bool cs_ok = 2 * (S - 1) * kNumEpiWarps * blk <= G::kOffOut && W % 32 == 0;
+  if (!cs_ok) record_error(a, NF4_ERR_UNSUPPORTED_SHAPE);
+  if (cs_ok) {
+    // 1. The partials of the other slices into the outgoing blocks (block slot of
+    // rank p: p, skipping this rank).
+    for (int p = 0; p < S; ++p) {
+      if (p == rank) continue;
+      uint8_t* dst = smem + out_off(p < rank ? p : p - 1, q) + lane * pitch * 4;
+      for (int c0 = 0; c0 < W && p * W + c0 < ntok; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(taddr + p * W + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<uint4*>(dst + (c0 + j) * 4) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+    }
+    fence_proxy_async_smem();  // the stores above, then the bulk copies that read them
+    __syncwarp();
+    // 2. This rank expects its receive blocks, then tells every other rank that its
+    // rings are idle.
+    if (q == 0 && lane == 0) {
+      mbar_arrive_expect_tx(bar_at(sh, kBarCsRecv), static_cast<uint32_t>((S - 1) * kNumEpiWarps * blk));
+      for (int p = 0; p < S; ++p)
+        if (p != rank) mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarCsFree), static_cast<uint32_t>(p)));
+    }
+    // 3. Once every other rank's rings are idle, send each its blocks (this rank's
+    // block slot there: rank, skipping p).
+    cs_ok = wait_phase_cluster(bar_at(sh, kBarCsFree), 0, sh, a);
+    if (cs_ok && lane == 0)
+      for (int p = 0; p < S; ++p) {
+        if (p == rank) continue;
+        bulk_copy_s2cluster(mapa_shared(sbase + recv_off(rank < p ? rank : rank - 1, q), static_cast<uint32_t>(p)),
+                            sbase + out_off(p < rank ? p : p - 1, q), static_cast<uint32_t>(blk),
+                            mapa_shared(bar_at(sh, kBarCsRecv), static_cast<uint32_t>(p)));
+      }
+  }
+  // 4. This rank's slice: the ranks' partials added in rank order, to bf16.
+  if (cs_ok) cs_ok = wait_phase_cluster(bar_at(sh, kBarCsRecv), 0, sh, a);
+  if (cs_ok) {
+    const int t0 = rank * W;
+    uint16_t* stg = reinterpret_cast<uint16_t*>(smem + G::kOffOut + q * kOutWarpBytes);
+    const uint32_t stg_addr = sbase + G::kOffOut + q * kOutWarpBytes;
+#pragma unroll 1
+    for (int c0 = 0; c0 < W && t0 + c0 < ntok; c0 += 32) {
+      if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
+      __syncwarp();
+#pragma unroll 1
+      for (int h = 0; h < 32; h += 16) {  // two 16-token halves of the chunk
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(taddr + t0 + c0 + h, v);
+        tmem_wait_ld();
+        float acc[16];
+#pragma unroll 1
+        for (int r = 0; r < S; ++r) {
+          if (r == rank) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[j] = r == 0 ? __uint_as_float(v[j]) : __fadd_rn(acc[j], __uint_as_float(v[j]));
+          } else {
+            const int slot = r < rank ? r : r - 1;
+            const float* src = reinterpret_cast<const float*>(smem + recv_off(slot, q) + lane * pitch * 4) + c0 + h;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(src + j);
+              acc[j] = r == 0 ? f.x : __fadd_rn(acc[j], f.x);
+              acc[j + 1] = r == 0 ? f.y : __fadd_rn(acc[j + 1], f.y);
+              acc[j + 2] = r == 0 ? f.z : __fadd_rn(acc[j + 2], f.z);
+              acc[j + 3] = r == 0 ? f.w : __fadd_rn(acc[j + 3], f.w);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg[(h + j) * 32 + lane] = to16<F16>(acc[j]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmap_out, stg_addr, static_cast<int32_t>(it.col0 + 32 * q),
+                     static_cast<int32_t>(it.tok0 + t0 + c0));
+        bulk_commit_group();
+      }
+    }
+  }
+}
+
 template <int MODE, int BT, int BITS, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
@@ -492,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumEpiWarps; ++i) mbar_init(bar_at(sh, kBarSkPart + i), 1);
     const int cs_peers = a.cs > 1 ? a.cs - 1 : 1;
     mbar_init(bar_at(sh, kBarCsFree), cs_peers);                  // one arrival per other rank
-    mbar_init(bar_at(sh, kBarCsRecv), cs_peers * kNumEpiWarps);   // each of their epilogue warps
+    mbar_init(bar_at(sh, kBarCsRecv), 1);  // this rank's expect-tx (the blocks complete it)
     *sh.abort_flag = 0;
     *dep_done(sh) = early ? 0 : 1;
     fence_mbar_init();
@@ -756,100 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       };
       if (a.cs > 1) {
-        // Cluster split: the cs CTAs of this cluster hold one contraction slice each
-        // of the same tile, and rank p finishes token slice p (W = BT / cs tokens).
-        // Each rank writes its fp32 partial of the other slices into their owners'
-        // activation rings (idle once the tile's MMAs are done) through distributed
-        // shared memory, then adds the partials of its own slice in rank order and
-        // stores it in bf16.  In rank p's ring, the block of (sending rank, with p
-        // itself skipped, row quarter) holds 32 rows x W tokens fp32 at a row pitch of
-        // W + 4 floats, so that the owner's 16-byte row reads are conflict-free.
-        const int S = a.cs;
-        const int rank = static_cast<int>(cluster_ctarank());
-        const int W = BT / S;
-        const int pitch = W + 4;
-        auto recv_off = [&](int slot, int qq) {  // byte offset of a block in the ring
-          return ((slot * kNumEpiWarps + qq) * 32) * pitch * 4;
-        };
-        bool cs_ok = (S - 1) * kNumEpiWarps * 32 * pitch * 4 <= G::kStagesX * G::kXStage && W % 32 == 0;
-        if (!cs_ok) record_error(a, NF4_ERR_UNSUPPORTED_SHAPE);
-        // 1. This rank's ring is free (its MMAs are done): tell every other rank.
-        if (cs_ok && q == 0 && lane == 0)
-          for (int p = 0; p < S; ++p)
-            if (p != rank) mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarCsFree), static_cast<uint32_t>(p)));
-        // 2. Once every other rank's ring is free, send each its slice of this partial.
-        if (cs_ok) cs_ok = wait_phase_cluster(bar_at(sh, kBarCsFree), 0, sh, a);
-        if (cs_ok) {
-          for (int p = 0; p < S; ++p) {
-            if (p == rank) continue;
-            const int slot = rank < p ? rank : rank - 1;
-            const uint32_t dst = mapa_shared(sbase + G::kOffX + static_cast<uint32_t>(recv_off(slot, q) + lane * pitch * 4),
-                                             static_cast<uint32_t>(p));
-            for (int c0 = 0; c0 < W && p * W + c0 < ntok; c0 += 16) {
-              uint32_t v[16];
-              tmem_ld_32x32b_x16(taddr + p * W + c0, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int k = 0; k < 16; k += 4)
-                st_cluster_v4(dst + static_cast<uint32_t>((c0 + k) * 4), v[k], v[k + 1], v[k + 2], v[k + 3]);
-            }
-          }
-          asm volatile("fence.acq_rel.cluster;" ::: "memory");  // this lane's stores, then the arrival
-          __syncwarp();
-          if (lane == 0)
-            for (int p = 0; p < S; ++p)
-              if (p != rank) mbar_arrive_cluster(mapa_shared(bar_at(sh, kBarCsRecv), static_cast<uint32_t>(p)));
-        }
-        // 3. This rank's slice: the ranks' partials added in rank order, to bf16,
-        // through shared-memory staging and bulk tensor stores (tokens past M are not
-        // written).
-        if (cs_ok) cs_ok = wait_phase_cluster(bar_at(sh, kBarCsRecv), 0, sh, a);
-        if (cs_ok) {
-          const int t0 = rank * W;
-          uint16_t* stg = reinterpret_cast<uint16_t*>(smem + G::kOffOut + q * kOutWarpBytes);
-          const uint32_t stg_addr = sbase + G::kOffOut + q * kOutWarpBytes;
-#pragma unroll 1
-          for (int c0 = 0; c0 < W && t0 + c0 < ntok; c0 += 32) {
-            if (lane == 0) bulk_wait_read_all();  // the previous chunk has left the buffer
-            __syncwarp();
-#pragma unroll 1
-            for (int h = 0; h < 32; h += 16) {  // two 16-token halves of the chunk
-              uint32_t v[16];
-              tmem_ld_32x32b_x16(taddr + t0 + c0 + h, v);
-              tmem_wait_ld();
-              float acc[16];
-#pragma unroll 1
-              for (int r = 0; r < S; ++r) {
-                if (r == rank) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    acc[j] = r == 0 ? __uint_as_float(v[j]) : __fadd_rn(acc[j], __uint_as_float(v[j]));
-                } else {
-                  const int slot = r < rank ? r : r - 1;
-                  const float* src = reinterpret_cast<const float*>(smem + G::kOffX + recv_off(slot, q) +
-                                                                    lane * pitch * 4) + c0 + h;
-#pragma unroll
-                  for (int j = 0; j < 16; j += 4) {
-                    const float4 f = *reinterpret_cast<const float4*>(src + j);
-                    acc[j] = r == 0 ? f.x : __fadd_rn(acc[j], f.x);
-                    acc[j + 1] = r == 0 ? f.y : __fadd_rn(acc[j + 1], f.y);
-                    acc[j + 2] = r == 0 ? f.z : __fadd_rn(acc[j + 2], f.z);
-                    acc[j + 3] = r == 0 ? f.w : __fadd_rn(acc[j + 3], f.w);
-                  }
-                }
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) stg[(h + j) * 32 + lane] = to16<F16>(acc[j]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmap_out, stg_addr, static_cast<int32_t>(it.col0 + 32 * q),
-                           static_cast<int32_t>(it.tok0 + t0 + c0));
-              bulk_commit_group();
-            }
-          }
-        }
+        cs_epilogue<BT, BITS, F16>(a, sh, smem, sbase, &tmap_out, it, taddr, q, ntok);
       } else if (sk_part) {
         float* dst = sk_slot(unit);
 #pragma unroll 1
@@ -1397,17 +1416,17 @@ cudaError_t launch_gemm_8bit(int mode, int bt, const GemmArgs& a, const CUtensor
 }
 #else
 
-size_t gemm_ring_bytes(int bt, int bits) {
+size_t gemm_exchange_bytes(int bt, int bits) {
   switch (bits == 8 ? bt + 1 : bt) {
-    case 16: return size_t(Geo<16, 4>::kStagesX) * Geo<16, 4>::kXStage;
-    case 32: return size_t(Geo<32, 4>::kStagesX) * Geo<32, 4>::kXStage;
-    case 64: return size_t(Geo<64, 4>::kStagesX) * Geo<64, 4>::kXStage;
-    case 128: return size_t(Geo<128, 4>::kStagesX) * Geo<128, 4>::kXStage;
-    case 256: return size_t(Geo<256, 4>::kStagesX) * Geo<256, 4>::kXStage;
-    case 17: return size_t(Geo<16, 8>::kStagesX) * Geo<16, 8>::kXStage;
-    case 33: return size_t(Geo<32, 8>::kStagesX) * Geo<32, 8>::kXStage;
-    case 65: return size_t(Geo<64, 8>::kStagesX) * Geo<64, 8>::kXStage;
-    case 129: return size_t(Geo<128, 8>::kStagesX) * Geo<128, 8>::kXStage;
+    case 16: return size_t(Geo<16, 4>::kOffOut);
+    case 32: return size_t(Geo<32, 4>::kOffOut);
+    case 64: return size_t(Geo<64, 4>::kOffOut);
+    case 128: return size_t(Geo<128, 4>::kOffOut);
+    case 256: return size_t(Geo<256, 4>::kOffOut);
+    case 17: return size_t(Geo<16, 8>::kOffOut);
+    case 33: return size_t(Geo<32, 8>::kOffOut);
+    case 65: return size_t(Geo<64, 8>::kOffOut);
+    case 129: return size_t(Geo<128, 8>::kOffOut);
     default: return 0;
   }
 }

@@ -186,6 +186,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
 // Bulk copy (no tensor map) of `bytes` from global memory into this CTA's shared
 // memory, completing on `bar` as transaction bytes.  Both addresses 16-byte
 // aligned, `bytes` a multiple of 16.
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory to the shared memory of a CTA of the cluster (`dst` and `bar`
+// are shared::cluster addresses in that CTA); completes on its barrier `bar`.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                    uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
   asm volatile(

@@ -49,9 +49,10 @@ def test_plans_of_the_measured_workloads():
         p = q(op, 512, 4096, 4096)
         assert (p["token_tile"], p["splits"], p["cluster_split"], p["grid"], p["workspace_bytes"]) == \
             (256, 2, 2, 128, 0), p
-    # Llama-3.1-8B set at M = 512: k/v forward as 8-way cluster splits, k/v input
-    # gradient as 2-way cluster splits.
-    assert q(FWD, 512, 1024, 4096)["cluster_split"] == 8
+    # Llama-3.1-8B set at M = 512: k/v forward as 4-way cluster splits of 128-token
+    # tiles, k/v input gradient as 2-way cluster splits.
+    p = q(FWD, 512, 1024, 4096)
+    assert (p["token_tile"], p["cluster_split"]) == (128, 4), p
     p = q(DGRAD, 512, 1024, 4096)
     assert (p["token_tile"], p["cluster_split"], p["stream_k"]) == (256, 2, 0)
     # gate / up forward and down input gradient (224 tiles of 64 steps) on
