@@ -1048,7 +1048,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar_at(sh, kBarAccEmpty + ab));
       }
     }
-    if (lane == 0) bulk_wait_all();  // output tiles written before the CTA exits
+    // The output tiles' bulk stores have read their staging before the CTA exits (the
+    // writes complete with the grid, before any dependent grid reads them).
+    if (lane == 0) bulk_wait_read_all();
     __syncwarp();
   } else {
     // ------------------------------------------------------------ decoders --
