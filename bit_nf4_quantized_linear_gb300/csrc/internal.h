@@ -128,7 +128,9 @@ struct SkinnyLayout {
 };
 
 struct SkinnyArgs {
-  const __nv_bfloat16* act;  // x [M, K] (forward) or grad_y [M, N] (input gradient)
+  // x [M, K] (forward) or grad_y [M, N] (input gradient); like `out`, bf16, or
+  // IEEE fp16 bits when f16 is set.
+  const __nv_bfloat16* act;
   int64_t ld_act;
   const uint8_t* packed;
   int64_t N, K, KB;
@@ -139,6 +141,7 @@ struct SkinnyArgs {
   const float* code4;
   const float* code8;
   int dq;
+  int f16;        // fp16 operands and output
   __nv_bfloat16* out;
   int64_t ld_out;
   int64_t M;
@@ -165,7 +168,7 @@ struct SkinnyPlan {
 };
 
 // Plans and launches (S CTAs per cluster along the contraction).
-bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* p);
+bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* p, bool f16 = false);
 // tmap: the packed codes [N rows, K/2 bytes] as a uint8 tensor with a box of
 // 128 bytes x 16 rows and 128B swizzle (forward) or 32 bytes x 64 rows and 32B
 // swizzle (input gradient).

@@ -252,10 +252,12 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
   const int64_t contract = mode == 0 ? K : N;
   const int small = g_small_m_path.load(std::memory_order_relaxed);
   nf4::SkinnyPlan sk;
-  // 8-bit codes (tiles of <= 128 tokens) and the fp16 dtype run the fused tcgen05
-  // kernel at every M.
-  const bool fused_only = bits == 8 || f16;
-  if (!fused_only && M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk)) {
+  // 8-bit codes (tiles of <= 128 tokens) run the fused tcgen05 kernel at every M;
+  // small M with 4-bit codes takes the warp-MMA kernels (bf16 or fp16 operands),
+  // or the SIMT GEMV (bf16 only).
+  const bool skinny_ok = bits == 4;
+  const bool gemv_ok = bits == 4 && !f16;
+  if (skinny_ok && M > 0 && small == NF4_SMALL_M_AUTO && nf4::skinny_plan(mode, M, N, K, sms, &sk, f16)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.skinny = true;
     p.sk = sk;
@@ -263,7 +265,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     p.ws_bytes = 0;
     return p;
   }
-  if (!fused_only && M > 0 && small != NF4_SMALL_M_TILES &&
+  if (gemv_ok && M > 0 && small != NF4_SMALL_M_TILES &&
       M <= (mode == 0 ? nf4::kGemvMaxMFwd : nf4::kGemvMaxMDgrad)) {
     Plan p = make_plan(M, ncols, contract, 16, 1);
     p.gemv = true;
@@ -438,6 +440,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     k.code4 = w->code4;
     k.code8 = w->code8;
     k.dq = w->double_quant;
+    k.f16 = f16 ? 1 : 0;
     k.out = static_cast<__nv_bfloat16*>(out);
     k.ld_out = ld_out;
     k.M = M;

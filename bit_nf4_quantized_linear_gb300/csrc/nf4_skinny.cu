@@ -42,6 +42,7 @@
 // block scales and the first units' packed codes are read before that wait.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -89,13 +90,30 @@ __device__ __forceinline__ void allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// d += a * b: one warp-level 16x8x16 bf16 product, fp32 accumulation.
+// d += a * b: one warp-level 16x8x16 bf16 (or fp16 when F16) product, fp32
+// accumulation.
+template <bool F16>
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  if constexpr (F16)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One output value: bf16, or IEEE fp16 when F16 (round to nearest even).
+template <bool F16>
+__device__ __forceinline__ void store16(__nv_bfloat16* p, float v) {
+  if constexpr (F16)
+    *reinterpret_cast<__half*>(p) = __float2half_rn(v);
+  else
+    *p = __float2bfloat16_rn(v);
 }
 
 // The byte-pair table: entry e = (code4[e >> 4], code4[e & 15]) as two fp32 (the
@@ -127,11 +145,12 @@ __device__ __forceinline__ void store_table(uint8_t* smem, const TableSrc& src) 
   for (int k = 0; k < 8; ++k) t[k * kThreads + tid] = make_uint4(src.hi[k], src.lo, src.hi[k], src.lo);
 }
 
-// Dequantised bf16 pair of the packed byte that `sel` picks from w:
-// bf16(fp32(code4[q] * s)) for both nibbles, the even value in the low half.
+// Dequantised pair of the packed byte that `sel` picks from w: bf16(fp32(code4[q]
+// * s)) (fp16 when F16) for both nibbles, the even value in the low half.
 // The permute puts the byte into bits 8..15 and lane*8 (byte 0 of lane8) into
 // bits 0..7 of the table offset; s2 holds the two values' scales (low word:
 // even value).
+template <bool F16>
 __device__ __forceinline__ uint32_t lookup(const uint8_t* smem, uint32_t w, uint32_t lane8,
                                            uint32_t sel, uint64_t s2) {
   const uint2 c = *reinterpret_cast<const uint2*>(smem + __byte_perm(w, lane8, sel));
@@ -139,9 +158,15 @@ __device__ __forceinline__ uint32_t lookup(const uint8_t* smem, uint32_t w, uint
   asm("mul.rn.f32x2 %0, %1, %2;"
       : "=l"(p)
       : "l"((static_cast<uint64_t>(c.y) << 32) | c.x), "l"(s2));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(static_cast<uint32_t>(p)),
-                                                 __uint_as_float(static_cast<uint32_t>(p >> 32)));
-  return *reinterpret_cast<const uint32_t*>(&b);
+  const float lo = __uint_as_float(static_cast<uint32_t>(p));
+  const float hi = __uint_as_float(static_cast<uint32_t>(p >> 32));
+  if constexpr (F16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+  }
 }
 
 __device__ __forceinline__ uint64_t pair2(float lo, float hi) {
@@ -369,7 +394,7 @@ __host__ __device__ inline Layout make_layout(int mode, int mt, int S, int64_t c
 // sits in shared memory as 64-value chunks per token whose eight 16-byte units
 // are XOR-swizzled by (chunk & 3) | (token & 1) << 2, so the eight lanes of a
 // quarter warp (two tokens, four chunks, one unit index) hit different banks.
-template <int MT>  // 8-token MMA tiles: 1 (M <= 8) or 2 (M <= 16)
+template <int MT, bool F16>  // 8-token MMA tiles: 1 (M <= 8) or 2 (M <= 16); fp16 operands
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_fwd_kernel(const __grid_constant__ CUtensorMap tmap, const SkinnyArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -550,18 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < MT; ++t) xv[t] = xr[t][u ^ f];
       // word u holds values 8u .. 8u+7 of the block: bytes 0, 1 feed MMA 2u, bytes 2, 3 MMA 2u+1
-      const uint32_t af[4] = {lookup(smem, wa[u], lane8, kSel0, sA2),
-                              lookup(smem, wb[u], lane8, kSel0, sB2),
-                              lookup(smem, wa[u], lane8, kSel1, sA2),
-                              lookup(smem, wb[u], lane8, kSel1, sB2)};
+      const uint32_t af[4] = {lookup<F16>(smem, wa[u], lane8, kSel0, sA2),
+                              lookup<F16>(smem, wb[u], lane8, kSel0, sB2),
+                              lookup<F16>(smem, wa[u], lane8, kSel1, sA2),
+                              lookup<F16>(smem, wb[u], lane8, kSel1, sB2)};
 #pragma unroll
-      for (int t = 0; t < MT; ++t) mma16816(acc[t], af, xv[t].x, xv[t].y);
-      const uint32_t ag[4] = {lookup(smem, wa[u], lane8, kSel2, sA2),
-                              lookup(smem, wb[u], lane8, kSel2, sB2),
-                              lookup(smem, wa[u], lane8, kSel3, sA2),
-                              lookup(smem, wb[u], lane8, kSel3, sB2)};
+      for (int t = 0; t < MT; ++t) mma16816<F16>(acc[t], af, xv[t].x, xv[t].y);
+      const uint32_t ag[4] = {lookup<F16>(smem, wa[u], lane8, kSel2, sA2),
+                              lookup<F16>(smem, wb[u], lane8, kSel2, sB2),
+                              lookup<F16>(smem, wa[u], lane8, kSel3, sA2),
+                              lookup<F16>(smem, wb[u], lane8, kSel3, sB2)};
 #pragma unroll
-      for (int t = 0; t < MT; ++t) mma16816(acc[t], ag, xv[t].z, xv[t].w);
+      for (int t = 0; t < MT; ++t) mma16816<F16>(acc[t], ag, xv[t].z, xv[t].w);
     }
     __syncwarp();
     s0 = s1;
@@ -582,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto store = [&](int e, float v) {
     const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
     const int64_t n = (tile0 + i) * 16 + (r & 15);
-    if ((r >> 4) < M && n < a.N) a.out[(r >> 4) * a.ld_out + n] = __float2bfloat16_rn(v);
+    if ((r >> 4) < M && n < a.N) store16<F16>(a.out + (r >> 4) * a.ld_out + n, v);
   };
   for (int e = threadIdx.x; e < total; e += kThreads) {
     const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
@@ -609,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // weight rows, looked up in the same table and scaled by the two rows' block
 // scales; a lane's accumulators stay on its own 16 in-features for the whole
 // column.  The unit's grad_y values travel in the same ring slot as its codes.
-template <int MT>
+template <int MT, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_dgrad_kernel(const __grid_constant__ CUtensorMap tmap, const SkinnyArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -830,10 +855,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const uint32_t sel = lookup_sel(static_cast<uint32_t>(m));
-        const uint32_t af[4] = {lookup(smem, e01, lane8, sel, s01), lookup(smem, o01, lane8, sel, s01),
-                                lookup(smem, e23, lane8, sel, s23), lookup(smem, o23, lane8, sel, s23)};
+        const uint32_t af[4] = {lookup<F16>(smem, e01, lane8, sel, s01), lookup<F16>(smem, o01, lane8, sel, s01),
+                                lookup<F16>(smem, e23, lane8, sel, s23), lookup<F16>(smem, o23, lane8, sel, s23)};
 #pragma unroll
-        for (int t = 0; t < MT; ++t) mma16816(acc[t][m], af, b[t][0], b[t][1]);
+        for (int t = 0; t < MT; ++t) mma16816<F16>(acc[t][m], af, b[t][0], b[t][1]);
       }
     }
     __syncwarp();
@@ -853,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* last = reinterpret_cast<const float*>(smem + L.ring);
   auto store = [&](int e, float v) {
     const int i = e / (M * 64), r = e - i * M * 64;
-    a.out[(r >> 6) * a.ld_out + (col0 + i) * 64 + (r & 63)] = __float2bfloat16_rn(v);
+    store16<F16>(a.out + (r >> 6) * a.ld_out + (col0 + i) * 64 + (r & 63), v);
   };
   for (int e = threadIdx.x; e < total; e += kThreads) {
     const int i = e / (M * 64), r = e - i * M * 64;
@@ -868,9 +893,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 using SkinnyKernel = void (*)(CUtensorMap, SkinnyArgs);
 
-template <int MODE, int MT>
+template <int MODE, int MT, bool F16>
 cudaError_t configure(SkinnyKernel& kern) {
-  kern = MODE == 0 ? skinny_fwd_kernel<MT> : skinny_dgrad_kernel<MT>;
+  kern = MODE == 0 ? skinny_fwd_kernel<MT, F16> : skinny_dgrad_kernel<MT, F16>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -882,10 +907,10 @@ cudaError_t configure(SkinnyKernel& kern) {
 }
 
 // Clusters of S CTAs (with `smem` bytes each) that can be resident at once.
-template <int MODE, int MT>
+template <int MODE, int MT, bool F16>
 int max_clusters_mt(int S, size_t smem) {
   SkinnyKernel kern = nullptr;
-  if (configure<MODE, MT>(kern) != cudaSuccess) return 0;
+  if (configure<MODE, MT, F16>(kern) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(S), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -905,10 +930,10 @@ int max_clusters_mt(int S, size_t smem) {
   return n;
 }
 
-// Cached per (mode, tiles, S, shared-memory size).
-int max_clusters(int mode, int mt, int S, size_t smem) {
+// Cached per (mode, tiles, operand type, S, shared-memory size).
+int max_clusters(int mode, int mt, bool f16, int S, size_t smem) {
   struct Entry {
-    int mode, mt, S;
+    int mode, mt, f16, S;
     size_t smem;
     int n;
   };
@@ -916,21 +941,29 @@ int max_clusters(int mode, int mt, int S, size_t smem) {
   static std::vector<Entry> cache;
   std::lock_guard<std::mutex> lk(mu);
   for (const Entry& e : cache)
-    if (e.mode == mode && e.mt == mt && e.S == S && e.smem == smem) return e.n;
+    if (e.mode == mode && e.mt == mt && e.f16 == static_cast<int>(f16) && e.S == S && e.smem == smem)
+      return e.n;
   int n;
-  if (mode == 0)
-    n = mt == 1 ? max_clusters_mt<0, 1>(S, smem) : max_clusters_mt<0, 2>(S, smem);
-  else
-    n = mt == 1 ? max_clusters_mt<1, 1>(S, smem) : max_clusters_mt<1, 2>(S, smem);
-  cache.push_back(Entry{mode, mt, S, smem, n});
+  if (f16) {
+    if (mode == 0)
+      n = mt == 1 ? max_clusters_mt<0, 1, true>(S, smem) : max_clusters_mt<0, 2, true>(S, smem);
+    else
+      n = mt == 1 ? max_clusters_mt<1, 1, true>(S, smem) : max_clusters_mt<1, 2, true>(S, smem);
+  } else {
+    if (mode == 0)
+      n = mt == 1 ? max_clusters_mt<0, 1, false>(S, smem) : max_clusters_mt<0, 2, false>(S, smem);
+    else
+      n = mt == 1 ? max_clusters_mt<1, 1, false>(S, smem) : max_clusters_mt<1, 2, false>(S, smem);
+  }
+  cache.push_back(Entry{mode, mt, static_cast<int>(f16), S, smem, n});
   return n;
 }
 
-template <int MODE, int MT>
+template <int MODE, int MT, bool F16>
 cudaError_t launch_mt(const SkinnyArgs& a, const SkinnyPlan& p, const CUtensorMap& tmap,
                       cudaStream_t s) {
   SkinnyKernel kern = nullptr;
-  cudaError_t ce = configure<MODE, MT>(kern);
+  cudaError_t ce = configure<MODE, MT, F16>(kern);
   if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.C * p.S), 1, 1);
@@ -962,7 +995,7 @@ cudaError_t launch_mt(const SkinnyArgs& a, const SkinnyPlan& p, const CUtensorMa
 // cluster reduction.  A warp's unit range must touch at most two tiles, and the
 // shared memory must fit.  A deterministic function of the shape and the SM
 // count.
-bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* out) {
+bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan* out, bool f16) {
   if (M < 1 || M > kSkinnyMaxM || sms < 1 || K % 64 != 0) return false;
   const int mt = M <= 8 ? 1 : 2;
   const int64_t KB = K / 64;
@@ -984,7 +1017,7 @@ bool skinny_plan(int mode, int64_t M, int64_t N, int64_t K, int sms, SkinnyPlan*
     Layout L = make_layout(mode, mt, S, per * gran, nt_max);
     // clusters must all be resident at once (a GPC holds whole clusters only)
     for (int it = 0; S > 1 && it < 4; ++it) {
-      const int cmax = max_clusters(mode, mt, S, static_cast<size_t>(L.total));
+      const int cmax = max_clusters(mode, mt, f16, S, static_cast<size_t>(L.total));
       if (cmax >= C) break;
       C = cmax;
       if (C < 1) break;
@@ -1021,8 +1054,12 @@ cudaError_t launch_skinny(int mode, const SkinnyArgs& args, const SkinnyPlan& p,
   a.tr = static_cast<int>(p.T % p.C);
   a.log2S = p.S == 1 ? 0 : p.S == 2 ? 1 : p.S == 4 ? 2 : 3;
   a.lay = make_layout(mode, mt1 ? 1 : 2, p.S, p.cc, a.nt_max);
-  if (mode == 0) return mt1 ? launch_mt<0, 1>(a, p, tmap, s) : launch_mt<0, 2>(a, p, tmap, s);
-  return mt1 ? launch_mt<1, 1>(a, p, tmap, s) : launch_mt<1, 2>(a, p, tmap, s);
+  if (a.f16) {
+    if (mode == 0) return mt1 ? launch_mt<0, 1, true>(a, p, tmap, s) : launch_mt<0, 2, true>(a, p, tmap, s);
+    return mt1 ? launch_mt<1, 1, true>(a, p, tmap, s) : launch_mt<1, 2, true>(a, p, tmap, s);
+  }
+  if (mode == 0) return mt1 ? launch_mt<0, 1, false>(a, p, tmap, s) : launch_mt<0, 2, false>(a, p, tmap, s);
+  return mt1 ? launch_mt<1, 1, false>(a, p, tmap, s) : launch_mt<1, 2, false>(a, p, tmap, s);
 }
 
 }  // namespace nf4

@@ -179,9 +179,9 @@ nf4_status nf4_dequantize(const nf4_weight* w, void* out, int32_t out_dtype, voi
  *   ws: device workspace of nf4_workspace_size(NF4_OP_LINEAR_FWD, M, N, K, 0)
  *   bytes (split-K partials for small M; may be NULL when that size is 0).
  *   Paths (nf4_get_path_counters tells which ran): M <= 16 runs the warp-MMA
- *   small-M kernels (mma.sync bf16, fixed-order cluster reduction; see
+ *   small-M kernels for 4-bit codes (mma.sync, fixed-order cluster reduction; see
  *   nf4_set_small_m_path for the SIMT GEMV and tiled alternatives); larger M, and
- *   every M for 8-bit codes and the fp16 dtype, runs the tcgen05 kernel (fp32
+ *   every M for 8-bit codes, runs the tcgen05 kernel (fp32
  *   accumulation in tensor memory) with the classic or stream-K schedule
  *   (nf4_set_stream_k).  Split partials are summed in a fixed order, by a second
  *   kernel (classic) or by the CTA finishing the tile (stream-K).  No atomics. */
@@ -203,9 +203,11 @@ nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_w
  * Linear4bit, which computes in the activations' half-precision type): x / grad_y
  * and y / grad_x are IEEE fp16, and the operand is fp16(fp32(code4[q] * absmax'))
  * (round to nearest even) instead of bf16.  Same arguments, workspace and
- * determinism as nf4_linear_fwd / nf4_linear_dgrad; every M runs the fused tcgen05
- * kernel (fp16 tcgen05 MMAs, fp32 accumulation).  4-bit codes only (bits == 8 ->
- * NF4_ERR_UNSUPPORTED). */
+ * determinism as nf4_linear_fwd / nf4_linear_dgrad; M <= 16 runs the warp-MMA
+ * small-M kernels with fp16 MMAs (the SIMT GEMV alternative is bf16 only, so
+ * NF4_SMALL_M_SIMT sends fp16 to the fused kernel), larger M the fused tcgen05
+ * kernel (fp16 tcgen05 MMAs); fp32 accumulation throughout.  4-bit codes only
+ * (bits == 8 -> NF4_ERR_UNSUPPORTED). */
 nf4_status nf4_linear_fwd_f16(const void* x, int64_t M, int64_t ldx, const nf4_weight* w, void* y,
                               int64_t ldy, void* ws, size_t ws_bytes, void* stream);
 nf4_status nf4_linear_dgrad_f16(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w,

@@ -726,7 +726,7 @@ def test_8bit_stream_k_and_grouped(restore_stream_k):
 
 # ------------------------------------------------------------- fp16 dtype --
 # fp16 activations, operand fp16(fp32(code4[q] * scale)) and fp16 outputs: the
-# fused kernel at every M.
+# warp-MMA kernels for M <= 16, the fused kernel above.
 
 def _f16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
@@ -744,12 +744,52 @@ def test_f16_fwd_dgrad_parity_and_reruns(M, N, K):
     gx = nf4.linear_dgrad(gy, w)
     c = nf4.path_counters()
     assert y.dtype == torch.float16 and gx.dtype == torch.float16
-    assert c["linear_fwd"] == 1 and c["linear_dgrad"] == 1, c
+    if M <= 8:
+        assert c["skinny_fwd"] == 1 and c["skinny_dgrad"] == 1, c
+    assert c["skinny_fwd"] + c["linear_fwd"] == 1 and c["skinny_dgrad"] + c["linear_dgrad"] == 1, c
     parity(y, oracle.linear_fwd(_f16_bits(x), wf, dtype="f16"), f"f16 fwd {M}x{N}x{K}")
     parity(gx, oracle.linear_dgrad(_f16_bits(gy), wf, dtype="f16"), f"f16 dgrad {M}x{N}x{K}")
     for _ in range(3):
         assert torch.equal(nf4.linear_fwd(x, w).view(torch.int16), y.view(torch.int16))
         assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (3, 136, 1088), (8, 4096, 1024), (9, 520, 2112),
+                                   (16, 4096, 4096), (2, 14336, 4096)])
+def test_f16_small_m_parity(M, N, K):
+    """fp16 products at M <= 16 on the warp-MMA kernels (fp16 MMA, operand
+    fp16(fp32(code4[q] * scale)), fp32 accumulation, fixed-order reductions)."""
+    w, st, g = _quant_pair(N, K, True, seed=5 * M + N + K)
+    x = synth.activation(M, K, g).float().half().to(DEV)
+    gy = synth.activation(M, N, g).float().half().to(DEV)
+    wf = oracle.dequantize_f16(st)
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(x, w)
+    gx = nf4.linear_dgrad(gy, w)
+    c = nf4.path_counters()
+    if M <= 8:
+        assert c["skinny_fwd"] == 1 and c["skinny_dgrad"] == 1, c
+    assert c["skinny_fwd"] + c["linear_fwd"] == 1 and c["skinny_dgrad"] + c["linear_dgrad"] == 1, c
+    assert y.dtype == torch.float16 and gx.dtype == torch.float16
+    parity(y, oracle.linear_fwd(_f16_bits(x), wf, dtype="f16"), f"f16 small-M fwd {M}x{N}x{K}")
+    parity(gx, oracle.linear_dgrad(_f16_bits(gy), wf, dtype="f16"), f"f16 small-M dgrad {M}x{N}x{K}")
+    assert torch.equal(nf4.linear_fwd(x, w).view(torch.int16), y.view(torch.int16))
+    assert torch.equal(nf4.linear_dgrad(gy, w).view(torch.int16), gx.view(torch.int16))
+
+
+@pytest.mark.parametrize("N,K", [(64, 128), (296, 2048), (4096, 4096)])
+def test_f16_small_m_identity_probe_exact(N, K):
+    """One-hot fp16 rows read single weight values back through the small-M
+    kernels: their operands are exactly the dequantised fp16 weights."""
+    w, st, _ = _quant_pair(N, K, True, seed=N + K + 1)
+    wf = oracle.dequantize_f16(st)
+    nf4.reset_path_counters()
+    y = nf4.linear_fwd(torch.eye(K, dtype=torch.float16)[:4].contiguous().to(DEV), w)
+    gx = nf4.linear_dgrad(torch.eye(N, dtype=torch.float16)[:4].contiguous().to(DEV), w)
+    c = nf4.path_counters()
+    assert c["skinny_fwd"] == 1 and c["skinny_dgrad"] == 1, c
+    np.testing.assert_array_equal(_f16_bits(y), np.ascontiguousarray(wf.T[:4]))
+    np.testing.assert_array_equal(_f16_bits(gx), wf[:4])
 
 
 def test_f16_identity_probes_exact():

@@ -63,11 +63,13 @@ def test_plans_of_the_measured_workloads():
     for op, N, K in [(DGRAD, 14336, 4096), (FWD, 4096, 14336)]:
         p = q(op, 512, N, K)
         assert (p["cluster_split"], p["stream_k"], p["workspace_bytes"]) == (2, 0, 0), p
-    # Small M: the warp-MMA kernels for a 4-bit bf16 product; fp16 compute and
+    # Small M: the warp-MMA kernels for 4-bit codes, bf16 or fp16 operands;
     # one-byte codes always take the fused kernel.
     assert q(FWD, 1, 4096, 4096)["kernel"] == "small_m_mma"
     assert q(DGRAD, 8, 4096, 4096)["kernel"] == "small_m_mma"
-    assert q(FWD, 1, 4096, 4096, f16=True)["kernel"] == "fused"
+    assert q(FWD, 1, 4096, 4096, f16=True)["kernel"] == "small_m_mma"
+    assert q(DGRAD, 8, 4096, 4096, f16=True)["kernel"] == "small_m_mma"
+    assert q(FWD, 17, 4096, 4096, f16=True)["kernel"] == "fused"
     assert q(FWD, 1, 4096, 4096, bits=8)["kernel"] == "fused"
 
 
@@ -81,8 +83,10 @@ def test_plan_invariants(bits, f16):
         p = q(op, M, N, K, bits=bits, f16=f16)
         assert p == q(op, M, N, K, bits=bits, f16=f16)  # deterministic
         ncols, contract = (N, K) if op == FWD else (K, N)
-        if bits == 8 or f16:
+        if bits == 8:
             assert p["kernel"] == "fused"
+        if f16:  # fp16: the warp-MMA kernels or the fused kernel, never the SIMT GEMV
+            assert p["kernel"] in ("fused", "small_m_mma")
         if p["kernel"] != "fused":
             assert M <= 16 and p["workspace_bytes"] >= 0
             continue
