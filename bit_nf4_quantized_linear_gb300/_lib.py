@@ -11,7 +11,8 @@ import re
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libnf4.so")
+# NF4_CHECKED=1 selects the checked debug build (in-kernel index checks).
+LIB_PATH = os.path.join(PKG, "libnf4_checked.so" if os.environ.get("NF4_CHECKED") == "1" else "libnf4.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "nf4.h")
 
 NF4_OK = 0
@@ -19,7 +20,7 @@ NOALLOC_SCRATCH_BYTES = 2 << 20  # NF4_NOALLOC_SCRATCH_BYTES of include/nf4.h
 STATUS_NAMES = {
     0: "NF4_OK", 1: "NF4_ERR_INVALID_ARG", 2: "NF4_ERR_UNSUPPORTED_SHAPE", 3: "NF4_ERR_ALIGNMENT",
     4: "NF4_ERR_WORKSPACE", 5: "NF4_ERR_CUDA", 6: "NF4_ERR_TIMEOUT", 7: "NF4_ERR_UNSUPPORTED",
-    8: "NF4_ERR_BAD_OFFSETS",
+    8: "NF4_ERR_BAD_OFFSETS", 9: "NF4_ERR_BOUNDS",
 }
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD, OP_GROUPED_SWIGLU_BWD = range(6)
@@ -114,6 +115,8 @@ def lib() -> ctypes.CDLL:
                                        P, I64, P, P, SZ, P],
             "nf4_workspace_size": [I32, I64, I64, I64, I32],
             "nf4_status_string": [I32],
+            "nf4_checked_build": [],
+            "nf4_inject_bounds_failure": [],
             "nf4_get_path_counters": [P],
             "nf4_reset_path_counters": [],
             "nf4_device_status": [P, I32],
@@ -143,6 +146,7 @@ def lib() -> ctypes.CDLL:
         L.nf4_set_cluster_split.restype = None
         L.nf4_set_token_tile.restype = None
         L.nf4_inject_stream_k_timeout.restype = None
+        L.nf4_inject_bounds_failure.restype = None
         _lib = L
         return _lib
 
@@ -178,6 +182,18 @@ def set_small_m_path(path: int):
 
 
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_FORCE = 0, 1, 2
+
+
+def inject_bounds_failure():
+    """Checked build only: the next fused-kernel product's statistics-load index
+    checks fail (loads skipped, NF4_ERR_BOUNDS recorded); see
+    nf4_inject_bounds_failure."""
+    lib().nf4_inject_bounds_failure()
+
+
+def checked_build() -> bool:
+    """True when the loaded library is the checked debug build."""
+    return bool(lib().nf4_checked_build())
 
 
 def set_stream_k(mode: int):

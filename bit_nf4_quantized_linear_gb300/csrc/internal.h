@@ -15,6 +15,28 @@ namespace nf4 {
 constexpr int kStatusTimeout = NF4_ERR_TIMEOUT;
 constexpr int kStatusBadOffsets = NF4_ERR_BAD_OFFSETS;
 
+// Checked debug build (-DNF4_CHECKED=1, libnf4_checked.so): the kernels test the
+// index of each computed global or shared-memory access with in_bounds() before
+// it; a false test records NF4_ERR_BOUNDS in the status word (first error wins)
+// and the caller skips the access.  In the normal build in_bounds() is the
+// constant true and the tests compile to nothing.
+#ifndef NF4_CHECKED
+#define NF4_CHECKED 0
+#endif
+
+#ifdef __CUDACC__
+__device__ __forceinline__ bool in_bounds(bool ok, int* status) {
+#if NF4_CHECKED
+  if (!ok && status) atomicCAS(status, 0, NF4_ERR_BOUNDS);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+#endif
+
 // Upper bound of experts the grouped kernels accept.
 constexpr int kMaxExperts = 512;
 
@@ -86,6 +108,7 @@ struct GemmArgs {
   uint64_t sk_epoch;    // value this launch publishes (never 0)
   uint64_t sk_wait_xor; // the finishing CTA waits for sk_epoch ^ sk_wait_xor (0; the
                         // failure-path test sets a bit no contributor publishes)
+  int chk_inject;       // checked build: fail the statistics-load index check (test hook)
 };
 
 // Stream-K workspace: partial tiles, then the ready flags (8 bytes per CTA and row

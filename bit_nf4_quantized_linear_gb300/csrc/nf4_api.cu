@@ -194,8 +194,10 @@ std::atomic<int> g_weight_prefetch{0};
 // Kernels for M <= 16 (nf4_set_small_m_path).
 std::atomic<int> g_small_m_path{NF4_SMALL_M_AUTO};
 
-// One-shot failure-path test hook (nf4_inject_stream_k_timeout).
+// One-shot failure-path test hooks (nf4_inject_stream_k_timeout,
+// nf4_inject_bounds_failure).
 std::atomic<int> g_inject_sk_timeout{0};
+std::atomic<int> g_inject_bounds{0};
 
 // Stream-K schedule of the fused kernel (nf4_set_stream_k).
 std::atomic<int> g_stream_k{NF4_STREAM_K_AUTO};
@@ -541,6 +543,7 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
     a.cs = p.cs;  // items = tiles x cs, one per CTA, the clusters in one wave
     grid = static_cast<int>(p.items);
   }
+  a.chk_inject = g_inject_bounds.exchange(0, std::memory_order_relaxed);
   if (p.stream_k) {
     a.sk = 1;
     a.sk_units = p.items * p.ksteps;
@@ -865,9 +868,12 @@ const char* nf4_status_string(nf4_status s) {
     case NF4_ERR_TIMEOUT: return "device wait timed out";
     case NF4_ERR_UNSUPPORTED: return "unsupported device or parameter";
     case NF4_ERR_BAD_OFFSETS: return "expert offsets out of contract";
+    case NF4_ERR_BOUNDS: return "an in-kernel index check failed (checked build)";
   }
   return "unknown status";
 }
+
+int32_t nf4_checked_build(void) { return NF4_CHECKED ? 1 : 0; }
 
 void nf4_get_path_counters(uint64_t* out) {
   if (!out) return;
@@ -915,6 +921,8 @@ void nf4_set_token_tile(int32_t tokens) {
 }
 
 void nf4_inject_stream_k_timeout(void) { g_inject_sk_timeout.store(1, std::memory_order_relaxed); }
+
+void nf4_inject_bounds_failure(void) { g_inject_bounds.store(1, std::memory_order_relaxed); }
 
 nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t sms, int32_t bits,
                           int32_t f16, nf4_plan_info* out) {

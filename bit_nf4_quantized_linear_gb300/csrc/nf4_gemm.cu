@@ -399,6 +399,7 @@ __device__ __forceinline__ RawScale fetch_scale(const GemmArgs& a, int64_t n, in
   RawScale r{0.0f, 0u};
   if (n >= a.N_total || kb >= a.KB) return r;
   const int64_t b = n * a.KB + kb;
+  if (!in_bounds(n >= 0 && kb >= 0 && !a.chk_inject, a.status)) return r;
   if (!a.dq) {
     r.v = ldg_keep_f32(a.absmax + b);
   } else {
@@ -800,8 +801,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTAs (always the highest-index CTA on it) adds the partials of the lower
       // CTAs, from the nearest down, before rounding.  Waits only go to lower CTAs,
       // which are dispatched first, so the grid needs no co-residency.
-      const bool sk_part = a.sk && it.ks1 < a.ksteps;
-      const bool sk_own = a.sk && it.ks1 == a.ksteps && it.ks0 > 0;
+      // (checked build: the CTAs whose partial slots and flags this one touches,
+      // own_first .. unit with own_first >= 0, are CTAs of the launch)
+      const bool sk_in = !a.sk || in_bounds(unit >= 0 && unit < a.sk_ctas, a.status);
+      const bool sk_part = a.sk && sk_in && it.ks1 < a.ksteps;
+      const bool sk_own = a.sk && sk_in && it.ks1 == a.ksteps && it.ks0 > 0;
       int64_t own_first = unit;  // lowest CTA holding steps of an owned split tile
       if (sk_own) {
         const int64_t tile0 = it.idx * a.ksteps;
@@ -946,7 +950,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         it.col0 / 2 + row
                                   : nullptr;
         float* drw = (bwd && a.ep_drw) ? a.ep_drw + ((it.col0 >> 7) * 2 + q) * a.M + it.tok0 : nullptr;
-        const bool gate_ok = q < 2 && it.col0 / 2 + row < a.ncols / 2;
+        // (checked build: the item's tokens and this lane's output columns inside
+        // the output, and the routing-weight partial row inside its array)
+        const bool gate_ok =
+            q < 2 && it.col0 / 2 + row < a.ncols / 2 &&
+            in_bounds(it.tok0 >= 0 && it.tok_end <= a.M &&
+                          (bwd ? it.col0 + row + 64 < a.ld_out : it.col0 / 2 + row < a.ld_out) &&
+                          (!drw || ((it.col0 >> 7) * 2 + q) * 64 < a.N_e),
+                      a.status);
 #pragma unroll 1
         for (int c0 = 0; c0 < ntok && ep_ok; c0 += kBatch, ++xb) {
           uint32_t v[kBatch];
@@ -1020,8 +1031,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[j] = __float_as_uint(f);
             }
           }
-          if (col_ok) {
-            const int nj = ntok - c0;  // valid tokens in this batch when fewer than kWide
+          const int nj = ntok - c0;  // valid tokens in this batch when fewer than kWide
+          const int64_t tok_hi = it.tok0 + c0 + (nj < kWide ? nj : kWide);  // one past the batch's last token
+          if (col_ok && in_bounds(it.tok0 >= 0 && tok_hi <= a.M && col >= 0 &&
+                                      (a.splits > 1 ? it.split < a.splits : col < a.ld_out),
+                                  a.status)) {
             if (a.splits > 1) {
 #pragma unroll
               for (int j = 0; j < kWide; ++j)
@@ -1104,6 +1118,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) pkc[c] = nl * 128 + (((4 * j + c) ^ (nl & 7)) << 4);
     }
+    // Checked build: this thread's fixed offsets stay inside one decoded stage and
+    // one code stage (a failing thread skips its loads and stores).
+    const bool dec_in = in_bounds(
+        line_off >= 0 && line_off + 128 <= kAStage &&
+            (BITS == 4 ? (pk0 >= 0 && pk0 + 16 <= kPkStage && pk1 >= 0 && pk1 + 16 <= kPkStage)
+                       : (pkc[0] >= 0 && pkc[0] + 16 <= kPkStage && pkc[1] >= 0 && pkc[1] + 16 <= kPkStage &&
+                          pkc[2] >= 0 && pkc[2] + 16 <= kPkStage && pkc[3] >= 0 && pkc[3] + 16 <= kPkStage)),
+        a.status);
     // The statistics of this group's steps are fetched kAhead owned steps ahead
     // into a register ring (global-memory latency hides behind the decodes in
     // between).  A walker over (item, step) supplies them; q == kNoStep marks the
@@ -1155,14 +1177,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
       ring[kAhead - 1] = fetch_next();
       if (!wait_phase(bar_at(sh, kBarPFull + sp), php, sh, a)) break;
+      if (!in_bounds(sp < static_cast<uint32_t>(G::kStagesP) && sa < static_cast<uint32_t>(G::kStagesA) &&
+                         sx < static_cast<uint32_t>(G::kStagesX) && ms < static_cast<uint32_t>(G::kStagesX),
+                     a.status))
+        break;
       const uint8_t* pk = smem + G::kOffPk + sp * kPkStage;
-      uint4 wc[4];
+      uint4 wc[4] = {};
       Lut L;
       if (BITS == 4) {
-        wc[0] = *reinterpret_cast<const uint4*>(pk + pk0);
-        wc[1] = *reinterpret_cast<const uint4*>(pk + pk1);
+        if (dec_in) {
+          wc[0] = *reinterpret_cast<const uint4*>(pk + pk0);
+          wc[1] = *reinterpret_cast<const uint4*>(pk + pk1);
+        }
         L = make_lut<F16>(code2, s);
-      } else {
+      } else if (dec_in) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) wc[c] = *reinterpret_cast<const uint4*>(pk + pkc[c]);
       }
@@ -1172,7 +1200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
       }
       uint8_t* A = smem + G::kOffA + sa * kAStage + line_off;
-      if (BITS == 4) {
+      if (!dec_in) {
+        // (checked build: offsets outside the stage; nothing is written)
+      } else if (BITS == 4) {
         const uint32_t wv[8] = {wc[0].x, wc[0].y, wc[0].z, wc[0].w, wc[1].x, wc[1].y, wc[1].z, wc[1].w};
 #pragma unroll
         for (int c = 0; c < 8; ++c)

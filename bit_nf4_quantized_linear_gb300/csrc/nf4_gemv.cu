@@ -59,6 +59,7 @@ struct Raw {
 __device__ __forceinline__ Raw fetch_raw(const GemvArgs& a, int64_t n, int64_t kb) {
   const int64_t b = n * a.KB + kb;
   Raw r;
+  if (!in_bounds(b >= 0 && b < a.N * a.KB, a.status)) return Raw{0.0f, 0u};  // (checked build)
   if (!a.dq) {
     r.v = __ldg(a.absmax + b);
     r.q = 0;
@@ -113,7 +114,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_fwd_kernel(const GemvArg
     for (int i = 0; i < kSteps; ++i) {
       const int64_t n = n0 + r;
       const int64_t k = static_cast<int64_t>(s0 + i) * kStepK + lane * kChunk;
-      if (s0 + i < s1 && n < a.N && k < a.K) {
+      if (s0 + i < s1 && n < a.N && k < a.K &&
+          in_bounds(n >= 0 && k >= 0 && k / 2 + 16 <= row_bytes, a.status)) {
         w4[r][i] = __ldg(reinterpret_cast<const uint4*>(a.packed + n * row_bytes + k / 2));
         raw[r][i] = fetch_raw(a, n, k / 64);
       } else {
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_fwd_kernel(const GemvArg
     float v = red[g * kseg][r][m];
     for (int s = 1; s < kseg; ++s) v = __fadd_rn(v, red[g * kseg + s][r][m]);
     const int64_t n = static_cast<int64_t>(blockIdx.x) * rows_cta + rl;
-    if (n < a.N) a.out[(a.m0 + m) * a.ld_out + n] = __float2bfloat16_rn(v);
+    if (n < a.N && in_bounds(a.m0 + m < a.M && n < a.ld_out, a.status))
+      a.out[(a.m0 + m) * a.ld_out + n] = __float2bfloat16_rn(v);
   }
 }
 
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_dgrad_kernel(const GemvA
 #pragma unroll
       for (int r = 0; r < kBatch; ++r) {
         const int64_t n = nbase + r0 + r;
-        if (n < a.N) {
+        if (n < a.N && in_bounds(n >= 0 && k >= 0 && k / 2 + 16 <= row_bytes && a.m0 + MG <= a.M, a.status)) {
           w4[r] = __ldg(reinterpret_cast<const uint4*>(a.packed + n * row_bytes + k / 2));
           raw[r] = fetch_raw(a, n, k / 64);
 #pragma unroll
@@ -264,6 +267,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_dgrad_kernel(const GemvA
     const int ln = kk / kChunk, j = kk % kChunk;
     const int64_t kout = static_cast<int64_t>(kg) * kStepK + kk;
     if (kout >= a.K) continue;
+    if (!in_bounds(a.m0 + m < a.M && kout < a.ld_out, a.status)) continue;  // (checked build)
     float v = red[((0 * MG + m) * kChunk + j) * 33 + ln];
     for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[((w * MG + m) * kChunk + j) * 33 + ln]);
     if (a.ws)

@@ -189,6 +189,8 @@ struct Raw {
 
 __device__ __forceinline__ Raw fetch_raw(const SkinnyArgs& a, int64_t b, bool valid) {
   Raw r;
+  // (checked build: a valid block lies inside the statistics arrays)
+  if (valid && !in_bounds(b >= 0 && b < a.N * a.KB, a.status)) valid = false;
   const int64_t bi = valid ? b : 0;
   r.ok = valid;
   if (!a.dq) {
@@ -607,7 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto store = [&](int e, float v) {
     const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
     const int64_t n = (tile0 + i) * 16 + (r & 15);
-    if ((r >> 4) < M && n < a.N) store16<F16>(a.out + (r >> 4) * a.ld_out + n, v);
+    if ((r >> 4) < M && n < a.N && in_bounds(n >= 0 && n < a.ld_out, a.status))
+      store16<F16>(a.out + (r >> 4) * a.ld_out + n, v);
   };
   for (int e = threadIdx.x; e < total; e += kThreads) {
     const int i = e >> kSlotShift, r = e & (kSlotElems - 1);
@@ -878,7 +881,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* last = reinterpret_cast<const float*>(smem + L.ring);
   auto store = [&](int e, float v) {
     const int i = e / (M * 64), r = e - i * M * 64;
-    store16<F16>(a.out + (r >> 6) * a.ld_out + (col0 + i) * 64 + (r & 63), v);
+    const int64_t k = (col0 + i) * 64 + (r & 63);  // in-feature
+    if (in_bounds((r >> 6) < a.M && k >= 0 && k < a.K && k < a.ld_out, a.status))
+      store16<F16>(a.out + (r >> 6) * a.ld_out + k, v);
   };
   for (int e = threadIdx.x; e < total; e += kThreads) {
     const int i = e / (M * 64), r = e - i * M * 64;

@@ -57,7 +57,8 @@ typedef enum {
   NF4_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed              */
   NF4_ERR_TIMEOUT = 6,           /* a bounded device wait ran out (device status)    */
   NF4_ERR_UNSUPPORTED = 7,       /* no sm_100-family device, or feature not built    */
-  NF4_ERR_BAD_OFFSETS = 8        /* grouped: expert offsets not monotone / in range  */
+  NF4_ERR_BAD_OFFSETS = 8,       /* grouped: expert offsets not monotone / in range  */
+  NF4_ERR_BOUNDS = 9             /* checked build: an in-kernel index check failed   */
 } nf4_status;
 
 enum { NF4_DTYPE_F32 = 0, NF4_DTYPE_BF16 = 1 };
@@ -311,6 +312,16 @@ size_t nf4_workspace_size(int32_t op, int64_t M, int64_t N, int64_t K, int32_t E
 /* Static string naming a status code. */
 const char* nf4_status_string(nf4_status s);
 
+/* 1 when this library is the checked debug build (libnf4_checked.so, compiled
+ * with NF4_CHECKED=1), else 0.  The checked build tests the indices of the
+ * kernels' computed global and shared-memory accesses (statistics loads, the
+ * output, split and stream-K partial stores, the small-M kernels' loads and
+ * stores, the decoders' shared-memory offsets) before each access; an index
+ * outside its buffer skips that access and records NF4_ERR_BOUNDS in the device
+ * status word (nf4_device_status).  It stands in for a memory checker on devices
+ * where none can run; results are otherwise those of the normal build. */
+int32_t nf4_checked_build(void);
+
 /* Copies the NF4_NUM_PATHS host-side launch counters into out (host array of
  * NF4_NUM_PATHS entries). */
 void nf4_get_path_counters(uint64_t* out);
@@ -424,6 +435,15 @@ nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t s
  * hold, and exits normally; the device stays usable and later launches are
  * unaffected.  The affected call's output is unspecified. */
 void nf4_inject_stream_k_timeout(void);
+
+/* Failure-path test hook of the checked build (nf4_checked_build): one-shot for
+ * the next product launched on the fused tcgen05 kernel (nf4_linear_* at an M
+ * that takes it) by this process, whose statistics-load index checks then fail.
+ * Each such load is skipped (its block reads as scale 0; nothing is accessed out
+ * of range) and NF4_ERR_BOUNDS is recorded in the device status word; the kernel
+ * finishes normally and later launches are unaffected.  The affected call's
+ * output is unspecified.  No effect in the normal build. */
+void nf4_inject_bounds_failure(void);
 
 /* Human-readable message of the last CUDA error that made a call of this thread
  * return NF4_ERR_CUDA ("no error" if none).  Static string. */

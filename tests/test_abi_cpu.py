@@ -21,10 +21,22 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_checked_build_loads_and_exports_every_declared_symbol(L):
+    """The checked debug build (NF4_CHECKED=1: in-kernel index checks) is the same
+    C ABI; it reports itself as such and the normal build does not."""
+    path = build.build(checked=True)
+    C = ctypes.CDLL(path)
+    for n in _lib.header_functions():
+        assert hasattr(C, n), n
+    C.nf4_checked_build.restype = ctypes.c_int32
+    assert C.nf4_checked_build() == 1
+    assert L.nf4_checked_build() == 0
+
+
 def test_status_strings(L):
-    for code in range(9):
+    for code in range(10):
         s = L.nf4_status_string(code)
-        assert isinstance(s, bytes) and len(s) > 0
+        assert isinstance(s, bytes) and len(s) > 0 and s != b"unknown status"
     assert L.nf4_status_string(0) == b"ok"
 
 
