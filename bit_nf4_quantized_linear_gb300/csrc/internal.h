@@ -44,6 +44,35 @@ constexpr int kMaxExperts = 512;
 constexpr int kTileW = 128;  // rows of the dequantised operand per tile (MMA M)
 constexpr int kTileK = 64;   // contraction per pipeline stage (one 64-value block)
 
+// Multi-product launches (nf4_linear_fwd_multi / nf4_linear_dgrad_multi): up to
+// kMaxProds independent products with the same M and in-features K, each with its
+// own weight, activation and output, whose work items share one grid.
+constexpr int kMaxProds = 4;
+
+// One product of a multi-product launch.
+struct ProdArgs {
+  const float* absmax;
+  const uint8_t* absmax_q;
+  const float* nested_absmax;
+  const float* nested_offset;
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  int64_t N_total;  // rows of this weight
+  int64_t ncols;    // output columns (forward: this weight's rows; input gradient: K)
+  int ksteps;       // contraction steps of an item
+  int wtiles;       // tiles over the output columns
+  int64_t item0;    // first item of this product in the launch's item order
+};
+
+// Tensor maps of a launch: activations, packed codes and output, one per product
+// (N = 1 for single-product launches).
+template <int N>
+struct MapSet {
+  CUtensorMap act[N];
+  CUtensorMap pk[N];
+  CUtensorMap out[N];
+};
+
 // Parameters of the fused product kernel (everything but the tensor maps).
 struct GemmArgs {
   int64_t M;        // activation rows (dense) or T (grouped)
@@ -109,6 +138,11 @@ struct GemmArgs {
   uint64_t sk_wait_xor; // the finishing CTA waits for sk_epoch ^ sk_wait_xor (0; the
                         // failure-path test sets a bit no contributor publishes)
   int chk_inject;       // checked build: fail the statistics-load index check (test hook)
+  // Multi-product launches: nprod products (items of product p from prod[p].item0),
+  // classic schedule, no splits; the single-product fields above are unused for
+  // the per-product quantities.
+  int nprod;
+  ProdArgs prod[kMaxProds];
 };
 
 // Stream-K workspace: partial tiles, then the ready flags (8 bytes per CTA and row
@@ -210,6 +244,10 @@ int64_t gemv_dgrad_row_groups(int64_t N);
 // tmap_out: 16-bit output [M, ncols] with a 32 x 32 box, used when a.tma_out is set.
 // bits: code width of the weight (4, or 8 with bt <= 128).  f16: fp16 activations,
 // operand and output instead of bf16 (4-bit codes).
+// Multi-product launch (a.nprod products, bf16, 4-bit codes, bt 128 or 256,
+// classic schedule); maps.act/pk/out[p] are product p's tensor maps.
+cudaError_t launch_gemm_multi(int mode, int bt, const GemmArgs& a, const MapSet<kMaxProds>& maps, int grid,
+                              cudaStream_t s);
 cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,
                         const CUtensorMap& tmap_act, const CUtensorMap& tmap_packed,
                         const CUtensorMap& tmap_out, int grid, cudaStream_t s);

@@ -11,6 +11,8 @@
 #include <cstring>
 #include <cstdlib>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "nf4.h"
@@ -680,6 +682,135 @@ nf4_status run_grouped(int mode, const void* act, const int32_t* offsets, int32_
   return NF4_OK;
 }
 
+// Multi-product launch (nf4_linear_fwd_multi / nf4_linear_dgrad_multi).
+nf4_status run_multi(int mode, int32_t nprod, const void* const* act, int64_t M, const int64_t* ld_act,
+                     const nf4_weight* const* w, void* const* out, const int64_t* ld_out, void* stream) {
+  if (nprod < 1 || nprod > nf4::kMaxProds || !act || !ld_act || !w || !out || !ld_out || M < 0)
+    return NF4_ERR_INVALID_ARG;
+  int64_t K = -1;
+  for (int p = 0; p < nprod; ++p) {
+    nf4_status st = check_weight(w[p]);
+    if (st != NF4_OK) return st;
+    if (w[p]->bits == 8) return NF4_ERR_UNSUPPORTED;
+    if (p == 0) K = w[p]->K;
+    if (w[p]->K != K || w[p]->double_quant != w[0]->double_quant || w[p]->code4 != w[0]->code4 ||
+        (w[0]->double_quant && w[p]->code8 != w[0]->code8))
+      return NF4_ERR_INVALID_ARG;
+    const int64_t act_cols = mode == 0 ? K : w[p]->N;
+    const int64_t out_cols = mode == 0 ? w[p]->N : K;
+    if (ld_act[p] < act_cols || ld_out[p] < out_cols) return NF4_ERR_INVALID_ARG;
+    if (w[p]->N > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (K % 64 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return NF4_OK;
+  for (int p = 0; p < nprod; ++p) {
+    if (!act[p] || !out[p]) return NF4_ERR_INVALID_ARG;
+    if (ld_act[p] % 8 != 0 || ld_out[p] % 8 != 0 || !aligned16(act[p]) || !aligned16(out[p]) ||
+        !aligned16(w[p]->packed))
+      return NF4_ERR_ALIGNMENT;
+  }
+  if (M > INT32_MAX || K > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
+  DevInfo dev;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
+  if (!dev.supported) return NF4_ERR_UNSUPPORTED;
+  // Products in order of decreasing contraction (longest items dealt first).
+  int order[nf4::kMaxProds];
+  for (int p = 0; p < nprod; ++p) order[p] = p;
+  auto ksteps_of = [&](int p) { return mode == 0 ? K / 64 : (w[p]->N + 63) / 64; };
+  auto wtiles_of = [&](int p) { return ((mode == 0 ? w[p]->N : K) + nf4::kTileW - 1) / nf4::kTileW; };
+  for (int i = 1; i < nprod; ++i)
+    for (int j = i; j > 0 && ksteps_of(order[j]) > ksteps_of(order[j - 1]); --j) std::swap(order[j], order[j - 1]);
+  // Token tile: the busiest CTA of the classic round-robin deal, in SM clocks.
+  int best_bt = 128;
+  double best = 1e300;
+  for (int bt : {256, 128}) {
+    const int64_t ttiles = (M + bt - 1) / bt;
+    int64_t total = 0;
+    for (int i = 0; i < nprod; ++i) total += ttiles * wtiles_of(order[i]);
+    const int64_t grid = total < dev.sms ? total : dev.sms;
+    std::vector<int64_t> steps(static_cast<size_t>(grid), 0);
+    int64_t idx = 0;
+    for (int i = 0; i < nprod; ++i) {
+      const int64_t n = ttiles * wtiles_of(order[i]);
+      for (int64_t k = 0; k < n; ++k, ++idx) {  // the kernel's deal: odd rounds in reverse
+        const int64_t r = idx / grid, pos = idx % grid;
+        steps[static_cast<size_t>((r & 1) ? grid - 1 - pos : pos)] += ksteps_of(order[i]);
+      }
+    }
+    int64_t busiest = 0;
+    for (int64_t v : steps) busiest = v > busiest ? v : busiest;
+    const double cost = static_cast<double>(busiest) * step_cycles(bt);
+    if (cost < best * 0.999) {
+      best = cost;
+      best_bt = bt;
+    }
+  }
+  const int bt = best_bt;
+  const int64_t ttiles = (M + bt - 1) / bt;
+  nf4::GemmArgs a{};
+  nf4::MapSet<nf4::kMaxProds> maps;
+  std::memset(&maps, 0, sizeof(maps));
+  int64_t item0 = 0;
+  for (int i = 0; i < nprod; ++i) {
+    const int p = order[i];
+    const nf4_weight* wp = w[p];
+    nf4::ProdArgs& pa = a.prod[i];
+    pa.absmax = wp->absmax;
+    pa.absmax_q = wp->absmax_q;
+    pa.nested_absmax = wp->nested_absmax;
+    pa.nested_offset = wp->nested_offset;
+    pa.out = static_cast<__nv_bfloat16*>(out[p]);
+    pa.ld_out = ld_out[p];
+    pa.N_total = wp->N;
+    pa.ncols = mode == 0 ? wp->N : K;
+    pa.ksteps = static_cast<int>(ksteps_of(p));
+    pa.wtiles = static_cast<int>(wtiles_of(p));
+    pa.item0 = item0;
+    item0 += ttiles * pa.wtiles;
+    const int64_t act_cols = mode == 0 ? K : wp->N;
+    const int64_t out_cols = mode == 0 ? wp->N : K;
+    if (!encode_2d(&maps.act[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, act[p], act_cols, M, ld_act[p] * 2, 64, bt,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_codes(&maps.pk[i], wp, mode) ||
+        !encode_2d(&maps.out[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out[p], out_cols, M, ld_out[p] * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+  }
+  if (item0 > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
+  a.M = M;
+  a.K = K;
+  a.KB = K / 64;
+  a.ncols = a.prod[0].ncols;
+  a.N_total = a.prod[0].N_total;
+  a.N_e = a.prod[0].N_total;
+  a.ksteps = a.prod[0].ksteps;
+  a.wtiles = a.prod[0].wtiles;
+  a.ttiles = static_cast<int>(ttiles);
+  a.splits = 1;
+  a.total_items = item0;
+  a.grouped = 0;
+  a.E = 1;
+  a.absmax = a.prod[0].absmax;
+  a.absmax_q = a.prod[0].absmax_q;
+  a.nested_absmax = a.prod[0].nested_absmax;
+  a.nested_offset = a.prod[0].nested_offset;
+  a.code4 = w[0]->code4;
+  a.code8 = w[0]->code8;
+  a.dq = w[0]->double_quant;
+  a.out = a.prod[0].out;
+  a.ld_out = a.prod[0].ld_out;
+  a.status = dev.status;
+  a.prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+  a.tma_out = 1;
+  a.nprod = nprod;
+  a.chk_inject = g_inject_bounds.exchange(0, std::memory_order_relaxed);
+  const int grid = static_cast<int>(item0 < dev.sms ? item0 : dev.sms);
+  cudaError_t le = nf4::launch_gemm_multi(mode, bt, a, maps, grid, static_cast<cudaStream_t>(stream));
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+  count(NF4_PATH_MULTI);
+  return NF4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -874,6 +1005,17 @@ const char* nf4_status_string(nf4_status s) {
 }
 
 int32_t nf4_checked_build(void) { return NF4_CHECKED ? 1 : 0; }
+
+nf4_status nf4_linear_fwd_multi(int32_t nprod, const void* const* x, int64_t M, const int64_t* ldx,
+                                const nf4_weight* const* w, void* const* y, const int64_t* ldy, void* stream) {
+  return run_multi(0, nprod, x, M, ldx, w, y, ldy, stream);
+}
+
+nf4_status nf4_linear_dgrad_multi(int32_t nprod, const void* const* gy, int64_t M, const int64_t* ldgy,
+                                  const nf4_weight* const* w, void* const* gx, const int64_t* ldgx,
+                                  void* stream) {
+  return run_multi(1, nprod, gy, M, ldgy, w, gx, ldgx, stream);
+}
 
 void nf4_get_path_counters(uint64_t* out) {
   if (!out) return;

@@ -158,6 +158,7 @@ struct Item {
   int64_t col0;   // first output column of the tile
   int ks0, ks1;   // contraction steps of this segment of the item
   int split;
+  int p;          // product of a multi-product launch (0 otherwise)
 };
 
 struct Shared {
@@ -292,10 +293,32 @@ __device__ __noinline__ bool flag_wait(const uint64_t* f, uint64_t v, const Shar
   }
 }
 
-template <int MODE, int BT>
+template <int MODE, int BT, bool MULTI>
 __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const Shared& sh) {
   Item it;
   it.idx = idx;
+  it.p = 0;
+  if constexpr (MULTI) {
+    // Multi-product launch: the product holding item idx, then its (token tile,
+    // weight tile); whole items (no splits), one 128-row weight tile each.
+    int p = 0;
+#pragma unroll
+    for (int q = 1; q < kMaxProds; ++q)
+      if (q < a.nprod && idx >= a.prod[q].item0) p = q;
+    const int r = static_cast<int>(idx - a.prod[p].item0);  // (items of a launch fit in 32 bits)
+    const int wtiles = a.prod[p].wtiles;
+    const int wt = r % wtiles;
+    const int tt = r / wtiles;
+    it.p = p;
+    it.tok0 = static_cast<int64_t>(tt) * BT;
+    it.tok_end = min(a.M, it.tok0 + BT);
+    it.ks0 = 0;
+    it.ks1 = a.prod[p].ksteps;
+    it.split = 0;
+    it.col0 = static_cast<int64_t>(wt) * kTileW;
+    it.wrow0 = (MODE == 0) ? it.col0 : 0;
+    return it;
+  }
   if (!a.grouped) {
     const int64_t s = idx % a.splits;
     const int64_t r = idx / a.splits;
@@ -342,31 +365,44 @@ __device__ __forceinline__ Item get_item(int64_t idx, const GemmArgs& a, const S
 // CTA walks the same sequence.
 struct Cursor {
   int64_t pos, end;  // stream-K: the run's first step and the end of what is left
+  int64_t unit;      // multi-product launches: this CTA (pos counts its rounds)
 };
 
 __device__ __forceinline__ int64_t sk_first_unit(const GemmArgs& a, int64_t cta) {
   return cta * a.sk_units / a.sk_ctas;
 }
 
+template <bool MULTI>
 __device__ __forceinline__ Cursor cursor_begin(const GemmArgs& a, int64_t unit,
                                                int64_t total_items) {
-  if (a.sk) return Cursor{sk_first_unit(a, unit), sk_first_unit(a, unit + 1)};
-  return Cursor{unit, total_items};
+  if (MULTI) return Cursor{0, total_items, unit};
+  if (a.sk) return Cursor{sk_first_unit(a, unit), sk_first_unit(a, unit + 1), unit};
+  return Cursor{unit, total_items, unit};
 }
 
-template <int MODE, int BT>
+template <int MODE, int BT, bool MULTI>
 __device__ __forceinline__ bool cursor_next(Cursor& c, const GemmArgs& a, const Shared& sh,
                                             int64_t nunits, Item& it) {
+  if constexpr (MULTI) {
+    // Multi-product launches deal whole items in rounds of nunits, odd rounds in
+    // reverse CTA order (the items come longest first, so a CTA that took a long
+    // item in one round takes a short one in the next).
+    const int64_t idx = c.pos * nunits + ((c.pos & 1) ? nunits - 1 - c.unit : c.unit);
+    if (idx >= c.end) return false;
+    ++c.pos;
+    it = get_item<MODE, BT, MULTI>(idx, a, sh);
+    return true;
+  }
   if (c.pos >= c.end) return false;
   if (!a.sk) {
-    it = get_item<MODE, BT>(c.pos, a, sh);
+    it = get_item<MODE, BT, MULTI>(c.pos, a, sh);
     c.pos += nunits;
     return true;
   }
   const int64_t idx = (c.end - 1) / a.ksteps;  // last item with steps left
   const int64_t tile0 = idx * a.ksteps;
   const int64_t seg0 = c.pos > tile0 ? c.pos : tile0;
-  it = get_item<MODE, BT>(idx, a, sh);
+  it = get_item<MODE, BT, MULTI>(idx, a, sh);
   it.ks0 = static_cast<int>(seg0 - tile0);
   it.ks1 = static_cast<int>(c.end - tile0);
   c.end = seg0;
@@ -395,24 +431,32 @@ __device__ __forceinline__ uint32_t ldg_keep_u8(const uint8_t* p) {
   return v;
 }
 
-__device__ __forceinline__ RawScale fetch_scale(const GemmArgs& a, int64_t n, int64_t kb) {
-  RawScale r{0.0f, 0u};
-  if (n >= a.N_total || kb >= a.KB) return r;
+// Multi-product launches: the statistics of product p, whose index travels in
+// bits 8.. of q.
+template <bool MULTI>
+__device__ __forceinline__ RawScale fetch_scale(const GemmArgs& a, int p, int64_t n, int64_t kb) {
+  RawScale r{0.0f, MULTI ? static_cast<uint32_t>(p) << 8 : 0u};
+  const int64_t N_total = MULTI ? a.prod[p].N_total : a.N_total;
+  if (n >= N_total || kb >= a.KB) return r;
   const int64_t b = n * a.KB + kb;
   if (!in_bounds(n >= 0 && kb >= 0 && !a.chk_inject, a.status)) return r;
   if (!a.dq) {
-    r.v = ldg_keep_f32(a.absmax + b);
+    r.v = ldg_keep_f32((MULTI ? a.prod[p].absmax : a.absmax) + b);
   } else {
-    r.q = ldg_keep_u8(a.absmax_q + b);
-    r.v = ldg_keep_f32(a.nested_absmax + (b >> 8));
+    r.q |= ldg_keep_u8((MULTI ? a.prod[p].absmax_q : a.absmax_q) + b);
+    r.v = ldg_keep_f32((MULTI ? a.prod[p].nested_absmax : a.nested_absmax) + (b >> 8));
   }
   return r;
 }
 
-// Decoded block scale: absmax, or fp32(fp32(code8[q] * nested) + offset).
+// Decoded block scale: absmax, or fp32(fp32(code8[q] * nested) + offset), with the
+// nested offset of the block's product (multi-product launches: offsets_s[p], in
+// shared memory).
+template <bool MULTI>
 __device__ __forceinline__ float finish_scale(const GemmArgs& a, const float* code8_s,
-                                              const RawScale& r, float offset) {
+                                              const RawScale& r, float offset, const float* offsets_s) {
   if (!a.dq) return r.v;
+  if constexpr (MULTI) return __fadd_rn(__fmul_rn(code8_s[r.q & 255u], r.v), offsets_s[r.q >> 8]);
   return __fadd_rn(__fmul_rn(code8_s[r.q], r.v), offset);
 }
 
@@ -535,12 +579,15 @@ __device__ __forceinline__ void cs_epilogue(const GemmArgs& a, const Shared& sh,
   }
 }
 
-template <int MODE, int BT, int BITS, bool F16>
+// MULTI: a multi-product launch (tensor maps and statistics per product).
+template <int MODE, int BT, int BITS, bool F16, bool MULTI = false>
 __global__ void __launch_bounds__(kThreads, 1)
-    nf4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act,
-                    const __grid_constant__ CUtensorMap tmap_pk,
-                    const __grid_constant__ CUtensorMap tmap_out, const GemmArgs a) {
+    nf4_gemm_kernel(const __grid_constant__ MapSet<MULTI ? kMaxProds : 1> tm, const GemmArgs a) {
   using G = Geo<BT, BITS>;
+  static_assert(!MULTI || (BT <= 256 && BITS == 4), "multi-product launches: single-CTA tiles, 4-bit codes");
+  const CUtensorMap& tmap_act = tm.act[0];
+  const CUtensorMap& tmap_pk = tm.pk[0];
+  const CUtensorMap& tmap_out = tm.out[0];
   constexpr int kPkStage = G::kPkStage;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -610,8 +657,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *dep_done(sh) = early ? 0 : 1;
     fence_mbar_init();
   }
-  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tmap_pk);
-  if (warp == kWarpTmaX && lane == 0) prefetch_tensormap(&tmap_act);
+  if (warp == kWarpTma && lane == 0)
+    for (int p = 0; p < (MULTI ? a.nprod : 1); ++p) prefetch_tensormap(&tm.pk[p]);
+  if (warp == kWarpTmaX && lane == 0)
+    for (int p = 0; p < (MULTI ? a.nprod : 1); ++p) prefetch_tensormap(&tm.act[p]);
   if (warp == kWarpMma) {
     if (kPair) {
       tmem_alloc_pair(smem_addr(sh.tmem_slot), G::kTmemCols);
@@ -667,9 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = is_pk ? kPkStage : G::kXStage;
       uint32_t st = 0, ph = 0, issued = 0, par = 0;
       bool ok = true;
-      Cursor cur = cursor_begin(a, unit, total_items);
+      Cursor cur = cursor_begin<MULTI>(a, unit, total_items);
       Item it;
-      while (ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it)) {
+      while (ok && cursor_next<MODE, BT, MULTI>(cur, a, sh, nunits, it)) {
         for (int ks = it.ks0; ks < it.ks1; ++ks) {
           if (!wait_phase(bar_at(sh, bar_empty + st), ph ^ 1u, sh, a)) { ok = false; break; }
           const uint32_t full = bar_at(sh, bar_full + st);
@@ -678,14 +727,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Pairs: this CTA's 128 tokens of each 256-token half of the tile.
 #pragma unroll
             for (int h = 0; h < G::kXParts; ++h)
-              tma_load_2d(sbase + G::kOffX + st * G::kXStage + h * (G::kXStage / G::kXParts), &tmap_act,
+              tma_load_2d(sbase + G::kOffX + st * G::kXStage + h * (G::kXStage / G::kXParts), &tm.act[MULTI ? it.p : 0],
                           full, ks * kTileK,
                           static_cast<int32_t>(it.tok0 + (kPair ? 256 * h + 128 * static_cast<int>(sh.rank) : 0)));
           } else if (MODE == 0)
-            tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full, ks * (kTileK * BITS / 8),
+            tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tm.pk[MULTI ? it.p : 0], full, ks * (kTileK * BITS / 8),
                         static_cast<int32_t>(it.wrow0));
           else
-            tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tmap_pk, full,
+            tma_load_2d(sbase + G::kOffPk + st * kPkStage, &tm.pk[MULTI ? it.p : 0], full,
                         static_cast<int32_t>(it.col0 * BITS / 8),
                         static_cast<int32_t>(it.wrow0 + static_cast<int64_t>(ks) * kTileK));
           issued |= 1u << st;
@@ -724,9 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sx = 0, phx = 0, sa = 0, pha = 0;
       int acc_i = 0;
       bool ok = true;
-      Cursor cur = cursor_begin(a, unit, total_items);
+      Cursor cur = cursor_begin<MULTI>(a, unit, total_items);
       Item it;
-      for (; ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it); ++acc_i) {
+      for (; ok && cursor_next<MODE, BT, MULTI>(cur, a, sh, nunits, it); ++acc_i) {
         const int ab = acc_i % G::kAccBufs;
         const uint32_t acc_ph = (acc_i / G::kAccBufs) & 1;
         if (!wait_in(kBarAccEmpty + ab, acc_ph ^ 1u)) break;
@@ -783,9 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc_i = 0;
     uint32_t xb = 0;    // SwiGLU exchange batches so far (barrier phases)
     bool ep_ok = true;  // false once an exchange wait gave up
-    Cursor cur = cursor_begin(a, unit, total_items);
+    Cursor cur = cursor_begin<MULTI>(a, unit, total_items);
     Item it;
-    for (; ep_ok && cursor_next<MODE, BT>(cur, a, sh, nunits, it); ++acc_i) {
+    for (; ep_ok && cursor_next<MODE, BT, MULTI>(cur, a, sh, nunits, it); ++acc_i) {
       const int ab = acc_i % G::kAccBufs;
       const uint32_t acc_ph = (acc_i / G::kAccBufs) & 1;
       if (kPair ? !wait_phase_cluster(bar_at(sh, kBarAccFull + ab), acc_ph, sh, a)
@@ -793,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       tc_fence_after();
       const int64_t col = it.col0 + row;
-      const bool col_ok = col < a.ncols;
+      const bool col_ok = col < (MULTI ? a.prod[it.p].ncols : a.ncols);
       const int ntok = static_cast<int>(it.tok_end - it.tok0);  // tokens in this tile (<= BT)
       // Stream-K: a segment that stops before the tile's last step publishes its
       // fp32 partial (this warp's quarter of the rows, lane-contiguous per token) in
@@ -925,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmap_out, stg_addr, static_cast<int32_t>(it.col0 + 32 * q),
+            tma_store_2d(&tm.out[MULTI ? it.p : 0], stg_addr, static_cast<int32_t>(it.col0 + 32 * q),
                          static_cast<int32_t>(it.tok0 + c0));
             bulk_commit_group();
           }
@@ -1015,7 +1064,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Direct stores, one token row per element: y / gx in bf16, or this split's
         // fp32 partials.  Grouped forward epilogue: bias per weight row, scale per
         // output row.
-        uint16_t* op = reinterpret_cast<uint16_t*>(a.out) + it.tok0 * a.ld_out + col;
+        const int64_t ld_out = MULTI ? a.prod[it.p].ld_out : a.ld_out;
+        uint16_t* op = reinterpret_cast<uint16_t*>(MULTI ? a.prod[it.p].out : a.out) + it.tok0 * ld_out + col;
         float* wp = a.ws + (static_cast<int64_t>(it.split) * a.M + it.tok0) * a.ncols + col;
         const float bias = MODE == 0 && a.ep_bias && col_ok ? __ldg(a.ep_bias + it.wrow0 + row) : 0.0f;
 #pragma unroll 1
@@ -1034,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nj = ntok - c0;  // valid tokens in this batch when fewer than kWide
           const int64_t tok_hi = it.tok0 + c0 + (nj < kWide ? nj : kWide);  // one past the batch's last token
           if (col_ok && in_bounds(it.tok0 >= 0 && tok_hi <= a.M && col >= 0 &&
-                                      (a.splits > 1 ? it.split < a.splits : col < a.ld_out),
+                                      (a.splits > 1 ? it.split < a.splits : col < ld_out),
                                   a.status)) {
             if (a.splits > 1) {
 #pragma unroll
@@ -1043,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int j = 0; j < kWide; ++j)
-                if (j < nj) op[static_cast<int64_t>(c0 + j) * a.ld_out] = to16<F16>(__uint_as_float(v[j]));
+                if (j < nj) op[static_cast<int64_t>(c0 + j) * ld_out] = to16<F16>(__uint_as_float(v[j]));
             }
           }
         }
@@ -1075,7 +1125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dw = warp - kWarpDec0;
     const int grp = dw >> 2;
     const int rb = ((dw & 3) << 5) | lane;     // row-block 0..127
-    const float offset = a.dq ? __ldg(a.nested_offset) : 0.0f;
+    const float offset = (a.dq && !MULTI) ? __ldg(a.nested_offset) : 0.0f;
     uint64_t code2[8];
     if (BITS == 4) {
 #pragma unroll
@@ -1089,6 +1139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* valtab = reinterpret_cast<float*>(smem + G::kOffMisc + kMiscBase);
     const int dtid = dw * 32 + lane;
     if (a.dq && dtid < 256) sh.code8[dtid] = __ldg(a.code8 + dtid);
+    // Multi-product launches: the products' nested offsets in shared memory (the
+    // expert table's words, unused by these launches).
+    float* offsets_s = reinterpret_cast<float*>(sh.starts);
+    if (MULTI && a.dq && dtid < a.nprod) offsets_s[dtid] = __ldg(a.prod[dtid].nested_offset);
     if (BITS == 8)
       for (int i = dtid; i < 256 * 32; i += kNumDecWarps * 32) valtab[i] = __ldg(a.code4 + (i >> 5));
     const float* vt = valtab + lane;  // this lane's copy: entry e at vt[32 e]
@@ -1132,15 +1186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // end of the CTA's sequence.
     constexpr uint32_t kNoStep = 0xffffffffu;
     constexpr int kAhead = 3;
-    Cursor fcur = cursor_begin(a, unit, total_items);
+    Cursor fcur = cursor_begin<MULTI>(a, unit, total_items);
     Item fit{};
-    bool fvalid = cursor_next<MODE, BT>(fcur, a, sh, nunits, fit);
+    bool fvalid = cursor_next<MODE, BT, MULTI>(fcur, a, sh, nunits, fit);
     int fks = fit.ks0;
     auto walk = [&](int n) {  // advance the walker n steps
       fks += n;
       while (fvalid && fks >= fit.ks1) {
         const int over = fks - fit.ks1;
-        fvalid = cursor_next<MODE, BT>(fcur, a, sh, nunits, fit);
+        fvalid = cursor_next<MODE, BT, MULTI>(fcur, a, sh, nunits, fit);
         if (fvalid) fks = fit.ks0 + over;
       }
     };
@@ -1155,7 +1209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           n = fit.wrow0 + static_cast<int64_t>(fks) * kTileK + (rb & 63);
           kb = (fit.col0 >> 6) + (rb >> 6);
         }
-        r = fetch_scale(a, n, kb);
+        r = fetch_scale<MULTI>(a, fit.p, n, kb);
         walk(kDecGroups);
       }
       return r;
@@ -1172,7 +1226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int m = grp - G::kStagesA;
     uint32_t ms = 0, mph = 0;
     while (ring[0].q != kNoStep) {
-      const float s = finish_scale(a, sh.code8, ring[0], offset);
+      const float s = finish_scale<MULTI>(a, sh.code8, ring[0], offset, offsets_s);
 #pragma unroll
       for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
       ring[kAhead - 1] = fetch_next();
@@ -1391,8 +1445,38 @@ cudaError_t launch_one(const GemmArgs& a, const CUtensorMap& ta, const CUtensorM
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cluster > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tp, to, a);
+  MapSet<1> maps;
+  maps.act[0] = ta;
+  maps.pk[0] = tp;
+  maps.out[0] = to;
+  return cudaLaunchKernelEx(&cfg, kern, maps, a);
 }
+
+#if NF4_GEMM_MAIN_TU
+// A multi-product launch (classic schedule, no clusters).
+template <int MODE, int BT>
+cudaError_t launch_multi_one(const GemmArgs& a, const MapSet<kMaxProds>& maps, int grid, cudaStream_t s) {
+  static bool configured = false;
+  auto kern = nf4_gemm_kernel<MODE, BT, 4, false, true>;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Geo<BT, 4>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Geo<BT, 4>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps, a);
+}
+#endif
 
 template <int MODE>
 cudaError_t launch_mode(int bt, const GemmArgs& a, const CUtensorMap& ta, const CUtensorMap& tp,
@@ -1516,6 +1600,19 @@ int gemm_cluster_capacity(int mode, int bt, int cs) {
   }
   if (used < 64) cache[used++] = Entry{dev, mode, bt, cs, n};
   return n;
+}
+
+cudaError_t launch_gemm_multi(int mode, int bt, const GemmArgs& a, const MapSet<kMaxProds>& maps, int grid,
+                              cudaStream_t s) {
+  if (a.nprod < 1 || a.nprod > kMaxProds || a.sk || a.cs > 1 || a.splits != 1 || a.grouped)
+    return cudaErrorInvalidValue;
+  switch (mode * 1000 + bt) {
+    case 128: return launch_multi_one<0, 128>(a, maps, grid, s);
+    case 256: return launch_multi_one<0, 256>(a, maps, grid, s);
+    case 1128: return launch_multi_one<1, 128>(a, maps, grid, s);
+    case 1256: return launch_multi_one<1, 256>(a, maps, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_gemm(int mode, int bt, int bits, bool f16, const GemmArgs& a,

@@ -102,11 +102,13 @@ def quantize(W: torch.Tensor, double_quant: bool = True, code4: Optional[torch.T
     N, K = W.shape
     numel = N * K
     nblocks = (numel + BLOCKSIZE - 1) // BLOCKSIZE
-    code4 = (codebooks.code_for(quant_type) if code4 is None else code4).to(dev, torch.float32).contiguous()
+    code4 = (_device_codebook(quant_type, dev, lambda: codebooks.code_for(quant_type)) if code4 is None
+             else code4.to(dev, torch.float32).contiguous())
     if code4.numel() not in (16, 256):
         raise ValueError("quantize: the value codebook must have 16 or 256 levels")
     bits = 8 if code4.numel() == 256 else 4
-    code8 = (codebooks.dynamic_code8() if code8 is None else code8).to(dev, torch.float32).contiguous()
+    code8 = (_device_codebook("dynamic8", dev, codebooks.dynamic_code8) if code8 is None
+             else code8.to(dev, torch.float32).contiguous())
     packed = torch.empty(numel if bits == 8 else (numel + 1) // 2, dtype=torch.uint8, device=dev)
     absmax = torch.empty(nblocks, dtype=torch.float32, device=dev)
     absmax_q = nested = offset = ws = None
@@ -143,6 +145,21 @@ def dequantize(w: NF4Weight, dtype: torch.dtype = torch.bfloat16,
     _lib.check(_lib.lib().nf4_dequantize(ctypes.byref(s), _ptr(out), code, _stream()),
                "nf4_dequantize")
     return out
+
+
+_CODEBOOKS = {}
+
+
+def _device_codebook(kind: str, dev: torch.device, make) -> torch.Tensor:
+    """One read-only device copy of a default codebook per device, shared by every
+    weight quantised with it (so that weights can share a multi-product launch,
+    which takes one codebook)."""
+    key = (kind, str(dev))
+    t = _CODEBOOKS.get(key)
+    if t is None:
+        t = make().to(dev, torch.float32).contiguous()
+        _CODEBOOKS[key] = t
+    return t
 
 
 def _check_act(name, a: torch.Tensor, cols: int, f16_ok: bool = False):
@@ -191,6 +208,46 @@ def linear_dgrad(gy: torch.Tensor, w: NF4Weight, out: Optional[torch.Tensor] = N
             gx.stride(0), _ptr(ws) if need else None, need, _stream())
     _lib.check(rc, "nf4_linear_dgrad")
     return gx
+
+
+def _multi(name, fn, acts, ws, outs, out_cols):
+    n = len(ws)
+    if not 1 <= n <= MAX_MULTI or len(acts) != n:
+        raise ValueError(f"{name}: 1..{MAX_MULTI} products, one activation per weight")
+    M = acts[0].shape[0]
+    if outs is None:
+        outs = [torch.empty(M, out_cols(w), dtype=torch.bfloat16, device=acts[0].device) for w in ws]
+    if len(outs) != n:
+        raise ValueError(f"{name}: one output per weight")
+    structs = [w.struct() for w in ws]
+    P = ctypes.c_void_p
+    a_arr = (P * n)(*[a.data_ptr() for a in acts])
+    o_arr = (P * n)(*[o.data_ptr() for o in outs])
+    la = (ctypes.c_int64 * n)(*[a.stride(0) for a in acts])
+    lo = (ctypes.c_int64 * n)(*[o.stride(0) for o in outs])
+    w_arr = (P * n)(*[ctypes.addressof(st) for st in structs])
+    rc = fn(n, a_arr, M, la, w_arr, o_arr, lo, _stream())
+    _lib.check(rc, name)
+    return outs
+
+
+MAX_MULTI = 4  # NF4_MAX_MULTI of include/nf4.h
+
+
+def linear_fwd_multi(xs, ws, outs=None):
+    """nf4_linear_fwd_multi: y[p] = xs[p] W[p]^T for up to four weights in one launch
+    (bf16; the same M and K; xs may repeat one tensor).  Returns the list of y."""
+    for x, w in zip(xs, ws):
+        _check_act("linear_fwd_multi", x, w.K)
+    return _multi("nf4_linear_fwd_multi", _lib.lib().nf4_linear_fwd_multi, xs, ws, outs, lambda w: w.N)
+
+
+def linear_dgrad_multi(gys, ws, outs=None):
+    """nf4_linear_dgrad_multi: gx[p] = gys[p] W[p] for up to four weights in one
+    launch (bf16; the same M and K).  Returns the list of gx."""
+    for gy, w in zip(gys, ws):
+        _check_act("linear_dgrad_multi", gy, w.N)
+    return _multi("nf4_linear_dgrad_multi", _lib.lib().nf4_linear_dgrad_multi, gys, ws, outs, lambda w: w.K)
 
 
 def grouped_fwd(x: torch.Tensor, offsets: torch.Tensor, w: NF4Weight, experts: int,

@@ -90,7 +90,8 @@ enum {
   NF4_PATH_SKINNY_DGRAD = 11,/* small-M tensor-core input gradient         */
   NF4_PATH_STREAM_K = 12,    /* fused launch with the stream-K schedule     */
   NF4_PATH_CLUSTER_SPLIT = 13,/* fused launch with the cluster split         */
-  NF4_NUM_PATHS = 14
+  NF4_PATH_MULTI = 14,       /* multi-product fused launch                  */
+  NF4_NUM_PATHS = 15
 };
 
 /* A quantised weight: the tensors of the pages' QuantState as plain device
@@ -198,6 +199,33 @@ nf4_status nf4_linear_fwd(const void* x, int64_t M, int64_t ldx, const nf4_weigh
  *   NF4_OP_LINEAR_DGRAD. */
 nf4_status nf4_linear_dgrad(const void* gy, int64_t M, int64_t ldgy, const nf4_weight* w, void* gx,
                             int64_t ldgx, void* ws, size_t ws_bytes, void* stream);
+
+/* nf4_linear_fwd_multi / nf4_linear_dgrad_multi -- up to NF4_MAX_MULTI
+ * independent products of nf4_linear_fwd / nf4_linear_dgrad in ONE launch of the
+ * fused tcgen05 kernel, for products that become ready together (for instance
+ * the q, k and v projections of one input, or gate and up): product p computes
+ *   forward:        y[p]  = x[p] W[p]^T   (x[p] [M, K], y[p] [M, N_p]),
+ *   input gradient: gx[p] = gy[p] W[p]    (gy[p] [M, N_p], gx[p] [M, K]),
+ * each exactly as the single-product call computes it (same operands, fp32
+ * accumulation in tensor memory, bf16 output, bit-identical reruns), but the
+ * products' work items share one grid, so a small product no longer pays a whole
+ * launch's start-up and drain.  The arrays are host arrays of nprod entries
+ * (device pointers, leading dimensions in elements); the x pointers may be equal.
+ * Requirements: 1 <= nprod <= NF4_MAX_MULTI; the same M and K for every product;
+ * 4-bit codes, the same double_quant setting and the same code4 / code8 tables
+ * (pointer-equal) for every weight; bf16 activations and outputs; K % 64 == 0;
+ * activations, outputs and packed codes 16-byte aligned with leading dimensions
+ * multiples of 8 (NF4_ERR_ALIGNMENT otherwise); no workspace.  M == 0 is a
+ * no-op.  Products are scheduled in order of decreasing contraction length with
+ * the classic schedule and 128- or 256-token tiles (a deterministic function of
+ * the shapes and the SM count). */
+#define NF4_MAX_MULTI 4
+nf4_status nf4_linear_fwd_multi(int32_t nprod, const void* const* x, int64_t M, const int64_t* ldx,
+                                const nf4_weight* const* w, void* const* y, const int64_t* ldy,
+                                void* stream);
+nf4_status nf4_linear_dgrad_multi(int32_t nprod, const void* const* gy, int64_t M, const int64_t* ldgy,
+                                  const nf4_weight* const* w, void* const* gx, const int64_t* ldgx,
+                                  void* stream);
 
 /* nf4_linear_fwd_f16 / nf4_linear_dgrad_f16 -- the same products for the fp16
  * compute dtype (Soup issue #842, "Design sketch": keep the dtype handling of

@@ -109,6 +109,25 @@ def grouped_swiglu(seed=0):
     print("ok grouped swiglu", flush=True)
 
 
+def multi(seed=0):
+    K, M, Ns = 320, 300, (264, 136, 392)
+    g = synth.generator(seed)
+    ws, wbs = [], []
+    for N in Ns:
+        w32 = synth.weight(N, K, g)
+        ws.append(nf4.quantize(w32.to(DEV), double_quant=True))
+        wbs.append(oracle.dequantize(oracle_state(w32, True), "bf16"))
+    x = synth.activation(M, K, g)
+    gys = [synth.activation(M, N, g) for N in Ns]
+    ys = ops.linear_fwd_multi([x.to(DEV)] * len(Ns), ws)
+    gxs = ops.linear_dgrad_multi([gy.to(DEV) for gy in gys], ws)
+    for p, wb in enumerate(wbs):
+        parity(ys[p], oracle.linear_fwd(bf16_bits(x), wb), f"multi fwd p{p}")
+        parity(gxs[p], oracle.linear_dgrad(bf16_bits(gys[p]), wb), f"multi dgrad p{p}")
+    status_clean("multi")
+    print("ok multi", flush=True)
+
+
 def main():
     assert _lib.checked_build(), "NF4_CHECKED=1 must load the checked build"
     nf4.device_status(clear=True)
@@ -139,6 +158,7 @@ def main():
         dense(M, 264, 320, seed=50 + M, what="8-bit codes", quant_type="int8")
     grouped(seed=60)
     grouped_swiglu(seed=61)
+    multi(seed=62)
     # the check itself: a failure injected into the next fused launch's index checks
     # is recorded (its loads are skipped), and the next launch is clean again
     _lib.inject_bounds_failure()

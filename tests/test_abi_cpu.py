@@ -131,3 +131,33 @@ def test_swiglu_backward_host_validation(L):
     # T == 0 is a no-op
     assert L.nf4_grouped_swiglu_bwd(x, off, 1, 0, 128, ctypes.byref(w), N_e, ctypes.byref(ep), None,
                                     128, None, 128, None, None, 0, None) == 0
+
+
+def test_multi_product_host_validation(L):
+    """nf4_linear_*_multi reject bad arguments on the host, before any device call."""
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    dummy = 0x1000
+
+    def call(ws, M=4, ld=256, nprod=None, aligned=True, fn=L.nf4_linear_fwd_multi):
+        n = len(ws) if nprod is None else nprod
+        k = max(n, len(ws), 1)
+        ptr = dummy if aligned else dummy + 2
+        acts = (P * k)(*([ptr] * k))
+        outs = (P * k)(*([ptr] * k))
+        lds = (I64 * k)(*([ld] * k))
+        warr = (P * k)(*([ctypes.addressof(w) for w in ws] + [None] * (k - len(ws))))
+        return fn(n, acts, M, lds, warr, outs, lds, None)
+
+    a, b = _weight(N=128, K=128), _weight(N=256, K=128)
+    assert call([a, b], nprod=0) == 1
+    assert call([a] * 5) == 1                     # more than NF4_MAX_MULTI products
+    assert call([a, _weight(N=128, K=192)]) == 1  # different K
+    assert call([a, _weight(N=128, K=128, dq=1)]) == 1  # different double_quant
+    w8 = _weight(N=128, K=128)
+    w8.bits = 8
+    assert call([a, w8]) == 7                     # one-byte codes
+    assert call([_weight(N=128, K=100)] * 2, ld=256) == 2  # K % 64
+    assert call([a, b], ld=64) == 1               # leading dimension below the width
+    assert call([a, b], aligned=False) == 3       # misaligned activations / outputs
+    assert call([a, b], M=0) == 0                 # M == 0: nothing to do
+    assert call([a, b], ld=256, fn=L.nf4_linear_dgrad_multi, aligned=False) == 3

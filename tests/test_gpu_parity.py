@@ -1004,3 +1004,75 @@ def test_pair_tiles_identity_probe_and_f16(restore_token_tile):
     parity(yh, oracle.linear_fwd(_f16_bits(x), wh, dtype="f16"), "pair f16 fwd")
     parity(gxh, oracle.linear_dgrad(_f16_bits(gy), wh, dtype="f16"), "pair f16 dgrad")
     assert nf4.device_status() == 0
+
+
+# ------------------------------------------------------ multi-product launches --
+# nf4_linear_fwd_multi / nf4_linear_dgrad_multi: several products of the same M and
+# K in one launch, each against the oracle.
+
+def _multi_case(Ns, K, M, seed):
+    g = synth.generator(seed)
+    ws, sts = [], []
+    for N in Ns:
+        w32 = synth.weight(N, K, g)
+        ws.append(nf4.quantize(w32.to(DEV), double_quant=True))
+        sts.append(oracle_state(w32, True))
+    x = synth.activation(M, K, g)
+    gys = [synth.activation(M, N, g) for N in Ns]
+    return ws, sts, x, gys
+
+
+@pytest.mark.parametrize("M", [1, 40, 300, 513])
+@pytest.mark.parametrize("Ns", [(264, 136, 392), (128, 1000), (520,), (96, 384, 1024, 200)])
+def test_multi_product_parity(M, Ns):
+    K = 320
+    ws, sts, x, gys = _multi_case(Ns, K, M, seed=M + sum(Ns))
+    nf4.reset_path_counters()
+    ys = ops.linear_fwd_multi([x.to(DEV)] * len(Ns), ws)
+    gxs = ops.linear_dgrad_multi([gy.to(DEV) for gy in gys], ws)
+    c = nf4.path_counters()
+    assert c["multi"] == 2 and c["linear_fwd"] == 0 and c["linear_dgrad"] == 0, c
+    for p, (N, st) in enumerate(zip(Ns, sts)):
+        wb = oracle.dequantize(st, "bf16")
+        assert ys[p].shape == (M, N) and gxs[p].shape == (M, K)
+        parity(ys[p], oracle.linear_fwd(bf16_bits(x), wb), f"multi fwd p{p} {M}x{N}x{K}")
+        parity(gxs[p], oracle.linear_dgrad(bf16_bits(gys[p]), wb), f"multi dgrad p{p} {M}x{N}x{K}")
+    ys2 = ops.linear_fwd_multi([x.to(DEV)] * len(Ns), ws)
+    gxs2 = ops.linear_dgrad_multi([gy.to(DEV) for gy in gys], ws)
+    for a, b in zip(ys + gxs, ys2 + gxs2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_multi_product_llama_qkv_rows():
+    # The Llama-3.1-8B q, k, v projections at M = 512 in one launch each way,
+    # sampled output rows against the oracle.
+    M, K, Ns = 512, 4096, (4096, 1024, 1024)
+    ws, sts, x, gys = _multi_case(Ns, K, M, seed=77)
+    ys = ops.linear_fwd_multi([x.to(DEV)] * 3, ws)
+    gxs = ops.linear_dgrad_multi([gy.to(DEV) for gy in gys], ws)
+    rows = np.array([0, 1, 127, 128, 255, 300, 511])
+    rows_d = torch.from_numpy(rows).to(DEV)
+    for p, st in enumerate(sts):
+        wb = oracle.dequantize(st, "bf16")
+        parity(ys[p][rows_d], oracle.linear_fwd(bf16_bits(x), wb, rows=rows), f"qkv fwd p{p}")
+        parity(gxs[p][rows_d], oracle.linear_dgrad(bf16_bits(gys[p]), wb, rows=rows), f"qkv dgrad p{p}")
+    assert nf4.device_status() == 0
+
+
+def test_multi_product_validation():
+    K = 256
+    ws, _, x, gys = _multi_case((128, 256), K, 8, seed=5)
+    xd = x.to(DEV)
+    with pytest.raises(ValueError):
+        ops.linear_fwd_multi([xd] * 5, ws * 3)  # more than four products
+    w_other, _, _, _ = _multi_case((128,), 320, 8, seed=6)
+    with pytest.raises(_lib.NF4Error) as e:  # different K
+        ops._multi("nf4_linear_fwd_multi", _lib.lib().nf4_linear_fwd_multi, [xd, xd], [ws[0], w_other[0]],
+                   None, lambda w: w.N)
+    assert e.value.code == 1
+    w8 = nf4.quantize(synth.weight(128, K, synth.generator(7)).to(DEV), double_quant=True, quant_type="int8")
+    with pytest.raises(_lib.NF4Error) as e:  # one-byte codes
+        ops.linear_fwd_multi([xd, xd], [ws[0], w8])
+    assert e.value.code == 7
+    y0 = ops.linear_fwd_multi([xd[:0]] * 2, ws)  # M == 0
+    assert y0[0].shape == (0, 128)
