@@ -115,6 +115,52 @@ def nf4_grouped_swiglu(x: torch.Tensor, offsets: torch.Tensor, w: ops.NF4Weight,
                                     w.double_quant)
 
 
+class NF4MultiLinearFn(torch.autograd.Function):
+    """y_p = x_p W_p^T for up to four frozen NF4 weights of the same in-features in
+    one multi-product launch (nf4_linear_fwd_multi), and their input gradients in
+    one nf4_linear_dgrad_multi launch.  Arguments: n, the weights' (N, double_quant)
+    pairs, the n activations (the same tensor when the products share an input:
+    autograd then adds their gradients), then the seven tensors of each weight, all
+    saved through save_for_backward."""
+
+    @staticmethod
+    def forward(ctx, n: int, meta: tuple, K: int, *args):
+        xs, tens = args[:n], args[n:]
+        ws = [ops.NF4Weight.from_tensors(tuple(tens[7 * p:7 * p + 7]), meta[p][0], K, meta[p][1])
+              for p in range(n)]
+        lead = tuple(xs[0].shape[:-1])
+        ys = ops.linear_fwd_multi([x.reshape(-1, K).contiguous() for x in xs], ws)
+        ctx.save_for_backward(*tens)
+        ctx.n, ctx.meta, ctx.K, ctx.lead = int(n), tuple((int(N), bool(dq)) for N, dq in meta), int(K), lead
+        return tuple(y.reshape(*lead, meta[p][0]) for p, y in enumerate(ys))
+
+    @staticmethod
+    def backward(ctx, *gys):
+        n, K = ctx.n, ctx.K
+        saved = ctx.saved_tensors
+        if not any(ctx.needs_input_grad[3:3 + n]):
+            return (None,) * (3 + len(saved) + n)
+        ws = [ops.NF4Weight.from_tensors(tuple(saved[7 * p:7 * p + 7]), ctx.meta[p][0], K, ctx.meta[p][1])
+              for p in range(n)]
+        gxs = ops.linear_dgrad_multi([g.reshape(-1, ctx.meta[p][0]).contiguous() for p, g in enumerate(gys)], ws)
+        gxs = [gx.reshape(*ctx.lead, K) if ctx.needs_input_grad[3 + p] else None for p, gx in enumerate(gxs)]
+        return (None, None, None, *gxs) + (None,) * len(saved)
+
+
+def nf4_linear_multi(x: torch.Tensor, ws) -> tuple:
+    """Frozen NF4 Linears that share their input (for instance q, k and v, or gate and
+    up): one multi-product launch forward and one backward (bf16 compute; other
+    input dtypes are cast to bf16 and the outputs cast back).  Returns one output
+    per weight."""
+    dt = x.dtype
+    xb = x if dt == torch.bfloat16 else x.to(torch.bfloat16)
+    K = ws[0].K
+    meta = tuple((w.N, w.double_quant) for w in ws)
+    tens = [t for w in ws for t in w.tensors()]
+    ys = NF4MultiLinearFn.apply(len(ws), meta, K, *([xb] * len(ws)), *tens)
+    return ys if dt == torch.bfloat16 else tuple(y.to(dt) for y in ys)
+
+
 def nf4_linear(x: torch.Tensor, w: ops.NF4Weight) -> torch.Tensor:
     """Frozen NF4 Linear: the compute dtype is the activations' half-precision type,
     bf16 or fp16 (the dtype handling of Linear4bit, which Soup issue #842's "Design

@@ -99,3 +99,43 @@ def test_grouped_function_grad():
     offs = offsets.numpy()
     parity(y, oracle.grouped_fwd(bf16_bits(x), offs, wb), "grouped fn fwd")
     parity(xd.grad, oracle.grouped_dgrad(bf16_bits(gy), offs, wb), "grouped fn dgrad")
+
+
+def test_multi_linear_function_grad_matches_oracle():
+    """q/k/v-shaped weights sharing their input through nf4_linear_multi: one
+    multi-product launch each way; each output and the summed input gradient (the
+    engine adds the products' gradients) against the oracle."""
+    M, K, Ns = 48, 256, (256, 128, 128)
+    g = synth.generator(17)
+    ws, wbs = [], []
+    for N in Ns:
+        w32 = synth.weight(N, K, g)
+        ws.append(nf4.quantize(w32.to(DEV), double_quant=True))
+        wbs.append(oracle.dequantize(oracle_state(w32, True), "bf16"))
+    x = synth.activation(M, K, g)
+    gys = [synth.activation(M, N, g) for N in Ns]
+    xd = x.to(DEV).requires_grad_(True)
+    nf4.reset_path_counters()
+    ys = nf4.nf4_linear_multi(xd, ws)
+    torch.autograd.backward(ys, [gy.to(DEV) for gy in gys])
+    c = nf4.path_counters()
+    assert c["multi"] == 2 and c["linear_fwd"] == 0 and c["linear_dgrad"] == 0, c
+    for y, wb, N in zip(ys, wbs, Ns):
+        assert y.shape == (M, N)
+        parity(y, oracle.linear_fwd(bf16_bits(x), wb), f"multi fwd {N}")
+    ref = sum(oracle.linear_dgrad(bf16_bits(gy), wb) for gy, wb in zip(gys, wbs))
+    parity(xd.grad, ref, "multi grad_x (sum over the products)")
+
+
+def test_multi_linear_function_saves_no_weight_shaped_tensor():
+    K, Ns = 256, (256, 128)
+    g = synth.generator(18)
+    ws = [nf4.quantize(synth.weight(N, K, g).to(DEV), double_quant=True) for N in Ns]
+    x = synth.activation(8, K, g).to(DEV).requires_grad_(True)
+    ys = nf4.nf4_linear_multi(x, ws)
+    fn = ys[0].grad_fn
+    assert type(fn).__name__.startswith("NF4MultiLinearFn")
+    saved = [t for t in fn.saved_tensors if t is not None]
+    for t in saved:
+        assert t.shape != (Ns[0], K) and t.shape != (Ns[1], K)
+    assert not [k for k, v in vars(fn).items() if isinstance(v, torch.Tensor)]
