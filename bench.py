@@ -390,6 +390,14 @@ def run_ours(args, rank, world, local_rank):
             launch_flops += [fl] * 2
     mean_ms = sum(launch_ms) / len(launch_ms)
     mean_flops = sum(launch_flops) / len(launch_flops)
+    # Per launch of the step (each run alone between events), mean over the pass.
+    per_launch = {}
+    names = [p[0] for p in synth.LLAMA8B_PROJ]
+    for gi, grp in enumerate(LAUNCH_GROUPS):
+        tag = "+".join(names[j] for j in grp)
+        for d, off in (("fwd", 0), ("dgrad", 1)):
+            v = [launch_ms[(i * len(LAUNCH_GROUPS) + gi) * 2 + off] for i in range(n_ev)]
+            per_launch[f"{tag} {d}"] = round(sum(v) / len(v) * 1e3, 2)
     achieved = mean_flops / (mean_ms * 1e-3) / 1e12
     pk, pk_src = peaks()
     peak = pk["bf16_tflops"]
@@ -514,6 +522,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_kind": f"bf16 dense burst (launches timed alone), of {pk_src}",
             "traffic": traffic_per_launch(), "launches_timed": len(launch_ms),
             "mean_launch_ms": round(mean_ms, 5),
+            "launch_us": per_launch,
             "timing": "separate pass after the timed region, CUDA events around each launch",
         },
         "e2e": {"value": round(e2e_val, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -858,6 +867,30 @@ def run_grouped(dev, pk):
     out["swiglu_gate_up_fwd"] = {"us_fused_epilogue": round(t_f * 1e6, 2),
                                  "us_unfused_torch_glue": round(t_u * 1e6, 2),
                                  "tflops_fused": round(2.0 * T * 2 * I * H / t_f / 1e12, 2)}
+
+    # The top-k combine of the down projection's rows ([T, H] -> [tokens, H]) and its
+    # backward, over 16 row buffers (268 MB > L2) in turn.  Bytes: rows in, tokens
+    # out, the route table (forward); the reverse (backward).
+    tokens, topk = c["tokens"], c["topk"]
+    tr = ops.route_rows(row_token.to(dev), tokens, topk)
+    nbuf = 16
+    rows_b = [synth.activation(T, H, g).to(dev) for _ in range(nbuf)]
+    grads_b = [synth.activation(tokens, H, g).to(dev) for _ in range(nbuf)]
+    comb = torch.empty(tokens, H, dtype=torch.bfloat16, device=dev)
+    grows = torch.empty(T, H, dtype=torch.bfloat16, device=dev)  # every row is routed once
+    state = {"i": 0}
+    def combine():
+        ops.moe_combine(rows_b[state["i"] % nbuf], tr, out=comb)
+        state["i"] += 1
+    def combine_bwd():
+        ops.moe_combine_bwd(grads_b[state["i"] % nbuf], tr, T, out=grows)
+        state["i"] += 1
+    t_c, t_cb = time_graph(combine, reps=nbuf), time_graph(combine_bwd, reps=nbuf)
+    b_c = 2 * T * H + 2 * tokens * H + 4 * tokens * topk
+    out["topk_combine"] = {"rows": T, "tokens": tokens, "H": H,
+                           "us_fwd": round(t_c * 1e6, 2), "gbs_fwd": round(b_c / t_c / 1e9, 1),
+                           "us_bwd": round(t_cb * 1e6, 2), "gbs_bwd": round(b_c / t_cb / 1e9, 1),
+                           "frac_hbm_fwd": round(b_c / t_c / 1e9 / pk["hbm_gbs"], 4)}
     return out
 
 

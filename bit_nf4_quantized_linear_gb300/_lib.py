@@ -26,7 +26,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_DGRAD, OP_GROUPED_FWD, OP_GROUPED_DGRAD, OP_GROUPED_SWIGLU_BWD = range(6)
 PATHS = ["linear_fwd", "linear_dgrad", "splitk_reduce", "grouped_fwd", "grouped_dgrad",
          "dequantize", "quantize", "total", "gemv_fwd", "gemv_dgrad", "skinny_fwd",
-         "skinny_dgrad", "stream_k", "cluster_split", "multi"]
+         "skinny_dgrad", "stream_k", "cluster_split", "multi", "moe_combine"]
 
 
 class NF4Error(RuntimeError):
@@ -107,6 +107,8 @@ def lib() -> ctypes.CDLL:
             "nf4_linear_fwd": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_linear_dgrad": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_linear_fwd_multi": [I32, P, I64, P, P, P, P, P],
+            "nf4_moe_combine": [P, I64, I64, P, I64, I32, I64, P, I64, P],
+            "nf4_moe_combine_bwd": [P, I64, I64, P, I32, I64, I64, P, I64, P],
             "nf4_linear_dgrad_multi": [I32, P, I64, P, P, P, P, P],
             "nf4_linear_fwd_f16": [P, I64, I64, W, P, I64, P, SZ, P],
             "nf4_linear_dgrad_f16": [P, I64, I64, W, P, I64, P, SZ, P],

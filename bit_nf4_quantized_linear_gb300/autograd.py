@@ -161,6 +161,30 @@ def nf4_linear_multi(x: torch.Tensor, ws) -> tuple:
     return ys if dt == torch.bfloat16 else tuple(y.to(dt) for y in ys)
 
 
+class NF4MoECombineFn(torch.autograd.Function):
+    """The top-k combine of the grouped experts (nf4_moe_combine): token t's output
+    is the sum of its routed rows; the backward (nf4_moe_combine_bwd) copies each
+    token's gradient to its rows.  The route table goes through save_for_backward."""
+
+    @staticmethod
+    def forward(ctx, rows, token_rows):
+        y = ops.moe_combine(rows.contiguous(), token_rows)
+        ctx.save_for_backward(token_rows)
+        ctx.R = int(rows.shape[0])
+        return y
+
+    @staticmethod
+    def backward(ctx, gy):
+        (token_rows,) = ctx.saved_tensors
+        g = ops.moe_combine_bwd(gy.contiguous(), token_rows, ctx.R) if ctx.needs_input_grad[0] else None
+        return g, None
+
+
+def nf4_combine(rows: torch.Tensor, token_rows: torch.Tensor) -> torch.Tensor:
+    """Sum each token's routed expert rows (bf16; see ops.route_rows for the table)."""
+    return NF4MoECombineFn.apply(rows, token_rows)
+
+
 def nf4_linear(x: torch.Tensor, w: ops.NF4Weight) -> torch.Tensor:
     """Frozen NF4 Linear: the compute dtype is the activations' half-precision type,
     bf16 or fp16 (the dtype handling of Linear4bit, which Soup issue #842's "Design

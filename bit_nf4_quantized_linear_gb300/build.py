@@ -23,7 +23,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libnf4.so")
 CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
 CHECKED_LIB_PATH = os.path.join(PKG, "libnf4_checked.so")
-SOURCES = ["nf4_api.cu", "nf4_gemm.cu", "nf4_gemm8.cu", "nf4_gemm_f16.cu", "nf4_gemv.cu", "nf4_quant.cu", "nf4_skinny.cu"]
+SOURCES = ["nf4_api.cu", "nf4_gemm.cu", "nf4_gemm8.cu", "nf4_gemm_f16.cu", "nf4_gemv.cu", "nf4_moe.cu", "nf4_quant.cu",
+           "nf4_skinny.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

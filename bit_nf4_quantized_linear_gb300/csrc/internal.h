@@ -44,6 +44,23 @@ constexpr int kMaxExperts = 512;
 constexpr int kTileW = 128;  // rows of the dequantised operand per tile (MMA M)
 constexpr int kTileK = 64;   // contraction per pipeline stage (one 64-value block)
 
+// Top-k combine of the grouped experts and its backward (nf4_moe_combine,
+// nf4_moe_combine_bwd).  Forward: rows = the grouped output [R, H], out = [tokens,
+// H]; backward: rows = the gradient of the combined output [tokens, H], out = the
+// rows' gradient [R, H].  token_rows [tokens, k]: row of each (token, route), -1
+// for none.
+struct MoeArgs {
+  const __nv_bfloat16* rows;
+  int64_t ld_rows;
+  const int32_t* token_rows;
+  int32_t k;
+  int64_t tokens, R, H;
+  __nv_bfloat16* out;
+  int64_t ld_out;
+  int* status;
+};
+cudaError_t launch_moe(bool backward, const MoeArgs& a, cudaStream_t s);
+
 // Multi-product launches (nf4_linear_fwd_multi / nf4_linear_dgrad_multi): up to
 // kMaxProds independent products with the same M and in-features K, each with its
 // own weight, activation and output, whose work items share one grid.

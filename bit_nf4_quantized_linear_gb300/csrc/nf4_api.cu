@@ -811,6 +811,36 @@ nf4_status run_multi(int mode, int32_t nprod, const void* const* act, int64_t M,
   return NF4_OK;
 }
 
+// Top-k combine of the experts, or its backward (nf4_moe_combine / _bwd).
+nf4_status run_moe(bool backward, const void* src, int64_t src_rows, int64_t ld_src,
+                          const int32_t* token_rows, int64_t tokens, int32_t k, int64_t R, int64_t H, void* dst,
+                          int64_t ld_dst, void* stream) {
+  if (k < 1 || tokens < 0 || R < 0 || H < 0 || src_rows < 0) return NF4_ERR_INVALID_ARG;
+  if (ld_src < H || ld_dst < H) return NF4_ERR_INVALID_ARG;
+  if (H % 8 != 0) return NF4_ERR_UNSUPPORTED_SHAPE;
+  if (tokens == 0 || H == 0) return NF4_OK;
+  if (!src || !dst || !token_rows) return NF4_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst) || ld_src % 8 != 0 || ld_dst % 8 != 0) return NF4_ERR_ALIGNMENT;
+  if (tokens > INT32_MAX || R > INT32_MAX || H > INT32_MAX) return NF4_ERR_UNSUPPORTED_SHAPE;
+  DevInfo dev;
+  if (!current_device(&dev)) return cuda_fail(cudaGetLastError(), "device query");
+  nf4::MoeArgs a{};
+  a.rows = static_cast<const __nv_bfloat16*>(src);
+  a.ld_rows = ld_src;
+  a.token_rows = token_rows;
+  a.k = k;
+  a.tokens = tokens;
+  a.R = R;
+  a.H = H;
+  a.out = static_cast<__nv_bfloat16*>(dst);
+  a.ld_out = ld_dst;
+  a.status = dev.status;
+  cudaError_t le = nf4::launch_moe(backward, a, static_cast<cudaStream_t>(stream));
+  if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+  count(NF4_PATH_MOE_COMBINE);
+  return NF4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1005,6 +1035,18 @@ const char* nf4_status_string(nf4_status s) {
 }
 
 int32_t nf4_checked_build(void) { return NF4_CHECKED ? 1 : 0; }
+
+nf4_status nf4_moe_combine(const void* rows, int64_t R, int64_t ld_rows, const int32_t* token_rows,
+                           int64_t tokens, int32_t k, int64_t H, void* out, int64_t ld_out, void* stream) {
+  return run_moe(false, rows, R, ld_rows, token_rows, tokens, k, R, H, out, ld_out, stream);
+}
+
+nf4_status nf4_moe_combine_bwd(const void* grad_out, int64_t tokens, int64_t ld_grad_out,
+                               const int32_t* token_rows, int32_t k, int64_t R, int64_t H, void* grad_rows,
+                               int64_t ld_grad_rows, void* stream) {
+  return run_moe(true, grad_out, tokens, ld_grad_out, token_rows, tokens, k, R, H, grad_rows, ld_grad_rows,
+                 stream);
+}
 
 nf4_status nf4_linear_fwd_multi(int32_t nprod, const void* const* x, int64_t M, const int64_t* ldx,
                                 const nf4_weight* const* w, void* const* y, const int64_t* ldy, void* stream) {

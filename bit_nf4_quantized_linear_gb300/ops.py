@@ -231,6 +231,49 @@ def _multi(name, fn, acts, ws, outs, out_cols):
     return outs
 
 
+def route_rows(row_token: torch.Tensor, tokens: int, k: int) -> torch.Tensor:
+    """The route table of the top-k combine from the grouped rows' token map
+    (row r of the expert-sorted batch belongs to token row_token[r]): int32
+    [tokens, k], token t's rows in ascending order.  Every token must hold exactly
+    k rows (top-k routing)."""
+    if row_token.numel() != tokens * k:
+        raise ValueError("route_rows: expected tokens * k grouped rows")
+    order = torch.argsort(row_token.to(torch.int64), stable=True)
+    return order.to(torch.int32).reshape(tokens, k).contiguous()
+
+
+def moe_combine(rows: torch.Tensor, token_rows: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_moe_combine: out[t] = sum over j of rows[token_rows[t, j]] (bf16 [R, H] ->
+    [tokens, H]; fp32 sum in route order, rounded once)."""
+    _check_act("moe_combine", rows, rows.shape[1] if rows.dim() == 2 else -1)
+    _need_cuda("moe_combine", token_rows)
+    if token_rows.dtype != torch.int32 or token_rows.dim() != 2 or not token_rows.is_contiguous():
+        raise ValueError("moe_combine: token_rows must be a contiguous int32 [tokens, k] tensor")
+    tokens, k = token_rows.shape
+    R, H = rows.shape
+    y = torch.empty(tokens, H, dtype=torch.bfloat16, device=rows.device) if out is None else out
+    rc = _lib.lib().nf4_moe_combine(_ptr(rows), R, rows.stride(0), _ptr(token_rows), tokens, k, H, _ptr(y),
+                                    y.stride(0), _stream())
+    _lib.check(rc, "nf4_moe_combine")
+    return y
+
+
+def moe_combine_bwd(grad_out: torch.Tensor, token_rows: torch.Tensor, R: int,
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """nf4_moe_combine_bwd: each routed row receives its token's gradient (bf16
+    [tokens, H] -> [R, H]).  Rows no route names are zero in a new tensor, and left
+    as they are in a given `out`."""
+    _check_act("moe_combine_bwd", grad_out, grad_out.shape[1] if grad_out.dim() == 2 else -1)
+    _need_cuda("moe_combine_bwd", token_rows)
+    tokens, k = token_rows.shape
+    H = grad_out.shape[1]
+    g = torch.zeros(R, H, dtype=torch.bfloat16, device=grad_out.device) if out is None else out
+    rc = _lib.lib().nf4_moe_combine_bwd(_ptr(grad_out), tokens, grad_out.stride(0), _ptr(token_rows), k, R, H,
+                                        _ptr(g), g.stride(0), _stream())
+    _lib.check(rc, "nf4_moe_combine_bwd")
+    return g
+
+
 MAX_MULTI = 4  # NF4_MAX_MULTI of include/nf4.h
 
 

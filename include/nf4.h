@@ -91,7 +91,8 @@ enum {
   NF4_PATH_STREAM_K = 12,    /* fused launch with the stream-K schedule     */
   NF4_PATH_CLUSTER_SPLIT = 13,/* fused launch with the cluster split         */
   NF4_PATH_MULTI = 14,       /* multi-product fused launch                  */
-  NF4_NUM_PATHS = 15
+  NF4_PATH_MOE_COMBINE = 15, /* top-k combine of the experts, or its backward */
+  NF4_NUM_PATHS = 16
 };
 
 /* A quantised weight: the tensors of the pages' QuantState as plain device
@@ -226,6 +227,27 @@ nf4_status nf4_linear_fwd_multi(int32_t nprod, const void* const* x, int64_t M, 
 nf4_status nf4_linear_dgrad_multi(int32_t nprod, const void* const* gy, int64_t M, const int64_t* ldgy,
                                   const nf4_weight* const* w, void* const* gx, const int64_t* ldgx,
                                   void* stream);
+
+/* nf4_moe_combine -- the top-k combine of the grouped experts: the grouped
+ * products leave one bf16 row per (token, routed expert), rows [R, H] (row pitch
+ * ld_rows), typically after the down projection with the routing weights applied
+ * as its row scale (nf4_grouped_fwd_ep); token t's output is the sum of its rows
+ *   out[t][c] = bf16( sum_{j < k, token_rows[t*k + j] >= 0} rows[token_rows[t*k + j]][c] )
+ * in fp32, in route order j, rounded once (round to nearest even); deterministic.
+ * token_rows: device int32 [tokens, k], the row of each (token, route), -1 for an
+ * absent route; an index >= R is skipped and recorded as NF4_ERR_BAD_OFFSETS in
+ * the device status word.  out [tokens, H] bf16 (row pitch ld_out).  H % 8 == 0,
+ * rows / out 16-byte aligned with pitches multiples of 8 (NF4_ERR_ALIGNMENT),
+ * k >= 1, tokens, R >= 0 (tokens == 0 or H == 0: nothing to do).
+ * nf4_moe_combine_bwd -- its backward: grad_rows[token_rows[t*k + j]] =
+ * grad_out[t] (an exact copy) for every present route; rows that no route names
+ * are not written.  grad_out [tokens, H] (pitch ld_grad_out), grad_rows [R, H]
+ * (pitch ld_grad_rows); the same requirements. */
+nf4_status nf4_moe_combine(const void* rows, int64_t R, int64_t ld_rows, const int32_t* token_rows,
+                           int64_t tokens, int32_t k, int64_t H, void* out, int64_t ld_out, void* stream);
+nf4_status nf4_moe_combine_bwd(const void* grad_out, int64_t tokens, int64_t ld_grad_out,
+                               const int32_t* token_rows, int32_t k, int64_t R, int64_t H, void* grad_rows,
+                               int64_t ld_grad_rows, void* stream);
 
 /* nf4_linear_fwd_f16 / nf4_linear_dgrad_f16 -- the same products for the fp16
  * compute dtype (Soup issue #842, "Design sketch": keep the dtype handling of

@@ -411,3 +411,34 @@ def grouped_dgrad(gy_bf16: np.ndarray, offsets, wb_stack_bf16: np.ndarray) -> np
         if b > a:
             gx[a:b] = linear_dgrad(gy_bf16[a:b], wb_stack_bf16[e])
     return gx
+
+
+def moe_combine(rows_bf16: np.ndarray, token_rows: np.ndarray) -> np.ndarray:
+    """Top-k combine of the grouped experts' output rows (fork PR "Experts
+    trainability", commits 1-2: per-expert segments of a token-sorted batch; Soup
+    issue #842, expert path): token t's output is the sum of the rows it was routed
+    to, token_rows[t, j] (j = 0 .. k-1; -1 for an absent route).  rows_bf16: bf16
+    bit patterns [R, H].  Returns the exact fp64 sums [tokens, H]."""
+    rows = bf16_bits_to_f32(np.ascontiguousarray(rows_bf16, dtype=np.uint16)).astype(np.float64)
+    tokens, k = token_rows.shape
+    out = np.zeros((tokens, rows.shape[1]), dtype=np.float64)
+    for t in range(tokens):
+        for j in range(k):
+            r = int(token_rows[t, j])
+            if r >= 0:
+                out[t] += rows[r]
+    return out
+
+
+def moe_combine_bwd(grad_bf16: np.ndarray, token_rows: np.ndarray, R: int) -> np.ndarray:
+    """Backward of moe_combine: each row routed from token t receives grad[t]
+    unchanged (bf16 bit patterns [R, H]; rows no route names stay 0)."""
+    g = np.ascontiguousarray(grad_bf16, dtype=np.uint16)
+    out = np.zeros((R, g.shape[1]), dtype=np.uint16)
+    tokens, k = token_rows.shape
+    for t in range(tokens):
+        for j in range(k):
+            r = int(token_rows[t, j])
+            if r >= 0:
+                out[r] = g[t]
+    return out

@@ -161,3 +161,13 @@ def test_multi_product_host_validation(L):
     assert call([a, b], aligned=False) == 3       # misaligned activations / outputs
     assert call([a, b], M=0) == 0                 # M == 0: nothing to do
     assert call([a, b], ld=256, fn=L.nf4_linear_dgrad_multi, aligned=False) == 3
+
+
+def test_moe_combine_host_validation(L):
+    x = ctypes.c_void_p(0x1000)
+    assert L.nf4_moe_combine(x, 8, 64, x, 4, 0, 64, x, 64, None) == 1      # k < 1
+    assert L.nf4_moe_combine(x, 8, 64, x, 4, 2, 60, x, 64, None) == 2      # H % 8
+    assert L.nf4_moe_combine(x, 8, 32, x, 4, 2, 64, x, 64, None) == 1      # pitch below H
+    assert L.nf4_moe_combine(ctypes.c_void_p(0x1002), 8, 64, x, 4, 2, 64, x, 64, None) == 3  # misaligned
+    assert L.nf4_moe_combine(x, 8, 64, x, 0, 2, 64, x, 64, None) == 0      # no tokens
+    assert L.nf4_moe_combine_bwd(x, 4, 64, x, 2, 8, 64, ctypes.c_void_p(0x1002), 64, None) == 3

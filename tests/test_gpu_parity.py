@@ -1076,3 +1076,55 @@ def test_multi_product_validation():
     assert e.value.code == 7
     y0 = ops.linear_fwd_multi([xd[:0]] * 2, ws)  # M == 0
     assert y0[0].shape == (0, 128)
+
+
+# ------------------------------------------------------------ top-k combine --
+# nf4_moe_combine / nf4_moe_combine_bwd against oracle.moe_combine(_bwd).
+
+def _combine_case(seed, tokens=512, experts=64, topk=8, H=2048):
+    g = synth.generator(seed)
+    row_token, _ = synth.routing(tokens, experts, topk, g)
+    R = row_token.numel()
+    rows = synth.activation(R, H, g)
+    tr = ops.route_rows(row_token.to(DEV), tokens, topk)
+    return rows, tr, g
+
+
+def test_moe_combine_olmoe_against_oracle():
+    rows, tr, g = _combine_case(51)
+    nf4.reset_path_counters()
+    y = ops.moe_combine(rows.to(DEV), tr)
+    assert nf4.path_counters()["moe_combine"] == 1
+    tr_h = tr.cpu().numpy()
+    assert sorted(tr_h.reshape(-1).tolist()) == list(range(rows.shape[0]))  # each row routed once
+    parity(y, oracle.moe_combine(bf16_bits(rows), tr_h), "moe combine")
+    assert torch.equal(ops.moe_combine(rows.to(DEV), tr).view(torch.int16), y.view(torch.int16))
+    gy = synth.activation(y.shape[0], y.shape[1], g)
+    gr = ops.moe_combine_bwd(gy.to(DEV), tr, rows.shape[0])
+    np.testing.assert_array_equal(bf16_bits(gr), oracle.moe_combine_bwd(bf16_bits(gy), tr_h, rows.shape[0]))
+    assert nf4.device_status() == 0
+
+
+def test_moe_combine_absent_routes_and_bad_index():
+    g = synth.generator(52)
+    R, H = 10, 64
+    rows = synth.activation(R, H, g)
+    tr = torch.tensor([[0, 3, -1], [9, -1, -1], [1, 2, 4]], dtype=torch.int32)
+    y = ops.moe_combine(rows.to(DEV), tr.to(DEV))
+    parity(y, oracle.moe_combine(bf16_bits(rows), tr.numpy()), "combine with absent routes")
+    nf4.device_status(clear=True)
+    bad = torch.tensor([[0, 10], [1, 2]], dtype=torch.int32, device=DEV)  # 10 >= R
+    y2 = ops.moe_combine(rows.to(DEV), bad)
+    assert nf4.device_status(clear=True) == 8  # NF4_ERR_BAD_OFFSETS, the route skipped
+    parity(y2[1:], oracle.moe_combine(bf16_bits(rows), bad[1:].cpu().numpy()), "rows with valid routes")
+
+
+def test_moe_combine_autograd():
+    rows, tr, g = _combine_case(53, tokens=64, experts=8, topk=2, H=256)
+    rd = rows.to(DEV).requires_grad_(True)
+    y = nf4.nf4_combine(rd, tr)
+    gy = synth.activation(y.shape[0], y.shape[1], g)
+    y.backward(gy.to(DEV))
+    tr_h = tr.cpu().numpy()
+    parity(y, oracle.moe_combine(bf16_bits(rows), tr_h), "combine fwd")
+    np.testing.assert_array_equal(bf16_bits(rd.grad), oracle.moe_combine_bwd(bf16_bits(gy), tr_h, rows.shape[0]))

@@ -671,3 +671,32 @@ def test_grouped_swiglu_dgrad_one_hot_literals():
     s2 = 1.0 / (1.0 + math.exp(-2.0))
     assert gxb[0, 0] == oracle.bf16_bits_to_f32(oracle.f32_to_bf16_bits(
         np.float32(0.5 * 2.0 * s2 * (1 + 2.0 * (1 - s2)))))
+
+
+def test_moe_combine_literals():
+    """The top-k combine: token 0 takes rows 0 and 2, token 1 row 1 only (route 1
+    absent); exact sums of bf16 values; the backward copies each token's gradient
+    to its rows and leaves a row no route names at zero."""
+    vals = np.array([[1.0, 2.0], [3.0, 4.0], [5.0, -6.5], [7.0, 8.0]], dtype=np.float32)
+    rows = (vals.view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16
+    tr = np.array([[0, 2], [1, -1]], dtype=np.int32)
+    out = oracle.moe_combine(rows, tr)
+    np.testing.assert_array_equal(out, np.array([[6.0, -4.5], [3.0, 4.0]]))
+    g = (np.array([[0.5, -1.0], [2.0, 0.25]], dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    gr = oracle.moe_combine_bwd(g, tr, 4)
+    np.testing.assert_array_equal(gr[0], g[0])
+    np.testing.assert_array_equal(gr[2], g[0])
+    np.testing.assert_array_equal(gr[1], g[1])
+    np.testing.assert_array_equal(gr[3], np.zeros(2, dtype=np.uint16))
+
+
+def test_moe_combine_single_route_is_identity_and_sum_is_linear():
+    rng = np.random.default_rng(3)
+    R, H = 12, 16
+    rows = oracle.f32_to_bf16_bits(rng.standard_normal((R, H)).astype(np.float32))
+    perm = rng.permutation(R).astype(np.int32).reshape(R, 1)
+    np.testing.assert_array_equal(oracle.moe_combine(rows, perm),
+                                  oracle.bf16_bits_to_f32(rows[perm[:, 0]]).astype(np.float64))
+    tr = rng.permutation(R).astype(np.int32).reshape(R // 3, 3)
+    expect = sum(oracle.bf16_bits_to_f32(rows[tr[:, j]]).astype(np.float64) for j in range(3))
+    np.testing.assert_allclose(oracle.moe_combine(rows, tr), expect, rtol=0, atol=1e-12)
