@@ -128,6 +128,21 @@ def multi(seed=0):
     print("ok multi", flush=True)
 
 
+def combine(seed=0):
+    g = synth.generator(seed)
+    row_token, _ = synth.routing(64, 8, 2, g)
+    R = row_token.numel()
+    rows = synth.activation(R, 256, g)
+    tr = ops.route_rows(row_token.to(DEV), 64, 2)
+    y = ops.moe_combine(rows.to(DEV), tr)
+    parity(y, oracle.moe_combine(bf16_bits(rows), tr.cpu().numpy()), "combine")
+    gy = synth.activation(64, 256, g)
+    gr = ops.moe_combine_bwd(gy.to(DEV), tr, R)
+    assert np.array_equal(bf16_bits(gr), oracle.moe_combine_bwd(bf16_bits(gy), tr.cpu().numpy(), R))
+    status_clean("combine")
+    print("ok combine", flush=True)
+
+
 def main():
     assert _lib.checked_build(), "NF4_CHECKED=1 must load the checked build"
     nf4.device_status(clear=True)
@@ -159,6 +174,7 @@ def main():
     grouped(seed=60)
     grouped_swiglu(seed=61)
     multi(seed=62)
+    combine(seed=63)
     # the check itself: a failure injected into the next fused launch's index checks
     # is recorded (its loads are skipped), and the next launch is clean again
     _lib.inject_bounds_failure()
