@@ -71,6 +71,8 @@ class nf4_plan_info(ctypes.Structure):
         ("items", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64),
         ("cluster_split", ctypes.c_int32),
+        ("tail_tokens", ctypes.c_int32),
+        ("tail_token_tile", ctypes.c_int32),
     ]
 
 

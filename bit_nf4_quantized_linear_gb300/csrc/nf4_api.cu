@@ -174,6 +174,10 @@ struct Plan {
   bool stream_k = false;  // fused kernel with the stream-K schedule
   int sk_ctas = 0;
   int cs = 0;  // cluster split: CTAs per tile (one cluster), 0 for none
+  // Token split: the last `tail` tokens run as a second launch with tail_bt-token
+  // single-CTA tiles (the plan's other fields describe the first M - tail tokens).
+  int64_t tail = 0;
+  int tail_bt = 0;
 };
 
 Plan make_plan(int64_t M, int64_t ncols, int64_t contract, int bt, int splits) {
@@ -251,7 +255,8 @@ double step_cycles(int bt) {
 // model in SM clocks -- waves of items times contraction steps, plus the split
 // partials' round trip through memory.
 Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_sk = true,
-                int bits = 4, bool f16 = false, bool allow_cs = true, bool query_device = false) {
+                int bits = 4, bool f16 = false, bool allow_cs = true, bool query_device = false,
+                int force_bt = 0) {
   const int64_t ncols = mode == 0 ? N : K;
   const int64_t contract = mode == 0 ? K : N;
   const int small = g_small_m_path.load(std::memory_order_relaxed);
@@ -295,7 +300,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
   }
   // A fixed tile (nf4_set_token_tile) is the only candidate.  512-token tiles are
   // CTA-pair tiles (4-bit codes, from M = 1024).
-  const int fixed_bt = g_token_tile.load(std::memory_order_relaxed);
+  const int fixed_bt = force_bt > 0 ? force_bt : g_token_tile.load(std::memory_order_relaxed);
   int bt_max = bits == 8 && choose_bt(M) > 128 ? 128 : (bits == 4 && M >= 1024 ? 512 : choose_bt(M));
   if (fixed_bt > 0) bt_max = bits == 8 && fixed_bt > 128 ? 128 : fixed_bt;
   const int bt_min = fixed_bt > 0 ? bt_max : 0;
@@ -386,6 +391,44 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
   }
   double best_any = best_t;
   Plan chosen = best;
+  // Token split of a CTA-pair plan: the first tA 512-token tiles on pairs, the rest
+  // in one more launch of 256-token single-CTA tiles, when the pairs' last round
+  // would be mostly empty (each round of pair tiles after the first also waits for
+  // the previous accumulator's drain, in the 6000-cycle term).  Cost of a launch
+  // beyond the first: about 20000 cycles of start-up and drain (measured at
+  // M = 512).  Taken when 3% cheaper: at K = N = 4096 from M = 8192 (four pair
+  // rounds become three plus one round of single tiles).
+  if (chosen.bt == 512 && fixed_bt == 0 && bits == 4 && !f16 && skm != NF4_STREAM_K_FORCE) {
+    const int64_t wt2 = (ncols + 2 * nf4::kTileW - 1) / (2 * nf4::kTileW);
+    const int64_t pairs = cluster_capacity(mode, 512, 2, sms, query_device);
+    if (pairs >= 1) {
+      const int64_t ks = (contract + nf4::kTileK - 1) / nf4::kTileK;
+      auto pair_cost = [&](int64_t m) {
+        const int64_t items = wt2 * ((m + 511) / 512);
+        return static_cast<double>((items + pairs - 1) / pairs) * (ks * step_cycles(512) + 6000.0);
+      };
+      auto single_cost = [&](int64_t m) {
+        const int64_t items = wtiles * ((m + 255) / 256);
+        return static_cast<double>((items + sms - 1) / sms) * (ks * step_cycles(256) + 3000.0);
+      };
+      const double launch = 20000.0;
+      double split_t = pair_cost(M) + launch;
+      int64_t split_a = 0;
+      for (int64_t ta = 1; ta * 512 < M; ++ta) {
+        const double t = pair_cost(ta * 512) + single_cost(M - ta * 512) + 2.0 * launch;
+        if (t < split_t * 0.97) {
+          split_t = t;
+          split_a = ta * 512;
+        }
+      }
+      if (split_a > 0) {
+        chosen = make_plan(split_a, ncols, contract, 512, 1);
+        chosen.tail = M - split_a;
+        chosen.tail_bt = 256;
+        return chosen;
+      }
+    }
+  }
   if (sk_best.stream_k && (skm == NF4_STREAM_K_FORCE || sk_t < best_t * 0.97)) {
     chosen = sk_best;
     best_any = sk_t;
@@ -404,7 +447,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
 
 nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const nf4_weight* w,
                      void* out, int64_t ld_out, void* ws, size_t ws_bytes, void* stream,
-                     bool allow_sk = true, bool f16 = false) {
+                     bool allow_sk = true, bool f16 = false, int force_bt = 0) {
   nf4_status st = check_weight(w);
   if (st != NF4_OK) return st;
   const int64_t N = w->N, K = w->K;
@@ -425,8 +468,20 @@ nf4_status run_dense(int mode, const void* act, int64_t M, int64_t ld_act, const
   // A cluster split stores its bf16 tile with bulk tensor stores, which need a
   // 16-byte aligned output and row pitch.
   const bool out_tma_ok = aligned16(out) && ld_out % 8 == 0;
-  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk, bits, f16, out_tma_ok, true);
+  // (a forced tile -- the parts of a token split -- takes the classic schedule)
+  const Plan p = plan_dense(mode, M, N, K, dev.sms, allow_sk && force_bt == 0, bits, f16,
+                            out_tma_ok && force_bt == 0, true, force_bt);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes)) return NF4_ERR_WORKSPACE;
+  if (p.tail > 0) {
+    // Token split: two launches over row slices of the activations and the output
+    // (each row computed exactly as in one launch).
+    const int64_t ma = M - p.tail;
+    nf4_status st2 = run_dense(mode, act, ma, ld_act, w, out, ld_out, ws, ws_bytes, stream, false, f16, 512);
+    if (st2 != NF4_OK) return st2;
+    const uint8_t* act_b = static_cast<const uint8_t*>(act) + ma * ld_act * 2;
+    uint8_t* out_b = static_cast<uint8_t*>(out) + ma * ld_out * 2;
+    return run_dense(mode, act_b, p.tail, ld_act, w, out_b, ld_out, ws, ws_bytes, stream, false, f16, p.tail_bt);
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.skinny) {
@@ -1133,6 +1188,8 @@ nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t s
   r.items = p.items;
   r.workspace_bytes = p.ws_bytes;
   r.cluster_split = p.cs;
+  r.tail_tokens = static_cast<int32_t>(p.tail);
+  r.tail_token_tile = p.tail_bt;
   *out = r;
   return NF4_OK;
 }

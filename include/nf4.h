@@ -473,6 +473,10 @@ typedef struct nf4_plan_info {
   int64_t items;           /* fused: work items (tiles x splits)                        */
   uint64_t workspace_bytes;/* workspace this plan needs                                */
   int32_t cluster_split;   /* fused: CTAs of a cluster sharing each tile (splits), or 0 */
+  int32_t tail_tokens;     /* fused token split: the last tail_tokens tokens run as a   */
+                           /* second launch (the fields above describe the first        */
+                           /* M - tail_tokens), or 0                                    */
+  int32_t tail_token_tile; /* tokens per tile of that second launch (256), or 0          */
 } nf4_plan_info;
 nf4_status nf4_plan_query(int32_t op, int64_t M, int64_t N, int64_t K, int32_t sms, int32_t bits,
                           int32_t f16, nf4_plan_info* out);

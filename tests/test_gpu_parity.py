@@ -1128,3 +1128,23 @@ def test_moe_combine_autograd():
     tr_h = tr.cpu().numpy()
     parity(y, oracle.moe_combine(bf16_bits(rows), tr_h), "combine fwd")
     np.testing.assert_array_equal(bf16_bits(rd.grad), oracle.moe_combine_bwd(bf16_bits(gy), tr_h, rows.shape[0]))
+
+
+def test_token_split_at_m8192_rows():
+    """M = 8192 at K = N = 4096 runs as CTA-pair tiles over the first 7168 tokens and
+    one launch of 256-token tiles over the rest: sampled rows on both sides of the
+    boundary and in the tail against the oracle, bit-identical reruns."""
+    M, N, K = 8192, 4096, 4096
+    assert ops.plan_query(1, M, N, K, 152)["tail_tokens"] == 1024
+    w, st, g = _quant_pair(N, K, True, seed=81)
+    x = synth.activation(M, K, g)
+    gy = synth.activation(M, N, g)
+    wb = oracle.dequantize(st, "bf16")
+    y = nf4.linear_fwd(x.to(DEV), w)
+    gx = nf4.linear_dgrad(gy.to(DEV), w)
+    rows = np.array([0, 511, 4000, 7166, 7167, 7168, 7169, 7423, 7424, 8000, 8191])
+    rows_d = torch.from_numpy(rows).to(DEV)
+    parity(y[rows_d], oracle.linear_fwd(bf16_bits(x), wb, rows=rows), "split fwd rows")
+    parity(gx[rows_d], oracle.linear_dgrad(bf16_bits(gy), wb, rows=rows), "split dgrad rows")
+    assert torch.equal(nf4.linear_fwd(x.to(DEV), w).view(torch.int16), y.view(torch.int16))
+    assert nf4.device_status() == 0

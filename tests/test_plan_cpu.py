@@ -77,6 +77,24 @@ SHAPES = list(itertools.product([1, 3, 16, 17, 32, 33, 100, 129, 300, 512, 700, 
                                 [64, 320, 1000, 4096], [64, 1024, 4096]))
 
 
+def test_token_split_of_pair_plans():
+    # M = 8192 at K = N = 4096: four rounds of CTA-pair tiles become three (the first
+    # 7168 tokens) plus one launch of 256-token tiles over the last 1024; M = 4096
+    # and 16384 divide into whole rounds and keep one launch.
+    for op in (FWD, DGRAD):
+        p = q(op, 8192, 4096, 4096)
+        assert (p["token_tile"], p["items"], p["tail_tokens"], p["tail_token_tile"]) == (512, 224, 1024, 256), p
+        assert p["workspace_bytes"] == 0
+        for M in (2048, 4096, 16384):
+            assert q(op, M, 4096, 4096)["tail_tokens"] == 0
+    assert q(FWD, 8192, 4096, 4096, bits=8)["tail_tokens"] == 0   # (no pairs for one-byte codes)
+    _lib.set_token_tile(512)
+    try:
+        assert q(FWD, 8192, 4096, 4096)["tail_tokens"] == 0        # a fixed tile is never split
+    finally:
+        _lib.set_token_tile(0)
+
+
 @pytest.mark.parametrize("bits,f16", [(4, False), (8, False), (4, True)])
 def test_plan_invariants(bits, f16):
     for (M, N, K), op in itertools.product(SHAPES, (FWD, DGRAD)):
@@ -93,7 +111,7 @@ def test_plan_invariants(bits, f16):
         bt = p["token_tile"]
         assert bt in (16, 32, 64, 128, 256, 512) and (bits == 4 or bt <= 128)
         assert 1 <= p["grid"] <= SMS
-        ttiles = -(-M // bt)
+        ttiles = -(-(M - p["tail_tokens"]) // bt)
         wtiles = -(-ncols // (256 if bt == 512 else 128))  # CTA pairs: 256-row weight tiles
         if bt == 512:
             assert M >= 1024 and p["grid"] % 2 == 0 and not p["stream_k"] and not p["cluster_split"]
