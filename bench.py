@@ -3,7 +3,9 @@
 
 One step = the whole hot path over one batch: the forward y = x W^T and the input
 gradient grad_x = grad_y W of the seven projections of a Llama-3.1-8B-shaped layer
-(q, k, v, o, gate, up, down) at M = 512 tokens, NF4 with double-quantised absmax.
+(q, k, v, o, gate, up, down) at M = 512 tokens, NF4 with double-quantised absmax,
+as 8 launches: q/k/v and gate/up each as one multi-product launch per direction
+(the products become ready together in a layer), o and down alone.
 Weights ~ N(0, 0.02) and activations ~ N(0, 1) are seeded synthetic stand-ins for
 the checkpoint; three replicas of the quantised weights rotate across steps so the
 weights read by a step (337 MB in total) are never L2-resident from the step before.
