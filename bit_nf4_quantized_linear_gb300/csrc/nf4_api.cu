@@ -323,6 +323,7 @@ Plan plan_dense(int mode, int64_t M, int64_t N, int64_t K, int sms, bool allow_s
     for (int si = 0; si < 7; ++si) {
       const int S = sp[si];
       if (S > 1 && ksteps / S < 8) break;
+      if (S > 1 && force_bt > 0) break;  // the parts of a token split: whole contractions, no workspace
       const int64_t items = wt * ttiles * S;
       const int64_t waves = (items + units - 1) / units;
       const int64_t kps = (ksteps + S - 1) / S;
