@@ -88,6 +88,18 @@ def test_token_split_of_pair_plans():
         for M in (2048, 4096, 16384):
             assert q(op, M, 4096, 4096)["tail_tokens"] == 0
     assert q(FWD, 8192, 4096, 4096, bits=8)["tail_tokens"] == 0   # (no pairs for one-byte codes)
+    # the parts of a split run whole contractions: no workspace, whatever the shape
+    # (the 32B-shaped stack splits several of its products at M = 4096)
+    seen = 0
+    for M in (2048, 4096, 6144, 8192, 12288):
+        for N, K in ((5120, 5120), (1024, 5120), (27648, 5120), (5120, 27648), (14336, 4096), (4096, 14336)):
+            for op in (FWD, DGRAD):
+                p = q(op, M, N, K)
+                if p["tail_tokens"]:
+                    seen += 1
+                    assert p["workspace_bytes"] == 0 and p["tail_token_tile"] == 256, (M, N, K, op, p)
+                    assert p["tail_tokens"] % 512 == 0 and p["tail_tokens"] < M
+    assert seen > 0
     _lib.set_token_tile(512)
     try:
         assert q(FWD, 8192, 4096, 4096)["tail_tokens"] == 0        # a fixed tile is never split
