@@ -121,7 +121,7 @@ def traffic_per_launch():
 
 
 class _Nvml:
-    """Minimal ctypes view of NVML (the driver's management library): SM clock,
+    """Minimal ctypes view of NVML (NVIDIA's management library): SM clock,
     its maximum, power draw and the active clock-event (throttle) reasons of one
     device.  Read-only; nothing here changes a device setting."""
 
